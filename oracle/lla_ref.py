@@ -1,0 +1,291 @@
+"""Plain float64 CPU oracle for the causal Local Linear Attention (LLA) forward pass.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports this module: only
+the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py``
+call it.  It shares no code with the CUDA path.
+
+It is the plain definition written out, one query at a time, in float64:
+
+* Local Linear Attention reading notes, section 2.1 ("one intercept per query"),
+  Eqs. (6)-(8): for query i, with z_ij = k_j - q_i and kernel weights w_ij over
+  the causal prefix j <= i,
+      omega_i = sum_j w_ij,   mu_i = sum_j w_ij z_ij,
+      Sigma_i = sum_j w_ij z_ij z_ij^T + lambda I,   rho_i = Sigma_i^{-1} mu_i,
+      s_ij    = w_ij (1 - z_ij^T rho_i) / (omega_i - mu_i^T rho_i),
+      b_i     = sum_j s_ij v_j.
+  Every z_ij is formed explicitly and Sigma_i is built densely and factorised by
+  Cholesky (the "naive" form of section 2.2, per row, never used on the GPU).
+* The kernel weight is the dot-product exponential with the row maximum
+  subtracted, w_ij = exp(tau q_i.k_j - max_{l<=i} tau q_i.k_l): the reading notes
+  section 2.2 / Algorithm 1 accumulate the moments "with an online maximum",
+  and the largest weight of a row is therefore 1.  lambda is absolute, so this
+  normalisation is part of the definition (the result is not scale invariant).
+* ``cg_solve`` is textbook conjugate gradient on the dense Sigma_i (reading notes
+  section 2.2, Sec. 3.1: Sigma_i rho_i = mu_i solved by CG using only products
+  Sigma_i p).  It exists to separate CG truncation from floating-point error;
+  the reference output itself uses the exact (Cholesky) solve.
+* ``lla_row_deflated_cg`` solves the same system through the exact identity
+  Sigma_i = C_i + omega_i delta_i delta_i^T, with C_i the weighted key scatter about
+  the weighted key mean kbar_i plus lambda I and delta_i = kbar_i - q_i (so mu_i =
+  omega_i delta_i).  By Sherman-Morrison, rho_i = rho'_i / (1 + delta_i.rho'_i) with
+  (C_i / omega_i) rho'_i = delta_i, the denominator is omega_i / (1 + delta_i.rho'_i),
+  and b_i = sum_j wbar_ij (1 - (k_j - kbar_i).rho'_i) v_j: the softmax output minus
+  a softmax-weighted value/key covariance times a probe (the form the Parallax page
+  describes).  rho'_i is found by CG on the centred system; at convergence this is
+  the same rho_i, but at a fixed iteration cap the iterates differ from CG on
+  Sigma_i.  It is the float64 restatement of the iteration the CUDA path runs.
+* ``softmax_ref`` is the Nadaraya-Watson / softmax local-constant estimate with the
+  same weights (reading notes section 1, Eq. (4); kernel-methods blog chapter 1),
+  the lambda -> infinity limit stated in section 2.1 (Sec. 2.3 of the paper).
+* ``brute_force_fit`` minimises the weighted ridge objective of section 2.1 over
+  (b, W) directly by SVD least squares, without the closed form.  Reading: the
+  ridge term that reproduces Eq. (7)'s "+ lambda I" is (lambda/2)||W||_F^2 (the
+  printed objective's lambda||W||_F^2 would give 2 lambda I).
+
+Inputs are numpy arrays shaped [B, H, n, d]; whatever dtype they arrive in is
+converted exactly to float64 (bf16 and fp32 values are exact in float64).
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import scipy.linalg
+
+__all__ = [
+    "row_weights",
+    "row_moments",
+    "row_moments_split",
+    "lla_row",
+    "lla_ref",
+    "lla_row_deflated_cg",
+    "softmax_row",
+    "softmax_ref",
+    "cg_solve",
+    "lla_row_cg",
+    "brute_force_fit",
+    "ridge_objective",
+    "slope_hat",
+]
+
+
+def _f64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+def row_weights(q_i, K_prefix, tau):
+    """Max-subtracted dot-product exponential weights of one query.
+
+    Returns (w, m) with w_j = exp(tau q_i.k_j - m), m = max_j tau q_i.k_j, over the
+    causal prefix K_prefix = [k_0 .. k_i] (reading notes section 2.1 / 2.2).
+    """
+    q_i = _f64(q_i)
+    K = _f64(K_prefix)
+    logits = tau * (K @ q_i)
+    m = logits.max()
+    return np.exp(logits - m), m
+
+
+def row_moments(q_i, K_prefix, w, lam):
+    """omega, mu, Sigma of Eq. (7) from the explicit differences z_j = k_j - q_i."""
+    q_i = _f64(q_i)
+    Z = _f64(K_prefix) - q_i[None, :]
+    omega = w.sum()
+    mu = Z.T @ w
+    Sigma = (Z * w[:, None]).T @ Z + lam * np.eye(q_i.shape[0])
+    return omega, mu, Sigma, Z
+
+
+def row_moments_split(q_i, K_prefix, w, lam):
+    """The same moments through the key/query split of Eqs. (10)-(12).
+
+    mu~ = sum_j w_j k_j, mu = mu~ - omega q;  Sigma~ = sum_j w_j k_j k_j^T + lambda I,
+    Sigma = Sigma~ - mu~ q^T - q mu~^T + omega q q^T  (reading notes section 2.2).
+    """
+    q_i = _f64(q_i)
+    K = _f64(K_prefix)
+    omega = w.sum()
+    mu_t = K.T @ w
+    mu = mu_t - omega * q_i
+    Sigma_t = (K * w[:, None]).T @ K + lam * np.eye(q_i.shape[0])
+    Sigma = Sigma_t - np.outer(mu_t, q_i) - np.outer(q_i, mu_t) + omega * np.outer(q_i, q_i)
+    return omega, mu_t, mu, Sigma
+
+
+def _output_from_rho(w, Z, V, omega, mu, rho):
+    """Eq. (8): s_j = w_j (1 - z_j.rho) / (omega - mu.rho), b = sum_j s_j v_j."""
+    denom = omega - mu @ rho
+    s = w * (1.0 - Z @ rho) / denom
+    return s @ _f64(V), s, denom
+
+
+def lla_row(q_i, K_prefix, V_prefix, tau, lam):
+    """LLA output of one query from its causal prefix, exact solve (Cholesky).
+
+    Returns a dict with out, rho, denom, omega, mu, m, s (the mixing weights s_ij)
+    and cond (2-norm condition number of Sigma_i).
+    """
+    w, m = row_weights(q_i, K_prefix, tau)
+    omega, mu, Sigma, Z = row_moments(q_i, K_prefix, w, lam)
+    rho = scipy.linalg.cho_solve(scipy.linalg.cho_factor(Sigma, lower=True), mu)
+    out, s, denom = _output_from_rho(w, Z, V_prefix, omega, mu, rho)
+    return {"out": out, "rho": rho, "denom": denom, "omega": omega, "mu": mu,
+            "m": m, "w": w, "s": s, "Sigma": Sigma}
+
+
+def cg_solve(Sigma, mu, max_iters, tol):
+    """Unpreconditioned conjugate gradient for Sigma x = mu, x_0 = 0.
+
+    Rules (the pages say only "CG"; this is the reading the GPU path follows):
+    the residual is kept by recurrence; before every iteration the run stops if
+    ||r||_2 <= tol * ||mu||_2 (tol = 0 therefore runs exactly max_iters
+    iterations unless the residual is exactly zero); mu = 0 gives x = 0 after 0
+    iterations; a direction with no positive curvature (p.Sigma p <= 0, which for
+    an SPD matrix means the direction has underflowed to nothing) ends the run
+    without being counted.  Returns (x, iterations executed).
+    """
+    Sigma = _f64(Sigma)
+    mu = _f64(mu)
+    x = np.zeros_like(mu)
+    r = mu.copy()
+    p = r.copy()
+    gamma = r @ r
+    mu_norm = np.sqrt(gamma)
+    it = 0
+    while it < max_iters:
+        if gamma == 0.0 or np.sqrt(gamma) <= tol * mu_norm:
+            break
+        Sp = Sigma @ p
+        pSp = p @ Sp
+        if not pSp > 0.0:
+            break
+        alpha = gamma / pSp
+        x = x + alpha * p
+        r = r - alpha * Sp
+        gamma_new = r @ r
+        p = r + (gamma_new / gamma) * p
+        gamma = gamma_new
+        it += 1
+    return x, it
+
+
+def lla_row_cg(q_i, K_prefix, V_prefix, tau, lam, max_iters, tol):
+    """As ``lla_row`` but rho from ``cg_solve`` (truncation diagnostics)."""
+    w, m = row_weights(q_i, K_prefix, tau)
+    omega, mu, Sigma, Z = row_moments(q_i, K_prefix, w, lam)
+    rho, iters = cg_solve(Sigma, mu, max_iters, tol)
+    out, s, denom = _output_from_rho(w, Z, V_prefix, omega, mu, rho)
+    return {"out": out, "rho": rho, "denom": denom, "iters": iters, "m": m, "omega": omega}
+
+
+def lla_row_deflated_cg(q_i, K_prefix, V_prefix, tau, lam, max_iters, tol):
+    """LLA of one query with rho from CG on the centred key scatter.
+
+    Steps: weights; omega, kbar = sum_j w_j k_j / omega; delta = kbar - q;
+    Cn = sum_j wbar_j (k_j - kbar)(k_j - kbar)^T + (lambda/omega) I (dense);
+    rho' = ``cg_solve``(Cn, delta, max_iters, tol); then
+    g = 1 + delta.rho', rho = rho'/g, denom = omega/g and
+    out = sum_j wbar_j (1 - (k_j - kbar).rho') v_j.
+    """
+    q_i = _f64(q_i)
+    K = _f64(K_prefix)
+    w, m = row_weights(q_i, K, tau)
+    omega = w.sum()
+    wbar = w / omega
+    kbar = wbar @ K
+    delta = kbar - q_i
+    Kc = K - kbar[None, :]
+    Cn = (Kc * wbar[:, None]).T @ Kc + (lam / omega) * np.eye(q_i.shape[0])
+    rho_p, iters = cg_solve(Cn, delta, max_iters, tol)
+    g = 1.0 + delta @ rho_p
+    s = wbar * (1.0 - Kc @ rho_p)
+    return {"out": s @ _f64(V_prefix), "rho": rho_p / g, "denom": omega / g,
+            "rho_probe": rho_p, "iters": iters, "m": m, "omega": omega, "s": s}
+
+
+def softmax_row(q_i, K_prefix, V_prefix, tau):
+    """Local-constant (Nadaraya-Watson / softmax) estimate: sum_j (w_j/omega) v_j."""
+    w, _ = row_weights(q_i, K_prefix, tau)
+    return (w / w.sum()) @ _f64(V_prefix)
+
+
+def _rows_iter(shape, rows):
+    B, H, n, _ = shape
+    if rows is None:
+        for b in range(B):
+            for h in range(H):
+                for i in range(n):
+                    yield b, h, i
+    else:
+        for r in rows:
+            yield tuple(int(t) for t in r)
+
+
+def lla_ref(q, k, v, tau, lam, rows=None, cg=None, deflated=None):
+    """Causal LLA over [B, H, n, d] inputs, row by row.
+
+    rows: None (every (b, h, i)) or an iterable of (b, h, i) triples.
+    cg: None for the exact solve, else (max_iters, tol) to solve with ``cg_solve``
+        on Sigma_i; deflated: (max_iters, tol) to use ``lla_row_deflated_cg``.
+    Returns (out [R, d], rho [R, d], denom [R]) in float64, R rows in the order
+    given (row-major over b, h, i when rows is None).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    outs, rhos, dens = [], [], []
+    for b, h, i in _rows_iter(q.shape, rows):
+        if deflated is not None:
+            r = lla_row_deflated_cg(q[b, h, i], k[b, h, : i + 1], v[b, h, : i + 1], tau, lam,
+                                    deflated[0], deflated[1])
+        elif cg is None:
+            r = lla_row(q[b, h, i], k[b, h, : i + 1], v[b, h, : i + 1], tau, lam)
+        else:
+            r = lla_row_cg(q[b, h, i], k[b, h, : i + 1], v[b, h, : i + 1], tau, lam, cg[0], cg[1])
+        outs.append(r["out"])
+        rhos.append(r["rho"])
+        dens.append(r["denom"])
+    d = q.shape[-1]
+    return (np.array(outs).reshape(-1, d), np.array(rhos).reshape(-1, d), np.array(dens))
+
+
+def softmax_ref(q, k, v, tau, rows=None):
+    """Causal softmax attention with the same max-subtracted weights, row by row."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    outs = [softmax_row(q[b, h, i], k[b, h, : i + 1], v[b, h, : i + 1], tau)
+            for b, h, i in _rows_iter(q.shape, rows)]
+    return np.array(outs).reshape(-1, q.shape[-1])
+
+
+def ridge_objective(b, W, q_i, K_prefix, V_prefix, w, ridge):
+    """0.5 sum_j w_j ||v_j - b - W z_j||^2 + ridge ||W||_F^2 (section 2.1 objective)."""
+    Z = _f64(K_prefix) - _f64(q_i)[None, :]
+    R = _f64(V_prefix) - b[None, :] - Z @ W.T
+    return 0.5 * np.sum(w * np.sum(R * R, axis=1)) + ridge * np.sum(W * W)
+
+
+def brute_force_fit(q_i, K_prefix, V_prefix, w, ridge):
+    """Minimise ``ridge_objective`` over (b, W) by SVD least squares.
+
+    Each output coordinate is an independent weighted ridge regression on the
+    augmented design [1, z_j^T]; the ridge penalty becomes d extra rows
+    sqrt(2 ridge) [0, e_k^T] -> 0.  No normal equations, no closed form.
+    Returns (b [d], W [d, d]).
+    """
+    Z = _f64(K_prefix) - _f64(q_i)[None, :]
+    n, d = Z.shape
+    sw = np.sqrt(_f64(w))
+    A_data = sw[:, None] * np.hstack([np.ones((n, 1)), Z])
+    A_ridge = np.hstack([np.zeros((d, 1)), np.sqrt(2.0 * ridge) * np.eye(d)])
+    A = np.vstack([A_data, A_ridge])
+    Y = np.vstack([sw[:, None] * _f64(V_prefix), np.zeros((d, _f64(V_prefix).shape[1]))])
+    theta, *_ = np.linalg.lstsq(A, Y, rcond=None)
+    return theta[0], theta[1:].T
+
+
+def slope_hat(q_i, K_prefix, V_prefix, w, lam, b):
+    """Local slope W_i of the fit, from the W normal equation at the optimum.
+
+    With the "+ lambda I" reading: (sum_j w_j (v_j - b) z_j^T) Sigma_i^{-1}.
+    Used to check Eq. (9): b_i = W_i q_i + sum_j wbar_j (v_j - W_i k_j).
+    """
+    omega, mu, Sigma, Z = row_moments(q_i, K_prefix, w, lam)
+    C = ((_f64(V_prefix) - b[None, :]) * w[:, None]).T @ Z
+    return np.linalg.solve(Sigma.T, C.T).T
