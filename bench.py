@@ -1,0 +1,398 @@
+"""Benchmark of the causal LLA forward pass (one JSON line on stdout, rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload lm_bf16] [--path auto|tensor|fp32] [--no-cpu-baseline]
+
+A step is one lla_forward call over the whole workload (all heads, all queries):
+max sweep, moment sweep, CG sweeps and output sweep.  Inputs are seeded synthetic
+tensors already resident in HBM; L2 is flushed (a 512 MiB write) before every timed
+step, outside the timed interval.  Timing uses CUDA events on the launching stream.
+
+N > 1 (torchrun): every rank runs the same workload on its own GPU with its own seed
+(weak scaling; heads are independent, there is no collective on the data path);
+value = tokens of all ranks / max over ranks of the timed seconds.
+
+--impl reference times the float64 CPU oracle (the only reference this project has)
+on a bounded sample of the workload's rows on rank 0 and extrapolates to the workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "causal LLA fwd tokens/s & TFLOP/s at d=128 bf16; fraction of BF16 tensor peak"
+
+
+def useful_flops(w, T):
+    """(2 + 3T + 2) causal GEMM passes of 2d flops per pair (moment, CG, output)."""
+    pairs = w.n * (w.n + 1) / 2 * w.B * w.H
+    return (4 + 3 * T) * 2 * w.d * pairs
+
+
+def executed_flops(w, T, path):
+    """Adds the logits-only max sweep and the output sweep's rho.k product."""
+    pairs = w.n * (w.n + 1) / 2 * w.B * w.H
+    return (6 + 3 * T) * 2 * w.d * pairs
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "sm_max_mhz": 2070.0}, "fallback"
+
+
+def fp32_alu_peak_tflops(sm_mhz):
+    """152 SMs x 128 fp32 lanes x 2 flops (FMA) per clock."""
+    return 152 * 128 * 2 * sm_mhz * 1e6 / 1e12
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[j] for r in rows for j in range(4) if r[5 + j].lower() == "active"})
+        loaded = [s for s in sm if s > 0.5 * (max(sm) if sm else 1)]
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "local_linear_attention_flashlla_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".h", ".cuh")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kernel, workload_name):
+    """DRAM bytes per launch from the committed ncu summary, if taken on this exact source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            doc = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = doc.get(f"{kernel}:{workload_name}")
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+
+def _oracle_rows_worker(job):
+    import numpy as np
+    from oracle.lla_ref import lla_row
+    q, k, v, tau, lam, rows = job
+    out = []
+    for (b, h, i) in rows:
+        t0 = time.perf_counter()
+        lla_row(q[b, h, i], k[b, h, : i + 1], v[b, h, : i + 1], tau, lam)
+        out.append((i, time.perf_counter() - t0))
+    return out
+
+
+def cpu_oracle_throughput(w, qkv, budget_s=15.0, seed=123):
+    """Time the oracle on a bounded random sample of rows on all host cores; extrapolate.
+
+    Per-row cost is fitted as a + b (i + 1) (the dense Sigma build is (i+1) d^2) and
+    integrated over every (b, h, i) of the workload.
+    """
+    import multiprocessing as mp
+
+    import numpy as np
+
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    cores = os.cpu_count() or 1
+    rng = np.random.default_rng(seed)
+    q, k, v = (t.double().numpy() for t in qkv)
+    # calibrate: one row at the mean causal length
+    from oracle.lla_ref import lla_row
+    t0 = time.perf_counter()
+    i_mid = w.n // 2
+    lla_row(q[0, 0, i_mid], k[0, 0, : i_mid + 1], v[0, 0, : i_mid + 1], w.tau, w.lam)
+    per_row = max(time.perf_counter() - t0, 1e-4)
+    n_rows = int(max(cores * 2, min(4096, budget_s * cores / per_row)))
+    rows = [(int(rng.integers(w.B)), int(rng.integers(w.H)), int(rng.integers(w.n))) for _ in range(n_rows)]
+    chunks = [rows[c::cores] for c in range(cores)]
+    ctx = mp.get_context("spawn")
+    t0 = time.perf_counter()
+    with ctx.Pool(cores) as pool:
+        res = pool.map(_oracle_rows_worker, [(q, k, v, w.tau, w.lam, ch) for ch in chunks])
+    wall = time.perf_counter() - t0
+    pts = [p for r in res for p in r]
+    i_arr = np.array([p[0] + 1 for p in pts], dtype=np.float64)
+    t_arr = np.array([p[1] for p in pts])
+    A = np.stack([np.ones_like(i_arr), i_arr], axis=1)
+    (a, b), *_ = np.linalg.lstsq(A, t_arr, rcond=None)
+    a, b = max(a, 0.0), max(b, 1e-12)
+    total_single = w.B * w.H * (w.n * a + b * w.n * (w.n + 1) / 2)
+    eff = min(1.0, t_arr.sum() / (wall * cores))       # measured parallel efficiency of the pool
+    est_wall = total_single / (cores * eff)
+    tokens = w.B * w.n
+    return {"value": tokens / est_wall, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": (f"{len(pts)} random (b,h,i) rows of {w.name} solved exactly (float64, dense Sigma, "
+                       f"Cholesky) in {wall:.1f} s on {cores} processes; per-row cost a+b(i+1) fitted and "
+                       f"integrated over all {w.B * w.H * w.n} rows: est. {est_wall:.0f} s per step"),
+            "est_seconds_per_step": est_wall}
+
+
+# ----------------------------------------------------------------------------- main
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="lm_bf16")
+    ap.add_argument("--path", choices=["auto", "tensor", "fp32"], default="auto")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    from local_linear_attention_flashlla_gb300.inputs import make_inputs, workload
+    w = workload(args.workload)
+    qkv = make_inputs(w)
+    steps = []
+    cb = None
+    for s in range(args.warmup + args.steps):
+        cb = cpu_oracle_throughput(w, qkv, budget_s=4.0, seed=1000 + s)
+        if s >= args.warmup:
+            steps.append(cb["est_seconds_per_step"])
+    sec = statistics.mean(steps)
+    value = w.B * w.n / sec
+    T = w.cg_max_iters
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{w.name} B={w.B} H={w.H} n={w.n} d={w.d} tau={w.tau:.5g} lambda={w.lam} "
+                                   f"cg_iters={T} cg_tol={w.cg_tol}", "l2": "n/a (CPU)"},
+            "tflops": useful_flops(w, T) / sec / 1e12,
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cb["cores"], "kind": "oracle",
+                             "sample": cb["sample"]},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    import numpy as np
+    import torch
+
+    import local_linear_attention_flashlla_gb300 as lla
+    from local_linear_attention_flashlla_gb300.inputs import make_inputs, workload
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workload(args.workload)
+    path = {"auto": lla.LLA_PATH_AUTO, "tensor": lla.LLA_PATH_TENSOR, "fp32": lla.LLA_PATH_FP32}[args.path]
+    dtype_code = lla.LLA_DTYPE_BF16 if w.dtype == "bf16" else lla.LLA_DTYPE_FP32
+    rpath = lla.lla_resolve_path(dtype_code, path, w.d)
+    qkv_host = make_inputs(w.with_(seed=w.seed + rank))
+    q, k, v = (t.to(dev) for t in qkv_host)
+    out = torch.empty_like(q)
+    rho = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    den = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    ws_bytes = lla.lla_workspace_size(dtype_code, path, w.B, w.H, w.n, w.d)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        lla.forward(q, k, v, w.tau, w.lam, w.cg_max_iters, w.cg_tol, path=path, out=out, rho=rho, denom=den,
+                    workspace=ws if ws_bytes else None)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    lla.lla_sync_status()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    lla.lla_sync_status()
+    total_ms = sum(times)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    tokens = w.B * w.n
+    value = world * tokens * args.steps / (total_ms / 1e3)
+    T = w.cg_max_iters if w.cg_tol == 0 else None
+    if T is None:   # tolerance-driven: count the executed iterations
+        _, _, _, its = lla.forward(q, k, v, w.tau, w.lam, w.cg_max_iters, w.cg_tol, path=path, return_iters=True)
+        T = float(its.float().max().item())
+    flops = useful_flops(w, T)
+    tflops = world * flops * args.steps / (total_ms / 1e3) / 1e12
+
+    # end to end through the public API from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (t.pin_memory() for t in qkv_host)
+        ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hr = torch.empty(rho.shape, dtype=rho.dtype).pin_memory()
+        hd = torch.empty(den.shape, dtype=den.dtype).pin_memory()
+        dq, dk, dv = (torch.empty_like(t) for t in (q, k, v))
+        e2e_ms = []
+        for it in range(args.warmup + args.steps):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            lla.forward(dq, dk, dv, w.tau, w.lam, w.cg_max_iters, w.cg_tol, path=path, out=out, rho=rho,
+                        denom=den, workspace=ws if ws_bytes else None)
+            ho.copy_(out, non_blocking=True)
+            hr.copy_(rho, non_blocking=True)
+            hd.copy_(den, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            if it >= args.warmup:
+                e2e_ms.append(e0.elapsed_time(e1))
+        tot = sum(e2e_ms)
+        if world > 1:
+            t = torch.tensor([tot], dtype=torch.float64, device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            tot = float(t.item())
+        e2e = {"value": world * tokens * len(e2e_ms) / (tot / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hq, hk, hv)),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in (ho, hr, hd))}
+
+    peaks, peak_kind = load_peaks()
+    launches_per_step = 1 if rpath == lla.LLA_PATH_FP32 else 2
+    kern_name = "lla_simt_kernel" if rpath == lla.LLA_PATH_FP32 else "lla_tc_kernel"
+    dominant_ms = ms_per_step     # the fp32 path is a single kernel per step
+    achieved = flops / (dominant_ms / 1e3) / 1e12
+    if rpath == lla.LLA_PATH_FP32:
+        peak = fp32_alu_peak_tflops(peaks.get("sm_max_mhz", 2070.0))
+        roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": load_traffic(kern_name, w.name),
+                "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 flops x max SM clock",
+                "flops_counted": "useful (4+3T) passes x 2d per causal pair"}
+        dtype = "f32"
+    else:
+        peak = peaks["bf16_tflops"]
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": load_traffic(kern_name, w.name), "peak_source": f"{peak_kind} bf16 burst",
+                "flops_counted": "useful (4+3T) passes x 2d per causal pair"}
+        dtype = "f16"
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+            "config": {"workload": f"{w.name} B={w.B} H={w.H} n={w.n} d={w.d} tau={w.tau:.5g} lambda={w.lam} "
+                                   f"cg_iters={w.cg_max_iters} cg_tol={w.cg_tol}",
+                       "path": {1: "tensor", 2: "fp32"}[rpath], "l2": "flushed before every step (512 MiB write)",
+                       "inputs": "bf16 q,k,v resident in HBM" if w.dtype == "bf16" else "fp32 q,k,v in HBM"},
+            "tflops": tflops, "tflops_executed": world * executed_flops(w, T, rpath) * args.steps / (total_ms / 1e3) / 1e12,
+            "roofline": roof, "clocks": clocks, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+            "cg_iters_counted": T}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_throughput(w, qkv_host)
+        line["cpu_baseline"].pop("est_seconds_per_step", None)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,111 @@
+/*
+ * lla.h -- C ABI of the causal Local Linear Attention (LLA) forward pass on GB300 (sm_103a).
+ *
+ * What is computed (Local Linear Attention reading notes, section 2.1, Eqs. (6)-(8); section
+ * 2.2, Eqs. (10)-(12) and the FlashLLA three-phase query-tile sweep of Algorithm 1):
+ * for every batch b, head h and query position i, over the causal prefix j <= i,
+ *
+ *     w_ij    = exp(tau q_i.k_j - m_i),  m_i = max_{l<=i} tau q_i.k_l     (largest weight is 1)
+ *     omega_i = sum_j w_ij,   mu_i = sum_j w_ij (k_j - q_i),
+ *     Sigma_i = sum_j w_ij (k_j - q_i)(k_j - q_i)^T + lambda I,   Sigma_i rho_i = mu_i,
+ *     denom_i = omega_i - mu_i.rho_i,
+ *     out_i   = sum_j w_ij (1 - (k_j - q_i).rho_i) v_j / denom_i.
+ *
+ * rho_i is found by conjugate gradient (section 2.2, "matrix-free CG").  The CG runs on the
+ * centred key scatter: with kbar_i = sum_j w_ij k_j / omega_i and delta_i = kbar_i - q_i,
+ * Sigma_i = C_i + omega_i delta_i delta_i^T exactly, so CG solves
+ * (C_i / omega_i) rho'_i = delta_i and rho_i = rho'_i / (1 + delta_i.rho'_i),
+ * denom_i = omega_i / (1 + delta_i.rho'_i) (Sherman-Morrison).  At convergence this is the same
+ * rho_i; at a fixed iteration cap the centred system, having no dominant mean direction,
+ * converges further and is stable in low precision.
+ *
+ * Layout: q, k, v, out are contiguous row-major [B, H, n, d]; rho is [B, H, n, d] fp32;
+ * denom and cg_iters are [B, H, n].  All pointers are DEVICE pointers on the current device,
+ * 16-byte aligned.  The caller owns every buffer.  All calls are asynchronous on `stream`
+ * (a cudaStream_t passed as void*; NULL = legacy default stream).
+ *
+ * Errors: every entry point returns an lla_status.  Invalid arguments are rejected on the host
+ * before anything is launched; no exception crosses this boundary.  lla_last_error() gives a
+ * message for the calling thread's last failure.
+ */
+#ifndef LLA_H_
+#define LLA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LLA_OK = 0,
+    LLA_ERR_INVALID_ARG = 1,     /* null pointer, bad size, tau/lambda <= 0, cap < 1, ... */
+    LLA_ERR_UNSUPPORTED = 2,     /* head dim or dtype/path combination not built */
+    LLA_ERR_CUDA = 3,            /* a CUDA runtime/driver call failed; see lla_last_error() */
+    LLA_ERR_DEVICE_TIMEOUT = 4   /* a bounded device-side wait gave up (reported by lla_sync_status) */
+} lla_status;
+
+typedef enum {
+    LLA_DTYPE_BF16 = 0,          /* q, k, v, out are bfloat16 */
+    LLA_DTYPE_FP32 = 1           /* q, k, v, out are float32 */
+} lla_dtype;
+
+typedef enum {
+    LLA_PATH_AUTO = 0,           /* bf16 -> LLA_PATH_TENSOR when d in {64,128}, else LLA_PATH_FP32 */
+    LLA_PATH_TENSOR = 1,         /* tcgen05/TMEM/TMA kernel, fp16 operands, fp32 accumulate/state */
+    LLA_PATH_FP32 = 2            /* CUDA-core fp32 kernel: every product and the CG state in fp32 */
+} lla_path;
+
+/*
+ * lla_forward -- causal LLA forward, bf16 q/k/v/out, LLA_PATH_AUTO.
+ *
+ * q, k, v   [B,H,n,d] bf16, read only.      out   [B,H,n,d] bf16, written.
+ * rho       [B,H,n,d] fp32, written: rho_i.  denom [B,H,n] fp32, written: omega_i - mu_i.rho_i.
+ * B, H, n >= 1; d in {16, 32, 64, 128}; tau > 0 (logit scale); lambda > 0 (ridge, absolute,
+ * applied to the max-normalised weights); cg_max_iters >= 1; cg_tol >= 0: a query stops once
+ * ||r|| <= cg_tol ||delta_i|| (cg_tol == 0: exactly cg_max_iters iterations).
+ * Scratch (the tensor path's fp16 operand copies) is taken from the CUDA stream-ordered pool
+ * with cudaMallocAsync/cudaFreeAsync on `stream`; use lla_forward_ex to pass it instead.
+ */
+int lla_forward(const void* q, const void* k, const void* v, void* out, float* rho, float* denom,
+                int B, int H, int n, int d, float tau, float lambda, int cg_max_iters, float cg_tol,
+                void* stream);
+
+/*
+ * lla_forward_ex -- as lla_forward with the dtype and path chosen by the caller.
+ *
+ * dtype      LLA_DTYPE_BF16 or LLA_DTYPE_FP32 (q, k, v and out share it).
+ * path       an lla_path value.  LLA_PATH_TENSOR needs bf16 and d in {64, 128}.
+ * cg_iters   NULL, or [B,H,n] int32 device buffer: CG iterations each query executed.
+ * workspace  NULL (scratch from the stream-ordered pool) or a device buffer of at least
+ *            lla_workspace_size(...) bytes, 256-byte aligned, not used concurrently by
+ *            another call.
+ */
+int lla_forward_ex(int dtype, int path, const void* q, const void* k, const void* v, void* out,
+                   float* rho, float* denom, int* cg_iters, int B, int H, int n, int d, float tau,
+                   float lambda, int cg_max_iters, float cg_tol, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/* Bytes of scratch lla_forward_ex needs for these arguments (0 for the fp32 path). */
+size_t lla_workspace_size(int dtype, int path, int B, int H, int n, int d);
+
+/* The path LLA_PATH_AUTO resolves to for (dtype, d): LLA_PATH_TENSOR or LLA_PATH_FP32. */
+int lla_resolve_path(int dtype, int path, int d);
+
+/*
+ * lla_sync_status -- synchronise `stream`, then report and clear the library's device error
+ * word (set when a bounded wait inside a kernel gave up: LLA_ERR_DEVICE_TIMEOUT).
+ */
+int lla_sync_status(void* stream);
+
+/* Message for the calling thread's most recent failure ("" if none). Owned by the library. */
+const char* lla_last_error(void);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+int lla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LLA_H_ */

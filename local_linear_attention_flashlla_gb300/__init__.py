@@ -1,0 +1,156 @@
+"""Causal Local Linear Attention (LLA) forward pass for GB300 (sm_103a).
+
+Thin ctypes binding over liblla.so, whose C ABI is declared in include/lla.h.  The
+binding only marshals arguments: every step of the computation runs in the
+library's CUDA kernels.  PyTorch supplies device memory and the current stream.
+
+There is no CPU fallback: if liblla.so is missing or cannot load, every call
+raises ``LLAError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "LLAError", "load_library", "library_path", "forward", "lla_forward", "lla_forward_ex",
+    "lla_workspace_size", "lla_resolve_path", "lla_sync_status", "lla_last_error", "lla_version",
+    "LLA_OK", "LLA_ERR_INVALID_ARG", "LLA_ERR_UNSUPPORTED", "LLA_ERR_CUDA", "LLA_ERR_DEVICE_TIMEOUT",
+    "LLA_DTYPE_BF16", "LLA_DTYPE_FP32", "LLA_PATH_AUTO", "LLA_PATH_TENSOR", "LLA_PATH_FP32",
+    "EXPORTED_SYMBOLS",
+]
+
+LLA_OK, LLA_ERR_INVALID_ARG, LLA_ERR_UNSUPPORTED, LLA_ERR_CUDA, LLA_ERR_DEVICE_TIMEOUT = range(5)
+LLA_DTYPE_BF16, LLA_DTYPE_FP32 = 0, 1
+LLA_PATH_AUTO, LLA_PATH_TENSOR, LLA_PATH_FP32 = 0, 1, 2
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+_c_int, _c_float, _c_size, _vp = ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_void_p
+
+# name -> (restype, argtypes); mirrors include/lla.h
+_SIGNATURES = {
+    "lla_forward": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_float, _c_float,
+                             _c_int, _c_float, _vp]),
+    "lla_forward_ex": (_c_int, [_c_int, _c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                _c_float, _c_float, _c_int, _c_float, _vp, _c_size, _vp]),
+    "lla_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "lla_resolve_path": (_c_int, [_c_int, _c_int, _c_int]),
+    "lla_sync_status": (_c_int, [_vp]),
+    "lla_last_error": (ctypes.c_char_p, []),
+    "lla_version": (_c_int, []),
+}
+EXPORTED_SYMBOLS = tuple(_SIGNATURES)
+
+
+class LLAError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__(f"LLA status {status}: {message}")
+        self.status = status
+
+
+def library_path():
+    return os.environ.get("LLA_LIBRARY", os.path.join(_HERE, "liblla.so"))
+
+
+def load_library():
+    """Load liblla.so (built by ``build.build()``); raises LLAError if it is absent."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = library_path()
+    if not os.path.exists(path):
+        raise LLAError(-1, f"{path} not found: build it with local_linear_attention_flashlla_gb300.build.build()")
+    try:
+        lib = ctypes.CDLL(path)
+    except OSError as e:
+        raise LLAError(-1, f"cannot load {path}: {e}") from e
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def _check(status):
+    if status != LLA_OK:
+        raise LLAError(status, load_library().lla_last_error().decode(errors="replace"))
+
+
+def lla_last_error():
+    return load_library().lla_last_error().decode(errors="replace")
+
+
+def lla_version():
+    return load_library().lla_version()
+
+
+def lla_resolve_path(dtype, path, d):
+    return load_library().lla_resolve_path(dtype, path, d)
+
+
+def lla_workspace_size(dtype, path, B, H, n, d):
+    return load_library().lla_workspace_size(dtype, path, B, H, n, d)
+
+
+def lla_sync_status(stream=None):
+    """Synchronise the stream and raise if a kernel recorded a device-side wait timeout."""
+    _check(load_library().lla_sync_status(_stream_ptr(stream)))
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def lla_forward(q_ptr, k_ptr, v_ptr, out_ptr, rho_ptr, denom_ptr, B, H, n, d, tau, lam, cg_max_iters, cg_tol,
+                stream_ptr):
+    """Raw C entry point on device pointers (ints); raises LLAError on a non-zero status."""
+    _check(load_library().lla_forward(q_ptr, k_ptr, v_ptr, out_ptr, rho_ptr, denom_ptr, B, H, n, d, tau, lam,
+                                      cg_max_iters, cg_tol, stream_ptr))
+
+
+def lla_forward_ex(dtype, path, q_ptr, k_ptr, v_ptr, out_ptr, rho_ptr, denom_ptr, iters_ptr, B, H, n, d, tau, lam,
+                   cg_max_iters, cg_tol, ws_ptr, ws_bytes, stream_ptr):
+    """Raw C entry point with dtype/path/iteration-count/workspace arguments."""
+    _check(load_library().lla_forward_ex(dtype, path, q_ptr, k_ptr, v_ptr, out_ptr, rho_ptr, denom_ptr, iters_ptr,
+                                         B, H, n, d, tau, lam, cg_max_iters, cg_tol, ws_ptr, ws_bytes, stream_ptr))
+
+
+def forward(q, k, v, tau, lam, cg_max_iters, cg_tol=0.0, *, path=LLA_PATH_AUTO, return_iters=False,
+            out=None, rho=None, denom=None, workspace=None, stream=None):
+    """Causal LLA forward on CUDA tensors q, k, v of shape [B, H, n, d] (bf16 or fp32).
+
+    Returns (out, rho, denom) or, with return_iters, (out, rho, denom, cg_iters).
+    Output tensors are allocated with torch unless passed in.  Asynchronous on the
+    current (or given) stream.
+    """
+    import torch
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise LLAError(LLA_ERR_INVALID_ARG, "q, k, v must be CUDA tensors (there is no CPU path)")
+    if q.shape != k.shape or q.shape != v.shape or q.dim() != 4:
+        raise LLAError(LLA_ERR_INVALID_ARG, f"q, k, v must share one [B, H, n, d] shape, got {tuple(q.shape)}, "
+                                            f"{tuple(k.shape)}, {tuple(v.shape)}")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.bfloat16, torch.float32):
+        raise LLAError(LLA_ERR_INVALID_ARG, "q, k, v must all be bf16 or all fp32")
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    B, H, n, d = q.shape
+    dtype = LLA_DTYPE_BF16 if q.dtype == torch.bfloat16 else LLA_DTYPE_FP32
+    if out is None:
+        out = torch.empty_like(q)
+    if rho is None:
+        rho = torch.empty((B, H, n, d), dtype=torch.float32, device=q.device)
+    if denom is None:
+        denom = torch.empty((B, H, n), dtype=torch.float32, device=q.device)
+    iters = torch.empty((B, H, n), dtype=torch.int32, device=q.device) if return_iters else None
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    lla_forward_ex(dtype, path, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), rho.data_ptr(),
+                   denom.data_ptr(), None if iters is None else iters.data_ptr(), B, H, n, d, float(tau), float(lam),
+                   int(cg_max_iters), float(cg_tol), ws_ptr, ws_bytes, _stream_ptr(stream))
+    if return_iters:
+        return out, rho, denom, iters
+    return out, rho, denom

@@ -1,0 +1,148 @@
+// C ABI of liblla.so: argument checks, path selection, scratch handling, error reporting.
+// The operation itself is described in include/lla.h.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "../../include/lla.h"
+#include "lla_internal.h"
+
+namespace lla {
+
+namespace {
+thread_local char g_msg[512] = "";
+
+int fail(int status, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return status;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(LLA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+}  // namespace
+
+__device__ unsigned g_device_error = 0;
+
+unsigned* device_error_word() {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_device_error) != cudaSuccess) return nullptr;
+    return static_cast<unsigned*>(ptr);
+}
+
+cudaError_t read_and_clear_device_error(unsigned* out, cudaStream_t stream) {
+    unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_device_error, sizeof(unsigned), 0, cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    if (*out) {
+        e = cudaMemcpyToSymbolAsync(g_device_error, &zero, sizeof(unsigned), 0, cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) return e;
+        e = cudaStreamSynchronize(stream);
+    }
+    return e;
+}
+
+}  // namespace lla
+
+using lla::fail;
+using lla::aligned16;
+
+extern "C" {
+
+int lla_version(void) { return 10000; }
+
+const char* lla_last_error(void) { return lla::g_msg; }
+
+int lla_resolve_path(int dtype, int path, int d) {
+    if (path != LLA_PATH_AUTO) return path;
+    (void)dtype; (void)d;  // the tensor path is selected automatically once it is built
+    return LLA_PATH_FP32;
+}
+
+size_t lla_workspace_size(int dtype, int path, int B, int H, int n, int d) {
+    if (B < 1 || H < 1 || n < 1 || d < 1) return 0;
+    if (lla_resolve_path(dtype, path, d) != LLA_PATH_TENSOR) return 0;
+    return lla::tensor_workspace_bytes(B, H, n, d);
+}
+
+int lla_forward_ex(int dtype, int path, const void* q, const void* k, const void* v, void* out, float* rho,
+                   float* denom, int* cg_iters, int B, int H, int n, int d, float tau, float lambda,
+                   int cg_max_iters, float cg_tol, void* workspace, size_t workspace_bytes, void* stream_) {
+    lla::g_msg[0] = '\0';
+    if (!q || !k || !v || !out || !rho || !denom) return fail(LLA_ERR_INVALID_ARG, "null tensor pointer");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(rho) ||
+        !aligned16(denom))
+        return fail(LLA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    if (B < 1 || H < 1 || n < 1) return fail(LLA_ERR_INVALID_ARG, "B, H, n must be >= 1 (got %d, %d, %d)", B, H, n);
+    if ((long long)B * H > 65535LL * 1024) return fail(LLA_ERR_INVALID_ARG, "B*H too large");
+    if ((long long)B * H * n * d > (1LL << 40)) return fail(LLA_ERR_INVALID_ARG, "problem too large");
+    if (d != 16 && d != 32 && d != 64 && d != 128)
+        return fail(LLA_ERR_INVALID_ARG, "head dim d must be 16, 32, 64 or 128 (got %d)", d);
+    if (!(tau > 0.f) || !(tau < 1e30f)) return fail(LLA_ERR_INVALID_ARG, "tau must be finite and > 0");
+    if (!(lambda > 0.f) || !(lambda < 1e30f)) return fail(LLA_ERR_INVALID_ARG, "lambda must be finite and > 0");
+    if (cg_max_iters < 1 || cg_max_iters > 4096) return fail(LLA_ERR_INVALID_ARG, "cg_max_iters must be in [1, 4096]");
+    if (!(cg_tol >= 0.f) || !(cg_tol < 1e30f)) return fail(LLA_ERR_INVALID_ARG, "cg_tol must be finite and >= 0");
+    if (dtype != LLA_DTYPE_BF16 && dtype != LLA_DTYPE_FP32) return fail(LLA_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+    if (path < LLA_PATH_AUTO || path > LLA_PATH_FP32) return fail(LLA_ERR_INVALID_ARG, "unknown path %d", path);
+    const int rpath = lla_resolve_path(dtype, path, d);
+    if (rpath == LLA_PATH_TENSOR && (dtype != LLA_DTYPE_BF16 || (d != 64 && d != 128)))
+        return fail(LLA_ERR_UNSUPPORTED, "tensor path needs bf16 inputs and d in {64, 128}");
+
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    lla::Problem p{q, k, v, out, rho, denom, cg_iters, B, H, n, d, tau, lambda, cg_max_iters, cg_tol, dtype};
+
+    if (rpath == LLA_PATH_FP32) {
+        cudaError_t e = lla::launch_simt(p, stream);
+        if (e != cudaSuccess) return lla::cuda_fail(e, "fp32 path launch");
+        return LLA_OK;
+    }
+
+    const size_t need = lla::tensor_workspace_bytes(B, H, n, d);
+    void* ws = workspace;
+    bool owned = false;
+    if (ws) {
+        if (workspace_bytes < need)
+            return fail(LLA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+        if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+            return fail(LLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    } else {
+        cudaError_t e = cudaMallocAsync(&ws, need, stream);
+        if (e != cudaSuccess) return lla::cuda_fail(e, "cudaMallocAsync(workspace)");
+        owned = true;
+    }
+    const char* why = nullptr;
+    cudaError_t e = lla::launch_tensor(p, ws, stream, &why);
+    if (owned) {
+        cudaError_t e2 = cudaFreeAsync(ws, stream);
+        if (e == cudaSuccess && e2 != cudaSuccess) return lla::cuda_fail(e2, "cudaFreeAsync(workspace)");
+    }
+    if (e != cudaSuccess) return lla::cuda_fail(e, why ? why : "tensor path launch");
+    return LLA_OK;
+}
+
+int lla_forward(const void* q, const void* k, const void* v, void* out, float* rho, float* denom, int B, int H,
+                int n, int d, float tau, float lambda, int cg_max_iters, float cg_tol, void* stream) {
+    return lla_forward_ex(LLA_DTYPE_BF16, LLA_PATH_AUTO, q, k, v, out, rho, denom, nullptr, B, H, n, d, tau,
+                          lambda, cg_max_iters, cg_tol, nullptr, 0, stream);
+}
+
+int lla_sync_status(void* stream) {
+    lla::g_msg[0] = '\0';
+    unsigned word = 0;
+    cudaError_t e = lla::read_and_clear_device_error(&word, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return lla::cuda_fail(e, "lla_sync_status");
+    if (word & lla::kDevErrMbarTimeout)
+        return fail(LLA_ERR_DEVICE_TIMEOUT, "a bounded device-side wait gave up (error word 0x%x)", word);
+    return LLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,40 @@
+// Internal declarations shared by the translation units of liblla.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace lla {
+
+// Problem description handed from the C ABI to a path's launcher (already validated).
+struct Problem {
+    const void* q;
+    const void* k;
+    const void* v;
+    void* out;
+    float* rho;
+    float* denom;
+    int* cg_iters;       // may be null
+    int B, H, n, d;
+    float tau, lambda;
+    int cg_max_iters;
+    float cg_tol;
+    int dtype;           // lla_dtype
+};
+
+// Device error word: bit flags set by kernels whose bounded waits gave up.
+enum DeviceError : unsigned { kDevErrMbarTimeout = 1u };
+
+// fp32 CUDA-core path (any d in {16,32,64,128}, fp32 or bf16 inputs).
+cudaError_t launch_simt(const Problem& p, cudaStream_t stream);
+
+// Tensor-core path (bf16 inputs, d in {64,128}).
+size_t tensor_workspace_bytes(int B, int H, int n, int d);
+cudaError_t launch_tensor(const Problem& p, void* workspace, cudaStream_t stream, const char** why);
+
+// Library-owned device error word (defined in lla_api.cu).
+cudaError_t read_and_clear_device_error(unsigned* out, cudaStream_t stream);
+unsigned* device_error_word();
+
+}  // namespace lla

@@ -1,0 +1,73 @@
+"""The C-ABI library builds, loads, exports every symbol include/lla.h declares, and
+rejects bad arguments on the host (no GPU needed: nothing is launched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import local_linear_attention_flashlla_gb300 as lla
+from local_linear_attention_flashlla_gb300 import build as lla_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(lla.library_path()):
+        lla_build.build()
+    return lla.load_library()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "lla.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lla_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_bound_entry_points():
+    assert _declared_functions() == sorted(lla.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    assert lib.lla_version() == 10000
+
+
+def _call_ex(lib, **kw):
+    a = dict(dtype=0, path=0, q=16, k=32, v=48, out=64, rho=80, den=96, it=None, B=1, H=1, n=8, d=64,
+             tau=0.1, lam=1.0, T=4, tol=0.0, ws=None, wsb=0, stream=None)
+    a.update(kw)
+    return lib.lla_forward_ex(a["dtype"], a["path"], a["q"], a["k"], a["v"], a["out"], a["rho"], a["den"], a["it"],
+                              a["B"], a["H"], a["n"], a["d"], a["tau"], a["lam"], a["T"], a["tol"], a["ws"], a["wsb"],
+                              a["stream"])
+
+
+@pytest.mark.parametrize("bad", [
+    dict(q=None), dict(out=None), dict(rho=None), dict(den=None), dict(q=17), dict(B=0), dict(n=0), dict(H=-1),
+    dict(d=48), dict(d=256), dict(tau=0.0), dict(tau=-1.0), dict(tau=float("nan")), dict(lam=0.0),
+    dict(lam=float("inf")), dict(T=0), dict(T=5000), dict(tol=-1.0), dict(dtype=7), dict(path=9),
+])
+def test_invalid_arguments_rejected_before_launch(lib, bad):
+    assert _call_ex(lib, **bad) == lla.LLA_ERR_INVALID_ARG
+    assert lib.lla_last_error().decode()
+
+
+def test_tensor_path_needs_bf16_and_supported_dim(lib):
+    assert _call_ex(lib, dtype=1, path=lla.LLA_PATH_TENSOR) == lla.LLA_ERR_UNSUPPORTED
+    assert _call_ex(lib, d=32, path=lla.LLA_PATH_TENSOR) == lla.LLA_ERR_UNSUPPORTED
+
+
+def test_path_resolution_and_workspace_size(lib):
+    assert lib.lla_resolve_path(lla.LLA_DTYPE_FP32, lla.LLA_PATH_AUTO, 128) == lla.LLA_PATH_FP32
+    assert lib.lla_resolve_path(lla.LLA_DTYPE_BF16, lla.LLA_PATH_FP32, 128) == lla.LLA_PATH_FP32
+    assert lib.lla_workspace_size(lla.LLA_DTYPE_FP32, lla.LLA_PATH_AUTO, 2, 2, 64, 64) == 0
+    assert lib.lla_workspace_size(lla.LLA_DTYPE_BF16, lla.LLA_PATH_TENSOR, 2, 2, 64, 64) > 0
+
+
+def test_binding_refuses_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(1, 1, 4, 16)
+    with pytest.raises(lla.LLAError):
+        lla.forward(x, x, x, 0.25, 0.1, 4)
