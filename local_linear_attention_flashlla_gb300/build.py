@@ -16,6 +16,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblla.so")
+PROBE_LIB = os.path.join(PKG, "liblla_probe.so")   # test-only tcgen05 descriptor probe
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -29,8 +30,9 @@ def nvcc_path():
     raise RuntimeError("nvcc not found: the CUDA toolkit is required to build liblla.so")
 
 
-def sources():
-    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+def sources(sub=""):
+    d = os.path.join(CSRC, sub)
+    return sorted(os.path.join(d, f) for f in os.listdir(d) if f.endswith(".cu"))
 
 
 def _run(cmd):
@@ -41,12 +43,15 @@ def _run(cmd):
 
 
 def build(verbose=False, extra_flags=()):
-    """Build liblla.so; returns its path."""
+    """Build liblla.so (and the test-only liblla_probe.so); returns the liblla.so path."""
     nvcc = nvcc_path()
     os.makedirs(BUILD, exist_ok=True)
-    srcs = sources()
-    objs = [os.path.join(BUILD, os.path.basename(s)[:-3] + ".o") for s in srcs]
-    cmds = [[nvcc, *ARCH, *NVFLAGS, *extra_flags, "-c", s, "-o", o] for s, o in zip(srcs, objs)]
+    groups = {LIB: sources(), PROBE_LIB: sources("probe")}
+    jobs = []
+    for lib, srcs in groups.items():
+        for s in srcs:
+            jobs.append((lib, s, os.path.join(BUILD, os.path.basename(s)[:-3] + ".o")))
+    cmds = [[nvcc, *ARCH, *NVFLAGS, *extra_flags, "-c", s, "-o", o] for _, s, o in jobs]
     with ThreadPoolExecutor(max_workers=max(1, min(len(cmds), os.cpu_count() or 1))) as ex:
         outs = list(ex.map(_run, cmds))
     if verbose:
@@ -54,9 +59,11 @@ def build(verbose=False, extra_flags=()):
             print(" ".join(c))
             if o.strip():
                 print(o)
-    tmp = LIB + ".tmp"
-    _run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"])
-    os.replace(tmp, LIB)
+    for lib in groups:
+        objs = [o for l, _, o in jobs if l == lib]
+        tmp = lib + ".tmp"
+        _run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"])
+        os.replace(tmp, lib)
     return LIB
 
 

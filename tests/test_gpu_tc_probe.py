@@ -1,0 +1,37 @@
+"""tcgen05 descriptor/TMA/TMEM helpers checked on single 128x128x128 fp16 products
+against torch fp32 matmul (the helpers the LLA tensor kernel is built from)."""
+import ctypes
+import os
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+PROBE = os.path.join(os.path.dirname(HERE), "local_linear_attention_flashlla_gb300", "liblla_probe.so")
+
+
+def test_umma_descriptors_match_matmul(lla_gpu):
+    lib = ctypes.CDLL(PROBE)
+    lib.lla_probe_umma.restype = ctypes.c_int
+    lib.lla_probe_umma.argtypes = [ctypes.c_void_p] * 6
+    g = torch.Generator().manual_seed(0)
+    dev = torch.device("cuda:0")
+    A, B, B2 = (torch.randint(-8, 9, (128, 128), generator=g).to(torch.float16).to(dev) / 4 for _ in range(3))
+    D = [torch.full((128, 128), float("nan"), device=dev) for _ in range(3)]
+    rc = lib.lla_probe_umma(A.data_ptr(), B.data_ptr(), B2.data_ptr(), *(d.data_ptr() for d in D))
+    torch.cuda.synchronize()
+    assert rc == 0, rc
+    Af, Bf, B2f = A.float(), B.float(), B2.float()
+    want = [Af @ Bf.T, Af @ B2f, Af @ Bf.T]
+    names = ["SS K-major (TMA A)", "TS MN-major B", "SS K-major (thread-written A)"]
+    msgs = []
+    for name, d, w in zip(names, D, want):
+        err = (d - w).abs().max().item()
+        if not err <= 1e-3:
+            alt = {"A B2^T": (Af @ B2f.T), "A^T B": Af.T @ Bf, "(A B^T)^T": (Af @ Bf.T).T}
+            close = [k for k, v in alt.items() if (d - v).abs().max().item() < 1e-3]
+            msgs.append(f"{name}: max err {err} (matches {close})")
+    assert not msgs, "; ".join(msgs)
