@@ -286,12 +286,13 @@ def main():
     torch.cuda.synchronize()
     lla.lla_sync_status()
 
+    lla.lla_profile_enable(True)      # events around the dominant kernel of every call
     sampler = ClockSampler(local)
     sampler.start()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    times = []
+    times, main_times = [], []
     for _ in range(args.steps):
         flush.zero_()
         e0 = torch.cuda.Event(enable_timing=True)
@@ -301,10 +302,12 @@ def main():
         e1.record(stream)
         e1.synchronize()
         times.append(e0.elapsed_time(e1))
+        main_times.append(lla.lla_profile_read()[0])
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
+    lla.lla_profile_enable(False)
     lla.lla_sync_status()
     total_ms = sum(times)
     if world > 1:
@@ -357,9 +360,10 @@ def main():
                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in (ho, hr, hd))}
 
     peaks, peak_kind = load_peaks()
-    launches_per_step = 1 if rpath == lla.LLA_PATH_FP32 else 2
+    # fp32 path: one kernel per step; tensor path: max|x| pre-pass, fp16 conversion, fused sweep kernel
+    launches_per_step = 1 if rpath == lla.LLA_PATH_FP32 else 3
     kern_name = "lla_simt_kernel" if rpath == lla.LLA_PATH_FP32 else "lla_tc_kernel"
-    dominant_ms = ms_per_step     # the fp32 path is a single kernel per step
+    dominant_ms = sum(main_times) / len(main_times)
     achieved = flops / (dominant_ms / 1e3) / 1e12
     if rpath == lla.LLA_PATH_FP32:
         peak = fp32_alu_peak_tflops(peaks.get("sm_max_mhz", 2070.0))
@@ -384,6 +388,8 @@ def main():
                        "inputs": "bf16 q,k,v resident in HBM" if w.dtype == "bf16" else "fp32 q,k,v in HBM"},
             "tflops": tflops, "tflops_executed": world * executed_flops(w, T, rpath) * args.steps / (total_ms / 1e3) / 1e12,
             "roofline": roof, "clocks": clocks, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+            "dominant_kernel": {"name": kern_name, "ms_per_launch": dominant_ms,
+                                "share_of_step": dominant_ms / ms_per_step},
             "cg_iters_counted": T}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_throughput(w, qkv_host)

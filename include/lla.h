@@ -98,6 +98,17 @@ int lla_resolve_path(int dtype, int path, int d);
  */
 int lla_sync_status(void* stream);
 
+/*
+ * lla_profile_enable -- on != 0: every later call records CUDA events on its stream around its
+ * dominant kernel (the fused sweep kernel) and around the whole call; on == 0 stops.
+ * lla_profile_read -- elapsed milliseconds of the most recent profiled call: main_ms for the
+ * dominant kernel, total_ms for the whole call (either pointer may be NULL).  Waits for that
+ * call's events.  Returns LLA_ERR_INVALID_ARG if no call was profiled yet.  Measurement support
+ * for benchmarks; not thread-safe across concurrent profiled calls.
+ */
+int lla_profile_enable(int on);
+int lla_profile_read(float* main_ms, float* total_ms);
+
 /* Message for the calling thread's most recent failure ("" if none). Owned by the library. */
 const char* lla_last_error(void);
 

@@ -15,6 +15,7 @@ import os
 __all__ = [
     "LLAError", "load_library", "library_path", "forward", "lla_forward", "lla_forward_ex",
     "lla_workspace_size", "lla_resolve_path", "lla_sync_status", "lla_last_error", "lla_version",
+    "lla_profile_enable", "lla_profile_read",
     "LLA_OK", "LLA_ERR_INVALID_ARG", "LLA_ERR_UNSUPPORTED", "LLA_ERR_CUDA", "LLA_ERR_DEVICE_TIMEOUT",
     "LLA_DTYPE_BF16", "LLA_DTYPE_FP32", "LLA_PATH_AUTO", "LLA_PATH_TENSOR", "LLA_PATH_FP32",
     "EXPORTED_SYMBOLS",
@@ -39,6 +40,8 @@ _SIGNATURES = {
     "lla_resolve_path": (_c_int, [_c_int, _c_int, _c_int]),
     "lla_sync_status": (_c_int, [_vp]),
     "lla_last_error": (ctypes.c_char_p, []),
+    "lla_profile_enable": (_c_int, [_c_int]),
+    "lla_profile_read": (_c_int, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]),
     "lla_version": (_c_int, []),
 }
 EXPORTED_SYMBOLS = tuple(_SIGNATURES)
@@ -93,6 +96,18 @@ def lla_resolve_path(dtype, path, d):
 
 def lla_workspace_size(dtype, path, B, H, n, d):
     return load_library().lla_workspace_size(dtype, path, B, H, n, d)
+
+
+def lla_profile_enable(on=True):
+    """Record CUDA events around each later call's dominant kernel (measurement support)."""
+    _check(load_library().lla_profile_enable(1 if on else 0))
+
+
+def lla_profile_read():
+    """(dominant-kernel ms, whole-call ms) of the most recent profiled call."""
+    a, b = ctypes.c_float(), ctypes.c_float()
+    _check(load_library().lla_profile_read(ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
 
 
 def lla_sync_status(stream=None):

@@ -31,6 +31,13 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 __device__ unsigned g_device_error = 0;
 
+namespace {
+// Profiling events (call begin, main kernel begin, main kernel end, call end).
+bool g_prof_on = false;
+bool g_prof_valid = false;
+cudaEvent_t g_ev[4] = {nullptr, nullptr, nullptr, nullptr};
+}  // namespace
+
 unsigned* device_error_word() {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_device_error) != cudaSuccess) return nullptr;
@@ -64,7 +71,7 @@ const char* lla_last_error(void) { return lla::g_msg; }
 
 int lla_resolve_path(int dtype, int path, int d) {
     if (path != LLA_PATH_AUTO) return path;
-    (void)dtype; (void)d;  // the tensor path is selected automatically once it is built
+    if (dtype == LLA_DTYPE_BF16 && (d == 64 || d == 128)) return LLA_PATH_TENSOR;
     return LLA_PATH_FP32;
 }
 
@@ -98,11 +105,28 @@ int lla_forward_ex(int dtype, int path, const void* q, const void* k, const void
         return fail(LLA_ERR_UNSUPPORTED, "tensor path needs bf16 inputs and d in {64, 128}");
 
     cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-    lla::Problem p{q, k, v, out, rho, denom, cg_iters, B, H, n, d, tau, lambda, cg_max_iters, cg_tol, dtype};
+    lla::Problem p{q, k, v, out, rho, denom, cg_iters, B, H, n, d, tau, lambda, cg_max_iters, cg_tol, dtype,
+                   nullptr, nullptr};
+    if (lla::g_prof_on) {
+        for (int i = 0; i < 4; ++i)
+            if (!lla::g_ev[i]) {
+                cudaError_t e = cudaEventCreate(&lla::g_ev[i]);
+                if (e != cudaSuccess) return lla::cuda_fail(e, "profiling event");
+            }
+        p.ev_main_begin = lla::g_ev[1];
+        p.ev_main_end = lla::g_ev[2];
+        cudaError_t e = cudaEventRecord(lla::g_ev[0], stream);
+        if (e != cudaSuccess) return lla::cuda_fail(e, "profiling event record");
+    }
 
     if (rpath == LLA_PATH_FP32) {
         cudaError_t e = lla::launch_simt(p, stream);
         if (e != cudaSuccess) return lla::cuda_fail(e, "fp32 path launch");
+        if (lla::g_prof_on) {
+            e = cudaEventRecord(lla::g_ev[3], stream);
+            if (e != cudaSuccess) return lla::cuda_fail(e, "profiling event record");
+            lla::g_prof_valid = true;
+        }
         return LLA_OK;
     }
 
@@ -126,6 +150,28 @@ int lla_forward_ex(int dtype, int path, const void* q, const void* k, const void
         if (e == cudaSuccess && e2 != cudaSuccess) return lla::cuda_fail(e2, "cudaFreeAsync(workspace)");
     }
     if (e != cudaSuccess) return lla::cuda_fail(e, why ? why : "tensor path launch");
+    if (lla::g_prof_on) {
+        e = cudaEventRecord(lla::g_ev[3], stream);
+        if (e != cudaSuccess) return lla::cuda_fail(e, "profiling event record");
+        lla::g_prof_valid = true;
+    }
+    return LLA_OK;
+}
+
+int lla_profile_enable(int on) {
+    lla::g_prof_on = on != 0;
+    return LLA_OK;
+}
+
+int lla_profile_read(float* main_ms, float* total_ms) {
+    lla::g_msg[0] = '\0';
+    if (!lla::g_prof_valid) return fail(LLA_ERR_INVALID_ARG, "no profiled call yet");
+    cudaError_t e = cudaEventSynchronize(lla::g_ev[3]);
+    if (e != cudaSuccess) return lla::cuda_fail(e, "lla_profile_read");
+    if (main_ms && (e = cudaEventElapsedTime(main_ms, lla::g_ev[1], lla::g_ev[2])) != cudaSuccess)
+        return lla::cuda_fail(e, "lla_profile_read");
+    if (total_ms && (e = cudaEventElapsedTime(total_ms, lla::g_ev[0], lla::g_ev[3])) != cudaSuccess)
+        return lla::cuda_fail(e, "lla_profile_read");
     return LLA_OK;
 }
 

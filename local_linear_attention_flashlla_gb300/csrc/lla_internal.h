@@ -21,6 +21,8 @@ struct Problem {
     int cg_max_iters;
     float cg_tol;
     int dtype;           // lla_dtype
+    cudaEvent_t ev_main_begin;   // recorded just before / after the dominant kernel when profiling
+    cudaEvent_t ev_main_end;     // (null otherwise)
 };
 
 // Device error word: bit flags set by kernels whose bounded waits gave up.

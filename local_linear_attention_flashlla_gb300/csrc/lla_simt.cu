@@ -313,10 +313,13 @@ cudaError_t launch_typed(const Problem& p, cudaStream_t stream) {
     cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
     dim3 grid(n_tiles, p.B * p.H);
+    if (p.ev_main_begin && (err = cudaEventRecord(p.ev_main_begin, stream)) != cudaSuccess) return err;
     kern<<<grid, NT, smem, stream>>>(static_cast<const T*>(p.q), static_cast<const T*>(p.k),
                                      static_cast<const T*>(p.v), static_cast<T*>(p.out), p.rho, p.denom,
                                      p.cg_iters, p.n, n_tiles, p.tau, p.lambda, p.cg_max_iters, p.cg_tol);
-    return cudaGetLastError();
+    err = cudaGetLastError();
+    if (err == cudaSuccess && p.ev_main_end) err = cudaEventRecord(p.ev_main_end, stream);
+    return err;
 }
 
 template <typename T>

@@ -1,17 +1,968 @@
-// Tensor-core path of the causal LLA forward pass (placeholder until the tcgen05 kernel lands).
+// Tensor-core path of the causal LLA forward pass on sm_103a (tcgen05 + TMEM + TMA).
+//
+// Operands.  A pre-pass scales q, k, v (bf16) by per-tensor powers of two and stores them
+// as fp16 (exact for every value in fp16's normal range; the scale puts each tensor's
+// largest magnitude at or below 2^14).  fp16 is used instead of bf16 because the CG
+// products need the extra mantissa bits: the matrix-vector products of CG are only as
+// accurate as their rounded operands.  Every in-kernel operand (CG direction p, the
+// per-pair coefficients, rho') is likewise stored as fp16 times a per-row power of two
+// chosen from a bound on its magnitude, so nothing overflows and the exact unscaling is a
+// multiplication by a power of two.
+//
+// Kernel.  One CTA owns a tile of 128 queries of one (b, h) and runs the FlashLLA sweeps
+// of the Local Linear Attention reading notes (section 2.2, Algorithm 1) over the causal
+// key blocks of 128 keys (tile t sees blocks 0..t, the last one masked):
+//   MAX     S = Q K^T                                   -> exact row maxima m_i
+//   MOMENT  S, W = 2^(S*c - m) -> Y = W K                 -> omega_i, kbar_i = mu~_i / omega_i
+//   CG xT   S, A' = P K^T, M = W o (A' - kbar.p) -> Y = M K  -> (C_i/omega_i) p, CG update
+//   OUT     S, T = (R_hi + R_lo) K^T, U = W o (c - T) -> Y = U V -> out_i
+// CG runs on the centred system (C_i/omega_i) rho'_i = delta_i with delta_i = kbar_i - q_i;
+// rho_i = rho'_i / (1 + delta_i.rho'_i), denom_i = omega_i / (1 + delta_i.rho'_i), and
+// out_i = sum_j w_ij (1 - (k_j - kbar_i).rho'_i) v_j / sum_j w_ij (1 - (k_j - kbar_i).rho'_i)
+// (Eqs. (6)-(8) with Sigma_i = C_i + omega_i delta_i delta_i^T, Sherman-Morrison).
+//
+// Roles (384 threads, three warpgroups): warp 0 lane 0 issues TMA (Q once, then K/V blocks
+// into a 3-slot ring); warp 1 lane 0 issues every tcgen05.mma and commit (warps 2-3 idle);
+// warpgroups 1-2 (256 threads) do the elementwise work and the CG vector updates, thread =
+// (query row, half of the key block / half of the head dimension).  setmaxnreg moves
+// registers from warpgroup 0 (72 each) to the elementwise warpgroups (216 each):
+// 128 x 72 + 256 x 216 = 384 x 168, the launch allocation.  TMEM (512 columns): S double buffer (2 x 128), A' (128),
+// Y accumulator (d).  The pairwise weights never leave TMEM/registers; working memory in
+// HBM is the fp16 operand copies, the CG iterate (kept in the rho output) and kbar.
+// Every mbarrier wait is bounded (about 2 s); on a timeout the CTA drains its in-flight
+// copies and MMAs, frees TMEM and records the failure in the library's device error word.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <math.h>
 
 #include "lla_internal.h"
+#include "tc_host.h"
+#include "tc_ptx.cuh"
 
 namespace lla {
+namespace {
+using namespace tc;
 
-size_t tensor_workspace_bytes(int B, int H, int n, int d) {
-    return (size_t)3 * B * H * n * d * 2 + 256;
+constexpr int BQ = 128;            // queries per tile (MMA M)
+constexpr int BK = 128;            // keys per block (MMA N of QK^T, K of the Y product)
+constexpr int NTHREADS = 384;
+constexpr int NEW = 256;           // elementwise threads
+constexpr int NSLOT = 3;           // K/V ring slots
+constexpr int EW_BAR = 1;          // named barrier of the elementwise warps
+constexpr int HDR_BYTES = 256;
+
+enum SweepType : int { SW_MAX = 0, SW_MOMENT = 1, SW_CG = 2, SW_OUT = 3 };
+
+struct Header {
+    unsigned maxabs[3];            // float bits of max |q|, max |k|, max |v|
+    int abort;                     // set by a CTA whose bounded wait gave up: the others stop early
+};
+
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ceil(log2(x)) for finite x > 0
+__device__ __forceinline__ int ceil_log2f(float x) {
+    int e;
+    const float f = frexpf(x, &e);      // x = f 2^e, f in [0.5, 1)
+    return f == 0.5f ? e - 1 : e;
+}
+// exponent s such that x 2^s <= 2^14 with x 2^s > 2^13 (0 when x == 0)
+__device__ __forceinline__ int scale_exp(float maxabs) {
+    if (!(maxabs > 0.f)) return 0;
+    int s = 14 - ceil_log2f(maxabs);
+    return s < -100 ? -100 : (s > 100 ? 100 : s);
 }
 
-cudaError_t launch_tensor(const Problem&, void*, cudaStream_t, const char** why) {
-    *why = "tensor path not built";
-    return cudaErrorNotSupported;
+// ------------------------------------------------------------------------------------------
+// Pre-pass: max |x| per tensor, then scaled fp16 copies.
+__global__ void lla_maxabs_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                                  const __nv_bfloat16* __restrict__ v, size_t count8, Header* hdr) {
+    float m[3] = {0.f, 0.f, 0.f};
+    const __nv_bfloat16* src[3] = {q, k, v};
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < count8; idx += (size_t)gridDim.x * blockDim.x) {
+#pragma unroll
+        for (int t = 0; t < 3; ++t) {
+            const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src[t]) + idx);
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 f = __bfloat1622float2(h[u]);
+                m[t] = fmaxf(m[t], fmaxf(fabsf(f.x), fabsf(f.y)));
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < 3; ++t) {
+        float x = m[t];
+        for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+        if ((threadIdx.x & 31) == 0) atomicMax(&hdr->maxabs[t], __float_as_uint(x));
+    }
+}
+
+__global__ void lla_to_half_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
+                                   const __nv_bfloat16* __restrict__ v, __half* q16, __half* k16, __half* v16,
+                                   size_t count8, const Header* __restrict__ hdr) {
+    const __nv_bfloat16* src[3] = {q, k, v};
+    __half* dst[3] = {q16, k16, v16};
+    float sc[3];
+#pragma unroll
+    for (int t = 0; t < 3; ++t) sc[t] = pow2i(scale_exp(__uint_as_float(hdr->maxabs[t])));
+    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < count8; idx += (size_t)gridDim.x * blockDim.x) {
+#pragma unroll
+        for (int t = 0; t < 3; ++t) {
+            const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src[t]) + idx);
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+            uint4 o;
+            uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 f = __bfloat1622float2(h[u]);
+                ow[u] = pack_half2(f.x * sc[t], f.y * sc[t]);
+            }
+            reinterpret_cast<uint4*>(dst[t])[idx] = o;
+        }
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+template <int D>
+struct TcSmem {
+    static constexpr int NB = D / 64;                  // 64-column (128-byte) boxes per row
+    static constexpr int TILE = BQ * D * 2;            // bytes of a [128 x D] fp16 tile
+    unsigned char q[TILE];                             // queries (TMA)
+    unsigned char p[TILE];                             // CG direction P, then R_hi (rho', threads)
+    unsigned char rlo[TILE];                           // R_lo (output sweep); P_lo (CG sweeps of tile 0)
+    unsigned char slot[NSLOT][TILE];                   // K / V blocks (TMA)
+    uint64_t slot_full[NSLOT], slot_empty[NSLOT];
+    uint64_t q_full, s_full[2], ew_done[2], a_free, y_done, p_ready, mma_final;
+    float xch[6][2][BQ];                               // row-scalar exchange between the two halves
+    uint32_t tmem_base;
+    int err;
+    int next_type;
+};
+
+struct TcParams {
+    Header* hdr;
+    float* kbar;          // kbar, tile-transposed: [B*H][n_tiles][D][128] fp32 scratch
+    float* xs;            // CG iterate rho', same layout
+    __nv_bfloat16* out;
+    float* rho;
+    float* denom;
+    int* cg_iters;
+    unsigned* dev_err;
+    int n, n_tiles;
+    float tau, lambda, cg_tol;
+    int cg_max_iters;
+};
+
+// Sum (or max) of a per-row value over the two half-threads of the row.
+struct Xch {
+    float (*buf)[2][BQ];
+    int idx, half, row;
+    __device__ float sum(float v) {
+        float* b = &buf[idx][0][0];
+        idx = idx == 5 ? 0 : idx + 1;
+        b[half * BQ + row] = v;
+        named_bar_sync(EW_BAR, NEW);
+        return v + b[(1 - half) * BQ + row];
+    }
+    __device__ float max(float v) {
+        float* b = &buf[idx][0][0];
+        idx = idx == 5 ? 0 : idx + 1;
+        b[half * BQ + row] = v;
+        named_bar_sync(EW_BAR, NEW);
+        return fmaxf(v, b[(1 - half) * BQ + row]);
+    }
+};
+
+__device__ __forceinline__ bool ew_any(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, 1, 256, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+
+// Drain wait: ignores the error flag, bounded by its own timer (used only on exit).
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > 2000000000ull) return;
+}
+
+// fp16 element (row, col) of a swizzled [128 x D] tile
+__device__ __forceinline__ __half* tile_half(const unsigned char* t, int row, int col) {
+    return reinterpret_cast<__half*>(const_cast<unsigned char*>(t) + sw128_offset(row, col, BQ));
+}
+
+// max |res + beta p_old| over this thread's DH coordinates (p_old = (hi [+ lo] tile values) * osc)
+template <int DH>
+__device__ __forceinline__ float dir_maxabs(const float (&res)[DH], const unsigned char* ptile, const unsigned char* plo,
+                                            bool split, int row, int col0, float beta, bool keep_old, float osc) {
+    float mp = 0.f;
+#pragma unroll
+    for (int e0 = 0; e0 < DH; e0 += 8) {
+        const uint4 old = *reinterpret_cast<const uint4*>(tile_half(ptile, row, col0 + e0));
+        uint4 oldl = make_uint4(0u, 0u, 0u, 0u);
+        if (split) oldl = *reinterpret_cast<const uint4*>(tile_half(plo, row, col0 + e0));
+        const __half* oh = reinterpret_cast<const __half*>(&old);
+        const __half* ol = reinterpret_cast<const __half*>(&oldl);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float pold = keep_old ? (__half2float(oh[u]) + __half2float(ol[u])) * osc : 0.f;
+            mp = fmaxf(mp, fabsf(fmaf(beta, pold, res[e0 + u])));
+        }
+    }
+    return mp;
+}
+
+// Store fp16((res + beta p_old) * nsc) over the old values (and, when split, the fp16 remainder
+// in the lo tile, so hi + lo carries about 22 bits); returns kbar . p_hat (partial), p_hat being
+// the stored value.  kbt: this thread's kbar coordinates, stride BQ floats (tile-transposed).
+template <int DH>
+__device__ __forceinline__ float dir_store(const float (&res)[DH], unsigned char* ptile, unsigned char* plo, bool split,
+                                           int row, int col0, float beta, bool keep_old, float osc, float nsc,
+                                           float nisc, const float* kbt) {
+    float kp = 0.f;
+#pragma unroll
+    for (int e0 = 0; e0 < DH; e0 += 8) {
+        __half* hp = tile_half(ptile, row, col0 + e0);   // 8 consecutive columns = one 16-byte chunk
+        __half* lp = tile_half(plo, row, col0 + e0);
+        const uint4 old = *reinterpret_cast<const uint4*>(hp);
+        uint4 oldl = make_uint4(0u, 0u, 0u, 0u);
+        if (split) oldl = *reinterpret_cast<const uint4*>(lp);
+        const __half* oh = reinterpret_cast<const __half*>(&old);
+        const __half* ol = reinterpret_cast<const __half*>(&oldl);
+        uint4 pk, pl;
+        uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
+        uint32_t* plw = reinterpret_cast<uint32_t*>(&pl);
+#pragma unroll
+        for (int u = 0; u < 8; u += 2) {
+            const float o0 = keep_old ? (__half2float(oh[u]) + __half2float(ol[u])) * osc : 0.f;
+            const float o1 = keep_old ? (__half2float(oh[u + 1]) + __half2float(ol[u + 1])) * osc : 0.f;
+            const float p0 = fmaf(beta, o0, res[e0 + u]) * nsc;
+            const float p1 = fmaf(beta, o1, res[e0 + u + 1]) * nsc;
+            pw[u >> 1] = pack_half2(p0, p1);
+            float2 ph = __half22float2(*reinterpret_cast<const __half2*>(&pw[u >> 1]));
+            if (split) {
+                plw[u >> 1] = pack_half2(p0 - ph.x, p1 - ph.y);
+                const float2 pl2 = __half22float2(*reinterpret_cast<const __half2*>(&plw[u >> 1]));
+                ph.x += pl2.x;
+                ph.y += pl2.y;
+            }
+            kp = fmaf(kbt[(e0 + u) * BQ], ph.x * nisc, kp);
+            kp = fmaf(kbt[(e0 + u + 1) * BQ], ph.y * nisc, kp);
+        }
+        *reinterpret_cast<uint4*>(hp) = pk;
+        if (split) *reinterpret_cast<uint4*>(lp) = pl;
+    }
+    return kp;
+}
+
+// One 32-coordinate chunk of (C/omega) p and of p_hat for this thread's row.
+__device__ __forceinline__ void cp_chunk32(uint32_t ty, const unsigned char* ptile, const unsigned char* plo, bool split,
+                                           int row, int col, const float* kbt_c, float ysc, float msc, float lam_n,
+                                           float psc, float (&cp)[32], float (&ph)[32]) {
+    float v[32];
+    tmem_ld32(ty, v);
+#pragma unroll
+    for (int j = 0; j < 32; j += 8) {
+        const uint4 pr = *reinterpret_cast<const uint4*>(tile_half(ptile, row, col + j));
+        uint4 prl = make_uint4(0u, 0u, 0u, 0u);
+        if (split) prl = *reinterpret_cast<const uint4*>(tile_half(plo, row, col + j));
+        const __half* phh = reinterpret_cast<const __half*>(&pr);
+        const __half* phl = reinterpret_cast<const __half*>(&prl);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) ph[j + u] = (__half2float(phh[u]) + __half2float(phl[u])) * psc;
+    }
+    float kv[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) kv[j] = kbt_c[j * BQ];
+    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) cp[j] = fmaf(v[j], ysc, fmaf(-kv[j], msc, lam_n * ph[j]));
+}
+
+// Per-pair coefficients of one 32-key chunk (chunk C of this thread's 64 keys):
+//   HAS_A:  out_j = 2^(s_j c - off) (base + sign a_j)     (CG: base = -kbar.p, sign = +1;
+//                                                          output: base = c, sign = -1)
+//   !HAS_A: out_j = 2^(s_j c - off)                       (moments)
+// zero where MASKED and key column > lim.  Packs pairs to fp16 and accumulates their sum.
+template <bool MASKED, bool HAS_A, int C>
+__device__ __forceinline__ void coef_chunk(const float (&v)[32], const float (&a)[64], float c_log2, float off,
+                                           float base, float sign, int col0, int lim, float& sum,
+                                           uint32_t (&pk)[16]) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        float m0 = ex2(fmaf(v[j], c_log2, -off));
+        float m1 = ex2(fmaf(v[j + 1], c_log2, -off));
+        if (HAS_A) {
+            m0 *= fmaf(sign, a[C * 32 + j], base);
+            m1 *= fmaf(sign, a[C * 32 + j + 1], base);
+        }
+        if (MASKED) {
+            m0 = (col0 + j <= lim) ? m0 : 0.f;
+            m1 = (col0 + j + 1 <= lim) ? m1 : 0.f;
+        }
+        sum += m0 + m1;
+        pk[j >> 1] = pack_half2(m0, m1);
+    }
+}
+
+// One 128 x 128 x D product D[tmem] = A[smem] B[smem]^T, both K-major SW128 tiles, D/16 k-steps.
+// Descriptors are built once; each k-step adds a compile-time start-address offset (bytes >> 4),
+// which never carries out of the 14-bit field for tiles inside the 228 KB of shared memory.
+template <int D, bool ACC_FIRST>
+__device__ __forceinline__ void gemm_qk(uint32_t d_tmem, uint32_t a_addr, uint32_t b_addr) {
+    constexpr uint32_t ID = idesc_f16(BQ, BK, false);
+    const uint64_t a0 = sdesc_sw128(a_addr, 16, 1024), b0 = sdesc_sw128(b_addr, 16, 1024);
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        const uint64_t off = (uint64_t)((((ks >> 2) * (BQ * 128)) + (ks & 3) * 32) >> 4);
+        if (ks == 0 && !ACC_FIRST) umma_ss_c<false>(d_tmem, a0 + off, b0 + off, ID);
+        else umma_ss_c<true>(d_tmem, a0 + off, b0 + off, ID);
+    }
+}
+// Y[tmem] (+)= M[tmem] (128 x 128 keys, fp16 pairs at columns 64h + 0..31 per key half h) x B,
+// B = a [128 keys x D] K/V slot read MN-major.
+template <int D>
+__device__ __forceinline__ void gemm_y(uint32_t y_tmem, uint32_t m_tmem, uint32_t b_addr, bool acc) {
+    constexpr uint32_t ID = idesc_f16(BQ, D, true);
+    const uint64_t b0 = sdesc_sw128(b_addr, BK * 128, 1024);
+    if (acc) umma_ts_c<true>(y_tmem, m_tmem, b0, ID);
+    else umma_ts_c<false>(y_tmem, m_tmem, b0, ID);
+#pragma unroll
+    for (int ks = 1; ks < BK / 16; ++ks)
+        umma_ts_c<true>(y_tmem, m_tmem + (ks >> 2) * 64 + (ks & 3) * 8, b0 + (uint64_t)((ks * 2048) >> 4), ID);
+}
+
+template <int D>
+__global__ void __launch_bounds__(NTHREADS, 1)
+lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v, const TcParams prm) {
+    using S = TcSmem<D>;
+    constexpr int NB = S::NB;
+    constexpr int DH = D / 2;                       // head-dim coordinates per elementwise thread
+
+    extern __shared__ unsigned char smem_raw[];
+    S& s = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    volatile int* err = &s.err;
+    volatile int* abort_flag = &prm.hdr->abort;
+#define WAIT(bar, par, e) mbar_wait_abortable(bar, par, e, abort_flag)
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int tile = prm.n_tiles - 1 - (int)blockIdx.x;
+    const int head = blockIdx.y;
+    const int n = prm.n;
+    const int nkb = tile + 1;
+    const bool dynamic = prm.cg_tol > 0.f;
+
+    if (tid == 0) {
+        s.err = *abort_flag ? 1 : 0;           // another CTA of this launch already gave up
+        s.next_type = SW_CG;
+        for (int i = 0; i < NSLOT; ++i) {
+            mbar_init(&s.slot_full[i], 1);
+            mbar_init(&s.slot_empty[i], 1);
+        }
+        mbar_init(&s.q_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s.s_full[i], 1);
+            mbar_init(&s.ew_done[i], NEW);
+        }
+        mbar_init(&s.a_free, NEW);
+        mbar_init(&s.y_done, 1);
+        mbar_init(&s.p_ready, NEW);
+        mbar_init(&s.mma_final, 1);
+        mbar_fence_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&s.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tS0 = s.tmem_base, tA = s.tmem_base + 256, tY = s.tmem_base + 384;
+
+    if (warp < 4) {
+    // warpgroup 0: the register release dominates the producer and MMA code, so both are
+    // compiled within 72 registers
+    setmaxnreg_dec72();
+    if (warp == 0) {
+        // =============================== TMA producer ===============================
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            mbar_arrive_expect_tx(&s.q_full, S::TILE);
+            for (int bx = 0; bx < NB; ++bx) tma_load_3d(s.q + bx * BQ * 128, &tm_q, &s.q_full, bx * 64, tile * BQ, head);
+            uint32_t fill = 0, pr = 0;
+            int cg_sweeps = 0;
+            int type = SW_MAX;
+            for (int sweep = 0; !*err; ++sweep) {
+                if (sweep == 0) type = SW_MAX;
+                else if (sweep == 1) type = SW_MOMENT;
+                else if (!dynamic) type = cg_sweeps < prm.cg_max_iters ? SW_CG : SW_OUT;
+                else {
+                    if (!WAIT(&s.p_ready, pr & 1, err)) break;
+                    ++pr;
+                    type = s.next_type;
+                }
+                if (type == SW_CG) ++cg_sweeps;
+                for (int kb = 0; kb < nkb && !*err; ++kb) {
+                    const int nload = type == SW_OUT ? 2 : 1;
+                    for (int l = 0; l < nload; ++l) {
+                        const int sl = fill % NSLOT;
+                        if (!WAIT(&s.slot_empty[sl], ((fill / NSLOT) & 1) ^ 1, err)) break;
+                        mbar_arrive_expect_tx(&s.slot_full[sl], S::TILE);
+                        const CUtensorMap* tm = l == 0 ? &tm_k : &tm_v;
+                        for (int bx = 0; bx < NB; ++bx)
+                            tma_load_3d(s.slot[sl] + bx * BK * 128, tm, &s.slot_full[sl], bx * 64, kb * BK, head);
+                        ++fill;
+                    }
+                }
+                if (type == SW_OUT) break;
+            }
+            // drain: every armed slot's last fill must land before the CTA exits
+            for (uint32_t f = fill > NSLOT ? fill - NSLOT : 0; f < fill; ++f)
+                mbar_drain(&s.slot_full[f % NSLOT], (f / NSLOT) & 1);
+            mbar_drain(&s.q_full, 0);
+        }
+    } else if (warp == 1) {
+        // =============================== MMA issuer ===============================
+        if (lane == 0) {
+            const uint32_t q_addr = smem_u32(s.q), p_addr = smem_u32(s.p), rlo_addr = smem_u32(s.rlo);
+            uint32_t fill = 0, pr = 0, g = 0, ew_seen = 0, ga = 0;
+            auto wait_ew = [&](uint32_t upto) {          // elementwise work of blocks < upto finished
+                while (ew_seen < upto) {
+                    if (!WAIT(&s.ew_done[ew_seen & 1], (ew_seen >> 1) & 1, err)) return false;
+                    ++ew_seen;
+                }
+                return true;
+            };
+            bool ok = WAIT(&s.q_full, 0, err);
+            int cg_sweeps = 0;
+            for (int sweep = 0; ok; ++sweep) {
+                int type;
+                bool have_p = false;
+                if (sweep == 0) type = SW_MAX;
+                else if (sweep == 1) type = SW_MOMENT;
+                else if (!dynamic) type = cg_sweeps < prm.cg_max_iters ? SW_CG : SW_OUT;
+                else {
+                    if (!(ok = WAIT(&s.p_ready, pr & 1, err))) break;
+                    ++pr;
+                    have_p = true;
+                    type = s.next_type;
+                }
+                if (type == SW_CG) ++cg_sweeps;
+                const bool two = type == SW_CG || type == SW_OUT;
+                uint32_t prev_k = 0, prev_v = 0;
+                for (int kb = 0; kb < nkb && ok; ++kb) {
+                    const uint32_t fk = fill++;
+                    const uint32_t fv = type == SW_OUT ? fill++ : 0;
+                    const int sk = fk % NSLOT;
+                    if (!(ok = WAIT(&s.slot_full[sk], (fk / NSLOT) & 1, err))) break;
+                    const uint32_t b = g & 1;
+                    if (g >= 2 && !(ok = wait_ew(g - 1))) break;
+                    tc_fence_after();
+                    const uint32_t k_addr = smem_u32(s.slot[sk]);
+                    const uint32_t tS = tS0 + b * 128;
+                    gemm_qk<D, false>(tS, q_addr, k_addr);
+                    if (two) {
+                        if (!have_p) {
+                            if (!(ok = WAIT(&s.p_ready, pr & 1, err))) break;
+                            ++pr;
+                            have_p = true;
+                        }
+                        // A' is single-buffered: the elementwise threads release it as soon as they
+                        // have copied the previous block's A' into registers
+                        if (ga >= 1 && !(ok = WAIT(&s.a_free, (ga - 1) & 1, err))) break;
+                        ++ga;
+                        tc_fence_after();
+                        gemm_qk<D, false>(tA, p_addr, k_addr);
+                        // T = (R_hi + R_lo) K^T; in the first tile also A' = (P_hi + P_lo) K^T
+                        if (type == SW_OUT || tile == 0) gemm_qk<D, true>(tA, rlo_addr, k_addr);
+                    }
+                    umma_commit(&s.s_full[b]);
+                    if (type == SW_MAX) umma_commit(&s.slot_empty[sk]);
+                    // Y product of the previous block
+                    auto issue_y = [&](uint32_t gb, uint32_t f_k, uint32_t f_v, bool acc) {
+                        if (!wait_ew(gb + 1)) return false;
+                        if (type == SW_OUT && !WAIT(&s.slot_full[f_v % NSLOT], (f_v / NSLOT) & 1, err)) return false;
+                        tc_fence_after();
+                        const uint32_t src = smem_u32(s.slot[(type == SW_OUT ? f_v : f_k) % NSLOT]);
+                        const uint32_t tM = tS0 + (gb & 1) * 128;
+                        gemm_y<D>(tY, tM, src, acc);
+                        umma_commit(&s.slot_empty[f_k % NSLOT]);
+                        if (type == SW_OUT) umma_commit(&s.slot_empty[f_v % NSLOT]);
+                        return true;
+                    };
+                    if (type != SW_MAX && kb >= 1 && !(ok = issue_y(g - 1, prev_k, prev_v, kb - 1 > 0))) break;
+                    prev_k = fk;
+                    prev_v = fv;
+                    ++g;
+                    if (type != SW_MAX && kb == nkb - 1) {
+                        if (!(ok = issue_y(g - 1, prev_k, prev_v, nkb - 1 > 0))) break;
+                        umma_commit(&s.y_done);
+                    }
+                }
+                if (type == SW_OUT) break;
+            }
+            umma_commit(&s.mma_final);
+            mbar_drain(&s.mma_final, 0);
+        }
+    }
+    } else {
+        // =========================== elementwise + CG warps ===========================
+        setmaxnreg_inc216();
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        const int half = (warp - 4) >> 2;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        const int i = tile * BQ + row;
+        const bool row_ok = i < n;
+        const bool tile_full = (tile + 1) * BQ <= n;     // every row of the tile exists
+        // the first tile holds the rows i < d whose key scatter is rank-deficient: there the CG
+        // direction is kept to about 22 bits (hi + lo fp16 halves, one extra MMA per CG block)
+        const bool split_p = tile == 0;
+        const size_t row_g = ((size_t)head * n + (row_ok ? i : 0)) * D + half * DH;
+        // tile-transposed fp32 scratch: coordinate e of this thread's row at [e * BQ] (coalesced)
+        const size_t tbase = ((size_t)(head * prm.n_tiles + tile) * D + half * DH) * BQ + row;
+        float* xt = prm.xs + tbase;             // CG iterate x = rho'
+        float* kbt = prm.kbar + tbase;          // kbar
+        Xch xch{s.xch, 0, half, row};
+
+        const float mk = __uint_as_float(prm.hdr->maxabs[1]);
+        const int eq = scale_exp(__uint_as_float(prm.hdr->maxabs[0]));
+        const int ek = scale_exp(mk);
+        const int ev = scale_exp(__uint_as_float(prm.hdr->maxabs[2]));
+        const float c_log2 = prm.tau * 1.4426950408889634f * pow2i(-(eq + ek));
+        const float kbound = 2.f * (float)D * mk;      // |(k_j - kbar).u| <= kbound * max|u|
+        uint32_t g = 0, yd = 0;
+        bool ok = WAIT(&s.q_full, 0, err);
+        const float a_none[64] = {};                   // placeholder operand of the moment sweep
+        // last valid key column of block kb for this row (-1: none)
+        auto lim_of = [&](int kb) { return row_ok ? (kb < tile ? BK - 1 : i - kb * BK) : -1; };
+        auto wait_s = [&](uint32_t gg) {
+            const bool r = WAIT(&s.s_full[gg & 1], (gg >> 1) & 1, err);
+            tc_fence_after();
+            return r;
+        };
+        auto done_block = [&](uint32_t gg) {
+            tc_fence_before();
+            mbar_arrive(&s.ew_done[gg & 1]);
+        };
+        auto wait_y = [&]() {
+            const bool r = WAIT(&s.y_done, yd & 1, err);
+            ++yd;
+            tc_fence_after();
+            return r;
+        };
+
+        // ---------------- MAX sweep ----------------
+        float mx = -INFINITY;
+        for (int kb = 0; kb < nkb; ++kb, ++g) {
+            ok = ok && wait_s(g);
+            const uint32_t tS = tS0 + (g & 1) * 128 + lane_off + half * 64;
+            float v0[32], v1[32];
+            tmem_ld32(tS, v0);
+            tmem_ld32(tS + 32, v1);
+            tmem_ld_wait();
+            done_block(g);
+            const int lim = lim_of(kb);
+            if (tile_full && kb < tile) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) mx = fmaxf(mx, fmaxf(v0[j], v1[j]));
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    mx = fmaxf(mx, (half * 64 + j <= lim) ? v0[j] : -INFINITY);
+                    mx = fmaxf(mx, (half * 64 + 32 + j <= lim) ? v1[j] : -INFINITY);
+                }
+            }
+        }
+        mx = xch.max(mx);
+        const float m2 = row_ok ? mx * c_log2 : 0.f;
+
+        // ---------------- MOMENT sweep ----------------
+        float om_part = 0.f;
+        for (int kb = 0; kb < nkb; ++kb, ++g) {
+            ok = ok && wait_s(g);
+            const uint32_t tS = tS0 + (g & 1) * 128 + lane_off + half * 64;
+            const int lim = lim_of(kb);
+            const bool masked = !(tile_full && kb < tile);
+            float v[32];
+            uint32_t pk[16];
+            tmem_ld32(tS, v);
+            tmem_ld_wait();
+            if (masked) coef_chunk<true, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, half * 64, lim, om_part, pk);
+            else coef_chunk<false, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, 0, 0, om_part, pk);
+            tmem_st16(tS, pk);
+            tmem_ld32(tS + 32, v);
+            tmem_ld_wait();
+            if (masked) coef_chunk<true, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, half * 64 + 32, lim, om_part, pk);
+            else coef_chunk<false, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, 0, 0, om_part, pk);
+            tmem_st16(tS + 16, pk);
+            tmem_st_wait();
+            done_block(g);
+        }
+        ok = ok && wait_y();
+        const float om_all = xch.sum(om_part);      // every elementwise thread joins the exchange
+        const float omega = row_ok ? om_all * pow2i(-14) : 1.f;
+        const float inv_om = 1.f / omega;
+        const float lam_n = prm.lambda * inv_om;
+
+        // kbar, delta, CG initialisation (this thread: coordinates half*DH .. half*DH+DH-1)
+        float res[DH];
+        {
+            const float ysc = pow2i(-(14 + ek)) * inv_om;
+            const float qsc = pow2i(-eq);
+#pragma unroll
+            for (int c = 0; c < DH / 32; ++c) {
+                float v[32];
+                tmem_ld32(tY + lane_off + half * DH + c * 32, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; j += 8) {
+                    const uint4 qr = *reinterpret_cast<const uint4*>(tile_half(s.q, row, half * DH + c * 32 + j));
+                    const __half* qh = reinterpret_cast<const __half*>(&qr);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const float kb_ = v[j + u] * ysc;
+                        kbt[(c * 32 + j + u) * BQ] = kb_;
+                        xt[(c * 32 + j + u) * BQ] = 0.f;
+                        res[c * 32 + j + u] = row_ok ? kb_ - __half2float(qh[u]) * qsc : 0.f;
+                    }
+                }
+            }
+        }
+
+        float gamma;
+        {
+            float gp = 0.f;
+#pragma unroll
+            for (int e = 0; e < DH; ++e) gp = fmaf(res[e], res[e], gp);
+            gamma = xch.sum(gp);
+        }
+        const float rn0 = sqrtf(gamma);
+        bool active = row_ok && gamma > 0.f && !(sqrtf(gamma) <= prm.cg_tol * rn0);
+        int iters = 0;
+
+        // p = res + beta p_old as the next direction (fp16 x 2^sp); per-row params of the sweep
+        int sp = 0, sM = 0;
+        float kp_acc = 0.f, offM = 0.f;
+#define LLA_SET_DIRECTION(BETA, KEEP)                                                                      \
+        {                                                                                                  \
+            const float osc_ = pow2i(-sp);                                                                 \
+            const float mp_ = xch.max(dir_maxabs<DH>(res, s.p, s.rlo, split_p, row, half * DH, (BETA), (KEEP), \
+                                                      osc_));                                              \
+            const int sp_new_ = min(scale_exp(mp_), 100 - ek);   /* keeps 2^(sp+ek) finite */             \
+            const float kp_ = xch.sum(dir_store<DH>(res, s.p, s.rlo, split_p, row, half * DH, (BETA), (KEEP), \
+                                                    osc_,                                                  \
+                                                    pow2i(sp_new_), pow2i(-sp_new_), kbt));                \
+            sp = sp_new_;                                                                                  \
+            sM = scale_exp(kbound * mp_ * 1.001f);                                                         \
+            offM = m2 - (float)sM + (float)sp + (float)ek;                                                 \
+            kp_acc = kp_ * pow2i(sp + ek);                                                                 \
+        }
+        LLA_SET_DIRECTION(0.f, false);
+
+        // ---------------- CG sweeps ----------------
+        int cg_sweeps = 0;
+        while (true) {                         // uniform across the elementwise threads
+            bool go;
+            if (!dynamic) go = cg_sweeps < prm.cg_max_iters;
+            else go = ew_any(active) && cg_sweeps < prm.cg_max_iters;
+            if (!go) break;
+            if (tid == 128) s.next_type = SW_CG;
+            fence_proxy_async_smem();
+            mbar_arrive(&s.p_ready);
+            ++cg_sweeps;
+            float msum_part = 0.f;
+            for (int kb = 0; kb < nkb; ++kb, ++g) {
+                ok = ok && wait_s(g);
+                const uint32_t tS = tS0 + (g & 1) * 128 + lane_off + half * 64;
+                const uint32_t tAh = tA + lane_off + half * 64;
+                const int lim = lim_of(kb);
+                const bool masked = !(tile_full && kb < tile);
+                float a[64], v[32];
+                uint32_t pk[16];
+                tmem_ld32(tAh, *reinterpret_cast<float(*)[32]>(&a[0]));
+                tmem_ld32(tAh + 32, *reinterpret_cast<float(*)[32]>(&a[32]));
+                tmem_ld32(tS, v);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&s.a_free);
+                if (masked) coef_chunk<true, true, 0>(v, a, c_log2, offM, -kp_acc, 1.f, half * 64, lim, msum_part, pk);
+                else coef_chunk<false, true, 0>(v, a, c_log2, offM, -kp_acc, 1.f, 0, 0, msum_part, pk);
+                tmem_st16(tS, pk);
+                tmem_ld32(tS + 32, v);
+                tmem_ld_wait();
+                if (masked) coef_chunk<true, true, 1>(v, a, c_log2, offM, -kp_acc, 1.f, half * 64 + 32, lim, msum_part, pk);
+                else coef_chunk<false, true, 1>(v, a, c_log2, offM, -kp_acc, 1.f, 0, 0, msum_part, pk);
+                tmem_st16(tS + 16, pk);
+                tmem_st_wait();
+                done_block(g);
+            }
+            ok = ok && wait_y();
+            // ---- CG update: (C/omega) p = [Y 2^-(sM+ek) - kbar msum 2^-sM] / omega + (lambda/omega) p
+            const float msum = xch.sum(msum_part);
+            const float ysc = pow2i(-(sM + ek)) * inv_om;
+            const float msc = msum * pow2i(-sM) * inv_om;
+            const float psc = pow2i(-sp);
+            float pcp = 0.f;
+#pragma unroll
+            for (int c = 0; c < DH / 32; ++c) {
+                float cp[32], ph[32];
+                cp_chunk32(tY + lane_off + half * DH + c * 32, s.p, s.rlo, split_p, row, half * DH + c * 32, kbt + c * 32 * BQ, ysc,
+                           msc, lam_n, psc, cp, ph);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) pcp = fmaf(ph[j], cp[j], pcp);
+            }
+            pcp = xch.sum(pcp);
+            const bool upd = active && pcp > 0.f;
+            const float alpha = upd ? gamma / pcp : 0.f;
+            float g2 = 0.f;
+#pragma unroll
+            for (int c = 0; c < DH / 32; ++c) {
+                float cp[32], ph[32];
+                cp_chunk32(tY + lane_off + half * DH + c * 32, s.p, s.rlo, split_p, row, half * DH + c * 32, kbt + c * 32 * BQ, ysc,
+                           msc, lam_n, psc, cp, ph);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    if (upd) {
+                        xt[(c * 32 + j) * BQ] = fmaf(alpha, ph[j], xt[(c * 32 + j) * BQ]);
+                        res[c * 32 + j] = fmaf(-alpha, cp[j], res[c * 32 + j]);
+                    }
+                    g2 = fmaf(res[c * 32 + j], res[c * 32 + j], g2);
+                }
+            }
+            g2 = xch.sum(g2);
+            float beta = 0.f;
+            if (upd) {
+                beta = g2 / gamma;
+                gamma = g2;
+                ++iters;
+                if (gamma == 0.f || sqrtf(gamma) <= prm.cg_tol * rn0) active = false;
+            } else {
+                active = false;
+            }
+            if (!active) {
+#pragma unroll
+                for (int e = 0; e < DH; ++e) res[e] = 0.f;   // finished rows keep a zero direction
+                beta = 0.f;
+            }
+            LLA_SET_DIRECTION(beta, true);
+        }
+
+        // ---------------- finalise rho, denom; R = rho' (hi + lo) for the output sweep ----------------
+        float dx = 0.f, mxx = 0.f;
+        {
+            const float qsc = pow2i(-eq);
+#pragma unroll
+            for (int e0 = 0; e0 < DH; e0 += 8) {
+                const uint4 qr = *reinterpret_cast<const uint4*>(tile_half(s.q, row, half * DH + e0));
+                const __half* qh = reinterpret_cast<const __half*>(&qr);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const float xv = xt[(e0 + u) * BQ];
+                    dx = fmaf(kbt[(e0 + u) * BQ] - __half2float(qh[u]) * qsc, xv, dx);
+                    mxx = fmaxf(mxx, fabsf(xv));
+                }
+            }
+            if (!row_ok) { dx = 0.f; mxx = 0.f; }
+        }
+        dx = xch.sum(dx);
+        mxx = xch.max(mxx);
+        const float inv_g = 1.f / (1.f + dx);
+        const int sr = min(scale_exp(mxx), 100 - ek);
+        float kx = 0.f;
+        {
+            const float rs = pow2i(sr), ris = pow2i(-sr);
+#pragma unroll
+            for (int e0 = 0; e0 < DH; e0 += 8) {
+                uint4 pk, pl;
+                uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
+                uint32_t* plw = reinterpret_cast<uint32_t*>(&pl);
+                float xr[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) xr[u] = row_ok ? xt[(e0 + u) * BQ] : 0.f;
+#pragma unroll
+                for (int u = 0; u < 8; u += 2) {
+                    const float x0 = xr[u] * rs, x1 = xr[u + 1] * rs;
+                    pw[u >> 1] = pack_half2(x0, x1);
+                    const float2 xh = __half22float2(*reinterpret_cast<const __half2*>(&pw[u >> 1]));
+                    plw[u >> 1] = pack_half2(x0 - xh.x, x1 - xh.y);
+                    const float2 xl = __half22float2(*reinterpret_cast<const __half2*>(&plw[u >> 1]));
+                    kx = fmaf(kbt[(e0 + u) * BQ], (xh.x + xl.x) * ris, kx);
+                    kx = fmaf(kbt[(e0 + u + 1) * BQ], (xh.y + xl.y) * ris, kx);
+                }
+                *reinterpret_cast<uint4*>(tile_half(s.p, row, half * DH + e0)) = pk;
+                *reinterpret_cast<uint4*>(tile_half(s.rlo, row, half * DH + e0)) = pl;
+                if (row_ok) {   // rho = rho' / (1 + delta.rho'), row-major output
+                    *reinterpret_cast<float4*>(prm.rho + row_g + e0) =
+                        make_float4(xr[0] * inv_g, xr[1] * inv_g, xr[2] * inv_g, xr[3] * inv_g);
+                    *reinterpret_cast<float4*>(prm.rho + row_g + e0 + 4) =
+                        make_float4(xr[4] * inv_g, xr[5] * inv_g, xr[6] * inv_g, xr[7] * inv_g);
+                }
+            }
+            if (!row_ok) kx = 0.f;
+        }
+        kx = xch.sum(kx);
+        if (row_ok && half == 0) {
+            prm.denom[(size_t)head * n + i] = omega * inv_g;
+            if (prm.cg_iters) prm.cg_iters[(size_t)head * n + i] = iters;
+        }
+        const int sU = scale_exp((1.f + kbound * mxx) * 1.001f);
+        const float offU = m2 - (float)sU + (float)sr + (float)ek;
+        const float c_acc = (1.f + kx) * pow2i(sr + ek);
+        if (tid == 128) s.next_type = SW_OUT;
+        fence_proxy_async_smem();
+        mbar_arrive(&s.p_ready);
+
+        // ---------------- OUT sweep ----------------
+        float us_part = 0.f;
+        for (int kb = 0; kb < nkb; ++kb, ++g) {
+            ok = ok && wait_s(g);
+            const uint32_t tS = tS0 + (g & 1) * 128 + lane_off + half * 64;
+            const uint32_t tAh = tA + lane_off + half * 64;
+            const int lim = lim_of(kb);
+            const bool masked = !(tile_full && kb < tile);
+            float a[64], v[32];
+            uint32_t pk[16];
+            tmem_ld32(tAh, *reinterpret_cast<float(*)[32]>(&a[0]));
+            tmem_ld32(tAh + 32, *reinterpret_cast<float(*)[32]>(&a[32]));
+            tmem_ld32(tS, v);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&s.a_free);
+            if (masked) coef_chunk<true, true, 0>(v, a, c_log2, offU, c_acc, -1.f, half * 64, lim, us_part, pk);
+            else coef_chunk<false, true, 0>(v, a, c_log2, offU, c_acc, -1.f, 0, 0, us_part, pk);
+            tmem_st16(tS, pk);
+            tmem_ld32(tS + 32, v);
+            tmem_ld_wait();
+            if (masked) coef_chunk<true, true, 1>(v, a, c_log2, offU, c_acc, -1.f, half * 64 + 32, lim, us_part, pk);
+            else coef_chunk<false, true, 1>(v, a, c_log2, offU, c_acc, -1.f, 0, 0, us_part, pk);
+            tmem_st16(tS + 16, pk);
+            tmem_st_wait();
+            done_block(g);
+        }
+        ok = ok && wait_y();
+        const float usum = xch.sum(us_part);
+        const float osc = pow2i(-ev) / usum;
+#pragma unroll
+        for (int c = 0; c < DH / 32; ++c) {
+            float v[32];
+            tmem_ld32(tY + lane_off + half * DH + c * 32, v);
+            tmem_ld_wait();
+            if (row_ok) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 8) {
+                    uint4 o;
+                    __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) ob[u] = __floats2bfloat162_rn(v[j + 2 * u] * osc, v[j + 2 * u + 1] * osc);
+                    *reinterpret_cast<uint4*>(prm.out + row_g + c * 32 + j) = o;
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();                           // the dealloc is warp-wide and aligned
+        tmem_dealloc(s.tmem_base, 512);
+    }
+    if (tid == 0 && s.err) atomicOr(prm.dev_err, (unsigned)kDevErrMbarTimeout);
+#undef WAIT
+#undef LLA_SET_DIRECTION
+}
+
+template <int D>
+cudaError_t launch_d(const Problem& p, void* ws, cudaStream_t stream, const char** why) {
+    const size_t N = (size_t)p.B * p.H * p.n * D;
+    unsigned char* base = static_cast<unsigned char*>(ws);
+    Header* hdr = reinterpret_cast<Header*>(base);
+    __half* q16 = reinterpret_cast<__half*>(base + HDR_BYTES);
+    __half* k16 = reinterpret_cast<__half*>(base + HDR_BYTES + align256(N * 2));
+    __half* v16 = reinterpret_cast<__half*>(base + HDR_BYTES + 2 * align256(N * 2));
+    const size_t NT = (size_t)p.B * p.H * ((p.n + BQ - 1) / BQ) * BQ * D;   // padded to whole tiles
+    float* kbar = reinterpret_cast<float*>(base + HDR_BYTES + 3 * align256(N * 2));
+    float* xs = reinterpret_cast<float*>(base + HDR_BYTES + 3 * align256(N * 2) + align256(NT * 4));
+
+    cudaError_t e = cudaMemsetAsync(hdr, 0, HDR_BYTES, stream);
+    if (e != cudaSuccess) { *why = "workspace header clear"; return e; }
+    const size_t count8 = N / 8;
+    const int pre_blocks = (int)((count8 + 255) / 256 < 152 * 8 ? (count8 + 255) / 256 : 152 * 8);
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
+    const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(p.k);
+    const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(p.v);
+    lla_maxabs_kernel<<<pre_blocks, 256, 0, stream>>>(q, k, v, count8, hdr);
+    lla_to_half_kernel<<<pre_blocks, 256, 0, stream>>>(q, k, v, q16, k16, v16, count8, hdr);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) { *why = "operand pre-pass launch"; return e; }
+
+    CUtensorMap tq, tk, tv;
+    const uint64_t slices = (uint64_t)p.B * p.H;
+    if (!make_tmap_f16_3d(&tq, q16, D, p.n, slices, BQ) || !make_tmap_f16_3d(&tk, k16, D, p.n, slices, BK) ||
+        !make_tmap_f16_3d(&tv, v16, D, p.n, slices, BK)) {
+        *why = "cuTensorMapEncodeTiled";
+        return cudaErrorInvalidValue;
+    }
+    TcParams prm;
+    prm.hdr = hdr;
+    prm.kbar = kbar;
+    prm.xs = xs;
+    prm.out = static_cast<__nv_bfloat16*>(p.out);
+    prm.rho = p.rho;
+    prm.denom = p.denom;
+    prm.cg_iters = p.cg_iters;
+    prm.dev_err = device_error_word();
+    prm.n = p.n;
+    prm.n_tiles = (p.n + BQ - 1) / BQ;
+    prm.tau = p.tau;
+    prm.lambda = p.lambda;
+    prm.cg_tol = p.cg_tol;
+    prm.cg_max_iters = p.cg_max_iters;
+    if (!prm.dev_err) { *why = "device error word"; return cudaErrorInvalidSymbol; }
+
+    const size_t smem = sizeof(TcSmem<D>) + 1024;
+    auto kern = lla_tc_kernel<D>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) { *why = "tensor kernel shared-memory attribute"; return e; }
+    dim3 grid(prm.n_tiles, (unsigned)slices);
+    if (p.ev_main_begin && (e = cudaEventRecord(p.ev_main_begin, stream)) != cudaSuccess) {
+        *why = "profiling event record";
+        return e;
+    }
+    kern<<<grid, NTHREADS, smem, stream>>>(tq, tk, tv, prm);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) { *why = "tensor kernel launch"; return e; }
+    if (p.ev_main_end && (e = cudaEventRecord(p.ev_main_end, stream)) != cudaSuccess) *why = "profiling event record";
+    return e;
+}
+
+}  // namespace
+
+size_t tensor_workspace_bytes(int B, int H, int n, int d) {
+    const size_t N = (size_t)B * H * n * d;
+    const size_t NT = (size_t)B * H * ((n + BQ - 1) / BQ) * BQ * d;
+    return HDR_BYTES + 3 * align256(N * 2) + 2 * align256(NT * 4);
+}
+
+cudaError_t launch_tensor(const Problem& p, void* ws, cudaStream_t stream, const char** why) {
+    if (p.d == 128) return launch_d<128>(p, ws, stream, why);
+    if (p.d == 64) return launch_d<64>(p, ws, stream, why);
+    *why = "tensor path supports d in {64, 128}";
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace lla

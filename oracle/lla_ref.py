@@ -177,8 +177,12 @@ def lla_row_cg(q_i, K_prefix, V_prefix, tau, lam, max_iters, tol):
     return {"out": out, "rho": rho, "denom": denom, "iters": iters, "m": m, "omega": omega}
 
 
-def lla_row_deflated_cg(q_i, K_prefix, V_prefix, tau, lam, max_iters, tol):
+def lla_row_deflated_cg(q_i, K_prefix, V_prefix, tau, lam, max_iters, tol, weight_noise=None):
     """LLA of one query with rho from CG on the centred key scatter.
+
+    weight_noise: None, or relative perturbations xi_j applied as w_j (1 + xi_j) after the
+    weights are formed (used only to measure how sensitive a row's result is to rounding
+    of the per-pair coefficients; the default computes the unperturbed iteration).
 
     Steps: weights; omega, kbar = sum_j w_j k_j / omega; delta = kbar - q;
     Cn = sum_j wbar_j (k_j - kbar)(k_j - kbar)^T + (lambda/omega) I (dense);
@@ -189,6 +193,8 @@ def lla_row_deflated_cg(q_i, K_prefix, V_prefix, tau, lam, max_iters, tol):
     q_i = _f64(q_i)
     K = _f64(K_prefix)
     w, m = row_weights(q_i, K, tau)
+    if weight_noise is not None:
+        w = w * (1.0 + _f64(weight_noise))
     omega = w.sum()
     wbar = w / omega
     kbar = wbar @ K
@@ -220,12 +226,14 @@ def _rows_iter(shape, rows):
             yield tuple(int(t) for t in r)
 
 
-def lla_ref(q, k, v, tau, lam, rows=None, cg=None, deflated=None):
+def lla_ref(q, k, v, tau, lam, rows=None, cg=None, deflated=None, noise_rel=None, noise_seed=0):
     """Causal LLA over [B, H, n, d] inputs, row by row.
 
     rows: None (every (b, h, i)) or an iterable of (b, h, i) triples.
     cg: None for the exact solve, else (max_iters, tol) to solve with ``cg_solve``
-        on Sigma_i; deflated: (max_iters, tol) to use ``lla_row_deflated_cg``.
+        on Sigma_i; deflated: (max_iters, tol) to use ``lla_row_deflated_cg``;
+    noise_rel: with ``deflated``, perturb every weight by a seeded relative amount
+        uniform in [-noise_rel, noise_rel] (sensitivity analysis).
     Returns (out [R, d], rho [R, d], denom [R]) in float64, R rows in the order
     given (row-major over b, h, i when rows is None).
     """
@@ -233,8 +241,12 @@ def lla_ref(q, k, v, tau, lam, rows=None, cg=None, deflated=None):
     outs, rhos, dens = [], [], []
     for b, h, i in _rows_iter(q.shape, rows):
         if deflated is not None:
+            xi = None
+            if noise_rel:
+                rng = np.random.Generator(np.random.PCG64([noise_seed, b, h, i]))
+                xi = rng.uniform(-noise_rel, noise_rel, size=i + 1)
             r = lla_row_deflated_cg(q[b, h, i], k[b, h, : i + 1], v[b, h, : i + 1], tau, lam,
-                                    deflated[0], deflated[1])
+                                    deflated[0], deflated[1], weight_noise=xi)
         elif cg is None:
             r = lla_row(q[b, h, i], k[b, h, : i + 1], v[b, h, : i + 1], tau, lam)
         else:

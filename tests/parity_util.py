@@ -33,14 +33,20 @@ def pick(arr, rows):
     return np.array([a[b, h, i] for b, h, i in rows])
 
 
-def oracle_rows(qkv, w, rows, lam=None, iters=None, tol=None):
+def oracle_rows(qkv, w, rows, lam=None, iters=None, tol=None, sensitivity=False):
+    """Exact solve and float64 CG (same cap/tol) on the rows; with sensitivity=True also the
+    CG result with every weight perturbed by up to 2^-10 relative (fp16 coefficient resolution)."""
     qn, kn, vn = (t.double().numpy() for t in qkv)
     lam = w.lam if lam is None else lam
     T = w.cg_max_iters if iters is None else iters
     tol = w.cg_tol if tol is None else tol
     exact = lla_ref(qn, kn, vn, w.tau, lam, rows=rows)
     cg = lla_ref(qn, kn, vn, w.tau, lam, rows=rows, deflated=(T, tol))
-    return exact, cg, math.sqrt(float(np.mean(vn ** 2)))
+    rms_v = math.sqrt(float(np.mean(vn ** 2)))
+    if not sensitivity:
+        return exact, cg, rms_v
+    pert = lla_ref(qn, kn, vn, w.tau, lam, rows=rows, deflated=(T, tol), noise_rel=2.0 ** -10)
+    return exact, cg, rms_v, pert
 
 
 def errors(g_out, g_rho, g_den, ref, rms_v):
@@ -63,3 +69,28 @@ def rows_for(w, count):
 def softmax_rows(qkv, w, rows):
     qn, kn, vn = (t.double().numpy() for t in qkv)
     return softmax_ref(qn, kn, vn, w.tau, rows=rows)
+
+
+def bf16_gate(w, rows, path, lam=None, tol=None, iters=None, gate=2e-2, min_ok_frac=0.5, conv_tol=2e-3,
+              sens_tol=5e-3):
+    """Run the GPU path and gate out against the exact solve on the rows that are
+    (a) converged: the oracle's own float64 CG at the same cap and tolerance is within
+        conv_tol RMS(v) of the exact solve, and
+    (b) stable: perturbing every weight by up to 2^-10 relative (the resolution of the
+        tensor path's fp16 per-pair coefficients) moves the float64 CG result by at most
+        sens_tol RMS(v).
+    Both criteria are computed by the oracle alone.  Every row must be finite with
+    denom > 0.  Returns (per-row out error vs exact, gated mask, iteration counts)."""
+    qkv, (out, rho, den, its) = run_gpu(w, path, lam=lam, tol=tol, iters=iters)
+    exact, cg, rms_v, pert = oracle_rows(qkv, w, rows, lam=lam, iters=iters, tol=tol, sensitivity=True)
+    g_out, g_rho, g_den = pick(out, rows), pick(rho, rows), pick(den, rows)
+    assert np.isfinite(g_out).all() and np.isfinite(g_rho).all() and (g_den > 0).all()
+    trunc = np.abs(cg[0] - exact[0]).max(axis=1) / rms_v
+    sens = np.abs(pert[0] - cg[0]).max(axis=1) / rms_v
+    ok = (trunc <= conv_tol) & (sens <= sens_tol)
+    assert ok.mean() >= min_ok_frac, f"only {ok.mean():.2f} of rows converged in the oracle"
+    e_out, e_rho, e_den = errors(g_out, g_rho, g_den, exact, rms_v)
+    bad = np.nonzero(ok & (e_out > gate))[0]
+    assert bad.size == 0, (f"{bad.size} converged rows over {gate}: worst {e_out[ok].max():.3e} "
+                           f"at {rows[int(np.argmax(np.where(ok, e_out, -1)))]}")
+    return e_out, ok, its

@@ -61,6 +61,9 @@ def test_tensor_path_needs_bf16_and_supported_dim(lib):
 
 def test_path_resolution_and_workspace_size(lib):
     assert lib.lla_resolve_path(lla.LLA_DTYPE_FP32, lla.LLA_PATH_AUTO, 128) == lla.LLA_PATH_FP32
+    assert lib.lla_resolve_path(lla.LLA_DTYPE_BF16, lla.LLA_PATH_AUTO, 128) == lla.LLA_PATH_TENSOR
+    assert lib.lla_resolve_path(lla.LLA_DTYPE_BF16, lla.LLA_PATH_AUTO, 64) == lla.LLA_PATH_TENSOR
+    assert lib.lla_resolve_path(lla.LLA_DTYPE_BF16, lla.LLA_PATH_AUTO, 32) == lla.LLA_PATH_FP32
     assert lib.lla_resolve_path(lla.LLA_DTYPE_BF16, lla.LLA_PATH_FP32, 128) == lla.LLA_PATH_FP32
     assert lib.lla_workspace_size(lla.LLA_DTYPE_FP32, lla.LLA_PATH_AUTO, 2, 2, 64, 64) == 0
     assert lib.lla_workspace_size(lla.LLA_DTYPE_BF16, lla.LLA_PATH_TENSOR, 2, 2, 64, 64) > 0

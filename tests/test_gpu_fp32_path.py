@@ -16,7 +16,7 @@ import torch
 import local_linear_attention_flashlla_gb300 as lla
 from local_linear_attention_flashlla_gb300.inputs import workload
 
-from parity_util import all_rows, errors, oracle_rows, pick, rows_for, run_gpu, softmax_rows
+from parity_util import all_rows, bf16_gate, errors, oracle_rows, pick, rows_for, run_gpu, softmax_rows
 
 pytestmark = pytest.mark.gpu
 FP32 = lla.LLA_PATH_FP32
@@ -59,19 +59,7 @@ def test_fp32_path_edges_converged(lla_gpu, d, n):
     _check_fp32(w, all_rows(w), gate=2e-4)
 
 
-def _bf16_gate(w, rows, path, lam=None, tol=None, iters=None, gate=2e-2, min_ok_frac=0.5):
-    qkv, (out, rho, den, its) = run_gpu(w, path, lam=lam, tol=tol, iters=iters)
-    exact, cg, rms_v = oracle_rows(qkv, w, rows, lam=lam, iters=iters, tol=tol)
-    g_out, g_rho, g_den = pick(out, rows), pick(rho, rows), pick(den, rows)
-    assert np.isfinite(g_out).all() and np.isfinite(g_rho).all() and (g_den > 0).all()
-    trunc = np.abs(cg[0] - exact[0]).max(axis=1) / rms_v
-    ok = trunc <= 2e-3
-    assert ok.mean() >= min_ok_frac, f"only {ok.mean():.2f} of rows converged in the oracle"
-    e_out, e_rho, e_den = errors(g_out, g_rho, g_den, exact, rms_v)
-    bad = np.nonzero(ok & (e_out > gate))[0]
-    assert bad.size == 0, (f"{bad.size} converged rows over {gate}: worst {e_out[ok].max():.3e} "
-                           f"at {rows[int(np.argmax(np.where(ok, e_out, -1)))]}")
-    return e_out, ok, its
+_bf16_gate = bf16_gate
 
 
 @pytest.mark.parametrize("d", [16, 32, 64, 128])

@@ -280,3 +280,17 @@ def test_lla_ref_batched_layout_matches_rows():
     o2, _, _ = O.lla_ref(q, k, v, 0.5, 0.3, rows=[(1, 2, 4), (0, 0, 0)])
     assert np.abs(o2[0] - r["out"]).max() == 0.0
     assert np.abs(o2[1] - v[0, 0, 0]).max() < 1e-12
+
+
+def test_weight_noise_hook_is_inert_by_default_and_small_when_used():
+    """The sensitivity hook: zero noise reproduces the plain iteration exactly, small noise
+    moves a well-conditioned row by about the noise level."""
+    q, k, v = _rand(15, 30, 4)
+    i = 29
+    a = O.lla_row_deflated_cg(q[i], k[: i + 1], v[: i + 1], 0.6, 0.5, 100, 0.0)
+    b = O.lla_row_deflated_cg(q[i], k[: i + 1], v[: i + 1], 0.6, 0.5, 100, 0.0, weight_noise=np.zeros(i + 1))
+    assert np.abs(a["out"] - b["out"]).max() == 0.0
+    c = O.lla_row_deflated_cg(q[i], k[: i + 1], v[: i + 1], 0.6, 0.5, 100, 0.0,
+                              weight_noise=np.full(i + 1, 1e-6))
+    # a common relative factor on every weight: kbar, wbar unchanged; only lambda/omega shifts
+    assert np.abs(a["out"] - c["out"]).max() < 1e-5
