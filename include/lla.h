@@ -109,6 +109,29 @@ int lla_sync_status(void* stream);
 int lla_profile_enable(int on);
 int lla_profile_read(float* main_ms, float* total_ms);
 
+/*
+ * lla_forward_noalloc -- lla_forward (bf16, tensor path, d in {64, 128}) for callers that cannot
+ * allocate device memory when they run it.  The paper has no counterpart: this is an interface
+ * for hosts whose device memory is owned by another allocator (for example a framework that
+ * reserves the GPU's memory up front) or that must not pay for an allocation on this path.
+ *
+ * Scratch lives in a fixed device array of LLA_NOALLOC_SCRATCH_BYTES that every GPU loading the
+ * library holds until the process exits; the call makes no cudaMalloc/cudaFree or other
+ * allocating call.  Arguments and outputs are as for lla_forward; q, k, v, out, rho, denom are
+ * still the caller's buffers.  A problem whose lla_workspace_size(LLA_DTYPE_BF16,
+ * LLA_PATH_TENSOR, ...) exceeds the array is rejected with LLA_ERR_INVALID_ARG before anything is
+ * launched; d outside {64, 128} gives LLA_ERR_UNSUPPORTED.
+ *
+ * The first call on each device looks up the array's device address (cudaGetSymbolAddress with
+ * that device current); make that first call before any stream capture.  All calls share the
+ * array: calls that overlap on the GPU (on different streams, or from different threads) race on
+ * it and must be serialised by the caller.  Each call re-initialises what must start at zero.
+ */
+#define LLA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+int lla_forward_noalloc(const void* q, const void* k, const void* v, void* out, float* rho, float* denom,
+                        int B, int H, int n, int d, float tau, float lambda, int cg_max_iters, float cg_tol,
+                        void* stream);
+
 /* Message for the calling thread's most recent failure ("" if none). Owned by the library. */
 const char* lla_last_error(void);
 

@@ -15,7 +15,7 @@ import os
 __all__ = [
     "LLAError", "load_library", "library_path", "forward", "lla_forward", "lla_forward_ex",
     "lla_workspace_size", "lla_resolve_path", "lla_sync_status", "lla_last_error", "lla_version",
-    "lla_profile_enable", "lla_profile_read",
+    "lla_profile_enable", "lla_profile_read", "lla_forward_noalloc",
     "LLA_OK", "LLA_ERR_INVALID_ARG", "LLA_ERR_UNSUPPORTED", "LLA_ERR_CUDA", "LLA_ERR_DEVICE_TIMEOUT",
     "LLA_DTYPE_BF16", "LLA_DTYPE_FP32", "LLA_PATH_AUTO", "LLA_PATH_TENSOR", "LLA_PATH_FP32",
     "EXPORTED_SYMBOLS",
@@ -40,6 +40,8 @@ _SIGNATURES = {
     "lla_resolve_path": (_c_int, [_c_int, _c_int, _c_int]),
     "lla_sync_status": (_c_int, [_vp]),
     "lla_last_error": (ctypes.c_char_p, []),
+    "lla_forward_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_float,
+                                     _c_float, _c_int, _c_float, _vp]),
     "lla_profile_enable": (_c_int, [_c_int]),
     "lla_profile_read": (_c_int, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]),
     "lla_version": (_c_int, []),
@@ -127,6 +129,13 @@ def lla_forward(q_ptr, k_ptr, v_ptr, out_ptr, rho_ptr, denom_ptr, B, H, n, d, ta
     """Raw C entry point on device pointers (ints); raises LLAError on a non-zero status."""
     _check(load_library().lla_forward(q_ptr, k_ptr, v_ptr, out_ptr, rho_ptr, denom_ptr, B, H, n, d, tau, lam,
                                       cg_max_iters, cg_tol, stream_ptr))
+
+
+def lla_forward_noalloc(q_ptr, k_ptr, v_ptr, out_ptr, rho_ptr, denom_ptr, B, H, n, d, tau, lam, cg_max_iters,
+                        cg_tol, stream_ptr):
+    """C entry point that uses the library's fixed device scratch instead of allocating."""
+    _check(load_library().lla_forward_noalloc(q_ptr, k_ptr, v_ptr, out_ptr, rho_ptr, denom_ptr, B, H, n, d, tau,
+                                              lam, cg_max_iters, cg_tol, stream_ptr))
 
 
 def lla_forward_ex(dtype, path, q_ptr, k_ptr, v_ptr, out_ptr, rho_ptr, denom_ptr, iters_ptr, B, H, n, d, tau, lam,

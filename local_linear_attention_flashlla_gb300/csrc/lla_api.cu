@@ -29,6 +29,8 @@ int cuda_fail(cudaError_t e, const char* what) {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 }  // namespace
 
+int set_error(int status, const char* message) { return fail(status, "%s", message); }
+
 __device__ unsigned g_device_error = 0;
 
 namespace {

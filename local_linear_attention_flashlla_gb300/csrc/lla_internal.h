@@ -35,6 +35,9 @@ cudaError_t launch_simt(const Problem& p, cudaStream_t stream);
 size_t tensor_workspace_bytes(int B, int H, int n, int d);
 cudaError_t launch_tensor(const Problem& p, void* workspace, cudaStream_t stream, const char** why);
 
+// Record a failure for lla_last_error() and return status (defined in lla_api.cu).
+int set_error(int status, const char* message);
+
 // Library-owned device error word (defined in lla_api.cu).
 cudaError_t read_and_clear_device_error(unsigned* out, cudaStream_t stream);
 unsigned* device_error_word();
