@@ -373,11 +373,11 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         mbar_init(&s.q_full, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s.s_full[i], 1);
-            mbar_init(&s.ew_done[i], NEW);
+            mbar_init(&s.ew_done[i], NEW / 32);       // one arrive per elementwise warp
         }
-        mbar_init(&s.a_free, NEW);
+        mbar_init(&s.a_free, NEW / 32);
         mbar_init(&s.y_done, 1);
-        mbar_init(&s.p_ready, NEW);
+        mbar_init(&s.p_ready, 1);                   // one arrive after the elementwise threads' barrier
         mbar_init(&s.mma_final, 1);
         mbar_fence_init();
     }
@@ -554,9 +554,27 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             tc_fence_after();
             return r;
         };
+        // Per-block signals are one arrive per warp (not per thread): fewer atomics on the
+        // barrier word the MMA thread polls.
         auto done_block = [&](uint32_t gg) {
             tc_fence_before();
-            mbar_arrive(&s.ew_done[gg & 1]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.ew_done[gg & 1]);
+        };
+        auto release_a = [&]() {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.a_free);
+        };
+        // P/R tile written: every thread fences its generic-proxy writes for the async proxy, the
+        // elementwise threads meet, and one thread arrives.
+        auto publish_p = [&](int next_type) {
+            fence_proxy_async_smem();
+            named_bar_sync(EW_BAR, NEW);
+            if (tid == 128) {
+                s.next_type = next_type;
+                mbar_arrive(&s.p_ready);
+            }
         };
         auto wait_y = [&]() {
             const bool r = WAIT(&s.y_done, yd & 1, err);
@@ -680,9 +698,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             if (!dynamic) go = cg_sweeps < prm.cg_max_iters;
             else go = ew_any(active) && cg_sweeps < prm.cg_max_iters;
             if (!go) break;
-            if (tid == 128) s.next_type = SW_CG;
-            fence_proxy_async_smem();
-            mbar_arrive(&s.p_ready);
+            publish_p(SW_CG);
             ++cg_sweeps;
             float msum_part = 0.f;
             for (int kb = 0; kb < nkb; ++kb, ++g) {
@@ -697,8 +713,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 tmem_ld32(tAh + 32, *reinterpret_cast<float(*)[32]>(&a[32]));
                 tmem_ld32(tS, v);
                 tmem_ld_wait();
-                tc_fence_before();
-                mbar_arrive(&s.a_free);
+                release_a();
                 if (masked) coef_chunk<true, true, 0>(v, a, c_log2, offM, -kp_acc, 1.f, half * 64, lim, msum_part, pk);
                 else coef_chunk<false, true, 0>(v, a, c_log2, offM, -kp_acc, 1.f, 0, 0, msum_part, pk);
                 tmem_st16(tS, pk);
@@ -822,9 +837,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int sU = scale_exp((1.f + kbound * mxx) * 1.001f);
         const float offU = m2 - (float)sU + (float)sr + (float)ek;
         const float c_acc = (1.f + kx) * pow2i(sr + ek);
-        if (tid == 128) s.next_type = SW_OUT;
-        fence_proxy_async_smem();
-        mbar_arrive(&s.p_ready);
+        publish_p(SW_OUT);
 
         // ---------------- OUT sweep ----------------
         float us_part = 0.f;
@@ -840,8 +853,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             tmem_ld32(tAh + 32, *reinterpret_cast<float(*)[32]>(&a[32]));
             tmem_ld32(tS, v);
             tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(&s.a_free);
+            release_a();
             if (masked) coef_chunk<true, true, 0>(v, a, c_log2, offU, c_acc, -1.f, half * 64, lim, us_part, pk);
             else coef_chunk<false, true, 0>(v, a, c_log2, offU, c_acc, -1.f, 0, 0, us_part, pk);
             tmem_st16(tS, pk);
