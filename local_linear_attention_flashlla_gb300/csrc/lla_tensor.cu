@@ -22,7 +22,8 @@
 // (Eqs. (6)-(8) with Sigma_i = C_i + omega_i delta_i delta_i^T, Sherman-Morrison).
 //
 // Roles (384 threads, three warpgroups): warp 0 lane 0 issues TMA (Q once, then K/V blocks
-// into a 3-slot ring); warp 1 lane 0 issues every tcgen05.mma and commit (warps 2-3 idle);
+// into a 3-slot ring); warp 1 lane 0 issues the S and A'/T products, warp 2 lane 0 the Y
+// products (two issue streams, synchronised through mbarriers; warp 3 idle);
 // warpgroups 1-2 (256 threads) do the elementwise work and the CG vector updates, thread =
 // (query row, half of the key block / half of the head dimension).  setmaxnreg moves
 // registers from warpgroup 0 (72 each) to the elementwise warpgroups (216 each):
@@ -135,8 +136,9 @@ struct TcSmem {
     unsigned char rlo[TILE];                           // R_lo (output sweep); P_lo (CG sweeps of tile 0)
     unsigned char slot[NSLOT][TILE];                   // K / V blocks (TMA)
     uint64_t slot_full[NSLOT], slot_empty[NSLOT];
-    uint64_t q_full, s_full[2], ew_done[2], a_free, y_done, p_ready, mma_final;
-    float xch[6][2][BQ];                               // row-scalar exchange between the two halves
+    float stg[2][2][8][BQ];                            // CG iterate increments: [buffer][half][coord][row]
+    uint64_t q_full, s_full[2], ew_done[2], m_free[2], a_free, y_done, p_ready, final_sa, final_y;
+    float xch[2][2][BQ];                               // row-scalar exchange between the two halves
     uint32_t tmem_base;
     int err;
     int next_type;
@@ -156,20 +158,22 @@ struct TcParams {
     int cg_max_iters;
 };
 
-// Sum (or max) of a per-row value over the two half-threads of the row.
+// Sum (or max) of a per-row value over the two half-threads of the row.  Two buffers used in
+// turn suffice: a thread writes a buffer again only after the next exchange's barrier, which its
+// partner reaches only after reading that buffer.
 struct Xch {
     float (*buf)[2][BQ];
     int idx, half, row;
     __device__ float sum(float v) {
         float* b = &buf[idx][0][0];
-        idx = idx == 5 ? 0 : idx + 1;
+        idx ^= 1;
         b[half * BQ + row] = v;
         named_bar_sync(EW_BAR, NEW);
         return v + b[(1 - half) * BQ + row];
     }
     __device__ float max(float v) {
         float* b = &buf[idx][0][0];
-        idx = idx == 5 ? 0 : idx + 1;
+        idx ^= 1;
         b[half * BQ + row] = v;
         named_bar_sync(EW_BAR, NEW);
         return fmaxf(v, b[(1 - half) * BQ + row]);
@@ -224,11 +228,11 @@ __device__ __forceinline__ float dir_maxabs(const float (&res)[DH], const unsign
 
 // Store fp16((res + beta p_old) * nsc) over the old values (and, when split, the fp16 remainder
 // in the lo tile, so hi + lo carries about 22 bits); returns kbar . p_hat (partial), p_hat being
-// the stored value.  kbt: this thread's kbar coordinates, stride BQ floats (tile-transposed).
+// the stored value.  kv: this thread's kbar coordinates.
 template <int DH>
 __device__ __forceinline__ float dir_store(const float (&res)[DH], unsigned char* ptile, unsigned char* plo, bool split,
                                            int row, int col0, float beta, bool keep_old, float osc, float nsc,
-                                           float nisc, const float* kbt) {
+                                           float nisc, const float (&kv)[DH]) {
     float kp = 0.f;
 #pragma unroll
     for (int e0 = 0; e0 < DH; e0 += 8) {
@@ -256,8 +260,8 @@ __device__ __forceinline__ float dir_store(const float (&res)[DH], unsigned char
                 ph.x += pl2.x;
                 ph.y += pl2.y;
             }
-            kp = fmaf(kbt[(e0 + u) * BQ], ph.x * nisc, kp);
-            kp = fmaf(kbt[(e0 + u + 1) * BQ], ph.y * nisc, kp);
+            kp = fmaf(kv[e0 + u], ph.x * nisc, kp);
+            kp = fmaf(kv[e0 + u + 1], ph.y * nisc, kp);
         }
         *reinterpret_cast<uint4*>(hp) = pk;
         if (split) *reinterpret_cast<uint4*>(lp) = pl;
@@ -265,14 +269,16 @@ __device__ __forceinline__ float dir_store(const float (&res)[DH], unsigned char
     return kp;
 }
 
-// One 32-coordinate chunk of (C/omega) p and of p_hat for this thread's row.
-__device__ __forceinline__ void cp_chunk32(uint32_t ty, const unsigned char* ptile, const unsigned char* plo, bool split,
-                                           int row, int col, const float* kbt_c, float ysc, float msc, float lam_n,
-                                           float psc, float (&cp)[32], float (&ph)[32]) {
-    float v[32];
-    tmem_ld32(ty, v);
+// One 16-coordinate chunk (chunk C of this thread's DH) of (C/omega) p and of p_hat for this
+// thread's row; kv holds this thread's kbar coordinates.
+template <int C, int DH>
+__device__ __forceinline__ void cp_chunk16(uint32_t ty, const unsigned char* ptile, const unsigned char* plo, bool split,
+                                           int row, int col, const float (&kv)[DH], float ysc, float msc, float lam_n,
+                                           float psc, float (&cp)[16], float (&ph)[16]) {
+    float v[16];
+    tmem_ld16(ty, v);
 #pragma unroll
-    for (int j = 0; j < 32; j += 8) {
+    for (int j = 0; j < 16; j += 8) {
         const uint4 pr = *reinterpret_cast<const uint4*>(tile_half(ptile, row, col + j));
         uint4 prl = make_uint4(0u, 0u, 0u, 0u);
         if (split) prl = *reinterpret_cast<const uint4*>(tile_half(plo, row, col + j));
@@ -281,38 +287,45 @@ __device__ __forceinline__ void cp_chunk32(uint32_t ty, const unsigned char* pti
 #pragma unroll
         for (int u = 0; u < 8; ++u) ph[j + u] = (__half2float(phh[u]) + __half2float(phl[u])) * psc;
     }
-    float kv[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) kv[j] = kbt_c[j * BQ];
     tmem_ld_wait();
 #pragma unroll
-    for (int j = 0; j < 32; ++j) cp[j] = fmaf(v[j], ysc, fmaf(-kv[j], msc, lam_n * ph[j]));
+    for (int j = 0; j < 16; ++j) cp[j] = fmaf(v[j], ysc, fmaf(-kv[C * 16 + j], msc, lam_n * ph[j]));
 }
 
 // Per-pair coefficients of one 32-key chunk (chunk C of this thread's 64 keys):
 //   HAS_A:  out_j = 2^(s_j c - off) (base + sign a_j)     (CG: base = -kbar.p, sign = +1;
 //                                                          output: base = c, sign = -1)
 //   !HAS_A: out_j = 2^(s_j c - off)                       (moments)
-// zero where MASKED and key column > lim.  Packs pairs to fp16 and accumulates their sum.
+// zero where MASKED and key column > lim.  Packs pairs to fp16 and accumulates their sum into
+// two running fp32 partial sums (even and odd keys).  Key pairs go through f32x2 arithmetic.
 template <bool MASKED, bool HAS_A, int C>
 __device__ __forceinline__ void coef_chunk(const float (&v)[32], const float (&a)[64], float c_log2, float off,
-                                           float base, float sign, int col0, int lim, float& sum,
+                                           float base, float sign, int col0, int lim, uint64_t& sum2,
                                            uint32_t (&pk)[16]) {
+    const uint64_t cc = f2_pack(c_log2, c_log2), oo = f2_pack(-off, -off);
+    const uint64_t bb = f2_pack(base, base), sg = f2_pack(sign, sign);
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
-        float m0 = ex2(fmaf(v[j], c_log2, -off));
-        float m1 = ex2(fmaf(v[j + 1], c_log2, -off));
-        if (HAS_A) {
-            m0 *= fmaf(sign, a[C * 32 + j], base);
-            m1 *= fmaf(sign, a[C * 32 + j + 1], base);
-        }
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(v[j], v[j + 1]), cc, oo), x0, x1);
+        uint64_t m = f2_pack(ex2(x0), ex2(x1));
+        if (HAS_A) m = f2_mul(m, f2_fma(sg, f2_pack(a[C * 32 + j], a[C * 32 + j + 1]), bb));
+        float m0, m1;
+        f2_unpack(m, m0, m1);
         if (MASKED) {
             m0 = (col0 + j <= lim) ? m0 : 0.f;
             m1 = (col0 + j + 1 <= lim) ? m1 : 0.f;
+            m = f2_pack(m0, m1);
         }
-        sum += m0 + m1;
+        sum2 = f2_add(sum2, m);
         pk[j >> 1] = pack_half2(m0, m1);
     }
+}
+
+__device__ __forceinline__ float f2_total(uint64_t s2) {
+    float lo, hi;
+    f2_unpack(s2, lo, hi);
+    return lo + hi;
 }
 
 // One 128 x 128 x D product D[tmem] = A[smem] B[smem]^T, both K-major SW128 tiles, D/16 k-steps.
@@ -376,9 +389,11 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             mbar_init(&s.ew_done[i], NEW / 32);       // one arrive per elementwise warp
         }
         mbar_init(&s.a_free, NEW / 32);
+        for (int i = 0; i < 2; ++i) mbar_init(&s.m_free[i], 1);
         mbar_init(&s.y_done, 1);
         mbar_init(&s.p_ready, 1);                   // one arrive after the elementwise threads' barrier
-        mbar_init(&s.mma_final, 1);
+        mbar_init(&s.final_sa, 1);
+        mbar_init(&s.final_y, 1);
         mbar_fence_init();
     }
     if (warp == 1) {
@@ -435,17 +450,10 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             mbar_drain(&s.q_full, 0);
         }
     } else if (warp == 1) {
-        // =============================== MMA issuer ===============================
+        // ========================= MMA issuer 1: S = Q K^T and A' / T =========================
         if (lane == 0) {
             const uint32_t q_addr = smem_u32(s.q), p_addr = smem_u32(s.p), rlo_addr = smem_u32(s.rlo);
-            uint32_t fill = 0, pr = 0, g = 0, ew_seen = 0, ga = 0;
-            auto wait_ew = [&](uint32_t upto) {          // elementwise work of blocks < upto finished
-                while (ew_seen < upto) {
-                    if (!WAIT(&s.ew_done[ew_seen & 1], (ew_seen >> 1) & 1, err)) return false;
-                    ++ew_seen;
-                }
-                return true;
-            };
+            uint32_t fill = 0, pr = 0, g = 0, ga = 0;
             bool ok = WAIT(&s.q_full, 0, err);
             int cg_sweeps = 0;
             for (int sweep = 0; ok; ++sweep) {
@@ -462,18 +470,17 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
                 if (type == SW_CG) ++cg_sweeps;
                 const bool two = type == SW_CG || type == SW_OUT;
-                uint32_t prev_k = 0, prev_v = 0;
-                for (int kb = 0; kb < nkb && ok; ++kb) {
+                for (int kb = 0; kb < nkb; ++kb, ++g) {
                     const uint32_t fk = fill++;
-                    const uint32_t fv = type == SW_OUT ? fill++ : 0;
+                    if (type == SW_OUT) ++fill;           // the V block of this key block
                     const int sk = fk % NSLOT;
-                    if (!(ok = WAIT(&s.slot_full[sk], (fk / NSLOT) & 1, err))) break;
                     const uint32_t b = g & 1;
-                    if (g >= 2 && !(ok = wait_ew(g - 1))) break;
+                    if (!(ok = WAIT(&s.slot_full[sk], (fk / NSLOT) & 1, err))) break;
+                    // S buffer b was last used by block g - 2: its coefficients must have been read
+                    if (g >= 2 && !(ok = WAIT(&s.m_free[b], ((g - 2) >> 1) & 1, err))) break;
                     tc_fence_after();
                     const uint32_t k_addr = smem_u32(s.slot[sk]);
-                    const uint32_t tS = tS0 + b * 128;
-                    gemm_qk<D, false>(tS, q_addr, k_addr);
+                    gemm_qk<D, false>(tS0 + b * 128, q_addr, k_addr);
                     if (two) {
                         if (!have_p) {
                             if (!(ok = WAIT(&s.p_ready, pr & 1, err))) break;
@@ -490,32 +497,53 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         if (type == SW_OUT || tile == 0) gemm_qk<D, true>(tA, rlo_addr, k_addr);
                     }
                     umma_commit(&s.s_full[b]);
-                    if (type == SW_MAX) umma_commit(&s.slot_empty[sk]);
-                    // Y product of the previous block
-                    auto issue_y = [&](uint32_t gb, uint32_t f_k, uint32_t f_v, bool acc) {
-                        if (!wait_ew(gb + 1)) return false;
-                        if (type == SW_OUT && !WAIT(&s.slot_full[f_v % NSLOT], (f_v / NSLOT) & 1, err)) return false;
-                        tc_fence_after();
-                        const uint32_t src = smem_u32(s.slot[(type == SW_OUT ? f_v : f_k) % NSLOT]);
-                        const uint32_t tM = tS0 + (gb & 1) * 128;
-                        gemm_y<D>(tY, tM, src, acc);
-                        umma_commit(&s.slot_empty[f_k % NSLOT]);
-                        if (type == SW_OUT) umma_commit(&s.slot_empty[f_v % NSLOT]);
-                        return true;
-                    };
-                    if (type != SW_MAX && kb >= 1 && !(ok = issue_y(g - 1, prev_k, prev_v, kb - 1 > 0))) break;
-                    prev_k = fk;
-                    prev_v = fv;
-                    ++g;
-                    if (type != SW_MAX && kb == nkb - 1) {
-                        if (!(ok = issue_y(g - 1, prev_k, prev_v, nkb - 1 > 0))) break;
-                        umma_commit(&s.y_done);
-                    }
+                    // a K block read only by this issuer is free once these products complete
+                    if (type == SW_MAX || type == SW_OUT) umma_commit(&s.slot_empty[sk]);
                 }
                 if (type == SW_OUT) break;
             }
-            umma_commit(&s.mma_final);
-            mbar_drain(&s.mma_final, 0);
+            umma_commit(&s.final_sa);
+            mbar_drain(&s.final_sa, 0);
+        }
+    } else if (warp == 2) {
+        // ============== MMA issuer 2: Y += M K (moments, CG) or U V (output) ==============
+        // A separate warp, so that its issue stream and the first issuer's overlap: each MMA
+        // warp shares its sub-partition's scheduler with two elementwise warps.
+        if (lane == 0) {
+            uint32_t fill = 0, pr = 0, g = 0;
+            bool ok = WAIT(&s.q_full, 0, err);
+            int cg_sweeps = 0;
+            for (int sweep = 0; ok; ++sweep) {
+                int type;
+                if (sweep == 0) type = SW_MAX;
+                else if (sweep == 1) type = SW_MOMENT;
+                else if (!dynamic) type = cg_sweeps < prm.cg_max_iters ? SW_CG : SW_OUT;
+                else {
+                    if (!(ok = WAIT(&s.p_ready, pr & 1, err))) break;
+                    ++pr;
+                    type = s.next_type;
+                }
+                if (type == SW_CG) ++cg_sweeps;
+                const uint32_t ty_acc = tY;
+                for (int kb = 0; kb < nkb; ++kb, ++g) {
+                    const uint32_t fk = fill++;
+                    const uint32_t fv = type == SW_OUT ? fill++ : 0;
+                    const uint32_t b = g & 1;
+                    if (!(ok = WAIT(&s.ew_done[b], (g >> 1) & 1, err))) break;
+                    if (type != SW_MAX) {
+                        if (type == SW_OUT && !(ok = WAIT(&s.slot_full[fv % NSLOT], (fv / NSLOT) & 1, err))) break;
+                        tc_fence_after();
+                        const uint32_t src = smem_u32(s.slot[(type == SW_OUT ? fv : fk) % NSLOT]);
+                        gemm_y<D>(ty_acc, tS0 + b * 128, src, kb > 0);
+                        umma_commit(&s.slot_empty[(type == SW_OUT ? fv : fk) % NSLOT]);
+                        if (kb == nkb - 1) umma_commit(&s.y_done);
+                    }
+                    umma_commit(&s.m_free[b]);
+                }
+                if (type == SW_OUT) break;
+            }
+            umma_commit(&s.final_y);
+            mbar_drain(&s.final_y, 0);
         }
     }
     } else {
@@ -534,7 +562,8 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const size_t row_g = ((size_t)head * n + (row_ok ? i : 0)) * D + half * DH;
         // tile-transposed fp32 scratch: coordinate e of this thread's row at [e * BQ] (coalesced)
         const size_t tbase = ((size_t)(head * prm.n_tiles + tile) * D + half * DH) * BQ + row;
-        float* xt = prm.xs + tbase;             // CG iterate x = rho'
+        float* xt = prm.xs + tbase;             // CG iterate x = rho' (this thread's coordinates)
+        float* xtile = prm.xs + (size_t)(head * prm.n_tiles + tile) * D * BQ;   // the whole tile's x
         float* kbt = prm.kbar + tbase;          // kbar
         Xch xch{s.xch, 0, half, row};
 
@@ -609,7 +638,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const float m2 = row_ok ? mx * c_log2 : 0.f;
 
         // ---------------- MOMENT sweep ----------------
-        float om_part = 0.f;
+        uint64_t om_part = 0;              // two fp32 partial sums (bit pattern 0 = +0.0f, +0.0f)
         for (int kb = 0; kb < nkb; ++kb, ++g) {
             ok = ok && wait_s(g);
             const uint32_t tS = tS0 + (g & 1) * 128 + lane_off + half * 64;
@@ -631,14 +660,36 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             done_block(g);
         }
         ok = ok && wait_y();
-        const float om_all = xch.sum(om_part);      // every elementwise thread joins the exchange
+        const float om_all = xch.sum(f2_total(om_part));      // every elementwise thread joins the exchange
         const float omega = row_ok ? om_all * pow2i(-14) : 1.f;
         const float inv_om = 1.f / omega;
         const float lam_n = prm.lambda * inv_om;
 
         // kbar, delta, CG initialisation (this thread: coordinates half*DH .. half*DH+DH-1)
         float res[DH];
+        float gamma, rn0;
+        bool active;
+        int iters = 0;
+        // p = res + beta p_old as the next direction (fp16 x 2^sp); per-row params of the sweep
+        int sp = 0, sM = 0;
+        float kp_acc = 0.f, offM = 0.f;
+        // kv: this thread's kbar coordinates in registers (named kv wherever this is expanded)
+#define LLA_SET_DIRECTION(BETA, KEEP)                                                                      \
+        {                                                                                                  \
+            const float osc_ = pow2i(-sp);                                                                 \
+            const float mp_ = xch.max(dir_maxabs<DH>(res, s.p, s.rlo, split_p, row, half * DH, (BETA), (KEEP), \
+                                                      osc_));                                              \
+            const int sp_new_ = min(scale_exp(mp_), 100 - ek);   /* keeps 2^(sp+ek) finite */             \
+            const float kp_ = xch.sum(dir_store<DH>(res, s.p, s.rlo, split_p, row, half * DH, (BETA), (KEEP), \
+                                                    osc_,                                                  \
+                                                    pow2i(sp_new_), pow2i(-sp_new_), kv));                 \
+            sp = sp_new_;                                                                                  \
+            sM = scale_exp(kbound * mp_ * 1.001f);                                                         \
+            offM = m2 - (float)sM + (float)sp + (float)ek;                                                 \
+            kp_acc = kp_ * pow2i(sp + ek);                                                                 \
+        }
         {
+            float kv[DH];
             const float ysc = pow2i(-(14 + ek)) * inv_om;
             const float qsc = pow2i(-eq);
 #pragma unroll
@@ -653,43 +704,20 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
                         const float kb_ = v[j + u] * ysc;
+                        kv[c * 32 + j + u] = kb_;
                         kbt[(c * 32 + j + u) * BQ] = kb_;
-                        xt[(c * 32 + j + u) * BQ] = 0.f;
                         res[c * 32 + j + u] = row_ok ? kb_ - __half2float(qh[u]) * qsc : 0.f;
                     }
                 }
             }
-        }
-
-        float gamma;
-        {
             float gp = 0.f;
 #pragma unroll
             for (int e = 0; e < DH; ++e) gp = fmaf(res[e], res[e], gp);
             gamma = xch.sum(gp);
+            rn0 = sqrtf(gamma);
+            active = row_ok && gamma > 0.f && !(sqrtf(gamma) <= prm.cg_tol * rn0);
+            LLA_SET_DIRECTION(0.f, false);
         }
-        const float rn0 = sqrtf(gamma);
-        bool active = row_ok && gamma > 0.f && !(sqrtf(gamma) <= prm.cg_tol * rn0);
-        int iters = 0;
-
-        // p = res + beta p_old as the next direction (fp16 x 2^sp); per-row params of the sweep
-        int sp = 0, sM = 0;
-        float kp_acc = 0.f, offM = 0.f;
-#define LLA_SET_DIRECTION(BETA, KEEP)                                                                      \
-        {                                                                                                  \
-            const float osc_ = pow2i(-sp);                                                                 \
-            const float mp_ = xch.max(dir_maxabs<DH>(res, s.p, s.rlo, split_p, row, half * DH, (BETA), (KEEP), \
-                                                      osc_));                                              \
-            const int sp_new_ = min(scale_exp(mp_), 100 - ek);   /* keeps 2^(sp+ek) finite */             \
-            const float kp_ = xch.sum(dir_store<DH>(res, s.p, s.rlo, split_p, row, half * DH, (BETA), (KEEP), \
-                                                    osc_,                                                  \
-                                                    pow2i(sp_new_), pow2i(-sp_new_), kbt));                \
-            sp = sp_new_;                                                                                  \
-            sM = scale_exp(kbound * mp_ * 1.001f);                                                         \
-            offM = m2 - (float)sM + (float)sp + (float)ek;                                                 \
-            kp_acc = kp_ * pow2i(sp + ek);                                                                 \
-        }
-        LLA_SET_DIRECTION(0.f, false);
 
         // ---------------- CG sweeps ----------------
         int cg_sweeps = 0;
@@ -700,7 +728,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             if (!go) break;
             publish_p(SW_CG);
             ++cg_sweeps;
-            float msum_part = 0.f;
+            uint64_t msum_part = 0;
             for (int kb = 0; kb < nkb; ++kb, ++g) {
                 ok = ok && wait_s(g);
                 const uint32_t tS = tS0 + (g & 1) * 128 + lane_off + half * 64;
@@ -725,39 +753,75 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 tmem_st_wait();
                 done_block(g);
             }
+            // kbar for the update, loaded while the sweep's last Y products run; the update then
+            // reaches global memory only through fire-and-forget reductions into x
+            float kv[DH];
+#pragma unroll
+            for (int e = 0; e < DH; ++e) kv[e] = kbt[e * BQ];
             ok = ok && wait_y();
             // ---- CG update: (C/omega) p = [Y 2^-(sM+ek) - kbar msum 2^-sM] / omega + (lambda/omega) p
-            const float msum = xch.sum(msum_part);
+            const float msum = xch.sum(f2_total(msum_part));
             const float ysc = pow2i(-(sM + ek)) * inv_om;
             const float msc = msum * pow2i(-sM) * inv_om;
             const float psc = pow2i(-sp);
+            const uint32_t ty = tY + lane_off + half * DH;
             float pcp = 0.f;
-#pragma unroll
-            for (int c = 0; c < DH / 32; ++c) {
-                float cp[32], ph[32];
-                cp_chunk32(tY + lane_off + half * DH + c * 32, s.p, s.rlo, split_p, row, half * DH + c * 32, kbt + c * 32 * BQ, ysc,
-                           msc, lam_n, psc, cp, ph);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) pcp = fmaf(ph[j], cp[j], pcp);
+#define LLA_CP_DOT(C)                                                                                      \
+            if constexpr ((C) * 16 < DH) {                                                                 \
+                float cp[16], ph[16];                                                                      \
+                cp_chunk16<C, DH>(ty + (C) * 16, s.p, s.rlo, split_p, row, half * DH + (C) * 16, kv, ysc,   \
+                                  msc, lam_n, psc, cp, ph);                                                \
+                _Pragma("unroll") for (int j = 0; j < 16; ++j) pcp = fmaf(ph[j], cp[j], pcp);             \
             }
+            LLA_CP_DOT(0);
+            LLA_CP_DOT(1);
+            LLA_CP_DOT(2);
+            LLA_CP_DOT(3);
+#undef LLA_CP_DOT
             pcp = xch.sum(pcp);
             const bool upd = active && pcp > 0.f;
             const float alpha = upd ? gamma / pcp : 0.f;
             float g2 = 0.f;
-#pragma unroll
-            for (int c = 0; c < DH / 32; ++c) {
-                float cp[32], ph[32];
-                cp_chunk32(tY + lane_off + half * DH + c * 32, s.p, s.rlo, split_p, row, half * DH + c * 32, kbt + c * 32 * BQ, ysc,
-                           msc, lam_n, psc, cp, ph);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    if (upd) {
-                        xt[(c * 32 + j) * BQ] = fmaf(alpha, ph[j], xt[(c * 32 + j) * BQ]);
-                        res[c * 32 + j] = fmaf(-alpha, cp[j], res[c * 32 + j]);
-                    }
-                    g2 = fmaf(res[c * 32 + j], res[c * 32 + j], g2);
-                }
+// x += alpha p_hat goes through shared memory: the increments of 8 coordinates x 128 rows per
+// half are staged, and one thread has the TMA engine add them to x in global memory (the first
+// sweep copies instead, so x needs no initialisation).  One barrier per 8 coordinates; a staging
+// buffer is rewritten only after the bulk operation two rounds back has finished reading it.
+#define LLA_X_ROUND(R, OFF)                                                                                \
+            {                                                                                              \
+                float* st_ = &s.stg[(R) & 1][half][0][row];                                                \
+                _Pragma("unroll") for (int j = 0; j < 8; ++j) st_[j * BQ] = upd ? alpha * ph[(OFF) + j] : 0.f;   \
+                fence_proxy_async_smem();                                                                  \
+                if (tid == 128) bulk_wait_read_all();                                                      \
+                named_bar_sync(EW_BAR, NEW);                                                               \
+                if (tid == 128) {                                                                          \
+                    _Pragma("unroll") for (int h_ = 0; h_ < 2; ++h_) {                                     \
+                        float* dst_ = xtile + (size_t)(h_ * DH + (R) * 8) * BQ;                            \
+                        if (cg_sweeps == 1) bulk_copy_s2g(dst_, &s.stg[(R) & 1][h_][0][0], 8 * BQ * 4);    \
+                        else bulk_add_f32_s2g(dst_, &s.stg[(R) & 1][h_][0][0], 8 * BQ * 4);               \
+                    }                                                                                      \
+                    bulk_commit();                                                                         \
+                }                                                                                          \
             }
+#define LLA_CP_STEP(C)                                                                                     \
+            if constexpr ((C) * 16 < DH) {                                                                 \
+                float cp[16], ph[16];                                                                      \
+                cp_chunk16<C, DH>(ty + (C) * 16, s.p, s.rlo, split_p, row, half * DH + (C) * 16, kv, ysc,   \
+                                  msc, lam_n, psc, cp, ph);                                                \
+                _Pragma("unroll") for (int j = 0; j < 16; ++j) {                                           \
+                    if (upd) res[(C) * 16 + j] = fmaf(-alpha, cp[j], res[(C) * 16 + j]);                   \
+                    g2 = fmaf(res[(C) * 16 + j], res[(C) * 16 + j], g2);                                   \
+                }                                                                                          \
+                LLA_X_ROUND(2 * (C), 0);                                                                  \
+                LLA_X_ROUND(2 * (C) + 1, 8);                                                          \
+            }
+            // the previous sweep's bulk operations on x are complete before this sweep's land
+            if (tid == 128) bulk_wait_all();
+            LLA_CP_STEP(0);
+            LLA_CP_STEP(1);
+            LLA_CP_STEP(2);
+            LLA_CP_STEP(3);
+#undef LLA_CP_STEP
+#undef LLA_X_ROUND
             g2 = xch.sum(g2);
             float beta = 0.f;
             if (upd) {
@@ -777,6 +841,19 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
 
         // ---------------- finalise rho, denom; R = rho' (hi + lo) for the output sweep ----------------
+        // x and kbar in registers, loaded in one batch; x through L2 (.cg), where its reductions landed
+        if (tid == 128) {
+            bulk_wait_all();                  // x's last additions are performed ...
+            fence_proxy_async_global();       // ... and ordered before the loads below
+        }
+        named_bar_sync(EW_BAR, NEW);
+        float xv[DH], kv[DH];
+        const bool have_x = row_ok && cg_sweeps > 0;   // no sweep ran: x = 0
+#pragma unroll
+        for (int e = 0; e < DH; ++e) {
+            xv[e] = have_x ? __ldcg(xt + e * BQ) : 0.f;
+            kv[e] = kbt[e * BQ];
+        }
         float dx = 0.f, mxx = 0.f;
         {
             const float qsc = pow2i(-eq);
@@ -786,9 +863,8 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 const __half* qh = reinterpret_cast<const __half*>(&qr);
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    const float xv = xt[(e0 + u) * BQ];
-                    dx = fmaf(kbt[(e0 + u) * BQ] - __half2float(qh[u]) * qsc, xv, dx);
-                    mxx = fmaxf(mxx, fabsf(xv));
+                    dx = fmaf(kv[e0 + u] - __half2float(qh[u]) * qsc, xv[e0 + u], dx);
+                    mxx = fmaxf(mxx, fabsf(xv[e0 + u]));
                 }
             }
             if (!row_ok) { dx = 0.f; mxx = 0.f; }
@@ -805,26 +881,23 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 uint4 pk, pl;
                 uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
                 uint32_t* plw = reinterpret_cast<uint32_t*>(&pl);
-                float xr[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) xr[u] = row_ok ? xt[(e0 + u) * BQ] : 0.f;
 #pragma unroll
                 for (int u = 0; u < 8; u += 2) {
-                    const float x0 = xr[u] * rs, x1 = xr[u + 1] * rs;
+                    const float x0 = xv[e0 + u] * rs, x1 = xv[e0 + u + 1] * rs;
                     pw[u >> 1] = pack_half2(x0, x1);
                     const float2 xh = __half22float2(*reinterpret_cast<const __half2*>(&pw[u >> 1]));
                     plw[u >> 1] = pack_half2(x0 - xh.x, x1 - xh.y);
                     const float2 xl = __half22float2(*reinterpret_cast<const __half2*>(&plw[u >> 1]));
-                    kx = fmaf(kbt[(e0 + u) * BQ], (xh.x + xl.x) * ris, kx);
-                    kx = fmaf(kbt[(e0 + u + 1) * BQ], (xh.y + xl.y) * ris, kx);
+                    kx = fmaf(kv[e0 + u], (xh.x + xl.x) * ris, kx);
+                    kx = fmaf(kv[e0 + u + 1], (xh.y + xl.y) * ris, kx);
                 }
                 *reinterpret_cast<uint4*>(tile_half(s.p, row, half * DH + e0)) = pk;
                 *reinterpret_cast<uint4*>(tile_half(s.rlo, row, half * DH + e0)) = pl;
                 if (row_ok) {   // rho = rho' / (1 + delta.rho'), row-major output
                     *reinterpret_cast<float4*>(prm.rho + row_g + e0) =
-                        make_float4(xr[0] * inv_g, xr[1] * inv_g, xr[2] * inv_g, xr[3] * inv_g);
+                        make_float4(xv[e0] * inv_g, xv[e0 + 1] * inv_g, xv[e0 + 2] * inv_g, xv[e0 + 3] * inv_g);
                     *reinterpret_cast<float4*>(prm.rho + row_g + e0 + 4) =
-                        make_float4(xr[4] * inv_g, xr[5] * inv_g, xr[6] * inv_g, xr[7] * inv_g);
+                        make_float4(xv[e0 + 4] * inv_g, xv[e0 + 5] * inv_g, xv[e0 + 6] * inv_g, xv[e0 + 7] * inv_g);
                 }
             }
             if (!row_ok) kx = 0.f;
@@ -840,7 +913,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         publish_p(SW_OUT);
 
         // ---------------- OUT sweep ----------------
-        float us_part = 0.f;
+        uint64_t us_part = 0;
         for (int kb = 0; kb < nkb; ++kb, ++g) {
             ok = ok && wait_s(g);
             const uint32_t tS = tS0 + (g & 1) * 128 + lane_off + half * 64;
@@ -866,7 +939,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             done_block(g);
         }
         ok = ok && wait_y();
-        const float usum = xch.sum(us_part);
+        const float usum = xch.sum(f2_total(us_part));
         const float osc = pow2i(-ev) / usum;
 #pragma unroll
         for (int c = 0; c < DH / 32; ++c) {
