@@ -136,9 +136,8 @@ struct TcSmem {
     unsigned char rlo[TILE];                           // R_lo (output sweep); P_lo (CG sweeps of tile 0)
     unsigned char slot[NSLOT][TILE];                   // K / V blocks (TMA)
     uint64_t slot_full[NSLOT], slot_empty[NSLOT];
-    float stg[2][2][8][BQ];                            // CG iterate increments: [buffer][half][coord][row]
     uint64_t q_full, s_full[2], ew_done[2], m_free[2], a_free, y_done, p_ready, final_sa, final_y;
-    float xch[2][2][BQ];                               // row-scalar exchange between the two halves
+    float2 xch[2][2][BQ];                              // row-scalar exchange between the two halves
     uint32_t tmem_base;
     int err;
     int next_type;
@@ -162,22 +161,21 @@ struct TcParams {
 // turn suffice: a thread writes a buffer again only after the next exchange's barrier, which its
 // partner reaches only after reading that buffer.
 struct Xch {
-    float (*buf)[2][BQ];
+    float2 (*buf)[2][BQ];
     int idx, half, row;
-    __device__ float sum(float v) {
-        float* b = &buf[idx][0][0];
+    __device__ float2 swap(float2 v) {
+        float2* b = &buf[idx][0][0];
         idx ^= 1;
         b[half * BQ + row] = v;
         named_bar_sync(EW_BAR, NEW);
-        return v + b[(1 - half) * BQ + row];
+        return b[(1 - half) * BQ + row];
     }
-    __device__ float max(float v) {
-        float* b = &buf[idx][0][0];
-        idx ^= 1;
-        b[half * BQ + row] = v;
-        named_bar_sync(EW_BAR, NEW);
-        return fmaxf(v, b[(1 - half) * BQ + row]);
+    __device__ float sum(float v) { return v + swap(make_float2(v, 0.f)).x; }
+    __device__ float2 sum2(float a, float c) {
+        const float2 o = swap(make_float2(a, c));
+        return make_float2(a + o.x, c + o.y);
     }
+    __device__ float max(float v) { return fmaxf(v, swap(make_float2(v, 0.f)).x); }
 };
 
 __device__ __forceinline__ bool ew_any(bool pred) {
@@ -205,91 +203,51 @@ __device__ __forceinline__ __half* tile_half(const unsigned char* t, int row, in
     return reinterpret_cast<__half*>(const_cast<unsigned char*>(t) + sw128_offset(row, col, BQ));
 }
 
-// max |res + beta p_old| over this thread's DH coordinates (p_old = (hi [+ lo] tile values) * osc)
-template <int DH>
-__device__ __forceinline__ float dir_maxabs(const float (&res)[DH], const unsigned char* ptile, const unsigned char* plo,
-                                            bool split, int row, int col0, float beta, bool keep_old, float osc) {
-    float mp = 0.f;
+// 8 consecutive coordinates (from col) of this thread's row of a direction tile, unscaled:
+// o = (hi [+ lo]) * sc.  split: the tile carries an fp16 remainder in lo (about 22 bits in all).
+__device__ __forceinline__ void load_dir8(const unsigned char* hi, const unsigned char* lo, bool split, int row, int col,
+                                          float sc, float (&o)[8]) {
+    const uint4 h = *reinterpret_cast<const uint4*>(tile_half(hi, row, col));
+    const __half2* h2 = reinterpret_cast<const __half2*>(&h);
+    const uint64_t sc2 = f2_pack(sc, sc);
+    if (split) {
+        const uint4 l = *reinterpret_cast<const uint4*>(tile_half(lo, row, col));
+        const __half2* l2 = reinterpret_cast<const __half2*>(&l);
 #pragma unroll
-    for (int e0 = 0; e0 < DH; e0 += 8) {
-        const uint4 old = *reinterpret_cast<const uint4*>(tile_half(ptile, row, col0 + e0));
-        uint4 oldl = make_uint4(0u, 0u, 0u, 0u);
-        if (split) oldl = *reinterpret_cast<const uint4*>(tile_half(plo, row, col0 + e0));
-        const __half* oh = reinterpret_cast<const __half*>(&old);
-        const __half* ol = reinterpret_cast<const __half*>(&oldl);
+        for (int u = 0; u < 4; ++u) {
+            const float2 a = __half22float2(h2[u]), b = __half22float2(l2[u]);
+            f2_unpack(f2_mul(f2_add(f2_pack(a.x, a.y), f2_pack(b.x, b.y)), sc2), o[2 * u], o[2 * u + 1]);
+        }
+    } else {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const float pold = keep_old ? (__half2float(oh[u]) + __half2float(ol[u])) * osc : 0.f;
-            mp = fmaxf(mp, fabsf(fmaf(beta, pold, res[e0 + u])));
+        for (int u = 0; u < 4; ++u) {
+            const float2 a = __half22float2(h2[u]);
+            f2_unpack(f2_mul(f2_pack(a.x, a.y), sc2), o[2 * u], o[2 * u + 1]);
         }
     }
-    return mp;
 }
 
-// Store fp16((res + beta p_old) * nsc) over the old values (and, when split, the fp16 remainder
-// in the lo tile, so hi + lo carries about 22 bits); returns kbar . p_hat (partial), p_hat being
-// the stored value.  kv: this thread's kbar coordinates.
-template <int DH>
-__device__ __forceinline__ float dir_store(const float (&res)[DH], unsigned char* ptile, unsigned char* plo, bool split,
-                                           int row, int col0, float beta, bool keep_old, float osc, float nsc,
-                                           float nisc, const float (&kv)[DH]) {
-    float kp = 0.f;
-#pragma unroll
-    for (int e0 = 0; e0 < DH; e0 += 8) {
-        __half* hp = tile_half(ptile, row, col0 + e0);   // 8 consecutive columns = one 16-byte chunk
-        __half* lp = tile_half(plo, row, col0 + e0);
-        const uint4 old = *reinterpret_cast<const uint4*>(hp);
-        uint4 oldl = make_uint4(0u, 0u, 0u, 0u);
-        if (split) oldl = *reinterpret_cast<const uint4*>(lp);
-        const __half* oh = reinterpret_cast<const __half*>(&old);
-        const __half* ol = reinterpret_cast<const __half*>(&oldl);
-        uint4 pk, pl;
-        uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
-        uint32_t* plw = reinterpret_cast<uint32_t*>(&pl);
-#pragma unroll
-        for (int u = 0; u < 8; u += 2) {
-            const float o0 = keep_old ? (__half2float(oh[u]) + __half2float(ol[u])) * osc : 0.f;
-            const float o1 = keep_old ? (__half2float(oh[u + 1]) + __half2float(ol[u + 1])) * osc : 0.f;
-            const float p0 = fmaf(beta, o0, res[e0 + u]) * nsc;
-            const float p1 = fmaf(beta, o1, res[e0 + u + 1]) * nsc;
-            pw[u >> 1] = pack_half2(p0, p1);
-            float2 ph = __half22float2(*reinterpret_cast<const __half2*>(&pw[u >> 1]));
-            if (split) {
-                plw[u >> 1] = pack_half2(p0 - ph.x, p1 - ph.y);
-                const float2 pl2 = __half22float2(*reinterpret_cast<const __half2*>(&plw[u >> 1]));
-                ph.x += pl2.x;
-                ph.y += pl2.y;
-            }
-            kp = fmaf(kv[e0 + u], ph.x * nisc, kp);
-            kp = fmaf(kv[e0 + u + 1], ph.y * nisc, kp);
-        }
-        *reinterpret_cast<uint4*>(hp) = pk;
-        if (split) *reinterpret_cast<uint4*>(lp) = pl;
-    }
-    return kp;
-}
-
-// One 16-coordinate chunk (chunk C of this thread's DH) of (C/omega) p and of p_hat for this
-// thread's row; kv holds this thread's kbar coordinates.
+// CG update, first pass over one 16-coordinate chunk C of this thread's DH coordinates:
+//   cp = (C/omega) p_hat = Y ysc - kbar msc + lam_n p_hat   (kept for the second pass)
+// and the partial dot p_hat.cp (two fp32 partial sums).
 template <int C, int DH>
-__device__ __forceinline__ void cp_chunk16(uint32_t ty, const unsigned char* ptile, const unsigned char* plo, bool split,
-                                           int row, int col, const float (&kv)[DH], float ysc, float msc, float lam_n,
-                                           float psc, float (&cp)[16], float (&ph)[16]) {
-    float v[16];
-    tmem_ld16(ty, v);
-#pragma unroll
-    for (int j = 0; j < 16; j += 8) {
-        const uint4 pr = *reinterpret_cast<const uint4*>(tile_half(ptile, row, col + j));
-        uint4 prl = make_uint4(0u, 0u, 0u, 0u);
-        if (split) prl = *reinterpret_cast<const uint4*>(tile_half(plo, row, col + j));
-        const __half* phh = reinterpret_cast<const __half*>(&pr);
-        const __half* phl = reinterpret_cast<const __half*>(&prl);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) ph[j + u] = (__half2float(phh[u]) + __half2float(phl[u])) * psc;
-    }
+__device__ __forceinline__ void cg_apply_chunk(uint32_t ty, const unsigned char* ptile, const unsigned char* plo, bool split,
+                                               int row, int col, const float (&kv)[DH], float ysc, float msc, float lam_n,
+                                               float psc, float (&cp)[DH], uint64_t& pcp2) {
+    float y[16], p0[8], p1[8];
+    tmem_ld16(ty + C * 16, y);
+    load_dir8(ptile, plo, split, row, col + C * 16, psc, p0);
+    load_dir8(ptile, plo, split, row, col + C * 16 + 8, psc, p1);
     tmem_ld_wait();
+    const uint64_t ysc2 = f2_pack(ysc, ysc), nmsc2 = f2_pack(-msc, -msc), lam2 = f2_pack(lam_n, lam_n);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) cp[j] = fmaf(v[j], ysc, fmaf(-kv[C * 16 + j], msc, lam_n * ph[j]));
+    for (int j = 0; j < 16; j += 2) {
+        const uint64_t ph = j < 8 ? f2_pack(p0[j], p0[j + 1]) : f2_pack(p1[j - 8], p1[j - 7]);
+        const uint64_t kb = f2_pack(kv[C * 16 + j], kv[C * 16 + j + 1]);
+        const uint64_t c2 = f2_fma(f2_pack(y[j], y[j + 1]), ysc2, f2_fma(kb, nmsc2, f2_mul(ph, lam2)));
+        f2_unpack(c2, cp[C * 16 + j], cp[C * 16 + j + 1]);
+        pcp2 = f2_fma(ph, c2, pcp2);
+    }
 }
 
 // Per-pair coefficients of one 32-key chunk (chunk C of this thread's 64 keys):
@@ -562,8 +520,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const size_t row_g = ((size_t)head * n + (row_ok ? i : 0)) * D + half * DH;
         // tile-transposed fp32 scratch: coordinate e of this thread's row at [e * BQ] (coalesced)
         const size_t tbase = ((size_t)(head * prm.n_tiles + tile) * D + half * DH) * BQ + row;
-        float* xt = prm.xs + tbase;             // CG iterate x = rho' (this thread's coordinates)
-        float* xtile = prm.xs + (size_t)(head * prm.n_tiles + tile) * D * BQ;   // the whole tile's x
+        float* xt = prm.xs + tbase;             // CG iterate x = rho'
         float* kbt = prm.kbar + tbase;          // kbar
         Xch xch{s.xch, 0, half, row};
 
@@ -670,23 +627,60 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         float gamma, rn0;
         bool active;
         int iters = 0;
-        // p = res + beta p_old as the next direction (fp16 x 2^sp); per-row params of the sweep
-        int sp = 0, sM = 0;
-        float kp_acc = 0.f, offM = 0.f;
-        // kv: this thread's kbar coordinates in registers (named kv wherever this is expanded)
-#define LLA_SET_DIRECTION(BETA, KEEP)                                                                      \
+        int sp = 0, sM = 0;                  // scale exponents of the direction tile and of M
+        float kp_acc = 0.f, offM = 0.f;      // per-row parameters of the next CG sweep
+        // kbar.res (a dot product each iteration) and kbar.p (by recurrence, p = res + beta p_old),
+        // whole row.  kbar.p only centres the per-pair coefficients (the kbar msum term of the
+        // update cancels any offset exactly), so it need not match the rounded direction bit for
+        // bit; kbar.res is recomputed, not updated, because a converging residual cancels.
+        float kbr = 0.f, kpx = 0.f;
+        int cg_sweeps = 0;
+        // New direction p = res + beta p_old (PN: DH floats of scratch), stored in the direction
+        // tile as fp16 x 2^sp (hi, and lo when split_p); with XUPD also x += ALPHA p_old (the
+        // direction of the sweep just finished; the first sweep stores instead of adding).
+#define LLA_SET_DIRECTION(BETA, KEEP, XUPD, ALPHA, PN)                                                     \
         {                                                                                                  \
             const float osc_ = pow2i(-sp);                                                                 \
-            const float mp_ = xch.max(dir_maxabs<DH>(res, s.p, s.rlo, split_p, row, half * DH, (BETA), (KEEP), \
-                                                      osc_));                                              \
+            const uint64_t b2_ = f2_pack((BETA), (BETA));                                                  \
+            float mp_ = 0.f;                                                                               \
+            _Pragma("unroll") for (int e0 = 0; e0 < DH; e0 += 8) {                                         \
+                float po_[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};                                   \
+                if (KEEP) load_dir8(s.p, s.rlo, split_p, row, half * DH + e0, osc_, po_);                  \
+                _Pragma("unroll") for (int u = 0; u < 8; u += 2) {                                         \
+                    f2_unpack(f2_fma(b2_, f2_pack(po_[u], po_[u + 1]), f2_pack(res[e0 + u], res[e0 + u + 1])), \
+                              PN[e0 + u], PN[e0 + u + 1]);                                                 \
+                    mp_ = fmaxf(mp_, fmaxf(fabsf(PN[e0 + u]), fabsf(PN[e0 + u + 1])));                    \
+                }                                                                                          \
+            }                                                                                              \
+            mp_ = xch.max(mp_);                                                                            \
             const int sp_new_ = min(scale_exp(mp_), 100 - ek);   /* keeps 2^(sp+ek) finite */             \
-            const float kp_ = xch.sum(dir_store<DH>(res, s.p, s.rlo, split_p, row, half * DH, (BETA), (KEEP), \
-                                                    osc_,                                                  \
-                                                    pow2i(sp_new_), pow2i(-sp_new_), kv));                 \
+            const float nsc_ = pow2i(sp_new_);                                                             \
+            _Pragma("unroll") for (int e0 = 0; e0 < DH; e0 += 8) {                                         \
+                if (XUPD) {                                                                                \
+                    float po_[8];                                                                          \
+                    load_dir8(s.p, s.rlo, split_p, row, half * DH + e0, osc_, po_);                        \
+                    _Pragma("unroll") for (int u = 0; u < 8; ++u) {                                        \
+                        if (cg_sweeps == 1) xt[(e0 + u) * BQ] = (ALPHA) * po_[u];                          \
+                        else red_add_f32(xt + (e0 + u) * BQ, (ALPHA) * po_[u]);                            \
+                    }                                                                                      \
+                }                                                                                          \
+                uint4 hk_, lk_;                                                                            \
+                uint32_t* hw_ = reinterpret_cast<uint32_t*>(&hk_);                                         \
+                uint32_t* lw_ = reinterpret_cast<uint32_t*>(&lk_);                                         \
+                _Pragma("unroll") for (int u = 0; u < 8; u += 2) {                                         \
+                    const float x0_ = PN[e0 + u] * nsc_, x1_ = PN[e0 + u + 1] * nsc_;                      \
+                    hw_[u >> 1] = pack_half2(x0_, x1_);                                                    \
+                    const float2 hf_ = __half22float2(*reinterpret_cast<const __half2*>(&hw_[u >> 1]));   \
+                    lw_[u >> 1] = pack_half2(x0_ - hf_.x, x1_ - hf_.y);                                    \
+                }                                                                                          \
+                *reinterpret_cast<uint4*>(tile_half(s.p, row, half * DH + e0)) = hk_;                      \
+                if (split_p) *reinterpret_cast<uint4*>(tile_half(s.rlo, row, half * DH + e0)) = lk_;       \
+            }                                                                                              \
             sp = sp_new_;                                                                                  \
             sM = scale_exp(kbound * mp_ * 1.001f);                                                         \
             offM = m2 - (float)sM + (float)sp + (float)ek;                                                 \
-            kp_acc = kp_ * pow2i(sp + ek);                                                                 \
+            kpx = kbr + (BETA) * kpx;                                                                      \
+            kp_acc = kpx * pow2i(sp + ek);                                                                 \
         }
         {
             float kv[DH];
@@ -710,17 +704,22 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     }
                 }
             }
-            float gp = 0.f;
+            float gp = 0.f, kr = 0.f;
 #pragma unroll
-            for (int e = 0; e < DH; ++e) gp = fmaf(res[e], res[e], gp);
-            gamma = xch.sum(gp);
+            for (int e = 0; e < DH; ++e) {
+                gp = fmaf(res[e], res[e], gp);
+                kr = fmaf(kv[e], res[e], kr);
+            }
+            const float2 t = xch.sum2(gp, kr);
+            gamma = t.x;
+            kbr = t.y;
             rn0 = sqrtf(gamma);
             active = row_ok && gamma > 0.f && !(sqrtf(gamma) <= prm.cg_tol * rn0);
-            LLA_SET_DIRECTION(0.f, false);
+            float pn[DH];
+            LLA_SET_DIRECTION(0.f, false, false, 0.f, pn);
         }
 
         // ---------------- CG sweeps ----------------
-        int cg_sweeps = 0;
         while (true) {                         // uniform across the elementwise threads
             bool go;
             if (!dynamic) go = cg_sweeps < prm.cg_max_iters;
@@ -753,8 +752,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 tmem_st_wait();
                 done_block(g);
             }
-            // kbar for the update, loaded while the sweep's last Y products run; the update then
-            // reaches global memory only through fire-and-forget reductions into x
+            // kbar for the update, loaded while the sweep's last Y products run
             float kv[DH];
 #pragma unroll
             for (int e = 0; e < DH; ++e) kv[e] = kbt[e * BQ];
@@ -765,69 +763,37 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const float msc = msum * pow2i(-sM) * inv_om;
             const float psc = pow2i(-sp);
             const uint32_t ty = tY + lane_off + half * DH;
-            float pcp = 0.f;
-#define LLA_CP_DOT(C)                                                                                      \
-            if constexpr ((C) * 16 < DH) {                                                                 \
-                float cp[16], ph[16];                                                                      \
-                cp_chunk16<C, DH>(ty + (C) * 16, s.p, s.rlo, split_p, row, half * DH + (C) * 16, kv, ysc,   \
-                                  msc, lam_n, psc, cp, ph);                                                \
-                _Pragma("unroll") for (int j = 0; j < 16; ++j) pcp = fmaf(ph[j], cp[j], pcp);             \
+            float cp[DH];
+            uint64_t pcp2 = 0;
+            cg_apply_chunk<0, DH>(ty, s.p, s.rlo, split_p, row, half * DH, kv, ysc, msc, lam_n, psc, cp, pcp2);
+            cg_apply_chunk<1, DH>(ty, s.p, s.rlo, split_p, row, half * DH, kv, ysc, msc, lam_n, psc, cp, pcp2);
+            if constexpr (DH > 32) {
+                cg_apply_chunk<2, DH>(ty, s.p, s.rlo, split_p, row, half * DH, kv, ysc, msc, lam_n, psc, cp, pcp2);
+                cg_apply_chunk<3, DH>(ty, s.p, s.rlo, split_p, row, half * DH, kv, ysc, msc, lam_n, psc, cp, pcp2);
             }
-            LLA_CP_DOT(0);
-            LLA_CP_DOT(1);
-            LLA_CP_DOT(2);
-            LLA_CP_DOT(3);
-#undef LLA_CP_DOT
-            pcp = xch.sum(pcp);
+            const float pcp = xch.sum(f2_total(pcp2));
             const bool upd = active && pcp > 0.f;
             const float alpha = upd ? gamma / pcp : 0.f;
-            float g2 = 0.f;
-// x += alpha p_hat goes through shared memory: the increments of 8 coordinates x 128 rows per
-// half are staged, and one thread has the TMA engine add them to x in global memory (the first
-// sweep copies instead, so x needs no initialisation).  One barrier per 8 coordinates; a staging
-// buffer is rewritten only after the bulk operation two rounds back has finished reading it.
-#define LLA_X_ROUND(R, OFF)                                                                                \
-            {                                                                                              \
-                float* st_ = &s.stg[(R) & 1][half][0][row];                                                \
-                _Pragma("unroll") for (int j = 0; j < 8; ++j) st_[j * BQ] = upd ? alpha * ph[(OFF) + j] : 0.f;   \
-                fence_proxy_async_smem();                                                                  \
-                if (tid == 128) bulk_wait_read_all();                                                      \
-                named_bar_sync(EW_BAR, NEW);                                                               \
-                if (tid == 128) {                                                                          \
-                    _Pragma("unroll") for (int h_ = 0; h_ < 2; ++h_) {                                     \
-                        float* dst_ = xtile + (size_t)(h_ * DH + (R) * 8) * BQ;                            \
-                        if (cg_sweeps == 1) bulk_copy_s2g(dst_, &s.stg[(R) & 1][h_][0][0], 8 * BQ * 4);    \
-                        else bulk_add_f32_s2g(dst_, &s.stg[(R) & 1][h_][0][0], 8 * BQ * 4);               \
-                    }                                                                                      \
-                    bulk_commit();                                                                         \
-                }                                                                                          \
+            uint64_t g22 = 0, kr2 = 0;
+            {
+                const uint64_t na2 = f2_pack(-alpha, -alpha);
+#pragma unroll
+                for (int e = 0; e < DH; e += 2) {
+                    uint64_t r2 = f2_pack(res[e], res[e + 1]);
+                    if (upd) r2 = f2_fma(na2, f2_pack(cp[e], cp[e + 1]), r2);
+                    f2_unpack(r2, res[e], res[e + 1]);
+                    g22 = f2_fma(r2, r2, g22);
+                    kr2 = f2_fma(f2_pack(kv[e], kv[e + 1]), r2, kr2);
+                }
             }
-#define LLA_CP_STEP(C)                                                                                     \
-            if constexpr ((C) * 16 < DH) {                                                                 \
-                float cp[16], ph[16];                                                                      \
-                cp_chunk16<C, DH>(ty + (C) * 16, s.p, s.rlo, split_p, row, half * DH + (C) * 16, kv, ysc,   \
-                                  msc, lam_n, psc, cp, ph);                                                \
-                _Pragma("unroll") for (int j = 0; j < 16; ++j) {                                           \
-                    if (upd) res[(C) * 16 + j] = fmaf(-alpha, cp[j], res[(C) * 16 + j]);                   \
-                    g2 = fmaf(res[(C) * 16 + j], res[(C) * 16 + j], g2);                                   \
-                }                                                                                          \
-                LLA_X_ROUND(2 * (C), 0);                                                                  \
-                LLA_X_ROUND(2 * (C) + 1, 8);                                                          \
-            }
-            // the previous sweep's bulk operations on x are complete before this sweep's land
-            if (tid == 128) bulk_wait_all();
-            LLA_CP_STEP(0);
-            LLA_CP_STEP(1);
-            LLA_CP_STEP(2);
-            LLA_CP_STEP(3);
-#undef LLA_CP_STEP
-#undef LLA_X_ROUND
-            g2 = xch.sum(g2);
+            const float2 gk = xch.sum2(f2_total(g22), f2_total(kr2));   // res.res, kbar.res
+            const float g2 = gk.x;
             float beta = 0.f;
             if (upd) {
                 beta = g2 / gamma;
                 gamma = g2;
                 ++iters;
+                kbr = gk.y;
                 if (gamma == 0.f || sqrtf(gamma) <= prm.cg_tol * rn0) active = false;
             } else {
                 active = false;
@@ -836,17 +802,13 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
                 for (int e = 0; e < DH; ++e) res[e] = 0.f;   // finished rows keep a zero direction
                 beta = 0.f;
+                kbr = 0.f;
             }
-            LLA_SET_DIRECTION(beta, true);
+            LLA_SET_DIRECTION(beta, true, true, alpha, cp);      // cp's storage holds the new direction
         }
 
         // ---------------- finalise rho, denom; R = rho' (hi + lo) for the output sweep ----------------
         // x and kbar in registers, loaded in one batch; x through L2 (.cg), where its reductions landed
-        if (tid == 128) {
-            bulk_wait_all();                  // x's last additions are performed ...
-            fence_proxy_async_global();       // ... and ordered before the loads below
-        }
-        named_bar_sync(EW_BAR, NEW);
         float xv[DH], kv[DH];
         const bool have_x = row_ok && cg_sweeps > 0;   // no sweep ran: x = 0
 #pragma unroll

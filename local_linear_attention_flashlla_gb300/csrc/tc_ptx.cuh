@@ -237,29 +237,6 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// ------------------------------------------------------------------ bulk async copies
-// Contiguous shared -> global transfers run by the TMA engine (no tensor map): a plain copy, or
-// an element-wise fp32 add into global memory.  Both addresses 16-byte aligned, bytes a multiple
-// of 16.  The source must have been made visible to the async proxy (fence_proxy_async_smem).
-__device__ __forceinline__ void bulk_copy_s2g(void* gdst, const void* ssrc, uint32_t bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(smem_u32(ssrc)),
-                 "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_add_f32_s2g(float* gdst, const void* ssrc, uint32_t bytes) {
-    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(gdst),
-                 "r"(smem_u32(ssrc)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// every committed bulk group of this thread has finished reading its shared-memory source
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// every committed bulk group of this thread has completed (its global writes are performed)
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void fence_proxy_async_global() {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 // Fire-and-forget fp32 add to global memory, performed at L2 (no value comes back, so the
 // issuing thread never waits on it).  Adds from one thread to one address apply in program order.
 __device__ __forceinline__ void red_add_f32(float* addr, float v) {
