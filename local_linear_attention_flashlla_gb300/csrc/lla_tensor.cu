@@ -227,13 +227,13 @@ __device__ __forceinline__ void load_dir8(const unsigned char* hi, const unsigne
     }
 }
 
-// CG update, first pass over one 16-coordinate chunk C of this thread's DH coordinates:
-//   cp = (C/omega) p_hat = Y ysc - kbar msc + lam_n p_hat   (kept for the second pass)
-// and the partial dot p_hat.cp (two fp32 partial sums).
-template <int C, int DH>
+// One 16-coordinate chunk C of this thread's DH coordinates of
+//   cp = (C/omega) p_hat = Y ysc - kbar msc + lam_n p_hat
+// (and, with DOT, the partial dot p_hat.cp as two fp32 partial sums).
+template <int C, int DH, bool DOT>
 __device__ __forceinline__ void cg_apply_chunk(uint32_t ty, const unsigned char* ptile, const unsigned char* plo, bool split,
                                                int row, int col, const float (&kv)[DH], float ysc, float msc, float lam_n,
-                                               float psc, float (&cp)[DH], uint64_t& pcp2) {
+                                               float psc, float (&cp)[16], uint64_t& pcp2) {
     float y[16], p0[8], p1[8];
     tmem_ld16(ty + C * 16, y);
     load_dir8(ptile, plo, split, row, col + C * 16, psc, p0);
@@ -245,8 +245,8 @@ __device__ __forceinline__ void cg_apply_chunk(uint32_t ty, const unsigned char*
         const uint64_t ph = j < 8 ? f2_pack(p0[j], p0[j + 1]) : f2_pack(p1[j - 8], p1[j - 7]);
         const uint64_t kb = f2_pack(kv[C * 16 + j], kv[C * 16 + j + 1]);
         const uint64_t c2 = f2_fma(f2_pack(y[j], y[j + 1]), ysc2, f2_fma(kb, nmsc2, f2_mul(ph, lam2)));
-        f2_unpack(c2, cp[C * 16 + j], cp[C * 16 + j + 1]);
-        pcp2 = f2_fma(ph, c2, pcp2);
+        f2_unpack(c2, cp[j], cp[j + 1]);
+        if (DOT) pcp2 = f2_fma(ph, c2, pcp2);
     }
 }
 
@@ -635,10 +635,11 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // bit; kbar.res is recomputed, not updated, because a converging residual cancels.
         float kbr = 0.f, kpx = 0.f;
         int cg_sweeps = 0;
-        // New direction p = res + beta p_old (PN: DH floats of scratch), stored in the direction
-        // tile as fp16 x 2^sp (hi, and lo when split_p); with XUPD also x += ALPHA p_old (the
-        // direction of the sweep just finished; the first sweep stores instead of adding).
-#define LLA_SET_DIRECTION(BETA, KEEP, XUPD, ALPHA, PN)                                                     \
+        // New direction p = res + beta p_old, stored in the direction tile as fp16 x 2^sp (hi, and
+        // lo when split_p): one pass for max |p| (which fixes sp), one to store.  With XUPD also
+        // x += ALPHA p_old, p_old being the direction of the sweep just finished (x is this
+        // thread's own data, written by it in the previous sweep; the first sweep only stores).
+#define LLA_SET_DIRECTION(BETA, KEEP, XUPD, ALPHA)                                                         \
         {                                                                                                  \
             const float osc_ = pow2i(-sp);                                                                 \
             const uint64_t b2_ = f2_pack((BETA), (BETA));                                                  \
@@ -647,28 +648,31 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 float po_[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};                                   \
                 if (KEEP) load_dir8(s.p, s.rlo, split_p, row, half * DH + e0, osc_, po_);                  \
                 _Pragma("unroll") for (int u = 0; u < 8; u += 2) {                                         \
+                    float n0_, n1_;                                                                        \
                     f2_unpack(f2_fma(b2_, f2_pack(po_[u], po_[u + 1]), f2_pack(res[e0 + u], res[e0 + u + 1])), \
-                              PN[e0 + u], PN[e0 + u + 1]);                                                 \
-                    mp_ = fmaxf(mp_, fmaxf(fabsf(PN[e0 + u]), fabsf(PN[e0 + u + 1])));                    \
+                              n0_, n1_);                                                                   \
+                    mp_ = fmaxf(mp_, fmaxf(fabsf(n0_), fabsf(n1_)));                                       \
                 }                                                                                          \
             }                                                                                              \
             mp_ = xch.max(mp_);                                                                            \
             const int sp_new_ = min(scale_exp(mp_), 100 - ek);   /* keeps 2^(sp+ek) finite */             \
-            const float nsc_ = pow2i(sp_new_);                                                             \
+            const uint64_t nsc2_ = f2_pack(pow2i(sp_new_), pow2i(sp_new_));                                \
             _Pragma("unroll") for (int e0 = 0; e0 < DH; e0 += 8) {                                         \
+                float po_[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};                                   \
+                if (KEEP) load_dir8(s.p, s.rlo, split_p, row, half * DH + e0, osc_, po_);                  \
                 if (XUPD) {                                                                                \
-                    float po_[8];                                                                          \
-                    load_dir8(s.p, s.rlo, split_p, row, half * DH + e0, osc_, po_);                        \
                     _Pragma("unroll") for (int u = 0; u < 8; ++u) {                                        \
-                        if (cg_sweeps == 1) xt[(e0 + u) * BQ] = (ALPHA) * po_[u];                          \
-                        else red_add_f32(xt + (e0 + u) * BQ, (ALPHA) * po_[u]);                            \
+                        const float xold_ = cg_sweeps > 1 ? xt[(e0 + u) * BQ] : 0.f;                       \
+                        xt[(e0 + u) * BQ] = fmaf((ALPHA), po_[u], xold_);                                  \
                     }                                                                                      \
                 }                                                                                          \
                 uint4 hk_, lk_;                                                                            \
                 uint32_t* hw_ = reinterpret_cast<uint32_t*>(&hk_);                                         \
                 uint32_t* lw_ = reinterpret_cast<uint32_t*>(&lk_);                                         \
                 _Pragma("unroll") for (int u = 0; u < 8; u += 2) {                                         \
-                    const float x0_ = PN[e0 + u] * nsc_, x1_ = PN[e0 + u + 1] * nsc_;                      \
+                    float x0_, x1_;                                                                        \
+                    f2_unpack(f2_mul(f2_fma(b2_, f2_pack(po_[u], po_[u + 1]),                              \
+                                            f2_pack(res[e0 + u], res[e0 + u + 1])), nsc2_), x0_, x1_);     \
                     hw_[u >> 1] = pack_half2(x0_, x1_);                                                    \
                     const float2 hf_ = __half22float2(*reinterpret_cast<const __half2*>(&hw_[u >> 1]));   \
                     lw_[u >> 1] = pack_half2(x0_ - hf_.x, x1_ - hf_.y);                                    \
@@ -715,8 +719,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             kbr = t.y;
             rn0 = sqrtf(gamma);
             active = row_ok && gamma > 0.f && !(sqrtf(gamma) <= prm.cg_tol * rn0);
-            float pn[DH];
-            LLA_SET_DIRECTION(0.f, false, false, 0.f, pn);
+            LLA_SET_DIRECTION(0.f, false, false, 0.f);
         }
 
         // ---------------- CG sweeps ----------------
@@ -763,29 +766,46 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const float msc = msum * pow2i(-sM) * inv_om;
             const float psc = pow2i(-sp);
             const uint32_t ty = tY + lane_off + half * DH;
-            float cp[DH];
             uint64_t pcp2 = 0;
-            cg_apply_chunk<0, DH>(ty, s.p, s.rlo, split_p, row, half * DH, kv, ysc, msc, lam_n, psc, cp, pcp2);
-            cg_apply_chunk<1, DH>(ty, s.p, s.rlo, split_p, row, half * DH, kv, ysc, msc, lam_n, psc, cp, pcp2);
-            if constexpr (DH > 32) {
-                cg_apply_chunk<2, DH>(ty, s.p, s.rlo, split_p, row, half * DH, kv, ysc, msc, lam_n, psc, cp, pcp2);
-                cg_apply_chunk<3, DH>(ty, s.p, s.rlo, split_p, row, half * DH, kv, ysc, msc, lam_n, psc, cp, pcp2);
+#define LLA_CG_CHUNK(C, DOT)                                                                               \
+            cg_apply_chunk<C, DH, DOT>(ty, s.p, s.rlo, split_p, row, half * DH, kv, ysc, msc, lam_n, psc, cp, pcp2)
+            {
+                float cp[16];
+                LLA_CG_CHUNK(0, true);
+                LLA_CG_CHUNK(1, true);
+                if constexpr (DH > 32) {
+                    LLA_CG_CHUNK(2, true);
+                    LLA_CG_CHUNK(3, true);
+                }
             }
             const float pcp = xch.sum(f2_total(pcp2));
             const bool upd = active && pcp > 0.f;
             const float alpha = upd ? gamma / pcp : 0.f;
+            // second pass: Cp again (cheaper than holding it), res -= alpha Cp, res.res, kbar.res
             uint64_t g22 = 0, kr2 = 0;
             {
                 const uint64_t na2 = f2_pack(-alpha, -alpha);
-#pragma unroll
-                for (int e = 0; e < DH; e += 2) {
-                    uint64_t r2 = f2_pack(res[e], res[e + 1]);
-                    if (upd) r2 = f2_fma(na2, f2_pack(cp[e], cp[e + 1]), r2);
-                    f2_unpack(r2, res[e], res[e + 1]);
-                    g22 = f2_fma(r2, r2, g22);
-                    kr2 = f2_fma(f2_pack(kv[e], kv[e + 1]), r2, kr2);
+#define LLA_CG_STEP(C)                                                                                     \
+                {                                                                                          \
+                    float cp[16];                                                                          \
+                    LLA_CG_CHUNK(C, false);                                                                \
+                    _Pragma("unroll") for (int j = 0; j < 16; j += 2) {                                    \
+                        uint64_t r2 = f2_pack(res[(C) * 16 + j], res[(C) * 16 + j + 1]);                   \
+                        if (upd) r2 = f2_fma(na2, f2_pack(cp[j], cp[j + 1]), r2);                          \
+                        f2_unpack(r2, res[(C) * 16 + j], res[(C) * 16 + j + 1]);                           \
+                        g22 = f2_fma(r2, r2, g22);                                                         \
+                        kr2 = f2_fma(f2_pack(kv[(C) * 16 + j], kv[(C) * 16 + j + 1]), r2, kr2);            \
+                    }                                                                                      \
                 }
+                LLA_CG_STEP(0);
+                LLA_CG_STEP(1);
+                if constexpr (DH > 32) {
+                    LLA_CG_STEP(2);
+                    LLA_CG_STEP(3);
+                }
+#undef LLA_CG_STEP
             }
+#undef LLA_CG_CHUNK
             const float2 gk = xch.sum2(f2_total(g22), f2_total(kr2));   // res.res, kbar.res
             const float g2 = gk.x;
             float beta = 0.f;
@@ -804,7 +824,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 beta = 0.f;
                 kbr = 0.f;
             }
-            LLA_SET_DIRECTION(beta, true, true, alpha, cp);      // cp's storage holds the new direction
+            LLA_SET_DIRECTION(beta, true, true, alpha);
         }
 
         // ---------------- finalise rho, denom; R = rho' (hi + lo) for the output sweep ----------------

@@ -237,12 +237,6 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Fire-and-forget fp32 add to global memory, performed at L2 (no value comes back, so the
-// issuing thread never waits on it).  Adds from one thread to one address apply in program order.
-__device__ __forceinline__ void red_add_f32(float* addr, float v) {
-    asm volatile("red.relaxed.gpu.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
-}
-
 // Packed fp32 pairs (sm_100+ f32x2 arithmetic: one instruction for two IEEE fp32 operations,
 // each rounded to nearest even exactly as its scalar form).  Halves the issue slots of
 // elementwise loops, which share a sub-partition's scheduler with the MMA-issuing warp.
