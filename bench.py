@@ -204,6 +204,8 @@ def parse():
     ap.add_argument("--path", choices=["auto", "tensor", "fp32"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch B (a smaller case for profiler captures)")
     return ap.parse_args()
 
 
@@ -225,7 +227,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return
     from local_linear_attention_flashlla_gb300.inputs import make_inputs, workload
-    w = workload(args.workload)
+    w = workload(args.workload) if args.batch is None else workload(args.workload, B=args.batch)
     qkv = make_inputs(w)
     steps = []
     cb = None
@@ -263,7 +265,7 @@ def main():
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    w = workload(args.workload)
+    w = workload(args.workload) if args.batch is None else workload(args.workload, B=args.batch)
     path = {"auto": lla.LLA_PATH_AUTO, "tensor": lla.LLA_PATH_TENSOR, "fp32": lla.LLA_PATH_FP32}[args.path]
     dtype_code = lla.LLA_DTYPE_BF16 if w.dtype == "bf16" else lla.LLA_DTYPE_FP32
     rpath = lla.lla_resolve_path(dtype_code, path, w.d)

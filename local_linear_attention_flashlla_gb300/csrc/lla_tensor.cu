@@ -22,8 +22,9 @@
 // (Eqs. (6)-(8) with Sigma_i = C_i + omega_i delta_i delta_i^T, Sherman-Morrison).
 //
 // Roles (384 threads, three warpgroups): warp 0 lane 0 issues TMA (Q once, then K/V blocks
-// into a 3-slot ring); warp 1 lane 0 issues the S and A'/T products, warp 2 lane 0 the Y
-// products (two issue streams, synchronised through mbarriers; warp 3 idle);
+// into a 3-slot ring); lane 0 of warps 1, 3 and 2 issues the S, the A'/T and the Y products
+// (three issue streams, synchronised through mbarriers: each MMA-issuing warp shares its
+// sub-partition's scheduler with two elementwise warps, so one stream per warp keeps up);
 // warpgroups 1-2 (256 threads) do the elementwise work and the CG vector updates, thread =
 // (query row, half of the key block / half of the head dimension).  setmaxnreg moves
 // registers from warpgroup 0 (72 each) to the elementwise warpgroups (216 each):
@@ -136,7 +137,7 @@ struct TcSmem {
     unsigned char rlo[TILE];                           // R_lo (output sweep); P_lo (CG sweeps of tile 0)
     unsigned char slot[NSLOT][TILE];                   // K / V blocks (TMA)
     uint64_t slot_full[NSLOT], slot_empty[NSLOT];
-    uint64_t q_full, s_full[2], ew_done[2], m_free[2], a_free, y_done, p_ready, final_sa, final_y;
+    uint64_t q_full, s_full[2], ew_done[2], m_free[2], a_free, y_done, p_ready, final_s, final_a, final_y;
     float2 xch[2][2][BQ];                              // row-scalar exchange between the two halves
     uint32_t tmem_base;
     int err;
@@ -343,14 +344,15 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
         mbar_init(&s.q_full, 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&s.s_full[i], 1);
+            mbar_init(&s.s_full[i], 2);             // the S product and the A'/T product
             mbar_init(&s.ew_done[i], NEW / 32);       // one arrive per elementwise warp
         }
         mbar_init(&s.a_free, NEW / 32);
         for (int i = 0; i < 2; ++i) mbar_init(&s.m_free[i], 1);
         mbar_init(&s.y_done, 1);
         mbar_init(&s.p_ready, 1);                   // one arrive after the elementwise threads' barrier
-        mbar_init(&s.final_sa, 1);
+        mbar_init(&s.final_s, 1);
+        mbar_init(&s.final_a, 1);
         mbar_init(&s.final_y, 1);
         mbar_fence_init();
     }
@@ -408,11 +410,48 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             mbar_drain(&s.q_full, 0);
         }
     } else if (warp == 1) {
-        // ========================= MMA issuer 1: S = Q K^T and A' / T =========================
+        // ============================ MMA issuer 1: S = Q K^T ============================
         if (lane == 0) {
-            const uint32_t q_addr = smem_u32(s.q), p_addr = smem_u32(s.p), rlo_addr = smem_u32(s.rlo);
-            uint32_t fill = 0, pr = 0, g = 0, ga = 0;
+            const uint32_t q_addr = smem_u32(s.q);
+            uint32_t fill = 0, pr = 0, g = 0;
             bool ok = WAIT(&s.q_full, 0, err);
+            int cg_sweeps = 0;
+            for (int sweep = 0; ok; ++sweep) {
+                int type;
+                if (sweep == 0) type = SW_MAX;
+                else if (sweep == 1) type = SW_MOMENT;
+                else if (!dynamic) type = cg_sweeps < prm.cg_max_iters ? SW_CG : SW_OUT;
+                else {
+                    if (!(ok = WAIT(&s.p_ready, pr & 1, err))) break;
+                    ++pr;
+                    type = s.next_type;
+                }
+                if (type == SW_CG) ++cg_sweeps;
+                for (int kb = 0; kb < nkb; ++kb, ++g) {
+                    const uint32_t fk = fill++;
+                    if (type == SW_OUT) ++fill;           // the V block of this key block
+                    const int sk = fk % NSLOT;
+                    const uint32_t b = g & 1;
+                    if (!(ok = WAIT(&s.slot_full[sk], (fk / NSLOT) & 1, err))) break;
+                    // S buffer b was last used by block g - 2: its coefficients must have been read
+                    if (g >= 2 && !(ok = WAIT(&s.m_free[b], ((g - 2) >> 1) & 1, err))) break;
+                    tc_fence_after();
+                    gemm_qk<D, false>(tS0 + b * 128, q_addr, smem_u32(s.slot[sk]));
+                    umma_commit(&s.s_full[b]);
+                    if (type == SW_MAX || type == SW_MOMENT) umma_commit(&s.s_full[b]);   // no A' product
+                    if (type == SW_MAX) umma_commit(&s.slot_empty[sk]);   // read by S alone
+                }
+                if (type == SW_OUT) break;
+            }
+            umma_commit(&s.final_s);
+            mbar_drain(&s.final_s, 0);
+        }
+    } else if (warp == 3) {
+        // ================= MMA issuer 3: A' = P K^T (CG) or T = R K^T (output) =================
+        if (lane == 0) {
+            const uint32_t p_addr = smem_u32(s.p), rlo_addr = smem_u32(s.rlo);
+            uint32_t fill = 0, pr = 0, g = 0, ga = 0;
+            bool ok = true;
             int cg_sweeps = 0;
             for (int sweep = 0; ok; ++sweep) {
                 int type;
@@ -427,46 +466,39 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     type = s.next_type;
                 }
                 if (type == SW_CG) ++cg_sweeps;
-                const bool two = type == SW_CG || type == SW_OUT;
+                if (type == SW_MAX || type == SW_MOMENT) {   // no product of this issuer
+                    fill += nkb;
+                    g += nkb;
+                    continue;
+                }
                 for (int kb = 0; kb < nkb; ++kb, ++g) {
                     const uint32_t fk = fill++;
-                    if (type == SW_OUT) ++fill;           // the V block of this key block
+                    if (type == SW_OUT) ++fill;
                     const int sk = fk % NSLOT;
-                    const uint32_t b = g & 1;
                     if (!(ok = WAIT(&s.slot_full[sk], (fk / NSLOT) & 1, err))) break;
-                    // S buffer b was last used by block g - 2: its coefficients must have been read
-                    if (g >= 2 && !(ok = WAIT(&s.m_free[b], ((g - 2) >> 1) & 1, err))) break;
+                    if (!have_p) {
+                        if (!(ok = WAIT(&s.p_ready, pr & 1, err))) break;
+                        ++pr;
+                        have_p = true;
+                    }
+                    // A' is single-buffered: the elementwise threads release it as soon as they
+                    // have copied the previous block's A' into registers
+                    if (ga >= 1 && !(ok = WAIT(&s.a_free, (ga - 1) & 1, err))) break;
+                    ++ga;
                     tc_fence_after();
                     const uint32_t k_addr = smem_u32(s.slot[sk]);
-                    gemm_qk<D, false>(tS0 + b * 128, q_addr, k_addr);
-                    if (two) {
-                        if (!have_p) {
-                            if (!(ok = WAIT(&s.p_ready, pr & 1, err))) break;
-                            ++pr;
-                            have_p = true;
-                        }
-                        // A' is single-buffered: the elementwise threads release it as soon as they
-                        // have copied the previous block's A' into registers
-                        if (ga >= 1 && !(ok = WAIT(&s.a_free, (ga - 1) & 1, err))) break;
-                        ++ga;
-                        tc_fence_after();
-                        gemm_qk<D, false>(tA, p_addr, k_addr);
-                        // T = (R_hi + R_lo) K^T; in the first tile also A' = (P_hi + P_lo) K^T
-                        if (type == SW_OUT || tile == 0) gemm_qk<D, true>(tA, rlo_addr, k_addr);
-                    }
-                    umma_commit(&s.s_full[b]);
-                    // a K block read only by this issuer is free once these products complete
-                    if (type == SW_MAX || type == SW_OUT) umma_commit(&s.slot_empty[sk]);
+                    gemm_qk<D, false>(tA, p_addr, k_addr);
+                    // T = (R_hi + R_lo) K^T; in the first tile also A' = (P_hi + P_lo) K^T
+                    if (type == SW_OUT || tile == 0) gemm_qk<D, true>(tA, rlo_addr, k_addr);
+                    umma_commit(&s.s_full[g & 1]);
                 }
                 if (type == SW_OUT) break;
             }
-            umma_commit(&s.final_sa);
-            mbar_drain(&s.final_sa, 0);
+            umma_commit(&s.final_a);
+            mbar_drain(&s.final_a, 0);
         }
     } else if (warp == 2) {
         // ============== MMA issuer 2: Y += M K (moments, CG) or U V (output) ==============
-        // A separate warp, so that its issue stream and the first issuer's overlap: each MMA
-        // warp shares its sub-partition's scheduler with two elementwise warps.
         if (lane == 0) {
             uint32_t fill = 0, pr = 0, g = 0;
             bool ok = WAIT(&s.q_full, 0, err);
@@ -494,6 +526,9 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         const uint32_t src = smem_u32(s.slot[(type == SW_OUT ? fv : fk) % NSLOT]);
                         gemm_y<D>(ty_acc, tS0 + b * 128, src, kb > 0);
                         umma_commit(&s.slot_empty[(type == SW_OUT ? fv : fk) % NSLOT]);
+                        // the output sweep's K block: S and T completed before the elementwise
+                        // warps could finish this block
+                        if (type == SW_OUT) umma_commit(&s.slot_empty[fk % NSLOT]);
                         if (kb == nkb - 1) umma_commit(&s.y_done);
                     }
                     umma_commit(&s.m_free[b]);
