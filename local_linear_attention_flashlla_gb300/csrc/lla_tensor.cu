@@ -671,27 +671,15 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         float kbr = 0.f, kpx = 0.f;
         int cg_sweeps = 0;
         // New direction p = res + beta p_old, stored in the direction tile as fp16 x 2^sp (hi, and
-        // lo when split_p): one pass for max |p| (which fixes sp), one to store.  With XUPD also
-        // x += ALPHA p_old, p_old being the direction of the sweep just finished (x is this
-        // thread's own data, written by it in the previous sweep; the first sweep only stores).
-#define LLA_SET_DIRECTION(BETA, KEEP, XUPD, ALPHA)                                                         \
+        // lo when split_p).  First pass: p into PN (DH floats of registers) and max |p|, which
+        // fixes sp; with XUPD it also applies x += ALPHA p_old, p_old being the direction of the
+        // sweep just finished (x is this thread's own scratch; the first sweep only stores).
+        // Second pass: pack and store.
+#define LLA_SET_DIRECTION(BETA, KEEP, XUPD, ALPHA, PN)                                                     \
         {                                                                                                  \
             const float osc_ = pow2i(-sp);                                                                 \
             const uint64_t b2_ = f2_pack((BETA), (BETA));                                                  \
             float mp_ = 0.f;                                                                               \
-            _Pragma("unroll") for (int e0 = 0; e0 < DH; e0 += 8) {                                         \
-                float po_[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};                                   \
-                if (KEEP) load_dir8(s.p, s.rlo, split_p, row, half * DH + e0, osc_, po_);                  \
-                _Pragma("unroll") for (int u = 0; u < 8; u += 2) {                                         \
-                    float n0_, n1_;                                                                        \
-                    f2_unpack(f2_fma(b2_, f2_pack(po_[u], po_[u + 1]), f2_pack(res[e0 + u], res[e0 + u + 1])), \
-                              n0_, n1_);                                                                   \
-                    mp_ = fmaxf(mp_, fmaxf(fabsf(n0_), fabsf(n1_)));                                       \
-                }                                                                                          \
-            }                                                                                              \
-            mp_ = xch.max(mp_);                                                                            \
-            const int sp_new_ = min(scale_exp(mp_), 100 - ek);   /* keeps 2^(sp+ek) finite */             \
-            const uint64_t nsc2_ = f2_pack(pow2i(sp_new_), pow2i(sp_new_));                                \
             _Pragma("unroll") for (int e0 = 0; e0 < DH; e0 += 8) {                                         \
                 float po_[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};                                   \
                 if (KEEP) load_dir8(s.p, s.rlo, split_p, row, half * DH + e0, osc_, po_);                  \
@@ -701,13 +689,22 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         xt[(e0 + u) * BQ] = fmaf((ALPHA), po_[u], xold_);                                  \
                     }                                                                                      \
                 }                                                                                          \
+                _Pragma("unroll") for (int u = 0; u < 8; u += 2) {                                         \
+                    f2_unpack(f2_fma(b2_, f2_pack(po_[u], po_[u + 1]), f2_pack(res[e0 + u], res[e0 + u + 1])), \
+                              PN[e0 + u], PN[e0 + u + 1]);                                                 \
+                    mp_ = fmaxf(mp_, fmaxf(fabsf(PN[e0 + u]), fabsf(PN[e0 + u + 1])));                    \
+                }                                                                                          \
+            }                                                                                              \
+            mp_ = xch.max(mp_);                                                                            \
+            const int sp_new_ = min(scale_exp(mp_), 100 - ek);   /* keeps 2^(sp+ek) finite */             \
+            const uint64_t nsc2_ = f2_pack(pow2i(sp_new_), pow2i(sp_new_));                                \
+            _Pragma("unroll") for (int e0 = 0; e0 < DH; e0 += 8) {                                         \
                 uint4 hk_, lk_;                                                                            \
                 uint32_t* hw_ = reinterpret_cast<uint32_t*>(&hk_);                                         \
                 uint32_t* lw_ = reinterpret_cast<uint32_t*>(&lk_);                                         \
                 _Pragma("unroll") for (int u = 0; u < 8; u += 2) {                                         \
                     float x0_, x1_;                                                                        \
-                    f2_unpack(f2_mul(f2_fma(b2_, f2_pack(po_[u], po_[u + 1]),                              \
-                                            f2_pack(res[e0 + u], res[e0 + u + 1])), nsc2_), x0_, x1_);     \
+                    f2_unpack(f2_mul(f2_pack(PN[e0 + u], PN[e0 + u + 1]), nsc2_), x0_, x1_);               \
                     hw_[u >> 1] = pack_half2(x0_, x1_);                                                    \
                     const float2 hf_ = __half22float2(*reinterpret_cast<const __half2*>(&hw_[u >> 1]));   \
                     lw_[u >> 1] = pack_half2(x0_ - hf_.x, x1_ - hf_.y);                                    \
@@ -754,7 +751,8 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             kbr = t.y;
             rn0 = sqrtf(gamma);
             active = row_ok && gamma > 0.f && !(sqrtf(gamma) <= prm.cg_tol * rn0);
-            LLA_SET_DIRECTION(0.f, false, false, 0.f);
+            float pn[DH];
+            LLA_SET_DIRECTION(0.f, false, false, 0.f, pn);
         }
 
         // ---------------- CG sweeps ----------------
@@ -801,32 +799,40 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const float msc = msum * pow2i(-sM) * inv_om;
             const float psc = pow2i(-sp);
             const uint32_t ty = tY + lane_off + half * DH;
+            // first pass: Cp and p.Cp; Cp goes to the A' columns of TMEM, idle until the next
+            // sweep's first A' product (which waits for this update's direction)
+            const uint32_t tcp = tA + lane_off + half * 64;
             uint64_t pcp2 = 0;
-#define LLA_CG_CHUNK(C, DOT)                                                                               \
-            cg_apply_chunk<C, DH, DOT>(ty, s.p, s.rlo, split_p, row, half * DH, kv, ysc, msc, lam_n, psc, cp, pcp2)
-            {
-                float cp[16];
-                LLA_CG_CHUNK(0, true);
-                LLA_CG_CHUNK(1, true);
-                if constexpr (DH > 32) {
-                    LLA_CG_CHUNK(2, true);
-                    LLA_CG_CHUNK(3, true);
-                }
+#define LLA_CG_CHUNK(C)                                                                                    \
+            if constexpr ((C) * 16 < DH) {                                                                 \
+                float cp_[16];                                                                             \
+                uint32_t cb_[16];                                                                          \
+                cg_apply_chunk<C, DH, true>(ty, s.p, s.rlo, split_p, row, half * DH, kv, ysc, msc, lam_n,   \
+                                            psc, cp_, pcp2);                                               \
+                _Pragma("unroll") for (int j = 0; j < 16; ++j) cb_[j] = __float_as_uint(cp_[j]);          \
+                tmem_st16(tcp + (C) * 16, cb_);                                                            \
             }
+            LLA_CG_CHUNK(0);
+            LLA_CG_CHUNK(1);
+            LLA_CG_CHUNK(2);
+            LLA_CG_CHUNK(3);
+#undef LLA_CG_CHUNK
+            tmem_st_wait();
             const float pcp = xch.sum(f2_total(pcp2));
             const bool upd = active && pcp > 0.f;
             const float alpha = upd ? gamma / pcp : 0.f;
-            // second pass: Cp again (cheaper than holding it), res -= alpha Cp, res.res, kbar.res
+            // second pass: res -= alpha Cp, res.res, kbar.res
             uint64_t g22 = 0, kr2 = 0;
             {
                 const uint64_t na2 = f2_pack(-alpha, -alpha);
 #define LLA_CG_STEP(C)                                                                                     \
-                {                                                                                          \
-                    float cp[16];                                                                          \
-                    LLA_CG_CHUNK(C, false);                                                                \
+                if constexpr ((C) * 16 < DH) {                                                             \
+                    float cp_[16];                                                                         \
+                    tmem_ld16(tcp + (C) * 16, cp_);                                                        \
+                    tmem_ld_wait();                                                                        \
                     _Pragma("unroll") for (int j = 0; j < 16; j += 2) {                                    \
                         uint64_t r2 = f2_pack(res[(C) * 16 + j], res[(C) * 16 + j + 1]);                   \
-                        if (upd) r2 = f2_fma(na2, f2_pack(cp[j], cp[j + 1]), r2);                          \
+                        if (upd) r2 = f2_fma(na2, f2_pack(cp_[j], cp_[j + 1]), r2);                        \
                         f2_unpack(r2, res[(C) * 16 + j], res[(C) * 16 + j + 1]);                           \
                         g22 = f2_fma(r2, r2, g22);                                                         \
                         kr2 = f2_fma(f2_pack(kv[(C) * 16 + j], kv[(C) * 16 + j + 1]), r2, kr2);            \
@@ -834,13 +840,10 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
                 LLA_CG_STEP(0);
                 LLA_CG_STEP(1);
-                if constexpr (DH > 32) {
-                    LLA_CG_STEP(2);
-                    LLA_CG_STEP(3);
-                }
+                LLA_CG_STEP(2);
+                LLA_CG_STEP(3);
 #undef LLA_CG_STEP
             }
-#undef LLA_CG_CHUNK
             const float2 gk = xch.sum2(f2_total(g22), f2_total(kr2));   // res.res, kbar.res
             const float g2 = gk.x;
             float beta = 0.f;
@@ -859,7 +862,8 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 beta = 0.f;
                 kbr = 0.f;
             }
-            LLA_SET_DIRECTION(beta, true, true, alpha);
+            float pn[DH];
+            LLA_SET_DIRECTION(beta, true, true, alpha, pn);
         }
 
         // ---------------- finalise rho, denom; R = rho' (hi + lo) for the output sweep ----------------
