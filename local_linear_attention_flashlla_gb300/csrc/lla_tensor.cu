@@ -672,10 +672,9 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         int cg_sweeps = 0;
         // New direction p = res + beta p_old, stored in the direction tile as fp16 x 2^sp (hi, and
         // lo when split_p).  First pass: p into PN (DH floats of registers) and max |p|, which
-        // fixes sp; with XUPD it also applies x += ALPHA p_old, p_old being the direction of the
-        // sweep just finished (x is this thread's own scratch; the first sweep only stores).
-        // Second pass: pack and store.
-#define LLA_SET_DIRECTION(BETA, KEEP, XUPD, ALPHA, PN)                                                     \
+        // fixes sp; with XUPD it also stores x = XO + ALPHA p_old, p_old being the direction of
+        // the sweep just finished and XO (DH floats) the previous x.  Second pass: pack and store.
+#define LLA_SET_DIRECTION(BETA, KEEP, XUPD, ALPHA, PN, XO)                                                 \
         {                                                                                                  \
             const float osc_ = pow2i(-sp);                                                                 \
             const uint64_t b2_ = f2_pack((BETA), (BETA));                                                  \
@@ -684,10 +683,8 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 float po_[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};                                   \
                 if (KEEP) load_dir8(s.p, s.rlo, split_p, row, half * DH + e0, osc_, po_);                  \
                 if (XUPD) {                                                                                \
-                    _Pragma("unroll") for (int u = 0; u < 8; ++u) {                                        \
-                        const float xold_ = cg_sweeps > 1 ? xt[(e0 + u) * BQ] : 0.f;                       \
-                        xt[(e0 + u) * BQ] = fmaf((ALPHA), po_[u], xold_);                                  \
-                    }                                                                                      \
+                    _Pragma("unroll") for (int u = 0; u < 8; ++u)                                          \
+                        xt[(e0 + u) * BQ] = fmaf((ALPHA), po_[u], XO[e0 + u]);                             \
                 }                                                                                          \
                 _Pragma("unroll") for (int u = 0; u < 8; u += 2) {                                         \
                     f2_unpack(f2_fma(b2_, f2_pack(po_[u], po_[u + 1]), f2_pack(res[e0 + u], res[e0 + u + 1])), \
@@ -752,7 +749,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             rn0 = sqrtf(gamma);
             active = row_ok && gamma > 0.f && !(sqrtf(gamma) <= prm.cg_tol * rn0);
             float pn[DH];
-            LLA_SET_DIRECTION(0.f, false, false, 0.f, pn);
+            LLA_SET_DIRECTION(0.f, false, false, 0.f, pn, pn);
         }
 
         // ---------------- CG sweeps ----------------
@@ -844,6 +841,10 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 LLA_CG_STEP(3);
 #undef LLA_CG_STEP
             }
+            // the previous x (this thread's own scratch), loaded while the exchange below waits
+            float xo[DH];
+#pragma unroll
+            for (int e = 0; e < DH; ++e) xo[e] = cg_sweeps > 1 ? xt[e * BQ] : 0.f;
             const float2 gk = xch.sum2(f2_total(g22), f2_total(kr2));   // res.res, kbar.res
             const float g2 = gk.x;
             float beta = 0.f;
@@ -863,7 +864,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 kbr = 0.f;
             }
             float pn[DH];
-            LLA_SET_DIRECTION(beta, true, true, alpha, pn);
+            LLA_SET_DIRECTION(beta, true, true, alpha, pn, xo);
         }
 
         // ---------------- finalise rho, denom; R = rho' (hi + lo) for the output sweep ----------------
