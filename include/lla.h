@@ -94,7 +94,9 @@ int lla_resolve_path(int dtype, int path, int d);
 
 /*
  * lla_sync_status -- synchronise `stream`, then report and clear the library's device error
- * word (set when a bounded wait inside a kernel gave up: LLA_ERR_DEVICE_TIMEOUT).
+ * word: set when a bounded wait inside a kernel gave up (LLA_ERR_DEVICE_TIMEOUT), or when the
+ * tensor kernel found its dynamic shared memory not 1024-byte aligned and did no work
+ * (LLA_ERR_CUDA).
  */
 int lla_sync_status(void* stream);
 

@@ -188,6 +188,9 @@ int lla_sync_status(void* stream) {
     unsigned word = 0;
     cudaError_t e = lla::read_and_clear_device_error(&word, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return lla::cuda_fail(e, "lla_sync_status");
+    if (word & lla::kDevErrSmemAlign)
+        return fail(LLA_ERR_CUDA, "tensor kernel: dynamic shared memory not 1024-byte aligned, no work done (error word 0x%x)",
+                    word);
     if (word & lla::kDevErrMbarTimeout)
         return fail(LLA_ERR_DEVICE_TIMEOUT, "a bounded device-side wait gave up (error word 0x%x)", word);
     return LLA_OK;

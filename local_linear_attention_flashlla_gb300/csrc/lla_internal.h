@@ -25,8 +25,9 @@ struct Problem {
     cudaEvent_t ev_main_end;     // (null otherwise)
 };
 
-// Device error word: bit flags set by kernels whose bounded waits gave up.
-enum DeviceError : unsigned { kDevErrMbarTimeout = 1u };
+// Device error word: bit flags set by kernels that gave up (a bounded wait ran out, or the
+// tensor kernel found its dynamic shared memory misaligned and did no work).
+enum DeviceError : unsigned { kDevErrMbarTimeout = 1u, kDevErrSmemAlign = 2u };
 
 // fp32 CUDA-core path (any d in {16,32,64,128}, fp32 or bf16 inputs).
 cudaError_t launch_simt(const Problem& p, cudaStream_t stream);

@@ -134,15 +134,21 @@ struct TcSmem {
     static constexpr int TILE = BQ * D * 2;            // bytes of a [128 x D] fp16 tile
     unsigned char q[TILE];                             // queries (TMA)
     unsigned char p[TILE];                             // CG direction P, then R_hi (rho', threads)
-    unsigned char rlo[TILE];                           // R_lo (output sweep); P_lo (CG sweeps of tile 0)
+    // R_lo (output sweep); P_lo (CG sweeps of tile 0); in the CG sweeps of the other tiles, the
+    // fp32 CG iterate x of coordinates 0 .. D/2-1 as [coordinate][row]
+    unsigned char rlo[TILE];
+    unsigned char xb[TILE];                            // x of coordinates D/2 .. D-1 (tiles > 0)
     unsigned char slot[NSLOT][TILE];                   // K / V blocks (TMA)
     uint64_t slot_full[NSLOT], slot_empty[NSLOT];
     uint64_t q_full, s_full[2], ew_done[2], m_free[2], a_free, y_done, p_ready, final_s, final_a, final_y;
-    float2 xch[2][2][BQ];                              // row-scalar exchange between the two halves
+    float xch[2][2][BQ];                               // row-scalar exchange between the two halves
     uint32_t tmem_base;
     int err;
     int next_type;
 };
+
+// 227 KB: the most dynamic shared memory a block may have on sm_103a
+static_assert(sizeof(TcSmem<128>) <= 232448 && sizeof(TcSmem<64>) <= 232448, "shared memory layout too large");
 
 struct TcParams {
     Header* hdr;
@@ -162,21 +168,17 @@ struct TcParams {
 // turn suffice: a thread writes a buffer again only after the next exchange's barrier, which its
 // partner reaches only after reading that buffer.
 struct Xch {
-    float2 (*buf)[2][BQ];
+    float (*buf)[2][BQ];
     int idx, half, row;
-    __device__ float2 swap(float2 v) {
-        float2* b = &buf[idx][0][0];
+    __device__ float swap(float v) {
+        float* b = &buf[idx][0][0];
         idx ^= 1;
         b[half * BQ + row] = v;
         named_bar_sync(EW_BAR, NEW);
         return b[(1 - half) * BQ + row];
     }
-    __device__ float sum(float v) { return v + swap(make_float2(v, 0.f)).x; }
-    __device__ float2 sum2(float a, float c) {
-        const float2 o = swap(make_float2(a, c));
-        return make_float2(a + o.x, c + o.y);
-    }
-    __device__ float max(float v) { return fmaxf(v, swap(make_float2(v, 0.f)).x); }
+    __device__ float sum(float v) { return v + swap(v); }
+    __device__ float max(float v) { return fmaxf(v, swap(v)); }
 };
 
 __device__ __forceinline__ bool ew_any(bool pred) {
@@ -322,8 +324,15 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     constexpr int NB = S::NB;
     constexpr int DH = D / 2;                       // head-dim coordinates per elementwise thread
 
-    extern __shared__ unsigned char smem_raw[];
-    S& s = *reinterpret_cast<S*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // The swizzled tiles need 1024-byte alignment.  Dynamic shared memory begins 1024-aligned
+    // (right after the block's reserved kilobyte), so no padding is requested; a launch where it
+    // does not is refused here, by every thread alike, before anything is touched.
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    if (smem_u32(smem_raw) & 1023u) {
+        if (threadIdx.x == 0) atomicOr(prm.dev_err, (unsigned)kDevErrSmemAlign);
+        return;
+    }
+    S& s = *reinterpret_cast<S*>(smem_raw);
     volatile int* err = &s.err;
     volatile int* abort_flag = &prm.hdr->abort;
 #define WAIT(bar, par, e) mbar_wait_abortable(bar, par, e, abort_flag)
@@ -555,7 +564,11 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const size_t row_g = ((size_t)head * n + (row_ok ? i : 0)) * D + half * DH;
         // tile-transposed fp32 scratch: coordinate e of this thread's row at [e * BQ] (coalesced)
         const size_t tbase = ((size_t)(head * prm.n_tiles + tile) * D + half * DH) * BQ + row;
-        float* xt = prm.xs + tbase;             // CG iterate x = rho'
+        // CG iterate x = rho': shared memory ([coordinate][row], rlo for the first half of the
+        // coordinates and xb for the second), except in the first tile, whose rlo holds P_lo
+        // and whose x uses the global scratch (same layout)
+        float* xt = split_p ? prm.xs + tbase
+                            : reinterpret_cast<float*>(half == 0 ? s.rlo : s.xb) + row;
         float* kbt = prm.kbar + tbase;          // kbar
         Xch xch{s.xch, 0, half, row};
 
@@ -743,9 +756,8 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 gp = fmaf(res[e], res[e], gp);
                 kr = fmaf(kv[e], res[e], kr);
             }
-            const float2 t = xch.sum2(gp, kr);
-            gamma = t.x;
-            kbr = t.y;
+            gamma = xch.sum(gp);
+            kbr = xch.sum(kr);
             rn0 = sqrtf(gamma);
             active = row_ok && gamma > 0.f && !(sqrtf(gamma) <= prm.cg_tol * rn0);
             float pn[DH];
@@ -845,14 +857,14 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             float xo[DH];
 #pragma unroll
             for (int e = 0; e < DH; ++e) xo[e] = cg_sweeps > 1 ? xt[e * BQ] : 0.f;
-            const float2 gk = xch.sum2(f2_total(g22), f2_total(kr2));   // res.res, kbar.res
-            const float g2 = gk.x;
+            const float g2 = xch.sum(f2_total(g22));       // res.res
+            const float kbr_new = xch.sum(f2_total(kr2));  // kbar.res
             float beta = 0.f;
             if (upd) {
                 beta = g2 / gamma;
                 gamma = g2;
                 ++iters;
-                kbr = gk.y;
+                kbr = kbr_new;
                 if (gamma == 0.f || sqrtf(gamma) <= prm.cg_tol * rn0) active = false;
             } else {
                 active = false;
@@ -873,7 +885,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const bool have_x = row_ok && cg_sweeps > 0;   // no sweep ran: x = 0
 #pragma unroll
         for (int e = 0; e < DH; ++e) {
-            xv[e] = have_x ? __ldcg(xt + e * BQ) : 0.f;
+            xv[e] = have_x ? xt[e * BQ] : 0.f;
             kv[e] = kbt[e * BQ];
         }
         float dx = 0.f, mxx = 0.f;
@@ -1041,7 +1053,7 @@ cudaError_t launch_d(const Problem& p, void* ws, cudaStream_t stream, const char
     prm.cg_max_iters = p.cg_max_iters;
     if (!prm.dev_err) { *why = "device error word"; return cudaErrorInvalidSymbol; }
 
-    const size_t smem = sizeof(TcSmem<D>) + 1024;
+    const size_t smem = sizeof(TcSmem<D>);
     auto kern = lla_tc_kernel<D>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) { *why = "tensor kernel shared-memory attribute"; return e; }
