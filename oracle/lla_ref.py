@@ -37,6 +37,14 @@ It is the plain definition written out, one query at a time, in float64:
 * ``softmax_ref`` is the Nadaraya-Watson / softmax local-constant estimate with the
   same weights (reading notes section 1, Eq. (4); kernel-methods blog chapter 1),
   the lambda -> infinity limit stated in section 2.1 (Sec. 2.3 of the paper).
+* ``parallax_row`` / ``parallax_ref`` is the Parallax page's form with a caller-supplied
+  probe rho (the page's learned projection W_R is trained weights, out of scope): the
+  softmax output minus the softmax-weighted value/key covariance times the probe,
+      out_i = sum_j wbar_ij v_j - Sigma_KV,i rho_i,
+      Sigma_KV,i = sum_j wbar_ij (v_j - vbar_i)(k_j - kbar_i)^T,
+  with wbar the same max-subtracted causal softmax weights normalised to sum 1, vbar_i
+  and kbar_i their weighted means, and the page's boundary factor eta dropped (the page
+  removes it).  The covariance matrix is formed explicitly (d x d per query).
 * ``brute_force_fit`` minimises the weighted ridge objective of section 2.1 over
   (b, W) directly by SVD least squares, without the closed form.  Reading: the
   ridge term that reproduces Eq. (7)'s "+ lambda I" is (lambda/2)||W||_F^2 (the
@@ -60,6 +68,8 @@ __all__ = [
     "lla_row_deflated_cg",
     "softmax_row",
     "softmax_ref",
+    "parallax_row",
+    "parallax_ref",
     "cg_solve",
     "lla_row_cg",
     "brute_force_fit",
@@ -262,6 +272,29 @@ def softmax_ref(q, k, v, tau, rows=None):
     """Causal softmax attention with the same max-subtracted weights, row by row."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     outs = [softmax_row(q[b, h, i], k[b, h, : i + 1], v[b, h, : i + 1], tau)
+            for b, h, i in _rows_iter(q.shape, rows)]
+    return np.array(outs).reshape(-1, q.shape[-1])
+
+
+def parallax_row(q_i, K_prefix, V_prefix, rho_i, tau):
+    """Parallax form of one query: softmax output minus Sigma_KV rho (explicit covariance).
+
+    Returns a dict with out, softmax (the softmax output), cov (Sigma_KV, [d_v, d_k]),
+    kbar and vbar.
+    """
+    w, _ = row_weights(q_i, K_prefix, tau)
+    wbar = w / w.sum()
+    K, V = _f64(K_prefix), _f64(V_prefix)
+    kbar, vbar = wbar @ K, wbar @ V
+    cov = ((V - vbar[None, :]) * wbar[:, None]).T @ (K - kbar[None, :])
+    soft = wbar @ V
+    return {"out": soft - cov @ _f64(rho_i), "softmax": soft, "cov": cov, "kbar": kbar, "vbar": vbar}
+
+
+def parallax_ref(q, k, v, rho, tau, rows=None):
+    """Causal Parallax-form attention over [B, H, n, d] inputs with probe rho [B, H, n, d]."""
+    q, k, v, rho = _f64(q), _f64(k), _f64(v), _f64(rho)
+    outs = [parallax_row(q[b, h, i], k[b, h, : i + 1], v[b, h, : i + 1], rho[b, h, i], tau)["out"]
             for b, h, i in _rows_iter(q.shape, rows)]
     return np.array(outs).reshape(-1, q.shape[-1])
 

@@ -294,3 +294,63 @@ def test_weight_noise_hook_is_inert_by_default_and_small_when_used():
                               weight_noise=np.full(i + 1, 1e-6))
     # a common relative factor on every weight: kbar, wbar unchanged; only lambda/omega shifts
     assert np.abs(a["out"] - c["out"]).max() < 1e-5
+
+
+# --------------------------------------------------------------------------- Parallax form
+def test_parallax_zero_probe_is_softmax():
+    """Parallax page: with the probe projection set to zero the mechanism is exactly softmax."""
+    q, k, v = _rand(21, 20, 4)
+    for i in [0, 7, 19]:
+        r = O.parallax_row(q[i], k[: i + 1], v[: i + 1], np.zeros(4), 0.9)
+        assert np.abs(r["out"] - O.softmax_row(q[i], k[: i + 1], v[: i + 1], 0.9)).max() < 1e-14
+
+
+def test_parallax_with_the_centred_solve_is_lla():
+    """The Parallax rewrite of LLA: softmax minus Sigma_KV times the probe rho' = eta rho, where
+    rho, denom come from the Cholesky solve of Eq. (7) and eta = omega / denom (the boundary
+    factor the page drops by absorbing it into the probe)."""
+    for seed, n, d, tau, lam in CASES:
+        q, k, v = _rand(seed, n, d)
+        for i in range(n):
+            a = O.lla_row(q[i], k[: i + 1], v[: i + 1], tau, lam)
+            probe = (a["omega"] / a["denom"]) * a["rho"]
+            b = O.parallax_row(q[i], k[: i + 1], v[: i + 1], probe, tau)
+            assert np.abs(a["out"] - b["out"]).max() < 1e-10 * (1 + np.abs(a["out"]).max())
+
+
+def test_parallax_is_affine_in_the_probe():
+    q, k, v = _rand(22, 25, 5)
+    rng = np.random.default_rng(3)
+    i = 24
+    r1, r2 = rng.standard_normal(5), rng.standard_normal(5)
+    f = lambda r: O.parallax_row(q[i], k[: i + 1], v[: i + 1], r, 0.6)["out"]
+    lhs = f(2.0 * r1 - 0.5 * r2)
+    rhs = f(np.zeros(5)) + 2.0 * (f(r1) - f(np.zeros(5))) - 0.5 * (f(r2) - f(np.zeros(5)))
+    assert np.abs(lhs - rhs).max() < 1e-12
+
+
+def test_parallax_uniform_weights_exact_rationals():
+    """tau = 0: every prefix weight is 1, so the output is mean(v) - cov(v, k) rho with the
+    population covariance, checked in exact rational arithmetic (d = 1)."""
+    ks = [Fraction(x) for x in (3, -1, 4, 1, -5)]
+    vs = [Fraction(x) for x in (2, 7, -1, 8, 2)]
+    rho = Fraction(3, 7)
+    K = np.array([[float(x)] for x in ks]); V = np.array([[float(x)] for x in vs])
+    Q = np.zeros_like(K)
+    for i in range(len(ks)):
+        m = i + 1
+        kb = sum(ks[: m]) / m
+        vb = sum(vs[: m]) / m
+        cov = sum((vs[j] - vb) * (ks[j] - kb) for j in range(m)) / m
+        want = vb - cov * rho
+        got = O.parallax_row(Q[i], K[: m], V[: m], np.array([float(rho)]), 0.0)["out"][0]
+        assert abs(got - float(want)) < 1e-13
+
+
+def test_parallax_ref_layout_matches_rows():
+    rng = np.random.default_rng(23)
+    q, k, v, r = (rng.standard_normal((2, 2, 5, 3)) for _ in range(4))
+    out = O.parallax_ref(q, k, v, r, 0.4)
+    assert out.shape == (20, 3)
+    one = O.parallax_row(q[1, 0, 3], k[1, 0, :4], v[1, 0, :4], r[1, 0, 3], 0.4)["out"]
+    assert np.abs(out[(1 * 2 + 0) * 5 + 3] - one).max() == 0.0
