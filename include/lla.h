@@ -134,6 +134,29 @@ int lla_forward_noalloc(const void* q, const void* k, const void* v, void* out, 
                         int B, int H, int n, int d, float tau, float lambda, int cg_max_iters, float cg_tol,
                         void* stream);
 
+/*
+ * lla_parallax_forward -- Parallax-form causal attention with a caller-supplied probe
+ * (Parallax: Parameterized Local Linear Attention, the "softmax output minus a covariance
+ * correction" rewrite of LLA; the page learns the probe as rho = RMSNorm(W_R x), here the
+ * caller supplies it, and the page's boundary factor eta is dropped as the page does):
+ *
+ *     wbar_ij     = exp(tau q_i.k_j - m_i) / omega_i     (the causal softmax weights, j <= i)
+ *     Sigma_KV,i  = sum_j wbar_ij (v_j - vbar_i)(k_j - kbar_i)^T
+ *     out_i       = sum_j wbar_ij v_j - Sigma_KV,i probe_i
+ *                 = sum_j wbar_ij (1 - (k_j - kbar_i).probe_i) v_j.
+ *
+ * With probe = 0 this is causal softmax attention.  With probe_i = omega_i rho_i / denom_i
+ * (the LLA solution and denominator of lla_forward) it equals the LLA output.
+ *
+ * dtype, path, q, k, v, out, B, H, n, d, tau, workspace, workspace_bytes, stream: as for
+ * lla_forward_ex (lla_workspace_size gives the same scratch size).  probe: [B,H,n,d] fp32
+ * device buffer, read only, 16-byte aligned.  No regression is solved, so there is no lambda,
+ * no iteration count and no rho/denom output.  Errors as for lla_forward_ex.
+ */
+int lla_parallax_forward(int dtype, int path, const void* q, const void* k, const void* v, const float* probe,
+                         void* out, int B, int H, int n, int d, float tau, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
 /* Message for the calling thread's most recent failure ("" if none). Owned by the library. */
 const char* lla_last_error(void);
 

@@ -15,7 +15,7 @@ import os
 __all__ = [
     "LLAError", "load_library", "library_path", "forward", "lla_forward", "lla_forward_ex",
     "lla_workspace_size", "lla_resolve_path", "lla_sync_status", "lla_last_error", "lla_version",
-    "lla_profile_enable", "lla_profile_read", "lla_forward_noalloc",
+    "lla_profile_enable", "lla_profile_read", "lla_forward_noalloc", "lla_parallax_forward", "parallax_forward",
     "LLA_OK", "LLA_ERR_INVALID_ARG", "LLA_ERR_UNSUPPORTED", "LLA_ERR_CUDA", "LLA_ERR_DEVICE_TIMEOUT",
     "LLA_DTYPE_BF16", "LLA_DTYPE_FP32", "LLA_PATH_AUTO", "LLA_PATH_TENSOR", "LLA_PATH_FP32",
     "EXPORTED_SYMBOLS",
@@ -42,6 +42,8 @@ _SIGNATURES = {
     "lla_last_error": (ctypes.c_char_p, []),
     "lla_forward_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_float,
                                      _c_float, _c_int, _c_float, _vp]),
+    "lla_parallax_forward": (_c_int, [_c_int, _c_int, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                      _c_float, _vp, _c_size, _vp]),
     "lla_profile_enable": (_c_int, [_c_int]),
     "lla_profile_read": (_c_int, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]),
     "lla_version": (_c_int, []),
@@ -143,6 +145,46 @@ def lla_forward_ex(dtype, path, q_ptr, k_ptr, v_ptr, out_ptr, rho_ptr, denom_ptr
     """Raw C entry point with dtype/path/iteration-count/workspace arguments."""
     _check(load_library().lla_forward_ex(dtype, path, q_ptr, k_ptr, v_ptr, out_ptr, rho_ptr, denom_ptr, iters_ptr,
                                          B, H, n, d, tau, lam, cg_max_iters, cg_tol, ws_ptr, ws_bytes, stream_ptr))
+
+
+def lla_parallax_forward(dtype, path, q_ptr, k_ptr, v_ptr, probe_ptr, out_ptr, B, H, n, d, tau, ws_ptr, ws_bytes,
+                         stream_ptr):
+    """Raw Parallax-form entry point on device pointers (ints); raises LLAError on failure."""
+    _check(load_library().lla_parallax_forward(dtype, path, q_ptr, k_ptr, v_ptr, probe_ptr, out_ptr, B, H, n, d, tau,
+                                               ws_ptr, ws_bytes, stream_ptr))
+
+
+def _check_qkv(q, k, v):
+    import torch
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise LLAError(LLA_ERR_INVALID_ARG, "q, k, v must be CUDA tensors (there is no CPU path)")
+    if q.shape != k.shape or q.shape != v.shape or q.dim() != 4:
+        raise LLAError(LLA_ERR_INVALID_ARG, f"q, k, v must share one [B, H, n, d] shape, got {tuple(q.shape)}, "
+                                            f"{tuple(k.shape)}, {tuple(v.shape)}")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.bfloat16, torch.float32):
+        raise LLAError(LLA_ERR_INVALID_ARG, "q, k, v must all be bf16 or all fp32")
+
+
+def parallax_forward(q, k, v, probe, tau, *, path=LLA_PATH_AUTO, out=None, workspace=None, stream=None):
+    """Parallax-form causal attention: softmax output minus Sigma_KV probe (see include/lla.h).
+
+    q, k, v: CUDA [B, H, n, d] bf16 or fp32; probe: [B, H, n, d] (converted to contiguous fp32).
+    Returns out (dtype of q).  Asynchronous on the current (or given) stream.
+    """
+    import torch
+    _check_qkv(q, k, v)
+    if tuple(probe.shape) != tuple(q.shape) or not probe.is_cuda:
+        raise LLAError(LLA_ERR_INVALID_ARG, f"probe must be a CUDA tensor of shape {tuple(q.shape)}")
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    probe = probe.to(torch.float32).contiguous()
+    B, H, n, d = q.shape
+    dtype = LLA_DTYPE_BF16 if q.dtype == torch.bfloat16 else LLA_DTYPE_FP32
+    if out is None:
+        out = torch.empty_like(q)
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    lla_parallax_forward(dtype, path, q.data_ptr(), k.data_ptr(), v.data_ptr(), probe.data_ptr(), out.data_ptr(),
+                         B, H, n, d, float(tau), ws_ptr, ws_bytes, _stream_ptr(stream))
+    return out
 
 
 def forward(q, k, v, tau, lam, cg_max_iters, cg_tol=0.0, *, path=LLA_PATH_AUTO, return_iters=False,

@@ -60,6 +60,60 @@ cudaError_t read_and_clear_device_error(unsigned* out, cudaStream_t stream) {
     return e;
 }
 
+
+// Launch a validated problem on the resolved path (workspace: caller's buffer, or null to take
+// one from the stream-ordered pool for the duration of the call).
+static int run_problem(Problem& p, int rpath, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (g_prof_on) {
+        for (int i = 0; i < 4; ++i)
+            if (!g_ev[i]) {
+                cudaError_t e = cudaEventCreate(&g_ev[i]);
+                if (e != cudaSuccess) return cuda_fail(e, "profiling event");
+            }
+        p.ev_main_begin = g_ev[1];
+        p.ev_main_end = g_ev[2];
+        cudaError_t e = cudaEventRecord(g_ev[0], stream);
+        if (e != cudaSuccess) return cuda_fail(e, "profiling event record");
+    }
+
+    if (rpath == LLA_PATH_FP32) {
+        cudaError_t e = launch_simt(p, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "fp32 path launch");
+        if (g_prof_on) {
+            e = cudaEventRecord(g_ev[3], stream);
+            if (e != cudaSuccess) return cuda_fail(e, "profiling event record");
+            g_prof_valid = true;
+        }
+        return LLA_OK;
+    }
+
+    const size_t need = tensor_workspace_bytes(p.B, p.H, p.n, p.d);
+    void* ws = workspace;
+    bool owned = false;
+    if (ws) {
+        if (workspace_bytes < need)
+            return fail(LLA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+        if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+            return fail(LLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    } else {
+        cudaError_t e = cudaMallocAsync(&ws, need, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(workspace)");
+        owned = true;
+    }
+    const char* why = nullptr;
+    cudaError_t e = launch_tensor(p, ws, stream, &why);
+    if (owned) {
+        cudaError_t e2 = cudaFreeAsync(ws, stream);
+        if (e == cudaSuccess && e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync(workspace)");
+    }
+    if (e != cudaSuccess) return cuda_fail(e, why ? why : "tensor path launch");
+    if (g_prof_on) {
+        e = cudaEventRecord(g_ev[3], stream);
+        if (e != cudaSuccess) return cuda_fail(e, "profiling event record");
+        g_prof_valid = true;
+    }
+    return LLA_OK;
+}
 }  // namespace lla
 
 using lla::fail;
@@ -106,58 +160,9 @@ int lla_forward_ex(int dtype, int path, const void* q, const void* k, const void
     if (rpath == LLA_PATH_TENSOR && (dtype != LLA_DTYPE_BF16 || (d != 64 && d != 128)))
         return fail(LLA_ERR_UNSUPPORTED, "tensor path needs bf16 inputs and d in {64, 128}");
 
-    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     lla::Problem p{q, k, v, out, rho, denom, cg_iters, B, H, n, d, tau, lambda, cg_max_iters, cg_tol, dtype,
-                   nullptr, nullptr};
-    if (lla::g_prof_on) {
-        for (int i = 0; i < 4; ++i)
-            if (!lla::g_ev[i]) {
-                cudaError_t e = cudaEventCreate(&lla::g_ev[i]);
-                if (e != cudaSuccess) return lla::cuda_fail(e, "profiling event");
-            }
-        p.ev_main_begin = lla::g_ev[1];
-        p.ev_main_end = lla::g_ev[2];
-        cudaError_t e = cudaEventRecord(lla::g_ev[0], stream);
-        if (e != cudaSuccess) return lla::cuda_fail(e, "profiling event record");
-    }
-
-    if (rpath == LLA_PATH_FP32) {
-        cudaError_t e = lla::launch_simt(p, stream);
-        if (e != cudaSuccess) return lla::cuda_fail(e, "fp32 path launch");
-        if (lla::g_prof_on) {
-            e = cudaEventRecord(lla::g_ev[3], stream);
-            if (e != cudaSuccess) return lla::cuda_fail(e, "profiling event record");
-            lla::g_prof_valid = true;
-        }
-        return LLA_OK;
-    }
-
-    const size_t need = lla::tensor_workspace_bytes(B, H, n, d);
-    void* ws = workspace;
-    bool owned = false;
-    if (ws) {
-        if (workspace_bytes < need)
-            return fail(LLA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
-        if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
-            return fail(LLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
-    } else {
-        cudaError_t e = cudaMallocAsync(&ws, need, stream);
-        if (e != cudaSuccess) return lla::cuda_fail(e, "cudaMallocAsync(workspace)");
-        owned = true;
-    }
-    const char* why = nullptr;
-    cudaError_t e = lla::launch_tensor(p, ws, stream, &why);
-    if (owned) {
-        cudaError_t e2 = cudaFreeAsync(ws, stream);
-        if (e == cudaSuccess && e2 != cudaSuccess) return lla::cuda_fail(e2, "cudaFreeAsync(workspace)");
-    }
-    if (e != cudaSuccess) return lla::cuda_fail(e, why ? why : "tensor path launch");
-    if (lla::g_prof_on) {
-        e = cudaEventRecord(lla::g_ev[3], stream);
-        if (e != cudaSuccess) return lla::cuda_fail(e, "profiling event record");
-        lla::g_prof_valid = true;
-    }
-    return LLA_OK;
+                   nullptr, nullptr, nullptr};
+    return lla::run_problem(p, rpath, workspace, workspace_bytes, static_cast<cudaStream_t>(stream_));
 }
 
 int lla_profile_enable(int on) {
@@ -181,6 +186,30 @@ int lla_forward(const void* q, const void* k, const void* v, void* out, float* r
                 int n, int d, float tau, float lambda, int cg_max_iters, float cg_tol, void* stream) {
     return lla_forward_ex(LLA_DTYPE_BF16, LLA_PATH_AUTO, q, k, v, out, rho, denom, nullptr, B, H, n, d, tau,
                           lambda, cg_max_iters, cg_tol, nullptr, 0, stream);
+}
+
+int lla_parallax_forward(int dtype, int path, const void* q, const void* k, const void* v, const float* probe,
+                         void* out, int B, int H, int n, int d, float tau, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+    lla::g_msg[0] = '\0';
+    if (!q || !k || !v || !probe || !out) return fail(LLA_ERR_INVALID_ARG, "null tensor pointer");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(probe) || !aligned16(out))
+        return fail(LLA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    if (B < 1 || H < 1 || n < 1) return fail(LLA_ERR_INVALID_ARG, "B, H, n must be >= 1 (got %d, %d, %d)", B, H, n);
+    if ((long long)B * H > 65535LL * 1024) return fail(LLA_ERR_INVALID_ARG, "B*H too large");
+    if ((long long)B * H * n * d > (1LL << 40)) return fail(LLA_ERR_INVALID_ARG, "problem too large");
+    if (d != 16 && d != 32 && d != 64 && d != 128)
+        return fail(LLA_ERR_INVALID_ARG, "head dim d must be 16, 32, 64 or 128 (got %d)", d);
+    if (!(tau > 0.f) || !(tau < 1e30f)) return fail(LLA_ERR_INVALID_ARG, "tau must be finite and > 0");
+    if (dtype != LLA_DTYPE_BF16 && dtype != LLA_DTYPE_FP32) return fail(LLA_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+    if (path < LLA_PATH_AUTO || path > LLA_PATH_FP32) return fail(LLA_ERR_INVALID_ARG, "unknown path %d", path);
+    const int rpath = lla_resolve_path(dtype, path, d);
+    if (rpath == LLA_PATH_TENSOR && (dtype != LLA_DTYPE_BF16 || (d != 64 && d != 128)))
+        return fail(LLA_ERR_UNSUPPORTED, "tensor path needs bf16 inputs and d in {64, 128}");
+    // no regression solve: lambda only enters the skipped CG; 1 keeps the shared code finite
+    lla::Problem p{q, k, v, out, nullptr, nullptr, nullptr, B, H, n, d, tau, 1.f, 0, 0.f, dtype,
+                   nullptr, nullptr, probe};
+    return lla::run_problem(p, rpath, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 int lla_sync_status(void* stream) {

@@ -23,6 +23,9 @@ struct Problem {
     int dtype;           // lla_dtype
     cudaEvent_t ev_main_begin;   // recorded just before / after the dominant kernel when profiling
     cudaEvent_t ev_main_end;     // (null otherwise)
+    // Parallax form: the caller's probe [B,H,n,d] fp32.  Non-null: no CG (cg_max_iters is 0),
+    // the output sweep takes this probe as rho', and rho / denom / cg_iters are not written.
+    const float* probe;
 };
 
 // Device error word: bit flags set by kernels that gave up (a bounded wait ran out, or the

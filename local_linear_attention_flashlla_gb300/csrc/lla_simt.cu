@@ -16,6 +16,9 @@
 //       output sweep out_i = sum_j u_ij v_j / sum_j u_ij, u_ij = w_ij (1 - (k_j - kbar_i).rho'_i),
 //       which is Eq. (8); sum_j u_ij equals omega_i exactly because sum_j w_ij (k_j - kbar_i) = 0,
 //       and normalising by the computed sum keeps sum_j s_ij = 1 in rounding as well.
+// Parallax form (a caller-supplied probe, Parallax page): phases (0), (1) and the output
+// sweep of (3) with the probe as rho', i.e. out_i = sum_j wbar_ij (1 - (k_j - kbar_i).probe_i) v_j,
+// the softmax output minus the softmax-weighted value/key covariance times the probe.
 // Every product, sum and CG quantity is fp32.  No global scratch.
 //
 // Thread layout (256 threads): row r = tid / 8 is owned by the 8 consecutive lanes
@@ -107,7 +110,7 @@ template <int D, typename T>
 __global__ void __launch_bounds__(NT, 1)
 lla_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, T* __restrict__ out,
                 float* __restrict__ rho, float* __restrict__ denom, int* __restrict__ cg_iters, int n, int n_tiles,
-                float tau, float lambda, int cg_max_iters, float cg_tol) {
+                float tau, float lambda, int cg_max_iters, float cg_tol, const float* __restrict__ probe) {
     constexpr int E = D / 8;  // coordinates per lane
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Smem<D>& sm = *reinterpret_cast<Smem<D>*>(smem_raw);
@@ -254,6 +257,12 @@ lla_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
     }
 
     // ---- (3) finalise and output sweep ---------------------------------------------------------
+    // Parallax form: no solve (cg_max_iters is 0); the caller's probe plays rho'
+    if (probe) {
+        const float* pr = probe + (head * (size_t)n + (row_ok ? i : 0)) * D;
+#pragma unroll
+        for (int c = 0; c < E; ++c) x[c] = row_ok ? pr[l8 + 8 * c] : 0.f;
+    }
     float dx = 0.f, kx = 0.f;
 #pragma unroll
     for (int c = 0; c < E; ++c) {
@@ -296,9 +305,9 @@ lla_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
         for (int c = 0; c < E; ++c) {
             const int e = l8 + 8 * c;
             st_f(out + base + e, acc[c] * inv_u);
-            rho[base + e] = x[c] * inv_g;
+            if (!probe) rho[base + e] = x[c] * inv_g;
         }
-        if (l8 == 0) {
+        if (l8 == 0 && !probe) {
             denom[head * (size_t)n + i] = omega * inv_g;
             if (cg_iters) cg_iters[head * (size_t)n + i] = iters;
         }
@@ -316,7 +325,7 @@ cudaError_t launch_typed(const Problem& p, cudaStream_t stream) {
     if (p.ev_main_begin && (err = cudaEventRecord(p.ev_main_begin, stream)) != cudaSuccess) return err;
     kern<<<grid, NT, smem, stream>>>(static_cast<const T*>(p.q), static_cast<const T*>(p.k),
                                      static_cast<const T*>(p.v), static_cast<T*>(p.out), p.rho, p.denom,
-                                     p.cg_iters, p.n, n_tiles, p.tau, p.lambda, p.cg_max_iters, p.cg_tol);
+                                     p.cg_iters, p.n, n_tiles, p.tau, p.lambda, p.cg_max_iters, p.cg_tol, p.probe);
     err = cudaGetLastError();
     if (err == cudaSuccess && p.ev_main_end) err = cudaEventRecord(p.ev_main_end, stream);
     return err;

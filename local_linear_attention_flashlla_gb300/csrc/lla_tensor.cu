@@ -21,6 +21,10 @@
 // out_i = sum_j w_ij (1 - (k_j - kbar_i).rho'_i) v_j / sum_j w_ij (1 - (k_j - kbar_i).rho'_i)
 // (Eqs. (6)-(8) with Sigma_i = C_i + omega_i delta_i delta_i^T, Sherman-Morrison).
 //
+// Parallax form (caller-supplied probe, Parallax page): MAX, MOMENT and OUT with the probe as
+// rho' (no CG sweep), i.e. out_i = sum_j wbar_ij (1 - (k_j - kbar_i).probe_i) v_j, the softmax
+// output minus the softmax-weighted value/key covariance times the probe.
+//
 // Roles (384 threads, three warpgroups): warp 0 lane 0 issues TMA (Q once, then K/V blocks
 // into a 3-slot ring); lane 0 of warps 1, 3 and 2 issues the S, the A'/T and the Y products
 // (three issue streams, synchronised through mbarriers: each MMA-issuing warp shares its
@@ -158,6 +162,7 @@ struct TcParams {
     float* rho;
     float* denom;
     int* cg_iters;
+    const float* probe;   // Parallax form: caller's probe [B,H,n,D] fp32 (null for LLA)
     unsigned* dev_err;
     int n, n_tiles;
     float tau, lambda, cg_tol;
@@ -888,6 +893,13 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             xv[e] = have_x ? xt[e * BQ] : 0.f;
             kv[e] = kbt[e * BQ];
         }
+        if (prm.probe && row_ok) {   // Parallax form: the caller's probe plays rho'
+#pragma unroll
+            for (int e0 = 0; e0 < DH; e0 += 4) {
+                const float4 t = *reinterpret_cast<const float4*>(prm.probe + row_g + e0);
+                xv[e0] = t.x; xv[e0 + 1] = t.y; xv[e0 + 2] = t.z; xv[e0 + 3] = t.w;
+            }
+        }
         float dx = 0.f, mxx = 0.f;
         {
             const float qsc = pow2i(-eq);
@@ -927,7 +939,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
                 *reinterpret_cast<uint4*>(tile_half(s.p, row, half * DH + e0)) = pk;
                 *reinterpret_cast<uint4*>(tile_half(s.rlo, row, half * DH + e0)) = pl;
-                if (row_ok) {   // rho = rho' / (1 + delta.rho'), row-major output
+                if (row_ok && !prm.probe) {   // rho = rho' / (1 + delta.rho'), row-major output
                     *reinterpret_cast<float4*>(prm.rho + row_g + e0) =
                         make_float4(xv[e0] * inv_g, xv[e0 + 1] * inv_g, xv[e0 + 2] * inv_g, xv[e0 + 3] * inv_g);
                     *reinterpret_cast<float4*>(prm.rho + row_g + e0 + 4) =
@@ -937,7 +949,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             if (!row_ok) kx = 0.f;
         }
         kx = xch.sum(kx);
-        if (row_ok && half == 0) {
+        if (row_ok && half == 0 && !prm.probe) {
             prm.denom[(size_t)head * n + i] = omega * inv_g;
             if (prm.cg_iters) prm.cg_iters[(size_t)head * n + i] = iters;
         }
@@ -1044,6 +1056,7 @@ cudaError_t launch_d(const Problem& p, void* ws, cudaStream_t stream, const char
     prm.rho = p.rho;
     prm.denom = p.denom;
     prm.cg_iters = p.cg_iters;
+    prm.probe = p.probe;
     prm.dev_err = device_error_word();
     prm.n = p.n;
     prm.n_tiles = (p.n + BQ - 1) / BQ;

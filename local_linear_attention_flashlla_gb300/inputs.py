@@ -120,6 +120,19 @@ def make_inputs(w: Workload):
             torch.from_numpy(np.ascontiguousarray(v)).to(td))
 
 
+def make_probe(w: Workload, seed_offset=1000):
+    """Parallax probe [B, H, n, d] fp32 (CPU torch), drawn after (q, k, v) from its own stream.
+
+    The page computes rho = RMSNorm(W_R x) from the layer input; without trained weights the
+    stand-in is an RMS-normalised Gaussian row divided by sqrt(d), so (k_j - kbar).rho is of
+    order one for the unit-RMS keys of the LM workloads (the correction is of the size of the
+    softmax output, neither negligible nor dominant).
+    """
+    rng = np.random.Generator(np.random.PCG64(w.seed + seed_offset))
+    r = _rmsnorm_rows(rng.standard_normal((w.B, w.H, w.n, w.d), dtype=np.float32))
+    return torch.from_numpy(np.ascontiguousarray(r * np.float32(1.0 / math.sqrt(w.d))))
+
+
 def sample_rows(w: Workload, count, seed=1, tile=128):
     """Stratified (b, h, i) rows for sampled parity checks at full size.
 

@@ -74,3 +74,32 @@ def test_binding_refuses_cpu_tensors():
     x = torch.zeros(1, 1, 4, 16)
     with pytest.raises(lla.LLAError):
         lla.forward(x, x, x, 0.25, 0.1, 4)
+
+
+def _call_parallax(lib, **kw):
+    a = dict(dtype=0, path=0, q=16, k=32, v=48, probe=80, out=64, B=1, H=1, n=8, d=64, tau=0.1, ws=None, wsb=0,
+             stream=None)
+    a.update(kw)
+    return lib.lla_parallax_forward(a["dtype"], a["path"], a["q"], a["k"], a["v"], a["probe"], a["out"], a["B"],
+                                    a["H"], a["n"], a["d"], a["tau"], a["ws"], a["wsb"], a["stream"])
+
+
+@pytest.mark.parametrize("bad", [
+    dict(q=None), dict(probe=None), dict(out=None), dict(probe=20), dict(B=0), dict(n=0), dict(d=48),
+    dict(tau=0.0), dict(tau=float("nan")), dict(dtype=5), dict(path=-1),
+])
+def test_parallax_invalid_arguments_rejected_before_launch(lib, bad):
+    assert _call_parallax(lib, **bad) == lla.LLA_ERR_INVALID_ARG
+    assert lib.lla_last_error().decode()
+
+
+def test_parallax_tensor_path_needs_bf16_and_supported_dim(lib):
+    assert _call_parallax(lib, dtype=1, path=lla.LLA_PATH_TENSOR) == lla.LLA_ERR_UNSUPPORTED
+    assert _call_parallax(lib, d=16, path=lla.LLA_PATH_TENSOR) == lla.LLA_ERR_UNSUPPORTED
+
+
+def test_parallax_binding_refuses_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(1, 1, 4, 16)
+    with pytest.raises(lla.LLAError):
+        lla.parallax_forward(x, x, x, x, 0.25)
