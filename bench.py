@@ -32,6 +32,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "causal LLA fwd tokens/s & TFLOP/s at d=128 bf16; fraction of BF16 tensor peak"
+METRIC_PARALLAX = "causal Parallax-form fwd (caller probe) tokens/s & TFLOP/s at d=128 bf16; fraction of BF16 tensor peak"
 
 
 def useful_flops(w, T):
@@ -44,6 +45,17 @@ def executed_flops(w, T, path):
     """Adds the logits-only max sweep and the output sweep's rho.k product."""
     pairs = w.n * (w.n + 1) / 2 * w.B * w.H
     return (6 + 3 * T) * 2 * w.d * pairs
+
+
+def parallax_useful_flops(w):
+    """Parallax form: q.k, the weighted key mean, probe.k and the value product: 4 passes of 2d."""
+    return 4 * 2 * w.d * (w.n * (w.n + 1) / 2 * w.B * w.H)
+
+
+def parallax_executed_flops(w, tensor):
+    """Adds the max sweep's q.k, the recomputed q.k of the moment and output sweeps and, on the
+    tensor path, the probe's lo-part product."""
+    return (7 if tensor else 6) * 2 * w.d * (w.n * (w.n + 1) / 2 * w.B * w.H)
 
 
 def load_peaks():
@@ -134,19 +146,24 @@ def load_traffic(kernel, workload_name):
 
 # ----------------------------------------------------------------------------- CPU oracle timing
 
+def _oracle_row(op, q, k, v, probe, tau, lam, b, h, i):
+    from oracle.lla_ref import lla_row, parallax_row
+    if op == "parallax":
+        return parallax_row(q[b, h, i], k[b, h, : i + 1], v[b, h, : i + 1], probe[b, h, i], tau)
+    return lla_row(q[b, h, i], k[b, h, : i + 1], v[b, h, : i + 1], tau, lam)
+
+
 def _oracle_rows_worker(job):
-    import numpy as np
-    from oracle.lla_ref import lla_row
-    q, k, v, tau, lam, rows = job
+    op, q, k, v, probe, tau, lam, rows = job
     out = []
     for (b, h, i) in rows:
         t0 = time.perf_counter()
-        lla_row(q[b, h, i], k[b, h, : i + 1], v[b, h, : i + 1], tau, lam)
+        _oracle_row(op, q, k, v, probe, tau, lam, b, h, i)
         out.append((i, time.perf_counter() - t0))
     return out
 
 
-def cpu_oracle_throughput(w, qkv, budget_s=15.0, seed=123):
+def cpu_oracle_throughput(w, qkv, budget_s=15.0, seed=123, op="lla", probe=None):
     """Time the oracle on a bounded random sample of rows on all host cores; extrapolate.
 
     Per-row cost is fitted as a + b (i + 1) (the dense Sigma build is (i+1) d^2) and
@@ -161,11 +178,11 @@ def cpu_oracle_throughput(w, qkv, budget_s=15.0, seed=123):
     cores = os.cpu_count() or 1
     rng = np.random.default_rng(seed)
     q, k, v = (t.double().numpy() for t in qkv)
+    pr = None if probe is None else probe.double().numpy()
     # calibrate: one row at the mean causal length
-    from oracle.lla_ref import lla_row
     t0 = time.perf_counter()
     i_mid = w.n // 2
-    lla_row(q[0, 0, i_mid], k[0, 0, : i_mid + 1], v[0, 0, : i_mid + 1], w.tau, w.lam)
+    _oracle_row(op, q, k, v, pr, w.tau, w.lam, 0, 0, i_mid)
     per_row = max(time.perf_counter() - t0, 1e-4)
     n_rows = int(max(cores * 2, min(4096, budget_s * cores / per_row)))
     rows = [(int(rng.integers(w.B)), int(rng.integers(w.H)), int(rng.integers(w.n))) for _ in range(n_rows)]
@@ -173,7 +190,7 @@ def cpu_oracle_throughput(w, qkv, budget_s=15.0, seed=123):
     ctx = mp.get_context("spawn")
     t0 = time.perf_counter()
     with ctx.Pool(cores) as pool:
-        res = pool.map(_oracle_rows_worker, [(q, k, v, w.tau, w.lam, ch) for ch in chunks])
+        res = pool.map(_oracle_rows_worker, [(op, q, k, v, pr, w.tau, w.lam, ch) for ch in chunks])
     wall = time.perf_counter() - t0
     pts = [p for r in res for p in r]
     i_arr = np.array([p[0] + 1 for p in pts], dtype=np.float64)
@@ -186,8 +203,10 @@ def cpu_oracle_throughput(w, qkv, budget_s=15.0, seed=123):
     est_wall = total_single / (cores * eff)
     tokens = w.B * w.n
     return {"value": tokens / est_wall, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": (f"{len(pts)} random (b,h,i) rows of {w.name} solved exactly (float64, dense Sigma, "
-                       f"Cholesky) in {wall:.1f} s on {cores} processes; per-row cost a+b(i+1) fitted and "
+            "sample": (f"{len(pts)} random (b,h,i) rows of {w.name} "
+                       + ("in the Parallax form (float64, explicit Sigma_KV)" if op == "parallax" else
+                          "solved exactly (float64, dense Sigma, Cholesky)")
+                       + f" in {wall:.1f} s on {cores} processes; per-row cost a+b(i+1) fitted and "
                        f"integrated over all {w.B * w.H * w.n} rows: est. {est_wall:.0f} s per step"),
             "est_seconds_per_step": est_wall}
 
@@ -204,6 +223,8 @@ def parse():
     ap.add_argument("--path", choices=["auto", "tensor", "fp32"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--op", choices=["lla", "parallax"], default="lla",
+                    help="lla: the LLA forward (default); parallax: the Parallax form with a synthetic probe")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch B (a smaller case for profiler captures)")
     return ap.parse_args()
@@ -226,24 +247,26 @@ def dist_setup(args):
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    from local_linear_attention_flashlla_gb300.inputs import make_inputs, workload
+    from local_linear_attention_flashlla_gb300.inputs import make_inputs, make_probe, workload
     w = workload(args.workload) if args.batch is None else workload(args.workload, B=args.batch)
     qkv = make_inputs(w)
+    parallax = args.op == "parallax"
+    probe = make_probe(w) if parallax else None
     steps = []
     cb = None
     for s in range(args.warmup + args.steps):
-        cb = cpu_oracle_throughput(w, qkv, budget_s=4.0, seed=1000 + s)
+        cb = cpu_oracle_throughput(w, qkv, budget_s=4.0, seed=1000 + s, op=args.op, probe=probe)
         if s >= args.warmup:
             steps.append(cb["est_seconds_per_step"])
     sec = statistics.mean(steps)
     value = w.B * w.n / sec
     T = w.cg_max_iters
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+    line = {"impl": "reference", "metric": METRIC_PARALLAX if parallax else METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": f"{w.name} B={w.B} H={w.H} n={w.n} d={w.d} tau={w.tau:.5g} lambda={w.lam} "
                                    f"cg_iters={T} cg_tol={w.cg_tol}", "l2": "n/a (CPU)"},
-            "tflops": useful_flops(w, T) / sec / 1e12,
+            "tflops": (parallax_useful_flops(w) if parallax else useful_flops(w, T)) / sec / 1e12,
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cb["cores"], "kind": "oracle",
                              "sample": cb["sample"]},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -261,7 +284,7 @@ def main():
     import torch
 
     import local_linear_attention_flashlla_gb300 as lla
-    from local_linear_attention_flashlla_gb300.inputs import make_inputs, workload
+    from local_linear_attention_flashlla_gb300.inputs import make_inputs, make_probe, workload
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -271,6 +294,9 @@ def main():
     rpath = lla.lla_resolve_path(dtype_code, path, w.d)
     qkv_host = make_inputs(w.with_(seed=w.seed + rank))
     q, k, v = (t.to(dev) for t in qkv_host)
+    parallax = args.op == "parallax"
+    probe_host = make_probe(w.with_(seed=w.seed + rank)) if parallax else None
+    probe = probe_host.to(dev) if parallax else None
     out = torch.empty_like(q)
     rho = torch.empty(q.shape, dtype=torch.float32, device=dev)
     den = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
@@ -280,8 +306,11 @@ def main():
     stream = torch.cuda.current_stream()
 
     def step():
-        lla.forward(q, k, v, w.tau, w.lam, w.cg_max_iters, w.cg_tol, path=path, out=out, rho=rho, denom=den,
-                    workspace=ws if ws_bytes else None)
+        if parallax:
+            lla.parallax_forward(q, k, v, probe, w.tau, path=path, out=out, workspace=ws if ws_bytes else None)
+        else:
+            lla.forward(q, k, v, w.tau, w.lam, w.cg_max_iters, w.cg_tol, path=path, out=out, rho=rho, denom=den,
+                        workspace=ws if ws_bytes else None)
 
     for _ in range(args.warmup):
         step()
@@ -319,21 +348,23 @@ def main():
     ms_per_step = total_ms / args.steps
     tokens = w.B * w.n
     value = world * tokens * args.steps / (total_ms / 1e3)
-    T = w.cg_max_iters if w.cg_tol == 0 else None
+    T = w.cg_max_iters if (w.cg_tol == 0 or parallax) else None
     if T is None:   # tolerance-driven: count the executed iterations
         _, _, _, its = lla.forward(q, k, v, w.tau, w.lam, w.cg_max_iters, w.cg_tol, path=path, return_iters=True)
         T = float(its.float().max().item())
-    flops = useful_flops(w, T)
+    flops = parallax_useful_flops(w) if parallax else useful_flops(w, T)
     tflops = world * flops * args.steps / (total_ms / 1e3) / 1e12
 
     # end to end through the public API from pinned host buffers
     e2e = None
     if not args.no_e2e:
         hq, hk, hv = (t.pin_memory() for t in qkv_host)
+        hp = probe_host.pin_memory() if parallax else None
         ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         hr = torch.empty(rho.shape, dtype=rho.dtype).pin_memory()
         hd = torch.empty(den.shape, dtype=den.dtype).pin_memory()
         dq, dk, dv = (torch.empty_like(t) for t in (q, k, v))
+        dp = torch.empty_like(probe) if parallax else None
         e2e_ms = []
         for it in range(args.warmup + args.steps):
             flush.zero_()
@@ -343,11 +374,16 @@ def main():
             dq.copy_(hq, non_blocking=True)
             dk.copy_(hk, non_blocking=True)
             dv.copy_(hv, non_blocking=True)
-            lla.forward(dq, dk, dv, w.tau, w.lam, w.cg_max_iters, w.cg_tol, path=path, out=out, rho=rho,
-                        denom=den, workspace=ws if ws_bytes else None)
-            ho.copy_(out, non_blocking=True)
-            hr.copy_(rho, non_blocking=True)
-            hd.copy_(den, non_blocking=True)
+            if parallax:
+                dp.copy_(hp, non_blocking=True)
+                lla.parallax_forward(dq, dk, dv, dp, w.tau, path=path, out=out, workspace=ws if ws_bytes else None)
+                ho.copy_(out, non_blocking=True)
+            else:
+                lla.forward(dq, dk, dv, w.tau, w.lam, w.cg_max_iters, w.cg_tol, path=path, out=out, rho=rho,
+                            denom=den, workspace=ws if ws_bytes else None)
+                ho.copy_(out, non_blocking=True)
+                hr.copy_(rho, non_blocking=True)
+                hd.copy_(den, non_blocking=True)
             e1.record(stream)
             e1.synchronize()
             if it >= args.warmup:
@@ -358,8 +394,8 @@ def main():
             torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
             tot = float(t.item())
         e2e = {"value": world * tokens * len(e2e_ms) / (tot / 1e3), "unit": "tokens/s",
-               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hq, hk, hv)),
-               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in (ho, hr, hd))}
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hq, hk, hv) + ((hp,) if parallax else ())),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in ((ho,) if parallax else (ho, hr, hd)))}
 
     peaks, peak_kind = load_peaks()
     # fp32 path: one kernel per step; tensor path: max|x| pre-pass, fp16 conversion, fused sweep kernel
@@ -377,24 +413,30 @@ def main():
     else:
         peak = peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": load_traffic(kern_name, w.name), "peak_source": f"{peak_kind} bf16 burst",
-                "flops_counted": "useful (4+3T) passes x 2d per causal pair"}
+                "traffic": None if parallax else load_traffic(kern_name, w.name), "peak_source": f"{peak_kind} bf16 burst",
+                "flops_counted": ("useful 4 passes (q.k, weighted key mean, probe.k, values) x 2d per causal pair"
+                                  if parallax else "useful (4+3T) passes x 2d per causal pair")}
         dtype = "f16"
 
-    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+    line = {"metric": METRIC_PARALLAX if parallax else METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": dtype, "data": "synthetic",
             "config": {"workload": f"{w.name} B={w.B} H={w.H} n={w.n} d={w.d} tau={w.tau:.5g} lambda={w.lam} "
                                    f"cg_iters={w.cg_max_iters} cg_tol={w.cg_tol}",
                        "path": {1: "tensor", 2: "fp32"}[rpath], "l2": "flushed before every step (512 MiB write)",
                        "inputs": "bf16 q,k,v resident in HBM" if w.dtype == "bf16" else "fp32 q,k,v in HBM"},
-            "tflops": tflops, "tflops_executed": world * executed_flops(w, T, rpath) * args.steps / (total_ms / 1e3) / 1e12,
+            "tflops": tflops,
+            "tflops_executed": world * (parallax_executed_flops(w, rpath == lla.LLA_PATH_TENSOR) if parallax else
+                                        executed_flops(w, T, rpath)) * args.steps / (total_ms / 1e3) / 1e12,
             "roofline": roof, "clocks": clocks, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
             "dominant_kernel": {"name": kern_name, "ms_per_launch": dominant_ms,
                                 "share_of_step": dominant_ms / ms_per_step},
-            "cg_iters_counted": T}
+            "cg_iters_counted": None if parallax else T}
+    if parallax:
+        line["config"]["workload"] = f"{w.name} B={w.B} H={w.H} n={w.n} d={w.d} tau={w.tau:.5g} (Parallax form, probe)"
+        line["config"]["probe"] = "seeded RMS-normalised Gaussian rows / sqrt(d), fp32"
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_oracle_throughput(w, qkv_host)
+        line["cpu_baseline"] = cpu_oracle_throughput(w, qkv_host, op=args.op, probe=probe_host)
         line["cpu_baseline"].pop("est_seconds_per_step", None)
     if rank == 0:
         print(json.dumps(line), flush=True)
