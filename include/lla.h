@@ -157,6 +157,30 @@ int lla_parallax_forward(int dtype, int path, const void* q, const void* k, cons
                          void* out, int B, int H, int n, int d, float tau, void* workspace, size_t workspace_bytes,
                          void* stream);
 
+/*
+ * lla_decode -- one decode step: a new query per (b, h) against its key/value cache (Local
+ * Linear Attention reading notes, section 2.2: the FlashLLA cache is Theta(n d); the new
+ * query's causal prefix is the whole cache).  The result equals row n-1 of lla_forward on the
+ * sequence whose keys and values are the cache, computed by the same centred CG (fp32
+ * arithmetic, CUDA cores: one query row per head makes the step bound by reading the cache).
+ *
+ * q       [B,H,d] in dtype, the new position's query.
+ * k, v    [B,H,n_cap,d] in dtype: rows 0..n-1 are the cache (the new key/value at n-1); rows
+ *         n..n_cap-1 are not read.  n_cap >= n is the row stride, so a preallocated cache can
+ *         be passed as it grows.
+ * out     [B,H,d] in dtype.  rho [B,H,d] fp32.  denom [B,H] fp32.  cg_iters NULL or [B,H] int32.
+ * tau, lambda, cg_max_iters, cg_tol: as for lla_forward.
+ * All pointers are device pointers, 16-byte aligned, owned by the caller.  No scratch.  The n
+ * weights of a head live in shared memory: n above lla_decode_max_n(d) gives
+ * LLA_ERR_UNSUPPORTED.  Other errors as for lla_forward_ex.
+ */
+int lla_decode(int dtype, const void* q, const void* k, const void* v, void* out, float* rho, float* denom,
+               int* cg_iters, int B, int H, int n, int n_cap, int d, float tau, float lambda, int cg_max_iters,
+               float cg_tol, void* stream);
+
+/* Largest cache length n that lla_decode accepts for head dim d (0 when d is unsupported). */
+int lla_decode_max_n(int d);
+
 /* Message for the calling thread's most recent failure ("" if none). Owned by the library. */
 const char* lla_last_error(void);
 

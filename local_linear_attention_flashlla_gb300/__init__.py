@@ -16,6 +16,7 @@ __all__ = [
     "LLAError", "load_library", "library_path", "forward", "lla_forward", "lla_forward_ex",
     "lla_workspace_size", "lla_resolve_path", "lla_sync_status", "lla_last_error", "lla_version",
     "lla_profile_enable", "lla_profile_read", "lla_forward_noalloc", "lla_parallax_forward", "parallax_forward",
+    "lla_decode", "lla_decode_max_n", "decode",
     "LLA_OK", "LLA_ERR_INVALID_ARG", "LLA_ERR_UNSUPPORTED", "LLA_ERR_CUDA", "LLA_ERR_DEVICE_TIMEOUT",
     "LLA_DTYPE_BF16", "LLA_DTYPE_FP32", "LLA_PATH_AUTO", "LLA_PATH_TENSOR", "LLA_PATH_FP32",
     "EXPORTED_SYMBOLS",
@@ -44,6 +45,9 @@ _SIGNATURES = {
                                      _c_float, _c_int, _c_float, _vp]),
     "lla_parallax_forward": (_c_int, [_c_int, _c_int, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                       _c_float, _vp, _c_size, _vp]),
+    "lla_decode": (_c_int, [_c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
+                            _c_float, _c_float, _c_int, _c_float, _vp]),
+    "lla_decode_max_n": (_c_int, [_c_int]),
     "lla_profile_enable": (_c_int, [_c_int]),
     "lla_profile_read": (_c_int, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]),
     "lla_version": (_c_int, []),
@@ -152,6 +156,51 @@ def lla_parallax_forward(dtype, path, q_ptr, k_ptr, v_ptr, probe_ptr, out_ptr, B
     """Raw Parallax-form entry point on device pointers (ints); raises LLAError on failure."""
     _check(load_library().lla_parallax_forward(dtype, path, q_ptr, k_ptr, v_ptr, probe_ptr, out_ptr, B, H, n, d, tau,
                                                ws_ptr, ws_bytes, stream_ptr))
+
+
+def lla_decode(dtype, q_ptr, k_ptr, v_ptr, out_ptr, rho_ptr, denom_ptr, iters_ptr, B, H, n, n_cap, d, tau, lam,
+               cg_max_iters, cg_tol, stream_ptr):
+    """Raw decode-step entry point on device pointers (ints); raises LLAError on failure."""
+    _check(load_library().lla_decode(dtype, q_ptr, k_ptr, v_ptr, out_ptr, rho_ptr, denom_ptr, iters_ptr, B, H, n,
+                                     n_cap, d, tau, lam, cg_max_iters, cg_tol, stream_ptr))
+
+
+def lla_decode_max_n(d):
+    return load_library().lla_decode_max_n(d)
+
+
+def decode(q, k_cache, v_cache, n, tau, lam, cg_max_iters, cg_tol=0.0, *, return_iters=False, out=None, rho=None,
+           denom=None, stream=None):
+    """One decode step: q [B, H, d] against caches [B, H, n_cap, d] whose first n rows are valid.
+
+    Returns (out [B, H, d], rho [B, H, d] fp32, denom [B, H] fp32) and, with return_iters, the
+    CG iteration counts [B, H].  Equals row n-1 of forward() on the cached sequence.
+    """
+    import torch
+    if not (q.is_cuda and k_cache.is_cuda and v_cache.is_cuda):
+        raise LLAError(LLA_ERR_INVALID_ARG, "q and the caches must be CUDA tensors (there is no CPU path)")
+    if q.dim() != 3 or k_cache.dim() != 4 or k_cache.shape != v_cache.shape or \
+            tuple(k_cache.shape[:2]) != tuple(q.shape[:2]) or k_cache.shape[3] != q.shape[2]:
+        raise LLAError(LLA_ERR_INVALID_ARG, f"q [B, H, d] and caches [B, H, n_cap, d] expected, got {tuple(q.shape)}, "
+                                            f"{tuple(k_cache.shape)}, {tuple(v_cache.shape)}")
+    if not (q.dtype == k_cache.dtype == v_cache.dtype) or q.dtype not in (torch.bfloat16, torch.float32):
+        raise LLAError(LLA_ERR_INVALID_ARG, "q and the caches must all be bf16 or all fp32")
+    q, k_cache, v_cache = q.contiguous(), k_cache.contiguous(), v_cache.contiguous()
+    B, H, n_cap, d = k_cache.shape
+    dtype = LLA_DTYPE_BF16 if q.dtype == torch.bfloat16 else LLA_DTYPE_FP32
+    if out is None:
+        out = torch.empty_like(q)
+    if rho is None:
+        rho = torch.empty((B, H, d), dtype=torch.float32, device=q.device)
+    if denom is None:
+        denom = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    iters = torch.empty((B, H), dtype=torch.int32, device=q.device) if return_iters else None
+    lla_decode(dtype, q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(), rho.data_ptr(),
+               denom.data_ptr(), None if iters is None else iters.data_ptr(), B, H, int(n), n_cap, d, float(tau),
+               float(lam), int(cg_max_iters), float(cg_tol), _stream_ptr(stream))
+    if return_iters:
+        return out, rho, denom, iters
+    return out, rho, denom
 
 
 def _check_qkv(q, k, v):

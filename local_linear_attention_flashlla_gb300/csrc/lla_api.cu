@@ -119,6 +119,9 @@ static int run_problem(Problem& p, int rpath, void* workspace, size_t workspace_
 using lla::fail;
 using lla::aligned16;
 
+// Dynamic shared memory a block may have on sm_103a (227 KB).
+#define LLA_DECODE_SMEM_LIMIT 232448
+
 extern "C" {
 
 int lla_version(void) { return 10000; }
@@ -210,6 +213,58 @@ int lla_parallax_forward(int dtype, int path, const void* q, const void* k, cons
     lla::Problem p{q, k, v, out, nullptr, nullptr, nullptr, B, H, n, d, tau, 1.f, 0, 0.f, dtype,
                    nullptr, nullptr, probe};
     return lla::run_problem(p, rpath, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+int lla_decode(int dtype, const void* q, const void* k, const void* v, void* out, float* rho, float* denom,
+               int* cg_iters, int B, int H, int n, int n_cap, int d, float tau, float lambda, int cg_max_iters,
+               float cg_tol, void* stream_) {
+    lla::g_msg[0] = '\0';
+    if (!q || !k || !v || !out || !rho || !denom) return fail(LLA_ERR_INVALID_ARG, "null tensor pointer");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(rho) ||
+        !aligned16(denom))
+        return fail(LLA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    if (B < 1 || H < 1 || n < 1) return fail(LLA_ERR_INVALID_ARG, "B, H, n must be >= 1 (got %d, %d, %d)", B, H, n);
+    if (n_cap < n) return fail(LLA_ERR_INVALID_ARG, "cache capacity n_cap (%d) must be >= n (%d)", n_cap, n);
+    if ((long long)B * H > (1LL << 31) - 1) return fail(LLA_ERR_INVALID_ARG, "B*H too large");
+    if ((long long)B * H * n_cap * d > (1LL << 40)) return fail(LLA_ERR_INVALID_ARG, "problem too large");
+    if (d != 16 && d != 32 && d != 64 && d != 128)
+        return fail(LLA_ERR_INVALID_ARG, "head dim d must be 16, 32, 64 or 128 (got %d)", d);
+    if (!(tau > 0.f) || !(tau < 1e30f)) return fail(LLA_ERR_INVALID_ARG, "tau must be finite and > 0");
+    if (!(lambda > 0.f) || !(lambda < 1e30f)) return fail(LLA_ERR_INVALID_ARG, "lambda must be finite and > 0");
+    if (cg_max_iters < 1 || cg_max_iters > 4096) return fail(LLA_ERR_INVALID_ARG, "cg_max_iters must be in [1, 4096]");
+    if (!(cg_tol >= 0.f) || !(cg_tol < 1e30f)) return fail(LLA_ERR_INVALID_ARG, "cg_tol must be finite and >= 0");
+    if (dtype != LLA_DTYPE_BF16 && dtype != LLA_DTYPE_FP32) return fail(LLA_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+    if (lla::decode_smem_bytes(n, d) > (size_t)LLA_DECODE_SMEM_LIMIT)
+        return fail(LLA_ERR_UNSUPPORTED, "decode keeps the n weights in shared memory: n = %d is above the limit %d",
+                    n, lla_decode_max_n(d));
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    lla::DecodeProblem p{q, k, v, out, rho, denom, cg_iters, B, H, n, n_cap, d, tau, lambda, cg_max_iters, cg_tol,
+                         dtype, nullptr, nullptr};
+    if (lla::g_prof_on) {
+        for (int i = 0; i < 4; ++i)
+            if (!lla::g_ev[i]) {
+                cudaError_t e = cudaEventCreate(&lla::g_ev[i]);
+                if (e != cudaSuccess) return lla::cuda_fail(e, "profiling event");
+            }
+        p.ev_main_begin = lla::g_ev[1];
+        p.ev_main_end = lla::g_ev[2];
+        cudaError_t e = cudaEventRecord(lla::g_ev[0], stream);
+        if (e != cudaSuccess) return lla::cuda_fail(e, "profiling event record");
+    }
+    cudaError_t e = lla::launch_decode(p, stream);
+    if (e != cudaSuccess) return lla::cuda_fail(e, "decode launch");
+    if (lla::g_prof_on) {
+        e = cudaEventRecord(lla::g_ev[3], stream);
+        if (e != cudaSuccess) return lla::cuda_fail(e, "profiling event record");
+        lla::g_prof_valid = true;
+    }
+    return LLA_OK;
+}
+
+int lla_decode_max_n(int d) {
+    if (d != 16 && d != 32 && d != 64 && d != 128) return 0;
+    const size_t base = lla::decode_smem_bytes(0, d);
+    return (int)(((size_t)LLA_DECODE_SMEM_LIMIT - base) / sizeof(float));
 }
 
 int lla_sync_status(void* stream) {

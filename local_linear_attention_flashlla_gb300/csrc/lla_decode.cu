@@ -1,0 +1,365 @@
+// Decode step of causal LLA: one new query per (b, h) against its key/value cache.
+//
+// The query at position n-1 sees every cached key j <= n-1, so the step is row n-1 of the
+// forward pass (Local Linear Attention reading notes, section 2.1, Eqs. (6)-(8); section 2.2:
+// "a KV cache of size Theta(n d)").  Per (b, h) it runs the FlashLLA phases over the cache:
+//   (1) one pass over K: logits s_j = tau q.k_j with an online maximum, the weights kept in
+//       shared memory, omega = sum_j w_j and mu~ = sum_j w_j k_j (rescaled as the maximum grows);
+//   (2) conjugate gradient on the centred system (C/omega) rho' = delta, delta = kbar - q, one
+//       pass over K per iteration: a_j = p.k_j, M_j = w_j (a_j - kbar.p), Y = sum_j M_j k_j,
+//       (C/omega) p = (Y - kbar sum_j M_j)/omega + (lambda/omega) p;
+//   (3) rho = rho'/(1 + delta.rho'), denom = omega/(1 + delta.rho') and one pass over K and V:
+//       out = sum_j u_j v_j / sum_j u_j, u_j = w_j (1 - (k_j - kbar).rho').
+// Every product, sum and CG quantity is fp32.
+//
+// With one query row the work per key is two length-d dot/axpy products per pass: the step is
+// bound by reading the cache (K once per pass, V once), so it runs on CUDA cores, not tensor
+// cores.  One CTA of 256 threads per (b, h): 32 groups of 8 lanes; group g takes keys
+// j = g, g+32, ...; lane l of a group holds coordinates l*D/8 .. l*D/8 + D/8-1, so a group reads
+// a key row as one contiguous segment and reduces its dot products with 3 shuffles.  Weights
+// live in shared memory (n floats).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "lla_internal.h"
+
+namespace lla {
+namespace {
+
+constexpr int DT = 256;              // threads per CTA
+constexpr int NG = DT / 8;           // key groups
+
+__device__ __forceinline__ float ldf(const float* p) { return *p; }
+__device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void stf(float* p, float x) { *p = x; }
+__device__ __forceinline__ void stf(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+
+// E consecutive elements of a row (E = D/8: 2, 4, 8 or 16) as floats, in the widest aligned
+// vector loads (the segment starts at an element index that is a multiple of E).
+template <int E>
+__device__ __forceinline__ void load_seg(const float* p, float (&o)[E]) {
+    if constexpr (E % 4 == 0) {
+#pragma unroll
+        for (int c = 0; c < E; c += 4) {
+            const float4 t = *reinterpret_cast<const float4*>(p + c);
+            o[c] = t.x; o[c + 1] = t.y; o[c + 2] = t.z; o[c + 3] = t.w;
+        }
+    } else {
+        const float2 t = *reinterpret_cast<const float2*>(p);
+        o[0] = t.x; o[1] = t.y;
+    }
+}
+template <int E>
+__device__ __forceinline__ void load_seg(const __nv_bfloat16* p, float (&o)[E]) {
+    if constexpr (E % 8 == 0) {
+#pragma unroll
+        for (int c = 0; c < E; c += 8) {
+            const uint4 t = *reinterpret_cast<const uint4*>(p + c);
+            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&t);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 f = __bfloat1622float2(h[u]);
+                o[c + 2 * u] = f.x; o[c + 2 * u + 1] = f.y;
+            }
+        }
+    } else if constexpr (E == 4) {
+        const uint2 t = *reinterpret_cast<const uint2*>(p);
+        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&t);
+        const float2 a = __bfloat1622float2(h[0]), b = __bfloat1622float2(h[1]);
+        o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
+    } else {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+        o[0] = f.x; o[1] = f.y;
+    }
+}
+
+__device__ __forceinline__ float group_sum(float x) {   // over the 8 lanes of a group
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    x += __shfl_xor_sync(0xffffffffu, x, 2);
+    x += __shfl_xor_sync(0xffffffffu, x, 4);
+    return x;
+}
+
+template <int D>
+struct DecSmem {
+    float part[NG][D];      // per-group partial vectors (Y, mu~, O)
+    float gs[NG][4];        // per-group partial scalars
+    float q[D], kbar[D], delta[D], x[D], r[D], p[D], cp[D];
+    float red[DT / 32][4];  // warp partials of block reductions
+    float bc[8];            // broadcast scalars
+};
+
+// Sum of v over the block (every thread passes its value; every thread gets the total).
+template <int D>
+__device__ __forceinline__ float block_sum(DecSmem<D>& sm, float v, int slot) {
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0) sm.red[threadIdx.x >> 5][slot] = v;
+    __syncthreads();
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < DT / 32; ++w) t += sm.red[w][slot];
+    __syncthreads();
+    return t;
+}
+
+// Column sums of part[NG][D] into dst[D] (thread t sums column t; D <= DT).
+template <int D>
+__device__ __forceinline__ void reduce_parts(DecSmem<D>& sm, float* dst) {
+    __syncthreads();
+    if (threadIdx.x < D) {
+        float t = 0.f;
+#pragma unroll 8
+        for (int g = 0; g < NG; ++g) t += sm.part[g][threadIdx.x];
+        dst[threadIdx.x] = t;
+    }
+    __syncthreads();
+}
+
+template <int D, typename T>
+__global__ void __launch_bounds__(DT)
+lla_decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, T* __restrict__ out,
+                  float* __restrict__ rho, float* __restrict__ denom, int* __restrict__ cg_iters, int n, int n_cap,
+                  float tau, float lambda, int cg_max_iters, float cg_tol) {
+    constexpr int E = D / 8;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    DecSmem<D>& sm = *reinterpret_cast<DecSmem<D>*>(smem_raw);
+    float* wts = reinterpret_cast<float*>(smem_raw + sizeof(DecSmem<D>));   // n weights
+
+    const size_t head = blockIdx.x;
+    const T* kh = k + head * (size_t)n_cap * D;
+    const T* vh = v + head * (size_t)n_cap * D;
+    const int tid = threadIdx.x, g = tid >> 3, l8 = tid & 7;
+    const int c0 = l8 * E;                          // first coordinate of this lane
+
+    if (tid < D) sm.q[tid] = ldf(q + head * D + tid);
+    __syncthreads();
+    float qv[E];
+#pragma unroll
+    for (int c = 0; c < E; ++c) qv[c] = sm.q[c0 + c];
+
+    // ---- (1) logits, online maximum, omega and mu~ in one pass ----------------------------
+    float mg = -INFINITY, og = 0.f, acc[E];
+#pragma unroll
+    for (int c = 0; c < E; ++c) acc[c] = 0.f;
+    // Every group runs the same number of iterations (the shuffles inside need all 32 lanes of
+    // the warp); a group whose key is past the end does no work in that iteration.
+    const int n_it = (n + NG - 1) / NG;
+    for (int it = 0; it < n_it; ++it) {
+        const int j = it * NG + g;
+        const bool valid = j < n;
+        float kv[E];
+        if (valid) load_seg<E>(kh + (size_t)j * D + c0, kv);
+        else {
+#pragma unroll
+            for (int c = 0; c < E; ++c) kv[c] = 0.f;
+        }
+        float s = 0.f;
+#pragma unroll
+        for (int c = 0; c < E; ++c) s = fmaf(qv[c], kv[c], s);
+        s = tau * group_sum(s);
+        if (!valid) continue;
+        if (l8 == 0) wts[j] = s;                    // logit for now; weight after the pass
+        if (s > mg) {                               // rescale this group's sums to the new maximum
+            const float f = expf(mg - s);
+            og *= f;
+#pragma unroll
+            for (int c = 0; c < E; ++c) acc[c] *= f;
+            mg = s;
+        }
+        const float w = expf(s - mg);
+        og += w;
+#pragma unroll
+        for (int c = 0; c < E; ++c) acc[c] = fmaf(w, kv[c], acc[c]);
+    }
+    if (l8 == 0) sm.gs[g][0] = mg;
+    __syncthreads();
+    float m = -INFINITY;
+#pragma unroll 8
+    for (int t = 0; t < NG; ++t) m = fmaxf(m, sm.gs[t][0]);
+    {
+        const float f = (mg == -INFINITY) ? 0.f : expf(mg - m);   // groups that saw no key add 0
+#pragma unroll
+        for (int c = 0; c < E; ++c) sm.part[g][c0 + c] = acc[c] * f;
+        if (l8 == 0) sm.gs[g][1] = og * f;
+    }
+    __syncthreads();
+    for (int j = tid; j < n; j += DT) wts[j] = expf(wts[j] - m);
+    float omega = 0.f;
+#pragma unroll 8
+    for (int t = 0; t < NG; ++t) omega += sm.gs[t][1];
+    reduce_parts<D>(sm, sm.kbar);                   // mu~ for now
+    const float inv_om = 1.f / omega;
+    if (tid < D) {
+        const float kb = sm.kbar[tid] * inv_om;
+        sm.kbar[tid] = kb;
+        sm.delta[tid] = kb - sm.q[tid];
+        sm.x[tid] = 0.f;
+        sm.r[tid] = sm.delta[tid];
+        sm.p[tid] = sm.delta[tid];
+    }
+    __syncthreads();
+
+    // ---- (2) CG on (C/omega) rho' = delta -------------------------------------------------------
+    float gamma = block_sum<D>(sm, tid < D ? sm.r[tid] * sm.r[tid] : 0.f, 0);
+    const float rn0 = sqrtf(gamma);
+    bool active = gamma > 0.f && !(rn0 <= cg_tol * rn0);
+    int iters = 0;
+    const float lam_n = lambda * inv_om;
+    float kbv[E];
+#pragma unroll
+    for (int c = 0; c < E; ++c) kbv[c] = sm.kbar[c0 + c];
+    for (int it = 0; it < cg_max_iters && active; ++it) {   // active is uniform over the block
+        float pv[E];
+#pragma unroll
+        for (int c = 0; c < E; ++c) pv[c] = sm.p[c0 + c];
+        float kp = 0.f;
+#pragma unroll
+        for (int c = 0; c < E; ++c) kp = fmaf(kbv[c], pv[c], kp);
+        kp = group_sum(kp);
+        float ms = 0.f;
+#pragma unroll
+        for (int c = 0; c < E; ++c) acc[c] = 0.f;
+        for (int it2 = 0; it2 < n_it; ++it2) {
+            const int j = it2 * NG + g;
+            const bool valid = j < n;
+            float kv[E];
+            if (valid) load_seg<E>(kh + (size_t)j * D + c0, kv);
+            else {
+#pragma unroll
+                for (int c = 0; c < E; ++c) kv[c] = 0.f;
+            }
+            float a = 0.f;
+#pragma unroll
+            for (int c = 0; c < E; ++c) a = fmaf(pv[c], kv[c], a);
+            a = group_sum(a);
+            const float mm = valid ? wts[j] * (a - kp) : 0.f;
+            ms += mm;
+#pragma unroll
+            for (int c = 0; c < E; ++c) acc[c] = fmaf(mm, kv[c], acc[c]);
+        }
+#pragma unroll
+        for (int c = 0; c < E; ++c) sm.part[g][c0 + c] = acc[c];
+        if (l8 == 0) sm.gs[g][2] = ms;
+        reduce_parts<D>(sm, sm.cp);                 // Y
+        float msum = 0.f;
+#pragma unroll 8
+        for (int t = 0; t < NG; ++t) msum += sm.gs[t][2];
+        float pcp_part = 0.f;
+        if (tid < D) {
+            const float cpv = (sm.cp[tid] - sm.kbar[tid] * msum) * inv_om + lam_n * sm.p[tid];
+            sm.cp[tid] = cpv;
+            pcp_part = sm.p[tid] * cpv;
+        }
+        const float pcp = block_sum<D>(sm, pcp_part, 1);
+        if (!(pcp > 0.f)) break;                    // no positive curvature left (uniform)
+        const float alpha = gamma / pcp;
+        float g2_part = 0.f;
+        if (tid < D) {
+            sm.x[tid] = fmaf(alpha, sm.p[tid], sm.x[tid]);
+            const float rv = fmaf(-alpha, sm.cp[tid], sm.r[tid]);
+            sm.r[tid] = rv;
+            g2_part = rv * rv;
+        }
+        const float g2 = block_sum<D>(sm, g2_part, 2);
+        const float beta = g2 / gamma;
+        gamma = g2;
+        ++iters;
+        if (tid < D) sm.p[tid] = fmaf(beta, sm.p[tid], sm.r[tid]);
+        __syncthreads();
+        if (gamma == 0.f || sqrtf(gamma) <= cg_tol * rn0) active = false;
+    }
+
+    // ---- (3) finalise and output pass -------------------------------------------------------------
+    const float dx = block_sum<D>(sm, tid < D ? sm.delta[tid] * sm.x[tid] : 0.f, 0);
+    const float kx = block_sum<D>(sm, tid < D ? sm.kbar[tid] * sm.x[tid] : 0.f, 1);
+    float xv[E];
+#pragma unroll
+    for (int c = 0; c < E; ++c) xv[c] = sm.x[c0 + c];
+    const float c1 = 1.f + kx;
+    float us = 0.f;
+#pragma unroll
+    for (int c = 0; c < E; ++c) acc[c] = 0.f;
+    for (int it = 0; it < n_it; ++it) {
+        const int j = it * NG + g;
+        const bool valid = j < n;
+        float kv[E], vv[E];
+        if (valid) {
+            load_seg<E>(kh + (size_t)j * D + c0, kv);
+            load_seg<E>(vh + (size_t)j * D + c0, vv);
+        } else {
+#pragma unroll
+            for (int c = 0; c < E; ++c) kv[c] = vv[c] = 0.f;
+        }
+        float t = 0.f;
+#pragma unroll
+        for (int c = 0; c < E; ++c) t = fmaf(xv[c], kv[c], t);
+        t = group_sum(t);
+        const float u = valid ? wts[j] * (c1 - t) : 0.f;
+        us += u;
+#pragma unroll
+        for (int c = 0; c < E; ++c) acc[c] = fmaf(u, vv[c], acc[c]);
+    }
+#pragma unroll
+    for (int c = 0; c < E; ++c) sm.part[g][c0 + c] = acc[c];
+    if (l8 == 0) sm.gs[g][3] = us;
+    reduce_parts<D>(sm, sm.cp);                     // O
+    float usum = 0.f;
+#pragma unroll 8
+    for (int t = 0; t < NG; ++t) usum += sm.gs[t][3];
+    if (tid < D) {
+        const float inv_g = 1.f / (1.f + dx);
+        stf(out + head * D + tid, sm.cp[tid] / usum);
+        rho[head * D + tid] = sm.x[tid] * inv_g;
+        if (tid == 0) {
+            denom[head] = omega * inv_g;
+            if (cg_iters) cg_iters[head] = iters;
+        }
+    }
+}
+
+template <int D, typename T>
+cudaError_t launch_dec(const DecodeProblem& p, cudaStream_t stream) {
+    const size_t smem = sizeof(DecSmem<D>) + (size_t)p.n * sizeof(float);
+    auto kern = lla_decode_kernel<D, T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (p.ev_main_begin && (e = cudaEventRecord(p.ev_main_begin, stream)) != cudaSuccess) return e;
+    kern<<<p.B * p.H, DT, smem, stream>>>(static_cast<const T*>(p.q), static_cast<const T*>(p.k),
+                                          static_cast<const T*>(p.v), static_cast<T*>(p.out), p.rho, p.denom,
+                                          p.cg_iters, p.n, p.n_cap, p.tau, p.lambda, p.cg_max_iters, p.cg_tol);
+    e = cudaGetLastError();
+    if (e == cudaSuccess && p.ev_main_end) e = cudaEventRecord(p.ev_main_end, stream);
+    return e;
+}
+
+template <typename T>
+cudaError_t launch_dec_dim(const DecodeProblem& p, cudaStream_t stream) {
+    switch (p.d) {
+        case 16: return launch_dec<16, T>(p, stream);
+        case 32: return launch_dec<32, T>(p, stream);
+        case 64: return launch_dec<64, T>(p, stream);
+        case 128: return launch_dec<128, T>(p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+size_t decode_smem_bytes(int n, int d) {
+    size_t base = 0;
+    switch (d) {
+        case 16: base = sizeof(DecSmem<16>); break;
+        case 32: base = sizeof(DecSmem<32>); break;
+        case 64: base = sizeof(DecSmem<64>); break;
+        default: base = sizeof(DecSmem<128>); break;
+    }
+    return base + (size_t)n * sizeof(float);
+}
+
+cudaError_t launch_decode(const DecodeProblem& p, cudaStream_t stream) {
+    if (p.dtype == 1) return launch_dec_dim<float>(p, stream);
+    return launch_dec_dim<__nv_bfloat16>(p, stream);
+}
+
+}  // namespace lla

@@ -32,6 +32,25 @@ struct Problem {
 // tensor kernel found its dynamic shared memory misaligned and did no work).
 enum DeviceError : unsigned { kDevErrMbarTimeout = 1u, kDevErrSmemAlign = 2u };
 
+// Decode step: one new query per (b, h) against a key/value cache of n rows (row stride n_cap).
+struct DecodeProblem {
+    const void* q;       // [B,H,d]
+    const void* k;       // [B,H,n_cap,d], rows 0..n-1 valid
+    const void* v;
+    void* out;           // [B,H,d]
+    float* rho;          // [B,H,d]
+    float* denom;        // [B,H]
+    int* cg_iters;       // [B,H] or null
+    int B, H, n, n_cap, d;
+    float tau, lambda;
+    int cg_max_iters;
+    float cg_tol;
+    int dtype;           // lla_dtype
+    cudaEvent_t ev_main_begin, ev_main_end;
+};
+size_t decode_smem_bytes(int n, int d);
+cudaError_t launch_decode(const DecodeProblem& p, cudaStream_t stream);
+
 // fp32 CUDA-core path (any d in {16,32,64,128}, fp32 or bf16 inputs).
 cudaError_t launch_simt(const Problem& p, cudaStream_t stream);
 

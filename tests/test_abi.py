@@ -103,3 +103,28 @@ def test_parallax_binding_refuses_cpu_tensors():
     x = torch.zeros(1, 1, 4, 16)
     with pytest.raises(lla.LLAError):
         lla.parallax_forward(x, x, x, x, 0.25)
+
+
+def _call_decode(lib, **kw):
+    a = dict(dtype=0, q=16, k=32, v=48, out=64, rho=80, den=96, it=None, B=1, H=1, n=8, n_cap=8, d=64, tau=0.1,
+             lam=1.0, T=4, tol=0.0, stream=None)
+    a.update(kw)
+    return lib.lla_decode(a["dtype"], a["q"], a["k"], a["v"], a["out"], a["rho"], a["den"], a["it"], a["B"], a["H"],
+                          a["n"], a["n_cap"], a["d"], a["tau"], a["lam"], a["T"], a["tol"], a["stream"])
+
+
+@pytest.mark.parametrize("bad", [
+    dict(q=None), dict(k=None), dict(rho=None), dict(den=None), dict(v=40), dict(B=0), dict(n=0), dict(n_cap=7),
+    dict(d=48), dict(tau=0.0), dict(lam=-1.0), dict(T=0), dict(tol=float("nan")), dict(dtype=3),
+])
+def test_decode_invalid_arguments_rejected_before_launch(lib, bad):
+    assert _call_decode(lib, **bad) == lla.LLA_ERR_INVALID_ARG
+    assert lib.lla_last_error().decode()
+
+
+def test_decode_cache_length_limit(lib):
+    for d in (16, 32, 64, 128):
+        m = lib.lla_decode_max_n(d)
+        assert 32768 <= m < 60000
+        assert _call_decode(lib, d=d, n=m + 1, n_cap=m + 1) == lla.LLA_ERR_UNSUPPORTED
+    assert lib.lla_decode_max_n(48) == 0

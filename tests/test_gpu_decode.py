@@ -1,0 +1,106 @@
+"""Decode step (one new query per (b, h) against a key/value cache) through the C ABI.
+
+The step is row n-1 of the forward pass on the cached sequence, so the float64 oracle is the
+LLA definition at that row.  Gates, per (b, h):
+* CG run to convergence (relative residual 1e-6, fp32 arithmetic throughout): out within
+  2^-8 |ref| + 1e-4 RMS(v) element by element (the first term covers the bf16 rounding of the
+  output for bf16 caches; it is 0-width for fp32), rho within 2e-4 of RMS(ref rho), denom within
+  2e-4 relative;
+* at the LM configuration's fixed cap T = 16 the reference is the oracle's float64 run of the
+  same centred CG for 16 iterations (truncation is part of the definition being compared), with
+  the same bounds as the fp32 forward path at a fixed cap on converged rows.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import local_linear_attention_flashlla_gb300 as lla
+from local_linear_attention_flashlla_gb300.inputs import make_inputs, workload
+from oracle.lla_ref import lla_row, lla_row_deflated_cg
+
+pytestmark = pytest.mark.gpu
+
+
+def _decode(w, n_cap=None, tol=None, iters=None):
+    q, k, v = make_inputs(w)                     # [B, H, n, d]; the last row is the new token
+    n = w.n
+    n_cap = n if n_cap is None else n_cap
+    dev = torch.device("cuda:0")
+    kc = torch.zeros((w.B, w.H, n_cap, w.d), dtype=k.dtype)
+    vc = torch.zeros_like(kc)
+    kc[:, :, :n] = k
+    vc[:, :, :n] = v
+    if n_cap > n:                                # rows past n must not be read
+        kc[:, :, n:] = float("nan")
+        vc[:, :, n:] = float("nan")
+    res = lla.decode(q[:, :, n - 1].to(dev), kc.to(dev), vc.to(dev), n, w.tau, w.lam,
+                     w.cg_max_iters if iters is None else iters, w.cg_tol if tol is None else tol, return_iters=True)
+    torch.cuda.synchronize()
+    lla.lla_sync_status()
+    return (q, k, v), [t.cpu() for t in res]
+
+
+def _gate(w, qkv, res, ref_fn):
+    q, k, v = (t.double().numpy() for t in qkv)
+    out, rho, den, its = (t.double().numpy() for t in res)
+    rms_v = math.sqrt(float(np.mean(v ** 2)))
+    n = w.n
+    for b in range(w.B):
+        for h in range(w.H):
+            r = ref_fn(q[b, h, n - 1], k[b, h, :n], v[b, h, :n])
+            diff = np.abs(out[b, h] - r["out"])
+            assert (diff <= 2.0 ** -8 * np.abs(r["out"]) * (w.dtype == "bf16") + 1e-4 * rms_v).all(), \
+                f"out err {diff.max() / rms_v:.3e} RMS(v) at {(b, h)}"
+            rms_rho = math.sqrt(float(np.mean(r["rho"] ** 2))) or 1.0
+            assert np.abs(rho[b, h] - r["rho"]).max() <= 2e-4 * rms_rho
+            assert abs(den[b, h] - r["denom"]) <= 2e-4 * abs(r["denom"])
+    assert (its <= w.cg_max_iters).all()
+
+
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
+@pytest.mark.parametrize("n", [1, 7, 33, 300])
+def test_decode_converged_matches_exact_solve(lla_gpu, dtype, d, n):
+    w = workload("lm_bf16", B=2, H=3, n=n, d=d, dtype=dtype, tau=1.0 / math.sqrt(d), cg_max_iters=4 * d + 64,
+                 cg_tol=1e-6)
+    qkv, res = _decode(w)
+    _gate(w, qkv, res, lambda qi, K, V: lla_row(qi, K, V, w.tau, w.lam))
+
+
+def test_decode_reads_only_the_valid_cache_rows(lla_gpu):
+    """n_cap > n: rows past n hold NaN and must not reach the result."""
+    w = workload("lm_bf16", B=2, H=2, n=200, d=128, tau=1.0 / math.sqrt(128), cg_max_iters=300, cg_tol=1e-6)
+    qkv, res = _decode(w, n_cap=333)
+    assert all(np.isfinite(t.double().numpy()).all() for t in res[:3])
+    _gate(w, qkv, res, lambda qi, K, V: lla_row(qi, K, V, w.tau, w.lam))
+
+
+def test_decode_at_the_lm_cap_matches_the_same_cg(lla_gpu):
+    """T = 16, tolerance 0 (the LM configuration): reference = float64 centred CG, 16 iterations."""
+    w = workload("lm_bf16", B=2, H=4, n=2048, d=128)
+    qkv, res = _decode(w)
+    q, k, v = (t.double().numpy() for t in qkv)
+    out = res[0].double().numpy()
+    rms_v = math.sqrt(float(np.mean(v ** 2)))
+    n = w.n
+    for b in range(w.B):
+        for h in range(w.H):
+            r = lla_row_deflated_cg(q[b, h, n - 1], k[b, h, :n], v[b, h, :n], w.tau, w.lam, 16, 0.0)
+            diff = np.abs(out[b, h] - r["out"])
+            assert (diff <= 2.0 ** -8 * np.abs(r["out"]) + 1e-3 * rms_v).all(), f"{diff.max() / rms_v:.3e}"
+    assert (res[3].numpy() == 16).all()
+
+
+def test_decode_equals_forward_last_row(lla_gpu):
+    """The step is the forward pass's row n-1: both fp32 GPU paths, same T, same inputs."""
+    w = workload("lm_bf16", B=2, H=2, n=500, d=64, tau=0.125, cg_max_iters=200, cg_tol=1e-6)
+    qkv, res = _decode(w)
+    dev = torch.device("cuda:0")
+    o, r, d_, _ = lla.forward(*(t.to(dev) for t in qkv), w.tau, w.lam, w.cg_max_iters, w.cg_tol,
+                              path=lla.LLA_PATH_FP32, return_iters=True)
+    torch.cuda.synchronize()
+    rms_v = math.sqrt(float(qkv[2].double().pow(2).mean()))
+    diff = (res[0].double() - o[:, :, -1].cpu().double()).abs()
+    assert float(diff.max()) <= 2.0 ** -7 * float(o[:, :, -1].abs().max()) + 1e-4 * rms_v
