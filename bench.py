@@ -32,6 +32,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "causal LLA fwd tokens/s & TFLOP/s at d=128 bf16; fraction of BF16 tensor peak"
+METRIC_DECODE = "LLA decode step tokens/s (one token per sequence) and HBM GB/s at d=128 bf16; fraction of HBM peak"
 METRIC_PARALLAX = "causal Parallax-form fwd (caller probe) tokens/s & TFLOP/s at d=128 bf16; fraction of BF16 tensor peak"
 
 
@@ -223,8 +224,9 @@ def parse():
     ap.add_argument("--path", choices=["auto", "tensor", "fp32"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--op", choices=["lla", "parallax"], default="lla",
-                    help="lla: the LLA forward (default); parallax: the Parallax form with a synthetic probe")
+    ap.add_argument("--op", choices=["lla", "parallax", "decode"], default="lla",
+                    help="lla: the LLA forward (default); parallax: the Parallax form with a synthetic probe; "
+                         "decode: one decode step (use --workload decode_bf16)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch B (a smaller case for profiler captures)")
     return ap.parse_args()
@@ -246,6 +248,9 @@ def dist_setup(args):
 
 def run_reference(args, world, rank):
     if rank != 0:
+        return
+    if args.op == "decode":
+        run_reference_decode(args)
         return
     from local_linear_attention_flashlla_gb300.inputs import make_inputs, make_probe, workload
     w = workload(args.workload) if args.batch is None else workload(args.workload, B=args.batch)
@@ -274,11 +279,209 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def decode_bytes(w, T):
+    """(compulsory, method) HBM bytes of one decode step.  Compulsory: the caches, q and the
+    outputs once.  Method: K read in each of the T + 2 passes (moments, T CG iterations, output)
+    and V once, as the three-phase algorithm reads them when the cache does not stay on chip."""
+    e = 2 if w.dtype == "bf16" else 4
+    heads = w.B * w.H
+    cache = heads * w.n * w.d * e
+    small = heads * w.d * (e + e + 4) + heads * 4          # q, out, rho, denom
+    return 2 * cache + small, (T + 2) * cache + cache + small
+
+
+def _decode_oracle_worker(job):
+    q, k, v, tau, lam, rows = job
+    from oracle.lla_ref import lla_row
+    out = []
+    for (b, h) in rows:
+        t0 = time.perf_counter()
+        lla_row(q[b, h], k[b, h], v[b, h], tau, lam)
+        out.append(time.perf_counter() - t0)
+    return out
+
+
+def decode_cpu_baseline(w, qd, k, v, budget_s=12.0, seed=7):
+    """The oracle (exact solve) on a bounded random sample of (b, h) decode rows, all host cores."""
+    import multiprocessing as mp
+
+    import numpy as np
+    from oracle.lla_ref import lla_row
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    cores = os.cpu_count() or 1
+    qn, kn, vn = (t.double().numpy() for t in (qd, k, v))
+    t0 = time.perf_counter()
+    lla_row(qn[0, 0], kn[0, 0], vn[0, 0], w.tau, w.lam)
+    per = max(time.perf_counter() - t0, 1e-4)
+    rng = np.random.default_rng(seed)
+    count = int(max(cores, min(w.B * w.H, 8 * cores, budget_s * cores / per)))
+    rows = [(int(rng.integers(w.B)), int(rng.integers(w.H))) for _ in range(count)]
+    with mp.get_context("spawn").Pool(cores) as pool:
+        t0 = time.perf_counter()
+        res = pool.map(_decode_oracle_worker, [(qn, kn, vn, w.tau, w.lam, rows[c::cores]) for c in range(cores)])
+        wall = time.perf_counter() - t0
+    times = [x for r in res for x in r]
+    eff = min(1.0, sum(times) / (wall * cores))
+    est = w.B * w.H * (sum(times) / len(times)) / (cores * eff)
+    return {"value": w.B / est, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": (f"{len(times)} random (b,h) decode rows of {w.name} solved exactly (float64, dense Sigma, "
+                       f"Cholesky) in {wall:.1f} s on {cores} processes; mean per-row cost times B*H = "
+                       f"{w.B * w.H} rows: est. {est:.1f} s per step")}
+
+
+def run_reference_decode(args):
+    """The oracle as the reference arm of the decode step: bounded samples of (b, h) rows."""
+    from local_linear_attention_flashlla_gb300.inputs import make_inputs, workload
+    name = args.workload if args.workload != "lm_bf16" else "decode_bf16"
+    w = workload(name) if args.batch is None else workload(name, B=args.batch)
+    q, k, v = make_inputs(w)
+    qd = q[:, :, w.n - 1].contiguous()
+    secs, cb = [], None
+    for s_ in range(args.warmup + args.steps):
+        cb = decode_cpu_baseline(w, qd, k, v, budget_s=4.0, seed=2000 + s_)
+        if s_ >= args.warmup:
+            secs.append(w.B / cb["value"])
+    sec = statistics.mean(secs)
+    value = w.B / sec
+    line = {"impl": "reference", "metric": METRIC_DECODE, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{w.name} B={w.B} H={w.H} cache n={w.n} d={w.d} tau={w.tau:.5g} lambda={w.lam} "
+                                   f"cg_iters={w.cg_max_iters} cg_tol={w.cg_tol}", "l2": "n/a (CPU)"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cb["cores"], "kind": "oracle",
+                             "sample": cb["sample"]},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def run_decode(args, world, rank, local):
+    import torch
+
+    import local_linear_attention_flashlla_gb300 as lla
+    from local_linear_attention_flashlla_gb300.inputs import make_inputs, workload
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    name = args.workload if args.workload != "lm_bf16" else "decode_bf16"
+    w = workload(name) if args.batch is None else workload(name, B=args.batch)
+    q, k, v = make_inputs(w.with_(seed=w.seed + rank))
+    qd_host = q[:, :, w.n - 1].contiguous()
+    qd, kc, vc = qd_host.to(dev), k.to(dev), v.to(dev)
+    del q
+    out = torch.empty_like(qd)
+    rho = torch.empty(qd.shape, dtype=torch.float32, device=dev)
+    den = torch.empty(qd.shape[:2], dtype=torch.float32, device=dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    T = w.cg_max_iters
+
+    def step(qq=qd):
+        lla.decode(qq, kc, vc, w.n, w.tau, w.lam, T, w.cg_tol, out=out, rho=rho, denom=den)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    lla.lla_sync_status()
+    lla.lla_profile_enable(True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    times, main_times = [], []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+        main_times.append(lla.lla_profile_read()[0])
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    lla.lla_profile_enable(False)
+    lla.lla_sync_status()
+    total_ms = sum(times)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * w.B * args.steps / (total_ms / 1e3)
+    comp, method = decode_bytes(w, T)
+    kern_ms = sum(main_times) / len(main_times)
+    peaks, peak_kind = load_peaks()
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    achieved = method / (kern_ms / 1e3) / 1e9
+
+    e2e = None
+    if not args.no_e2e:
+        hq = qd_host.pin_memory()
+        ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        hr = torch.empty(rho.shape, dtype=rho.dtype).pin_memory()
+        hd = torch.empty(den.shape, dtype=den.dtype).pin_memory()
+        dq = torch.empty_like(qd)
+        e2e_ms = []
+        for it in range(args.warmup + args.steps):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            dq.copy_(hq, non_blocking=True)          # the new token's query; the cache stays resident
+            step(dq)
+            ho.copy_(out, non_blocking=True)
+            hr.copy_(rho, non_blocking=True)
+            hd.copy_(den, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            if it >= args.warmup:
+                e2e_ms.append(e0.elapsed_time(e1))
+        tot = sum(e2e_ms)
+        if world > 1:
+            t = torch.tensor([tot], dtype=torch.float64, device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            tot = float(t.item())
+        e2e = {"value": world * w.B * len(e2e_ms) / (tot / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": hq.numel() * hq.element_size(),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in (ho, hr, hd))}
+
+    line = {"metric": METRIC_DECODE, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"{w.name} B={w.B} H={w.H} cache n={w.n} d={w.d} tau={w.tau:.5g} lambda={w.lam} "
+                                   f"cg_iters={T} cg_tol={w.cg_tol}", "l2": "flushed before every step (512 MiB write)",
+                       "inputs": f"{w.dtype} caches resident in HBM"},
+            "hbm_gbs": method / (ms_per_step / 1e3) / 1e9,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                         "traffic": None, "peak_source": f"{peak_kind} copy bandwidth",
+                         "bytes_counted": f"method bytes {method} per step: K in each of T+2 passes, V once, q and "
+                                          f"outputs once (compulsory: {comp})"},
+            "clocks": clocks, "e2e": e2e, "gpu_launches": args.steps,
+            "dominant_kernel": {"name": "lla_decode_kernel", "ms_per_launch": kern_ms,
+                                "share_of_step": kern_ms / ms_per_step},
+            "cg_iters_counted": T}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = decode_cpu_baseline(w, qd_host, k, v)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
         run_reference(args, world, rank)
+        return
+    if args.op == "decode":
+        run_decode(args, world, rank, local)
         return
     import numpy as np
     import torch

@@ -23,6 +23,9 @@ Workloads (all causal, [B, H, n, d] row-major):
 * ``long_bf16``        B=1,  H=8,  n=32768, d=128, bf16; generated as ``lm_bf16``.
 * ``illcond_bf16``     B=4,  H=8,  n=8192,  d=64,  bf16; generated as ``lm_bf16``;
                         tau=1/8, lambda in {1e-3, 1e-1, 1e6}, CG to 1e-4 (cap 64).
+* ``decode_bf16``      B=64, H=16, n=4096,  d=128, bf16; generated as ``lm_bf16``; a decode step:
+                        the caches are k, v and the new query is q's last row (64 sequences,
+                        one token each, against 4096 cached positions).
 """
 
 from __future__ import annotations
@@ -65,6 +68,9 @@ WORKLOADS = {
     "lm_bf16": Workload("lm_bf16", 8, 16, 4096, 128, "bf16", "gauss_rmsnorm", 1.0 / math.sqrt(128.0), 1.0, 16, 0.0),
     "long_bf16": Workload("long_bf16", 1, 8, 32768, 128, "bf16", "gauss_rmsnorm", 1.0 / math.sqrt(128.0), 1.0, 16, 0.0),
     "illcond_bf16": Workload("illcond_bf16", 4, 8, 8192, 64, "bf16", "gauss_rmsnorm", 0.125, 1e-1, 64, 1e-4),
+    # decode step: B sequences x H heads, each a cache of n rows (the query is row n-1)
+    "decode_bf16": Workload("decode_bf16", 64, 16, 4096, 128, "bf16", "gauss_rmsnorm", 1.0 / math.sqrt(128.0), 1.0, 16,
+                            0.0),
 }
 
 
