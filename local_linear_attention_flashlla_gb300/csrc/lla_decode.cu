@@ -14,7 +14,9 @@
 //
 // With one query row the work per key is two length-d dot/axpy products per pass: the step is
 // bound by reading the cache (K once per pass, V once), so it runs on CUDA cores, not tensor
-// cores.  One CTA of 256 threads per (b, h): 32 groups of 8 lanes; group g takes keys
+// cores.  Two forms: the streaming form below, and a cluster form (further down) that keeps
+// K in the shared memory of an 8-CTA cluster.  Streaming form: one CTA of 256 threads per
+// (b, h): 32 groups of 8 lanes; group g takes keys
 // j = g, g+32, ...; lane l of a group holds coordinates l*D/8 .. l*D/8 + D/8-1, so a group reads
 // a key row as one contiguous segment and reduces its dot products with 3 shuffles.  Weights
 // live in shared memory (n floats).
@@ -22,12 +24,17 @@
 #include <cuda_runtime.h>
 #include <math.h>
 
+#include <cooperative_groups.h>
+
 #include "lla_internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace lla {
 namespace {
 
 constexpr int DT = 256;              // threads per CTA
+constexpr int kMaxDynSmem = 232448;  // dynamic shared memory a block may have (227 KB)
 constexpr int NG = DT / 8;           // key groups
 
 __device__ __forceinline__ float ldf(const float* p) { return *p; }
@@ -71,6 +78,19 @@ __device__ __forceinline__ void load_seg(const __nv_bfloat16* p, float (&o)[E]) 
     } else {
         const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
         o[0] = f.x; o[1] = f.y;
+    }
+}
+
+// Copy E consecutive elements (a 16-byte multiple for every E used with it).
+template <int E, typename T>
+__device__ __forceinline__ void copy_seg(T* dst, const T* src) {
+    constexpr int N16 = E * (int)sizeof(T) / 16;
+    if constexpr (N16 >= 1) {
+#pragma unroll
+        for (int c = 0; c < N16; ++c) reinterpret_cast<uint4*>(dst)[c] = reinterpret_cast<const uint4*>(src)[c];
+    } else {
+#pragma unroll
+        for (int c = 0; c < E; ++c) dst[c] = src[c];
     }
 }
 
@@ -318,6 +338,274 @@ lla_decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
     }
 }
 
+// ---------------------------------------------------------------------------------------------
+// Cluster form: the cache of one (b, h) is split over the CL CTAs of a thread-block cluster, each
+// holding its slice of K in shared memory for the whole step, so K is read from HBM once instead
+// of once per pass.  Partial sums (the moments, each CG product, the output) are combined through
+// distributed shared memory: every CTA writes its partial to a double-buffered exchange slot,
+// the cluster synchronises once, and every CTA adds the CL slots in rank order, so all CTAs hold
+// bitwise identical CG state and take the same branches without a broadcast.
+constexpr int CL = 8;                // CTAs per cluster (portable cluster size)
+
+template <int D>
+struct ClSmem {
+    DecSmem<D> base;
+    float xbuf[2][D + 4];            // exchange slots: vector partial + up to 4 scalars
+};
+
+template <int D>
+__host__ __device__ constexpr size_t cl_off_w() { return (sizeof(ClSmem<D>) + 15) & ~size_t(15); }
+
+template <int D>
+__device__ __forceinline__ void cl_combine(cg::cluster_group& cl, ClSmem<D>& sm, int slot, float* vec_out,
+                                           float (&sc)[4]) {
+    // all CTAs' slot `slot` is complete after this sync; the read happens before this CTA's next
+    // arrival, which is what a peer's next write to the same slot waits for (two slots in turn)
+    cl.sync();
+    for (int c = threadIdx.x; c < D; c += DT) {
+        float t = 0.f;
+        for (int r = 0; r < CL; ++r) t += cl.map_shared_rank(&sm.xbuf[slot][0], r)[c];
+        vec_out[c] = t;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        float t = 0.f;
+        for (int r = 0; r < CL; ++r) t += cl.map_shared_rank(&sm.xbuf[slot][0], r)[D + u];
+        sc[u] = t;
+    }
+    __syncthreads();
+}
+
+template <int D, typename T>
+__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(DT, 1)
+lla_decode_cluster_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                          T* __restrict__ out, float* __restrict__ rho, float* __restrict__ denom,
+                          int* __restrict__ cg_iters, int n, int n_cap, int S, float tau, float lambda,
+                          int cg_max_iters, float cg_tol) {
+    constexpr int E = D / 8;
+    cg::cluster_group cl = cg::this_cluster();
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    ClSmem<D>& cs = *reinterpret_cast<ClSmem<D>*>(smem_raw);
+    DecSmem<D>& sm = cs.base;
+    float* wts = reinterpret_cast<float*>(smem_raw + cl_off_w<D>());              // S weights
+    T* ks = reinterpret_cast<T*>(smem_raw + cl_off_w<D>() + (size_t)S * sizeof(float));   // S x D keys (S % 4 == 0)
+
+    const int rank = (int)cl.block_rank();
+    const size_t head = blockIdx.x / CL;
+    const int j0 = rank * S;                                  // first key of this CTA's slice
+    const int ns = max(0, min(S, n - j0));                    // keys in the slice
+    const T* kh = k + head * (size_t)n_cap * D;
+    const T* vh = v + head * (size_t)n_cap * D;
+    const int tid = threadIdx.x, g = tid >> 3, l8 = tid & 7;
+    const int c0 = l8 * E;
+    const int n_it = (S + NG - 1) / NG;                       // same trip count in every group
+
+    if (tid < D) sm.q[tid] = ldf(q + head * D + tid);
+    __syncthreads();
+    float qv[E];
+#pragma unroll
+    for (int c = 0; c < E; ++c) qv[c] = sm.q[c0 + c];
+
+    // ---- (1) slice: copy K to shared memory, logits, online maximum, omega and mu~ -------------
+    float mg = -INFINITY, og = 0.f, acc[E];
+#pragma unroll
+    for (int c = 0; c < E; ++c) acc[c] = 0.f;
+    for (int it = 0; it < n_it; ++it) {
+        const int jj = it * NG + g;
+        const bool valid = jj < ns;
+        float kv[E];
+        if (valid) {
+            const T* src = kh + (size_t)(j0 + jj) * D + c0;
+            copy_seg<E>(ks + (size_t)jj * D + c0, src);
+            load_seg<E>(src, kv);
+        } else {
+#pragma unroll
+            for (int c = 0; c < E; ++c) kv[c] = 0.f;
+        }
+        float sv = 0.f;
+#pragma unroll
+        for (int c = 0; c < E; ++c) sv = fmaf(qv[c], kv[c], sv);
+        sv = tau * group_sum(sv);
+        if (!valid) continue;
+        if (l8 == 0) wts[jj] = sv;
+        if (sv > mg) {
+            const float f = expf(mg - sv);
+            og *= f;
+#pragma unroll
+            for (int c = 0; c < E; ++c) acc[c] *= f;
+            mg = sv;
+        }
+        const float w = expf(sv - mg);
+        og += w;
+#pragma unroll
+        for (int c = 0; c < E; ++c) acc[c] = fmaf(w, kv[c], acc[c]);
+    }
+    if (l8 == 0) sm.gs[g][0] = mg;
+    __syncthreads();
+    float m_cta = -INFINITY;
+#pragma unroll 8
+    for (int t = 0; t < NG; ++t) m_cta = fmaxf(m_cta, sm.gs[t][0]);
+    {
+        const float f = (mg == -INFINITY) ? 0.f : expf(mg - m_cta);
+#pragma unroll
+        for (int c = 0; c < E; ++c) sm.part[g][c0 + c] = acc[c] * f;
+        if (l8 == 0) sm.gs[g][1] = og * f;
+    }
+    reduce_parts<D>(sm, sm.cp);
+    float om_cta = 0.f;
+#pragma unroll 8
+    for (int t = 0; t < NG; ++t) om_cta += sm.gs[t][1];
+    // the cluster-wide maximum first (a max, so no rescaling order issue), then the sums
+    if (tid == 0) cs.xbuf[0][D] = m_cta;
+    cl.sync();
+    float m = -INFINITY;
+    for (int r = 0; r < CL; ++r) m = fmaxf(m, cl.map_shared_rank(&cs.xbuf[0][0], r)[D]);
+    const float f_cta = (m_cta == -INFINITY) ? 0.f : expf(m_cta - m);
+    cl.sync();                                                // everyone has read slot 0's maximum
+    for (int c = tid; c < D; c += DT) cs.xbuf[0][c] = sm.cp[c] * f_cta;
+    if (tid == 0) cs.xbuf[0][D] = om_cta * f_cta;
+    for (int jj = tid; jj < ns; jj += DT) wts[jj] = expf(wts[jj] - m);
+    float scal[4];
+    cl_combine<D>(cl, cs, 0, sm.kbar, scal);                  // mu~ and omega
+    const float omega = scal[0];
+    const float inv_om = 1.f / omega;
+    if (tid < D) {
+        const float kb = sm.kbar[tid] * inv_om;
+        sm.kbar[tid] = kb;
+        sm.delta[tid] = kb - sm.q[tid];
+        sm.x[tid] = 0.f;
+        sm.r[tid] = sm.delta[tid];
+        sm.p[tid] = sm.delta[tid];
+    }
+    __syncthreads();
+
+    // ---- (2) CG; every CTA carries the same state --------------------------------------------------
+    float gamma = block_sum<D>(sm, tid < D ? sm.r[tid] * sm.r[tid] : 0.f, 0);
+    const float rn0 = sqrtf(gamma);
+    bool active = gamma > 0.f && !(rn0 <= cg_tol * rn0);
+    int iters = 0, slot = 1;
+    const float lam_n = lambda * inv_om;
+    float kbv[E];
+#pragma unroll
+    for (int c = 0; c < E; ++c) kbv[c] = sm.kbar[c0 + c];
+    for (int it = 0; it < cg_max_iters && active; ++it) {
+        float pv[E];
+#pragma unroll
+        for (int c = 0; c < E; ++c) pv[c] = sm.p[c0 + c];
+        float kp = 0.f;
+#pragma unroll
+        for (int c = 0; c < E; ++c) kp = fmaf(kbv[c], pv[c], kp);
+        kp = group_sum(kp);
+        float ms = 0.f;
+#pragma unroll
+        for (int c = 0; c < E; ++c) acc[c] = 0.f;
+        for (int it2 = 0; it2 < n_it; ++it2) {
+            const int jj = it2 * NG + g;
+            const bool valid = jj < ns;
+            float kv[E];
+            if (valid) load_seg<E>(ks + (size_t)jj * D + c0, kv);
+            else {
+#pragma unroll
+                for (int c = 0; c < E; ++c) kv[c] = 0.f;
+            }
+            float a = 0.f;
+#pragma unroll
+            for (int c = 0; c < E; ++c) a = fmaf(pv[c], kv[c], a);
+            a = group_sum(a);
+            const float mm = valid ? wts[jj] * (a - kp) : 0.f;
+            ms += mm;
+#pragma unroll
+            for (int c = 0; c < E; ++c) acc[c] = fmaf(mm, kv[c], acc[c]);
+        }
+#pragma unroll
+        for (int c = 0; c < E; ++c) sm.part[g][c0 + c] = acc[c];
+        if (l8 == 0) sm.gs[g][2] = ms;
+        reduce_parts<D>(sm, sm.cp);
+        float ms_cta = 0.f;
+#pragma unroll 8
+        for (int t = 0; t < NG; ++t) ms_cta += sm.gs[t][2];
+        for (int c = tid; c < D; c += DT) cs.xbuf[slot][c] = sm.cp[c];
+        if (tid == 0) cs.xbuf[slot][D] = ms_cta;
+        cl_combine<D>(cl, cs, slot, sm.cp, scal);            // Y, msum over the whole cache
+        slot ^= 1;
+        const float msum = scal[0];
+        float pcp_part = 0.f;
+        if (tid < D) {
+            const float cpv = (sm.cp[tid] - sm.kbar[tid] * msum) * inv_om + lam_n * sm.p[tid];
+            sm.cp[tid] = cpv;
+            pcp_part = sm.p[tid] * cpv;
+        }
+        const float pcp = block_sum<D>(sm, pcp_part, 1);
+        if (!(pcp > 0.f)) break;
+        const float alpha = gamma / pcp;
+        float g2_part = 0.f;
+        if (tid < D) {
+            sm.x[tid] = fmaf(alpha, sm.p[tid], sm.x[tid]);
+            const float rv = fmaf(-alpha, sm.cp[tid], sm.r[tid]);
+            sm.r[tid] = rv;
+            g2_part = rv * rv;
+        }
+        const float g2 = block_sum<D>(sm, g2_part, 2);
+        const float beta = g2 / gamma;
+        gamma = g2;
+        ++iters;
+        if (tid < D) sm.p[tid] = fmaf(beta, sm.p[tid], sm.r[tid]);
+        __syncthreads();
+        if (gamma == 0.f || sqrtf(gamma) <= cg_tol * rn0) active = false;
+    }
+
+    // ---- (3) finalise and output over the slice (K from shared memory, V streamed) ----------------
+    const float dx = block_sum<D>(sm, tid < D ? sm.delta[tid] * sm.x[tid] : 0.f, 0);
+    const float kx = block_sum<D>(sm, tid < D ? sm.kbar[tid] * sm.x[tid] : 0.f, 1);
+    float xv[E];
+#pragma unroll
+    for (int c = 0; c < E; ++c) xv[c] = sm.x[c0 + c];
+    const float c1 = 1.f + kx;
+    float us = 0.f;
+#pragma unroll
+    for (int c = 0; c < E; ++c) acc[c] = 0.f;
+    for (int it = 0; it < n_it; ++it) {
+        const int jj = it * NG + g;
+        const bool valid = jj < ns;
+        float kv[E], vv[E];
+        if (valid) {
+            load_seg<E>(ks + (size_t)jj * D + c0, kv);
+            load_seg<E>(vh + (size_t)(j0 + jj) * D + c0, vv);
+        } else {
+#pragma unroll
+            for (int c = 0; c < E; ++c) kv[c] = vv[c] = 0.f;
+        }
+        float t = 0.f;
+#pragma unroll
+        for (int c = 0; c < E; ++c) t = fmaf(xv[c], kv[c], t);
+        t = group_sum(t);
+        const float u = valid ? wts[jj] * (c1 - t) : 0.f;
+        us += u;
+#pragma unroll
+        for (int c = 0; c < E; ++c) acc[c] = fmaf(u, vv[c], acc[c]);
+    }
+#pragma unroll
+    for (int c = 0; c < E; ++c) sm.part[g][c0 + c] = acc[c];
+    if (l8 == 0) sm.gs[g][3] = us;
+    reduce_parts<D>(sm, sm.cp);
+    float us_cta = 0.f;
+#pragma unroll 8
+    for (int t = 0; t < NG; ++t) us_cta += sm.gs[t][3];
+    for (int c = tid; c < D; c += DT) cs.xbuf[slot][c] = sm.cp[c];
+    if (tid == 0) cs.xbuf[slot][D] = us_cta;
+    cl_combine<D>(cl, cs, slot, sm.cp, scal);                // O and sum_j u_j over the cache
+    if (rank == 0 && tid < D) {
+        const float inv_g = 1.f / (1.f + dx);
+        stf(out + head * D + tid, sm.cp[tid] / scal[0]);
+        rho[head * D + tid] = sm.x[tid] * inv_g;
+        if (tid == 0) {
+            denom[head] = omega * inv_g;
+            if (cg_iters) cg_iters[head] = iters;
+        }
+    }
+    cl.sync();                       // no CTA leaves while a peer may still read its slots
+}
+
 template <int D, typename T>
 cudaError_t launch_dec(const DecodeProblem& p, cudaStream_t stream) {
     const size_t smem = sizeof(DecSmem<D>) + (size_t)p.n * sizeof(float);
@@ -333,13 +621,53 @@ cudaError_t launch_dec(const DecodeProblem& p, cudaStream_t stream) {
     return e;
 }
 
+// Keys per CTA of the cluster form (a multiple of 4, so the key slice stays 16-byte aligned).
+inline int cl_slice(int n) { return ((n + CL - 1) / CL + 3) & ~3; }
+
+template <int D, typename T>
+size_t cl_smem_bytes(int n) {
+    const size_t S = (size_t)cl_slice(n);
+    return cl_off_w<D>() + S * sizeof(float) + S * D * sizeof(T);
+}
+
+template <int D, typename T>
+cudaError_t launch_dec_cluster(const DecodeProblem& p, cudaStream_t stream) {
+    const int S = cl_slice(p.n);
+    const size_t smem = cl_smem_bytes<D, T>(p.n);
+    auto kern = lla_decode_cluster_kernel<D, T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (p.ev_main_begin && (e = cudaEventRecord(p.ev_main_begin, stream)) != cudaSuccess) return e;
+    kern<<<p.B * p.H * CL, DT, smem, stream>>>(static_cast<const T*>(p.q), static_cast<const T*>(p.k),
+                                               static_cast<const T*>(p.v), static_cast<T*>(p.out), p.rho, p.denom,
+                                               p.cg_iters, p.n, p.n_cap, S, p.tau, p.lambda, p.cg_max_iters,
+                                               p.cg_tol);
+    e = cudaGetLastError();
+    if (e == cudaSuccess && p.ev_main_end) e = cudaEventRecord(p.ev_main_end, stream);
+    return e;
+}
+
+// The cluster form reads K from HBM once but pays a cluster-wide exchange per pass; the streaming
+// form re-reads K every pass but keeps every SM busy with whole heads.  Measured on GB300 (bf16,
+// n = 4096, d = 128, 16 CG iterations): 16 heads 0.23 vs 0.76 ms, 64 heads 0.55 vs 0.77 ms, 256
+// heads 1.92 vs 1.47 ms, 1024 heads 7.3 vs 5.7 ms (cluster vs streaming): the cluster form wins
+// while there are too few heads to fill the GPU, up to about 128 heads.
+constexpr long long kClusterMaxHeads = 128;
+
+template <int D, typename T>
+cudaError_t launch_dec_pick(const DecodeProblem& p, cudaStream_t stream) {
+    if (cl_smem_bytes<D, T>(p.n) <= (size_t)kMaxDynSmem && (long long)p.B * p.H <= kClusterMaxHeads)
+        return launch_dec_cluster<D, T>(p, stream);
+    return launch_dec<D, T>(p, stream);
+}
+
 template <typename T>
 cudaError_t launch_dec_dim(const DecodeProblem& p, cudaStream_t stream) {
     switch (p.d) {
-        case 16: return launch_dec<16, T>(p, stream);
-        case 32: return launch_dec<32, T>(p, stream);
-        case 64: return launch_dec<64, T>(p, stream);
-        case 128: return launch_dec<128, T>(p, stream);
+        case 16: return launch_dec_pick<16, T>(p, stream);
+        case 32: return launch_dec_pick<32, T>(p, stream);
+        case 64: return launch_dec_pick<64, T>(p, stream);
+        case 128: return launch_dec_pick<128, T>(p, stream);
         default: return cudaErrorInvalidValue;
     }
 }

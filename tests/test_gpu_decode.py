@@ -69,6 +69,17 @@ def test_decode_converged_matches_exact_solve(lla_gpu, dtype, d, n):
     _gate(w, qkv, res, lambda qi, K, V: lla_row(qi, K, V, w.tau, w.lam))
 
 
+@pytest.mark.parametrize("dtype,n,B", [("bf16", 8000, 1), ("fp32", 4000, 1), ("bf16", 600, 50)])
+def test_decode_streaming_form(lla_gpu, dtype, n, B):
+    """The streaming form (K re-read every pass) serves caches too long for an eighth to sit in a
+    CTA's shared memory, and batches of more than 128 heads; the cluster form the rest.  Both
+    meet the same gate."""
+    w = workload("lm_bf16", B=B, H=3, n=n, d=128, dtype=dtype, tau=1.0 / math.sqrt(128), cg_max_iters=576,
+                 cg_tol=1e-6)
+    qkv, res = _decode(w)
+    _gate(w, qkv, res, lambda qi, K, V: lla_row(qi, K, V, w.tau, w.lam))
+
+
 def test_decode_reads_only_the_valid_cache_rows(lla_gpu):
     """n_cap > n: rows past n hold NaN and must not reach the result."""
     w = workload("lm_bf16", B=2, H=2, n=200, d=128, tau=1.0 / math.sqrt(128), cg_max_iters=300, cg_tol=1e-6)
