@@ -45,6 +45,19 @@ It is the plain definition written out, one query at a time, in float64:
   with wbar the same max-subtracted causal softmax weights normalised to sum 1, vbar_i
   and kbar_i their weighted means, and the page's boundary factor eta dropped (the page
   removes it).  The covariance matrix is formed explicitly (d x d per query).
+* ``lla_row_grad`` / ``lla_grad_ref`` give the gradient of L = sum_i g_i . out_i with respect to
+  q, k and v.  The pages give no backward formulas (the reading notes only say that it needs
+  further linear systems, appendix D); they are derived here by differentiating Eqs. (6)-(8)
+  through the exact solve: with h_j = g.v_j, den = omega - mu.rho and a_j = w_j (1 - z_j.rho),
+      dL/dv_j = (a_j / den) g,   dL/dden = -(g.out)/den,
+      G = -(1/den) sum_j w_j h_j z_j + (g.out/den) mu,   Sigma u = G   (the adjoint solve),
+      dL/domega = dL/dden,   dL/dmu = u - rho dL/dden,   dL/dSigma = -u rho^T,
+      dL/dw_j = (h_j/den)(1 - z_j.rho) + dL/domega + z_j.dL/dmu - (z_j.u)(z_j.rho),
+      dL/dz_j = -(w_j h_j/den) rho + w_j dL/dmu - w_j (u (rho.z_j) + rho (u.z_j)),
+  then through z_j = k_j - q_i, w_j = exp(s_j - m), s_j = tau q_i.k_j and the row maximum m
+  (lambda is absolute, so the output depends on m; its gradient goes to the first index that
+  attains the maximum).  ``tests/test_oracle.py`` checks it against central finite differences
+  of ``lla_ref``.
 * ``brute_force_fit`` minimises the weighted ridge objective of section 2.1 over
   (b, W) directly by SVD least squares, without the closed form.  Reading: the
   ridge term that reproduces Eq. (7)'s "+ lambda I" is (lambda/2)||W||_F^2 (the
@@ -70,6 +83,8 @@ __all__ = [
     "softmax_ref",
     "parallax_row",
     "parallax_ref",
+    "lla_row_grad",
+    "lla_grad_ref",
     "cg_solve",
     "lla_row_cg",
     "brute_force_fit",
@@ -297,6 +312,54 @@ def parallax_ref(q, k, v, rho, tau, rows=None):
     outs = [parallax_row(q[b, h, i], k[b, h, : i + 1], v[b, h, : i + 1], rho[b, h, i], tau)["out"]
             for b, h, i in _rows_iter(q.shape, rows)]
     return np.array(outs).reshape(-1, q.shape[-1])
+
+
+def lla_row_grad(q_i, K_prefix, V_prefix, g_i, tau, lam):
+    """Gradient of g_i . out_i for one query with respect to q_i, the prefix keys and values.
+
+    Returns (out, dq [d], dK [i+1, d], dV [i+1, d]); the exact (Cholesky) solves throughout.
+    """
+    q_i, K, V, g = _f64(q_i), _f64(K_prefix), _f64(V_prefix), _f64(g_i)
+    s = tau * (K @ q_i)
+    jm = int(np.argmax(s))                       # first index attaining the maximum
+    w = np.exp(s - s[jm])
+    omega, mu, Sigma, Z = row_moments(q_i, K, w, lam)
+    fac = scipy.linalg.cho_factor(Sigma, lower=True)
+    rho = scipy.linalg.cho_solve(fac, mu)
+    out, s_mix, den = _output_from_rho(w, Z, V, omega, mu, rho)
+    h = V @ g
+    d_den = -(g @ out) / den
+    G = -((w * h) @ Z) / den + (g @ out / den) * mu
+    u = scipy.linalg.cho_solve(fac, G)
+    d_mu = u - rho * d_den
+    zr, zu = Z @ rho, Z @ u
+    d_w = (h / den) * (1.0 - zr) + d_den + Z @ d_mu - zu * zr
+    d_Z = (-(w * h / den))[:, None] * rho[None, :] + w[:, None] * d_mu[None, :] \
+        - w[:, None] * (np.outer(zr, u) + np.outer(zu, rho))
+    ds = w * d_w
+    ds[jm] -= ds.sum()                           # through m = s_jm
+    dq = tau * (ds @ K) - d_Z.sum(axis=0)
+    dK = tau * np.outer(ds, q_i) + d_Z
+    dV = np.outer(s_mix, g)
+    return out, dq, dK, dV
+
+
+def lla_grad_ref(q, k, v, dout, tau, lam):
+    """Gradients of sum_{b,h,i} dout[b,h,i] . out[b,h,i] over [B, H, n, d] inputs (float64).
+
+    Returns (dq, dk, dv), each [B, H, n, d]; dk and dv sum every causal row's contribution.
+    """
+    q, k, v, g = _f64(q), _f64(k), _f64(v), _f64(dout)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    B, H, n, _ = q.shape
+    for b in range(B):
+        for h in range(H):
+            for i in range(n):
+                _, gq, gK, gV = lla_row_grad(q[b, h, i], k[b, h, : i + 1], v[b, h, : i + 1], g[b, h, i], tau, lam)
+                dq[b, h, i] += gq
+                dk[b, h, : i + 1] += gK
+                dv[b, h, : i + 1] += gV
+    return dq, dk, dv
 
 
 def ridge_objective(b, W, q_i, K_prefix, V_prefix, w, ridge):

@@ -354,3 +354,67 @@ def test_parallax_ref_layout_matches_rows():
     assert out.shape == (20, 3)
     one = O.parallax_row(q[1, 0, 3], k[1, 0, :4], v[1, 0, :4], r[1, 0, 3], 0.4)["out"]
     assert np.abs(out[(1 * 2 + 0) * 5 + 3] - one).max() == 0.0
+
+
+# --------------------------------------------------------------------------- backward
+def _fd_grads(q, k, v, g, tau, lam, eps=1e-6):
+    """Central finite differences of L = sum g . out over every input entry (float64)."""
+    def L(q_, k_, v_):
+        out, _, _ = O.lla_ref(q_, k_, v_, tau, lam)
+        return float((out.reshape(g.shape) * g).sum())
+    grads = []
+    for which in range(3):
+        base = [q, k, v]
+        gr = np.zeros_like(base[which])
+        it = np.nditer(base[which], flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            plus = [x.copy() for x in base]
+            minus = [x.copy() for x in base]
+            plus[which][idx] += eps
+            minus[which][idx] -= eps
+            gr[idx] = (L(*plus) - L(*minus)) / (2 * eps)
+        grads.append(gr)
+    return grads
+
+
+@pytest.mark.parametrize("seed,n,d,tau,lam", [(0, 7, 3, 0.8, 0.3), (1, 6, 4, 1.5, 0.05), (2, 5, 2, 0.3, 2.0)])
+def test_gradient_matches_finite_differences(seed, n, d, tau, lam):
+    """The derived backward equals central differences of the pinned forward on every entry,
+    including the rank-deficient early rows (i < d) and the path through the row maximum."""
+    rng = np.random.default_rng(seed)
+    q, k, v, g = (rng.standard_normal((1, 1, n, d)) for _ in range(4))
+    dq, dk, dv = O.lla_grad_ref(q, k, v, g, tau, lam)
+    fq, fk, fv = _fd_grads(q, k, v, g, tau, lam)
+    scale = max(np.abs(fq).max(), np.abs(fk).max(), np.abs(fv).max())
+    for a, b in [(dq, fq), (dk, fk), (dv, fv)]:
+        assert np.abs(a - b).max() <= 1e-6 * scale
+
+
+def test_gradient_large_lambda_is_softmax_gradient():
+    """lambda -> infinity: rho -> 0 and the backward tends to softmax attention's, whose closed
+    form is dv_j = sum_i p_ij g_i and ds_ij = p_ij (g_i.v_j - g_i.out_i), dq_i = tau sum_j ds_ij k_j."""
+    rng = np.random.default_rng(5)
+    n, d, tau = 6, 3, 0.9
+    q, k, v, g = (rng.standard_normal((1, 1, n, d)) for _ in range(4))
+    dq, dk, dv = O.lla_grad_ref(q, k, v, g, tau, 1e12)
+    Q, K, V, G = q[0, 0], k[0, 0], v[0, 0], g[0, 0]
+    P = np.zeros((n, n))
+    for i in range(n):
+        e = np.exp(tau * K[: i + 1] @ Q[i] - (tau * K[: i + 1] @ Q[i]).max())
+        P[i, : i + 1] = e / e.sum()
+    out = P @ V
+    dS = P * (G @ V.T - (G * out).sum(1, keepdims=True))
+    assert np.abs(dv[0, 0] - P.T @ G).max() < 1e-9
+    assert np.abs(dq[0, 0] - tau * dS @ K).max() < 1e-9
+    assert np.abs(dk[0, 0] - tau * dS.T @ Q).max() < 1e-9
+
+
+def test_gradient_is_linear_in_the_output_cotangent():
+    rng = np.random.default_rng(6)
+    q, k, v, g1, g2 = (rng.standard_normal((1, 1, 5, 3)) for _ in range(5))
+    a = O.lla_grad_ref(q, k, v, g1, 0.7, 0.4)
+    b = O.lla_grad_ref(q, k, v, g2, 0.7, 0.4)
+    c = O.lla_grad_ref(q, k, v, 2.0 * g1 - g2, 0.7, 0.4)
+    for x, y, z in zip(a, b, c):
+        assert np.abs(z - (2.0 * x - y)).max() < 1e-10
