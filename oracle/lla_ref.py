@@ -84,6 +84,7 @@ __all__ = [
     "parallax_row",
     "parallax_ref",
     "lla_row_grad",
+    "lla_row_grad_cg",
     "lla_grad_ref",
     "cg_solve",
     "lla_row_cg",
@@ -314,14 +315,18 @@ def parallax_ref(q, k, v, rho, tau, rows=None):
     return np.array(outs).reshape(-1, q.shape[-1])
 
 
-def lla_row_grad(q_i, K_prefix, V_prefix, g_i, tau, lam):
+def lla_row_grad(q_i, K_prefix, V_prefix, g_i, tau, lam, jm=None):
     """Gradient of g_i . out_i for one query with respect to q_i, the prefix keys and values.
 
     Returns (out, dq [d], dK [i+1, d], dV [i+1, d]); the exact (Cholesky) solves throughout.
+    jm: the key index whose logit is taken as the row maximum m (default: the first index
+    attaining it).  Where two logits tie the max-subtracted definition has one-sided
+    derivatives; passing the other index gives the other side.
     """
     q_i, K, V, g = _f64(q_i), _f64(K_prefix), _f64(V_prefix), _f64(g_i)
     s = tau * (K @ q_i)
-    jm = int(np.argmax(s))                       # first index attaining the maximum
+    if jm is None:
+        jm = int(np.argmax(s))                   # first index attaining the maximum
     w = np.exp(s - s[jm])
     omega, mu, Sigma, Z = row_moments(q_i, K, w, lam)
     fac = scipy.linalg.cho_factor(Sigma, lower=True)
@@ -344,10 +349,61 @@ def lla_row_grad(q_i, K_prefix, V_prefix, g_i, tau, lam):
     return out, dq, dK, dV
 
 
-def lla_grad_ref(q, k, v, dout, tau, lam):
+def lla_row_grad_cg(q_i, K_prefix, V_prefix, g_i, tau, lam, max_iters, tol, jm=None):
+    """The backward at a CG iteration cap: what a solver that stops early computes.
+
+    Steps: weights, omega, kbar, delta and the centred Cn of ``lla_row_deflated_cg``;
+    rho' = ``cg_solve``(Cn, delta); kappa = delta.rho', rho = rho'/(1 + kappa),
+    denom = omega/(1 + kappa); h_j = g.v_j; tbar = sum_j wbar_j h_j (k_j - kbar);
+    gout = sum_j wbar_j h_j - omega (rho.tbar)/denom; y = ``cg_solve``(Cn, tbar);
+    u = -y/denom; then per key A_j = 1 - z_j.rho, B_j = (h_j - gout)/denom + z_j.u,
+    ds_j = w_j A_j B_j and the gradients
+        dv_j = (w_j A_j/denom) g,  dk_j = tau ds_j q + w_j (A_j u - B_j rho),
+        dq = tau sum_j ds_j k_j - sum_j w_j (A_j u - B_j rho),
+    plus -tau (sum_j ds_j) at the maximum's index (to dq along k_jm, to dk_jm along q).
+    With both solves converged this equals ``lla_row_grad``: with C rho' = omega delta, the
+    adjoint solve Sigma u = G of the exact gradient reduces to u = -C^{-1} t / denom.
+    Returns (dq [d], dK [i+1, d], dV [i+1, d]).
+    """
+    q_i, K, V, g = _f64(q_i), _f64(K_prefix), _f64(V_prefix), _f64(g_i)
+    s = tau * (K @ q_i)
+    if jm is None:
+        jm = int(np.argmax(s))
+    w = np.exp(s - s[jm])
+    omega = w.sum()
+    wbar = w / omega
+    kbar = wbar @ K
+    delta = kbar - q_i
+    Kc = K - kbar[None, :]
+    Cn = (Kc * wbar[:, None]).T @ Kc + (lam / omega) * np.eye(q_i.shape[0])
+    rho_p, _ = cg_solve(Cn, delta, max_iters, tol)
+    kappa = delta @ rho_p
+    rho = rho_p / (1.0 + kappa)
+    den = omega / (1.0 + kappa)
+    h = V @ g
+    tbar = (wbar * h) @ Kc
+    gout = wbar @ h - omega * (rho @ tbar) / den
+    y, _ = cg_solve(Cn, tbar, max_iters, tol)
+    u = -y / den
+    Z = K - q_i[None, :]
+    A = 1.0 - Z @ rho
+    Bc = (h - gout) / den + Z @ u
+    ds = w * A * Bc
+    dZ = w[:, None] * (A[:, None] * u[None, :] - Bc[:, None] * rho[None, :])
+    sd = ds.sum()
+    dq = tau * (ds @ K) - dZ.sum(axis=0) - tau * sd * K[jm]
+    dK = tau * np.outer(ds, q_i) + dZ
+    dK[jm] -= tau * sd * q_i
+    dV = np.outer(w * A / den, g)
+    return dq, dK, dV
+
+
+def lla_grad_ref(q, k, v, dout, tau, lam, cg=None):
     """Gradients of sum_{b,h,i} dout[b,h,i] . out[b,h,i] over [B, H, n, d] inputs (float64).
 
-    Returns (dq, dk, dv), each [B, H, n, d]; dk and dv sum every causal row's contribution.
+    cg: None for the exact gradient (``lla_row_grad``), else (max_iters, tol) for
+    ``lla_row_grad_cg``.  Returns (dq, dk, dv), each [B, H, n, d]; dk and dv sum every causal
+    row's contribution.
     """
     q, k, v, g = _f64(q), _f64(k), _f64(v), _f64(dout)
     dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
@@ -355,7 +411,11 @@ def lla_grad_ref(q, k, v, dout, tau, lam):
     for b in range(B):
         for h in range(H):
             for i in range(n):
-                _, gq, gK, gV = lla_row_grad(q[b, h, i], k[b, h, : i + 1], v[b, h, : i + 1], g[b, h, i], tau, lam)
+                args = (q[b, h, i], k[b, h, : i + 1], v[b, h, : i + 1], g[b, h, i], tau, lam)
+                if cg is None:
+                    _, gq, gK, gV = lla_row_grad(*args)
+                else:
+                    gq, gK, gV = lla_row_grad_cg(*args, cg[0], cg[1])
                 dq[b, h, i] += gq
                 dk[b, h, : i + 1] += gK
                 dv[b, h, : i + 1] += gV

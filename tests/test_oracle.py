@@ -418,3 +418,52 @@ def test_gradient_is_linear_in_the_output_cotangent():
     c = O.lla_grad_ref(q, k, v, 2.0 * g1 - g2, 0.7, 0.4)
     for x, y, z in zip(a, b, c):
         assert np.abs(z - (2.0 * x - y)).max() < 1e-10
+
+
+def test_capped_gradient_converges_to_the_exact_gradient():
+    """The iteration-capped backward (CG for rho' and for the adjoint) with a cap of d and a
+    tight tolerance equals the finite-difference-pinned exact gradient."""
+    rng = np.random.default_rng(7)
+    q, k, v, g = (rng.standard_normal((1, 2, 9, 4)) for _ in range(4))
+    a = O.lla_grad_ref(q, k, v, g, 0.6, 0.2)
+    b = O.lla_grad_ref(q, k, v, g, 0.6, 0.2, cg=(40, 1e-14))
+    for x, y in zip(a, b):
+        assert np.abs(x - y).max() <= 1e-9 * np.abs(x).max()
+
+
+def test_capped_gradient_with_no_iterations_is_softmax_gradient():
+    """A cap of 0 leaves rho = u = 0: the backward of causal softmax attention (closed form)."""
+    rng = np.random.default_rng(8)
+    n, d, tau = 7, 3, 1.1
+    q, k, v, g = (rng.standard_normal((1, 1, n, d)) for _ in range(4))
+    dq, dk, dv = O.lla_grad_ref(q, k, v, g, tau, 0.5, cg=(0, 0.0))
+    Q, K, V, G = q[0, 0], k[0, 0], v[0, 0], g[0, 0]
+    P = np.zeros((n, n))
+    for i in range(n):
+        e = np.exp(tau * K[: i + 1] @ Q[i])
+        P[i, : i + 1] = e / e.sum()
+    dS = P * (G @ V.T - (G * (P @ V)).sum(1, keepdims=True))
+    assert np.abs(dv[0, 0] - P.T @ G).max() < 1e-12
+    assert np.abs(dq[0, 0] - tau * dS @ K).max() < 1e-12
+    assert np.abs(dk[0, 0] - tau * dS.T @ Q).max() < 1e-12
+
+
+def test_gradient_at_a_tie_takes_either_side():
+    """Two equal top logits: the default takes the first index; the other index gives the other
+    one-sided derivative, and the two differ only along the moved maximum."""
+    rng = np.random.default_rng(9)
+    d = 3
+    K = rng.standard_normal((5, d))
+    q = rng.standard_normal(d)
+    K[1] = K[3] = 3.0 * q / np.linalg.norm(q)     # identical keys: tied logits, and the largest
+    s = K @ q
+    assert s[1] == s[3] == s.max() and int(np.argmax(s)) == 1
+    V, g = rng.standard_normal((5, d)), rng.standard_normal(d)
+    _, dq1, dK1, dV1 = O.lla_row_grad(q, K, V, g, 0.9, 0.4)
+    _, dq3, dK3, dV3 = O.lla_row_grad(q, K, V, g, 0.9, 0.4, jm=3)
+    assert np.abs(dV1 - dV3).max() < 1e-12
+    # the maximum term moves from key 1 to key 3: dq equal (k_1 = k_3), dK swaps it between rows
+    assert np.abs(dq1 - dq3).max() < 1e-12
+    assert np.abs((dK1[1] + dK1[3]) - (dK3[1] + dK3[3])).max() < 1e-12
+    keep = [0, 2, 4]
+    assert np.abs(dK1[keep] - dK3[keep]).max() < 1e-12
