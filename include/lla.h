@@ -181,6 +181,46 @@ int lla_decode(int dtype, const void* q, const void* k, const void* v, void* out
 /* Largest cache length n that lla_decode accepts for head dim d (0 when d is unsupported). */
 int lla_decode_max_n(int d);
 
+/*
+ * lla_backward -- gradients of the causal LLA forward: with L = sum_{b,h,i} dout_i.out_i,
+ * dq = dL/dq, dk = dL/dk, dv = dL/dv.  The Local Linear Attention reading notes name the
+ * backward pass (appendix D: it needs further linear systems) without giving it; it is the
+ * derivative of Eqs. (6)-(8) (section 2.1) through the exact solve, written in centred form.
+ * Per query i (g_i = dout_i, wbar_ij = w_ij/omega_i, c_ij = k_j - kbar_i, h_ij = g_i.v_j,
+ * hbar_i = sum_j wbar_ij h_ij), one adjoint system on the forward's centred operator:
+ *
+ *     (C_i / omega_i) y_i = sum_j wbar_ij h_ij c_ij,     rho'_i = rho_i omega_i / denom_i,
+ *
+ * and per pair  Ahat = 1 - c.rho'_i,  Bhat = (h - hbar_i) - c.y_i,  ds = wbar Ahat Bhat:
+ *     dv_j += wbar Ahat g_i,   dk_j += tau ds q_i - wbar (Ahat y_i + Bhat rho'_i),
+ *     dq_i  = tau sum_j ds k_j + y_i,
+ * plus the path through the row maximum m_i (to the first key index attaining it), whose
+ * weight is sum_j ds = -(lambda/omega_i) rho'_i.y_i.  Every product and the CG state are fp32
+ * (CUDA cores).
+ *
+ * dtype      LLA_DTYPE_BF16 or LLA_DTYPE_FP32: q, k, v, dout share it.
+ * q, k, v    [B,H,n,d], the forward call's inputs.
+ * rho        [B,H,n,d] fp32, denom [B,H,n] fp32: the forward call's outputs for these inputs
+ *            (any path); the backward is exact to the extent they are.
+ * dout       [B,H,n,d] in dtype: dL/dout.
+ * dq, dk, dv [B,H,n,d] fp32, written (not accumulated into).
+ * cg_iters   NULL, or [B,H,n] int32: adjoint CG iterations each query executed.
+ * tau, lambda as for the forward call; cg_max_iters, cg_tol: the adjoint CG's cap and relative
+ *            tolerance (||r|| <= cg_tol ||sum_j wbar_ij h_ij c_ij||), as for lla_forward.
+ * workspace  NULL (scratch from the stream-ordered pool) or a device buffer of at least
+ *            lla_backward_workspace_size(B, H, n, d) bytes, 256-byte aligned, not used
+ *            concurrently by another call.
+ * B*H <= 65535.  All pointers are device pointers, 16-byte aligned, owned by the caller.
+ * Errors as for lla_forward_ex.
+ */
+int lla_backward(int dtype, const void* q, const void* k, const void* v, const float* rho, const float* denom,
+                 const void* dout, float* dq, float* dk, float* dv, int* cg_iters, int B, int H, int n, int d,
+                 float tau, float lambda, int cg_max_iters, float cg_tol, void* workspace, size_t workspace_bytes,
+                 void* stream);
+
+/* Bytes of scratch lla_backward needs (per-query records and the adjoint vectors y). */
+size_t lla_backward_workspace_size(int B, int H, int n, int d);
+
 /* Message for the calling thread's most recent failure ("" if none). Owned by the library. */
 const char* lla_last_error(void);
 

@@ -16,7 +16,7 @@ __all__ = [
     "LLAError", "load_library", "library_path", "forward", "lla_forward", "lla_forward_ex",
     "lla_workspace_size", "lla_resolve_path", "lla_sync_status", "lla_last_error", "lla_version",
     "lla_profile_enable", "lla_profile_read", "lla_forward_noalloc", "lla_parallax_forward", "parallax_forward",
-    "lla_decode", "lla_decode_max_n", "decode",
+    "lla_decode", "lla_decode_max_n", "decode", "lla_backward", "lla_backward_workspace_size", "backward",
     "LLA_OK", "LLA_ERR_INVALID_ARG", "LLA_ERR_UNSUPPORTED", "LLA_ERR_CUDA", "LLA_ERR_DEVICE_TIMEOUT",
     "LLA_DTYPE_BF16", "LLA_DTYPE_FP32", "LLA_PATH_AUTO", "LLA_PATH_TENSOR", "LLA_PATH_FP32",
     "EXPORTED_SYMBOLS",
@@ -48,6 +48,9 @@ _SIGNATURES = {
     "lla_decode": (_c_int, [_c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                             _c_float, _c_float, _c_int, _c_float, _vp]),
     "lla_decode_max_n": (_c_int, [_c_int]),
+    "lla_backward": (_c_int, [_c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
+                              _c_int, _c_float, _c_float, _c_int, _c_float, _vp, _c_size, _vp]),
+    "lla_backward_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
     "lla_profile_enable": (_c_int, [_c_int]),
     "lla_profile_read": (_c_int, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]),
     "lla_version": (_c_int, []),
@@ -201,6 +204,49 @@ def decode(q, k_cache, v_cache, n, tau, lam, cg_max_iters, cg_tol=0.0, *, return
     if return_iters:
         return out, rho, denom, iters
     return out, rho, denom
+
+
+def lla_backward(dtype, q_ptr, k_ptr, v_ptr, rho_ptr, denom_ptr, dout_ptr, dq_ptr, dk_ptr, dv_ptr, iters_ptr, B, H,
+                 n, d, tau, lam, cg_max_iters, cg_tol, ws_ptr, ws_bytes, stream_ptr):
+    """Raw backward entry point on device pointers (ints); raises LLAError on failure."""
+    _check(load_library().lla_backward(dtype, q_ptr, k_ptr, v_ptr, rho_ptr, denom_ptr, dout_ptr, dq_ptr, dk_ptr,
+                                       dv_ptr, iters_ptr, B, H, n, d, tau, lam, cg_max_iters, cg_tol, ws_ptr,
+                                       ws_bytes, stream_ptr))
+
+
+def lla_backward_workspace_size(B, H, n, d):
+    return load_library().lla_backward_workspace_size(B, H, n, d)
+
+
+def backward(q, k, v, rho, denom, dout, tau, lam, cg_max_iters, cg_tol=0.0, *, return_iters=False, dq=None,
+             dk=None, dv=None, workspace=None, stream=None):
+    """Gradients (dq, dk, dv) [B, H, n, d] fp32 of sum(dout * out) for the forward call that gave
+    rho [B, H, n, d] and denom [B, H, n] on q, k, v (see include/lla.h).  With return_iters also
+    the adjoint CG iteration counts [B, H, n].  Asynchronous on the current (or given) stream.
+    """
+    import torch
+    _check_qkv(q, k, v)
+    if tuple(dout.shape) != tuple(q.shape) or dout.dtype != q.dtype or not dout.is_cuda:
+        raise LLAError(LLA_ERR_INVALID_ARG, f"dout must be a CUDA tensor of shape {tuple(q.shape)} and dtype {q.dtype}")
+    B, H, n, d = q.shape
+    if tuple(rho.shape) != (B, H, n, d) or tuple(denom.shape) != (B, H, n) or \
+            rho.dtype != torch.float32 or denom.dtype != torch.float32:
+        raise LLAError(LLA_ERR_INVALID_ARG, "rho [B, H, n, d] and denom [B, H, n] must be the forward's fp32 outputs")
+    q, k, v, dout = q.contiguous(), k.contiguous(), v.contiguous(), dout.contiguous()
+    rho, denom = rho.contiguous(), denom.contiguous()
+    dtype = LLA_DTYPE_BF16 if q.dtype == torch.bfloat16 else LLA_DTYPE_FP32
+    grads = []
+    for t in (dq, dk, dv):
+        grads.append(torch.empty((B, H, n, d), dtype=torch.float32, device=q.device) if t is None else t)
+    iters = torch.empty((B, H, n), dtype=torch.int32, device=q.device) if return_iters else None
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel() * workspace.element_size())
+    lla_backward(dtype, q.data_ptr(), k.data_ptr(), v.data_ptr(), rho.data_ptr(), denom.data_ptr(), dout.data_ptr(),
+                 grads[0].data_ptr(), grads[1].data_ptr(), grads[2].data_ptr(),
+                 None if iters is None else iters.data_ptr(), B, H, n, d, float(tau), float(lam), int(cg_max_iters),
+                 float(cg_tol), ws_ptr, ws_bytes, _stream_ptr(stream))
+    if return_iters:
+        return (*grads, iters)
+    return tuple(grads)
 
 
 def _check_qkv(q, k, v):

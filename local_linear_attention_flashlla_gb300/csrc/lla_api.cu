@@ -261,6 +261,71 @@ int lla_decode(int dtype, const void* q, const void* k, const void* v, void* out
     return LLA_OK;
 }
 
+size_t lla_backward_workspace_size(int B, int H, int n, int d) {
+    if (B < 1 || H < 1 || n < 1 || d < 1) return 0;
+    return lla::backward_workspace_bytes(B, H, n, d);
+}
+
+int lla_backward(int dtype, const void* q, const void* k, const void* v, const float* rho, const float* denom,
+                 const void* dout, float* dq, float* dk, float* dv, int* cg_iters, int B, int H, int n, int d,
+                 float tau, float lambda, int cg_max_iters, float cg_tol, void* workspace, size_t workspace_bytes,
+                 void* stream_) {
+    lla::g_msg[0] = '\0';
+    if (!q || !k || !v || !rho || !denom || !dout || !dq || !dk || !dv)
+        return fail(LLA_ERR_INVALID_ARG, "null tensor pointer");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(rho) || !aligned16(denom) ||
+        !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return fail(LLA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+    if (B < 1 || H < 1 || n < 1) return fail(LLA_ERR_INVALID_ARG, "B, H, n must be >= 1 (got %d, %d, %d)", B, H, n);
+    if ((long long)B * H > 65535LL) return fail(LLA_ERR_INVALID_ARG, "B*H must be <= 65535");
+    if ((long long)B * H * n * d > (1LL << 40)) return fail(LLA_ERR_INVALID_ARG, "problem too large");
+    if (d != 16 && d != 32 && d != 64 && d != 128)
+        return fail(LLA_ERR_INVALID_ARG, "head dim d must be 16, 32, 64 or 128 (got %d)", d);
+    if (!(tau > 0.f) || !(tau < 1e30f)) return fail(LLA_ERR_INVALID_ARG, "tau must be finite and > 0");
+    if (!(lambda > 0.f) || !(lambda < 1e30f)) return fail(LLA_ERR_INVALID_ARG, "lambda must be finite and > 0");
+    if (cg_max_iters < 1 || cg_max_iters > 4096) return fail(LLA_ERR_INVALID_ARG, "cg_max_iters must be in [1, 4096]");
+    if (!(cg_tol >= 0.f) || !(cg_tol < 1e30f)) return fail(LLA_ERR_INVALID_ARG, "cg_tol must be finite and >= 0");
+    if (dtype != LLA_DTYPE_BF16 && dtype != LLA_DTYPE_FP32) return fail(LLA_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+    const size_t need = lla::backward_workspace_bytes(B, H, n, d);
+    if (workspace) {
+        if (workspace_bytes < need)
+            return fail(LLA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+            return fail(LLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    }
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    lla::BackwardProblem p{q, k, v, dout, rho, denom, dq, dk, dv, cg_iters, B, H, n, d, tau, lambda,
+                           cg_max_iters, cg_tol, dtype, nullptr, nullptr};
+    if (lla::g_prof_on) {
+        for (int i = 0; i < 4; ++i)
+            if (!lla::g_ev[i]) {
+                cudaError_t e = cudaEventCreate(&lla::g_ev[i]);
+                if (e != cudaSuccess) return lla::cuda_fail(e, "profiling event");
+            }
+        p.ev_main_begin = lla::g_ev[1];
+        p.ev_main_end = lla::g_ev[2];
+        cudaError_t e = cudaEventRecord(lla::g_ev[0], stream);
+        if (e != cudaSuccess) return lla::cuda_fail(e, "profiling event record");
+    }
+    void* ws = workspace;
+    if (!ws) {
+        cudaError_t e = cudaMallocAsync(&ws, need, stream);
+        if (e != cudaSuccess) return lla::cuda_fail(e, "cudaMallocAsync(workspace)");
+    }
+    cudaError_t e = lla::launch_backward(p, ws, stream);
+    if (!workspace) {
+        cudaError_t e2 = cudaFreeAsync(ws, stream);
+        if (e == cudaSuccess && e2 != cudaSuccess) return lla::cuda_fail(e2, "cudaFreeAsync(workspace)");
+    }
+    if (e != cudaSuccess) return lla::cuda_fail(e, "backward launch");
+    if (lla::g_prof_on) {
+        e = cudaEventRecord(lla::g_ev[3], stream);
+        if (e != cudaSuccess) return lla::cuda_fail(e, "profiling event record");
+        lla::g_prof_valid = true;
+    }
+    return LLA_OK;
+}
+
 int lla_decode_max_n(int d) {
     if (d != 16 && d != 32 && d != 64 && d != 128) return 0;
     const size_t base = lla::decode_smem_bytes(0, d);

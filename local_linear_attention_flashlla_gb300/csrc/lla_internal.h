@@ -51,6 +51,28 @@ struct DecodeProblem {
 size_t decode_smem_bytes(int n, int d);
 cudaError_t launch_decode(const DecodeProblem& p, cudaStream_t stream);
 
+// Backward pass: gradients of sum_i dout_i.out_i with respect to q, k, v (all fp32 outputs).
+struct BackwardProblem {
+    const void* q;       // [B,H,n,d] in dtype
+    const void* k;
+    const void* v;
+    const void* dout;
+    const float* rho;    // [B,H,n,d] fp32, the forward's rho
+    const float* denom;  // [B,H,n] fp32, the forward's denom
+    float* dq;           // [B,H,n,d] fp32
+    float* dk;
+    float* dv;
+    int* cg_iters;       // [B,H,n] adjoint CG iterations, or null
+    int B, H, n, d;
+    float tau, lambda;
+    int cg_max_iters;
+    float cg_tol;
+    int dtype;           // lla_dtype
+    cudaEvent_t ev_main_begin, ev_main_end;   // around the query-major kernel when profiling
+};
+size_t backward_workspace_bytes(int B, int H, int n, int d);
+cudaError_t launch_backward(const BackwardProblem& p, void* workspace, cudaStream_t stream);
+
 // fp32 CUDA-core path (any d in {16,32,64,128}, fp32 or bf16 inputs).
 cudaError_t launch_simt(const Problem& p, cudaStream_t stream);
 

@@ -155,3 +155,11 @@ def sample_rows(w: Workload, count, seed=1, tile=128):
     while len(rows) < count:
         rows.append((int(rng.integers(w.B)), int(rng.integers(w.H)), int(rng.integers(w.n))))
     return rows
+
+
+def make_cotangent(w: Workload, seed_offset=2000):
+    """Output cotangent dL/dout [B, H, n, d] (CPU torch, w's dtype) from its own stream: a unit
+    Gaussian per entry, the gradient a loss that is a random linear function of the output sends."""
+    rng = np.random.Generator(np.random.PCG64(w.seed + seed_offset))
+    g = rng.standard_normal((w.B, w.H, w.n, w.d), dtype=np.float32)
+    return torch.from_numpy(np.ascontiguousarray(g)).to(w.torch_dtype)

@@ -352,18 +352,19 @@ def lla_row_grad(q_i, K_prefix, V_prefix, g_i, tau, lam, jm=None):
 def lla_row_grad_cg(q_i, K_prefix, V_prefix, g_i, tau, lam, max_iters, tol, jm=None):
     """The backward at a CG iteration cap: what a solver that stops early computes.
 
-    Steps: weights, omega, kbar, delta and the centred Cn of ``lla_row_deflated_cg``;
-    rho' = ``cg_solve``(Cn, delta); kappa = delta.rho', rho = rho'/(1 + kappa),
-    denom = omega/(1 + kappa); h_j = g.v_j; tbar = sum_j wbar_j h_j (k_j - kbar);
-    gout = sum_j wbar_j h_j - omega (rho.tbar)/denom; y = ``cg_solve``(Cn, tbar);
-    u = -y/denom; then per key A_j = 1 - z_j.rho, B_j = (h_j - gout)/denom + z_j.u,
-    ds_j = w_j A_j B_j and the gradients
-        dv_j = (w_j A_j/denom) g,  dk_j = tau ds_j q + w_j (A_j u - B_j rho),
-        dq = tau sum_j ds_j k_j - sum_j w_j (A_j u - B_j rho),
-    plus -tau (sum_j ds_j) at the maximum's index (to dq along k_jm, to dk_jm along q).
-    With both solves converged this equals ``lla_row_grad``: with C rho' = omega delta, the
-    adjoint solve Sigma u = G of the exact gradient reduces to u = -C^{-1} t / denom.
-    Returns (dq [d], dK [i+1, d], dV [i+1, d]).
+    Centred form.  With c_j = k_j - kbar, wbar_j = w_j/omega, the centred Cn and delta of
+    ``lla_row_deflated_cg``, h_j = g.v_j, hbar = sum_j wbar_j h_j and tbar = sum_j wbar_j h_j c_j:
+        rho' = ``cg_solve``(Cn, delta),   y = ``cg_solve``(Cn, tbar),
+        Ahat_j = 1 - c_j.rho',   Bhat_j = (h_j - hbar) - c_j.y,   ds_j = wbar_j Ahat_j Bhat_j,
+        sd = -(lambda/omega) rho'.y                      (the path through the row maximum)
+        dv_j = wbar_j Ahat_j g,
+        dk_j = tau ds_j q - wbar_j (Ahat_j y + Bhat_j rho'),   dk_jm -= tau sd q,
+        dq = tau (sum_j ds_j k_j - sd k_jm) + y.
+    With both solves exact this is ``lla_row_grad``: writing z_j = c_j + delta, kappa = delta.rho',
+    rho = rho'/(1 + kappa), denom = omega/(1 + kappa), the exact gradient has
+    1 - z_j.rho = Ahat_j/(1 + kappa), adjoint solution u = -(1 + kappa) y/omega, and the identity
+    delta.y = rho'.tbar (both equal delta^T Cn^{-1} tbar) removes every term in delta.y; the sum
+    of ds_j over j reduces to sd.  Returns (dq [d], dK [i+1, d], dV [i+1, d]).
     """
     q_i, K, V, g = _f64(q_i), _f64(K_prefix), _f64(V_prefix), _f64(g_i)
     s = tau * (K @ q_i)
@@ -377,24 +378,18 @@ def lla_row_grad_cg(q_i, K_prefix, V_prefix, g_i, tau, lam, max_iters, tol, jm=N
     Kc = K - kbar[None, :]
     Cn = (Kc * wbar[:, None]).T @ Kc + (lam / omega) * np.eye(q_i.shape[0])
     rho_p, _ = cg_solve(Cn, delta, max_iters, tol)
-    kappa = delta @ rho_p
-    rho = rho_p / (1.0 + kappa)
-    den = omega / (1.0 + kappa)
     h = V @ g
+    hbar = wbar @ h
     tbar = (wbar * h) @ Kc
-    gout = wbar @ h - omega * (rho @ tbar) / den
     y, _ = cg_solve(Cn, tbar, max_iters, tol)
-    u = -y / den
-    Z = K - q_i[None, :]
-    A = 1.0 - Z @ rho
-    Bc = (h - gout) / den + Z @ u
-    ds = w * A * Bc
-    dZ = w[:, None] * (A[:, None] * u[None, :] - Bc[:, None] * rho[None, :])
-    sd = ds.sum()
-    dq = tau * (ds @ K) - dZ.sum(axis=0) - tau * sd * K[jm]
-    dK = tau * np.outer(ds, q_i) + dZ
+    Ahat = 1.0 - Kc @ rho_p
+    Bhat = (h - hbar) - Kc @ y
+    ds = wbar * Ahat * Bhat
+    sd = -(lam / omega) * (rho_p @ y)
+    dq = tau * (ds @ K - sd * K[jm]) + y
+    dK = tau * np.outer(ds, q_i) - wbar[:, None] * (Ahat[:, None] * y[None, :] + Bhat[:, None] * rho_p[None, :])
     dK[jm] -= tau * sd * q_i
-    dV = np.outer(w * A / den, g)
+    dV = np.outer(wbar * Ahat, g)
     return dq, dK, dV
 
 

@@ -128,3 +128,36 @@ def test_decode_cache_length_limit(lib):
         assert 32768 <= m < 60000
         assert _call_decode(lib, d=d, n=m + 1, n_cap=m + 1) == lla.LLA_ERR_UNSUPPORTED
     assert lib.lla_decode_max_n(48) == 0
+
+
+def _call_backward(lib, **kw):
+    a = dict(dtype=0, q=16, k=32, v=48, rho=64, den=80, dout=96, dq=112, dk=128, dv=144, it=None, B=1, H=1, n=8,
+             d=64, tau=0.1, lam=1.0, T=4, tol=0.0, ws=None, ws_bytes=0, stream=None)
+    a.update(kw)
+    return lib.lla_backward(a["dtype"], a["q"], a["k"], a["v"], a["rho"], a["den"], a["dout"], a["dq"], a["dk"],
+                            a["dv"], a["it"], a["B"], a["H"], a["n"], a["d"], a["tau"], a["lam"], a["T"], a["tol"],
+                            a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("bad", [
+    dict(q=None), dict(rho=None), dict(den=None), dict(dout=None), dict(dq=None), dict(dk=None), dict(dv=None),
+    dict(dv=40), dict(B=0), dict(n=0), dict(H=70000), dict(d=48), dict(tau=0.0), dict(lam=-1.0), dict(T=0),
+    dict(tol=float("nan")), dict(dtype=3), dict(ws=4096, ws_bytes=16), dict(ws=4096 + 16, ws_bytes=1 << 20),
+])
+def test_backward_invalid_arguments_rejected_before_launch(lib, bad):
+    assert _call_backward(lib, **bad) == lla.LLA_ERR_INVALID_ARG
+    assert lib.lla_last_error().decode()
+
+
+def test_backward_workspace_size(lib):
+    # one 32-byte record and one fp32 d-vector per query, each part rounded up to 256 bytes
+    assert lib.lla_backward_workspace_size(2, 3, 100, 64) == 19200 + 153600
+    assert lib.lla_backward_workspace_size(1, 1, 1, 16) == 256 + 256
+    assert lib.lla_backward_workspace_size(0, 1, 1, 16) == 0
+
+
+def test_backward_binding_refuses_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(1, 1, 4, 16)
+    with pytest.raises(lla.LLAError):
+        lla.backward(x, x, x, x, torch.zeros(1, 1, 4), x, 0.25, 1.0, 4)
