@@ -34,6 +34,7 @@ sys.path.insert(0, ROOT)
 METRIC = "causal LLA fwd tokens/s & TFLOP/s at d=128 bf16; fraction of BF16 tensor peak"
 METRIC_DECODE = "LLA decode step tokens/s (one token per sequence) and HBM GB/s at d=128 bf16; fraction of HBM peak"
 METRIC_PARALLAX = "causal Parallax-form fwd (caller probe) tokens/s & TFLOP/s at d=128 bf16; fraction of BF16 tensor peak"
+METRIC_BACKWARD = "causal LLA backward (dq, dk, dv) tokens/s & TFLOP/s at d=128, bf16 inputs; fraction of fp32 ALU peak"
 
 
 def useful_flops(w, T):
@@ -57,6 +58,19 @@ def parallax_executed_flops(w, tensor):
     """Adds the max sweep's q.k, the recomputed q.k of the moment and output sweeps and, on the
     tensor path, the probe's lo-part product."""
     return (7 if tensor else 6) * 2 * w.d * (w.n * (w.n + 1) / 2 * w.B * w.H)
+
+
+def backward_useful_flops(w, T):
+    """(11 + 2T) causal passes of 2d flops per pair: q.k, g.v, the two moment sums, T CG
+    iterations of (p.k, accumulate), rho'.k and y.k, and the dq, dk (three terms) and dv sums."""
+    return (11 + 2 * T) * 2 * w.d * (w.n * (w.n + 1) / 2 * w.B * w.H)
+
+
+def backward_executed_flops(w, T):
+    """As the two kernels run them: the query-major kernel recomputes q.k in its max sweep,
+    moment sweep, every CG iteration and the dq sweep (and g.v twice); the key-major kernel
+    recomputes q.k, rho'.k, y.k and g.v: (18 + 3T) passes of 2d per pair."""
+    return (18 + 3 * T) * 2 * w.d * (w.n * (w.n + 1) / 2 * w.B * w.H)
 
 
 def load_peaks():
@@ -147,10 +161,13 @@ def load_traffic(kernel, workload_name):
 
 # ----------------------------------------------------------------------------- CPU oracle timing
 
-def _oracle_row(op, q, k, v, probe, tau, lam, b, h, i):
-    from oracle.lla_ref import lla_row, parallax_row
+def _oracle_row(op, q, k, v, extra, tau, lam, b, h, i):
+    """One oracle row: extra is the probe (parallax) or the output cotangent (backward)."""
+    from oracle.lla_ref import lla_row, lla_row_grad, parallax_row
     if op == "parallax":
-        return parallax_row(q[b, h, i], k[b, h, : i + 1], v[b, h, : i + 1], probe[b, h, i], tau)
+        return parallax_row(q[b, h, i], k[b, h, : i + 1], v[b, h, : i + 1], extra[b, h, i], tau)
+    if op == "backward":
+        return lla_row_grad(q[b, h, i], k[b, h, : i + 1], v[b, h, : i + 1], extra[b, h, i], tau, lam)
     return lla_row(q[b, h, i], k[b, h, : i + 1], v[b, h, : i + 1], tau, lam)
 
 
@@ -206,7 +223,8 @@ def cpu_oracle_throughput(w, qkv, budget_s=15.0, seed=123, op="lla", probe=None)
     return {"value": tokens / est_wall, "unit": "tokens/s", "cores": cores, "kind": "oracle",
             "sample": (f"{len(pts)} random (b,h,i) rows of {w.name} "
                        + ("in the Parallax form (float64, explicit Sigma_KV)" if op == "parallax" else
-                          "solved exactly (float64, dense Sigma, Cholesky)")
+                          "differentiated exactly (float64, dense Sigma, Cholesky, adjoint solve)" if op == "backward"
+                          else "solved exactly (float64, dense Sigma, Cholesky)")
                        + f" in {wall:.1f} s on {cores} processes; per-row cost a+b(i+1) fitted and "
                        f"integrated over all {w.B * w.H * w.n} rows: est. {est_wall:.0f} s per step"),
             "est_seconds_per_step": est_wall}
@@ -224,9 +242,9 @@ def parse():
     ap.add_argument("--path", choices=["auto", "tensor", "fp32"], default="auto")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--op", choices=["lla", "parallax", "decode"], default="lla",
+    ap.add_argument("--op", choices=["lla", "parallax", "decode", "backward"], default="lla",
                     help="lla: the LLA forward (default); parallax: the Parallax form with a synthetic probe; "
-                         "decode: one decode step (use --workload decode_bf16)")
+                         "decode: one decode step (use --workload decode_bf16); backward: dq, dk, dv of the forward")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch B (a smaller case for profiler captures)")
     return ap.parse_args()
@@ -252,26 +270,29 @@ def run_reference(args, world, rank):
     if args.op == "decode":
         run_reference_decode(args)
         return
-    from local_linear_attention_flashlla_gb300.inputs import make_inputs, make_probe, workload
+    from local_linear_attention_flashlla_gb300.inputs import make_cotangent, make_inputs, make_probe, workload
     w = workload(args.workload) if args.batch is None else workload(args.workload, B=args.batch)
     qkv = make_inputs(w)
     parallax = args.op == "parallax"
-    probe = make_probe(w) if parallax else None
+    backward = args.op == "backward"
+    extra = make_probe(w) if parallax else make_cotangent(w) if backward else None
     steps = []
     cb = None
     for s in range(args.warmup + args.steps):
-        cb = cpu_oracle_throughput(w, qkv, budget_s=4.0, seed=1000 + s, op=args.op, probe=probe)
+        cb = cpu_oracle_throughput(w, qkv, budget_s=4.0, seed=1000 + s, op=args.op, probe=extra)
         if s >= args.warmup:
             steps.append(cb["est_seconds_per_step"])
     sec = statistics.mean(steps)
     value = w.B * w.n / sec
     T = w.cg_max_iters
-    line = {"impl": "reference", "metric": METRIC_PARALLAX if parallax else METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+    metric = METRIC_PARALLAX if parallax else METRIC_BACKWARD if backward else METRIC
+    flops = parallax_useful_flops(w) if parallax else backward_useful_flops(w, T) if backward else useful_flops(w, T)
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": f"{w.name} B={w.B} H={w.H} n={w.n} d={w.d} tau={w.tau:.5g} lambda={w.lam} "
                                    f"cg_iters={T} cg_tol={w.cg_tol}", "l2": "n/a (CPU)"},
-            "tflops": (parallax_useful_flops(w) if parallax else useful_flops(w, T)) / sec / 1e12,
+            "tflops": flops / sec / 1e12,
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cb["cores"], "kind": "oracle",
                              "sample": cb["sample"]},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -474,6 +495,137 @@ def run_decode(args, world, rank, local):
         torch.distributed.destroy_process_group()
 
 
+def run_backward(args, world, rank, local):
+    """One step = one lla_backward call over the whole workload: dq, dk, dv of sum(dout * out)
+    with q, k, v, dout and the forward's rho, denom resident in HBM (the forward runs once,
+    untimed, before the loop: its outputs are the backward's inputs)."""
+    import torch
+
+    import local_linear_attention_flashlla_gb300 as lla
+    from local_linear_attention_flashlla_gb300.inputs import make_cotangent, make_inputs, workload
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    w = workload(args.workload) if args.batch is None else workload(args.workload, B=args.batch)
+    wr = w.with_(seed=w.seed + rank)
+    qkv_host = make_inputs(wr)
+    g_host = make_cotangent(wr)
+    q, k, v = (t.to(dev) for t in qkv_host)
+    g = g_host.to(dev)
+    T = w.cg_max_iters
+    _, rho, den = lla.forward(q, k, v, w.tau, w.lam, T, w.cg_tol)
+    grads = [torch.empty(q.shape, dtype=torch.float32, device=dev) for _ in range(3)]
+    ws = torch.empty(lla.lla_backward_workspace_size(w.B, w.H, w.n, w.d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(qq=q, kk=k, vv=v, rr=rho, dd=den, gg=g):
+        lla.backward(qq, kk, vv, rr, dd, gg, w.tau, w.lam, T, w.cg_tol, dq=grads[0], dk=grads[1], dv=grads[2],
+                     workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    lla.lla_sync_status()
+    lla.lla_profile_enable(True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    times, main_times = [], []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1))
+        main_times.append(lla.lla_profile_read())
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    lla.lla_profile_enable(False)
+    lla.lla_sync_status()
+    total_ms = sum(times)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    tokens = w.B * w.n
+    value = world * tokens * args.steps / (total_ms / 1e3)
+    flops = backward_useful_flops(w, T)
+    q_ms = sum(m for m, _ in main_times) / len(main_times)          # query-major kernel
+    call_ms = sum(t_ for _, t_ in main_times) / len(main_times)     # the whole call
+    k_ms = max(call_ms - q_ms, 1e-9)                                 # key-major kernel
+    pairs_flops = 2 * w.d * (w.n * (w.n + 1) / 2 * w.B * w.H)
+    q_flops = (7 + 2 * T) * pairs_flops      # the query kernel's useful share: q.k, g.v, moments, CG, rho'.k, y.k, dq
+    k_flops = 4 * pairs_flops                # the key kernel's: dk (three terms) and dv sums
+    peaks, peak_kind = load_peaks()
+    peak = fp32_alu_peak_tflops(peaks.get("sm_max_mhz", 2070.0))
+    achieved = q_flops / (q_ms / 1e3) / 1e12
+
+    e2e = None
+    if not args.no_e2e:
+        hin = [t.pin_memory() for t in (*qkv_host, g_host)] + [rho.cpu().pin_memory(), den.cpu().pin_memory()]
+        hout = [torch.empty(q.shape, dtype=torch.float32).pin_memory() for _ in range(3)]
+        din = [torch.empty_like(t, device=dev) for t in hin]
+        e2e_ms = []
+        for it in range(args.warmup + args.steps):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for d_, h_ in zip(din, hin):
+                d_.copy_(h_, non_blocking=True)
+            step(din[0], din[1], din[2], din[4], din[5], din[3])
+            for h_, d_ in zip(hout, grads):
+                h_.copy_(d_, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            if it >= args.warmup:
+                e2e_ms.append(e0.elapsed_time(e1))
+        tot = sum(e2e_ms)
+        if world > 1:
+            t = torch.tensor([tot], dtype=torch.float64, device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            tot = float(t.item())
+        e2e = {"value": world * tokens * len(e2e_ms) / (tot / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout)}
+
+    line = {"metric": METRIC_BACKWARD, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"{w.name} B={w.B} H={w.H} n={w.n} d={w.d} tau={w.tau:.5g} lambda={w.lam} "
+                                   f"cg_iters={T} cg_tol={w.cg_tol} (forward and adjoint)",
+                       "l2": "flushed before every step (512 MiB write)",
+                       "inputs": f"{w.dtype} q,k,v,dout and the forward's fp32 rho, denom resident in HBM"},
+            "tflops": world * flops * args.steps / (total_ms / 1e3) / 1e12,
+            "tflops_executed": world * backward_executed_flops(w, T) * args.steps / (total_ms / 1e3) / 1e12,
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": load_traffic("lla_bwd_query_kernel", w.name),
+                         "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 flops x max SM clock",
+                         "flops_counted": "query-major kernel, useful (7+2T) passes x 2d per causal pair"},
+            "clocks": clocks, "e2e": e2e, "gpu_launches": 2 * args.steps,
+            "dominant_kernel": {"name": "lla_bwd_query_kernel", "ms_per_launch": q_ms,
+                                "share_of_step": q_ms / ms_per_step},
+            "second_kernel": {"name": "lla_bwd_key_kernel", "ms_per_launch": k_ms,
+                              "tflops_useful": k_flops / (k_ms / 1e3) / 1e12},
+            "cg_iters_counted": T}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_oracle_throughput(w, qkv_host, op="backward", probe=g_host)
+        line["cpu_baseline"].pop("est_seconds_per_step", None)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup(args)
@@ -482,6 +634,9 @@ def main():
         return
     if args.op == "decode":
         run_decode(args, world, rank, local)
+        return
+    if args.op == "backward":
+        run_backward(args, world, rank, local)
         return
     import numpy as np
     import torch
