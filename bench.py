@@ -559,12 +559,12 @@ def run_backward(args, world, rank, local):
     tokens = w.B * w.n
     value = world * tokens * args.steps / (total_ms / 1e3)
     flops = backward_useful_flops(w, T)
-    q_ms = sum(m for m, _ in main_times) / len(main_times)          # query-major kernel
+    q_ms = sum(m for m, _ in main_times) / len(main_times)          # stats kernel (moments and adjoint CG)
     call_ms = sum(t_ for _, t_ in main_times) / len(main_times)     # the whole call
-    k_ms = max(call_ms - q_ms, 1e-9)                                 # key-major kernel
+    k_ms = max(call_ms - q_ms, 1e-9)                                 # dq and key-major kernels
     pairs_flops = 2 * w.d * (w.n * (w.n + 1) / 2 * w.B * w.H)
-    q_flops = (7 + 2 * T) * pairs_flops      # the query kernel's useful share: q.k, g.v, moments, CG, rho'.k, y.k, dq
-    k_flops = 4 * pairs_flops                # the key kernel's: dk (three terms) and dv sums
+    q_flops = (4 + 2 * T) * pairs_flops      # the stats kernel's useful share: q.k, g.v, two moment sums, CG
+    k_flops = 7 * pairs_flops                # the rest: rho'.k, y.k, dq; dk (three terms) and dv
     peaks, peak_kind = load_peaks()
     peak = fp32_alu_peak_tflops(peaks.get("sm_max_mhz", 2070.0))
     achieved = q_flops / (q_ms / 1e3) / 1e12
@@ -608,13 +608,13 @@ def run_backward(args, world, rank, local):
             "tflops": world * flops * args.steps / (total_ms / 1e3) / 1e12,
             "tflops_executed": world * backward_executed_flops(w, T) * args.steps / (total_ms / 1e3) / 1e12,
             "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": load_traffic("lla_bwd_query_kernel", w.name),
+                         "frac": achieved / peak, "traffic": load_traffic("lla_bwd_stats_kernel", w.name),
                          "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 flops x max SM clock",
-                         "flops_counted": "query-major kernel, useful (7+2T) passes x 2d per causal pair"},
-            "clocks": clocks, "e2e": e2e, "gpu_launches": 2 * args.steps,
-            "dominant_kernel": {"name": "lla_bwd_query_kernel", "ms_per_launch": q_ms,
+                         "flops_counted": "stats kernel, useful (4+2T) passes x 2d per causal pair"},
+            "clocks": clocks, "e2e": e2e, "gpu_launches": 3 * args.steps,
+            "dominant_kernel": {"name": "lla_bwd_stats_kernel", "ms_per_launch": q_ms,
                                 "share_of_step": q_ms / ms_per_step},
-            "second_kernel": {"name": "lla_bwd_key_kernel", "ms_per_launch": k_ms,
+            "other_kernels": {"names": ["lla_bwd_dq_kernel", "lla_bwd_key_kernel"], "ms_per_step": k_ms,
                               "tflops_useful": k_flops / (k_ms / 1e3) / 1e12},
             "cg_iters_counted": T}
     if rank == 0 and not args.no_cpu_baseline:

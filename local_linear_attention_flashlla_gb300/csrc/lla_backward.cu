@@ -21,13 +21,13 @@
 // and the adjoint u = -(1 + delta.rho') y/omega carry the factor 1 + delta.rho', which is in the
 // thousands for a query outside the span of its keys and costs fp32 most of its digits.
 //
-// Two kernels and no atomics, so the result does not depend on scheduling:
-//  * query-major, one CTA per tile of BQ queries of one (b, h): the row maximum and its index,
-//    the moments omega, kbar, hbar, tbar (one sweep over keys and values), CG for y, then a
-//    sweep that forms dq_i.  Per-row scalars and y go to the workspace.
+// Three kernels and no atomics, so the result does not depend on scheduling:
+//  * stats, query-major, one CTA per tile of BQ queries of one (b, h): the row maximum and its
+//    index, the moments omega, kbar, hbar, tbar (one sweep over keys and values) and CG for y.
+//    Per-row scalars (RowRec) and y go to the workspace.
+//  * dq, query-major: one sweep over keys and values that forms dq_i from the records.
 //  * key-major, one CTA per block of BK keys: sweeps the query tiles at or after the block,
-//    forms Ahat, Bhat, ds for every pair from the per-row records and sums dk_j and dv_j in
-//    registers.
+//    forms Ahat, Bhat, ds for every pair from the records and sums dk_j and dv_j in registers.
 // Every product, sum and CG quantity is fp32.  Thread layout as in the fp32 forward path:
 // 256 threads, the 8 consecutive lanes 8r..8r+7 own row r (a query row in the first kernel, a
 // key row in the second); pair tiles split the other side's rows j = lane8 + 8c, d-vectors
@@ -177,9 +177,9 @@ struct KSmem {
 
 template <int D, typename T>
 __global__ void __launch_bounds__(NT, 1)
-lla_bwd_query_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+lla_bwd_stats_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                      const T* __restrict__ dout, const float* __restrict__ rho, const float* __restrict__ denom,
-                     float* __restrict__ dq, RowRec* __restrict__ rec, float* __restrict__ uvec,
+                     RowRec* __restrict__ rec, float* __restrict__ uvec,
                      int* __restrict__ cg_iters, int n, int n_tiles, float tau, float lambda, int cg_max_iters,
                      float cg_tol) {
     constexpr int E = D / 8;  // coordinates per lane
@@ -347,7 +347,7 @@ lla_bwd_query_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
         }
     }
 
-    // ---- the sweep that forms dq_i -------------------------------------------------------------
+    // ---- per-row record and y ------------------------------------------------------------------
     float kr = 0.f, ky = 0.f, ry = 0.f;
 #pragma unroll
     for (int c = 0; c < E; ++c) {
@@ -358,12 +358,60 @@ lla_bwd_query_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
     kr = row_sum8(kr);
     ky = row_sum8(ky);
     ry = row_sum8(ry);
-    const float sd = -lambda * inv_omega * ry;   // sum_j ds_j, the path through the row maximum
-    __syncthreads();
+    if (row_ok) {
 #pragma unroll
-    for (int c = 0; c < E; ++c) {
-        sm.p[r][l8 + 8 * c] = rp[c];
-        sm.u[r][l8 + 8 * c] = x[c];
+        for (int c = 0; c < E; ++c) uvec[rbase + l8 + 8 * c] = x[c];
+        if (l8 == 0) {
+            if (jm < 0 || jm > i) jm = 0;   // only when every logit of the row is NaN
+            RowRec o;
+            o.m = m_row;
+            o.jm = jm;
+            o.inv_omega = inv_omega;
+            o.hbar = hbar;
+            o.kb_rp = kr;
+            o.kb_y = ky;
+            o.sd = -lambda * inv_omega * ry;   // sum_j ds_j, the path through the row maximum
+            o.rp_scale = rp_scale;
+            rec[head * (size_t)n + i] = o;
+            if (cg_iters) cg_iters[head * (size_t)n + i] = iters;
+        }
+    }
+}
+
+// dq_i = tau (sum_j ds_ij k_j - sd_i k_jm) + y_i, one CTA per tile of BQ queries, from the
+// per-row records and y.
+template <int D, typename T>
+__global__ void __launch_bounds__(NT, 1)
+lla_bwd_dq_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                  const T* __restrict__ dout, const float* __restrict__ rho, const RowRec* __restrict__ rec,
+                  const float* __restrict__ uvec, float* __restrict__ dq, int n, int n_tiles, float tau) {
+    constexpr int E = D / 8;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    QSmem<D>& sm = *reinterpret_cast<QSmem<D>*>(smem_raw);
+
+    const int tile = n_tiles - 1 - (int)blockIdx.x;
+    const size_t head = blockIdx.y;
+    const size_t hoff = head * (size_t)n * D;
+    const T* kh = k + hoff;
+    const T* vh = v + hoff;
+    const int tid = threadIdx.x;
+    const int r = tid >> 3;
+    const int l8 = tid & 7;
+    const int i0 = tile * BQ;
+    const int i = i0 + r;
+    const bool row_ok = i < n;
+    const int last_key = min(n - 1, i0 + BQ - 1);
+    const int n_blocks = last_key / BK + 1;
+
+    RowRec R{};
+    if (row_ok) R = rec[head * (size_t)n + i];
+    load_rows<D>(sm.q, q + hoff, i0, BQ, n);
+    load_rows<D>(sm.g, dout + hoff, i0, BQ, n);
+    load_rows<D>(sm.u, uvec + hoff, i0, BQ, n);
+#pragma unroll
+    for (int c = 0; c < E; ++c) {   // rho' = (omega/denom) rho; each row is read by its own lanes only
+        const int e = l8 + 8 * c;
+        sm.p[r][e] = row_ok ? __ldg(rho + hoff + (size_t)i * D + e) * R.rp_scale : 0.f;
     }
     float dqa[E];
 #pragma unroll
@@ -379,35 +427,21 @@ lla_bwd_query_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
 #pragma unroll
         for (int c = 0; c < JPT; ++c) {
             const int j = kb * BK + l8 + 8 * c;
-            const float wb = (j <= i && row_ok) ? expf(tau * s[c] - m_row) * inv_omega : 0.f;
-            const float Ah = 1.f - (a1[c] - kr);
-            const float Bh = (hh[c] - hbar) - (a2[c] - ky);
+            const float wb = (j <= i && row_ok) ? expf(tau * s[c] - R.m) * R.inv_omega : 0.f;
+            const float Ah = 1.f - (a1[c] - R.kb_rp);
+            const float Bh = (hh[c] - R.hbar) - (a2[c] - R.kb_y);
             sm.m[r][l8 + 8 * c] = wb * Ah * Bh;
         }
         __syncwarp();
         acc_rows<D>(sm.m, sm.kb, r, l8, dqa);
     }
     if (row_ok) {
-        if (jm < 0 || jm > i) jm = 0;   // only when every logit of the row is NaN
-        const T* kjm = kh + (size_t)jm * D;
+        const T* kjm = kh + (size_t)R.jm * D;
+        const size_t rbase = hoff + (size_t)i * D;
 #pragma unroll
         for (int c = 0; c < E; ++c) {
             const int e = l8 + 8 * c;
-            dq[rbase + e] = fmaf(tau, dqa[c] - sd * ld_f(kjm + e), x[c]);
-            uvec[rbase + e] = x[c];
-        }
-        if (l8 == 0) {
-            RowRec o;
-            o.m = m_row;
-            o.jm = jm;
-            o.inv_omega = inv_omega;
-            o.hbar = hbar;
-            o.kb_rp = kr;
-            o.kb_y = ky;
-            o.sd = sd;
-            o.rp_scale = rp_scale;
-            rec[head * (size_t)n + i] = o;
-            if (cg_iters) cg_iters[head * (size_t)n + i] = iters;
+            dq[rbase + e] = fmaf(tau, dqa[c] - R.sd * ld_f(kjm + e), sm.u[r][e]);
         }
     }
 }
@@ -507,10 +541,13 @@ cudaError_t launch_bwd_typed(const BackwardProblem& p, void* workspace, cudaStre
     RowRec* rec = static_cast<RowRec*>(workspace);
     float* uvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * sizeof(RowRec)));
 
-    auto kq = lla_bwd_query_kernel<D, T>;
+    auto ks = lla_bwd_stats_kernel<D, T>;
+    auto kd = lla_bwd_dq_kernel<D, T>;
     auto kk = lla_bwd_key_kernel<D, T>;
     const size_t smq = sizeof(QSmem<D>), smk = sizeof(KSmem<D>);
-    cudaError_t err = cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smq);
+    cudaError_t err = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smq);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(kd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smq);
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smk);
     if (err != cudaSuccess) return err;
@@ -520,10 +557,12 @@ cudaError_t launch_bwd_typed(const BackwardProblem& p, void* workspace, cudaStre
     const T* v = static_cast<const T*>(p.v);
     const T* g = static_cast<const T*>(p.dout);
     if (p.ev_main_begin && (err = cudaEventRecord(p.ev_main_begin, stream)) != cudaSuccess) return err;
-    kq<<<grid, NT, smq, stream>>>(q, k, v, g, p.rho, p.denom, p.dq, rec, uvec, p.cg_iters, p.n, n_tiles, p.tau,
-                                  p.lambda, p.cg_max_iters, p.cg_tol);
+    ks<<<grid, NT, smq, stream>>>(q, k, v, g, p.rho, p.denom, rec, uvec, p.cg_iters, p.n, n_tiles, p.tau, p.lambda,
+                                  p.cg_max_iters, p.cg_tol);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     if (p.ev_main_end && (err = cudaEventRecord(p.ev_main_end, stream)) != cudaSuccess) return err;
+    kd<<<grid, NT, smq, stream>>>(q, k, v, g, p.rho, rec, uvec, p.dq, p.n, n_tiles, p.tau);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
     kk<<<grid, NT, smk, stream>>>(q, k, v, g, p.rho, rec, uvec, p.dk, p.dv, p.n, n_tiles, p.tau);
     return cudaGetLastError();
 }
