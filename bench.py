@@ -66,11 +66,15 @@ def backward_useful_flops(w, T):
     return (11 + 2 * T) * 2 * w.d * (w.n * (w.n + 1) / 2 * w.B * w.H)
 
 
-def backward_executed_flops(w, T):
-    """As the two kernels run them: the query-major kernel recomputes q.k in its max sweep,
-    moment sweep, every CG iteration and the dq sweep (and g.v twice); the key-major kernel
-    recomputes q.k, rho'.k, y.k and g.v: (18 + 3T) passes of 2d per pair."""
-    return (18 + 3 * T) * 2 * w.d * (w.n * (w.n + 1) / 2 * w.B * w.H)
+def backward_executed_flops(w, T, tensor=False):
+    """As the kernels run them.  fp32 stats kernel: q.k in the max sweep, q.k, g.v and the two
+    moment sums, 3 passes per CG iteration (5 + 3T).  Tensor stats kernel: S in the max sweep;
+    S, H = G V^T and the hi + lo weight products in the moment and TBAR sweeps; S, the hi + lo
+    direction products and the hi + lo coefficient products per CG iteration (9 + 5T).  Then the
+    dq kernel (q.k, rho'.k, y.k, g.v, dq: 5) and the key-major kernel (the same four dots, dk
+    three terms, dv: 8)."""
+    stats = (9 + 5 * T) if tensor else (5 + 3 * T)
+    return (stats + 13) * 2 * w.d * (w.n * (w.n + 1) / 2 * w.B * w.H)
 
 
 def load_peaks():
@@ -513,15 +517,19 @@ def run_backward(args, world, rank, local):
     q, k, v = (t.to(dev) for t in qkv_host)
     g = g_host.to(dev)
     T = w.cg_max_iters
+    path = {"auto": lla.LLA_PATH_AUTO, "tensor": lla.LLA_PATH_TENSOR, "fp32": lla.LLA_PATH_FP32}[args.path]
+    dtype_code = lla.LLA_DTYPE_BF16 if w.dtype == "bf16" else lla.LLA_DTYPE_FP32
+    rpath = lla.lla_resolve_path(dtype_code, path, w.d)
     _, rho, den = lla.forward(q, k, v, w.tau, w.lam, T, w.cg_tol)
     grads = [torch.empty(q.shape, dtype=torch.float32, device=dev) for _ in range(3)]
-    ws = torch.empty(lla.lla_backward_workspace_size(w.B, w.H, w.n, w.d), dtype=torch.uint8, device=dev)
+    ws = torch.empty(lla.lla_backward_workspace_size(dtype_code, path, w.B, w.H, w.n, w.d), dtype=torch.uint8,
+                     device=dev)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def step(qq=q, kk=k, vv=v, rr=rho, dd=den, gg=g):
-        lla.backward(qq, kk, vv, rr, dd, gg, w.tau, w.lam, T, w.cg_tol, dq=grads[0], dk=grads[1], dv=grads[2],
-                     workspace=ws)
+        lla.backward(qq, kk, vv, rr, dd, gg, w.tau, w.lam, T, w.cg_tol, path=path, dq=grads[0], dk=grads[1],
+                     dv=grads[2], workspace=ws)
 
     for _ in range(args.warmup):
         step()
@@ -561,13 +569,31 @@ def run_backward(args, world, rank, local):
     flops = backward_useful_flops(w, T)
     q_ms = sum(m for m, _ in main_times) / len(main_times)          # stats kernel (moments and adjoint CG)
     call_ms = sum(t_ for _, t_ in main_times) / len(main_times)     # the whole call
-    k_ms = max(call_ms - q_ms, 1e-9)                                 # dq and key-major kernels
+    k_ms = max(call_ms - q_ms, 1e-9)                                 # dq and key-major kernels (fp32; tensor path: + pre-pass)
     pairs_flops = 2 * w.d * (w.n * (w.n + 1) / 2 * w.B * w.H)
-    q_flops = (4 + 2 * T) * pairs_flops      # the stats kernel's useful share: q.k, g.v, two moment sums, CG
+    q_flops = (4 + 2 * T) * pairs_flops      # the stats stage's useful share: q.k, g.v, two moment sums, CG
     k_flops = 7 * pairs_flops                # the rest: rho'.k, y.k, dq; dk (three terms) and dv
     peaks, peak_kind = load_peaks()
-    peak = fp32_alu_peak_tflops(peaks.get("sm_max_mhz", 2070.0))
-    achieved = q_flops / (q_ms / 1e3) / 1e12
+    alu_peak = fp32_alu_peak_tflops(peaks.get("sm_max_mhz", 2070.0))
+    stats_tensor = rpath == lla.LLA_PATH_TENSOR
+    if stats_tensor:
+        stats_peak, stats_bound, stats_src = peaks["bf16_tflops"], "tensor", f"{peak_kind} bf16 burst"
+    else:
+        stats_peak, stats_bound, stats_src = alu_peak, "alu", "derived: 152 SMs x 128 fp32 FMA lanes x 2 flops x max SM clock"
+    stats_roof = {"bound": stats_bound, "achieved": q_flops / (q_ms / 1e3) / 1e12, "peak": stats_peak,
+                  "unit": "TFLOP/s", "frac": q_flops / (q_ms / 1e3) / 1e12 / stats_peak,
+                  "traffic": load_traffic("lla_tc_kernel_bwd" if stats_tensor else "lla_bwd_stats_kernel", w.name),
+                  "peak_source": stats_src,
+                  "flops_counted": "stats stage, useful (4+2T) passes x 2d per causal pair"
+                                   + ("; executed on tensor cores: (9+5T) passes (hi + lo operands)" if stats_tensor else "")}
+    rest_roof = {"bound": "alu", "achieved": k_flops / (k_ms / 1e3) / 1e12, "peak": alu_peak, "unit": "TFLOP/s",
+                 "frac": k_flops / (k_ms / 1e3) / 1e12 / alu_peak,
+                 "traffic": load_traffic("lla_bwd_dq_key_kernels", w.name),
+                 "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 flops x max SM clock",
+                 "flops_counted": "dq and key-major kernels, useful 7 passes x 2d per causal pair"}
+    stats_name = "lla_tc_kernel<128,bwd>" if stats_tensor else "lla_bwd_stats_kernel"
+    dominant_is_stats = q_ms >= k_ms
+    roof = stats_roof if dominant_is_stats else rest_roof
 
     e2e = None
     if not args.no_e2e:
@@ -600,22 +626,22 @@ def run_backward(args, world, rank, local):
 
     line = {"metric": METRIC_BACKWARD, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "vs_baseline": None, "dtype": "f16 hi+lo / f32" if stats_tensor else "f32", "data": "synthetic",
             "config": {"workload": f"{w.name} B={w.B} H={w.H} n={w.n} d={w.d} tau={w.tau:.5g} lambda={w.lam} "
                                    f"cg_iters={T} cg_tol={w.cg_tol} (forward and adjoint)",
                        "l2": "flushed before every step (512 MiB write)",
                        "inputs": f"{w.dtype} q,k,v,dout and the forward's fp32 rho, denom resident in HBM"},
             "tflops": world * flops * args.steps / (total_ms / 1e3) / 1e12,
-            "tflops_executed": world * backward_executed_flops(w, T) * args.steps / (total_ms / 1e3) / 1e12,
-            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": load_traffic("lla_bwd_stats_kernel", w.name),
-                         "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 flops x max SM clock",
-                         "flops_counted": "stats kernel, useful (4+2T) passes x 2d per causal pair"},
-            "clocks": clocks, "e2e": e2e, "gpu_launches": 3 * args.steps,
-            "dominant_kernel": {"name": "lla_bwd_stats_kernel", "ms_per_launch": q_ms,
-                                "share_of_step": q_ms / ms_per_step},
-            "other_kernels": {"names": ["lla_bwd_dq_kernel", "lla_bwd_key_kernel"], "ms_per_step": k_ms,
-                              "tflops_useful": k_flops / (k_ms / 1e3) / 1e12},
+            "tflops_executed": world * backward_executed_flops(w, T, stats_tensor) * args.steps / (total_ms / 1e3) / 1e12,
+            "roofline": roof, "clocks": clocks, "e2e": e2e,
+            "gpu_launches": (5 if stats_tensor else 3) * args.steps,
+            "dominant_kernel": {"name": stats_name if dominant_is_stats else "lla_bwd_dq_kernel + lla_bwd_key_kernel",
+                                "ms_per_launch": q_ms if dominant_is_stats else k_ms,
+                                "share_of_step": (q_ms if dominant_is_stats else k_ms) / ms_per_step},
+            "stages": {"stats": {"kernel": stats_name, "ms": q_ms, "roofline": stats_roof},
+                       "dq_dk_dv": {"kernels": ["lla_bwd_dq_kernel", "lla_bwd_key_kernel"], "ms": k_ms,
+                                    "roofline": rest_roof}},
+            "path": "tensor stats + fp32 dq/dk/dv" if stats_tensor else "fp32",
             "cg_iters_counted": T}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_throughput(w, qkv_host, op="backward", probe=g_host)

@@ -195,10 +195,17 @@ int lla_decode_max_n(int d);
  *     dv_j += wbar Ahat g_i,   dk_j += tau ds q_i - wbar (Ahat y_i + Bhat rho'_i),
  *     dq_i  = tau sum_j ds k_j + y_i,
  * plus the path through the row maximum m_i (to the first key index attaining it), whose
- * weight is sum_j ds = -(lambda/omega_i) rho'_i.y_i.  Every product and the CG state are fp32
- * (CUDA cores).
+ * weight is sum_j ds = -(lambda/omega_i) rho'_i.y_i.
+ *
+ * Three stages: stats (row maximum and its index, omega, kbar, hbar, the adjoint right-hand side
+ * and the adjoint CG), dq (a query-major sweep) and dk/dv (a key-major sweep).  On
+ * LLA_PATH_TENSOR the stats stage is the forward's tcgen05 kernel in its backward mode (fp16
+ * operands, fp32 accumulation and CG state); the dq and dk/dv stages, and every stage of
+ * LLA_PATH_FP32, are fp32 on CUDA cores.
  *
  * dtype      LLA_DTYPE_BF16 or LLA_DTYPE_FP32: q, k, v, dout share it.
+ * path       an lla_path value, resolved as for lla_forward_ex (LLA_PATH_TENSOR needs bf16 and
+ *            d in {64, 128}).
  * q, k, v    [B,H,n,d], the forward call's inputs.
  * rho        [B,H,n,d] fp32, denom [B,H,n] fp32: the forward call's outputs for these inputs
  *            (any path); the backward is exact to the extent they are.
@@ -208,18 +215,19 @@ int lla_decode_max_n(int d);
  * tau, lambda as for the forward call; cg_max_iters, cg_tol: the adjoint CG's cap and relative
  *            tolerance (||r|| <= cg_tol ||sum_j wbar_ij h_ij c_ij||), as for lla_forward.
  * workspace  NULL (scratch from the stream-ordered pool) or a device buffer of at least
- *            lla_backward_workspace_size(B, H, n, d) bytes, 256-byte aligned, not used
+ *            lla_backward_workspace_size(dtype, path, B, H, n, d) bytes, 256-byte aligned, not used
  *            concurrently by another call.
  * B*H <= 65535.  All pointers are device pointers, 16-byte aligned, owned by the caller.
  * Errors as for lla_forward_ex.
  */
-int lla_backward(int dtype, const void* q, const void* k, const void* v, const float* rho, const float* denom,
-                 const void* dout, float* dq, float* dk, float* dv, int* cg_iters, int B, int H, int n, int d,
-                 float tau, float lambda, int cg_max_iters, float cg_tol, void* workspace, size_t workspace_bytes,
-                 void* stream);
+int lla_backward(int dtype, int path, const void* q, const void* k, const void* v, const float* rho,
+                 const float* denom, const void* dout, float* dq, float* dk, float* dv, int* cg_iters, int B, int H,
+                 int n, int d, float tau, float lambda, int cg_max_iters, float cg_tol, void* workspace,
+                 size_t workspace_bytes, void* stream);
 
-/* Bytes of scratch lla_backward needs (per-query records and the adjoint vectors y). */
-size_t lla_backward_workspace_size(int B, int H, int n, int d);
+/* Bytes of scratch lla_backward needs for these arguments (per-query records, the adjoint
+ * vectors y and, on the tensor path, the fp16 operand copies and CG scratch). */
+size_t lla_backward_workspace_size(int dtype, int path, int B, int H, int n, int d);
 
 /* Message for the calling thread's most recent failure ("" if none). Owned by the library. */
 const char* lla_last_error(void);

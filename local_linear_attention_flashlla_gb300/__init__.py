@@ -48,9 +48,9 @@ _SIGNATURES = {
     "lla_decode": (_c_int, [_c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                             _c_float, _c_float, _c_int, _c_float, _vp]),
     "lla_decode_max_n": (_c_int, [_c_int]),
-    "lla_backward": (_c_int, [_c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
-                              _c_int, _c_float, _c_float, _c_int, _c_float, _vp, _c_size, _vp]),
-    "lla_backward_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int]),
+    "lla_backward": (_c_int, [_c_int, _c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int,
+                              _c_int, _c_int, _c_float, _c_float, _c_int, _c_float, _vp, _c_size, _vp]),
+    "lla_backward_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "lla_profile_enable": (_c_int, [_c_int]),
     "lla_profile_read": (_c_int, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]),
     "lla_version": (_c_int, []),
@@ -206,20 +206,20 @@ def decode(q, k_cache, v_cache, n, tau, lam, cg_max_iters, cg_tol=0.0, *, return
     return out, rho, denom
 
 
-def lla_backward(dtype, q_ptr, k_ptr, v_ptr, rho_ptr, denom_ptr, dout_ptr, dq_ptr, dk_ptr, dv_ptr, iters_ptr, B, H,
-                 n, d, tau, lam, cg_max_iters, cg_tol, ws_ptr, ws_bytes, stream_ptr):
+def lla_backward(dtype, path, q_ptr, k_ptr, v_ptr, rho_ptr, denom_ptr, dout_ptr, dq_ptr, dk_ptr, dv_ptr, iters_ptr,
+                 B, H, n, d, tau, lam, cg_max_iters, cg_tol, ws_ptr, ws_bytes, stream_ptr):
     """Raw backward entry point on device pointers (ints); raises LLAError on failure."""
-    _check(load_library().lla_backward(dtype, q_ptr, k_ptr, v_ptr, rho_ptr, denom_ptr, dout_ptr, dq_ptr, dk_ptr,
+    _check(load_library().lla_backward(dtype, path, q_ptr, k_ptr, v_ptr, rho_ptr, denom_ptr, dout_ptr, dq_ptr, dk_ptr,
                                        dv_ptr, iters_ptr, B, H, n, d, tau, lam, cg_max_iters, cg_tol, ws_ptr,
                                        ws_bytes, stream_ptr))
 
 
-def lla_backward_workspace_size(B, H, n, d):
-    return load_library().lla_backward_workspace_size(B, H, n, d)
+def lla_backward_workspace_size(dtype, path, B, H, n, d):
+    return load_library().lla_backward_workspace_size(dtype, path, B, H, n, d)
 
 
-def backward(q, k, v, rho, denom, dout, tau, lam, cg_max_iters, cg_tol=0.0, *, return_iters=False, dq=None,
-             dk=None, dv=None, workspace=None, stream=None):
+def backward(q, k, v, rho, denom, dout, tau, lam, cg_max_iters, cg_tol=0.0, *, path=LLA_PATH_AUTO,
+             return_iters=False, dq=None, dk=None, dv=None, workspace=None, stream=None):
     """Gradients (dq, dk, dv) [B, H, n, d] fp32 of sum(dout * out) for the forward call that gave
     rho [B, H, n, d] and denom [B, H, n] on q, k, v (see include/lla.h).  With return_iters also
     the adjoint CG iteration counts [B, H, n].  Asynchronous on the current (or given) stream.
@@ -240,7 +240,7 @@ def backward(q, k, v, rho, denom, dout, tau, lam, cg_max_iters, cg_tol=0.0, *, r
         grads.append(torch.empty((B, H, n, d), dtype=torch.float32, device=q.device) if t is None else t)
     iters = torch.empty((B, H, n), dtype=torch.int32, device=q.device) if return_iters else None
     ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(), workspace.numel() * workspace.element_size())
-    lla_backward(dtype, q.data_ptr(), k.data_ptr(), v.data_ptr(), rho.data_ptr(), denom.data_ptr(), dout.data_ptr(),
+    lla_backward(dtype, path, q.data_ptr(), k.data_ptr(), v.data_ptr(), rho.data_ptr(), denom.data_ptr(), dout.data_ptr(),
                  grads[0].data_ptr(), grads[1].data_ptr(), grads[2].data_ptr(),
                  None if iters is None else iters.data_ptr(), B, H, n, d, float(tau), float(lam), int(cg_max_iters),
                  float(cg_tol), ws_ptr, ws_bytes, _stream_ptr(stream))

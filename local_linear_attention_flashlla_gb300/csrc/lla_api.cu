@@ -261,15 +261,15 @@ int lla_decode(int dtype, const void* q, const void* k, const void* v, void* out
     return LLA_OK;
 }
 
-size_t lla_backward_workspace_size(int B, int H, int n, int d) {
+size_t lla_backward_workspace_size(int dtype, int path, int B, int H, int n, int d) {
     if (B < 1 || H < 1 || n < 1 || d < 1) return 0;
-    return lla::backward_workspace_bytes(B, H, n, d);
+    return lla::backward_workspace_bytes(lla_resolve_path(dtype, path, d), B, H, n, d);
 }
 
-int lla_backward(int dtype, const void* q, const void* k, const void* v, const float* rho, const float* denom,
-                 const void* dout, float* dq, float* dk, float* dv, int* cg_iters, int B, int H, int n, int d,
-                 float tau, float lambda, int cg_max_iters, float cg_tol, void* workspace, size_t workspace_bytes,
-                 void* stream_) {
+int lla_backward(int dtype, int path, const void* q, const void* k, const void* v, const float* rho,
+                 const float* denom, const void* dout, float* dq, float* dk, float* dv, int* cg_iters, int B, int H,
+                 int n, int d, float tau, float lambda, int cg_max_iters, float cg_tol, void* workspace,
+                 size_t workspace_bytes, void* stream_) {
     lla::g_msg[0] = '\0';
     if (!q || !k || !v || !rho || !denom || !dout || !dq || !dk || !dv)
         return fail(LLA_ERR_INVALID_ARG, "null tensor pointer");
@@ -286,7 +286,11 @@ int lla_backward(int dtype, const void* q, const void* k, const void* v, const f
     if (cg_max_iters < 1 || cg_max_iters > 4096) return fail(LLA_ERR_INVALID_ARG, "cg_max_iters must be in [1, 4096]");
     if (!(cg_tol >= 0.f) || !(cg_tol < 1e30f)) return fail(LLA_ERR_INVALID_ARG, "cg_tol must be finite and >= 0");
     if (dtype != LLA_DTYPE_BF16 && dtype != LLA_DTYPE_FP32) return fail(LLA_ERR_INVALID_ARG, "unknown dtype %d", dtype);
-    const size_t need = lla::backward_workspace_bytes(B, H, n, d);
+    if (path < LLA_PATH_AUTO || path > LLA_PATH_FP32) return fail(LLA_ERR_INVALID_ARG, "unknown path %d", path);
+    const int rpath = lla_resolve_path(dtype, path, d);
+    if (rpath == LLA_PATH_TENSOR && (dtype != LLA_DTYPE_BF16 || (d != 64 && d != 128)))
+        return fail(LLA_ERR_UNSUPPORTED, "tensor path needs bf16 inputs and d in {64, 128}");
+    const size_t need = lla::backward_workspace_bytes(rpath, B, H, n, d);
     if (workspace) {
         if (workspace_bytes < need)
             return fail(LLA_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, need);
@@ -312,12 +316,13 @@ int lla_backward(int dtype, const void* q, const void* k, const void* v, const f
         cudaError_t e = cudaMallocAsync(&ws, need, stream);
         if (e != cudaSuccess) return lla::cuda_fail(e, "cudaMallocAsync(workspace)");
     }
-    cudaError_t e = lla::launch_backward(p, ws, stream);
+    const char* why = nullptr;
+    cudaError_t e = lla::launch_backward(p, rpath, ws, stream, &why);
     if (!workspace) {
         cudaError_t e2 = cudaFreeAsync(ws, stream);
         if (e == cudaSuccess && e2 != cudaSuccess) return lla::cuda_fail(e2, "cudaFreeAsync(workspace)");
     }
-    if (e != cudaSuccess) return lla::cuda_fail(e, "backward launch");
+    if (e != cudaSuccess) return lla::cuda_fail(e, why ? why : "backward launch");
     if (lla::g_prof_on) {
         e = cudaEventRecord(lla::g_ev[3], stream);
         if (e != cudaSuccess) return lla::cuda_fail(e, "profiling event record");

@@ -46,17 +46,7 @@ constexpr int BK = 32;       // equal to BQ: query tile t and key block t start 
 constexpr int NT = 256;
 constexpr int JPT = BK / 8;  // pair columns per lane
 
-// Per-query record handed from the query-major to the key-major kernel.
-struct __align__(16) RowRec {
-    float m;         // row maximum of tau q_i.k_j
-    int jm;          // first key index attaining it
-    float inv_omega; // 1 / omega
-    float hbar;      // sum_j wbar_j g_i.v_j
-    float kb_rp;     // kbar.rho'
-    float kb_y;      // kbar.y
-    float sd;        // -(lambda/omega) rho'.y
-    float rp_scale;  // omega / denom: rho' = rp_scale rho
-};
+using RowRec = BwdRowRec;
 
 __device__ __forceinline__ float ld_f(const float* p) { return __ldg(p); }
 __device__ __forceinline__ float ld_f(const __nv_bfloat16* p) { return __bfloat162float(*p); }
@@ -535,19 +525,29 @@ lla_bwd_key_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 template <int D, typename T>
-cudaError_t launch_bwd_typed(const BackwardProblem& p, void* workspace, cudaStream_t stream) {
+cudaError_t launch_stats_typed(const BackwardProblem& p, RowRec* rec, float* uvec, cudaStream_t stream) {
     const int n_tiles = (p.n + BQ - 1) / BQ;
-    const size_t rows = (size_t)p.B * p.H * p.n;
-    RowRec* rec = static_cast<RowRec*>(workspace);
-    float* uvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * sizeof(RowRec)));
-
     auto ks = lla_bwd_stats_kernel<D, T>;
+    const size_t smq = sizeof(QSmem<D>);
+    cudaError_t err = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smq);
+    if (err != cudaSuccess) return err;
+    const dim3 grid(n_tiles, p.B * p.H);
+    if (p.ev_main_begin && (err = cudaEventRecord(p.ev_main_begin, stream)) != cudaSuccess) return err;
+    ks<<<grid, NT, smq, stream>>>(static_cast<const T*>(p.q), static_cast<const T*>(p.k), static_cast<const T*>(p.v),
+                                  static_cast<const T*>(p.dout), p.rho, p.denom, rec, uvec, p.cg_iters, p.n, n_tiles,
+                                  p.tau, p.lambda, p.cg_max_iters, p.cg_tol);
+    if ((err = cudaGetLastError()) != cudaSuccess) return err;
+    if (p.ev_main_end && (err = cudaEventRecord(p.ev_main_end, stream)) != cudaSuccess) return err;
+    return cudaSuccess;
+}
+
+template <int D, typename T>
+cudaError_t launch_rest_typed(const BackwardProblem& p, const RowRec* rec, const float* uvec, cudaStream_t stream) {
+    const int n_tiles = (p.n + BQ - 1) / BQ;
     auto kd = lla_bwd_dq_kernel<D, T>;
     auto kk = lla_bwd_key_kernel<D, T>;
     const size_t smq = sizeof(QSmem<D>), smk = sizeof(KSmem<D>);
-    cudaError_t err = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smq);
-    if (err != cudaSuccess) return err;
-    err = cudaFuncSetAttribute(kd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smq);
+    cudaError_t err = cudaFuncSetAttribute(kd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smq);
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smk);
     if (err != cudaSuccess) return err;
@@ -556,11 +556,6 @@ cudaError_t launch_bwd_typed(const BackwardProblem& p, void* workspace, cudaStre
     const T* k = static_cast<const T*>(p.k);
     const T* v = static_cast<const T*>(p.v);
     const T* g = static_cast<const T*>(p.dout);
-    if (p.ev_main_begin && (err = cudaEventRecord(p.ev_main_begin, stream)) != cudaSuccess) return err;
-    ks<<<grid, NT, smq, stream>>>(q, k, v, g, p.rho, p.denom, rec, uvec, p.cg_iters, p.n, n_tiles, p.tau, p.lambda,
-                                  p.cg_max_iters, p.cg_tol);
-    if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    if (p.ev_main_end && (err = cudaEventRecord(p.ev_main_end, stream)) != cudaSuccess) return err;
     kd<<<grid, NT, smq, stream>>>(q, k, v, g, p.rho, rec, uvec, p.dq, p.n, n_tiles, p.tau);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
     kk<<<grid, NT, smk, stream>>>(q, k, v, g, p.rho, rec, uvec, p.dk, p.dv, p.n, n_tiles, p.tau);
@@ -568,26 +563,62 @@ cudaError_t launch_bwd_typed(const BackwardProblem& p, void* workspace, cudaStre
 }
 
 template <typename T>
-cudaError_t launch_bwd_dim(const BackwardProblem& p, void* workspace, cudaStream_t stream) {
+cudaError_t stats_dim(const BackwardProblem& p, RowRec* rec, float* uvec, cudaStream_t stream) {
     switch (p.d) {
-        case 16: return launch_bwd_typed<16, T>(p, workspace, stream);
-        case 32: return launch_bwd_typed<32, T>(p, workspace, stream);
-        case 64: return launch_bwd_typed<64, T>(p, workspace, stream);
-        case 128: return launch_bwd_typed<128, T>(p, workspace, stream);
+        case 16: return launch_stats_typed<16, T>(p, rec, uvec, stream);
+        case 32: return launch_stats_typed<32, T>(p, rec, uvec, stream);
+        case 64: return launch_stats_typed<64, T>(p, rec, uvec, stream);
+        case 128: return launch_stats_typed<128, T>(p, rec, uvec, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+cudaError_t rest_dim(const BackwardProblem& p, const RowRec* rec, const float* uvec, cudaStream_t stream) {
+    switch (p.d) {
+        case 16: return launch_rest_typed<16, T>(p, rec, uvec, stream);
+        case 32: return launch_rest_typed<32, T>(p, rec, uvec, stream);
+        case 64: return launch_rest_typed<64, T>(p, rec, uvec, stream);
+        case 128: return launch_rest_typed<128, T>(p, rec, uvec, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-size_t backward_workspace_bytes(int B, int H, int n, int d) {
+size_t backward_records_bytes(int B, int H, int n, int d) {
     const size_t rows = (size_t)B * H * n;
     return align256(rows * sizeof(RowRec)) + align256(rows * (size_t)d * sizeof(float));
 }
 
-cudaError_t launch_backward(const BackwardProblem& p, void* workspace, cudaStream_t stream) {
-    if (p.dtype == 1) return launch_bwd_dim<float>(p, workspace, stream);
-    return launch_bwd_dim<__nv_bfloat16>(p, workspace, stream);
+size_t backward_workspace_bytes(int path, int B, int H, int n, int d) {
+    const size_t recs = backward_records_bytes(B, H, n, d);
+    return path == 1 ? recs + tensor_backward_stats_bytes(B, H, n, d) : recs;
+}
+
+cudaError_t launch_backward_rest(const BackwardProblem& p, const BwdRowRec* rec, const float* yvec,
+                                 cudaStream_t stream) {
+    if (p.dtype == 1) return rest_dim<float>(p, rec, yvec, stream);
+    return rest_dim<__nv_bfloat16>(p, rec, yvec, stream);
+}
+
+cudaError_t launch_backward(const BackwardProblem& p, int path, void* workspace, cudaStream_t stream,
+                            const char** why) {
+    const size_t rows = (size_t)p.B * p.H * p.n;
+    RowRec* rec = static_cast<RowRec*>(workspace);
+    float* yvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * sizeof(RowRec)));
+    cudaError_t err;
+    if (path == 1) {
+        void* tws = static_cast<char*>(workspace) + backward_records_bytes(p.B, p.H, p.n, p.d);
+        err = launch_tensor_backward_stats(p, tws, rec, yvec, stream, why);
+        if (err != cudaSuccess) return err;
+    } else {
+        err = p.dtype == 1 ? stats_dim<float>(p, rec, yvec, stream) : stats_dim<__nv_bfloat16>(p, rec, yvec, stream);
+        if (err != cudaSuccess) { *why = "fp32 backward stats launch"; return err; }
+    }
+    err = launch_backward_rest(p, rec, yvec, stream);
+    if (err != cudaSuccess) *why = "backward dq / key-major launch";
+    return err;
 }
 
 }  // namespace lla

@@ -70,8 +70,30 @@ struct BackwardProblem {
     int dtype;           // lla_dtype
     cudaEvent_t ev_main_begin, ev_main_end;   // around the query-major kernel when profiling
 };
-size_t backward_workspace_bytes(int B, int H, int n, int d);
-cudaError_t launch_backward(const BackwardProblem& p, void* workspace, cudaStream_t stream);
+// Per-query record of the backward pass, written by the stats stage (fp32 or tensor path) and
+// read by the dq and key-major stages.
+struct __align__(16) BwdRowRec {
+    float m;         // row maximum of tau q_i.k_j (natural units: w_ij = exp(tau q_i.k_j - m))
+    int jm;          // first key index attaining it
+    float inv_omega; // 1 / omega
+    float hbar;      // sum_j wbar_j dout_i.v_j
+    float kb_rp;     // kbar.rho'
+    float kb_y;      // kbar.y
+    float sd;        // -(lambda/omega) rho'.y
+    float rp_scale;  // omega / denom: rho' = rp_scale rho
+};
+size_t backward_records_bytes(int B, int H, int n, int d);   // records + y, 256-byte aligned parts
+size_t backward_workspace_bytes(int path, int B, int H, int n, int d);
+// Whole backward on the given path (LLA_PATH_FP32 or LLA_PATH_TENSOR).
+cudaError_t launch_backward(const BackwardProblem& p, int path, void* workspace, cudaStream_t stream,
+                            const char** why);
+// The dq and key-major stages (fp32 CUDA cores) from the records and y.
+cudaError_t launch_backward_rest(const BackwardProblem& p, const BwdRowRec* rec, const float* yvec,
+                                 cudaStream_t stream);
+// The stats stage (max, moments, adjoint CG) on the tensor path; writes rec and yvec.
+size_t tensor_backward_stats_bytes(int B, int H, int n, int d);
+cudaError_t launch_tensor_backward_stats(const BackwardProblem& p, void* ws, BwdRowRec* rec, float* yvec,
+                                         cudaStream_t stream, const char** why);
 
 // fp32 CUDA-core path (any d in {16,32,64,128}, fp32 or bf16 inputs).
 cudaError_t launch_simt(const Problem& p, cudaStream_t stream);

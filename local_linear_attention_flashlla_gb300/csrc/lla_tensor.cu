@@ -58,10 +58,25 @@ constexpr int NSLOT = 3;           // K/V ring slots
 constexpr int EW_BAR = 1;          // named barrier of the elementwise warps
 constexpr int HDR_BYTES = 256;
 
-enum SweepType : int { SW_MAX = 0, SW_MOMENT = 1, SW_CG = 2, SW_OUT = 3 };
+enum SweepType : int { SW_MAX = 0, SW_MOMENT = 1, SW_CG = 2, SW_OUT = 3, SW_TBAR = 4, SW_END = 5 };
+
+// Sweep order without a tolerance: MAX, MOMENT, (backward: TBAR), T x CG, then OUT (forward) or
+// the end (backward).  With a tolerance the elementwise threads publish each later sweep's type.
+template <bool BWD>
+__device__ __forceinline__ int static_sweep(int sweep, int cg_sweeps, int T) {
+    if (sweep == 0) return SW_MAX;
+    if (sweep == 1) return SW_MOMENT;
+    if (BWD && sweep == 2) return SW_TBAR;
+    return cg_sweeps < T ? SW_CG : (BWD ? SW_END : SW_OUT);
+}
+// Sweeps that read a V block after each K block.
+template <bool BWD>
+__device__ __forceinline__ bool two_loads(int type) {
+    return type == SW_OUT || (BWD && (type == SW_MOMENT || type == SW_TBAR));
+}
 
 struct Header {
-    unsigned maxabs[3];            // float bits of max |q|, max |k|, max |v|
+    unsigned maxabs[4];            // float bits of max |q|, max |k|, max |v|, max |dout| (backward)
     int abort;                     // set by a CTA whose bounded wait gave up: the others stop early
 };
 
@@ -82,13 +97,16 @@ __device__ __forceinline__ int scale_exp(float maxabs) {
 
 // ------------------------------------------------------------------------------------------
 // Pre-pass: max |x| per tensor, then scaled fp16 copies.
+// NTEN = 3: q, k, v; NTEN = 4 (backward): also dout.
+template <int NTEN>
 __global__ void lla_maxabs_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                                  const __nv_bfloat16* __restrict__ v, size_t count8, Header* hdr) {
-    float m[3] = {0.f, 0.f, 0.f};
-    const __nv_bfloat16* src[3] = {q, k, v};
+                                  const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ g,
+                                  size_t count8, Header* hdr) {
+    float m[4] = {0.f, 0.f, 0.f, 0.f};
+    const __nv_bfloat16* src[4] = {q, k, v, g};
     for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < count8; idx += (size_t)gridDim.x * blockDim.x) {
 #pragma unroll
-        for (int t = 0; t < 3; ++t) {
+        for (int t = 0; t < NTEN; ++t) {
             const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src[t]) + idx);
             const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
@@ -99,24 +117,26 @@ __global__ void lla_maxabs_kernel(const __nv_bfloat16* __restrict__ q, const __n
         }
     }
 #pragma unroll
-    for (int t = 0; t < 3; ++t) {
+    for (int t = 0; t < NTEN; ++t) {
         float x = m[t];
         for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
         if ((threadIdx.x & 31) == 0) atomicMax(&hdr->maxabs[t], __float_as_uint(x));
     }
 }
 
+template <int NTEN>
 __global__ void lla_to_half_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
-                                   const __nv_bfloat16* __restrict__ v, __half* q16, __half* k16, __half* v16,
-                                   size_t count8, const Header* __restrict__ hdr) {
-    const __nv_bfloat16* src[3] = {q, k, v};
-    __half* dst[3] = {q16, k16, v16};
-    float sc[3];
+                                   const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ g,
+                                   __half* q16, __half* k16, __half* v16, __half* g16, size_t count8,
+                                   const Header* __restrict__ hdr) {
+    const __nv_bfloat16* src[4] = {q, k, v, g};
+    __half* dst[4] = {q16, k16, v16, g16};
+    float sc[4];
 #pragma unroll
-    for (int t = 0; t < 3; ++t) sc[t] = pow2i(scale_exp(__uint_as_float(hdr->maxabs[t])));
+    for (int t = 0; t < NTEN; ++t) sc[t] = pow2i(scale_exp(__uint_as_float(hdr->maxabs[t])));
     for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < count8; idx += (size_t)gridDim.x * blockDim.x) {
 #pragma unroll
-        for (int t = 0; t < 3; ++t) {
+        for (int t = 0; t < NTEN; ++t) {
             const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src[t]) + idx);
             const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
             uint4 o;
@@ -145,6 +165,7 @@ struct TcSmem {
     unsigned char slot[NSLOT][TILE];                   // K / V blocks (TMA)
     uint64_t slot_full[NSLOT], slot_empty[NSLOT];
     uint64_t q_full, s_full[2], ew_done[2], m_free[2], a_free, y_done, p_ready, final_s, final_a, final_y;
+    uint64_t max_done;                                 // backward: the elementwise warps finished the MAX sweep
     float xch[2][2][BQ];                               // row-scalar exchange between the two halves
     uint32_t tmem_base;
     int err;
@@ -163,6 +184,11 @@ struct TcParams {
     float* denom;
     int* cg_iters;
     const float* probe;   // Parallax form: caller's probe [B,H,n,D] fp32 (null for LLA)
+    // backward mode: the forward's rho [B,H,n,D] and denom [B,H,n] in, records and y out
+    const float* rho_in;
+    const float* denom_in;
+    BwdRowRec* rec;
+    float* yvec;          // [B,H,n,D] fp32
     unsigned* dev_err;
     int n, n_tiles;
     float tau, lambda, cg_tol;
@@ -264,10 +290,11 @@ __device__ __forceinline__ void cg_apply_chunk(uint32_t ty, const unsigned char*
 //   !HAS_A: out_j = 2^(s_j c - off)                       (moments)
 // zero where MASKED and key column > lim.  Packs pairs to fp16 and accumulates their sum into
 // two running fp32 partial sums (even and odd keys).  Key pairs go through f32x2 arithmetic.
-template <bool MASKED, bool HAS_A, int C>
+// SPLIT: also the fp16 remainder of every coefficient in pl (hi + lo carry about 22 bits).
+template <bool MASKED, bool HAS_A, int C, bool SPLIT = false>
 __device__ __forceinline__ void coef_chunk(const float (&v)[32], const float (&a)[64], float c_log2, float off,
                                            float base, float sign, int col0, int lim, uint64_t& sum2,
-                                           uint32_t (&pk)[16]) {
+                                           uint32_t (&pk)[16], uint32_t* pl = nullptr) {
     const uint64_t cc = f2_pack(c_log2, c_log2), oo = f2_pack(-off, -off);
     const uint64_t bb = f2_pack(base, base), sg = f2_pack(sign, sign);
 #pragma unroll
@@ -285,6 +312,35 @@ __device__ __forceinline__ void coef_chunk(const float (&v)[32], const float (&a
         }
         sum2 = f2_add(sum2, m);
         pk[j >> 1] = pack_half2(m0, m1);
+        if (SPLIT) {
+            const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&pk[j >> 1]));
+            pl[j >> 1] = pack_half2(m0 - h.x, m1 - h.y);
+        }
+    }
+}
+
+// Backward moment sweep: out_j = 2^(s_j c - off) (the weights, as the moment sweep), with the
+// running sums of out_j and of out_j a_j (a = H = G V^T, the per-pair dout.v).
+template <bool MASKED, int C>
+__device__ __forceinline__ void coef_chunk_wh(const float (&v)[32], const float (&a)[64], float c_log2, float off,
+                                              int col0, int lim, uint64_t& sum2, uint64_t& wh2, uint32_t (&pk)[16],
+                                              uint32_t (&pl)[16]) {
+    const uint64_t cc = f2_pack(c_log2, c_log2), oo = f2_pack(-off, -off);
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(v[j], v[j + 1]), cc, oo), x0, x1);
+        float m0 = ex2(x0), m1 = ex2(x1);
+        if (MASKED) {
+            m0 = (col0 + j <= lim) ? m0 : 0.f;
+            m1 = (col0 + j + 1 <= lim) ? m1 : 0.f;
+        }
+        const uint64_t m = f2_pack(m0, m1);
+        sum2 = f2_add(sum2, m);
+        wh2 = f2_fma(m, f2_pack(a[C * 32 + j], a[C * 32 + j + 1]), wh2);
+        pk[j >> 1] = pack_half2(m0, m1);
+        const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&pk[j >> 1]));
+        pl[j >> 1] = pack_half2(m0 - h.x, m1 - h.y);
     }
 }
 
@@ -321,10 +377,28 @@ __device__ __forceinline__ void gemm_y(uint32_t y_tmem, uint32_t m_tmem, uint32_
         umma_ts_c<true>(y_tmem, m_tmem + (ks >> 2) * 64 + (ks & 3) * 8, b0 + (uint64_t)((ks * 2048) >> 4), ID);
 }
 
+// As gemm_y with hi + lo coefficients: key chunk c (32 keys) of key half h holds its fp16 hi pairs at
+// columns 64h + 32c + 0..15 and the lo pairs at 64h + 32c + 16..31.
 template <int D>
+__device__ __forceinline__ void gemm_y_split(uint32_t y_tmem, uint32_t m_tmem, uint32_t b_addr, bool acc) {
+    constexpr uint32_t ID = idesc_f16(BQ, D, true);
+    const uint64_t b0 = sdesc_sw128(b_addr, BK * 128, 1024);
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+#pragma unroll
+        for (int ks = 0; ks < BK / 16; ++ks) {
+            const uint32_t col = (ks >> 2) * 64 + ((ks & 3) >> 1) * 32 + (ks & 1) * 8 + part * 16;
+            const uint64_t bk = b0 + (uint64_t)((ks * 2048) >> 4);
+            if (part == 0 && ks == 0 && !acc) umma_ts_c<false>(y_tmem, m_tmem + col, bk, ID);
+            else umma_ts_c<true>(y_tmem, m_tmem + col, bk, ID);
+        }
+    }
+}
+
+template <int D, bool BWD>
 __global__ void __launch_bounds__(NTHREADS, 1)
 lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-              const __grid_constant__ CUtensorMap tm_v, const TcParams prm) {
+              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g, const TcParams prm) {
     using S = TcSmem<D>;
     constexpr int NB = S::NB;
     constexpr int DH = D / 2;                       // head-dim coordinates per elementwise thread
@@ -368,6 +442,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         mbar_init(&s.final_s, 1);
         mbar_init(&s.final_a, 1);
         mbar_init(&s.final_y, 1);
+        mbar_init(&s.max_done, NEW / 32);
         mbar_fence_init();
     }
     if (warp == 1) {
@@ -389,23 +464,26 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            mbar_arrive_expect_tx(&s.q_full, S::TILE);
+            // backward: dout's tile goes to the direction tile, the A operand of H = G V^T in
+            // the MOMENT and TBAR sweeps (the direction is first written after TBAR)
+            mbar_arrive_expect_tx(&s.q_full, BWD ? 2 * S::TILE : S::TILE);
             for (int bx = 0; bx < NB; ++bx) tma_load_3d(s.q + bx * BQ * 128, &tm_q, &s.q_full, bx * 64, tile * BQ, head);
+            if (BWD)
+                for (int bx = 0; bx < NB; ++bx) tma_load_3d(s.p + bx * BQ * 128, &tm_g, &s.q_full, bx * 64, tile * BQ, head);
             uint32_t fill = 0, pr = 0;
             int cg_sweeps = 0;
-            int type = SW_MAX;
             for (int sweep = 0; !*err; ++sweep) {
-                if (sweep == 0) type = SW_MAX;
-                else if (sweep == 1) type = SW_MOMENT;
-                else if (!dynamic) type = cg_sweeps < prm.cg_max_iters ? SW_CG : SW_OUT;
+                int type;
+                if (sweep < (BWD ? 3 : 2) || !dynamic) type = static_sweep<BWD>(sweep, cg_sweeps, prm.cg_max_iters);
                 else {
                     if (!WAIT(&s.p_ready, pr & 1, err)) break;
                     ++pr;
                     type = s.next_type;
                 }
+                if (type == SW_END) break;
                 if (type == SW_CG) ++cg_sweeps;
+                const int nload = two_loads<BWD>(type) ? 2 : 1;
                 for (int kb = 0; kb < nkb && !*err; ++kb) {
-                    const int nload = type == SW_OUT ? 2 : 1;
                     for (int l = 0; l < nload; ++l) {
                         const int sl = fill % NSLOT;
                         if (!WAIT(&s.slot_empty[sl], ((fill / NSLOT) & 1) ^ 1, err)) break;
@@ -432,27 +510,31 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             int cg_sweeps = 0;
             for (int sweep = 0; ok; ++sweep) {
                 int type;
-                if (sweep == 0) type = SW_MAX;
-                else if (sweep == 1) type = SW_MOMENT;
-                else if (!dynamic) type = cg_sweeps < prm.cg_max_iters ? SW_CG : SW_OUT;
+                if (sweep < (BWD ? 3 : 2) || !dynamic) type = static_sweep<BWD>(sweep, cg_sweeps, prm.cg_max_iters);
                 else {
                     if (!(ok = WAIT(&s.p_ready, pr & 1, err))) break;
                     ++pr;
                     type = s.next_type;
                 }
+                if (type == SW_END) break;
                 if (type == SW_CG) ++cg_sweeps;
+                const bool two = two_loads<BWD>(type);
+                // a sweep with no A'/T/H product: S completes both arrivals of s_full
+                const bool lone_s = type == SW_MAX || (!BWD && type == SW_MOMENT);
                 for (int kb = 0; kb < nkb; ++kb, ++g) {
                     const uint32_t fk = fill++;
-                    if (type == SW_OUT) ++fill;           // the V block of this key block
+                    if (two) ++fill;                      // the V block of this key block
                     const int sk = fk % NSLOT;
                     const uint32_t b = g & 1;
-                    if (!(ok = WAIT(&s.slot_full[sk], (fk / NSLOT) & 1, err))) break;
-                    // S buffer b was last used by block g - 2: its coefficients must have been read
+                    // S buffer b was last used by block g - 2: its coefficients must have been read.  Waited
+                    // before the slot: it also means every fill before this block's K landed, so the slot's
+                    // parity wait below cannot be answered by an older phase of the same slot.
                     if (g >= 2 && !(ok = WAIT(&s.m_free[b], ((g - 2) >> 1) & 1, err))) break;
+                    if (!(ok = WAIT(&s.slot_full[sk], (fk / NSLOT) & 1, err))) break;
                     tc_fence_after();
                     gemm_qk<D, false>(tS0 + b * 128, q_addr, smem_u32(s.slot[sk]));
                     umma_commit(&s.s_full[b]);
-                    if (type == SW_MAX || type == SW_MOMENT) umma_commit(&s.s_full[b]);   // no A' product
+                    if (lone_s) umma_commit(&s.s_full[b]);
                     if (type == SW_MAX) umma_commit(&s.slot_empty[sk]);   // read by S alone
                 }
                 if (type == SW_OUT) break;
@@ -461,49 +543,59 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             mbar_drain(&s.final_s, 0);
         }
     } else if (warp == 3) {
-        // ================= MMA issuer 3: A' = P K^T (CG) or T = R K^T (output) =================
+        // ======= MMA issuer 3: A' = P K^T (CG), T = R K^T (output) or H = G V^T (backward) =======
         if (lane == 0) {
             const uint32_t p_addr = smem_u32(s.p), rlo_addr = smem_u32(s.rlo);
             uint32_t fill = 0, pr = 0, g = 0, ga = 0;
-            bool ok = true;
+            bool ok = true, have_g = false;
             int cg_sweeps = 0;
             for (int sweep = 0; ok; ++sweep) {
                 int type;
                 bool have_p = false;
-                if (sweep == 0) type = SW_MAX;
-                else if (sweep == 1) type = SW_MOMENT;
-                else if (!dynamic) type = cg_sweeps < prm.cg_max_iters ? SW_CG : SW_OUT;
+                if (sweep < (BWD ? 3 : 2) || !dynamic) type = static_sweep<BWD>(sweep, cg_sweeps, prm.cg_max_iters);
                 else {
                     if (!(ok = WAIT(&s.p_ready, pr & 1, err))) break;
                     ++pr;
                     have_p = true;
                     type = s.next_type;
                 }
+                if (type == SW_END) break;
                 if (type == SW_CG) ++cg_sweeps;
-                if (type == SW_MAX || type == SW_MOMENT) {   // no product of this issuer
+                if (type == SW_MAX || (!BWD && type == SW_MOMENT)) {   // no product of this issuer
                     fill += nkb;
                     g += nkb;
                     continue;
                 }
+                const bool hprod = BWD && (type == SW_MOMENT || type == SW_TBAR);   // H = G V^T
+                const bool two = two_loads<BWD>(type);
+                // This issuer skips the fills of the sweeps above.  Before its first slot wait it learns
+                // that all of them landed, so no parity wait below is answered by an older phase of
+                // the same slot; from here on it waits every fill in order.  CG / output: P or R is
+                // published after the previous sweep's last Y product.  Backward moments: the
+                // elementwise warps have read every S product of the MAX sweep.
+                if (!hprod && !have_p) {
+                    if (!(ok = WAIT(&s.p_ready, pr & 1, err))) break;
+                    ++pr;
+                    have_p = true;
+                }
+                if (hprod && !have_g) {
+                    if (!(ok = WAIT(&s.q_full, 0, err)) || !(ok = WAIT(&s.max_done, 0, err))) break;
+                    have_g = true;
+                }
                 for (int kb = 0; kb < nkb; ++kb, ++g) {
                     const uint32_t fk = fill++;
-                    if (type == SW_OUT) ++fill;
-                    const int sk = fk % NSLOT;
-                    if (!(ok = WAIT(&s.slot_full[sk], (fk / NSLOT) & 1, err))) break;
-                    if (!have_p) {
-                        if (!(ok = WAIT(&s.p_ready, pr & 1, err))) break;
-                        ++pr;
-                        have_p = true;
-                    }
+                    const uint32_t fv = two ? fill++ : 0;
+                    if (!(ok = WAIT(&s.slot_full[fk % NSLOT], (fk / NSLOT) & 1, err))) break;
+                    if (two && !(ok = WAIT(&s.slot_full[fv % NSLOT], (fv / NSLOT) & 1, err))) break;
                     // A' is single-buffered: the elementwise threads release it as soon as they
                     // have copied the previous block's A' into registers
                     if (ga >= 1 && !(ok = WAIT(&s.a_free, (ga - 1) & 1, err))) break;
                     ++ga;
                     tc_fence_after();
-                    const uint32_t k_addr = smem_u32(s.slot[sk]);
-                    gemm_qk<D, false>(tA, p_addr, k_addr);
+                    const uint32_t b_addr = smem_u32(s.slot[(hprod ? fv : fk) % NSLOT]);
+                    gemm_qk<D, false>(tA, p_addr, b_addr);
                     // T = (R_hi + R_lo) K^T; in the first tile also A' = (P_hi + P_lo) K^T
-                    if (type == SW_OUT || tile == 0) gemm_qk<D, true>(tA, rlo_addr, k_addr);
+                    if (!hprod && (type == SW_OUT || tile == 0 || BWD)) gemm_qk<D, true>(tA, rlo_addr, b_addr);
                     umma_commit(&s.s_full[g & 1]);
                 }
                 if (type == SW_OUT) break;
@@ -512,37 +604,38 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             mbar_drain(&s.final_a, 0);
         }
     } else if (warp == 2) {
-        // ============== MMA issuer 2: Y += M K (moments, CG) or U V (output) ==============
+        // ===== MMA issuer 2: Y += M K (moments, CG; backward TBAR) or U V (output) =====
         if (lane == 0) {
             uint32_t fill = 0, pr = 0, g = 0;
             bool ok = WAIT(&s.q_full, 0, err);
             int cg_sweeps = 0;
             for (int sweep = 0; ok; ++sweep) {
                 int type;
-                if (sweep == 0) type = SW_MAX;
-                else if (sweep == 1) type = SW_MOMENT;
-                else if (!dynamic) type = cg_sweeps < prm.cg_max_iters ? SW_CG : SW_OUT;
+                if (sweep < (BWD ? 3 : 2) || !dynamic) type = static_sweep<BWD>(sweep, cg_sweeps, prm.cg_max_iters);
                 else {
                     if (!(ok = WAIT(&s.p_ready, pr & 1, err))) break;
                     ++pr;
                     type = s.next_type;
                 }
+                if (type == SW_END) break;
                 if (type == SW_CG) ++cg_sweeps;
+                const bool two = two_loads<BWD>(type);
                 const uint32_t ty_acc = tY;
                 for (int kb = 0; kb < nkb; ++kb, ++g) {
                     const uint32_t fk = fill++;
-                    const uint32_t fv = type == SW_OUT ? fill++ : 0;
+                    const uint32_t fv = two ? fill++ : 0;
                     const uint32_t b = g & 1;
                     if (!(ok = WAIT(&s.ew_done[b], (g >> 1) & 1, err))) break;
                     if (type != SW_MAX) {
                         if (type == SW_OUT && !(ok = WAIT(&s.slot_full[fv % NSLOT], (fv / NSLOT) & 1, err))) break;
                         tc_fence_after();
-                        const uint32_t src = smem_u32(s.slot[(type == SW_OUT ? fv : fk) % NSLOT]);
-                        gemm_y<D>(ty_acc, tS0 + b * 128, src, kb > 0);
-                        umma_commit(&s.slot_empty[(type == SW_OUT ? fv : fk) % NSLOT]);
-                        // the output sweep's K block: S and T completed before the elementwise
-                        // warps could finish this block
-                        if (type == SW_OUT) umma_commit(&s.slot_empty[fk % NSLOT]);
+                        const uint32_t fsrc = type == SW_OUT ? fv : fk;   // V for the output, K otherwise
+                        if (BWD) gemm_y_split<D>(ty_acc, tS0 + b * 128, smem_u32(s.slot[fsrc % NSLOT]), kb > 0);
+                        else gemm_y<D>(ty_acc, tS0 + b * 128, smem_u32(s.slot[fsrc % NSLOT]), kb > 0);
+                        umma_commit(&s.slot_empty[fsrc % NSLOT]);
+                        // the other block of a two-block sweep (the output's K, the backward's V): its
+                        // products completed before the elementwise warps could finish this block
+                        if (two) umma_commit(&s.slot_empty[(type == SW_OUT ? fk : fv) % NSLOT]);
                         if (kb == nkb - 1) umma_commit(&s.y_done);
                     }
                     umma_commit(&s.m_free[b]);
@@ -565,7 +658,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const bool tile_full = (tile + 1) * BQ <= n;     // every row of the tile exists
         // the first tile holds the rows i < d whose key scatter is rank-deficient: there the CG
         // direction is kept to about 22 bits (hi + lo fp16 halves, one extra MMA per CG block)
-        const bool split_p = tile == 0;
+        const bool split_p = BWD || tile == 0;
         const size_t row_g = ((size_t)head * n + (row_ok ? i : 0)) * D + half * DH;
         // tile-transposed fp32 scratch: coordinate e of this thread's row at [e * BQ] (coalesced)
         const size_t tbase = ((size_t)(head * prm.n_tiles + tile) * D + half * DH) * BQ + row;
@@ -624,6 +717,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
         // ---------------- MAX sweep ----------------
         float mx = -INFINITY;
+        int jmx = 0;                        // backward: first key index attaining the maximum
         for (int kb = 0; kb < nkb; ++kb, ++g) {
             ok = ok && wait_s(g);
             const uint32_t tS = tS0 + (g & 1) * 128 + lane_off + half * 64;
@@ -633,7 +727,14 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             tmem_ld_wait();
             done_block(g);
             const int lim = lim_of(kb);
-            if (tile_full && kb < tile) {
+            if (BWD) {                      // columns in increasing order: a strict > keeps the first
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (half * 64 + j <= lim && v0[j] > mx) { mx = v0[j]; jmx = kb * BK + half * 64 + j; }
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (half * 64 + 32 + j <= lim && v1[j] > mx) { mx = v1[j]; jmx = kb * BK + half * 64 + 32 + j; }
+            } else if (tile_full && kb < tile) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) mx = fmaxf(mx, fmaxf(v0[j], v1[j]));
             } else {
@@ -644,11 +745,21 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 }
             }
         }
-        mx = xch.max(mx);
+        if (BWD) {                          // half 0 holds the lower columns of every block
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s.max_done);
+            const float omx = xch.swap(mx);
+            const int ojm = __float_as_int(xch.swap(__int_as_float(jmx)));
+            if (omx > mx || (omx == mx && ojm < jmx)) { mx = omx; jmx = ojm; }
+        } else {
+            mx = xch.max(mx);
+        }
         const float m2 = row_ok ? mx * c_log2 : 0.f;
 
         // ---------------- MOMENT sweep ----------------
         uint64_t om_part = 0;              // two fp32 partial sums (bit pattern 0 = +0.0f, +0.0f)
+        uint64_t wh_part = 0;              // backward: sum of w h
         for (int kb = 0; kb < nkb; ++kb, ++g) {
             ok = ok && wait_s(g);
             const uint32_t tS = tS0 + (g & 1) * 128 + lane_off + half * 64;
@@ -656,16 +767,36 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const bool masked = !(tile_full && kb < tile);
             float v[32];
             uint32_t pk[16];
-            tmem_ld32(tS, v);
-            tmem_ld_wait();
-            if (masked) coef_chunk<true, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, half * 64, lim, om_part, pk);
-            else coef_chunk<false, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, 0, 0, om_part, pk);
-            tmem_st16(tS, pk);
-            tmem_ld32(tS + 32, v);
-            tmem_ld_wait();
-            if (masked) coef_chunk<true, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, half * 64 + 32, lim, om_part, pk);
-            else coef_chunk<false, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, 0, 0, om_part, pk);
-            tmem_st16(tS + 16, pk);
+            if (BWD) {
+                float a[64];
+                tmem_ld32(tA + lane_off + half * 64, *reinterpret_cast<float(*)[32]>(&a[0]));
+                tmem_ld32(tA + lane_off + half * 64 + 32, *reinterpret_cast<float(*)[32]>(&a[32]));
+                tmem_ld32(tS, v);
+                tmem_ld_wait();
+                release_a();
+                uint32_t pl[16];            // hi + lo weights, split layout (gemm_y_split)
+                if (masked) coef_chunk_wh<true, 0>(v, a, c_log2, m2 - 14.f, half * 64, lim, om_part, wh_part, pk, pl);
+                else coef_chunk_wh<false, 0>(v, a, c_log2, m2 - 14.f, 0, 0, om_part, wh_part, pk, pl);
+                tmem_st16(tS, pk);
+                tmem_st16(tS + 16, pl);
+                tmem_ld32(tS + 32, v);
+                tmem_ld_wait();
+                if (masked) coef_chunk_wh<true, 1>(v, a, c_log2, m2 - 14.f, half * 64 + 32, lim, om_part, wh_part, pk, pl);
+                else coef_chunk_wh<false, 1>(v, a, c_log2, m2 - 14.f, 0, 0, om_part, wh_part, pk, pl);
+                tmem_st16(tS + 32, pk);
+                tmem_st16(tS + 48, pl);
+            } else {
+                tmem_ld32(tS, v);
+                tmem_ld_wait();
+                if (masked) coef_chunk<true, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, half * 64, lim, om_part, pk);
+                else coef_chunk<false, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, 0, 0, om_part, pk);
+                tmem_st16(tS, pk);
+                tmem_ld32(tS + 32, v);
+                tmem_ld_wait();
+                if (masked) coef_chunk<true, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, half * 64 + 32, lim, om_part, pk);
+                else coef_chunk<false, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, 0, 0, om_part, pk);
+                tmem_st16(tS + 16, pk);
+            }
             tmem_st_wait();
             done_block(g);
         }
@@ -674,6 +805,10 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const float omega = row_ok ? om_all * pow2i(-14) : 1.f;
         const float inv_om = 1.f / omega;
         const float lam_n = prm.lambda * inv_om;
+        // backward: hbar in units of H (dout.v 2^(eg+ev)); TBAR's right-hand side, in res
+        const int eg = BWD ? scale_exp(__uint_as_float(prm.hdr->maxabs[3])) : 0;
+        const float wh_all = BWD ? xch.sum(f2_total(wh_part)) : 0.f;
+        const float hbar_a = (BWD && row_ok && om_all > 0.f) ? wh_all / om_all : 0.f;
 
         // kbar, delta, CG initialisation (this thread: coordinates half*DH .. half*DH+DH-1)
         float res[DH];
@@ -733,7 +868,78 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             kpx = kbr + (BETA) * kpx;                                                                      \
             kp_acc = kpx * pow2i(sp + ek);                                                                 \
         }
-        {
+        if constexpr (BWD) {
+            // kbar from the moment sweep's Y, before the TBAR sweep reuses the accumulator
+            {
+                const float ysc = pow2i(-(14 + ek)) * inv_om;
+#pragma unroll
+                for (int c = 0; c < DH / 32; ++c) {
+                    float v[32];
+                    tmem_ld32(tY + lane_off + half * DH + c * 32, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) kbt[(c * 32 + j) * BQ] = v[j] * ysc;
+                }
+            }
+            // ---------------- TBAR sweep: Y = sum_j w_j (h_j - hbar) k_j ----------------
+            // coefficient w (h - hbar) 2^sT; |h - hbar| <= 2 D max|dout| max|v| fixes sT
+            const int sT = scale_exp(2.f * (float)D * __uint_as_float(prm.hdr->maxabs[3]) *
+                                     __uint_as_float(prm.hdr->maxabs[2]) * 1.001f);
+            const float offT = m2 - (float)sT + (float)(eg + ev);
+            uint64_t ts_part = 0;
+            for (int kb = 0; kb < nkb; ++kb, ++g) {
+                ok = ok && wait_s(g);
+                const uint32_t tS = tS0 + (g & 1) * 128 + lane_off + half * 64;
+                const uint32_t tAh = tA + lane_off + half * 64;
+                const int lim = lim_of(kb);
+                const bool masked = !(tile_full && kb < tile);
+                float a[64], v[32];
+                uint32_t pk[16];
+                tmem_ld32(tAh, *reinterpret_cast<float(*)[32]>(&a[0]));
+                tmem_ld32(tAh + 32, *reinterpret_cast<float(*)[32]>(&a[32]));
+                tmem_ld32(tS, v);
+                tmem_ld_wait();
+                release_a();
+                uint32_t pl[16];
+                if (masked) coef_chunk<true, true, 0, true>(v, a, c_log2, offT, -hbar_a, 1.f, half * 64, lim, ts_part, pk, pl);
+                else coef_chunk<false, true, 0, true>(v, a, c_log2, offT, -hbar_a, 1.f, 0, 0, ts_part, pk, pl);
+                tmem_st16(tS, pk);
+                tmem_st16(tS + 16, pl);
+                tmem_ld32(tS + 32, v);
+                tmem_ld_wait();
+                if (masked) coef_chunk<true, true, 1, true>(v, a, c_log2, offT, -hbar_a, 1.f, half * 64 + 32, lim, ts_part, pk, pl);
+                else coef_chunk<false, true, 1, true>(v, a, c_log2, offT, -hbar_a, 1.f, 0, 0, ts_part, pk, pl);
+                tmem_st16(tS + 32, pk);
+                tmem_st16(tS + 48, pl);
+                tmem_st_wait();
+                done_block(g);
+            }
+            ok = ok && wait_y();
+            // right-hand side tbar = [Y 2^-(sT+ek) - kbar (sum of coefficients) 2^-sT] / omega
+            const float tsum = xch.sum(f2_total(ts_part));
+            const float tysc = pow2i(-(sT + ek)) * inv_om, tksc = tsum * pow2i(-sT) * inv_om;
+            float gp = 0.f, kr = 0.f;
+#pragma unroll
+            for (int c = 0; c < DH / 32; ++c) {
+                float v[32];
+                tmem_ld32(tY + lane_off + half * DH + c * 32, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const float kb_ = kbt[(c * 32 + j) * BQ];
+                    const float r_ = row_ok ? fmaf(v[j], tysc, -kb_ * tksc) : 0.f;
+                    res[c * 32 + j] = r_;
+                    gp = fmaf(r_, r_, gp);
+                    kr = fmaf(kb_, r_, kr);
+                }
+            }
+            gamma = xch.sum(gp);
+            kbr = xch.sum(kr);
+            rn0 = sqrtf(gamma);
+            active = row_ok && gamma > 0.f && !(sqrtf(gamma) <= prm.cg_tol * rn0);
+            float pn[DH];
+            LLA_SET_DIRECTION(0.f, false, false, 0.f, pn, pn);
+        } else {
             float kv[DH];
             const float ysc = pow2i(-(14 + ek)) * inv_om;
             const float qsc = pow2i(-eq);
@@ -791,14 +997,28 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 tmem_ld32(tS, v);
                 tmem_ld_wait();
                 release_a();
-                if (masked) coef_chunk<true, true, 0>(v, a, c_log2, offM, -kp_acc, 1.f, half * 64, lim, msum_part, pk);
-                else coef_chunk<false, true, 0>(v, a, c_log2, offM, -kp_acc, 1.f, 0, 0, msum_part, pk);
-                tmem_st16(tS, pk);
-                tmem_ld32(tS + 32, v);
-                tmem_ld_wait();
-                if (masked) coef_chunk<true, true, 1>(v, a, c_log2, offM, -kp_acc, 1.f, half * 64 + 32, lim, msum_part, pk);
-                else coef_chunk<false, true, 1>(v, a, c_log2, offM, -kp_acc, 1.f, 0, 0, msum_part, pk);
-                tmem_st16(tS + 16, pk);
+                if constexpr (BWD) {   // hi + lo coefficients, split layout (gemm_y_split)
+                    uint32_t pl[16];
+                    if (masked) coef_chunk<true, true, 0, true>(v, a, c_log2, offM, -kp_acc, 1.f, half * 64, lim, msum_part, pk, pl);
+                    else coef_chunk<false, true, 0, true>(v, a, c_log2, offM, -kp_acc, 1.f, 0, 0, msum_part, pk, pl);
+                    tmem_st16(tS, pk);
+                    tmem_st16(tS + 16, pl);
+                    tmem_ld32(tS + 32, v);
+                    tmem_ld_wait();
+                    if (masked) coef_chunk<true, true, 1, true>(v, a, c_log2, offM, -kp_acc, 1.f, half * 64 + 32, lim, msum_part, pk, pl);
+                    else coef_chunk<false, true, 1, true>(v, a, c_log2, offM, -kp_acc, 1.f, 0, 0, msum_part, pk, pl);
+                    tmem_st16(tS + 32, pk);
+                    tmem_st16(tS + 48, pl);
+                } else {
+                    if (masked) coef_chunk<true, true, 0>(v, a, c_log2, offM, -kp_acc, 1.f, half * 64, lim, msum_part, pk);
+                    else coef_chunk<false, true, 0>(v, a, c_log2, offM, -kp_acc, 1.f, 0, 0, msum_part, pk);
+                    tmem_st16(tS, pk);
+                    tmem_ld32(tS + 32, v);
+                    tmem_ld_wait();
+                    if (masked) coef_chunk<true, true, 1>(v, a, c_log2, offM, -kp_acc, 1.f, half * 64 + 32, lim, msum_part, pk);
+                    else coef_chunk<false, true, 1>(v, a, c_log2, offM, -kp_acc, 1.f, 0, 0, msum_part, pk);
+                    tmem_st16(tS + 16, pk);
+                }
                 tmem_st_wait();
                 done_block(g);
             }
@@ -884,122 +1104,164 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             LLA_SET_DIRECTION(beta, true, true, alpha, pn, xo);
         }
 
-        // ---------------- finalise rho, denom; R = rho' (hi + lo) for the output sweep ----------------
-        // x and kbar in registers, loaded in one batch; x through L2 (.cg), where its reductions landed
-        float xv[DH], kv[DH];
-        const bool have_x = row_ok && cg_sweeps > 0;   // no sweep ran: x = 0
-#pragma unroll
-        for (int e = 0; e < DH; ++e) {
-            xv[e] = have_x ? xt[e * BQ] : 0.f;
-            kv[e] = kbt[e * BQ];
-        }
-        if (prm.probe && row_ok) {   // Parallax form: the caller's probe plays rho'
+        if constexpr (BWD) {
+            // ---------------- backward: y and the per-row record ----------------
+            // rho' = rho omega/denom from the forward's outputs; kbar.rho', kbar.y, rho'.y
+            const bool have_x = row_ok && cg_sweeps > 0;   // no sweep ran: y = 0
+            const float den = row_ok ? prm.denom_in[(size_t)head * n + i] : 1.f;
+            const float rp_scale = omega / den;
+            float kr = 0.f, ky = 0.f, ry = 0.f;
 #pragma unroll
             for (int e0 = 0; e0 < DH; e0 += 4) {
-                const float4 t = *reinterpret_cast<const float4*>(prm.probe + row_g + e0);
-                xv[e0] = t.x; xv[e0 + 1] = t.y; xv[e0 + 2] = t.z; xv[e0 + 3] = t.w;
+                float xv[4], rv[4];
+                const float4 r4 = row_ok ? *reinterpret_cast<const float4*>(prm.rho_in + row_g + e0)
+                                         : make_float4(0.f, 0.f, 0.f, 0.f);
+                rv[0] = r4.x * rp_scale; rv[1] = r4.y * rp_scale; rv[2] = r4.z * rp_scale; rv[3] = r4.w * rp_scale;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    xv[u] = have_x ? xt[(e0 + u) * BQ] : 0.f;
+                    const float kb_ = kbt[(e0 + u) * BQ];
+                    kr = fmaf(kb_, rv[u], kr);
+                    ky = fmaf(kb_, xv[u], ky);
+                    ry = fmaf(rv[u], xv[u], ry);
+                }
+                if (row_ok) *reinterpret_cast<float4*>(prm.yvec + row_g + e0) = make_float4(xv[0], xv[1], xv[2], xv[3]);
             }
-        }
-        float dx = 0.f, mxx = 0.f;
-        {
-            const float qsc = pow2i(-eq);
+            kr = xch.sum(kr);
+            ky = xch.sum(ky);
+            ry = xch.sum(ry);
+            if (row_ok && half == 0) {
+                BwdRowRec o;
+                o.m = mx * prm.tau * pow2i(-(eq + ek));
+                o.jm = jmx;
+                o.inv_omega = inv_om;
+                o.hbar = hbar_a * pow2i(-(eg + ev));
+                o.kb_rp = kr;
+                o.kb_y = ky;
+                o.sd = -prm.lambda * inv_om * ry;
+                o.rp_scale = rp_scale;
+                prm.rec[(size_t)head * n + i] = o;
+                if (prm.cg_iters) prm.cg_iters[(size_t)head * n + i] = iters;
+            }
+            publish_p(SW_END);
+        } else {
+            // ---------------- finalise rho, denom; R = rho' (hi + lo) for the output sweep ----------------
+            // x and kbar in registers, loaded in one batch; x through L2 (.cg), where its reductions landed
+            float xv[DH], kv[DH];
+            const bool have_x = row_ok && cg_sweeps > 0;   // no sweep ran: x = 0
 #pragma unroll
-            for (int e0 = 0; e0 < DH; e0 += 8) {
-                const uint4 qr = *reinterpret_cast<const uint4*>(tile_half(s.q, row, half * DH + e0));
-                const __half* qh = reinterpret_cast<const __half*>(&qr);
+            for (int e = 0; e < DH; ++e) {
+                xv[e] = have_x ? xt[e * BQ] : 0.f;
+                kv[e] = kbt[e * BQ];
+            }
+            if (prm.probe && row_ok) {   // Parallax form: the caller's probe plays rho'
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    dx = fmaf(kv[e0 + u] - __half2float(qh[u]) * qsc, xv[e0 + u], dx);
-                    mxx = fmaxf(mxx, fabsf(xv[e0 + u]));
+                for (int e0 = 0; e0 < DH; e0 += 4) {
+                    const float4 t = *reinterpret_cast<const float4*>(prm.probe + row_g + e0);
+                    xv[e0] = t.x; xv[e0 + 1] = t.y; xv[e0 + 2] = t.z; xv[e0 + 3] = t.w;
                 }
             }
-            if (!row_ok) { dx = 0.f; mxx = 0.f; }
-        }
-        dx = xch.sum(dx);
-        mxx = xch.max(mxx);
-        const float inv_g = 1.f / (1.f + dx);
-        const int sr = min(scale_exp(mxx), 100 - ek);
-        float kx = 0.f;
-        {
-            const float rs = pow2i(sr), ris = pow2i(-sr);
+            float dx = 0.f, mxx = 0.f;
+            {
+                const float qsc = pow2i(-eq);
 #pragma unroll
-            for (int e0 = 0; e0 < DH; e0 += 8) {
-                uint4 pk, pl;
-                uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
-                uint32_t* plw = reinterpret_cast<uint32_t*>(&pl);
+                for (int e0 = 0; e0 < DH; e0 += 8) {
+                    const uint4 qr = *reinterpret_cast<const uint4*>(tile_half(s.q, row, half * DH + e0));
+                    const __half* qh = reinterpret_cast<const __half*>(&qr);
 #pragma unroll
-                for (int u = 0; u < 8; u += 2) {
-                    const float x0 = xv[e0 + u] * rs, x1 = xv[e0 + u + 1] * rs;
-                    pw[u >> 1] = pack_half2(x0, x1);
-                    const float2 xh = __half22float2(*reinterpret_cast<const __half2*>(&pw[u >> 1]));
-                    plw[u >> 1] = pack_half2(x0 - xh.x, x1 - xh.y);
-                    const float2 xl = __half22float2(*reinterpret_cast<const __half2*>(&plw[u >> 1]));
-                    kx = fmaf(kv[e0 + u], (xh.x + xl.x) * ris, kx);
-                    kx = fmaf(kv[e0 + u + 1], (xh.y + xl.y) * ris, kx);
+                    for (int u = 0; u < 8; ++u) {
+                        dx = fmaf(kv[e0 + u] - __half2float(qh[u]) * qsc, xv[e0 + u], dx);
+                        mxx = fmaxf(mxx, fabsf(xv[e0 + u]));
+                    }
                 }
-                *reinterpret_cast<uint4*>(tile_half(s.p, row, half * DH + e0)) = pk;
-                *reinterpret_cast<uint4*>(tile_half(s.rlo, row, half * DH + e0)) = pl;
-                if (row_ok && !prm.probe) {   // rho = rho' / (1 + delta.rho'), row-major output
-                    *reinterpret_cast<float4*>(prm.rho + row_g + e0) =
-                        make_float4(xv[e0] * inv_g, xv[e0 + 1] * inv_g, xv[e0 + 2] * inv_g, xv[e0 + 3] * inv_g);
-                    *reinterpret_cast<float4*>(prm.rho + row_g + e0 + 4) =
-                        make_float4(xv[e0 + 4] * inv_g, xv[e0 + 5] * inv_g, xv[e0 + 6] * inv_g, xv[e0 + 7] * inv_g);
-                }
+                if (!row_ok) { dx = 0.f; mxx = 0.f; }
             }
-            if (!row_ok) kx = 0.f;
-        }
-        kx = xch.sum(kx);
-        if (row_ok && half == 0 && !prm.probe) {
-            prm.denom[(size_t)head * n + i] = omega * inv_g;
-            if (prm.cg_iters) prm.cg_iters[(size_t)head * n + i] = iters;
-        }
-        const int sU = scale_exp((1.f + kbound * mxx) * 1.001f);
-        const float offU = m2 - (float)sU + (float)sr + (float)ek;
-        const float c_acc = (1.f + kx) * pow2i(sr + ek);
-        publish_p(SW_OUT);
+            dx = xch.sum(dx);
+            mxx = xch.max(mxx);
+            const float inv_g = 1.f / (1.f + dx);
+            const int sr = min(scale_exp(mxx), 100 - ek);
+            float kx = 0.f;
+            {
+                const float rs = pow2i(sr), ris = pow2i(-sr);
+#pragma unroll
+                for (int e0 = 0; e0 < DH; e0 += 8) {
+                    uint4 pk, pl;
+                    uint32_t* pw = reinterpret_cast<uint32_t*>(&pk);
+                    uint32_t* plw = reinterpret_cast<uint32_t*>(&pl);
+#pragma unroll
+                    for (int u = 0; u < 8; u += 2) {
+                        const float x0 = xv[e0 + u] * rs, x1 = xv[e0 + u + 1] * rs;
+                        pw[u >> 1] = pack_half2(x0, x1);
+                        const float2 xh = __half22float2(*reinterpret_cast<const __half2*>(&pw[u >> 1]));
+                        plw[u >> 1] = pack_half2(x0 - xh.x, x1 - xh.y);
+                        const float2 xl = __half22float2(*reinterpret_cast<const __half2*>(&plw[u >> 1]));
+                        kx = fmaf(kv[e0 + u], (xh.x + xl.x) * ris, kx);
+                        kx = fmaf(kv[e0 + u + 1], (xh.y + xl.y) * ris, kx);
+                    }
+                    *reinterpret_cast<uint4*>(tile_half(s.p, row, half * DH + e0)) = pk;
+                    *reinterpret_cast<uint4*>(tile_half(s.rlo, row, half * DH + e0)) = pl;
+                    if (row_ok && !prm.probe) {   // rho = rho' / (1 + delta.rho'), row-major output
+                        *reinterpret_cast<float4*>(prm.rho + row_g + e0) =
+                            make_float4(xv[e0] * inv_g, xv[e0 + 1] * inv_g, xv[e0 + 2] * inv_g, xv[e0 + 3] * inv_g);
+                        *reinterpret_cast<float4*>(prm.rho + row_g + e0 + 4) =
+                            make_float4(xv[e0 + 4] * inv_g, xv[e0 + 5] * inv_g, xv[e0 + 6] * inv_g, xv[e0 + 7] * inv_g);
+                    }
+                }
+                if (!row_ok) kx = 0.f;
+            }
+            kx = xch.sum(kx);
+            if (row_ok && half == 0 && !prm.probe) {
+                prm.denom[(size_t)head * n + i] = omega * inv_g;
+                if (prm.cg_iters) prm.cg_iters[(size_t)head * n + i] = iters;
+            }
+            const int sU = scale_exp((1.f + kbound * mxx) * 1.001f);
+            const float offU = m2 - (float)sU + (float)sr + (float)ek;
+            const float c_acc = (1.f + kx) * pow2i(sr + ek);
+            publish_p(SW_OUT);
 
-        // ---------------- OUT sweep ----------------
-        uint64_t us_part = 0;
-        for (int kb = 0; kb < nkb; ++kb, ++g) {
-            ok = ok && wait_s(g);
-            const uint32_t tS = tS0 + (g & 1) * 128 + lane_off + half * 64;
-            const uint32_t tAh = tA + lane_off + half * 64;
-            const int lim = lim_of(kb);
-            const bool masked = !(tile_full && kb < tile);
-            float a[64], v[32];
-            uint32_t pk[16];
-            tmem_ld32(tAh, *reinterpret_cast<float(*)[32]>(&a[0]));
-            tmem_ld32(tAh + 32, *reinterpret_cast<float(*)[32]>(&a[32]));
-            tmem_ld32(tS, v);
-            tmem_ld_wait();
-            release_a();
-            if (masked) coef_chunk<true, true, 0>(v, a, c_log2, offU, c_acc, -1.f, half * 64, lim, us_part, pk);
-            else coef_chunk<false, true, 0>(v, a, c_log2, offU, c_acc, -1.f, 0, 0, us_part, pk);
-            tmem_st16(tS, pk);
-            tmem_ld32(tS + 32, v);
-            tmem_ld_wait();
-            if (masked) coef_chunk<true, true, 1>(v, a, c_log2, offU, c_acc, -1.f, half * 64 + 32, lim, us_part, pk);
-            else coef_chunk<false, true, 1>(v, a, c_log2, offU, c_acc, -1.f, 0, 0, us_part, pk);
-            tmem_st16(tS + 16, pk);
-            tmem_st_wait();
-            done_block(g);
-        }
-        ok = ok && wait_y();
-        const float usum = xch.sum(f2_total(us_part));
-        const float osc = pow2i(-ev) / usum;
+            // ---------------- OUT sweep ----------------
+            uint64_t us_part = 0;
+            for (int kb = 0; kb < nkb; ++kb, ++g) {
+                ok = ok && wait_s(g);
+                const uint32_t tS = tS0 + (g & 1) * 128 + lane_off + half * 64;
+                const uint32_t tAh = tA + lane_off + half * 64;
+                const int lim = lim_of(kb);
+                const bool masked = !(tile_full && kb < tile);
+                float a[64], v[32];
+                uint32_t pk[16];
+                tmem_ld32(tAh, *reinterpret_cast<float(*)[32]>(&a[0]));
+                tmem_ld32(tAh + 32, *reinterpret_cast<float(*)[32]>(&a[32]));
+                tmem_ld32(tS, v);
+                tmem_ld_wait();
+                release_a();
+                if (masked) coef_chunk<true, true, 0>(v, a, c_log2, offU, c_acc, -1.f, half * 64, lim, us_part, pk);
+                else coef_chunk<false, true, 0>(v, a, c_log2, offU, c_acc, -1.f, 0, 0, us_part, pk);
+                tmem_st16(tS, pk);
+                tmem_ld32(tS + 32, v);
+                tmem_ld_wait();
+                if (masked) coef_chunk<true, true, 1>(v, a, c_log2, offU, c_acc, -1.f, half * 64 + 32, lim, us_part, pk);
+                else coef_chunk<false, true, 1>(v, a, c_log2, offU, c_acc, -1.f, 0, 0, us_part, pk);
+                tmem_st16(tS + 16, pk);
+                tmem_st_wait();
+                done_block(g);
+            }
+            ok = ok && wait_y();
+            const float usum = xch.sum(f2_total(us_part));
+            const float osc = pow2i(-ev) / usum;
 #pragma unroll
-        for (int c = 0; c < DH / 32; ++c) {
-            float v[32];
-            tmem_ld32(tY + lane_off + half * DH + c * 32, v);
-            tmem_ld_wait();
-            if (row_ok) {
+            for (int c = 0; c < DH / 32; ++c) {
+                float v[32];
+                tmem_ld32(tY + lane_off + half * DH + c * 32, v);
+                tmem_ld_wait();
+                if (row_ok) {
 #pragma unroll
-                for (int j = 0; j < 32; j += 8) {
-                    uint4 o;
-                    __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
+                    for (int j = 0; j < 32; j += 8) {
+                        uint4 o;
+                        __nv_bfloat162* ob = reinterpret_cast<__nv_bfloat162*>(&o);
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) ob[u] = __floats2bfloat162_rn(v[j + 2 * u] * osc, v[j + 2 * u + 1] * osc);
-                    *reinterpret_cast<uint4*>(prm.out + row_g + c * 32 + j) = o;
+                        for (int u = 0; u < 4; ++u) ob[u] = __floats2bfloat162_rn(v[j + 2 * u] * osc, v[j + 2 * u + 1] * osc);
+                        *reinterpret_cast<uint4*>(prm.out + row_g + c * 32 + j) = o;
+                    }
                 }
             }
         }
@@ -1017,69 +1279,92 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #undef LLA_SET_DIRECTION
 }
 
-template <int D>
-cudaError_t launch_d(const Problem& p, void* ws, cudaStream_t stream, const char** why) {
-    const size_t N = (size_t)p.B * p.H * p.n * D;
+// Workspace: header, fp16 copies of q, k, v (and dout for the backward), kbar and x scratch.
+struct TcWs {
+    Header* hdr;
+    __half *q16, *k16, *v16, *g16;
+    float *kbar, *xs;
+};
+TcWs carve(void* ws, size_t N, size_t NT, bool bwd) {
     unsigned char* base = static_cast<unsigned char*>(ws);
-    Header* hdr = reinterpret_cast<Header*>(base);
-    __half* q16 = reinterpret_cast<__half*>(base + HDR_BYTES);
-    __half* k16 = reinterpret_cast<__half*>(base + HDR_BYTES + align256(N * 2));
-    __half* v16 = reinterpret_cast<__half*>(base + HDR_BYTES + 2 * align256(N * 2));
-    const size_t NT = (size_t)p.B * p.H * ((p.n + BQ - 1) / BQ) * BQ * D;   // padded to whole tiles
-    float* kbar = reinterpret_cast<float*>(base + HDR_BYTES + 3 * align256(N * 2));
-    float* xs = reinterpret_cast<float*>(base + HDR_BYTES + 3 * align256(N * 2) + align256(NT * 4));
+    TcWs w;
+    w.hdr = reinterpret_cast<Header*>(base);
+    size_t off = HDR_BYTES;
+    w.q16 = reinterpret_cast<__half*>(base + off); off += align256(N * 2);
+    w.k16 = reinterpret_cast<__half*>(base + off); off += align256(N * 2);
+    w.v16 = reinterpret_cast<__half*>(base + off); off += align256(N * 2);
+    w.g16 = nullptr;
+    if (bwd) { w.g16 = reinterpret_cast<__half*>(base + off); off += align256(N * 2); }
+    w.kbar = reinterpret_cast<float*>(base + off); off += align256(NT * 4);
+    w.xs = reinterpret_cast<float*>(base + off);
+    return w;
+}
 
-    cudaError_t e = cudaMemsetAsync(hdr, 0, HDR_BYTES, stream);
+// Pre-pass, tensor maps and the sweep kernel.  BWD: the backward's stats stage (g = dout).
+template <int D, bool BWD>
+cudaError_t launch_d(int B, int H, int n, const void* qv, const void* kv, const void* vv, const void* gv,
+                     TcParams prm, void* ws, cudaEvent_t ev_begin, cudaEvent_t ev_end, cudaStream_t stream,
+                     const char** why) {
+    const size_t N = (size_t)B * H * n * D;
+    const size_t NT = (size_t)B * H * ((n + BQ - 1) / BQ) * BQ * D;   // padded to whole tiles
+    const TcWs w = carve(ws, N, NT, BWD);
+    cudaError_t e = cudaMemsetAsync(w.hdr, 0, HDR_BYTES, stream);
     if (e != cudaSuccess) { *why = "workspace header clear"; return e; }
     const size_t count8 = N / 8;
     const int pre_blocks = (int)((count8 + 255) / 256 < 152 * 8 ? (count8 + 255) / 256 : 152 * 8);
-    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(p.q);
-    const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(p.k);
-    const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(p.v);
-    lla_maxabs_kernel<<<pre_blocks, 256, 0, stream>>>(q, k, v, count8, hdr);
-    lla_to_half_kernel<<<pre_blocks, 256, 0, stream>>>(q, k, v, q16, k16, v16, count8, hdr);
+    const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(qv);
+    const __nv_bfloat16* k = static_cast<const __nv_bfloat16*>(kv);
+    const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(vv);
+    const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(gv);
+    lla_maxabs_kernel<BWD ? 4 : 3><<<pre_blocks, 256, 0, stream>>>(q, k, v, g, count8, w.hdr);
+    lla_to_half_kernel<BWD ? 4 : 3><<<pre_blocks, 256, 0, stream>>>(q, k, v, g, w.q16, w.k16, w.v16, w.g16, count8, w.hdr);
     e = cudaGetLastError();
     if (e != cudaSuccess) { *why = "operand pre-pass launch"; return e; }
 
-    CUtensorMap tq, tk, tv;
-    const uint64_t slices = (uint64_t)p.B * p.H;
-    if (!make_tmap_f16_3d(&tq, q16, D, p.n, slices, BQ) || !make_tmap_f16_3d(&tk, k16, D, p.n, slices, BK) ||
-        !make_tmap_f16_3d(&tv, v16, D, p.n, slices, BK)) {
+    CUtensorMap tq, tk, tv, tg;
+    const uint64_t slices = (uint64_t)B * H;
+    if (!make_tmap_f16_3d(&tq, w.q16, D, n, slices, BQ) || !make_tmap_f16_3d(&tk, w.k16, D, n, slices, BK) ||
+        !make_tmap_f16_3d(&tv, w.v16, D, n, slices, BK) ||
+        !make_tmap_f16_3d(&tg, BWD ? w.g16 : w.q16, D, n, slices, BQ)) {
         *why = "cuTensorMapEncodeTiled";
         return cudaErrorInvalidValue;
     }
-    TcParams prm;
-    prm.hdr = hdr;
-    prm.kbar = kbar;
-    prm.xs = xs;
+    prm.hdr = w.hdr;
+    prm.kbar = w.kbar;
+    prm.xs = w.xs;
+    prm.dev_err = device_error_word();
+    prm.n = n;
+    prm.n_tiles = (n + BQ - 1) / BQ;
+    if (!prm.dev_err) { *why = "device error word"; return cudaErrorInvalidSymbol; }
+
+    const size_t smem = sizeof(TcSmem<D>);
+    auto kern = lla_tc_kernel<D, BWD>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) { *why = "tensor kernel shared-memory attribute"; return e; }
+    dim3 grid(prm.n_tiles, (unsigned)slices);
+    if (ev_begin && (e = cudaEventRecord(ev_begin, stream)) != cudaSuccess) {
+        *why = "profiling event record";
+        return e;
+    }
+    kern<<<grid, NTHREADS, smem, stream>>>(tq, tk, tv, tg, prm);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) { *why = "tensor kernel launch"; return e; }
+    if (ev_end && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess) *why = "profiling event record";
+    return e;
+}
+
+TcParams forward_params(const Problem& p) {
+    TcParams prm{};
     prm.out = static_cast<__nv_bfloat16*>(p.out);
     prm.rho = p.rho;
     prm.denom = p.denom;
     prm.cg_iters = p.cg_iters;
     prm.probe = p.probe;
-    prm.dev_err = device_error_word();
-    prm.n = p.n;
-    prm.n_tiles = (p.n + BQ - 1) / BQ;
     prm.tau = p.tau;
     prm.lambda = p.lambda;
     prm.cg_tol = p.cg_tol;
     prm.cg_max_iters = p.cg_max_iters;
-    if (!prm.dev_err) { *why = "device error word"; return cudaErrorInvalidSymbol; }
-
-    const size_t smem = sizeof(TcSmem<D>);
-    auto kern = lla_tc_kernel<D>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) { *why = "tensor kernel shared-memory attribute"; return e; }
-    dim3 grid(prm.n_tiles, (unsigned)slices);
-    if (p.ev_main_begin && (e = cudaEventRecord(p.ev_main_begin, stream)) != cudaSuccess) {
-        *why = "profiling event record";
-        return e;
-    }
-    kern<<<grid, NTHREADS, smem, stream>>>(tq, tk, tv, prm);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) { *why = "tensor kernel launch"; return e; }
-    if (p.ev_main_end && (e = cudaEventRecord(p.ev_main_end, stream)) != cudaSuccess) *why = "profiling event record";
-    return e;
+    return prm;
 }
 
 }  // namespace
@@ -1091,8 +1376,39 @@ size_t tensor_workspace_bytes(int B, int H, int n, int d) {
 }
 
 cudaError_t launch_tensor(const Problem& p, void* ws, cudaStream_t stream, const char** why) {
-    if (p.d == 128) return launch_d<128>(p, ws, stream, why);
-    if (p.d == 64) return launch_d<64>(p, ws, stream, why);
+    const TcParams prm = forward_params(p);
+    if (p.d == 128)
+        return launch_d<128, false>(p.B, p.H, p.n, p.q, p.k, p.v, nullptr, prm, ws, p.ev_main_begin, p.ev_main_end,
+                                    stream, why);
+    if (p.d == 64)
+        return launch_d<64, false>(p.B, p.H, p.n, p.q, p.k, p.v, nullptr, prm, ws, p.ev_main_begin, p.ev_main_end,
+                                   stream, why);
+    *why = "tensor path supports d in {64, 128}";
+    return cudaErrorInvalidValue;
+}
+
+size_t tensor_backward_stats_bytes(int B, int H, int n, int d) {
+    return tensor_workspace_bytes(B, H, n, d) + align256((size_t)B * H * n * d * 2);
+}
+
+cudaError_t launch_tensor_backward_stats(const BackwardProblem& p, void* ws, BwdRowRec* rec, float* yvec,
+                                         cudaStream_t stream, const char** why) {
+    TcParams prm{};
+    prm.cg_iters = p.cg_iters;
+    prm.rho_in = p.rho;
+    prm.denom_in = p.denom;
+    prm.rec = rec;
+    prm.yvec = yvec;
+    prm.tau = p.tau;
+    prm.lambda = p.lambda;
+    prm.cg_tol = p.cg_tol;
+    prm.cg_max_iters = p.cg_max_iters;
+    if (p.d == 128)
+        return launch_d<128, true>(p.B, p.H, p.n, p.q, p.k, p.v, p.dout, prm, ws, p.ev_main_begin, p.ev_main_end,
+                                   stream, why);
+    if (p.d == 64)
+        return launch_d<64, true>(p.B, p.H, p.n, p.q, p.k, p.v, p.dout, prm, ws, p.ev_main_begin, p.ev_main_end,
+                                  stream, why);
     *why = "tensor path supports d in {64, 128}";
     return cudaErrorInvalidValue;
 }

@@ -131,29 +131,41 @@ def test_decode_cache_length_limit(lib):
 
 
 def _call_backward(lib, **kw):
-    a = dict(dtype=0, q=16, k=32, v=48, rho=64, den=80, dout=96, dq=112, dk=128, dv=144, it=None, B=1, H=1, n=8,
-             d=64, tau=0.1, lam=1.0, T=4, tol=0.0, ws=None, ws_bytes=0, stream=None)
+    a = dict(dtype=0, path=0, q=16, k=32, v=48, rho=64, den=80, dout=96, dq=112, dk=128, dv=144, it=None, B=1, H=1,
+             n=8, d=64, tau=0.1, lam=1.0, T=4, tol=0.0, ws=None, ws_bytes=0, stream=None)
     a.update(kw)
-    return lib.lla_backward(a["dtype"], a["q"], a["k"], a["v"], a["rho"], a["den"], a["dout"], a["dq"], a["dk"],
-                            a["dv"], a["it"], a["B"], a["H"], a["n"], a["d"], a["tau"], a["lam"], a["T"], a["tol"],
-                            a["ws"], a["ws_bytes"], a["stream"])
+    return lib.lla_backward(a["dtype"], a["path"], a["q"], a["k"], a["v"], a["rho"], a["den"], a["dout"], a["dq"],
+                            a["dk"], a["dv"], a["it"], a["B"], a["H"], a["n"], a["d"], a["tau"], a["lam"], a["T"],
+                            a["tol"], a["ws"], a["ws_bytes"], a["stream"])
 
 
 @pytest.mark.parametrize("bad", [
     dict(q=None), dict(rho=None), dict(den=None), dict(dout=None), dict(dq=None), dict(dk=None), dict(dv=None),
     dict(dv=40), dict(B=0), dict(n=0), dict(H=70000), dict(d=48), dict(tau=0.0), dict(lam=-1.0), dict(T=0),
-    dict(tol=float("nan")), dict(dtype=3), dict(ws=4096, ws_bytes=16), dict(ws=4096 + 16, ws_bytes=1 << 20),
+    dict(tol=float("nan")), dict(dtype=3), dict(path=7), dict(ws=4096, ws_bytes=16),
+    dict(ws=4096 + 16, ws_bytes=1 << 20),
 ])
 def test_backward_invalid_arguments_rejected_before_launch(lib, bad):
     assert _call_backward(lib, **bad) == lla.LLA_ERR_INVALID_ARG
     assert lib.lla_last_error().decode()
 
 
+def test_backward_tensor_path_needs_bf16_and_supported_dim(lib):
+    assert _call_backward(lib, dtype=1, path=lla.LLA_PATH_TENSOR) == lla.LLA_ERR_UNSUPPORTED
+    assert _call_backward(lib, d=32, path=lla.LLA_PATH_TENSOR) == lla.LLA_ERR_UNSUPPORTED
+
+
 def test_backward_workspace_size(lib):
-    # one 32-byte record and one fp32 d-vector per query, each part rounded up to 256 bytes
-    assert lib.lla_backward_workspace_size(2, 3, 100, 64) == 19200 + 153600
-    assert lib.lla_backward_workspace_size(1, 1, 1, 16) == 256 + 256
-    assert lib.lla_backward_workspace_size(0, 1, 1, 16) == 0
+    fp32 = lla.LLA_PATH_FP32
+    # fp32 path: one 32-byte record and one fp32 d-vector per query, each part rounded up to 256 bytes
+    assert lib.lla_backward_workspace_size(0, fp32, 2, 3, 100, 64) == 19200 + 153600
+    assert lib.lla_backward_workspace_size(1, fp32, 1, 1, 1, 16) == 256 + 256
+    assert lib.lla_backward_workspace_size(0, fp32, 0, 1, 1, 16) == 0
+    # tensor path (bf16, d = 64 resolves to it): the records plus the forward kernel's scratch and dout in fp16
+    recs = 19200 + 153600
+    fwd = lib.lla_workspace_size(0, lla.LLA_PATH_TENSOR, 2, 3, 100, 64)
+    g16 = ((2 * 3 * 100 * 64 * 2 + 255) // 256) * 256
+    assert lib.lla_backward_workspace_size(0, lla.LLA_PATH_AUTO, 2, 3, 100, 64) == recs + fwd + g16
 
 
 def test_backward_binding_refuses_cpu_tensors():

@@ -16,6 +16,11 @@ one-key prefix has dq = dk = 0 exactly, since the output is v_0 whatever q and k
   bound on out.  Truncation is part of the definition being compared there.
 A row whose two largest logits lie within 1e-5 relative of each other is a tie at fp32
 resolution: both one-sided oracle gradients are formed and the GPU must match one of them.
+
+Both paths are held to the same gates.  The tensor path runs the stats stage (moments, adjoint
+right-hand side, adjoint CG) on tcgen05 with fp16 operands whose every rounded quantity (weights,
+per-pair coefficients, CG direction) is carried as an fp16 hi + lo pair, about 22 bits, so its
+error budget is that of fp32 arithmetic; q, k, v and dout are bf16 and exact in fp16.
 """
 import math
 
@@ -82,9 +87,10 @@ def _rel_err(gpu, ref, floor):
     return float(np.abs(gpu - ref).max()) / scale
 
 
-def _run_backward(w, qkvg, rho, den, T, tol, return_iters=True):
+def _run_backward(w, qkvg, rho, den, T, tol, return_iters=True, path=lla.LLA_PATH_FP32):
     q, k, v, g = (t.to(DEV) for t in qkvg)
-    res = lla.backward(q, k, v, rho.to(DEV), den.to(DEV), g, w.tau, w.lam, T, tol, return_iters=return_iters)
+    res = lla.backward(q, k, v, rho.to(DEV), den.to(DEV), g, w.tau, w.lam, T, tol, path=path,
+                       return_iters=return_iters)
     torch.cuda.synchronize()
     lla.lla_sync_status()
     return [t.cpu() for t in res]
@@ -125,14 +131,30 @@ def test_backward_converged_every_entry(lla_gpu, d, n):
     _compare(w, (*qkv, g), grads, 4e-4)
 
 
+PATHS = [pytest.param(lla.LLA_PATH_FP32, id="fp32"), pytest.param(lla.LLA_PATH_TENSOR, id="tensor")]
+
+
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("d", [64, 128])
-def test_backward_bf16_inputs_ragged(lla_gpu, d):
+def test_backward_bf16_inputs_ragged(lla_gpu, d, path):
     """bf16 q, k, v and dout (exact in float64 too), several query tiles and a ragged tail."""
     w = workload("lm_bf16", B=2, H=2, n=333, d=d, tau=1.0 / np.sqrt(d))
     qkv = make_inputs(w)
     g = make_cotangent(w)
     rho, den = _exact_rho(qkv, w)
-    grads = _run_backward(w, (*qkv, g), rho, den, 4 * d + 64, 1e-6)
+    grads = _run_backward(w, (*qkv, g), rho, den, 4 * d + 64, 1e-6, path=path)
+    _compare(w, (*qkv, g), grads, 4e-4)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("n", [1, 5, 127, 128, 129, 257])
+def test_backward_tensor_path_edges(lla_gpu, d, n):
+    """The tensor path at tile boundaries and on rank-deficient short prefixes (n < d)."""
+    w = workload("lm_bf16", B=1, H=2, n=n, d=d, tau=1.0 / np.sqrt(d))
+    qkv = make_inputs(w)
+    g = make_cotangent(w)
+    rho, den = _exact_rho(qkv, w)
+    grads = _run_backward(w, (*qkv, g), rho, den, 4 * d + 64, 1e-6, path=lla.LLA_PATH_TENSOR)
     _compare(w, (*qkv, g), grads, 4e-4)
 
 
@@ -157,7 +179,8 @@ def test_backward_after_gpu_forward(lla_gpu):
     _compare(w, (*qkv, g), grads, 1e-3)
 
 
-def test_backward_fixed_cap_matches_capped_oracle(lla_gpu):
+@pytest.mark.parametrize("path", PATHS)
+def test_backward_fixed_cap_matches_capped_oracle(lla_gpu, path):
     """The LM configuration's cap T = 16 (tol 0) on a 1100-long bf16 sequence: rho/denom from the
     GPU fp32 forward at the same cap, the reference is the oracle's capped backward, compared on
     the last 64 positions (their dk/dv need only the rows after them).  Those rows see about 300
@@ -171,7 +194,7 @@ def test_backward_fixed_cap_matches_capped_oracle(lla_gpu):
     g = make_cotangent(w)
     q, k, v = (t.to(DEV) for t in qkv)
     _, rho, den = lla.forward(q, k, v, w.tau, w.lam, w.cg_max_iters, 0.0, path=lla.LLA_PATH_FP32)
-    grads = _run_backward(w, (*qkv, g), rho.cpu(), den.cpu(), w.cg_max_iters, 0.0)
+    grads = _run_backward(w, (*qkv, g), rho.cpu(), den.cpu(), w.cg_max_iters, 0.0, path=path)
     its = grads[3].numpy()
     assert (its <= w.cg_max_iters).all() and (its == w.cg_max_iters).mean() > 0.95
     for t in grads[:3]:
@@ -179,16 +202,18 @@ def test_backward_fixed_cap_matches_capped_oracle(lla_gpu):
     _compare(w, (*qkv, g), grads, 2e-3, rows_from=w.n - 64, cg=(w.cg_max_iters, 0.0))
 
 
-def test_backward_is_deterministic_and_takes_a_workspace(lla_gpu):
-    """No atomics: two runs agree bit for bit, with the pool's scratch or the caller's."""
+@pytest.mark.parametrize("path", PATHS)
+def test_backward_is_deterministic_and_takes_a_workspace(lla_gpu, path):
+    """No atomics on the data path: two runs agree bit for bit, with the pool's scratch or the caller's."""
     w = workload("lm_bf16", B=2, H=2, n=130, d=64, tau=0.125)
     qkv = make_inputs(w)
     g = make_cotangent(w)
     rho, den = _exact_rho(qkv, w)
-    a = _run_backward(w, (*qkv, g), rho, den, 24, 0.0, return_iters=False)
-    ws = torch.empty(lla.lla_backward_workspace_size(w.B, w.H, w.n, w.d), dtype=torch.uint8, device=DEV)
+    a = _run_backward(w, (*qkv, g), rho, den, 24, 0.0, return_iters=False, path=path)
+    ws = torch.empty(lla.lla_backward_workspace_size(lla.LLA_DTYPE_BF16, path, w.B, w.H, w.n, w.d),
+                     dtype=torch.uint8, device=DEV)
     q, k, v, gg = (t.to(DEV) for t in (*qkv, g))
-    b = lla.backward(q, k, v, rho.to(DEV), den.to(DEV), gg, w.tau, w.lam, 24, 0.0, workspace=ws)
+    b = lla.backward(q, k, v, rho.to(DEV), den.to(DEV), gg, w.tau, w.lam, 24, 0.0, path=path, workspace=ws)
     torch.cuda.synchronize()
     for x, y in zip(a, b):
         assert torch.equal(x, y.cpu())
@@ -209,7 +234,7 @@ def test_backward_single_key_rows(lla_gpu):
 @pytest.mark.slow
 def test_backward_lm_full_size_sampled(lla_gpu):
     """The LM workload at full size (8 x 16 heads x 4096, d = 128, bf16) in the configuration the
-    benchmark times (T = 16, tol 0): dq, dk and dv of the last 40 positions of two heads (their
+    benchmark times (T = 16, tol 0, the default path: tensor stats stage): dq, dk and dv of the last 40 positions of two heads (their
     dk/dv need every later row: 40 oracle rows each) against the capped oracle; every entry of
     every head finite."""
     w = workload("lm_bf16")
@@ -218,7 +243,8 @@ def test_backward_lm_full_size_sampled(lla_gpu):
     q, k, v = (t.to(DEV) for t in qkv)
     _, rho, den = lla.forward(q, k, v, w.tau, w.lam, w.cg_max_iters, 0.0, path=lla.LLA_PATH_FP32)
     del q, k, v
-    grads = _run_backward(w, (*qkv, g), rho.cpu(), den.cpu(), w.cg_max_iters, 0.0, return_iters=False)
+    grads = _run_backward(w, (*qkv, g), rho.cpu(), den.cpu(), w.cg_max_iters, 0.0, return_iters=False,
+                          path=lla.LLA_PATH_AUTO)
     for t in grads:
         assert torch.isfinite(t).all()
     _compare(w, (*qkv, g), grads, 2e-3, heads=[(0, 0), (w.B - 1, w.H - 1)], rows_from=w.n - 40,
