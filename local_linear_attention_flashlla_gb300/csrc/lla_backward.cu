@@ -150,20 +150,6 @@ struct QSmem {
     float m2[BQ][BK + 1];
 };
 
-template <int D>
-struct KSmem {
-    float k[BK][D + 1];    // this CTA's key rows
-    float v[BK][D + 1];    // and value rows
-    float q[BQ][D + 1];    // current query tile: q, g, rho', y
-    float g[BQ][D + 1];
-    float rho[BQ][D + 1];
-    float u[BQ][D + 1];
-    float cq[BK][BQ + 1];  // per-pair coefficients of q_i, y_i, rho'_i (for dk) and g_i (for dv)
-    float cu[BK][BQ + 1];
-    float cr[BK][BQ + 1];
-    float cv[BK][BQ + 1];
-    RowRec rec[BQ];
-};
 
 template <int D, typename T>
 __global__ void __launch_bounds__(NT, 1)
@@ -368,156 +354,320 @@ lla_bwd_stats_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
     }
 }
 
-// dq_i = tau (sum_j ds_ij k_j - sd_i k_jm) + y_i, one CTA per tile of BQ queries, from the
-// per-row records and y.
+// ---- dq and dk/dv: register-tiled fp32 sweeps over the records ----------------------------
+// Both kernels form, for a block of (query, key) pairs, the four dot products s = q.k,
+// a1 = rho'.k, a2 = y.k, h = g.v (phase A), the per-pair coefficients (phase B) and then the
+// gradient sums (phase C).  Each thread owns a small register tile of pairs or outputs and
+// reads its shared-memory operands as float4, so an FMA costs an eighth of a load instead of
+// one: q, rho', y, g rows are stored [row][coordinate], key rows [coordinate][key].
+constexpr int KB2 = 64;        // keys per CTA of the dk/dv kernel
+constexpr int QB2 = 32;        // queries per step of the dk/dv kernel
+constexpr int QB3 = 64;        // queries per CTA of the dq kernel
+constexpr int KS3 = 32;        // keys per step of the dq kernel
+
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float at4(const float4& v, int u) { return u == 0 ? v.x : u == 1 ? v.y : u == 2 ? v.z : v.w; }
+
+// EC consecutive floats (EC in {1, 2, 4, 8}; 16-byte aligned when EC >= 4)
+template <int EC>
+__device__ __forceinline__ void load_ec(const float* p, float (&o)[EC]) {
+    if constexpr (EC % 4 == 0) {
+#pragma unroll
+        for (int h = 0; h < EC; h += 4) {
+            const float4 t = ld4(p + h);
+            o[h] = t.x; o[h + 1] = t.y; o[h + 2] = t.z; o[h + 3] = t.w;
+        }
+    } else {
+#pragma unroll
+        for (int h = 0; h < EC; ++h) o[h] = p[h];
+    }
+}
+template <int EC>
+__device__ __forceinline__ void store_ec(float* p, const float (&o)[EC]) {
+    if constexpr (EC % 4 == 0) {
+#pragma unroll
+        for (int h = 0; h < EC; h += 4) *reinterpret_cast<float4*>(p + h) = make_float4(o[h], o[h + 1], o[h + 2], o[h + 3]);
+    } else {
+#pragma unroll
+        for (int h = 0; h < EC; ++h) p[h] = o[h];
+    }
+}
+
+// rows [row0, row0+rows) of a [n, D] slice into dst[row][0..D) (row stride DP), zero beyond n
+template <int D, int DP, typename T>
+__device__ __forceinline__ void stage_rows(float* dst, const T* src, int row0, int rows, int n, const RowRec* rec = nullptr) {
+    for (int idx = threadIdx.x; idx < rows * D; idx += NT) {
+        const int r = idx / D, e = idx - r * D;
+        const int gr = row0 + r;
+        float x = (gr < n) ? ld_f(src + (size_t)gr * D + e) : 0.f;
+        if (rec) x *= rec[r].rp_scale;        // rho' = (omega/denom) rho
+        dst[r * DP + e] = x;
+    }
+}
+// rows [row0, row0+rows) transposed into dst[coordinate][row] (row stride KP), zero beyond n
+template <int D, int KP, typename T>
+__device__ __forceinline__ void stage_cols(float* dst, const T* src, int row0, int rows, int n) {
+    for (int idx = threadIdx.x; idx < rows * D; idx += NT) {
+        const int r = idx / D, e = idx - r * D;
+        const int gr = row0 + r;
+        dst[e * KP + r] = (gr < n) ? ld_f(src + (size_t)gr * D + e) : 0.f;
+    }
+}
+
+// Phase A for two query rows (qa, qb: [row][coordinate] with stride DP) against four keys
+// (kT, vT: [coordinate][key] with stride KP, starting at the thread's first key).
+template <int D, int DP, int KP>
+__device__ __forceinline__ void pair_dots(const float* qa, const float* ra, const float* ya, const float* ga,
+                                          const float* kT, const float* vT, float (&s)[2][4], float (&a1)[2][4],
+                                          float (&a2)[2][4], float (&h)[2][4]) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) { s[u][c] = 0.f; a1[u][c] = 0.f; a2[u][c] = 0.f; h[u][c] = 0.f; }
+#pragma unroll 2
+    for (int e = 0; e < D; e += 4) {
+        const float4 q0 = ld4(qa + e), q1 = ld4(qa + DP + e);
+        const float4 r0 = ld4(ra + e), r1 = ld4(ra + DP + e);
+        const float4 y0 = ld4(ya + e), y1 = ld4(ya + DP + e);
+        const float4 g0 = ld4(ga + e), g1 = ld4(ga + DP + e);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float4 kk = ld4(kT + (e + u) * KP), vv = ld4(vT + (e + u) * KP);
+            const float kc[4] = {kk.x, kk.y, kk.z, kk.w}, vc[4] = {vv.x, vv.y, vv.z, vv.w};
+            const float qe[2] = {at4(q0, u), at4(q1, u)}, re[2] = {at4(r0, u), at4(r1, u)};
+            const float ye[2] = {at4(y0, u), at4(y1, u)}, ge[2] = {at4(g0, u), at4(g1, u)};
+#pragma unroll
+            for (int w = 0; w < 2; ++w)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    s[w][c] = fmaf(qe[w], kc[c], s[w][c]);
+                    a1[w][c] = fmaf(re[w], kc[c], a1[w][c]);
+                    a2[w][c] = fmaf(ye[w], kc[c], a2[w][c]);
+                    h[w][c] = fmaf(ge[w], vc[c], h[w][c]);
+                }
+        }
+    }
+}
+
+// Phase B for one pair: wbar Ahat, -wbar Bhat and ds - (path through the row maximum)
+__device__ __forceinline__ void pair_coef(const RowRec& R, bool valid, bool at_max, float tau, float s, float a1,
+                                          float a2, float h, float& cq, float& cw, float& cr) {
+    const float wb = valid ? expf(tau * s - R.m) * R.inv_omega : 0.f;
+    const float Ah = 1.f - (a1 - R.kb_rp);
+    const float Bh = (h - R.hbar) - (a2 - R.kb_y);
+    const float ds = wb * Ah * Bh;
+    cq = tau * (ds - (valid && at_max ? R.sd : 0.f));
+    cw = wb * Ah;
+    cr = -wb * Bh;
+}
+
+template <int D>
+struct K2Smem {
+    static constexpr int KP = KB2 + 4, DP = D + 4;
+    float kT[D * KP];              // this CTA's keys and values, [coordinate][key]
+    float vT[D * KP];
+    float q[QB2 * DP];             // the current query step, [query][coordinate]
+    float r[QB2 * DP];             // rho'
+    float y[QB2 * DP];
+    float g[QB2 * DP];
+    float cq[QB2 * KP];            // tau (ds - max path), [query][key]
+    float cw[QB2 * KP];            // wbar Ahat
+    float cr[QB2 * KP];            // -wbar Bhat
+    RowRec rec[QB2];
+};
+
+// dk_j = sum_{i >= j} [cq_ij q_i - cw_ij y_i + cr_ij rho'_i],  dv_j = sum_{i >= j} cw_ij g_i.
+template <int D, typename T>
+__global__ void __launch_bounds__(NT, 1)
+lla_bwd_key_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                   const T* __restrict__ dout, const float* __restrict__ rho, const RowRec* __restrict__ rec,
+                   const float* __restrict__ uvec, float* __restrict__ dk, float* __restrict__ dv, int n, float tau) {
+    using S = K2Smem<D>;
+    constexpr int KP = S::KP, DP = S::DP;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    S& sm = *reinterpret_cast<S*>(smem_raw);
+    const int tid = threadIdx.x;
+    const int j0 = (int)blockIdx.x * KB2;       // the earliest keys have the longest query range: first
+    const size_t head = blockIdx.y;
+    const size_t hoff = head * (size_t)n * D;
+
+    stage_cols<D, KP>(sm.kT, k + hoff, j0, KB2, n);
+    stage_cols<D, KP>(sm.vT, v + hoff, j0, KB2, n);
+    // phase A/B tile: 4 keys x 2 queries; phase C tile: 4 keys x EC coordinates
+    constexpr int EC = D / 16;
+    const int kg = tid & 15, qg = tid >> 4;
+    const int kc2 = tid >> 4, ec = (tid & 15) * EC;
+    float dka[4][EC], dva[4][EC];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+        for (int e = 0; e < EC; ++e) { dka[c][e] = 0.f; dva[c][e] = 0.f; }
+
+    for (int i0 = j0; i0 < n; i0 += QB2) {
+        __syncthreads();
+        if (tid < QB2) {
+            RowRec z{};
+            sm.rec[tid] = (i0 + tid < n) ? rec[head * (size_t)n + i0 + tid] : z;
+        }
+        stage_rows<D, DP>(sm.q, q + hoff, i0, QB2, n);
+        stage_rows<D, DP>(sm.g, dout + hoff, i0, QB2, n);
+        stage_rows<D, DP>(sm.y, uvec + hoff, i0, QB2, n);
+        __syncthreads();
+        stage_rows<D, DP>(sm.r, rho + hoff, i0, QB2, n, sm.rec);
+        __syncthreads();
+        {   // phases A and B
+            float s_[2][4], a1[2][4], a2[2][4], h[2][4];
+            const int ql = 2 * qg;
+            pair_dots<D, DP, KP>(sm.q + ql * DP, sm.r + ql * DP, sm.y + ql * DP, sm.g + ql * DP, sm.kT + 4 * kg,
+                                 sm.vT + 4 * kg, s_, a1, a2, h);
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+                const RowRec& R = sm.rec[ql + w];
+                const int i = i0 + ql + w;
+                float cq[4], cw[4], cr[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const int j = j0 + 4 * kg + c;
+                    const bool valid = j < n && i < n && j <= i;
+                    pair_coef(R, valid, j == R.jm, tau, s_[w][c], a1[w][c], a2[w][c], h[w][c], cq[c], cw[c], cr[c]);
+                }
+                *reinterpret_cast<float4*>(sm.cq + (ql + w) * KP + 4 * kg) = make_float4(cq[0], cq[1], cq[2], cq[3]);
+                *reinterpret_cast<float4*>(sm.cw + (ql + w) * KP + 4 * kg) = make_float4(cw[0], cw[1], cw[2], cw[3]);
+                *reinterpret_cast<float4*>(sm.cr + (ql + w) * KP + 4 * kg) = make_float4(cr[0], cr[1], cr[2], cr[3]);
+            }
+        }
+        __syncthreads();
+        // phase C
+#pragma unroll 2
+        for (int il = 0; il < QB2; ++il) {
+            const float4 cq4 = ld4(sm.cq + il * KP + 4 * kc2), cw4 = ld4(sm.cw + il * KP + 4 * kc2);
+            const float4 cr4 = ld4(sm.cr + il * KP + 4 * kc2);
+            const float cq[4] = {cq4.x, cq4.y, cq4.z, cq4.w}, cw[4] = {cw4.x, cw4.y, cw4.z, cw4.w};
+            const float cr[4] = {cr4.x, cr4.y, cr4.z, cr4.w};
+            float qv[EC], yv[EC], rv[EC], gv[EC];
+            load_ec<EC>(sm.q + il * DP + ec, qv);
+            load_ec<EC>(sm.y + il * DP + ec, yv);
+            load_ec<EC>(sm.r + il * DP + ec, rv);
+            load_ec<EC>(sm.g + il * DP + ec, gv);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int e = 0; e < EC; ++e) {
+                    float t = fmaf(cq[c], qv[e], dka[c][e]);
+                    t = fmaf(-cw[c], yv[e], t);
+                    dka[c][e] = fmaf(cr[c], rv[e], t);
+                    dva[c][e] = fmaf(cw[c], gv[e], dva[c][e]);
+                }
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int j = j0 + 4 * kc2 + c;
+        if (j < n) {
+            store_ec<EC>(dk + hoff + (size_t)j * D + ec, dka[c]);
+            store_ec<EC>(dv + hoff + (size_t)j * D + ec, dva[c]);
+        }
+    }
+}
+
+template <int D>
+struct Q3Smem {
+    static constexpr int KP = KS3 + 4, DP = D + 4, QP = QB3 + 4;
+    float q[QB3 * DP];             // this CTA's queries, [query][coordinate]
+    float r[QB3 * DP];
+    float y[QB3 * DP];
+    float g[QB3 * DP];
+    float kT[D * KP];              // the current key step, [coordinate][key]
+    float vT[D * KP];
+    float k[KS3 * DP];             // the same keys, [key][coordinate]
+    float ds[KS3 * QP];            // tau (ds - max path) / tau, [key][query]
+    RowRec rec[QB3];
+};
+
+// dq_i = tau (sum_j ds_ij k_j - sd_i k_jm) + y_i over the keys j <= i.
 template <int D, typename T>
 __global__ void __launch_bounds__(NT, 1)
 lla_bwd_dq_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                   const T* __restrict__ dout, const float* __restrict__ rho, const RowRec* __restrict__ rec,
                   const float* __restrict__ uvec, float* __restrict__ dq, int n, int n_tiles, float tau) {
-    constexpr int E = D / 8;
+    using S = Q3Smem<D>;
+    constexpr int KP = S::KP, DP = S::DP, QP = S::QP;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    QSmem<D>& sm = *reinterpret_cast<QSmem<D>*>(smem_raw);
-
-    const int tile = n_tiles - 1 - (int)blockIdx.x;
+    S& sm = *reinterpret_cast<S*>(smem_raw);
+    const int tid = threadIdx.x;
+    const int i0 = (n_tiles - 1 - (int)blockIdx.x) * QB3;    // longest causal ranges first
     const size_t head = blockIdx.y;
     const size_t hoff = head * (size_t)n * D;
-    const T* kh = k + hoff;
-    const T* vh = v + hoff;
-    const int tid = threadIdx.x;
-    const int r = tid >> 3;
-    const int l8 = tid & 7;
-    const int i0 = tile * BQ;
-    const int i = i0 + r;
-    const bool row_ok = i < n;
-    const int last_key = min(n - 1, i0 + BQ - 1);
-    const int n_blocks = last_key / BK + 1;
+    const int last_key = min(n - 1, i0 + QB3 - 1);
 
-    RowRec R{};
-    if (row_ok) R = rec[head * (size_t)n + i];
-    load_rows<D>(sm.q, q + hoff, i0, BQ, n);
-    load_rows<D>(sm.g, dout + hoff, i0, BQ, n);
-    load_rows<D>(sm.u, uvec + hoff, i0, BQ, n);
-#pragma unroll
-    for (int c = 0; c < E; ++c) {   // rho' = (omega/denom) rho; each row is read by its own lanes only
-        const int e = l8 + 8 * c;
-        sm.p[r][e] = row_ok ? __ldg(rho + hoff + (size_t)i * D + e) * R.rp_scale : 0.f;
+    if (tid < QB3) {
+        RowRec z{};
+        sm.rec[tid] = (i0 + tid < n) ? rec[head * (size_t)n + i0 + tid] : z;
     }
-    float dqa[E];
+    stage_rows<D, DP>(sm.q, q + hoff, i0, QB3, n);
+    stage_rows<D, DP>(sm.g, dout + hoff, i0, QB3, n);
+    stage_rows<D, DP>(sm.y, uvec + hoff, i0, QB3, n);
+    __syncthreads();
+    stage_rows<D, DP>(sm.r, rho + hoff, i0, QB3, n, sm.rec);
+    // phase A/B tile: 2 queries x 4 keys; phase C tile: 4 queries x EC coordinates
+    constexpr int EC = D / 16;
+    const int kg = tid & 7, qg = tid >> 3;
+    const int qc = (tid >> 4) * 4, ec = (tid & 15) * EC;
+    float dqa[4][EC];
 #pragma unroll
-    for (int c = 0; c < E; ++c) dqa[c] = 0.f;
-    for (int kb = 0; kb < n_blocks; ++kb) {
-        __syncthreads();
-        load_rows<D>(sm.kb, kh, kb * BK, BK, n);
-        load_rows<D>(sm.vb, vh, kb * BK, BK, n);
-        __syncthreads();
-        float s[JPT], a1[JPT], a2[JPT], hh[JPT], o1[JPT], o2[JPT];
-        dots_rows<D, 3>(sm.q, sm.p, sm.u, sm.kb, r, l8, s, a1, a2);
-        dots_rows<D, 1>(sm.g, nullptr, nullptr, sm.vb, r, l8, hh, o1, o2);
+    for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int c = 0; c < JPT; ++c) {
-            const int j = kb * BK + l8 + 8 * c;
-            const float wb = (j <= i && row_ok) ? expf(tau * s[c] - R.m) * R.inv_omega : 0.f;
-            const float Ah = 1.f - (a1[c] - R.kb_rp);
-            const float Bh = (hh[c] - R.hbar) - (a2[c] - R.kb_y);
-            sm.m[r][l8 + 8 * c] = wb * Ah * Bh;
-        }
-        __syncwarp();
-        acc_rows<D>(sm.m, sm.kb, r, l8, dqa);
-    }
-    if (row_ok) {
-        const T* kjm = kh + (size_t)R.jm * D;
-        const size_t rbase = hoff + (size_t)i * D;
-#pragma unroll
-        for (int c = 0; c < E; ++c) {
-            const int e = l8 + 8 * c;
-            dq[rbase + e] = fmaf(tau, dqa[c] - R.sd * ld_f(kjm + e), sm.u[r][e]);
-        }
-    }
-}
+        for (int e = 0; e < EC; ++e) dqa[c][e] = 0.f;
 
-template <int D, typename T>
-__global__ void __launch_bounds__(NT, 1)
-lla_bwd_key_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
-                   const T* __restrict__ dout, const float* __restrict__ rho, const RowRec* __restrict__ rec,
-                   const float* __restrict__ uvec, float* __restrict__ dk, float* __restrict__ dv, int n,
-                   int n_tiles, float tau) {
-    constexpr int E = D / 8;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    KSmem<D>& sm = *reinterpret_cast<KSmem<D>*>(smem_raw);
-
-    const int kblk = (int)blockIdx.x;  // the earliest keys have the longest query range: first
-    const size_t head = blockIdx.y;
-    const size_t hoff = head * (size_t)n * D;
-    const int tid = threadIdx.x;
-    const int r = tid >> 3;
-    const int l8 = tid & 7;
-    const int j0 = kblk * BK;
-    const int j = j0 + r;
-    const bool key_ok = j < n;
-
-    load_rows<D>(sm.k, k + hoff, j0, BK, n);
-    load_rows<D>(sm.v, v + hoff, j0, BK, n);
-    float dka[E], dva[E];
-#pragma unroll
-    for (int c = 0; c < E; ++c) { dka[c] = 0.f; dva[c] = 0.f; }
-
-    for (int qt = kblk; qt < n_tiles; ++qt) {
-        const int i0 = qt * BQ;
+    for (int j0 = 0; j0 <= last_key; j0 += KS3) {
         __syncthreads();
-        if (tid < BQ) {
-            RowRec z{};
-            sm.rec[tid] = (i0 + tid < n) ? rec[head * (size_t)n + i0 + tid] : z;
-        }
-        load_rows<D>(sm.q, q + hoff, i0, BQ, n);
-        load_rows<D>(sm.g, dout + hoff, i0, BQ, n);
-        load_rows<D>(sm.u, uvec + hoff, i0, BQ, n);
+        stage_cols<D, KP>(sm.kT, k + hoff, j0, KS3, n);
+        stage_cols<D, KP>(sm.vT, v + hoff, j0, KS3, n);
+        stage_rows<D, DP>(sm.k, k + hoff, j0, KS3, n);
         __syncthreads();
-        for (int idx = tid; idx < BQ * D; idx += NT) {   // rho' = (omega/denom) rho
-            const int rr = idx / D, e = idx - rr * D;
-            const int gi = i0 + rr;
-            sm.rho[rr][e] = (gi < n) ? __ldg(rho + hoff + (size_t)gi * D + e) * sm.rec[rr].rp_scale : 0.f;
-        }
-        __syncthreads();
-        float s[JPT], kr[JPT], ky[JPT], hh[JPT], o1[JPT], o2[JPT];
-        dots_blocks<D, 3>(sm.k, sm.q, sm.rho, sm.u, r, l8, s, kr, ky);
-        dots_blocks<D, 1>(sm.v, sm.g, nullptr, nullptr, r, l8, hh, o1, o2);
+        {
+            float s_[2][4], a1[2][4], a2[2][4], h[2][4];
+            const int ql = 2 * qg;
+            pair_dots<D, DP, KP>(sm.q + ql * DP, sm.r + ql * DP, sm.y + ql * DP, sm.g + ql * DP, sm.kT + 4 * kg,
+                                 sm.vT + 4 * kg, s_, a1, a2, h);
 #pragma unroll
-        for (int c = 0; c < JPT; ++c) {
-            const int ii = l8 + 8 * c;
-            const int i = i0 + ii;
-            const RowRec& R = sm.rec[ii];
-            const bool valid = key_ok && i < n && j <= i;
-            const float wb = valid ? expf(tau * s[c] - R.m) * R.inv_omega : 0.f;
-            const float Ah = 1.f - (kr[c] - R.kb_rp);
-            const float Bh = (hh[c] - R.hbar) - (ky[c] - R.kb_y);
-            const float ds = wb * Ah * Bh;
-            const float corr = (valid && j == R.jm) ? R.sd : 0.f;  // through the row maximum
-            sm.cq[r][ii] = tau * (ds - corr);
-            sm.cu[r][ii] = -wb * Ah;
-            sm.cr[r][ii] = -wb * Bh;
-            sm.cv[r][ii] = wb * Ah;
-        }
-        __syncwarp();
-#pragma unroll 2
-        for (int ii = 0; ii < BQ; ++ii) {
-            const float a = sm.cq[r][ii], bu = sm.cu[r][ii], br = sm.cr[r][ii], bv = sm.cv[r][ii];
+            for (int w = 0; w < 2; ++w) {
+                const RowRec& R = sm.rec[ql + w];
+                const int i = i0 + ql + w;
 #pragma unroll
-            for (int c = 0; c < E; ++c) {
-                const int e = l8 + 8 * c;
-                float t = fmaf(a, sm.q[ii][e], dka[c]);
-                t = fmaf(bu, sm.u[ii][e], t);
-                dka[c] = fmaf(br, sm.rho[ii][e], t);
-                dva[c] = fmaf(bv, sm.g[ii][e], dva[c]);
+                for (int c = 0; c < 4; ++c) {
+                    const int j = j0 + 4 * kg + c;
+                    const bool valid = j < n && i < n && j <= i;
+                    const float wb = valid ? expf(tau * s_[w][c] - R.m) * R.inv_omega : 0.f;
+                    const float Ah = 1.f - (a1[w][c] - R.kb_rp);
+                    const float Bh = (h[w][c] - R.hbar) - (a2[w][c] - R.kb_y);
+                    sm.ds[(4 * kg + c) * QP + ql + w] = wb * Ah * Bh;
+                }
             }
         }
-    }
-    if (key_ok) {
-        const size_t base = hoff + (size_t)j * D;
+        __syncthreads();
+#pragma unroll 2
+        for (int jl = 0; jl < KS3; ++jl) {
+            const float4 d4 = ld4(sm.ds + jl * QP + qc);
+            const float dsv[4] = {d4.x, d4.y, d4.z, d4.w};
+            float kv[EC];
+            load_ec<EC>(sm.k + jl * DP + ec, kv);
 #pragma unroll
-        for (int c = 0; c < E; ++c) {
-            dk[base + l8 + 8 * c] = dka[c];
-            dv[base + l8 + 8 * c] = dva[c];
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+                for (int e = 0; e < EC; ++e) dqa[c][e] = fmaf(dsv[c], kv[e], dqa[c][e]);
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int il = qc + c, i = i0 + il;
+        if (i < n) {
+            const RowRec& R = sm.rec[il];
+            const T* kjm = k + hoff + (size_t)R.jm * D + ec;
+            float o[EC];
+#pragma unroll
+            for (int e = 0; e < EC; ++e) o[e] = fmaf(tau, dqa[c][e] - R.sd * ld_f(kjm + e), sm.y[il * DP + ec + e]);
+            store_ec<EC>(dq + hoff + (size_t)i * D + ec, o);
         }
     }
 }
@@ -543,22 +693,22 @@ cudaError_t launch_stats_typed(const BackwardProblem& p, RowRec* rec, float* uve
 
 template <int D, typename T>
 cudaError_t launch_rest_typed(const BackwardProblem& p, const RowRec* rec, const float* uvec, cudaStream_t stream) {
-    const int n_tiles = (p.n + BQ - 1) / BQ;
     auto kd = lla_bwd_dq_kernel<D, T>;
     auto kk = lla_bwd_key_kernel<D, T>;
-    const size_t smq = sizeof(QSmem<D>), smk = sizeof(KSmem<D>);
-    cudaError_t err = cudaFuncSetAttribute(kd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smq);
+    const size_t smd = sizeof(Q3Smem<D>), smk = sizeof(K2Smem<D>);
+    cudaError_t err = cudaFuncSetAttribute(kd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smd);
     if (err != cudaSuccess) return err;
     err = cudaFuncSetAttribute(kk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smk);
     if (err != cudaSuccess) return err;
-    const dim3 grid(n_tiles, p.B * p.H);
     const T* q = static_cast<const T*>(p.q);
     const T* k = static_cast<const T*>(p.k);
     const T* v = static_cast<const T*>(p.v);
     const T* g = static_cast<const T*>(p.dout);
-    kd<<<grid, NT, smq, stream>>>(q, k, v, g, p.rho, rec, uvec, p.dq, p.n, n_tiles, p.tau);
+    const int dq_tiles = (p.n + QB3 - 1) / QB3;
+    kd<<<dim3(dq_tiles, p.B * p.H), NT, smd, stream>>>(q, k, v, g, p.rho, rec, uvec, p.dq, p.n, dq_tiles, p.tau);
     if ((err = cudaGetLastError()) != cudaSuccess) return err;
-    kk<<<grid, NT, smk, stream>>>(q, k, v, g, p.rho, rec, uvec, p.dk, p.dv, p.n, n_tiles, p.tau);
+    kk<<<dim3((p.n + KB2 - 1) / KB2, p.B * p.H), NT, smk, stream>>>(q, k, v, g, p.rho, rec, uvec, p.dk, p.dv, p.n,
+                                                                     p.tau);
     return cudaGetLastError();
 }
 
