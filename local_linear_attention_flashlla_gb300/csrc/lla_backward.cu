@@ -368,28 +368,36 @@ constexpr int KS3 = 32;        // keys per step of the dq kernel
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ float at4(const float4& v, int u) { return u == 0 ? v.x : u == 1 ? v.y : u == 2 ? v.z : v.w; }
 
-// EC consecutive floats (EC in {1, 2, 4, 8}; 16-byte aligned when EC >= 4)
-template <int EC>
-__device__ __forceinline__ void load_ec(const float* p, float (&o)[EC]) {
-    if constexpr (EC % 4 == 0) {
-#pragma unroll
-        for (int h = 0; h < EC; h += 4) {
-            const float4 t = ld4(p + h);
-            o[h] = t.x; o[h + 1] = t.y; o[h + 2] = t.z; o[h + 3] = t.w;
-        }
+// Phase C coordinates of thread group eg (0..15): EC = D/16 per thread.  With EC = 8 the two
+// float4 halves sit at 4 eg and D/2 + 4 eg, so the 16 groups of a warp read contiguous 256-byte
+// runs (no bank conflicts); otherwise EC consecutive coordinates from EC eg.
+template <int D, int EC>
+__device__ __forceinline__ int ec_col(int eg, int h) {
+    return EC == 8 ? (h < 4 ? 4 * eg + h : D / 2 + 4 * eg + h - 4) : EC * eg + h;
+}
+template <int D, int EC>
+__device__ __forceinline__ void load_ec(const float* row, int eg, float (&o)[EC]) {
+    if constexpr (EC == 8) {
+        const float4 a = ld4(row + 4 * eg), b = ld4(row + D / 2 + 4 * eg);
+        o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+    } else if constexpr (EC == 4) {
+        const float4 a = ld4(row + 4 * eg);
+        o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w;
     } else {
 #pragma unroll
-        for (int h = 0; h < EC; ++h) o[h] = p[h];
+        for (int h = 0; h < EC; ++h) o[h] = row[EC * eg + h];
     }
 }
-template <int EC>
-__device__ __forceinline__ void store_ec(float* p, const float (&o)[EC]) {
-    if constexpr (EC % 4 == 0) {
-#pragma unroll
-        for (int h = 0; h < EC; h += 4) *reinterpret_cast<float4*>(p + h) = make_float4(o[h], o[h + 1], o[h + 2], o[h + 3]);
+template <int D, int EC>
+__device__ __forceinline__ void store_ec(float* row, int eg, const float (&o)[EC]) {
+    if constexpr (EC == 8) {
+        *reinterpret_cast<float4*>(row + 4 * eg) = make_float4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<float4*>(row + D / 2 + 4 * eg) = make_float4(o[4], o[5], o[6], o[7]);
+    } else if constexpr (EC == 4) {
+        *reinterpret_cast<float4*>(row + 4 * eg) = make_float4(o[0], o[1], o[2], o[3]);
     } else {
 #pragma unroll
-        for (int h = 0; h < EC; ++h) p[h] = o[h];
+        for (int h = 0; h < EC; ++h) row[EC * eg + h] = o[h];
     }
 }
 
@@ -496,7 +504,7 @@ lla_bwd_key_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
     // phase A/B tile: 4 keys x 2 queries; phase C tile: 4 keys x EC coordinates
     constexpr int EC = D / 16;
     const int kg = tid & 15, qg = tid >> 4;
-    const int kc2 = tid >> 4, ec = (tid & 15) * EC;
+    const int kc2 = tid >> 4, eg = tid & 15;
     float dka[4][EC], dva[4][EC];
 #pragma unroll
     for (int c = 0; c < 4; ++c)
@@ -545,10 +553,10 @@ lla_bwd_key_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
             const float cq[4] = {cq4.x, cq4.y, cq4.z, cq4.w}, cw[4] = {cw4.x, cw4.y, cw4.z, cw4.w};
             const float cr[4] = {cr4.x, cr4.y, cr4.z, cr4.w};
             float qv[EC], yv[EC], rv[EC], gv[EC];
-            load_ec<EC>(sm.q + il * DP + ec, qv);
-            load_ec<EC>(sm.y + il * DP + ec, yv);
-            load_ec<EC>(sm.r + il * DP + ec, rv);
-            load_ec<EC>(sm.g + il * DP + ec, gv);
+            load_ec<D, EC>(sm.q + il * DP, eg, qv);
+            load_ec<D, EC>(sm.y + il * DP, eg, yv);
+            load_ec<D, EC>(sm.r + il * DP, eg, rv);
+            load_ec<D, EC>(sm.g + il * DP, eg, gv);
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -564,8 +572,8 @@ lla_bwd_key_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
     for (int c = 0; c < 4; ++c) {
         const int j = j0 + 4 * kc2 + c;
         if (j < n) {
-            store_ec<EC>(dk + hoff + (size_t)j * D + ec, dka[c]);
-            store_ec<EC>(dv + hoff + (size_t)j * D + ec, dva[c]);
+            store_ec<D, EC>(dk + hoff + (size_t)j * D, eg, dka[c]);
+            store_ec<D, EC>(dv + hoff + (size_t)j * D, eg, dva[c]);
         }
     }
 }
@@ -612,7 +620,7 @@ lla_bwd_dq_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
     // phase A/B tile: 2 queries x 4 keys; phase C tile: 4 queries x EC coordinates
     constexpr int EC = D / 16;
     const int kg = tid & 7, qg = tid >> 3;
-    const int qc = (tid >> 4) * 4, ec = (tid & 15) * EC;
+    const int qc = (tid >> 4) * 4, eg = tid & 15;
     float dqa[4][EC];
 #pragma unroll
     for (int c = 0; c < 4; ++c)
@@ -651,7 +659,7 @@ lla_bwd_dq_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
             const float4 d4 = ld4(sm.ds + jl * QP + qc);
             const float dsv[4] = {d4.x, d4.y, d4.z, d4.w};
             float kv[EC];
-            load_ec<EC>(sm.k + jl * DP + ec, kv);
+            load_ec<D, EC>(sm.k + jl * DP, eg, kv);
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -663,11 +671,14 @@ lla_bwd_dq_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
         const int il = qc + c, i = i0 + il;
         if (i < n) {
             const RowRec& R = sm.rec[il];
-            const T* kjm = k + hoff + (size_t)R.jm * D + ec;
+            const T* kjm = k + hoff + (size_t)R.jm * D;
             float o[EC];
 #pragma unroll
-            for (int e = 0; e < EC; ++e) o[e] = fmaf(tau, dqa[c][e] - R.sd * ld_f(kjm + e), sm.y[il * DP + ec + e]);
-            store_ec<EC>(dq + hoff + (size_t)i * D + ec, o);
+            for (int e = 0; e < EC; ++e) {
+                const int col = ec_col<D, EC>(eg, e);
+                o[e] = fmaf(tau, dqa[c][e] - R.sd * ld_f(kjm + col), sm.y[il * DP + col]);
+            }
+            store_ec<D, EC>(dq + hoff + (size_t)i * D, eg, o);
         }
     }
 }
