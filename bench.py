@@ -141,12 +141,22 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
-def kernel_source_hash():
+# the sources each captured kernel is compiled from (its traffic figure is void once any changes)
+KERNEL_SOURCES = {
+    "lla_tc_kernel": ("lla_tensor.cu", "tc_ptx.cuh", "tc_host.h", "lla_internal.h"),
+    "lla_tc_kernel_bwd": ("lla_tensor.cu", "tc_ptx.cuh", "tc_host.h", "lla_internal.h"),
+    "lla_simt_kernel": ("lla_simt.cu", "lla_internal.h"),
+    "lla_decode_kernel": ("lla_decode.cu", "lla_internal.h"),
+    "lla_bwd_stats_kernel": ("lla_backward.cu", "lla_internal.h"),
+    "lla_bwd_dq_key_kernels": ("lla_backward.cu", "lla_internal.h"),
+}
+
+
+def kernel_source_hash(kernel):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "local_linear_attention_flashlla_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".h", ".cuh")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in KERNEL_SOURCES[kernel]:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -158,7 +168,7 @@ def load_traffic(kernel, workload_name):
     except (OSError, ValueError):
         return None
     ent = doc.get(f"{kernel}:{workload_name}")
-    if not ent or ent.get("source_hash") != kernel_source_hash():
+    if not ent or kernel not in KERNEL_SOURCES or ent.get("source_hash") != kernel_source_hash(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 

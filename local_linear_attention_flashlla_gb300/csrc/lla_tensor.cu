@@ -527,7 +527,8 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     const int sk = fk % NSLOT;
                     const uint32_t b = g & 1;
                     // S buffer b was last used by block g - 2: its coefficients must have been read.  Waited
-                    // before the slot: it also means every fill before this block's K landed, so the slot's
+                    // before the slot: block g - 2's Y product has then consumed every fill before this
+                    // block's K (in a two-load sweep the slot's previous fill is block g - 2's V), so the
                     // parity wait below cannot be answered by an older phase of the same slot.
                     if (g >= 2 && !(ok = WAIT(&s.m_free[b], ((g - 2) >> 1) & 1, err))) break;
                     if (!(ok = WAIT(&s.slot_full[sk], (fk / NSLOT) & 1, err))) break;
@@ -585,8 +586,12 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 for (int kb = 0; kb < nkb; ++kb, ++g) {
                     const uint32_t fk = fill++;
                     const uint32_t fv = two ? fill++ : 0;
+                    // the output sweep's T reads only K: its V fills are waited one block late (the
+                    // order still holds: V(kb-1) precedes K(kb+1) in the slot that both use), so T
+                    // never waits for a V load
+                    if (type == SW_OUT && kb > 0 && !(ok = WAIT(&s.slot_full[(fk - 1) % NSLOT], ((fk - 1) / NSLOT) & 1, err))) break;
                     if (!(ok = WAIT(&s.slot_full[fk % NSLOT], (fk / NSLOT) & 1, err))) break;
-                    if (two && !(ok = WAIT(&s.slot_full[fv % NSLOT], (fv / NSLOT) & 1, err))) break;
+                    if (hprod && !(ok = WAIT(&s.slot_full[fv % NSLOT], (fv / NSLOT) & 1, err))) break;
                     // A' is single-buffered: the elementwise threads release it as soon as they
                     // have copied the previous block's A' into registers
                     if (ga >= 1 && !(ok = WAIT(&s.a_free, (ga - 1) & 1, err))) break;
