@@ -87,9 +87,33 @@ size_t backward_workspace_bytes(int path, int B, int H, int n, int d);
 // Whole backward on the given path (LLA_PATH_FP32 or LLA_PATH_TENSOR).
 cudaError_t launch_backward(const BackwardProblem& p, int path, void* workspace, cudaStream_t stream,
                             const char** why);
-// The dq and key-major stages (fp32 CUDA cores) from the records and y.
-cudaError_t launch_backward_rest(const BackwardProblem& p, const BwdRowRec* rec, const float* yvec,
-                                 cudaStream_t stream);
+// The fp16 operand copies the tensor stats stage leaves in its workspace, and their scales
+// (float bits of max |q|, |k|, |v|, |dout|; each copy is x 2^(14 - ceil log2 max)).
+struct TensorOperands {
+    const unsigned* maxabs;
+    const void* q16;
+    const void* k16;
+    const void* v16;
+    const void* g16;
+};
+TensorOperands tensor_backward_operands(void* ws, int B, int H, int n, int d);
+// The dk/dv stage on tcgen05 (lla_bwd_tc.cu): scratch bytes, and the launch.  kmax (per key, the
+// largest dk and dv coefficient in scaled units, float bits) is written by the fp32 dq kernel.
+size_t tensor_kv_bytes(int B, int H, int n, int d);
+struct KvScratch {
+    unsigned* hdr;        // float bits of max |rho'|, max |y|; an abort word
+    void *rh, *rl, *yh, *yl;
+    unsigned* kmax;       // [B*H*n][2]
+};
+KvScratch tensor_kv_scratch(void* ws, int B, int H, int n, int d);
+cudaError_t launch_tensor_kv_prep(const BackwardProblem& p, const BwdRowRec* rec, const float* yvec,
+                                  const KvScratch& kv, cudaStream_t stream);
+cudaError_t launch_tensor_kv(const BackwardProblem& p, const BwdRowRec* rec, const TensorOperands& ops,
+                             const KvScratch& kv, cudaStream_t stream, const char** why);
+// The dq stage (fp32); with kmax non-null it also records the per-key coefficient maxima.
+cudaError_t launch_backward_dq(const BackwardProblem& p, const BwdRowRec* rec, const float* yvec,
+                               const unsigned* maxabs, const unsigned* ry_hdr, unsigned* kmax, cudaStream_t stream);
+
 // The stats stage (max, moments, adjoint CG) on the tensor path; writes rec and yvec.
 size_t tensor_backward_stats_bytes(int B, int H, int n, int d);
 cudaError_t launch_tensor_backward_stats(const BackwardProblem& p, void* ws, BwdRowRec* rec, float* yvec,

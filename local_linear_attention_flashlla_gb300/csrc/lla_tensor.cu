@@ -1392,6 +1392,19 @@ cudaError_t launch_tensor(const Problem& p, void* ws, cudaStream_t stream, const
     return cudaErrorInvalidValue;
 }
 
+TensorOperands tensor_backward_operands(void* ws, int B, int H, int n, int d) {
+    const size_t N = (size_t)B * H * n * d;
+    const size_t NT = (size_t)B * H * ((n + BQ - 1) / BQ) * BQ * d;
+    const TcWs w = carve(ws, N, NT, true);
+    TensorOperands o;
+    o.maxabs = w.hdr->maxabs;
+    o.q16 = w.q16;
+    o.k16 = w.k16;
+    o.v16 = w.v16;
+    o.g16 = w.g16;
+    return o;
+}
+
 size_t tensor_backward_stats_bytes(int B, int H, int n, int d) {
     return tensor_workspace_bytes(B, H, n, d) + align256((size_t)B * H * n * d * 2);
 }

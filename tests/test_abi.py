@@ -161,11 +161,13 @@ def test_backward_workspace_size(lib):
     assert lib.lla_backward_workspace_size(0, fp32, 2, 3, 100, 64) == 19200 + 153600
     assert lib.lla_backward_workspace_size(1, fp32, 1, 1, 1, 16) == 256 + 256
     assert lib.lla_backward_workspace_size(0, fp32, 0, 1, 1, 16) == 0
-    # tensor path (bf16, d = 64 resolves to it): the records plus the forward kernel's scratch and dout in fp16
+    # tensor path (bf16, d = 64 resolves to it): the records, the forward kernel's scratch and dout in fp16,
+    # then the dk/dv stage's scratch: a 256-byte header, rho' and y as fp16 hi + lo, two words per key
     recs = 19200 + 153600
     fwd = lib.lla_workspace_size(0, lla.LLA_PATH_TENSOR, 2, 3, 100, 64)
-    g16 = ((2 * 3 * 100 * 64 * 2 + 255) // 256) * 256
-    assert lib.lla_backward_workspace_size(0, lla.LLA_PATH_AUTO, 2, 3, 100, 64) == recs + fwd + g16
+    half = ((2 * 3 * 100 * 64 * 2 + 255) // 256) * 256
+    kmax = ((2 * 3 * 100 * 8 + 255) // 256) * 256
+    assert lib.lla_backward_workspace_size(0, lla.LLA_PATH_AUTO, 2, 3, 100, 64) == recs + fwd + half + 256 + 4 * half + kmax
 
 
 def test_backward_binding_refuses_cpu_tensors():
