@@ -589,31 +589,15 @@ struct Q3Smem {
     float vT[D * KP];
     float k[KS3 * DP];             // the same keys, [key][coordinate]
     float ds[KS3 * QP];            // ds, [key][query]
-    unsigned kmx[KS3][2];          // per key of the step: largest dk / dv coefficient (float bits)
     RowRec rec[QB3];
 };
 
 // dq_i = tau (sum_j ds_ij k_j - sd_i k_jm) + y_i over the keys j <= i.
-// exponent s with x 2^s <= 2^14 (0 for x == 0): the scale rule of the tensor path's fp16 copies
-__device__ __forceinline__ int sc_exp(float m) {
-    if (!(m > 0.f)) return 0;
-    int e;
-    const float f = frexpf(m, &e);
-    const int s = 14 - (f == 0.5f ? e - 1 : e);
-    return s < -100 ? -100 : (s > 100 ? 100 : s);
-}
-__device__ __forceinline__ float p2(int e) { return __int_as_float((max(-126, min(127, e)) + 127) << 23); }
-
-// With kmax non-null (tensor path) the kernel also records, per key j, the largest coefficient of
-// the dk and dv sums in the units of the tcgen05 dk/dv stage:
-//   kmax[j][0] = max_i max(|cq| 2^-eq, |cw| 2^-ey, |cr| 2^-er),  kmax[j][1] = max_i |cw| 2^-eg
-// (eq, eg: the q and dout copies' scales from maxabs; er, ey: the rho' and y copies' from ry).
 template <int D, typename T>
 __global__ void __launch_bounds__(NT, 1)
 lla_bwd_dq_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
                   const T* __restrict__ dout, const float* __restrict__ rho, const RowRec* __restrict__ rec,
-                  const float* __restrict__ uvec, float* __restrict__ dq, int n, int n_tiles, float tau,
-                  const unsigned* __restrict__ maxabs, const unsigned* __restrict__ ry, unsigned* __restrict__ kmax) {
+                  const float* __restrict__ uvec, float* __restrict__ dq, int n, int n_tiles, float tau) {
     using S = Q3Smem<D>;
     constexpr int KP = S::KP, DP = S::DP, QP = S::QP;
     extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -642,17 +626,9 @@ lla_bwd_dq_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
     for (int c = 0; c < 4; ++c)
 #pragma unroll
         for (int e = 0; e < EC; ++e) dqa[c][e] = 0.f;
-    float geq = 0.f, gey = 0.f, ger = 0.f, geg = 0.f;
-    if (kmax) {
-        geq = p2(-sc_exp(__uint_as_float(maxabs[0])));
-        geg = p2(-sc_exp(__uint_as_float(maxabs[3])));
-        ger = p2(-sc_exp(__uint_as_float(ry[0])));
-        gey = p2(-sc_exp(__uint_as_float(ry[1])));
-    }
 
     for (int j0 = 0; j0 <= last_key; j0 += KS3) {
         __syncthreads();
-        if (kmax && tid < 2 * KS3) sm.kmx[tid >> 1][tid & 1] = 0u;
         stage_cols<D, KP>(sm.kT, k + hoff, j0, KS3, n);
         stage_cols<D, KP>(sm.vT, v + hoff, j0, KS3, n);
         stage_rows<D, DP>(sm.k, k + hoff, j0, KS3, n);
@@ -662,7 +638,6 @@ lla_bwd_dq_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
             const int ql = 2 * qg;
             pair_dots<D, DP, KP>(sm.q + ql * DP, sm.r + ql * DP, sm.y + ql * DP, sm.g + ql * DP, sm.kT + 4 * kg,
                                  sm.vT + 4 * kg, s_, a1, a2, h);
-            float mk[4] = {0.f, 0.f, 0.f, 0.f}, mv[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int w = 0; w < 2; ++w) {
                 const RowRec& R = sm.rec[ql + w];
@@ -674,27 +649,11 @@ lla_bwd_dq_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
                     const float wb = valid ? expf(tau * s_[w][c] - R.m) * R.inv_omega : 0.f;
                     const float Ah = 1.f - (a1[w][c] - R.kb_rp);
                     const float Bh = (h[w][c] - R.hbar) - (a2[w][c] - R.kb_y);
-                    const float ds = wb * Ah * Bh;
-                    sm.ds[(4 * kg + c) * QP + ql + w] = ds;
-                    if (kmax) {
-                        const float cq = tau * (ds - (valid && j == R.jm ? R.sd : 0.f));
-                        const float cw = wb * Ah, cr = -wb * Bh;
-                        mk[c] = fmaxf(mk[c], fmaxf(fabsf(cq) * geq, fmaxf(fabsf(cw) * gey, fabsf(cr) * ger)));
-                        mv[c] = fmaxf(mv[c], fabsf(cw) * geg);
-                    }
-                }
-            }
-            if (kmax) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    atomicMax(&sm.kmx[4 * kg + c][0], __float_as_uint(mk[c]));
-                    atomicMax(&sm.kmx[4 * kg + c][1], __float_as_uint(mv[c]));
+                    sm.ds[(4 * kg + c) * QP + ql + w] = wb * Ah * Bh;
                 }
             }
         }
         __syncthreads();
-        if (kmax && tid < 2 * KS3 && j0 + (tid >> 1) < n)
-            atomicMax(kmax + ((head * (size_t)n + j0 + (tid >> 1)) * 2 + (tid & 1)), sm.kmx[tid >> 1][tid & 1]);
 #pragma unroll 2
         for (int jl = 0; jl < KS3; ++jl) {
             const float4 d4 = ld4(sm.ds + jl * QP + qc);
@@ -744,8 +703,7 @@ cudaError_t launch_stats_typed(const BackwardProblem& p, RowRec* rec, float* uve
 }
 
 template <int D, typename T>
-cudaError_t launch_dq_typed(const BackwardProblem& p, const RowRec* rec, const float* uvec, const unsigned* maxabs,
-                            const unsigned* ry, unsigned* kmax, cudaStream_t stream) {
+cudaError_t launch_dq_typed(const BackwardProblem& p, const RowRec* rec, const float* uvec, cudaStream_t stream) {
     auto kd = lla_bwd_dq_kernel<D, T>;
     const size_t smd = sizeof(Q3Smem<D>);
     cudaError_t err = cudaFuncSetAttribute(kd, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smd);
@@ -753,7 +711,7 @@ cudaError_t launch_dq_typed(const BackwardProblem& p, const RowRec* rec, const f
     const int dq_tiles = (p.n + QB3 - 1) / QB3;
     kd<<<dim3(dq_tiles, p.B * p.H), NT, smd, stream>>>(static_cast<const T*>(p.q), static_cast<const T*>(p.k),
                                                        static_cast<const T*>(p.v), static_cast<const T*>(p.dout),
-                                                       p.rho, rec, uvec, p.dq, p.n, dq_tiles, p.tau, maxabs, ry, kmax);
+                                                       p.rho, rec, uvec, p.dq, p.n, dq_tiles, p.tau);
     return cudaGetLastError();
 }
 
@@ -781,13 +739,12 @@ cudaError_t stats_dim(const BackwardProblem& p, RowRec* rec, float* uvec, cudaSt
 }
 
 template <typename T>
-cudaError_t dq_dim(const BackwardProblem& p, const RowRec* rec, const float* uvec, const unsigned* maxabs,
-                   const unsigned* ry, unsigned* kmax, cudaStream_t stream) {
+cudaError_t dq_dim(const BackwardProblem& p, const RowRec* rec, const float* uvec, cudaStream_t stream) {
     switch (p.d) {
-        case 16: return launch_dq_typed<16, T>(p, rec, uvec, maxabs, ry, kmax, stream);
-        case 32: return launch_dq_typed<32, T>(p, rec, uvec, maxabs, ry, kmax, stream);
-        case 64: return launch_dq_typed<64, T>(p, rec, uvec, maxabs, ry, kmax, stream);
-        case 128: return launch_dq_typed<128, T>(p, rec, uvec, maxabs, ry, kmax, stream);
+        case 16: return launch_dq_typed<16, T>(p, rec, uvec, stream);
+        case 32: return launch_dq_typed<32, T>(p, rec, uvec, stream);
+        case 64: return launch_dq_typed<64, T>(p, rec, uvec, stream);
+        case 128: return launch_dq_typed<128, T>(p, rec, uvec, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -815,12 +772,6 @@ size_t backward_workspace_bytes(int path, int B, int H, int n, int d) {
     return path == 1 ? recs + tensor_backward_stats_bytes(B, H, n, d) + tensor_kv_bytes(B, H, n, d) : recs;
 }
 
-cudaError_t launch_backward_dq(const BackwardProblem& p, const BwdRowRec* rec, const float* yvec,
-                               const unsigned* maxabs, const unsigned* ry_hdr, unsigned* kmax, cudaStream_t stream) {
-    if (p.dtype == 1) return dq_dim<float>(p, rec, yvec, maxabs, ry_hdr, kmax, stream);
-    return dq_dim<__nv_bfloat16>(p, rec, yvec, maxabs, ry_hdr, kmax, stream);
-}
-
 cudaError_t launch_backward(const BackwardProblem& p, int path, void* workspace, cudaStream_t stream,
                             const char** why) {
     const size_t rows = (size_t)p.B * p.H * p.n;
@@ -828,22 +779,20 @@ cudaError_t launch_backward(const BackwardProblem& p, int path, void* workspace,
     float* yvec = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * sizeof(RowRec)));
     cudaError_t err;
     if (path == 1) {
-        // stats on tcgen05, dq on CUDA cores (recording the per-key coefficient maxima), dk/dv on tcgen05
+        // stats, dq (recording the per-key coefficient maxima) and dk/dv on tcgen05
         char* tws = static_cast<char*>(workspace) + backward_records_bytes(p.B, p.H, p.n, p.d);
         err = launch_tensor_backward_stats(p, tws, rec, yvec, stream, why);
         if (err != cudaSuccess) return err;
         const TensorOperands ops = tensor_backward_operands(tws, p.B, p.H, p.n, p.d);
         const KvScratch kv = tensor_kv_scratch(tws + tensor_backward_stats_bytes(p.B, p.H, p.n, p.d), p.B, p.H, p.n, p.d);
         if ((err = launch_tensor_kv_prep(p, rec, yvec, kv, stream)) != cudaSuccess) { *why = "dk/dv prep"; return err; }
-        if ((err = launch_backward_dq(p, rec, yvec, ops.maxabs, kv.hdr, kv.kmax, stream)) != cudaSuccess) {
-            *why = "backward dq launch";
-            return err;
-        }
+        if ((err = launch_tensor_dq(p, rec, yvec, ops, kv, stream, why)) != cudaSuccess) return err;
         return launch_tensor_kv(p, rec, ops, kv, stream, why);
     }
     err = p.dtype == 1 ? stats_dim<float>(p, rec, yvec, stream) : stats_dim<__nv_bfloat16>(p, rec, yvec, stream);
     if (err != cudaSuccess) { *why = "fp32 backward stats launch"; return err; }
-    if ((err = launch_backward_dq(p, rec, yvec, nullptr, nullptr, nullptr, stream)) != cudaSuccess) {
+    if ((err = p.dtype == 1 ? dq_dim<float>(p, rec, yvec, stream) : dq_dim<__nv_bfloat16>(p, rec, yvec, stream)) !=
+        cudaSuccess) {
         *why = "backward dq launch";
         return err;
     }

@@ -1,4 +1,4 @@
-// tcgen05 dk/dv stage of the LLA backward pass (tensor path, bf16 inputs, d in {64, 128}).
+// tcgen05 dq and dk/dv stages of the LLA backward pass (tensor path, bf16 inputs, d in {64, 128}).
 //
 // For a block of 128 keys j (one CTA, MMA M = 128) and every step of 32 queries i >= j (MMA N / K =
 // 32), the per-pair quantities of the backward (Local Linear Attention reading notes, section
@@ -12,7 +12,7 @@
 // q, k, v and dout are the stats stage's fp16 copies (exact for bf16 inputs, per-tensor power-of
 // -two scales); rho' = rho omega/denom and y are split into fp16 hi + lo pairs (about 22 bits) at
 // per-tensor scales by the prep kernels here.  Each key row's coefficients are scaled by a power
-// of two fixed from that row's largest coefficient, which the fp32 dq kernel records while it
+// of two fixed from that row's largest coefficient, which the dq kernel (below) records while it
 // forms the same coefficients; the row's sums are unscaled once.  With hi + lo coefficients and
 // operands every product keeps about 22 bits, so the stage is as accurate as fp32 arithmetic.
 //
@@ -369,6 +369,315 @@ lla_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
 #undef WAIT
 }
 
+// ---- the dq kernel ----------------------------------------------------------------------------------
+// For a tile of 128 queries (M = 128) and every step of 32 keys j up to the tile's last query, the
+// same four products with the roles of the two sides exchanged (S = Q K^T, A1 = R' K^T, A2 = Y K^T,
+// H = G V^T, the query-side tiles resident), the coefficient ds of every pair, and
+// dq_i += sum_j ds_ij k_j by a TS product into one of two TMEM partial-sum buffers.  A row's
+// coefficients of one step share a power-of-two scale fixed from their maximum; the elementwise
+// warps read each step's partial sums back, unscale them and add them in registers.  The kernel
+// also records, per key, the largest coefficient of the dk and dv sums (kmax, scaled units of the
+// dk/dv kernel).  At the end dq_i = tau (sum - sd_i k_jm) + y_i.
+template <int D>
+struct DqSmem {
+    static constexpr int RT = KB * D * 2;     // [128 x D] fp16 resident tile
+    static constexpr int ST = QS * D * 2;     // [32 x D] fp16 key-step tile
+    unsigned char res[NTILE][RT];             // q, g, rh, rl, yh, yl of the query tile
+    unsigned char st[2][2][ST];               // two stages of k, v
+    uint64_t res_full, st_full[2], st_empty[2], prod_full[2], coef_ready[2], acc_free[2], sum_full[2], dq_free[2];
+    unsigned kmx[2][QS][2];                   // per key of a step: largest dk / dv coefficient (float bits)
+    float xch[2][2][KB];                      // row maxima of the two halves (two steps in turn)
+    uint32_t tmem_base;
+    int err;
+};
+static_assert(sizeof(DqSmem<128>) <= 232448, "shared memory layout too large");
+
+struct DqParams {
+    const BwdRowRec* rec;
+    const __nv_bfloat16* k;    // the bf16 keys (dq's path through the row maximum)
+    const float* y;            // [B*H*n][D]
+    float* dq;
+    unsigned* kmax;
+    const unsigned* maxabs;
+    const unsigned* ry;
+    unsigned* dev_err;
+    int n, n_tiles;
+    float tau;
+};
+
+template <int D>
+__global__ void __launch_bounds__(NTH, 1)
+lla_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_g,
+                     const __grid_constant__ CUtensorMap tm_rh, const __grid_constant__ CUtensorMap tm_rl,
+                     const __grid_constant__ CUtensorMap tm_yh, const __grid_constant__ CUtensorMap tm_yl,
+                     const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const DqParams prm) {
+    using S = DqSmem<D>;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    if (smem_u32(smem_raw) & 1023u) {
+        if (threadIdx.x == 0) atomicOr(prm.dev_err, (unsigned)kDevErrSmemAlign);
+        return;
+    }
+    S& s = *reinterpret_cast<S*>(smem_raw);
+    volatile int* err = &s.err;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(const_cast<unsigned*>(prm.ry) + 2);
+#define WAIT(bar, par) mbar_wait_abortable(bar, par, err, abort_flag)
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int n = prm.n;
+    const int i0 = (prm.n_tiles - 1 - (int)blockIdx.x) * KB;   // longest causal ranges first
+    const int head = blockIdx.y;
+    const int last = min(n - 1, i0 + KB - 1);
+    const int nst = last / QS + 1;                              // key steps j0 = QS t
+
+    if (tid == 0) {
+        s.err = *abort_flag ? 1 : 0;
+        mbar_init(&s.res_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s.st_full[i], 1);
+            mbar_init(&s.st_empty[i], 1);
+            mbar_init(&s.prod_full[i], 1);
+            mbar_init(&s.coef_ready[i], NEW / 32);
+            mbar_init(&s.acc_free[i], 1);
+            mbar_init(&s.sum_full[i], 1);
+            mbar_init(&s.dq_free[i], NEW / 32);
+        }
+        mbar_fence_init();
+    }
+    if (tid < 2 * QS * 2) (&s.kmx[0][0][0])[tid] = 0u;
+    if (warp == 9) {
+        tmem_alloc(&s.tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tP = s.tmem_base, tQ = s.tmem_base + 256;   // two product buffers, two dq buffers
+
+    if (warp == 8) {
+        // ================================ TMA producer ================================
+        if (lane == 0) {
+            const CUtensorMap* maps[NTILE] = {&tm_q, &tm_g, &tm_rh, &tm_rl, &tm_yh, &tm_yl};
+            mbar_arrive_expect_tx(&s.res_full, NTILE * S::RT);
+            for (int m = 0; m < NTILE; ++m)
+                for (int bx = 0; bx < D / 64; ++bx) tma_load_3d(s.res[m] + bx * KB * 128, maps[m], &s.res_full, bx * 64, i0, head);
+            for (int t = 0; t < nst && !*err; ++t) {
+                const int st = t & 1, f = t >> 1;
+                if (f >= 1 && !WAIT(&s.st_empty[st], (f - 1) & 1)) break;
+                mbar_arrive_expect_tx(&s.st_full[st], 2 * S::ST);
+                for (int bx = 0; bx < D / 64; ++bx) {
+                    tma_load_3d(s.st[st][0] + bx * QS * 128, &tm_k, &s.st_full[st], bx * 64, QS * t, head);
+                    tma_load_3d(s.st[st][1] + bx * QS * 128, &tm_v, &s.st_full[st], bx * 64, QS * t, head);
+                }
+            }
+            for (int t = nst > 2 ? nst - 2 : 0; t < nst; ++t) drain(&s.st_full[t & 1], (t >> 1) & 1);
+            drain(&s.res_full, 0);
+        }
+    } else if (warp == 9) {
+        // ================================= MMA issuer =================================
+        if (lane == 0) {
+            const uint32_t qa = smem_u32(s.res[0]), ga = smem_u32(s.res[1]);
+            const uint32_t rha = smem_u32(s.res[2]), rla = smem_u32(s.res[3]);
+            const uint32_t yha = smem_u32(s.res[4]), yla = smem_u32(s.res[5]);
+            bool ok = WAIT(&s.res_full, 0);
+            for (int t = 0; t <= nst && ok; ++t) {
+                if (t < nst) {   // products of key step t into buffer t & 1
+                    const int st = t & 1, pb = t & 1;
+                    if (!(ok = WAIT(&s.st_full[st], (t >> 1) & 1))) break;
+                    if (t >= 2 && !(ok = WAIT(&s.acc_free[pb], ((t - 2) >> 1) & 1))) break;
+                    tc_fence_after();
+                    const uint32_t base = tP + pb * 128, ka = smem_u32(s.st[st][0]), va = smem_u32(s.st[st][1]);
+                    gemm_prod<D>(base, qa, ka, false);          // S = Q K^T
+                    gemm_prod<D>(base + 32, rha, ka, false);    // A1 = R' K^T
+                    gemm_prod<D>(base + 32, rla, ka, true);
+                    gemm_prod<D>(base + 64, yha, ka, false);    // A2 = Y K^T
+                    gemm_prod<D>(base + 64, yla, ka, true);
+                    gemm_prod<D>(base + 96, ga, va, false);     // H = G V^T
+                    umma_commit(&s.prod_full[pb]);
+                }
+                if (t >= 1) {    // partial dq of step t - 1
+                    const int u = t - 1, st = u & 1, pb = u & 1;
+                    if (!(ok = WAIT(&s.coef_ready[pb], (u >> 1) & 1))) break;
+                    if (u >= 2 && !(ok = WAIT(&s.dq_free[pb], ((u - 2) >> 1) & 1))) break;
+                    tc_fence_after();
+                    gemm_sum<D>(tQ + pb * D, tP + pb * 128, smem_u32(s.st[st][0]), false);   // ds K
+                    umma_commit(&s.sum_full[pb]);
+                    umma_commit(&s.st_empty[st]);
+                    umma_commit(&s.acc_free[pb]);
+                }
+            }
+            for (int u = nst > 2 ? nst - 2 : 0; u < nst; ++u) drain(&s.sum_full[u & 1], (u >> 1) & 1);
+        }
+    } else {
+        // ============================ elementwise warps ============================
+        const int quad = warp & 3, half = warp >> 2;
+        const int row = quad * 32 + lane;
+        const int i = i0 + row;
+        const bool row_ok = i < n;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        const int eq = sc_exp(__uint_as_float(prm.maxabs[0])), ek = sc_exp(__uint_as_float(prm.maxabs[1]));
+        const int ev = sc_exp(__uint_as_float(prm.maxabs[2])), eg = sc_exp(__uint_as_float(prm.maxabs[3]));
+        const int er = sc_exp(__uint_as_float(prm.ry[0])), ey = sc_exp(__uint_as_float(prm.ry[1]));
+        const float tau = prm.tau;
+        const float fs = tau * pow2i(-(eq + ek)), f1 = pow2i(-(ek + er)), f2 = pow2i(-(ek + ey)), fh = pow2i(-(ev + eg));
+        const float gq = pow2i(-eq), gy = pow2i(-ey), gr = pow2i(-er), gvv = pow2i(-eg), gk = pow2i(-ek);
+        BwdRowRec R{};
+        if (row_ok) R = prm.rec[(size_t)head * n + i];
+        float acc[D / 2];
+#pragma unroll
+        for (int e = 0; e < D / 2; ++e) acc[e] = 0.f;
+        float usc[2] = {1.f, 1.f};     // the unscale factors of the two partial-sum buffers
+        bool ok = true;
+        for (int t = 0; t <= nst; ++t) {
+            if (t < nst) {
+                const int pb = t & 1;
+                ok = ok && WAIT(&s.prod_full[pb], (t >> 1) & 1);
+                tc_fence_after();
+                const uint32_t base = tP + pb * 128 + lane_off + 16 * half;
+                float sv[16], a1[16], a2[16], hv[16];
+                tmem_ld16(base, sv);
+                tmem_ld16(base + 32, a1);
+                tmem_ld16(base + 64, a2);
+                tmem_ld16(base + 96, hv);
+                tmem_ld_wait();
+                const int jb = QS * t + 16 * half;
+                float dsv[16];
+                float mx = 0.f;
+#pragma unroll
+                for (int jj = 0; jj < 16; ++jj) {
+                    const int j = jb + jj;
+                    const bool valid = row_ok && j <= i;
+                    float ds = 0.f, mk = 0.f, mv = 0.f;
+                    if (valid) {
+                        const float wb = expf(fmaf(sv[jj], fs, -R.m)) * R.inv_omega;
+                        const float Ah = 1.f - fmaf(a1[jj], f1, -R.kb_rp);
+                        const float Bh = fmaf(hv[jj], fh, -R.hbar) - fmaf(a2[jj], f2, -R.kb_y);
+                        ds = wb * Ah * Bh;
+                        const float cq = tau * (ds - (j == R.jm ? R.sd : 0.f));
+                        const float cw = wb * Ah, cr = -wb * Bh;
+                        mk = fmaxf(fabsf(cq) * gq, fmaxf(fabsf(cw) * gy, fabsf(cr) * gr));
+                        mv = fabsf(cw) * gvv;
+                    }
+                    dsv[jj] = ds * gk;             // the k copy's scale folded in
+                    mx = fmaxf(mx, fabsf(dsv[jj]));
+                    // largest coefficient of key j over the warp's 32 query rows
+#pragma unroll
+                    for (int o = 16; o; o >>= 1) {
+                        mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, o));
+                        mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, o));
+                    }
+                    if (lane == 0 && (mk > 0.f || mv > 0.f)) {
+                        atomicMax(&s.kmx[t & 1][16 * half + jj][0], __float_as_uint(mk));
+                        atomicMax(&s.kmx[t & 1][16 * half + jj][1], __float_as_uint(mv));
+                    }
+                }
+                // the row's scale for this step: both halves' maxima
+                // (buffer t & 1: a thread rewrites it at step t + 2, after the next barrier, which its
+                // partner reaches only after reading this step's value)
+                s.xch[t & 1][half][row] = mx;
+                named_bar_sync(1, NEW);
+                const float rmx = fmaxf(mx, s.xch[t & 1][1 - half][row]);
+                const int sq = sc_exp(rmx * 1.01f);
+                const float up = pow2i(sq);
+                usc[pb] = pow2i(-sq);
+                uint32_t pk[16];
+#pragma unroll
+                for (int jj = 0; jj < 16; jj += 2) {
+                    const float x0 = dsv[jj] * up, x1 = dsv[jj + 1] * up;
+                    pk[jj >> 1] = pack_half2(x0, x1);
+                    const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&pk[jj >> 1]));
+                    pk[8 + (jj >> 1)] = pack_half2(x0 - h.x, x1 - h.y);
+                }
+                tmem_st16(base, pk);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.coef_ready[pb]);
+                // every warp's key maxima of this step are in: push them (two threads per key)
+                if (tid < 2 * QS) {
+                    const int j = QS * t + (tid >> 1);
+                    unsigned* slot = &s.kmx[t & 1][tid >> 1][tid & 1];
+                    if (j < n && *slot) atomicMax(prm.kmax + ((size_t)head * n + j) * 2 + (tid & 1), *slot);
+                    *slot = 0u;
+                }
+            }
+            if (t >= 1) {    // add step t - 1's partial sums
+                const int u = t - 1, pb = u & 1;
+                ok = ok && WAIT(&s.sum_full[pb], (u >> 1) & 1);
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < D / 2; c += 32) {
+                    float v[32];
+                    tmem_ld32(tQ + pb * D + lane_off + half * (D / 2) + c, v);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) acc[c + e] = fmaf(v[e], usc[pb], acc[c + e]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s.dq_free[pb]);
+            }
+        }
+        if (row_ok && ok) {
+            const size_t rb = ((size_t)head * n + i) * D + half * (D / 2);
+            const __nv_bfloat16* kjm = prm.k + ((size_t)head * n + R.jm) * D + half * (D / 2);
+#pragma unroll
+            for (int e = 0; e < D / 2; e += 4) {
+                float o[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    o[u] = fmaf(tau, acc[e + u] - R.sd * __bfloat162float(kjm[e + u]), __ldg(prm.y + rb + e + u));
+                *reinterpret_cast<float4*>(prm.dq + rb + e) = make_float4(o[0], o[1], o[2], o[3]);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 9) {
+        __syncwarp();
+        tmem_dealloc(s.tmem_base, 512);
+    }
+    if (tid == 0 && s.err) atomicOr(prm.dev_err, (unsigned)kDevErrMbarTimeout);
+#undef WAIT
+}
+
+template <int D>
+cudaError_t launch_dq_d(const BackwardProblem& p, const BwdRowRec* rec, const float* yvec, const TensorOperands& ops,
+                        const KvScratch& kv, cudaStream_t stream, const char** why) {
+    const uint64_t slices = (uint64_t)p.B * p.H;
+    CUtensorMap tq, tg, trh, trl, tyh, tyl, tk, tv;
+    if (!make_tmap_f16_3d(&tq, ops.q16, D, p.n, slices, KB) || !make_tmap_f16_3d(&tg, ops.g16, D, p.n, slices, KB) ||
+        !make_tmap_f16_3d(&trh, kv.rh, D, p.n, slices, KB) || !make_tmap_f16_3d(&trl, kv.rl, D, p.n, slices, KB) ||
+        !make_tmap_f16_3d(&tyh, kv.yh, D, p.n, slices, KB) || !make_tmap_f16_3d(&tyl, kv.yl, D, p.n, slices, KB) ||
+        !make_tmap_f16_3d(&tk, ops.k16, D, p.n, slices, QS) || !make_tmap_f16_3d(&tv, ops.v16, D, p.n, slices, QS)) {
+        *why = "cuTensorMapEncodeTiled (dq)";
+        return cudaErrorInvalidValue;
+    }
+    DqParams prm;
+    prm.rec = rec;
+    prm.k = static_cast<const __nv_bfloat16*>(p.k);
+    prm.y = yvec;
+    prm.dq = p.dq;
+    prm.kmax = kv.kmax;
+    prm.maxabs = ops.maxabs;
+    prm.ry = kv.hdr;
+    prm.dev_err = device_error_word();
+    prm.n = p.n;
+    prm.n_tiles = (p.n + KB - 1) / KB;
+    prm.tau = p.tau;
+    if (!prm.dev_err) { *why = "device error word"; return cudaErrorInvalidSymbol; }
+    const size_t smem = sizeof(DqSmem<D>);
+    auto kern = lla_bwd_dq_tc_kernel<D>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) { *why = "dq kernel shared-memory attribute"; return e; }
+    kern<<<dim3(prm.n_tiles, (unsigned)slices), NTH, smem, stream>>>(tq, tg, trh, trl, tyh, tyl, tk, tv, prm);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) *why = "dq kernel launch";
+    return e;
+}
+
 template <int D>
 cudaError_t launch_kv_d(const BackwardProblem& p, const BwdRowRec* rec, const TensorOperands& ops,
                         const KvScratch& kv, cudaStream_t stream, const char** why) {
@@ -441,6 +750,14 @@ cudaError_t launch_tensor_kv_prep(const BackwardProblem& p, const BwdRowRec* rec
         lla_bwd_ry16_kernel<64><<<blocks, 256, 0, stream>>>(p.rho, rec, yvec, rows, kv.hdr, rh, rl, yh, yl);
     }
     return cudaGetLastError();
+}
+
+cudaError_t launch_tensor_dq(const BackwardProblem& p, const BwdRowRec* rec, const float* yvec,
+                             const TensorOperands& ops, const KvScratch& kv, cudaStream_t stream, const char** why) {
+    if (p.d == 128) return launch_dq_d<128>(p, rec, yvec, ops, kv, stream, why);
+    if (p.d == 64) return launch_dq_d<64>(p, rec, yvec, ops, kv, stream, why);
+    *why = "tensor path supports d in {64, 128}";
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_tensor_kv(const BackwardProblem& p, const BwdRowRec* rec, const TensorOperands& ops,

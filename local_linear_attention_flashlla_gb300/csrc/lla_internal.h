@@ -97,8 +97,8 @@ struct TensorOperands {
     const void* g16;
 };
 TensorOperands tensor_backward_operands(void* ws, int B, int H, int n, int d);
-// The dk/dv stage on tcgen05 (lla_bwd_tc.cu): scratch bytes, and the launch.  kmax (per key, the
-// largest dk and dv coefficient in scaled units, float bits) is written by the fp32 dq kernel.
+// The dq and dk/dv stages on tcgen05 (lla_bwd_tc.cu): scratch bytes and launches.  kmax (per key,
+// the largest dk and dv coefficient in scaled units, float bits) is written by the dq kernel.
 size_t tensor_kv_bytes(int B, int H, int n, int d);
 struct KvScratch {
     unsigned* hdr;        // float bits of max |rho'|, max |y|; an abort word
@@ -110,9 +110,9 @@ cudaError_t launch_tensor_kv_prep(const BackwardProblem& p, const BwdRowRec* rec
                                   const KvScratch& kv, cudaStream_t stream);
 cudaError_t launch_tensor_kv(const BackwardProblem& p, const BwdRowRec* rec, const TensorOperands& ops,
                              const KvScratch& kv, cudaStream_t stream, const char** why);
-// The dq stage (fp32); with kmax non-null it also records the per-key coefficient maxima.
-cudaError_t launch_backward_dq(const BackwardProblem& p, const BwdRowRec* rec, const float* yvec,
-                               const unsigned* maxabs, const unsigned* ry_hdr, unsigned* kmax, cudaStream_t stream);
+// The dq stage on tcgen05 (also records kmax for the dk/dv stage).
+cudaError_t launch_tensor_dq(const BackwardProblem& p, const BwdRowRec* rec, const float* yvec,
+                             const TensorOperands& ops, const KvScratch& kv, cudaStream_t stream, const char** why);
 
 // The stats stage (max, moments, adjoint CG) on the tensor path; writes rec and yvec.
 size_t tensor_backward_stats_bytes(int B, int H, int n, int d);
