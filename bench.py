@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 METRIC = "causal LLA fwd tokens/s & TFLOP/s at d=128 bf16; fraction of BF16 tensor peak"
 METRIC_DECODE = "LLA decode step tokens/s (one token per sequence) and HBM GB/s at d=128 bf16; fraction of HBM peak"
 METRIC_PARALLAX = "causal Parallax-form fwd (caller probe) tokens/s & TFLOP/s at d=128 bf16; fraction of BF16 tensor peak"
-METRIC_BACKWARD = "causal LLA backward (dq, dk, dv) tokens/s & TFLOP/s at d=128, bf16 inputs; fraction of fp32 ALU peak"
+METRIC_BACKWARD = "causal LLA backward (dq, dk, dv) tokens/s & TFLOP/s at d=128, bf16 inputs; fraction of BF16 tensor peak"
 
 
 def useful_flops(w, T):
@@ -67,14 +67,17 @@ def backward_useful_flops(w, T):
 
 
 def backward_executed_flops(w, T, tensor=False):
-    """As the kernels run them.  fp32 stats kernel: q.k in the max sweep, q.k, g.v and the two
-    moment sums, 3 passes per CG iteration (5 + 3T).  Tensor stats kernel: S in the max sweep;
-    S, H = G V^T and the hi + lo weight products in the moment and TBAR sweeps; S, the hi + lo
-    direction products and the hi + lo coefficient products per CG iteration (9 + 5T).  Then the
-    dq kernel (q.k, rho'.k, y.k, g.v, dq: 5) and the key-major kernel (the same four dots, dk
-    three terms, dv: 8)."""
+    """As the kernels run them, in passes of 2d flops per causal pair.  fp32 path: the stats kernel
+    (q.k in the max sweep, q.k, g.v and the two moment sums, 3 per CG iteration: 5 + 3T), the dq
+    kernel (q.k, rho'.k, y.k, g.v, dq: 5) and the key-major kernel (the same four dots, dk's three
+    terms, dv: 8).  Tensor path: the stats kernel (S in the max sweep; S, H and the hi + lo weight
+    products in the moment and TBAR sweeps; S, the hi + lo direction and coefficient products per
+    CG iteration: 9 + 5T), the dq kernel (S, H and the hi + lo rho'.k and y.k products, the hi + lo
+    ds.k sum: 8) and the dk/dv kernel (the same six products, hi + lo coefficients against q, g and
+    the hi + lo y and rho': 18)."""
+    rest = 26 if tensor else 13
     stats = (9 + 5 * T) if tensor else (5 + 3 * T)
-    return (stats + 13) * 2 * w.d * (w.n * (w.n + 1) / 2 * w.B * w.H)
+    return (stats + rest) * 2 * w.d * (w.n * (w.n + 1) / 2 * w.B * w.H)
 
 
 def load_peaks():
@@ -579,7 +582,7 @@ def run_backward(args, world, rank, local):
     flops = backward_useful_flops(w, T)
     q_ms = sum(m for m, _ in main_times) / len(main_times)          # stats kernel (moments and adjoint CG)
     call_ms = sum(t_ for _, t_ in main_times) / len(main_times)     # the whole call
-    k_ms = max(call_ms - q_ms, 1e-9)                                 # dq and key-major kernels (fp32; tensor path: + pre-pass)
+    k_ms = max(call_ms - q_ms, 1e-9)                                 # dq and dk/dv stages (tensor path: with their prep)
     pairs_flops = 2 * w.d * (w.n * (w.n + 1) / 2 * w.B * w.H)
     q_flops = (4 + 2 * T) * pairs_flops      # the stats stage's useful share: q.k, g.v, two moment sums, CG
     k_flops = 7 * pairs_flops                # the rest: rho'.k, y.k, dq; dk (three terms) and dv
@@ -596,12 +599,17 @@ def run_backward(args, world, rank, local):
                   "peak_source": stats_src,
                   "flops_counted": "stats stage, useful (4+2T) passes x 2d per causal pair"
                                    + ("; executed on tensor cores: (9+5T) passes (hi + lo operands)" if stats_tensor else "")}
-    rest_roof = {"bound": "alu", "achieved": k_flops / (k_ms / 1e3) / 1e12, "peak": alu_peak, "unit": "TFLOP/s",
-                 "frac": k_flops / (k_ms / 1e3) / 1e12 / alu_peak,
-                 "traffic": load_traffic("lla_bwd_dq_key_kernels", w.name),
-                 "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 flops x max SM clock",
-                 "flops_counted": "dq and key-major kernels, useful 7 passes x 2d per causal pair"}
+    rest_peak = peaks["bf16_tflops"] if stats_tensor else alu_peak
+    rest_roof = {"bound": "tensor" if stats_tensor else "alu", "achieved": k_flops / (k_ms / 1e3) / 1e12,
+                 "peak": rest_peak, "unit": "TFLOP/s", "frac": k_flops / (k_ms / 1e3) / 1e12 / rest_peak,
+                 "traffic": None,
+                 "peak_source": f"{peak_kind} bf16 burst" if stats_tensor else
+                 "derived: 152 SMs x 128 fp32 FMA lanes x 2 flops x max SM clock",
+                 "flops_counted": "dq and dk/dv stages, useful 7 passes x 2d per causal pair"
+                                  + ("; executed on tensor cores: 26 passes (hi + lo operands)" if stats_tensor else "")}
     stats_name = "lla_tc_kernel<128,bwd>" if stats_tensor else "lla_bwd_stats_kernel"
+    rest_name = ("lla_bwd_dq_tc_kernel + lla_bwd_kv_tc_kernel (+ prep)" if stats_tensor
+                 else "lla_bwd_dq_kernel + lla_bwd_key_kernel")
     dominant_is_stats = q_ms >= k_ms
     roof = stats_roof if dominant_is_stats else rest_roof
 
@@ -644,14 +652,13 @@ def run_backward(args, world, rank, local):
             "tflops": world * flops * args.steps / (total_ms / 1e3) / 1e12,
             "tflops_executed": world * backward_executed_flops(w, T, stats_tensor) * args.steps / (total_ms / 1e3) / 1e12,
             "roofline": roof, "clocks": clocks, "e2e": e2e,
-            "gpu_launches": (5 if stats_tensor else 3) * args.steps,
-            "dominant_kernel": {"name": stats_name if dominant_is_stats else "lla_bwd_dq_kernel + lla_bwd_key_kernel",
+            "gpu_launches": (7 if stats_tensor else 3) * args.steps,
+            "dominant_kernel": {"name": stats_name if dominant_is_stats else rest_name,
                                 "ms_per_launch": q_ms if dominant_is_stats else k_ms,
                                 "share_of_step": (q_ms if dominant_is_stats else k_ms) / ms_per_step},
             "stages": {"stats": {"kernel": stats_name, "ms": q_ms, "roofline": stats_roof},
-                       "dq_dk_dv": {"kernels": ["lla_bwd_dq_kernel", "lla_bwd_key_kernel"], "ms": k_ms,
-                                    "roofline": rest_roof}},
-            "path": "tensor stats + fp32 dq/dk/dv" if stats_tensor else "fp32",
+                       "dq_dk_dv": {"kernels": rest_name, "ms": k_ms, "roofline": rest_roof}},
+            "path": "tensor (tcgen05 stats, dq, dk/dv)" if stats_tensor else "fp32",
             "cg_iters_counted": T}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_throughput(w, qkv_host, op="backward", probe=g_host)

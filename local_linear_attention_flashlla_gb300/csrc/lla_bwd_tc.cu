@@ -99,6 +99,7 @@ struct KvSmem {
     unsigned char k[KT];
     unsigned char v[KT];
     unsigned char st[2][NTILE][QT];           // two stages of q, g, rh, rl, yh, yl
+    BwdRowRec rec[2][QS];                     // and the step's per-query records
     uint64_t kv_full, st_full[2], st_empty[2], prod_full[2], coef_ready[2], acc_free[2], acc_done;
     uint32_t tmem_base;
     int err;
@@ -144,6 +145,13 @@ __device__ __forceinline__ void gemm_sum(uint32_t d_tmem, uint32_t c_tmem, uint3
             if (part == 0 && ks == 0 && !acc) umma_ts_c<false>(d_tmem, c_tmem + 16 * ks + 8 * part, bk, ID);
             else umma_ts_c<true>(d_tmem, c_tmem + 16 * ks + 8 * part, bk, ID);
         }
+}
+
+// Plain bulk copy global -> shared (16-byte aligned, bytes a multiple of 16) on an mbarrier.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
 }
 
 __device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity) {
@@ -210,10 +218,13 @@ lla_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             for (int t = 0; t < nst && !*err; ++t) {
                 const int st = t & 1, f = t >> 1;
                 if (f >= 1 && !WAIT(&s.st_empty[st], (f - 1) & 1)) break;
-                mbar_arrive_expect_tx(&s.st_full[st], NTILE * S::QT);
+                const int i0 = j0 + QS * t;
+                const uint32_t rbytes = (uint32_t)(min(QS, n - i0) * sizeof(BwdRowRec));   // rows past n: not read
+                mbar_arrive_expect_tx(&s.st_full[st], NTILE * S::QT + rbytes);
                 for (int m = 0; m < NTILE; ++m)
                     for (int bx = 0; bx < D / 64; ++bx)
-                        tma_load_3d(s.st[st][m] + bx * QS * 128, maps[m], &s.st_full[st], bx * 64, j0 + QS * t, head);
+                        tma_load_3d(s.st[st][m] + bx * QS * 128, maps[m], &s.st_full[st], bx * 64, i0, head);
+                bulk_load(s.rec[st], prm.rec + (size_t)head * n + i0, rbytes, &s.st_full[st]);
             }
             for (int t = nst > 2 ? nst - 2 : 0; t < nst; ++t) drain(&s.st_full[t & 1], (t >> 1) & 1);
             drain(&s.kv_full, 0);
@@ -274,7 +285,6 @@ lla_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         const float tau = prm.tau;
         const float fs = tau * pow2i(-(eq + ek)), f1 = pow2i(-(ek + er)), f2 = pow2i(-(ek + ey)), fh = pow2i(-(ev + eg));
         const float gq = pow2i(sK - eq), gy = -pow2i(sK - ey), gr = pow2i(sK - er), gv = pow2i(sV - eg);
-        const BwdRowRec* rech = prm.rec + (size_t)head * n;
         bool ok = true;
         for (int t = 0; t < nst; ++t) {
             const int pb = t & 1;
@@ -298,8 +308,8 @@ lla_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                     const bool valid = key_ok && i < n && j <= i;
                     float c_q = 0.f, c_w = 0.f, c_r = 0.f;
                     if (valid) {
-                        const float4 r0 = __ldg(reinterpret_cast<const float4*>(rech + i));
-                        const float4 r1 = __ldg(reinterpret_cast<const float4*>(rech + i) + 1);
+                        const float4* rp = reinterpret_cast<const float4*>(&s.rec[t & 1][16 * half + qq + w]);
+                        const float4 r0 = rp[0], r1 = rp[1];
                         // r0 = (m, jm, inv_omega, hbar), r1 = (kb_rp, kb_y, sd, rp_scale)
                         const float wb = expf(fmaf(sv[qq + w], fs, -r0.x)) * r0.z;
                         const float Ah = 1.f - fmaf(a1[qq + w], f1, -r1.x);
@@ -560,15 +570,13 @@ lla_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     }
                     dsv[jj] = ds * gk;             // the k copy's scale folded in
                     mx = fmaxf(mx, fabsf(dsv[jj]));
-                    // largest coefficient of key j over the warp's 32 query rows
-#pragma unroll
-                    for (int o = 16; o; o >>= 1) {
-                        mk = fmaxf(mk, __shfl_xor_sync(0xffffffffu, mk, o));
-                        mv = fmaxf(mv, __shfl_xor_sync(0xffffffffu, mv, o));
-                    }
-                    if (lane == 0 && (mk > 0.f || mv > 0.f)) {
-                        atomicMax(&s.kmx[t & 1][16 * half + jj][0], __float_as_uint(mk));
-                        atomicMax(&s.kmx[t & 1][16 * half + jj][1], __float_as_uint(mv));
+                    // largest coefficient of key j over the warp's 32 query rows (non-negative floats
+                    // order as their bit patterns)
+                    const unsigned wk = __reduce_max_sync(0xffffffffu, __float_as_uint(mk));
+                    const unsigned wv = __reduce_max_sync(0xffffffffu, __float_as_uint(mv));
+                    if (lane == 0 && (wk | wv)) {
+                        atomicMax(&s.kmx[t & 1][16 * half + jj][0], wk);
+                        atomicMax(&s.kmx[t & 1][16 * half + jj][1], wv);
                     }
                 }
                 // the row's scale for this step: both halves' maxima
