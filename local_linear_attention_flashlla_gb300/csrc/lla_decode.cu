@@ -81,6 +81,58 @@ __device__ __forceinline__ void load_seg(const __nv_bfloat16* p, float (&o)[E]) 
     }
 }
 
+// E consecutive elements of a row as raw bits.  The streaming passes fetch several rows into
+// these before using any of them, so each thread keeps that many loads in flight: with one row
+// at a time, two CTAs per SM hold too few bytes in flight to cover the HBM latency.
+template <int E, typename T>
+struct RawSeg {
+    static constexpr int W = E * (int)sizeof(T) / 4;   // 32-bit words: 1 .. 16
+    uint32_t w[W];
+};
+
+// Rows fetched ahead per pass: about 128 bytes per thread, at most 8 rows.
+template <int E, typename T>
+__host__ __device__ constexpr int rows_ahead() {
+    return E * (int)sizeof(T) >= 128 ? 1 : (128 / (E * (int)sizeof(T)) > 8 ? 8 : 128 / (E * (int)sizeof(T)));
+}
+
+// Load the segment at p (aligned to its size rounded down to a power of two, at most 16 bytes),
+// or zeros when !valid (p is then not read).
+template <int E, typename T>
+__device__ __forceinline__ void fetch_seg(const T* p, bool valid, RawSeg<E, T>& r) {
+    constexpr int W = RawSeg<E, T>::W;
+    const uint32_t* s = reinterpret_cast<const uint32_t*>(p);
+    if (!valid) {
+#pragma unroll
+        for (int c = 0; c < W; ++c) r.w[c] = 0u;
+    } else if constexpr (W % 4 == 0) {
+#pragma unroll
+        for (int c = 0; c < W; c += 4) {
+            const uint4 t = *reinterpret_cast<const uint4*>(s + c);
+            r.w[c] = t.x; r.w[c + 1] = t.y; r.w[c + 2] = t.z; r.w[c + 3] = t.w;
+        }
+    } else if constexpr (W == 2) {
+        const uint2 t = *reinterpret_cast<const uint2*>(s);
+        r.w[0] = t.x; r.w[1] = t.y;
+    } else {
+        r.w[0] = *s;
+    }
+}
+
+template <int E>
+__device__ __forceinline__ void unpack_seg(const RawSeg<E, float>& r, float (&o)[E]) {
+#pragma unroll
+    for (int c = 0; c < E; ++c) o[c] = __uint_as_float(r.w[c]);
+}
+template <int E>
+__device__ __forceinline__ void unpack_seg(const RawSeg<E, __nv_bfloat16>& r, float (&o)[E]) {
+#pragma unroll
+    for (int c = 0; c < E / 2; ++c) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.w[c]));
+        o[2 * c] = f.x; o[2 * c + 1] = f.y;
+    }
+}
+
 // Copy E consecutive elements (a 16-byte multiple for every E used with it).
 template <int E, typename T>
 __device__ __forceinline__ void copy_seg(T* dst, const T* src) {
@@ -136,12 +188,16 @@ __device__ __forceinline__ void reduce_parts(DecSmem<D>& sm, float* dst) {
     __syncthreads();
 }
 
+// Two CTAs per SM (at most 128 registers a thread): with the rows fetched ahead, two CTAs
+// keep enough loads in flight, and the register cap keeps the prefetched rows from spilling.
 template <int D, typename T>
-__global__ void __launch_bounds__(DT)
+__global__ void __launch_bounds__(DT, 2)
 lla_decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, T* __restrict__ out,
                   float* __restrict__ rho, float* __restrict__ denom, int* __restrict__ cg_iters, int n, int n_cap,
                   float tau, float lambda, int cg_max_iters, float cg_tol) {
     constexpr int E = D / 8;
+    constexpr int U = rows_ahead<E, T>();           // K rows in flight per thread (moments, CG)
+    constexpr int UO = U > 1 ? U / 2 : 1;           // K and V rows in flight (output)
     extern __shared__ __align__(16) unsigned char smem_raw[];
     DecSmem<D>& sm = *reinterpret_cast<DecSmem<D>*>(smem_raw);
     float* wts = reinterpret_cast<float*>(smem_raw + sizeof(DecSmem<D>));   // n weights
@@ -163,34 +219,48 @@ lla_decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
 #pragma unroll
     for (int c = 0; c < E; ++c) acc[c] = 0.f;
     // Every group runs the same number of iterations (the shuffles inside need all 32 lanes of
-    // the warp); a group whose key is past the end does no work in that iteration.
+    // the warp); a group whose key is past the end does no work in that iteration.  Group g takes
+    // the keys j = it NG + g in increasing it, U of them per step, all U fetched first.
     const int n_it = (n + NG - 1) / NG;
-    for (int it = 0; it < n_it; ++it) {
-        const int j = it * NG + g;
-        const bool valid = j < n;
-        float kv[E];
-        if (valid) load_seg<E>(kh + (size_t)j * D + c0, kv);
-        else {
+    auto key_of = [&](int it) { return it * NG + g; };
+    for (int it = 0; it < n_it; it += U) {
+        RawSeg<E, T> kr[U];
 #pragma unroll
-            for (int c = 0; c < E; ++c) kv[c] = 0.f;
+        for (int u = 0; u < U; ++u) {
+            const int j = key_of(it + u);
+            fetch_seg<E>(kh + (size_t)(j < n ? j : 0) * D + c0, j < n, kr[u]);
         }
-        float s = 0.f;
+        float s[U];
 #pragma unroll
-        for (int c = 0; c < E; ++c) s = fmaf(qv[c], kv[c], s);
-        s = tau * group_sum(s);
-        if (!valid) continue;
-        if (l8 == 0) wts[j] = s;                    // logit for now; weight after the pass
-        if (s > mg) {                               // rescale this group's sums to the new maximum
-            const float f = expf(mg - s);
-            og *= f;
+        for (int u = 0; u < U; ++u) {
+            float kv[E];
+            unpack_seg<E>(kr[u], kv);
+            float t = 0.f;
 #pragma unroll
-            for (int c = 0; c < E; ++c) acc[c] *= f;
-            mg = s;
+            for (int c = 0; c < E; ++c) t = fmaf(qv[c], kv[c], t);
+            s[u] = t;
         }
-        const float w = expf(s - mg);
-        og += w;
 #pragma unroll
-        for (int c = 0; c < E; ++c) acc[c] = fmaf(w, kv[c], acc[c]);
+        for (int u = 0; u < U; ++u) s[u] = tau * group_sum(s[u]);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = key_of(it + u);
+            if (j >= n) continue;
+            if (l8 == 0) wts[j] = s[u];             // logit for now; weight after the pass
+            if (s[u] > mg) {                        // rescale this group's sums to the new maximum
+                const float f = expf(mg - s[u]);
+                og *= f;
+#pragma unroll
+                for (int c = 0; c < E; ++c) acc[c] *= f;
+                mg = s[u];
+            }
+            const float w = expf(s[u] - mg);
+            og += w;
+            float kv[E];
+            unpack_seg<E>(kr[u], kv);
+#pragma unroll
+            for (int c = 0; c < E; ++c) acc[c] = fmaf(w, kv[c], acc[c]);
+        }
     }
     if (l8 == 0) sm.gs[g][0] = mg;
     __syncthreads();
@@ -226,37 +296,47 @@ lla_decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
     bool active = gamma > 0.f && !(rn0 <= cg_tol * rn0);
     int iters = 0;
     const float lam_n = lambda * inv_om;
-    float kbv[E];
-#pragma unroll
-    for (int c = 0; c < E; ++c) kbv[c] = sm.kbar[c0 + c];
     for (int it = 0; it < cg_max_iters && active; ++it) {   // active is uniform over the block
         float pv[E];
 #pragma unroll
         for (int c = 0; c < E; ++c) pv[c] = sm.p[c0 + c];
         float kp = 0.f;
 #pragma unroll
-        for (int c = 0; c < E; ++c) kp = fmaf(kbv[c], pv[c], kp);
+        for (int c = 0; c < E; ++c) kp = fmaf(sm.kbar[c0 + c], pv[c], kp);
         kp = group_sum(kp);
         float ms = 0.f;
 #pragma unroll
         for (int c = 0; c < E; ++c) acc[c] = 0.f;
-        for (int it2 = 0; it2 < n_it; ++it2) {
-            const int j = it2 * NG + g;
-            const bool valid = j < n;
-            float kv[E];
-            if (valid) load_seg<E>(kh + (size_t)j * D + c0, kv);
-            else {
+        for (int it2 = 0; it2 < n_it; it2 += U) {
+            RawSeg<E, T> kr[U];
 #pragma unroll
-                for (int c = 0; c < E; ++c) kv[c] = 0.f;
+            for (int u = 0; u < U; ++u) {
+                const int j = key_of(it2 + u);
+                fetch_seg<E>(kh + (size_t)(j < n ? j : 0) * D + c0, j < n, kr[u]);
             }
-            float a = 0.f;
+            float a[U];
 #pragma unroll
-            for (int c = 0; c < E; ++c) a = fmaf(pv[c], kv[c], a);
-            a = group_sum(a);
-            const float mm = valid ? wts[j] * (a - kp) : 0.f;
-            ms += mm;
+            for (int u = 0; u < U; ++u) {
+                float kv[E];
+                unpack_seg<E>(kr[u], kv);
+                float t = 0.f;
 #pragma unroll
-            for (int c = 0; c < E; ++c) acc[c] = fmaf(mm, kv[c], acc[c]);
+                for (int c = 0; c < E; ++c) t = fmaf(pv[c], kv[c], t);
+                a[u] = t;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) a[u] = group_sum(a[u]);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int j = key_of(it2 + u);
+                if (j >= n) continue;
+                const float mm = wts[j] * (a[u] - kp);
+                ms += mm;
+                float kv[E];
+                unpack_seg<E>(kr[u], kv);
+#pragma unroll
+                for (int c = 0; c < E; ++c) acc[c] = fmaf(mm, kv[c], acc[c]);
+            }
         }
 #pragma unroll
         for (int c = 0; c < E; ++c) sm.part[g][c0 + c] = acc[c];
@@ -300,25 +380,38 @@ lla_decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
     float us = 0.f;
 #pragma unroll
     for (int c = 0; c < E; ++c) acc[c] = 0.f;
-    for (int it = 0; it < n_it; ++it) {
-        const int j = it * NG + g;
-        const bool valid = j < n;
-        float kv[E], vv[E];
-        if (valid) {
-            load_seg<E>(kh + (size_t)j * D + c0, kv);
-            load_seg<E>(vh + (size_t)j * D + c0, vv);
-        } else {
+    for (int it = 0; it < n_it; it += UO) {
+        RawSeg<E, T> kr[UO], vr[UO];
 #pragma unroll
-            for (int c = 0; c < E; ++c) kv[c] = vv[c] = 0.f;
+        for (int u = 0; u < UO; ++u) {
+            const int j = key_of(it + u);
+            const size_t off = (size_t)(j < n ? j : 0) * D + c0;
+            fetch_seg<E>(kh + off, j < n, kr[u]);
+            fetch_seg<E>(vh + off, j < n, vr[u]);
         }
-        float t = 0.f;
+        float t[UO];
 #pragma unroll
-        for (int c = 0; c < E; ++c) t = fmaf(xv[c], kv[c], t);
-        t = group_sum(t);
-        const float u = valid ? wts[j] * (c1 - t) : 0.f;
-        us += u;
+        for (int u = 0; u < UO; ++u) {
+            float kv[E];
+            unpack_seg<E>(kr[u], kv);
+            float x = 0.f;
 #pragma unroll
-        for (int c = 0; c < E; ++c) acc[c] = fmaf(u, vv[c], acc[c]);
+            for (int c = 0; c < E; ++c) x = fmaf(xv[c], kv[c], x);
+            t[u] = x;
+        }
+#pragma unroll
+        for (int u = 0; u < UO; ++u) t[u] = group_sum(t[u]);
+#pragma unroll
+        for (int u = 0; u < UO; ++u) {
+            const int j = key_of(it + u);
+            if (j >= n) continue;
+            const float uj = wts[j] * (c1 - t[u]);
+            us += uj;
+            float vv[E];
+            unpack_seg<E>(vr[u], vv);
+#pragma unroll
+            for (int c = 0; c < E; ++c) acc[c] = fmaf(uj, vv[c], acc[c]);
+        }
     }
 #pragma unroll
     for (int c = 0; c < E; ++c) sm.part[g][c0 + c] = acc[c];
@@ -649,10 +742,10 @@ cudaError_t launch_dec_cluster(const DecodeProblem& p, cudaStream_t stream) {
 
 // The cluster form reads K from HBM once but pays a cluster-wide exchange per pass; the streaming
 // form re-reads K every pass but keeps every SM busy with whole heads.  Measured on GB300 (bf16,
-// n = 4096, d = 128, 16 CG iterations): 16 heads 0.23 vs 0.76 ms, 64 heads 0.55 vs 0.77 ms, 256
-// heads 1.92 vs 1.47 ms, 1024 heads 7.3 vs 5.7 ms (cluster vs streaming): the cluster form wins
-// while there are too few heads to fill the GPU, up to about 128 heads.
-constexpr long long kClusterMaxHeads = 128;
+// n = 4096, d = 128, 16 CG iterations), cluster vs streaming: 16 heads 0.22 vs 0.43 ms, 32 heads
+// 0.33 vs 0.44 ms, 48 heads 0.435 vs 0.441 ms, 64 heads 0.54 vs 0.44 ms, 128 heads 0.97 vs 0.67 ms.
+// The cluster form wins while there are too few heads to fill the GPU, up to about 48 heads.
+constexpr long long kClusterMaxHeads = 48;
 
 template <int D, typename T>
 cudaError_t launch_dec_pick(const DecodeProblem& p, cudaStream_t stream) {

@@ -72,7 +72,7 @@ def test_decode_converged_matches_exact_solve(lla_gpu, dtype, d, n):
 @pytest.mark.parametrize("dtype,n,B", [("bf16", 8000, 1), ("fp32", 4000, 1), ("bf16", 600, 50)])
 def test_decode_streaming_form(lla_gpu, dtype, n, B):
     """The streaming form (K re-read every pass) serves caches too long for an eighth to sit in a
-    CTA's shared memory, and batches of more than 128 heads; the cluster form the rest.  Both
+    CTA's shared memory, and batches of more than 48 heads; the cluster form the rest.  Both
     meet the same gate."""
     w = workload("lm_bf16", B=B, H=3, n=n, d=128, dtype=dtype, tau=1.0 / math.sqrt(128), cg_max_iters=576,
                  cg_tol=1e-6)
@@ -80,9 +80,23 @@ def test_decode_streaming_form(lla_gpu, dtype, n, B):
     _gate(w, qkv, res, lambda qi, K, V: lla_row(qi, K, V, w.tau, w.lam))
 
 
-def test_decode_reads_only_the_valid_cache_rows(lla_gpu):
-    """n_cap > n: rows past n hold NaN and must not reach the result."""
-    w = workload("lm_bf16", B=2, H=2, n=200, d=128, tau=1.0 / math.sqrt(128), cg_max_iters=300, cg_tol=1e-6)
+@pytest.mark.parametrize("dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("d", [16, 32, 64])
+def test_decode_streaming_form_small_heads(lla_gpu, dtype, d):
+    """The streaming form at every smaller head dimension (150 heads: past the cluster form's
+    range), with a cache length that leaves a ragged last group of keys and a ragged last batch
+    of the rows each thread fetches ahead."""
+    w = workload("lm_bf16", B=50, H=3, n=299, d=d, dtype=dtype, tau=1.0 / math.sqrt(d), cg_max_iters=4 * d + 64,
+                 cg_tol=1e-6)
+    qkv, res = _decode(w)
+    _gate(w, qkv, res, lambda qi, K, V: lla_row(qi, K, V, w.tau, w.lam))
+
+
+@pytest.mark.parametrize("B", [2, 75])
+def test_decode_reads_only_the_valid_cache_rows(lla_gpu, B):
+    """n_cap > n: rows past n hold NaN and must not reach the result (B = 2: the cluster form;
+    B = 75, 150 heads: the streaming form)."""
+    w = workload("lm_bf16", B=B, H=2, n=200, d=128, tau=1.0 / math.sqrt(128), cg_max_iters=300, cg_tol=1e-6)
     qkv, res = _decode(w, n_cap=333)
     assert all(np.isfinite(t.double().numpy()).all() for t in res[:3])
     _gate(w, qkv, res, lambda qi, K, V: lla_row(qi, K, V, w.tau, w.lam))
