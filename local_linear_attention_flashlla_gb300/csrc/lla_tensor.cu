@@ -263,15 +263,16 @@ __device__ __forceinline__ void load_dir8(const unsigned char* hi, const unsigne
 
 // One 16-coordinate chunk C of this thread's DH coordinates of
 //   cp = (C/omega) p_hat = Y ysc - kbar msc + lam_n p_hat
-// (and, with DOT, the partial dot p_hat.cp as two fp32 partial sums).
-template <int C, int DH, bool DOT>
-__device__ __forceinline__ void cg_apply_chunk(uint32_t ty, const unsigned char* ptile, const unsigned char* plo, bool split,
+// (and, with DOT, the partial dot p_hat.cp as two fp32 partial sums).  SPLIT: the direction tile
+// carries an fp16 remainder (hi + lo); a compile-time form, so the caller's loops hold no branch on it.
+template <int C, int DH, bool DOT, bool SPLIT>
+__device__ __forceinline__ void cg_apply_chunk(uint32_t ty, const unsigned char* ptile, const unsigned char* plo,
                                                int row, int col, const float (&kv)[DH], float ysc, float msc, float lam_n,
                                                float psc, float (&cp)[16], uint64_t& pcp2) {
     float y[16], p0[8], p1[8];
     tmem_ld16(ty + C * 16, y);
-    load_dir8(ptile, plo, split, row, col + C * 16, psc, p0);
-    load_dir8(ptile, plo, split, row, col + C * 16 + 8, psc, p1);
+    load_dir8(ptile, plo, SPLIT, row, col + C * 16, psc, p0);
+    load_dir8(ptile, plo, SPLIT, row, col + C * 16 + 8, psc, p1);
     tmem_ld_wait();
     const uint64_t ysc2 = f2_pack(ysc, ysc), nmsc2 = f2_pack(-msc, -msc), lam2 = f2_pack(lam_n, lam_n);
 #pragma unroll
@@ -829,17 +830,17 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         float kbr = 0.f, kpx = 0.f;
         int cg_sweeps = 0;
         // New direction p = res + beta p_old, stored in the direction tile as fp16 x 2^sp (hi, and
-        // lo when split_p).  First pass: p into PN (DH floats of registers) and max |p|, which
+        // lo when SPLITC, the direction's form).  First pass: p into PN (DH floats of registers) and max |p|, which
         // fixes sp; with XUPD it also stores x = XO + ALPHA p_old, p_old being the direction of
         // the sweep just finished and XO (DH floats) the previous x.  Second pass: pack and store.
-#define LLA_SET_DIRECTION(BETA, KEEP, XUPD, ALPHA, PN, XO)                                                 \
+#define LLA_SET_DIRECTION(BETA, KEEP, XUPD, ALPHA, PN, XO, SPLITC)                                         \
         {                                                                                                  \
             const float osc_ = pow2i(-sp);                                                                 \
             const uint64_t b2_ = f2_pack((BETA), (BETA));                                                  \
             float mp_ = 0.f;                                                                               \
             _Pragma("unroll") for (int e0 = 0; e0 < DH; e0 += 8) {                                         \
                 float po_[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};                                   \
-                if (KEEP) load_dir8(s.p, s.rlo, split_p, row, half * DH + e0, osc_, po_);                  \
+                if (KEEP) load_dir8(s.p, s.rlo, SPLITC, row, half * DH + e0, osc_, po_);                   \
                 if (XUPD) {                                                                                \
                     _Pragma("unroll") for (int u = 0; u < 8; ++u)                                          \
                         xt[(e0 + u) * BQ] = fmaf((ALPHA), po_[u], XO[e0 + u]);                             \
@@ -865,7 +866,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     lw_[u >> 1] = pack_half2(x0_ - hf_.x, x1_ - hf_.y);                                    \
                 }                                                                                          \
                 *reinterpret_cast<uint4*>(tile_half(s.p, row, half * DH + e0)) = hk_;                      \
-                if (split_p) *reinterpret_cast<uint4*>(tile_half(s.rlo, row, half * DH + e0)) = lk_;       \
+                if (SPLITC) *reinterpret_cast<uint4*>(tile_half(s.rlo, row, half * DH + e0)) = lk_;        \
             }                                                                                              \
             sp = sp_new_;                                                                                  \
             sM = scale_exp(kbound * mp_ * 1.001f);                                                         \
@@ -943,7 +944,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             rn0 = sqrtf(gamma);
             active = row_ok && gamma > 0.f && !(sqrtf(gamma) <= prm.cg_tol * rn0);
             float pn[DH];
-            LLA_SET_DIRECTION(0.f, false, false, 0.f, pn, pn);
+            LLA_SET_DIRECTION(0.f, false, false, 0.f, pn, pn, split_p);
         } else {
             float kv[DH];
             const float ysc = pow2i(-(14 + ek)) * inv_om;
@@ -977,7 +978,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             rn0 = sqrtf(gamma);
             active = row_ok && gamma > 0.f && !(sqrtf(gamma) <= prm.cg_tol * rn0);
             float pn[DH];
-            LLA_SET_DIRECTION(0.f, false, false, 0.f, pn, pn);
+            LLA_SET_DIRECTION(0.f, false, false, 0.f, pn, pn, split_p);
         }
 
         // ---------------- CG sweeps ----------------
@@ -1042,19 +1043,26 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // sweep's first A' product (which waits for this update's direction)
             const uint32_t tcp = tA + lane_off + half * 64;
             uint64_t pcp2 = 0;
-#define LLA_CG_CHUNK(C)                                                                                    \
+#define LLA_CG_CHUNK(C, SPLITC)                                                                            \
             if constexpr ((C) * 16 < DH) {                                                                 \
                 float cp_[16];                                                                             \
                 uint32_t cb_[16];                                                                          \
-                cg_apply_chunk<C, DH, true>(ty, s.p, s.rlo, split_p, row, half * DH, kv, ysc, msc, lam_n,   \
-                                            psc, cp_, pcp2);                                               \
+                cg_apply_chunk<C, DH, true, SPLITC>(ty, s.p, s.rlo, row, half * DH, kv, ysc, msc, lam_n,    \
+                                                    psc, cp_, pcp2);                                       \
                 _Pragma("unroll") for (int j = 0; j < 16; ++j) cb_[j] = __float_as_uint(cp_[j]);          \
                 tmem_st16(tcp + (C) * 16, cb_);                                                            \
             }
-            LLA_CG_CHUNK(0);
-            LLA_CG_CHUNK(1);
-            LLA_CG_CHUNK(2);
-            LLA_CG_CHUNK(3);
+            if (split_p) {
+                LLA_CG_CHUNK(0, true);
+                LLA_CG_CHUNK(1, true);
+                LLA_CG_CHUNK(2, true);
+                LLA_CG_CHUNK(3, true);
+            } else {
+                LLA_CG_CHUNK(0, false);
+                LLA_CG_CHUNK(1, false);
+                LLA_CG_CHUNK(2, false);
+                LLA_CG_CHUNK(3, false);
+            }
 #undef LLA_CG_CHUNK
             tmem_st_wait();
             const float pcp = xch.sum(f2_total(pcp2));
@@ -1064,23 +1072,25 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             uint64_t g22 = 0, kr2 = 0;
             {
                 const uint64_t na2 = f2_pack(-alpha, -alpha);
-#define LLA_CG_STEP(C)                                                                                     \
+                float c0[16], c1[16];
+                tmem_ld16(tcp, c0);
+                tmem_ld_wait();
+#define LLA_CG_STEP(C, CC, CN)                                                                             \
                 if constexpr ((C) * 16 < DH) {                                                             \
-                    float cp_[16];                                                                         \
-                    tmem_ld16(tcp + (C) * 16, cp_);                                                        \
-                    tmem_ld_wait();                                                                        \
+                    if constexpr (((C) + 1) * 16 < DH) tmem_ld16(tcp + ((C) + 1) * 16, CN);                \
                     _Pragma("unroll") for (int j = 0; j < 16; j += 2) {                                    \
                         uint64_t r2 = f2_pack(res[(C) * 16 + j], res[(C) * 16 + j + 1]);                   \
-                        if (upd) r2 = f2_fma(na2, f2_pack(cp_[j], cp_[j + 1]), r2);                        \
+                        if (upd) r2 = f2_fma(na2, f2_pack(CC[j], CC[j + 1]), r2);                          \
                         f2_unpack(r2, res[(C) * 16 + j], res[(C) * 16 + j + 1]);                           \
                         g22 = f2_fma(r2, r2, g22);                                                         \
                         kr2 = f2_fma(f2_pack(kv[(C) * 16 + j], kv[(C) * 16 + j + 1]), r2, kr2);            \
                     }                                                                                      \
+                    tmem_ld_wait();                                                                        \
                 }
-                LLA_CG_STEP(0);
-                LLA_CG_STEP(1);
-                LLA_CG_STEP(2);
-                LLA_CG_STEP(3);
+                LLA_CG_STEP(0, c0, c1);
+                LLA_CG_STEP(1, c1, c0);
+                LLA_CG_STEP(2, c0, c1);
+                LLA_CG_STEP(3, c1, c0);
 #undef LLA_CG_STEP
             }
             // the previous x (this thread's own scratch), loaded while the exchange below waits
@@ -1106,7 +1116,9 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 kbr = 0.f;
             }
             float pn[DH];
-            LLA_SET_DIRECTION(beta, true, true, alpha, pn, xo);
+            // the form as a constant: the loops over the coordinates carry no branch on it
+            if (split_p) LLA_SET_DIRECTION(beta, true, true, alpha, pn, xo, true)
+            else LLA_SET_DIRECTION(beta, true, true, alpha, pn, xo, false)
         }
 
         if constexpr (BWD) {
