@@ -163,17 +163,25 @@ def kernel_source_hash(kernel):
     return h.hexdigest()[:16]
 
 
-def load_traffic(kernel, workload_name):
-    """DRAM bytes per launch from the committed ncu summary, if taken on this exact source."""
+def load_traffic(kernel, w):
+    """DRAM bytes per launch from the committed ncu summary, if taken on this exact source.
+
+    The summary holds the bytes of the named workload at its default batch; the (b, h) slices are
+    independent, so a run at another batch B scales them by B / default B.  Any other change to
+    the workload's shape gives None."""
+    from local_linear_attention_flashlla_gb300.inputs import workload
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             doc = json.load(f)
     except (OSError, ValueError):
         return None
-    ent = doc.get(f"{kernel}:{workload_name}")
+    ent = doc.get(f"{kernel}:{w.name}")
     if not ent or kernel not in KERNEL_SOURCES or ent.get("source_hash") != kernel_source_hash(kernel):
         return None
-    return ent.get("dram_bytes_per_launch")
+    base = workload(w.name)
+    if w.with_(B=base.B) != base:
+        return None
+    return int(round(ent.get("dram_bytes_per_launch") * w.B / base.B))
 
 
 # ----------------------------------------------------------------------------- CPU oracle timing
@@ -497,7 +505,8 @@ def run_decode(args, world, rank, local):
                        "inputs": f"{w.dtype} caches resident in HBM"},
             "hbm_gbs": method / (ms_per_step / 1e3) / 1e9,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                         "traffic": None, "peak_source": f"{peak_kind} copy bandwidth",
+                         "traffic": load_traffic("lla_decode_kernel", w),
+                         "peak_source": f"{peak_kind} copy bandwidth",
                          "bytes_counted": f"method bytes {method} per step: K in each of T+2 passes, V once, q and "
                                           f"outputs once (compulsory: {comp})"},
             "clocks": clocks, "e2e": e2e, "gpu_launches": args.steps,
@@ -595,7 +604,7 @@ def run_backward(args, world, rank, local):
         stats_peak, stats_bound, stats_src = alu_peak, "alu", "derived: 152 SMs x 128 fp32 FMA lanes x 2 flops x max SM clock"
     stats_roof = {"bound": stats_bound, "achieved": q_flops / (q_ms / 1e3) / 1e12, "peak": stats_peak,
                   "unit": "TFLOP/s", "frac": q_flops / (q_ms / 1e3) / 1e12 / stats_peak,
-                  "traffic": load_traffic("lla_tc_kernel_bwd" if stats_tensor else "lla_bwd_stats_kernel", w.name),
+                  "traffic": load_traffic("lla_tc_kernel_bwd" if stats_tensor else "lla_bwd_stats_kernel", w),
                   "peak_source": stats_src,
                   "flops_counted": "stats stage, useful (4+2T) passes x 2d per causal pair"
                                    + ("; executed on tensor cores: (9+5T) passes (hi + lo operands)" if stats_tensor else "")}
@@ -807,14 +816,14 @@ def main():
     if rpath == lla.LLA_PATH_FP32:
         peak = fp32_alu_peak_tflops(peaks.get("sm_max_mhz", 2070.0))
         roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": load_traffic(kern_name, w.name),
+                "traffic": load_traffic(kern_name, w),
                 "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 flops x max SM clock",
                 "flops_counted": "useful (4+3T) passes x 2d per causal pair"}
         dtype = "f32"
     else:
         peak = peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": None if parallax else load_traffic(kern_name, w.name), "peak_source": f"{peak_kind} bf16 burst",
+                "traffic": None if parallax else load_traffic(kern_name, w), "peak_source": f"{peak_kind} bf16 burst",
                 "flops_counted": ("useful 4 passes (q.k, weighted key mean, probe.k, values) x 2d per causal pair"
                                   if parallax else "useful (4+3T) passes x 2d per causal pair")}
         dtype = "f16"
