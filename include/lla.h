@@ -101,6 +101,17 @@ int lla_resolve_path(int dtype, int path, int d);
 int lla_sync_status(void* stream);
 
 /*
+ * lla_selftest_device_timeout -- self-test of the timeout reporting above.  Launches on `stream`
+ * one small kernel whose single waiting thread calls the same bounded mbarrier wait the tensor
+ * kernels use, on a barrier that nothing arrives on.  After the wait's limit (about two seconds)
+ * the kernel records the timeout in the device error word and returns normally, so the next
+ * lla_sync_status(stream) returns LLA_ERR_DEVICE_TIMEOUT and clears the word; the CUDA context
+ * stays usable.  Returns LLA_OK once the kernel is launched (LLA_ERR_CUDA if the launch fails).
+ * For tests of a caller's error handling; it does no other work.
+ */
+int lla_selftest_device_timeout(void* stream);
+
+/*
  * lla_profile_enable -- on != 0: every later call records CUDA events on its stream around its
  * dominant kernel (the fused sweep kernel) and around the whole call; on == 0 stops.
  * lla_profile_read -- elapsed milliseconds of the most recent profiled call: main_ms for the

@@ -14,7 +14,8 @@ import os
 
 __all__ = [
     "LLAError", "load_library", "library_path", "forward", "lla_forward", "lla_forward_ex",
-    "lla_workspace_size", "lla_resolve_path", "lla_sync_status", "lla_last_error", "lla_version",
+    "lla_workspace_size", "lla_resolve_path", "lla_sync_status", "lla_selftest_device_timeout", "lla_last_error",
+    "lla_version",
     "lla_profile_enable", "lla_profile_read", "lla_forward_noalloc", "lla_parallax_forward", "parallax_forward",
     "lla_decode", "lla_decode_max_n", "decode", "lla_backward", "lla_backward_workspace_size", "backward",
     "LLA_OK", "LLA_ERR_INVALID_ARG", "LLA_ERR_UNSUPPORTED", "LLA_ERR_CUDA", "LLA_ERR_DEVICE_TIMEOUT",
@@ -40,6 +41,7 @@ _SIGNATURES = {
     "lla_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "lla_resolve_path": (_c_int, [_c_int, _c_int, _c_int]),
     "lla_sync_status": (_c_int, [_vp]),
+    "lla_selftest_device_timeout": (_c_int, [_vp]),
     "lla_last_error": (ctypes.c_char_p, []),
     "lla_forward_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_float,
                                      _c_float, _c_int, _c_float, _vp]),
@@ -124,6 +126,12 @@ def lla_profile_read():
 def lla_sync_status(stream=None):
     """Synchronise the stream and raise if a kernel recorded a device-side wait timeout."""
     _check(load_library().lla_sync_status(_stream_ptr(stream)))
+
+
+def lla_selftest_device_timeout(stream=None):
+    """Launch the library's timeout self-test kernel (a bounded wait that gives up after about two
+    seconds); the next lla_sync_status(stream) raises LLAError with LLA_ERR_DEVICE_TIMEOUT."""
+    _check(load_library().lla_selftest_device_timeout(_stream_ptr(stream)))
 
 
 def _stream_ptr(stream):

@@ -8,6 +8,7 @@
 
 #include "../../include/lla.h"
 #include "lla_internal.h"
+#include "tc_ptx.cuh"
 
 namespace lla {
 
@@ -60,6 +61,26 @@ cudaError_t read_and_clear_device_error(unsigned* out, cudaStream_t stream) {
     return e;
 }
 
+
+// Self-test of the timeout path.  One thread waits, through the same bounded, abortable mbarrier
+// wait the tensor kernels use, for a phase of a barrier that nothing arrives on.  The wait gives up
+// after its limit (about two seconds of wall time), raises the launch-wide abort word and returns;
+// the thread then records the timeout in the device error word exactly as a tensor kernel's CTA
+// does before it exits.  The kernel ends normally: no trap, no fault, nothing left waiting.
+__device__ int g_selftest_abort = 0;
+
+__global__ void lla_selftest_wait_kernel(unsigned* dev_err) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int err;
+    if (threadIdx.x == 0) {
+        err = 0;
+        tc::mbar_init(&bar, 1);
+        tc::mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && !tc::mbar_wait_abortable(&bar, 0, &err, &g_selftest_abort) && err)
+        atomicOr(dev_err, (unsigned)kDevErrMbarTimeout);
+}
 
 // Launch a validated problem on the resolved path (workspace: caller's buffer, or null to take
 // one from the stream-ordered pool for the duration of the call).
@@ -166,6 +187,20 @@ int lla_forward_ex(int dtype, int path, const void* q, const void* k, const void
     lla::Problem p{q, k, v, out, rho, denom, cg_iters, B, H, n, d, tau, lambda, cg_max_iters, cg_tol, dtype,
                    nullptr, nullptr, nullptr};
     return lla::run_problem(p, rpath, workspace, workspace_bytes, static_cast<cudaStream_t>(stream_));
+}
+
+int lla_selftest_device_timeout(void* stream) {
+    lla::g_msg[0] = '\0';
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned* word = lla::device_error_word();
+    if (!word) return fail(LLA_ERR_CUDA, "lla_selftest_device_timeout: device error word not found");
+    const int zero = 0;
+    cudaError_t e = cudaMemcpyToSymbolAsync(lla::g_selftest_abort, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return lla::cuda_fail(e, "lla_selftest_device_timeout: abort word reset");
+    lla::lla_selftest_wait_kernel<<<1, 32, 0, s>>>(word);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return lla::cuda_fail(e, "lla_selftest_device_timeout: launch");
+    return LLA_OK;
 }
 
 int lla_profile_enable(int on) {
