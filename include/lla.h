@@ -93,6 +93,40 @@ size_t lla_workspace_size(int dtype, int path, int B, int H, int n, int d);
 int lla_resolve_path(int dtype, int path, int d);
 
 /*
+ * lla_forward_host -- lla_forward_ex with q, k, v read from HOST memory and out, rho, denom
+ * (and cg_iters) written to HOST memory, the transfers overlapped with the computation.
+ *
+ * The B*H (b, h) slices are processed in chunks of chunk_slices consecutive slices (0: about
+ * eight chunks).  Chunk c runs on one of two library-owned CUDA streams with its own half of
+ * the device buffer: its inputs are copied in while chunk c-1 computes, and chunk c-1's results
+ * are copied out while chunk c computes.  Both library streams start after the work already on
+ * `stream`, and `stream` continues after both; the call returns once everything is queued, so
+ * the host buffers must stay valid, and out/rho/denom must not be read, until `stream` has
+ * reached that point (cudaStreamSynchronize or lla_sync_status).
+ *
+ * Each chunk's result is the result of lla_forward_ex on that chunk's slices (B = its slice
+ * count, H = 1): the tensor path chooses its fp16 operand scales per chunk, so its last bits
+ * can differ from one lla_forward_ex call on all slices; the fp32 path's results are identical.
+ *
+ * q, k, v      [B,H,n,d] host buffers of dtype; out the same; rho [B,H,n,d] and denom [B,H,n]
+ *              fp32; cg_iters NULL or [B,H,n] int32.  Pinned memory (cudaHostAlloc, or torch's
+ *              pin_memory) lets the copies run asynchronously; pageable memory works, slower.
+ * device_buffer NULL (taken from the stream-ordered pool for the call) or a device buffer of
+ *              lla_forward_host_buffer_size(...) bytes, 256-byte aligned, used by no other call
+ *              until `stream` has passed this one.
+ * Other arguments and errors as for lla_forward_ex; chunk_slices < 0 or a device buffer too
+ * small or misaligned gives LLA_ERR_INVALID_ARG before anything is queued.  The two library
+ * streams are shared by all calls: do not call this from several host threads at once.
+ */
+int lla_forward_host(int dtype, int path, const void* q, const void* k, const void* v, void* out,
+                     float* rho, float* denom, int* cg_iters, int B, int H, int n, int d, float tau,
+                     float lambda, int cg_max_iters, float cg_tol, int chunk_slices,
+                     void* device_buffer, size_t device_buffer_bytes, void* stream);
+
+/* Bytes of device buffer lla_forward_host needs for these arguments (0 for invalid ones). */
+size_t lla_forward_host_buffer_size(int dtype, int path, int B, int H, int n, int d, int chunk_slices);
+
+/*
  * lla_sync_status -- synchronise `stream`, then report and clear the library's device error
  * word: set when a bounded wait inside a kernel gave up (LLA_ERR_DEVICE_TIMEOUT), or when the
  * tensor kernel found its dynamic shared memory not 1024-byte aligned and did no work

@@ -13,7 +13,8 @@ import ctypes
 import os
 
 __all__ = [
-    "LLAError", "load_library", "library_path", "forward", "lla_forward", "lla_forward_ex",
+    "LLAError", "load_library", "library_path", "forward", "forward_host", "lla_forward", "lla_forward_ex",
+    "lla_forward_host", "lla_forward_host_buffer_size",
     "lla_workspace_size", "lla_resolve_path", "lla_sync_status", "lla_selftest_device_timeout", "lla_last_error",
     "lla_version",
     "lla_profile_enable", "lla_profile_read", "lla_forward_noalloc", "lla_parallax_forward", "parallax_forward",
@@ -39,6 +40,9 @@ _SIGNATURES = {
     "lla_forward_ex": (_c_int, [_c_int, _c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
                                 _c_float, _c_float, _c_int, _c_float, _vp, _c_size, _vp]),
     "lla_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "lla_forward_host": (_c_int, [_c_int, _c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                                  _c_float, _c_float, _c_int, _c_float, _c_int, _vp, _c_size, _vp]),
+    "lla_forward_host_buffer_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "lla_resolve_path": (_c_int, [_c_int, _c_int, _c_int]),
     "lla_sync_status": (_c_int, [_vp]),
     "lla_selftest_device_timeout": (_c_int, [_vp]),
@@ -160,6 +164,18 @@ def lla_forward_ex(dtype, path, q_ptr, k_ptr, v_ptr, out_ptr, rho_ptr, denom_ptr
     """Raw C entry point with dtype/path/iteration-count/workspace arguments."""
     _check(load_library().lla_forward_ex(dtype, path, q_ptr, k_ptr, v_ptr, out_ptr, rho_ptr, denom_ptr, iters_ptr,
                                          B, H, n, d, tau, lam, cg_max_iters, cg_tol, ws_ptr, ws_bytes, stream_ptr))
+
+
+def lla_forward_host(dtype, path, q_ptr, k_ptr, v_ptr, out_ptr, rho_ptr, denom_ptr, iters_ptr, B, H, n, d, tau, lam,
+                     cg_max_iters, cg_tol, chunk_slices, buf_ptr, buf_bytes, stream_ptr):
+    """Raw C entry point of the host-buffer forward (pointers are host addresses, buf_ptr a device one)."""
+    _check(load_library().lla_forward_host(dtype, path, q_ptr, k_ptr, v_ptr, out_ptr, rho_ptr, denom_ptr, iters_ptr,
+                                           B, H, n, d, tau, lam, cg_max_iters, cg_tol, chunk_slices, buf_ptr,
+                                           buf_bytes, stream_ptr))
+
+
+def lla_forward_host_buffer_size(dtype, path, B, H, n, d, chunk_slices=0):
+    return load_library().lla_forward_host_buffer_size(dtype, path, B, H, n, d, chunk_slices)
 
 
 def lla_parallax_forward(dtype, path, q_ptr, k_ptr, v_ptr, probe_ptr, out_ptr, B, H, n, d, tau, ws_ptr, ws_bytes,
@@ -320,6 +336,54 @@ def forward(q, k, v, tau, lam, cg_max_iters, cg_tol=0.0, *, path=LLA_PATH_AUTO, 
     lla_forward_ex(dtype, path, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), rho.data_ptr(),
                    denom.data_ptr(), None if iters is None else iters.data_ptr(), B, H, n, d, float(tau), float(lam),
                    int(cg_max_iters), float(cg_tol), ws_ptr, ws_bytes, _stream_ptr(stream))
+    if return_iters:
+        return out, rho, denom, iters
+    return out, rho, denom
+
+
+def forward_host(q, k, v, tau, lam, cg_max_iters, cg_tol=0.0, *, path=LLA_PATH_AUTO, chunk_slices=0,
+                 return_iters=False, out=None, rho=None, denom=None, device_buffer=None, stream=None):
+    """forward() on CPU tensors q, k, v [B, H, n, d] (bf16 or fp32; pin them for overlapped copies).
+
+    The library copies the (b, h) slices to the GPU in chunks, computes and copies the results
+    back into CPU tensors (pinned unless passed in), overlapping the transfers with the compute.
+    Asynchronous on the current (or given) stream: synchronise it before reading the results.
+    device_buffer: optional uint8 CUDA tensor of lla_forward_host_buffer_size(...) bytes.
+    """
+    import torch
+    if q.is_cuda or k.is_cuda or v.is_cuda:
+        raise LLAError(LLA_ERR_INVALID_ARG, "forward_host takes CPU tensors; use forward() for CUDA tensors")
+    if q.shape != k.shape or q.shape != v.shape or q.dim() != 4:
+        raise LLAError(LLA_ERR_INVALID_ARG, f"q, k, v must share one [B, H, n, d] shape, got {tuple(q.shape)}, "
+                                            f"{tuple(k.shape)}, {tuple(v.shape)}")
+    if not (q.dtype == k.dtype == v.dtype) or q.dtype not in (torch.bfloat16, torch.float32):
+        raise LLAError(LLA_ERR_INVALID_ARG, "q, k, v must all be bf16 or all fp32")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise LLAError(LLA_ERR_INVALID_ARG, "q, k, v must be contiguous (a copy would not stay alive for the call)")
+    B, H, n, d = q.shape
+    dtype = LLA_DTYPE_BF16 if q.dtype == torch.bfloat16 else LLA_DTYPE_FP32
+
+    def host_out(t, shape, dt):
+        if t is None:
+            return torch.empty(shape, dtype=dt).pin_memory()
+        if t.is_cuda or tuple(t.shape) != tuple(shape) or t.dtype != dt or not t.is_contiguous():
+            raise LLAError(LLA_ERR_INVALID_ARG, f"output must be a contiguous CPU {dt} tensor of shape {tuple(shape)}")
+        return t
+
+    out = host_out(out, (B, H, n, d), q.dtype)
+    rho = host_out(rho, (B, H, n, d), torch.float32)
+    denom = host_out(denom, (B, H, n), torch.float32)
+    iters = torch.empty((B, H, n), dtype=torch.int32).pin_memory() if return_iters else None
+    if device_buffer is None:
+        buf_ptr, buf_bytes = None, 0
+    else:
+        if not device_buffer.is_cuda:
+            raise LLAError(LLA_ERR_INVALID_ARG, "device_buffer must be a CUDA tensor")
+        buf_ptr, buf_bytes = device_buffer.data_ptr(), device_buffer.numel() * device_buffer.element_size()
+    lla_forward_host(dtype, path, q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), rho.data_ptr(),
+                     denom.data_ptr(), None if iters is None else iters.data_ptr(), B, H, n, d, float(tau),
+                     float(lam), int(cg_max_iters), float(cg_tol), int(chunk_slices), buf_ptr, buf_bytes,
+                     _stream_ptr(stream))
     if return_iters:
         return out, rho, denom, iters
     return out, rho, denom

@@ -135,6 +135,73 @@ static int run_problem(Problem& p, int rpath, void* workspace, size_t workspace_
     }
     return LLA_OK;
 }
+
+// Scalar and shape checks shared by the forward entry points (pointers are checked by each).
+static int check_forward_args(int dtype, int path, int B, int H, int n, int d, float tau, float lambda,
+                              int cg_max_iters, float cg_tol, int* rpath_out) {
+    if (B < 1 || H < 1 || n < 1) return fail(LLA_ERR_INVALID_ARG, "B, H, n must be >= 1 (got %d, %d, %d)", B, H, n);
+    if ((long long)B * H > 65535LL * 1024) return fail(LLA_ERR_INVALID_ARG, "B*H too large");
+    if ((long long)B * H * n * d > (1LL << 40)) return fail(LLA_ERR_INVALID_ARG, "problem too large");
+    if (d != 16 && d != 32 && d != 64 && d != 128)
+        return fail(LLA_ERR_INVALID_ARG, "head dim d must be 16, 32, 64 or 128 (got %d)", d);
+    if (!(tau > 0.f) || !(tau < 1e30f)) return fail(LLA_ERR_INVALID_ARG, "tau must be finite and > 0");
+    if (!(lambda > 0.f) || !(lambda < 1e30f)) return fail(LLA_ERR_INVALID_ARG, "lambda must be finite and > 0");
+    if (cg_max_iters < 1 || cg_max_iters > 4096) return fail(LLA_ERR_INVALID_ARG, "cg_max_iters must be in [1, 4096]");
+    if (!(cg_tol >= 0.f) || !(cg_tol < 1e30f)) return fail(LLA_ERR_INVALID_ARG, "cg_tol must be finite and >= 0");
+    if (dtype != LLA_DTYPE_BF16 && dtype != LLA_DTYPE_FP32) return fail(LLA_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+    if (path < LLA_PATH_AUTO || path > LLA_PATH_FP32) return fail(LLA_ERR_INVALID_ARG, "unknown path %d", path);
+    int rpath = path;
+    if (rpath == LLA_PATH_AUTO) rpath = (dtype == LLA_DTYPE_BF16 && (d == 64 || d == 128)) ? LLA_PATH_TENSOR : LLA_PATH_FP32;
+    if (rpath == LLA_PATH_TENSOR && (dtype != LLA_DTYPE_BF16 || (d != 64 && d != 128)))
+        return fail(LLA_ERR_UNSUPPORTED, "tensor path needs bf16 inputs and d in {64, 128}");
+    *rpath_out = rpath;
+    return LLA_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Host-buffer forward: the (b, h) slices go through the device in chunks, on two library streams
+// (chunk c on stream c % 2, with its own half of the device buffer), so chunk c's copy in runs
+// while chunk c-1 computes and chunk c-1's copy out runs while chunk c computes.
+namespace {
+cudaStream_t g_hs[2] = {nullptr, nullptr};
+cudaEvent_t g_he[3] = {nullptr, nullptr, nullptr};   // start (caller stream), done of stream 0 and 1
+
+int host_streams() {
+    for (int i = 0; i < 2; ++i)
+        if (!g_hs[i]) {
+            cudaError_t e = cudaStreamCreateWithFlags(&g_hs[i], cudaStreamNonBlocking);
+            if (e != cudaSuccess) return cuda_fail(e, "host-buffer forward: stream");
+        }
+    for (int i = 0; i < 3; ++i)
+        if (!g_he[i]) {
+            cudaError_t e = cudaEventCreateWithFlags(&g_he[i], cudaEventDisableTiming);
+            if (e != cudaSuccess) return cuda_fail(e, "host-buffer forward: event");
+        }
+    return LLA_OK;
+}
+
+inline size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// One half of the device buffer: q, k, v, out, rho, denom, cg_iters and the tensor workspace of a
+// chunk of C slices.
+struct HostChunk {
+    size_t tin, trho, tden, ws, half;
+    HostChunk(int dtype, int rpath, int C, int n, int d) {
+        const size_t es = dtype == LLA_DTYPE_BF16 ? 2 : 4;
+        tin = a256((size_t)C * n * d * es);
+        trho = a256((size_t)C * n * d * 4);
+        tden = a256((size_t)C * n * 4);
+        ws = rpath == LLA_PATH_TENSOR ? a256(tensor_workspace_bytes(C, 1, n, d)) : 0;
+        half = 4 * tin + trho + 2 * tden + ws;
+    }
+};
+
+int host_chunk_slices(int S, int chunk_slices) {
+    if (chunk_slices > 0) return chunk_slices < S ? chunk_slices : S;
+    const int c = (S + 7) / 8;   // about eight chunks
+    return c < 1 ? 1 : c;
+}
+}  // namespace
 }  // namespace lla
 
 using lla::fail;
@@ -169,24 +236,111 @@ int lla_forward_ex(int dtype, int path, const void* q, const void* k, const void
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(rho) ||
         !aligned16(denom))
         return fail(LLA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
-    if (B < 1 || H < 1 || n < 1) return fail(LLA_ERR_INVALID_ARG, "B, H, n must be >= 1 (got %d, %d, %d)", B, H, n);
-    if ((long long)B * H > 65535LL * 1024) return fail(LLA_ERR_INVALID_ARG, "B*H too large");
-    if ((long long)B * H * n * d > (1LL << 40)) return fail(LLA_ERR_INVALID_ARG, "problem too large");
-    if (d != 16 && d != 32 && d != 64 && d != 128)
-        return fail(LLA_ERR_INVALID_ARG, "head dim d must be 16, 32, 64 or 128 (got %d)", d);
-    if (!(tau > 0.f) || !(tau < 1e30f)) return fail(LLA_ERR_INVALID_ARG, "tau must be finite and > 0");
-    if (!(lambda > 0.f) || !(lambda < 1e30f)) return fail(LLA_ERR_INVALID_ARG, "lambda must be finite and > 0");
-    if (cg_max_iters < 1 || cg_max_iters > 4096) return fail(LLA_ERR_INVALID_ARG, "cg_max_iters must be in [1, 4096]");
-    if (!(cg_tol >= 0.f) || !(cg_tol < 1e30f)) return fail(LLA_ERR_INVALID_ARG, "cg_tol must be finite and >= 0");
-    if (dtype != LLA_DTYPE_BF16 && dtype != LLA_DTYPE_FP32) return fail(LLA_ERR_INVALID_ARG, "unknown dtype %d", dtype);
-    if (path < LLA_PATH_AUTO || path > LLA_PATH_FP32) return fail(LLA_ERR_INVALID_ARG, "unknown path %d", path);
-    const int rpath = lla_resolve_path(dtype, path, d);
-    if (rpath == LLA_PATH_TENSOR && (dtype != LLA_DTYPE_BF16 || (d != 64 && d != 128)))
-        return fail(LLA_ERR_UNSUPPORTED, "tensor path needs bf16 inputs and d in {64, 128}");
+    int rpath = 0;
+    const int st = lla::check_forward_args(dtype, path, B, H, n, d, tau, lambda, cg_max_iters, cg_tol, &rpath);
+    if (st != LLA_OK) return st;
 
     lla::Problem p{q, k, v, out, rho, denom, cg_iters, B, H, n, d, tau, lambda, cg_max_iters, cg_tol, dtype,
                    nullptr, nullptr, nullptr};
     return lla::run_problem(p, rpath, workspace, workspace_bytes, static_cast<cudaStream_t>(stream_));
+}
+
+size_t lla_forward_host_buffer_size(int dtype, int path, int B, int H, int n, int d, int chunk_slices) {
+    int rpath = 0;
+    if (lla::check_forward_args(dtype, path, B, H, n, d, 1.f, 1.f, 1, 0.f, &rpath) != LLA_OK || chunk_slices < 0)
+        return 0;
+    const int C = lla::host_chunk_slices(B * H, chunk_slices);
+    return 2 * lla::HostChunk(dtype, rpath, C, n, d).half;
+}
+
+int lla_forward_host(int dtype, int path, const void* q, const void* k, const void* v, void* out, float* rho,
+                     float* denom, int* cg_iters, int B, int H, int n, int d, float tau, float lambda,
+                     int cg_max_iters, float cg_tol, int chunk_slices, void* device_buffer,
+                     size_t device_buffer_bytes, void* stream_) {
+    lla::g_msg[0] = '\0';
+    if (!q || !k || !v || !out || !rho || !denom) return fail(LLA_ERR_INVALID_ARG, "null host pointer");
+    int rpath = 0;
+    int st = lla::check_forward_args(dtype, path, B, H, n, d, tau, lambda, cg_max_iters, cg_tol, &rpath);
+    if (st != LLA_OK) return st;
+    if (chunk_slices < 0) return fail(LLA_ERR_INVALID_ARG, "chunk_slices must be >= 0 (0: automatic)");
+    const int S = B * H;
+    const int C = lla::host_chunk_slices(S, chunk_slices);
+    const lla::HostChunk hc(dtype, rpath, C, n, d);
+    const size_t need = 2 * hc.half;
+    if (device_buffer) {
+        if (device_buffer_bytes < need)
+            return fail(LLA_ERR_INVALID_ARG, "device buffer too small: %zu < %zu bytes", device_buffer_bytes, need);
+        if ((reinterpret_cast<uintptr_t>(device_buffer) & 255u) != 0)
+            return fail(LLA_ERR_INVALID_ARG, "device buffer must be 256-byte aligned");
+    }
+    if ((st = lla::host_streams()) != LLA_OK) return st;
+
+    cudaStream_t cs = static_cast<cudaStream_t>(stream_);
+    unsigned char* buf = static_cast<unsigned char*>(device_buffer);
+    cudaError_t e = cudaSuccess;
+    if (!buf && (e = cudaMallocAsync(reinterpret_cast<void**>(&buf), need, cs)) != cudaSuccess)
+        return lla::cuda_fail(e, "cudaMallocAsync(host-forward buffer)");
+    // both library streams start after the caller's stream reaches this point
+    if ((e = cudaEventRecord(lla::g_he[0], cs)) != cudaSuccess) return lla::cuda_fail(e, "host forward: event record");
+    for (int i = 0; i < 2; ++i)
+        if ((e = cudaStreamWaitEvent(lla::g_hs[i], lla::g_he[0], 0)) != cudaSuccess)
+            return lla::cuda_fail(e, "host forward: stream wait");
+
+    const size_t es = dtype == LLA_DTYPE_BF16 ? 2 : 4;
+    const unsigned char* hq = static_cast<const unsigned char*>(q);
+    const unsigned char* hk = static_cast<const unsigned char*>(k);
+    const unsigned char* hv = static_cast<const unsigned char*>(v);
+    unsigned char* ho = static_cast<unsigned char*>(out);
+    int rc = LLA_OK;
+    for (int c = 0, s0 = 0; s0 < S && rc == LLA_OK; ++c, s0 += C) {
+        const int cnt = S - s0 < C ? S - s0 : C;
+        cudaStream_t sc = lla::g_hs[c & 1];
+        unsigned char* base = buf + (size_t)(c & 1) * hc.half;
+        unsigned char* dq = base;
+        unsigned char* dk = dq + hc.tin;
+        unsigned char* dv = dk + hc.tin;
+        unsigned char* dout = dv + hc.tin;
+        float* drho = reinterpret_cast<float*>(dout + hc.tin);
+        float* dden = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(drho) + hc.trho);
+        int* dits = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(dden) + hc.tden);
+        void* dws = reinterpret_cast<unsigned char*>(dits) + hc.tden;
+        const size_t tbytes = (size_t)cnt * n * d * es, off = (size_t)s0 * n * d * es;
+        const size_t rbytes = (size_t)cnt * n * d * 4, roff = (size_t)s0 * n * d;
+        const size_t dbytes = (size_t)cnt * n * 4, doff = (size_t)s0 * n;
+        if ((e = cudaMemcpyAsync(dq, hq + off, tbytes, cudaMemcpyHostToDevice, sc)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(dk, hk + off, tbytes, cudaMemcpyHostToDevice, sc)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(dv, hv + off, tbytes, cudaMemcpyHostToDevice, sc)) != cudaSuccess) {
+            rc = lla::cuda_fail(e, "host forward: copy in");
+            break;
+        }
+        lla::Problem p{dq, dk, dv, dout, drho, dden, cg_iters ? dits : nullptr, cnt, 1, n, d, tau, lambda,
+                       cg_max_iters, cg_tol, dtype, nullptr, nullptr, nullptr};
+        const char* why = nullptr;
+        e = rpath == LLA_PATH_FP32 ? lla::launch_simt(p, sc) : lla::launch_tensor(p, dws, sc, &why);
+        if (e != cudaSuccess) {
+            rc = lla::cuda_fail(e, why ? why : "host forward: launch");
+            break;
+        }
+        if ((e = cudaMemcpyAsync(ho + off, dout, tbytes, cudaMemcpyDeviceToHost, sc)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(rho + roff, drho, rbytes, cudaMemcpyDeviceToHost, sc)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(denom + doff, dden, dbytes, cudaMemcpyDeviceToHost, sc)) != cudaSuccess ||
+            (cg_iters && (e = cudaMemcpyAsync(cg_iters + doff, dits, dbytes, cudaMemcpyDeviceToHost, sc)) != cudaSuccess)) {
+            rc = lla::cuda_fail(e, "host forward: copy out");
+            break;
+        }
+    }
+    // the caller's stream continues after both library streams (also on an error, so that a
+    // pool buffer is released only after the work queued on it)
+    for (int i = 0; i < 2; ++i) {
+        cudaError_t e1 = cudaEventRecord(lla::g_he[1 + i], lla::g_hs[i]);
+        if (e1 == cudaSuccess) e1 = cudaStreamWaitEvent(cs, lla::g_he[1 + i], 0);
+        if (e1 != cudaSuccess && rc == LLA_OK) rc = lla::cuda_fail(e1, "host forward: join");
+    }
+    if (!device_buffer) {
+        cudaError_t e2 = cudaFreeAsync(buf, cs);
+        if (e2 != cudaSuccess && rc == LLA_OK) rc = lla::cuda_fail(e2, "cudaFreeAsync(host-forward buffer)");
+    }
+    return rc;
 }
 
 int lla_selftest_device_timeout(void* stream) {
