@@ -190,6 +190,58 @@ __device__ __forceinline__ void reduce_parts(DecSmem<D>& sm, float* dst) {
 
 // Two CTAs per SM (at most 128 registers a thread): with the rows fetched ahead, two CTAs
 // keep enough loads in flight, and the register cap keeps the prefetched rows from spilling.
+__device__ __forceinline__ float warp_sum(float x) {
+    for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// One CG step on the D-vector state in shared memory, by one warp (lane l: coordinates l, l+32,
+// ...; the dot products are warp reductions, so no block barrier is needed inside the step):
+//   cp = (Y - kbar msum)/omega + (lambda/omega) p,  alpha = gamma / p.cp,  x += alpha p,
+//   r -= alpha cp,  gamma' = r.r,  p = r + (gamma'/gamma) p.
+// y_of(c) gives coordinate c of Y.  Returns false, with nothing changed, when p.cp <= 0 (no
+// positive curvature left); otherwise updates x, r, p and gamma.
+template <int D, typename YF>
+__device__ __forceinline__ bool cg_step_warp(DecSmem<D>& sm, YF y_of, float msum, float inv_om, float lam_n,
+                                             float& gamma) {
+    constexpr int NPL = (D + 31) / 32;
+    const int lane = threadIdx.x & 31;
+    float cpv[NPL];
+    float pcp = 0.f;
+#pragma unroll
+    for (int u = 0; u < NPL; ++u) {
+        const int c = lane + 32 * u;
+        cpv[u] = 0.f;
+        if (c < D) {
+            cpv[u] = (y_of(c) - sm.kbar[c] * msum) * inv_om + lam_n * sm.p[c];
+            pcp = fmaf(sm.p[c], cpv[u], pcp);
+        }
+    }
+    pcp = warp_sum(pcp);
+    if (!(pcp > 0.f)) return false;
+    const float alpha = gamma / pcp;
+    float g2 = 0.f;
+#pragma unroll
+    for (int u = 0; u < NPL; ++u) {
+        const int c = lane + 32 * u;
+        if (c < D) {
+            sm.x[c] = fmaf(alpha, sm.p[c], sm.x[c]);
+            const float rv = fmaf(-alpha, cpv[u], sm.r[c]);
+            sm.r[c] = rv;
+            g2 = fmaf(rv, rv, g2);
+        }
+    }
+    g2 = warp_sum(g2);
+    const float beta = g2 / gamma;
+    gamma = g2;
+#pragma unroll
+    for (int u = 0; u < NPL; ++u) {
+        const int c = lane + 32 * u;
+        if (c < D) sm.p[c] = fmaf(beta, sm.p[c], sm.r[c]);
+    }
+    return true;
+}
+
 template <int D, typename T>
 __global__ void __launch_bounds__(DT, 2)
 lla_decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v, T* __restrict__ out,
@@ -342,31 +394,21 @@ lla_decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
         for (int c = 0; c < E; ++c) sm.part[g][c0 + c] = acc[c];
         if (l8 == 0) sm.gs[g][2] = ms;
         reduce_parts<D>(sm, sm.cp);                 // Y
-        float msum = 0.f;
+        // the CG step by warp 0, then one barrier that publishes p and the outcome
+        if (tid < 32) {
+            float msum = 0.f;
 #pragma unroll 8
-        for (int t = 0; t < NG; ++t) msum += sm.gs[t][2];
-        float pcp_part = 0.f;
-        if (tid < D) {
-            const float cpv = (sm.cp[tid] - sm.kbar[tid] * msum) * inv_om + lam_n * sm.p[tid];
-            sm.cp[tid] = cpv;
-            pcp_part = sm.p[tid] * cpv;
+            for (int t = 0; t < NG; ++t) msum += sm.gs[t][2];
+            const bool stepped = cg_step_warp<D>(sm, [&](int c) { return sm.cp[c]; }, msum, inv_om, lam_n, gamma);
+            if (tid == 0) {
+                sm.bc[0] = stepped ? 1.f : 0.f;
+                sm.bc[1] = gamma;
+            }
         }
-        const float pcp = block_sum<D>(sm, pcp_part, 1);
-        if (!(pcp > 0.f)) break;                    // no positive curvature left (uniform)
-        const float alpha = gamma / pcp;
-        float g2_part = 0.f;
-        if (tid < D) {
-            sm.x[tid] = fmaf(alpha, sm.p[tid], sm.x[tid]);
-            const float rv = fmaf(-alpha, sm.cp[tid], sm.r[tid]);
-            sm.r[tid] = rv;
-            g2_part = rv * rv;
-        }
-        const float g2 = block_sum<D>(sm, g2_part, 2);
-        const float beta = g2 / gamma;
-        gamma = g2;
-        ++iters;
-        if (tid < D) sm.p[tid] = fmaf(beta, sm.p[tid], sm.r[tid]);
         __syncthreads();
+        if (sm.bc[0] == 0.f) break;                 // no positive curvature left (uniform)
+        gamma = sm.bc[1];
+        ++iters;
         if (gamma == 0.f || sqrtf(gamma) <= cg_tol * rn0) active = false;
     }
 
@@ -613,37 +655,48 @@ lla_decode_cluster_kernel(const T* __restrict__ q, const T* __restrict__ k, cons
 #pragma unroll
         for (int c = 0; c < E; ++c) sm.part[g][c0 + c] = acc[c];
         if (l8 == 0) sm.gs[g][2] = ms;
-        reduce_parts<D>(sm, sm.cp);
-        float ms_cta = 0.f;
-#pragma unroll 8
-        for (int t = 0; t < NG; ++t) ms_cta += sm.gs[t][2];
-        for (int c = tid; c < D; c += DT) cs.xbuf[slot][c] = sm.cp[c];
-        if (tid == 0) cs.xbuf[slot][D] = ms_cta;
-        cl_combine<D>(cl, cs, slot, sm.cp, scal);            // Y, msum over the whole cache
-        slot ^= 1;
-        const float msum = scal[0];
-        float pcp_part = 0.f;
-        if (tid < D) {
-            const float cpv = (sm.cp[tid] - sm.kbar[tid] * msum) * inv_om + lam_n * sm.p[tid];
-            sm.cp[tid] = cpv;
-            pcp_part = sm.p[tid] * cpv;
-        }
-        const float pcp = block_sum<D>(sm, pcp_part, 1);
-        if (!(pcp > 0.f)) break;
-        const float alpha = gamma / pcp;
-        float g2_part = 0.f;
-        if (tid < D) {
-            sm.x[tid] = fmaf(alpha, sm.p[tid], sm.x[tid]);
-            const float rv = fmaf(-alpha, sm.cp[tid], sm.r[tid]);
-            sm.r[tid] = rv;
-            g2_part = rv * rv;
-        }
-        const float g2 = block_sum<D>(sm, g2_part, 2);
-        const float beta = g2 / gamma;
-        gamma = g2;
-        ++iters;
-        if (tid < D) sm.p[tid] = fmaf(beta, sm.p[tid], sm.r[tid]);
         __syncthreads();
+        // this CTA's partial Y and msum straight into its exchange slot (groups summed in order)
+        for (int c = tid; c < D; c += DT) {
+            float t = 0.f;
+#pragma unroll 8
+            for (int q2 = 0; q2 < NG; ++q2) t += sm.part[q2][c];
+            cs.xbuf[slot][c] = t;
+        }
+        if (tid == 0) {
+            float t = 0.f;
+#pragma unroll 8
+            for (int q2 = 0; q2 < NG; ++q2) t += sm.gs[q2][2];
+            cs.xbuf[slot][D] = t;
+        }
+        // every slot of the cluster is complete after this barrier; warp 0 reads them before this
+        // CTA's next arrival, which a peer's next write to the same slot waits for (two slots in turn)
+        cl.sync();
+        if (tid < 32) {
+            const float* xb[CL];
+#pragma unroll
+            for (int r = 0; r < CL; ++r) xb[r] = cl.map_shared_rank(&cs.xbuf[slot][0], r);
+            float msum = 0.f;
+#pragma unroll
+            for (int r = 0; r < CL; ++r) msum += xb[r][D];
+            auto y_of = [&](int c) {
+                float t = 0.f;
+#pragma unroll
+                for (int r = 0; r < CL; ++r) t += xb[r][c];
+                return t;
+            };
+            // the CG step on the cluster's sums, in rank order: identical in every CTA
+            const bool stepped = cg_step_warp<D>(sm, y_of, msum, inv_om, lam_n, gamma);
+            if (tid == 0) {
+                sm.bc[0] = stepped ? 1.f : 0.f;
+                sm.bc[1] = gamma;
+            }
+        }
+        slot ^= 1;
+        __syncthreads();
+        if (sm.bc[0] == 0.f) break;
+        gamma = sm.bc[1];
+        ++iters;
         if (gamma == 0.f || sqrtf(gamma) <= cg_tol * rn0) active = false;
     }
 
@@ -742,8 +795,8 @@ cudaError_t launch_dec_cluster(const DecodeProblem& p, cudaStream_t stream) {
 
 // The cluster form reads K from HBM once but pays a cluster-wide exchange per pass; the streaming
 // form re-reads K every pass but keeps every SM busy with whole heads.  Measured on GB300 (bf16,
-// n = 4096, d = 128, 16 CG iterations), cluster vs streaming: 16 heads 0.22 vs 0.43 ms, 32 heads
-// 0.33 vs 0.44 ms, 48 heads 0.435 vs 0.441 ms, 64 heads 0.54 vs 0.44 ms, 128 heads 0.97 vs 0.67 ms.
+// n = 4096, d = 128, 16 CG iterations), cluster vs streaming: 16 heads 0.21 vs 0.43 ms, 32 heads
+// 0.32 vs 0.44 ms, 48 heads 0.423 vs 0.437 ms, 64 heads 0.53 vs 0.44 ms, 128 heads 0.94 vs 0.67 ms.
 // The cluster form wins while there are too few heads to fill the GPU, up to about 48 heads.
 constexpr long long kClusterMaxHeads = 48;
 
