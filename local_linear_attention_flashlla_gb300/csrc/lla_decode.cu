@@ -42,48 +42,11 @@ __device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat16
 __device__ __forceinline__ void stf(float* p, float x) { *p = x; }
 __device__ __forceinline__ void stf(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
 
-// E consecutive elements of a row (E = D/8: 2, 4, 8 or 16) as floats, in the widest aligned
-// vector loads (the segment starts at an element index that is a multiple of E).
-template <int E>
-__device__ __forceinline__ void load_seg(const float* p, float (&o)[E]) {
-    if constexpr (E % 4 == 0) {
-#pragma unroll
-        for (int c = 0; c < E; c += 4) {
-            const float4 t = *reinterpret_cast<const float4*>(p + c);
-            o[c] = t.x; o[c + 1] = t.y; o[c + 2] = t.z; o[c + 3] = t.w;
-        }
-    } else {
-        const float2 t = *reinterpret_cast<const float2*>(p);
-        o[0] = t.x; o[1] = t.y;
-    }
-}
-template <int E>
-__device__ __forceinline__ void load_seg(const __nv_bfloat16* p, float (&o)[E]) {
-    if constexpr (E % 8 == 0) {
-#pragma unroll
-        for (int c = 0; c < E; c += 8) {
-            const uint4 t = *reinterpret_cast<const uint4*>(p + c);
-            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&t);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float2 f = __bfloat1622float2(h[u]);
-                o[c + 2 * u] = f.x; o[c + 2 * u + 1] = f.y;
-            }
-        }
-    } else if constexpr (E == 4) {
-        const uint2 t = *reinterpret_cast<const uint2*>(p);
-        const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&t);
-        const float2 a = __bfloat1622float2(h[0]), b = __bfloat1622float2(h[1]);
-        o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y;
-    } else {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
-        o[0] = f.x; o[1] = f.y;
-    }
-}
-
-// E consecutive elements of a row as raw bits.  The streaming passes fetch several rows into
-// these before using any of them, so each thread keeps that many loads in flight: with one row
-// at a time, two CTAs per SM hold too few bytes in flight to cover the HBM latency.
+// E = D/8 consecutive elements of a row (lane l of a group holds elements l*E .. l*E + E-1) as raw
+// bits.  Every pass fetches several rows into these before using any of them, so each thread keeps
+// that many loads in flight and works on independent rows: with one row at a time, two streaming
+// CTAs per SM hold too few bytes in flight to cover the HBM latency, and a cluster CTA's pass over
+// its shared-memory slice is one long dependent chain (load, dot, shuffles) per row.
 template <int E, typename T>
 struct RawSeg {
     static constexpr int W = E * (int)sizeof(T) / 4;   // 32-bit words: 1 .. 16
@@ -133,16 +96,44 @@ __device__ __forceinline__ void unpack_seg(const RawSeg<E, __nv_bfloat16>& r, fl
     }
 }
 
-// Copy E consecutive elements (a 16-byte multiple for every E used with it).
+// x . segment, with two interleaved partial sums: half the dependent FMA chain of one running sum.
 template <int E, typename T>
-__device__ __forceinline__ void copy_seg(T* dst, const T* src) {
-    constexpr int N16 = E * (int)sizeof(T) / 16;
-    if constexpr (N16 >= 1) {
+__device__ __forceinline__ float dot_seg(const float (&x)[E], const RawSeg<E, T>& r) {
+    float kv[E];
+    unpack_seg<E>(r, kv);
+    float t0 = 0.f, t1 = 0.f;
 #pragma unroll
-        for (int c = 0; c < N16; ++c) reinterpret_cast<uint4*>(dst)[c] = reinterpret_cast<const uint4*>(src)[c];
+    for (int c = 0; c < E; c += 2) {
+        t0 = fmaf(x[c], kv[c], t0);
+        t1 = fmaf(x[c + 1], kv[c + 1], t1);
+    }
+    return t0 + t1;
+}
+
+// x . segment as one running sum (the streaming form measured faster with it than with dot_seg;
+// its passes are bound by memory, not by this chain).
+template <int E, typename T>
+__device__ __forceinline__ float dot_seg1(const float (&x)[E], const RawSeg<E, T>& r) {
+    float kv[E];
+    unpack_seg<E>(r, kv);
+    float t = 0.f;
+#pragma unroll
+    for (int c = 0; c < E; ++c) t = fmaf(x[c], kv[c], t);
+    return t;
+}
+
+// Store a fetched segment at p (the alignment fetch_seg needs).
+template <int E, typename T>
+__device__ __forceinline__ void store_seg(T* p, const RawSeg<E, T>& r) {
+    constexpr int W = RawSeg<E, T>::W;
+    uint32_t* d = reinterpret_cast<uint32_t*>(p);
+    if constexpr (W % 4 == 0) {
+#pragma unroll
+        for (int c = 0; c < W; c += 4) *reinterpret_cast<uint4*>(d + c) = make_uint4(r.w[c], r.w[c + 1], r.w[c + 2], r.w[c + 3]);
+    } else if constexpr (W == 2) {
+        *reinterpret_cast<uint2*>(d) = make_uint2(r.w[0], r.w[1]);
     } else {
-#pragma unroll
-        for (int c = 0; c < E; ++c) dst[c] = src[c];
+        d[0] = r.w[0];
     }
 }
 
@@ -284,14 +275,7 @@ lla_decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
         }
         float s[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            float kv[E];
-            unpack_seg<E>(kr[u], kv);
-            float t = 0.f;
-#pragma unroll
-            for (int c = 0; c < E; ++c) t = fmaf(qv[c], kv[c], t);
-            s[u] = t;
-        }
+        for (int u = 0; u < U; ++u) s[u] = dot_seg1<E>(qv, kr[u]);
 #pragma unroll
         for (int u = 0; u < U; ++u) s[u] = tau * group_sum(s[u]);
 #pragma unroll
@@ -368,14 +352,7 @@ lla_decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
             }
             float a[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                float kv[E];
-                unpack_seg<E>(kr[u], kv);
-                float t = 0.f;
-#pragma unroll
-                for (int c = 0; c < E; ++c) t = fmaf(pv[c], kv[c], t);
-                a[u] = t;
-            }
+            for (int u = 0; u < U; ++u) a[u] = dot_seg1<E>(pv, kr[u]);
 #pragma unroll
             for (int u = 0; u < U; ++u) a[u] = group_sum(a[u]);
 #pragma unroll
@@ -433,14 +410,7 @@ lla_decode_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
         }
         float t[UO];
 #pragma unroll
-        for (int u = 0; u < UO; ++u) {
-            float kv[E];
-            unpack_seg<E>(kr[u], kv);
-            float x = 0.f;
-#pragma unroll
-            for (int c = 0; c < E; ++c) x = fmaf(xv[c], kv[c], x);
-            t[u] = x;
-        }
+        for (int u = 0; u < UO; ++u) t[u] = dot_seg1<E>(xv, kr[u]);
 #pragma unroll
         for (int u = 0; u < UO; ++u) t[u] = group_sum(t[u]);
 #pragma unroll
@@ -534,6 +504,10 @@ lla_decode_cluster_kernel(const T* __restrict__ q, const T* __restrict__ k, cons
     const int tid = threadIdx.x, g = tid >> 3, l8 = tid & 7;
     const int c0 = l8 * E;
     const int n_it = (S + NG - 1) / NG;                       // same trip count in every group
+    // rows fetched ahead per thread, as in the streaming form (K and V alike in the output pass)
+    constexpr int U = rows_ahead<E, T>();
+    constexpr int UO = U > 1 ? U / 2 : 1;
+    auto key_of = [&](int it) { return it * NG + g; };
 
     if (tid < D) sm.q[tid] = ldf(q + head * D + tid);
     __syncthreads();
@@ -545,35 +519,42 @@ lla_decode_cluster_kernel(const T* __restrict__ q, const T* __restrict__ k, cons
     float mg = -INFINITY, og = 0.f, acc[E];
 #pragma unroll
     for (int c = 0; c < E; ++c) acc[c] = 0.f;
-    for (int it = 0; it < n_it; ++it) {
-        const int jj = it * NG + g;
-        const bool valid = jj < ns;
-        float kv[E];
-        if (valid) {
-            const T* src = kh + (size_t)(j0 + jj) * D + c0;
-            copy_seg<E>(ks + (size_t)jj * D + c0, src);
-            load_seg<E>(src, kv);
-        } else {
+    for (int it = 0; it < n_it; it += U) {
+        RawSeg<E, T> kr[U];
 #pragma unroll
-            for (int c = 0; c < E; ++c) kv[c] = 0.f;
+        for (int u = 0; u < U; ++u) {
+            const int jj = key_of(it + u);
+            fetch_seg<E>(kh + (size_t)(j0 + (jj < ns ? jj : 0)) * D + c0, jj < ns, kr[u]);
         }
-        float sv = 0.f;
 #pragma unroll
-        for (int c = 0; c < E; ++c) sv = fmaf(qv[c], kv[c], sv);
-        sv = tau * group_sum(sv);
-        if (!valid) continue;
-        if (l8 == 0) wts[jj] = sv;
-        if (sv > mg) {
-            const float f = expf(mg - sv);
-            og *= f;
-#pragma unroll
-            for (int c = 0; c < E; ++c) acc[c] *= f;
-            mg = sv;
+        for (int u = 0; u < U; ++u) {
+            const int jj = key_of(it + u);
+            if (jj < ns) store_seg<E>(ks + (size_t)jj * D + c0, kr[u]);
         }
-        const float w = expf(sv - mg);
-        og += w;
+        float sv[U];
 #pragma unroll
-        for (int c = 0; c < E; ++c) acc[c] = fmaf(w, kv[c], acc[c]);
+        for (int u = 0; u < U; ++u) sv[u] = dot_seg<E>(qv, kr[u]);
+#pragma unroll
+        for (int u = 0; u < U; ++u) sv[u] = tau * group_sum(sv[u]);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int jj = key_of(it + u);
+            if (jj >= ns) continue;
+            if (l8 == 0) wts[jj] = sv[u];
+            if (sv[u] > mg) {
+                const float f = expf(mg - sv[u]);
+                og *= f;
+#pragma unroll
+                for (int c = 0; c < E; ++c) acc[c] *= f;
+                mg = sv[u];
+            }
+            const float w = expf(sv[u] - mg);
+            og += w;
+            float kv[E];
+            unpack_seg<E>(kr[u], kv);
+#pragma unroll
+            for (int c = 0; c < E; ++c) acc[c] = fmaf(w, kv[c], acc[c]);
+        }
     }
     if (l8 == 0) sm.gs[g][0] = mg;
     __syncthreads();
@@ -634,23 +615,29 @@ lla_decode_cluster_kernel(const T* __restrict__ q, const T* __restrict__ k, cons
         float ms = 0.f;
 #pragma unroll
         for (int c = 0; c < E; ++c) acc[c] = 0.f;
-        for (int it2 = 0; it2 < n_it; ++it2) {
-            const int jj = it2 * NG + g;
-            const bool valid = jj < ns;
-            float kv[E];
-            if (valid) load_seg<E>(ks + (size_t)jj * D + c0, kv);
-            else {
+        for (int it2 = 0; it2 < n_it; it2 += U) {
+            RawSeg<E, T> kr[U];
 #pragma unroll
-                for (int c = 0; c < E; ++c) kv[c] = 0.f;
+            for (int u = 0; u < U; ++u) {
+                const int jj = key_of(it2 + u);
+                fetch_seg<E>(ks + (size_t)(jj < ns ? jj : 0) * D + c0, jj < ns, kr[u]);
             }
-            float a = 0.f;
+            float a[U];
 #pragma unroll
-            for (int c = 0; c < E; ++c) a = fmaf(pv[c], kv[c], a);
-            a = group_sum(a);
-            const float mm = valid ? wts[jj] * (a - kp) : 0.f;
-            ms += mm;
+            for (int u = 0; u < U; ++u) a[u] = dot_seg<E>(pv, kr[u]);
 #pragma unroll
-            for (int c = 0; c < E; ++c) acc[c] = fmaf(mm, kv[c], acc[c]);
+            for (int u = 0; u < U; ++u) a[u] = group_sum(a[u]);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int jj = key_of(it2 + u);
+                if (jj >= ns) continue;
+                const float mm = wts[jj] * (a[u] - kp);
+                ms += mm;
+                float kv[E];
+                unpack_seg<E>(kr[u], kv);
+#pragma unroll
+                for (int c = 0; c < E; ++c) acc[c] = fmaf(mm, kv[c], acc[c]);
+            }
         }
 #pragma unroll
         for (int c = 0; c < E; ++c) sm.part[g][c0 + c] = acc[c];
@@ -710,25 +697,31 @@ lla_decode_cluster_kernel(const T* __restrict__ q, const T* __restrict__ k, cons
     float us = 0.f;
 #pragma unroll
     for (int c = 0; c < E; ++c) acc[c] = 0.f;
-    for (int it = 0; it < n_it; ++it) {
-        const int jj = it * NG + g;
-        const bool valid = jj < ns;
-        float kv[E], vv[E];
-        if (valid) {
-            load_seg<E>(ks + (size_t)jj * D + c0, kv);
-            load_seg<E>(vh + (size_t)(j0 + jj) * D + c0, vv);
-        } else {
+    for (int it = 0; it < n_it; it += UO) {
+        RawSeg<E, T> kr[UO], vr[UO];
 #pragma unroll
-            for (int c = 0; c < E; ++c) kv[c] = vv[c] = 0.f;
+        for (int u = 0; u < UO; ++u) {
+            const int jj = key_of(it + u);
+            const bool valid = jj < ns;
+            fetch_seg<E>(ks + (size_t)(valid ? jj : 0) * D + c0, valid, kr[u]);
+            fetch_seg<E>(vh + (size_t)(j0 + (valid ? jj : 0)) * D + c0, valid, vr[u]);
         }
-        float t = 0.f;
+        float t[UO];
 #pragma unroll
-        for (int c = 0; c < E; ++c) t = fmaf(xv[c], kv[c], t);
-        t = group_sum(t);
-        const float u = valid ? wts[jj] * (c1 - t) : 0.f;
-        us += u;
+        for (int u = 0; u < UO; ++u) t[u] = dot_seg<E>(xv, kr[u]);
 #pragma unroll
-        for (int c = 0; c < E; ++c) acc[c] = fmaf(u, vv[c], acc[c]);
+        for (int u = 0; u < UO; ++u) t[u] = group_sum(t[u]);
+#pragma unroll
+        for (int u = 0; u < UO; ++u) {
+            const int jj = key_of(it + u);
+            if (jj >= ns) continue;
+            const float uj = wts[jj] * (c1 - t[u]);
+            us += uj;
+            float vv[E];
+            unpack_seg<E>(vr[u], vv);
+#pragma unroll
+            for (int c = 0; c < E; ++c) acc[c] = fmaf(uj, vv[c], acc[c]);
+        }
     }
 #pragma unroll
     for (int c = 0; c < E; ++c) sm.part[g][c0 + c] = acc[c];
@@ -795,10 +788,10 @@ cudaError_t launch_dec_cluster(const DecodeProblem& p, cudaStream_t stream) {
 
 // The cluster form reads K from HBM once but pays a cluster-wide exchange per pass; the streaming
 // form re-reads K every pass but keeps every SM busy with whole heads.  Measured on GB300 (bf16,
-// n = 4096, d = 128, 16 CG iterations), cluster vs streaming: 16 heads 0.21 vs 0.43 ms, 32 heads
-// 0.32 vs 0.44 ms, 48 heads 0.423 vs 0.437 ms, 64 heads 0.53 vs 0.44 ms, 128 heads 0.94 vs 0.67 ms.
-// The cluster form wins while there are too few heads to fill the GPU, up to about 48 heads.
-constexpr long long kClusterMaxHeads = 48;
+// n = 4096, d = 128, 16 CG iterations), cluster vs streaming: 16 heads 0.17 vs 0.43 ms, 32 heads
+// 0.26 vs 0.44 ms, 48 heads 0.34 vs 0.44 ms, 64 heads 0.43 vs 0.44 ms, 128 heads 0.75 vs 0.67 ms.
+// The cluster form wins while there are too few heads to fill the GPU, up to about 64 heads.
+constexpr long long kClusterMaxHeads = 64;
 
 template <int D, typename T>
 cudaError_t launch_dec_pick(const DecodeProblem& p, cudaStream_t stream) {

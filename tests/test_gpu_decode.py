@@ -72,7 +72,7 @@ def test_decode_converged_matches_exact_solve(lla_gpu, dtype, d, n):
 @pytest.mark.parametrize("dtype,n,B", [("bf16", 8000, 1), ("fp32", 4000, 1), ("bf16", 600, 50)])
 def test_decode_streaming_form(lla_gpu, dtype, n, B):
     """The streaming form (K re-read every pass) serves caches too long for an eighth to sit in a
-    CTA's shared memory, and batches of more than 48 heads; the cluster form the rest.  Both
+    CTA's shared memory, and batches of more than 64 heads; the cluster form the rest.  Both
     meet the same gate."""
     w = workload("lm_bf16", B=B, H=3, n=n, d=128, dtype=dtype, tau=1.0 / math.sqrt(128), cg_max_iters=576,
                  cg_tol=1e-6)
