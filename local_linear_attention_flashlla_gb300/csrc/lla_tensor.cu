@@ -1163,7 +1163,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             publish_p(SW_END);
         } else {
             // ---------------- finalise rho, denom; R = rho' (hi + lo) for the output sweep ----------------
-            // x and kbar in registers, loaded in one batch; x through L2 (.cg), where its reductions landed
+            // x and kbar in registers, loaded in one batch (x from this thread's own scratch)
             float xv[DH], kv[DH];
             const bool have_x = row_ok && cg_sweeps > 0;   // no sweep ran: x = 0
 #pragma unroll
