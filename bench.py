@@ -622,22 +622,23 @@ def run_backward(args, world, rank, local):
     dominant_is_stats = q_ms >= k_ms
     roof = stats_roof if dominant_is_stats else rest_roof
 
+    # end to end through the C-ABI host-buffer call (lla_backward_host: chunked copies in and out
+    # overlapped with the compute), from and into pinned host buffers
     e2e = None
     if not args.no_e2e:
         hin = [t.pin_memory() for t in (*qkv_host, g_host)] + [rho.cpu().pin_memory(), den.cpu().pin_memory()]
         hout = [torch.empty(q.shape, dtype=torch.float32).pin_memory() for _ in range(3)]
-        din = [torch.empty_like(t, device=dev) for t in hin]
+        dtype_c = lla.LLA_DTYPE_BF16 if q.dtype == torch.bfloat16 else lla.LLA_DTYPE_FP32
+        hbuf = torch.empty(lla.lla_backward_host_buffer_size(dtype_c, path, w.B, w.H, w.n, w.d, 0),
+                           dtype=torch.uint8, device=dev)
         e2e_ms = []
         for it in range(args.warmup + args.steps):
             flush.zero_()
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            for d_, h_ in zip(din, hin):
-                d_.copy_(h_, non_blocking=True)
-            step(din[0], din[1], din[2], din[4], din[5], din[3])
-            for h_, d_ in zip(hout, grads):
-                h_.copy_(d_, non_blocking=True)
+            lla.backward_host(hin[0], hin[1], hin[2], hin[4], hin[5], hin[3], w.tau, w.lam, T, w.cg_tol, path=path,
+                              dq=hout[0], dk=hout[1], dv=hout[2], device_buffer=hbuf)
             e1.record(stream)
             e1.synchronize()
             if it >= args.warmup:

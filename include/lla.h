@@ -274,6 +274,26 @@ int lla_backward(int dtype, int path, const void* q, const void* k, const void* 
  * vectors y and, on the tensor path, the fp16 operand copies and CG scratch). */
 size_t lla_backward_workspace_size(int dtype, int path, int B, int H, int n, int d);
 
+/*
+ * lla_backward_host -- lla_backward with q, k, v, dout, rho, denom read from HOST memory and dq,
+ * dk, dv (and cg_iters) written to HOST memory, the transfers overlapped with the computation,
+ * exactly as lla_forward_host does for the forward: chunks of chunk_slices (b, h) slices (0:
+ * ceil(B*H/8)) on the two library streams, each chunk's result that of lla_backward on its slices
+ * (B = its slice count, H = 1; the tensor path chooses its operand scales per chunk), `stream`
+ * ordered before and after, host buffers valid until `stream` has passed the call, pinned memory
+ * for asynchronous copies.  device_buffer: NULL (stream-ordered pool) or
+ * lla_backward_host_buffer_size(...) bytes, 256-byte aligned.  Errors as for lla_backward, plus
+ * LLA_ERR_INVALID_ARG for chunk_slices < 0 or a device buffer too small or misaligned.  Not for
+ * concurrent use from several host threads (the library streams are shared).
+ */
+int lla_backward_host(int dtype, int path, const void* q, const void* k, const void* v, const float* rho,
+                      const float* denom, const void* dout, float* dq, float* dk, float* dv, int* cg_iters,
+                      int B, int H, int n, int d, float tau, float lambda, int cg_max_iters, float cg_tol,
+                      int chunk_slices, void* device_buffer, size_t device_buffer_bytes, void* stream);
+
+/* Bytes of device buffer lla_backward_host needs for these arguments (0 for invalid ones). */
+size_t lla_backward_host_buffer_size(int dtype, int path, int B, int H, int n, int d, int chunk_slices);
+
 /* Message for the calling thread's most recent failure ("" if none). Owned by the library. */
 const char* lla_last_error(void);
 

@@ -19,6 +19,7 @@ __all__ = [
     "lla_version",
     "lla_profile_enable", "lla_profile_read", "lla_forward_noalloc", "lla_parallax_forward", "parallax_forward",
     "lla_decode", "lla_decode_max_n", "decode", "lla_backward", "lla_backward_workspace_size", "backward",
+    "lla_backward_host", "lla_backward_host_buffer_size", "backward_host",
     "LLA_OK", "LLA_ERR_INVALID_ARG", "LLA_ERR_UNSUPPORTED", "LLA_ERR_CUDA", "LLA_ERR_DEVICE_TIMEOUT",
     "LLA_DTYPE_BF16", "LLA_DTYPE_FP32", "LLA_PATH_AUTO", "LLA_PATH_TENSOR", "LLA_PATH_FP32",
     "EXPORTED_SYMBOLS",
@@ -57,6 +58,9 @@ _SIGNATURES = {
     "lla_backward": (_c_int, [_c_int, _c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int,
                               _c_int, _c_int, _c_float, _c_float, _c_int, _c_float, _vp, _c_size, _vp]),
     "lla_backward_workspace_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
+    "lla_backward_host": (_c_int, [_c_int, _c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int,
+                                   _c_int, _c_int, _c_float, _c_float, _c_int, _c_float, _c_int, _vp, _c_size, _vp]),
+    "lla_backward_host_buffer_size": (_c_size, [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int]),
     "lla_profile_enable": (_c_int, [_c_int]),
     "lla_profile_read": (_c_int, [ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]),
     "lla_version": (_c_int, []),
@@ -268,6 +272,61 @@ def backward(q, k, v, rho, denom, dout, tau, lam, cg_max_iters, cg_tol=0.0, *, p
                  grads[0].data_ptr(), grads[1].data_ptr(), grads[2].data_ptr(),
                  None if iters is None else iters.data_ptr(), B, H, n, d, float(tau), float(lam), int(cg_max_iters),
                  float(cg_tol), ws_ptr, ws_bytes, _stream_ptr(stream))
+    if return_iters:
+        return (*grads, iters)
+    return tuple(grads)
+
+
+def lla_backward_host(dtype, path, q_ptr, k_ptr, v_ptr, rho_ptr, denom_ptr, dout_ptr, dq_ptr, dk_ptr, dv_ptr,
+                      iters_ptr, B, H, n, d, tau, lam, cg_max_iters, cg_tol, chunk_slices, buf_ptr, buf_bytes,
+                      stream_ptr):
+    """Raw host-buffer backward entry point (host addresses; buf_ptr a device one)."""
+    _check(load_library().lla_backward_host(dtype, path, q_ptr, k_ptr, v_ptr, rho_ptr, denom_ptr, dout_ptr, dq_ptr,
+                                            dk_ptr, dv_ptr, iters_ptr, B, H, n, d, tau, lam, cg_max_iters, cg_tol,
+                                            chunk_slices, buf_ptr, buf_bytes, stream_ptr))
+
+
+def lla_backward_host_buffer_size(dtype, path, B, H, n, d, chunk_slices=0):
+    return load_library().lla_backward_host_buffer_size(dtype, path, B, H, n, d, chunk_slices)
+
+
+def backward_host(q, k, v, rho, denom, dout, tau, lam, cg_max_iters, cg_tol=0.0, *, path=LLA_PATH_AUTO,
+                  chunk_slices=0, return_iters=False, dq=None, dk=None, dv=None, device_buffer=None, stream=None):
+    """backward() on CPU tensors (pin them for overlapped copies): q, k, v, dout [B, H, n, d] bf16 or
+    fp32, rho [B, H, n, d] and denom [B, H, n] fp32.  Returns CPU fp32 dq, dk, dv (pinned unless
+    passed in).  Asynchronous on the current (or given) stream: synchronise before reading."""
+    import torch
+    ins = (q, k, v, dout, rho, denom)
+    if any(t.is_cuda for t in ins):
+        raise LLAError(LLA_ERR_INVALID_ARG, "backward_host takes CPU tensors; use backward() for CUDA tensors")
+    if q.dim() != 4 or any(tuple(t.shape) != tuple(q.shape) for t in (k, v, dout, rho)):
+        raise LLAError(LLA_ERR_INVALID_ARG, "q, k, v, dout, rho must share one [B, H, n, d] shape")
+    B, H, n, d = q.shape
+    if tuple(denom.shape) != (B, H, n) or rho.dtype != torch.float32 or denom.dtype != torch.float32:
+        raise LLAError(LLA_ERR_INVALID_ARG, "rho [B, H, n, d] and denom [B, H, n] must be fp32")
+    if not (q.dtype == k.dtype == v.dtype == dout.dtype) or q.dtype not in (torch.bfloat16, torch.float32):
+        raise LLAError(LLA_ERR_INVALID_ARG, "q, k, v, dout must all be bf16 or all fp32")
+    if not all(t.is_contiguous() for t in ins):
+        raise LLAError(LLA_ERR_INVALID_ARG, "inputs must be contiguous (a copy would not stay alive for the call)")
+    dtype = LLA_DTYPE_BF16 if q.dtype == torch.bfloat16 else LLA_DTYPE_FP32
+    grads = []
+    for t in (dq, dk, dv):
+        if t is None:
+            t = torch.empty((B, H, n, d), dtype=torch.float32).pin_memory()
+        elif t.is_cuda or tuple(t.shape) != (B, H, n, d) or t.dtype != torch.float32 or not t.is_contiguous():
+            raise LLAError(LLA_ERR_INVALID_ARG, "gradient outputs must be contiguous CPU fp32 [B, H, n, d] tensors")
+        grads.append(t)
+    iters = torch.empty((B, H, n), dtype=torch.int32).pin_memory() if return_iters else None
+    if device_buffer is None:
+        buf_ptr, buf_bytes = None, 0
+    else:
+        if not device_buffer.is_cuda:
+            raise LLAError(LLA_ERR_INVALID_ARG, "device_buffer must be a CUDA tensor")
+        buf_ptr, buf_bytes = device_buffer.data_ptr(), device_buffer.numel() * device_buffer.element_size()
+    lla_backward_host(dtype, path, q.data_ptr(), k.data_ptr(), v.data_ptr(), rho.data_ptr(), denom.data_ptr(),
+                      dout.data_ptr(), grads[0].data_ptr(), grads[1].data_ptr(), grads[2].data_ptr(),
+                      None if iters is None else iters.data_ptr(), B, H, n, d, float(tau), float(lam),
+                      int(cg_max_iters), float(cg_tol), int(chunk_slices), buf_ptr, buf_bytes, _stream_ptr(stream))
     if return_iters:
         return (*grads, iters)
     return tuple(grads)

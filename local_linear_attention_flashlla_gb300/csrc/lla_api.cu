@@ -158,6 +158,14 @@ static int check_forward_args(int dtype, int path, int B, int H, int n, int d, f
     return LLA_OK;
 }
 
+// Scalar and shape checks of the backward entry points (pointers are checked by each).
+static int check_backward_args(int dtype, int path, int B, int H, int n, int d, float tau, float lambda,
+                               int cg_max_iters, float cg_tol, int* rpath_out) {
+    if (B < 1 || H < 1 || n < 1) return fail(LLA_ERR_INVALID_ARG, "B, H, n must be >= 1 (got %d, %d, %d)", B, H, n);
+    if ((long long)B * H > 65535LL) return fail(LLA_ERR_INVALID_ARG, "B*H must be <= 65535");
+    return check_forward_args(dtype, path, B, H, n, d, tau, lambda, cg_max_iters, cg_tol, rpath_out);
+}
+
 // ---------------------------------------------------------------------------------------------
 // Host-buffer forward: the (b, h) slices go through the device in chunks, on two library streams
 // (chunk c on stream c % 2, with its own half of the device buffer), so chunk c's copy in runs
@@ -193,6 +201,20 @@ struct HostChunk {
         tden = a256((size_t)C * n * 4);
         ws = rpath == LLA_PATH_TENSOR ? a256(tensor_workspace_bytes(C, 1, n, d)) : 0;
         half = 4 * tin + trho + 2 * tden + ws;
+    }
+};
+
+// The backward's half of the device buffer: q, k, v, dout (dtype), rho, dq, dk, dv (fp32),
+// denom and cg_iters, and the backward workspace of a chunk of C slices.
+struct HostBwdChunk {
+    size_t tin, tf, tden, ws, half;
+    HostBwdChunk(int dtype, int rpath, int C, int n, int d) {
+        const size_t es = dtype == LLA_DTYPE_BF16 ? 2 : 4;
+        tin = a256((size_t)C * n * d * es);
+        tf = a256((size_t)C * n * d * 4);
+        tden = a256((size_t)C * n * 4);
+        ws = a256(backward_workspace_bytes(rpath, C, 1, n, d));
+        half = 4 * tin + 4 * tf + 2 * tden + ws;
     }
 };
 
@@ -465,20 +487,9 @@ int lla_backward(int dtype, int path, const void* q, const void* k, const void* 
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(rho) || !aligned16(denom) ||
         !aligned16(dout) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
         return fail(LLA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
-    if (B < 1 || H < 1 || n < 1) return fail(LLA_ERR_INVALID_ARG, "B, H, n must be >= 1 (got %d, %d, %d)", B, H, n);
-    if ((long long)B * H > 65535LL) return fail(LLA_ERR_INVALID_ARG, "B*H must be <= 65535");
-    if ((long long)B * H * n * d > (1LL << 40)) return fail(LLA_ERR_INVALID_ARG, "problem too large");
-    if (d != 16 && d != 32 && d != 64 && d != 128)
-        return fail(LLA_ERR_INVALID_ARG, "head dim d must be 16, 32, 64 or 128 (got %d)", d);
-    if (!(tau > 0.f) || !(tau < 1e30f)) return fail(LLA_ERR_INVALID_ARG, "tau must be finite and > 0");
-    if (!(lambda > 0.f) || !(lambda < 1e30f)) return fail(LLA_ERR_INVALID_ARG, "lambda must be finite and > 0");
-    if (cg_max_iters < 1 || cg_max_iters > 4096) return fail(LLA_ERR_INVALID_ARG, "cg_max_iters must be in [1, 4096]");
-    if (!(cg_tol >= 0.f) || !(cg_tol < 1e30f)) return fail(LLA_ERR_INVALID_ARG, "cg_tol must be finite and >= 0");
-    if (dtype != LLA_DTYPE_BF16 && dtype != LLA_DTYPE_FP32) return fail(LLA_ERR_INVALID_ARG, "unknown dtype %d", dtype);
-    if (path < LLA_PATH_AUTO || path > LLA_PATH_FP32) return fail(LLA_ERR_INVALID_ARG, "unknown path %d", path);
-    const int rpath = lla_resolve_path(dtype, path, d);
-    if (rpath == LLA_PATH_TENSOR && (dtype != LLA_DTYPE_BF16 || (d != 64 && d != 128)))
-        return fail(LLA_ERR_UNSUPPORTED, "tensor path needs bf16 inputs and d in {64, 128}");
+    int rpath = 0;
+    const int st = lla::check_backward_args(dtype, path, B, H, n, d, tau, lambda, cg_max_iters, cg_tol, &rpath);
+    if (st != LLA_OK) return st;
     const size_t need = lla::backward_workspace_bytes(rpath, B, H, n, d);
     if (workspace) {
         if (workspace_bytes < need)
@@ -518,6 +529,100 @@ int lla_backward(int dtype, int path, const void* q, const void* k, const void* 
         lla::g_prof_valid = true;
     }
     return LLA_OK;
+}
+
+size_t lla_backward_host_buffer_size(int dtype, int path, int B, int H, int n, int d, int chunk_slices) {
+    int rpath = 0;
+    if (lla::check_backward_args(dtype, path, B, H, n, d, 1.f, 1.f, 1, 0.f, &rpath) != LLA_OK || chunk_slices < 0)
+        return 0;
+    const int C = lla::host_chunk_slices(B * H, chunk_slices);
+    return 2 * lla::HostBwdChunk(dtype, rpath, C, n, d).half;
+}
+
+int lla_backward_host(int dtype, int path, const void* q, const void* k, const void* v, const float* rho,
+                      const float* denom, const void* dout, float* dq, float* dk, float* dv, int* cg_iters, int B,
+                      int H, int n, int d, float tau, float lambda, int cg_max_iters, float cg_tol, int chunk_slices,
+                      void* device_buffer, size_t device_buffer_bytes, void* stream_) {
+    lla::g_msg[0] = '\0';
+    if (!q || !k || !v || !rho || !denom || !dout || !dq || !dk || !dv) return fail(LLA_ERR_INVALID_ARG, "null host pointer");
+    int rpath = 0;
+    int st = lla::check_backward_args(dtype, path, B, H, n, d, tau, lambda, cg_max_iters, cg_tol, &rpath);
+    if (st != LLA_OK) return st;
+    if (chunk_slices < 0) return fail(LLA_ERR_INVALID_ARG, "chunk_slices must be >= 0 (0: automatic)");
+    const int S = B * H;
+    const int C = lla::host_chunk_slices(S, chunk_slices);
+    const lla::HostBwdChunk hc(dtype, rpath, C, n, d);
+    const size_t need = 2 * hc.half;
+    if (device_buffer) {
+        if (device_buffer_bytes < need)
+            return fail(LLA_ERR_INVALID_ARG, "device buffer too small: %zu < %zu bytes", device_buffer_bytes, need);
+        if ((reinterpret_cast<uintptr_t>(device_buffer) & 255u) != 0)
+            return fail(LLA_ERR_INVALID_ARG, "device buffer must be 256-byte aligned");
+    }
+    if ((st = lla::host_streams()) != LLA_OK) return st;
+
+    cudaStream_t cs = static_cast<cudaStream_t>(stream_);
+    unsigned char* buf = static_cast<unsigned char*>(device_buffer);
+    cudaError_t e = cudaSuccess;
+    if (!buf && (e = cudaMallocAsync(reinterpret_cast<void**>(&buf), need, cs)) != cudaSuccess)
+        return lla::cuda_fail(e, "cudaMallocAsync(host-backward buffer)");
+    if ((e = cudaEventRecord(lla::g_he[0], cs)) != cudaSuccess) return lla::cuda_fail(e, "host backward: event record");
+    for (int i = 0; i < 2; ++i)
+        if ((e = cudaStreamWaitEvent(lla::g_hs[i], lla::g_he[0], 0)) != cudaSuccess)
+            return lla::cuda_fail(e, "host backward: stream wait");
+
+    const size_t es = dtype == LLA_DTYPE_BF16 ? 2 : 4;
+    const unsigned char* hin[4] = {static_cast<const unsigned char*>(q), static_cast<const unsigned char*>(k),
+                                   static_cast<const unsigned char*>(v), static_cast<const unsigned char*>(dout)};
+    float* hout[3] = {dq, dk, dv};
+    int rc = LLA_OK;
+    for (int c = 0, s0 = 0; s0 < S && rc == LLA_OK; ++c, s0 += C) {
+        const int cnt = S - s0 < C ? S - s0 : C;
+        cudaStream_t sc = lla::g_hs[c & 1];
+        unsigned char* base = buf + (size_t)(c & 1) * hc.half;
+        unsigned char* din[4] = {base, base + hc.tin, base + 2 * hc.tin, base + 3 * hc.tin};
+        float* drho = reinterpret_cast<float*>(base + 4 * hc.tin);
+        float* dg[3] = {reinterpret_cast<float*>(base + 4 * hc.tin + hc.tf),
+                        reinterpret_cast<float*>(base + 4 * hc.tin + 2 * hc.tf),
+                        reinterpret_cast<float*>(base + 4 * hc.tin + 3 * hc.tf)};
+        float* dden = reinterpret_cast<float*>(base + 4 * hc.tin + 4 * hc.tf);
+        int* dits = reinterpret_cast<int*>(base + 4 * hc.tin + 4 * hc.tf + hc.tden);
+        void* dws = base + 4 * hc.tin + 4 * hc.tf + 2 * hc.tden;
+        const size_t tbytes = (size_t)cnt * n * d * es, off = (size_t)s0 * n * d * es;
+        const size_t fbytes = (size_t)cnt * n * d * 4, foff = (size_t)s0 * n * d;
+        const size_t dbytes = (size_t)cnt * n * 4, doff = (size_t)s0 * n;
+        for (int t = 0; t < 4 && rc == LLA_OK; ++t)
+            if ((e = cudaMemcpyAsync(din[t], hin[t] + off, tbytes, cudaMemcpyHostToDevice, sc)) != cudaSuccess)
+                rc = lla::cuda_fail(e, "host backward: copy in");
+        if (rc == LLA_OK && ((e = cudaMemcpyAsync(drho, rho + foff, fbytes, cudaMemcpyHostToDevice, sc)) != cudaSuccess ||
+                             (e = cudaMemcpyAsync(dden, denom + doff, dbytes, cudaMemcpyHostToDevice, sc)) != cudaSuccess))
+            rc = lla::cuda_fail(e, "host backward: copy in");
+        if (rc != LLA_OK) break;
+        lla::BackwardProblem p{din[0], din[1], din[2], din[3], drho, dden, dg[0], dg[1], dg[2],
+                               cg_iters ? dits : nullptr, cnt, 1, n, d, tau, lambda, cg_max_iters, cg_tol, dtype,
+                               nullptr, nullptr};
+        const char* why = nullptr;
+        if ((e = lla::launch_backward(p, rpath, dws, sc, &why)) != cudaSuccess) {
+            rc = lla::cuda_fail(e, why ? why : "host backward: launch");
+            break;
+        }
+        for (int t = 0; t < 3 && rc == LLA_OK; ++t)
+            if ((e = cudaMemcpyAsync(hout[t] + foff, dg[t], fbytes, cudaMemcpyDeviceToHost, sc)) != cudaSuccess)
+                rc = lla::cuda_fail(e, "host backward: copy out");
+        if (rc == LLA_OK && cg_iters &&
+            (e = cudaMemcpyAsync(cg_iters + doff, dits, dbytes, cudaMemcpyDeviceToHost, sc)) != cudaSuccess)
+            rc = lla::cuda_fail(e, "host backward: copy out");
+    }
+    for (int i = 0; i < 2; ++i) {
+        cudaError_t e1 = cudaEventRecord(lla::g_he[1 + i], lla::g_hs[i]);
+        if (e1 == cudaSuccess) e1 = cudaStreamWaitEvent(cs, lla::g_he[1 + i], 0);
+        if (e1 != cudaSuccess && rc == LLA_OK) rc = lla::cuda_fail(e1, "host backward: join");
+    }
+    if (!device_buffer) {
+        cudaError_t e2 = cudaFreeAsync(buf, cs);
+        if (e2 != cudaSuccess && rc == LLA_OK) rc = lla::cuda_fail(e2, "cudaFreeAsync(host-backward buffer)");
+    }
+    return rc;
 }
 
 int lla_decode_max_n(int d) {

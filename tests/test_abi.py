@@ -229,3 +229,40 @@ def test_host_binding_refuses_non_contiguous_inputs():
     x = torch.zeros(1, 1, 8, 32)[..., ::2]
     with pytest.raises(lla.LLAError):
         lla.forward_host(x, x, x, 0.25, 0.1, 4)
+
+
+def _call_bwd_host(lib, **kw):
+    a = dict(dtype=0, path=0, q=16, k=32, v=48, rho=64, den=80, g=96, dq=112, dk=128, dv=144, it=None, B=1, H=1, n=8,
+             d=64, tau=0.1, lam=1.0, T=4, tol=0.0, chunk=0, buf=None, bufb=0, stream=None)
+    a.update(kw)
+    return lib.lla_backward_host(a["dtype"], a["path"], a["q"], a["k"], a["v"], a["rho"], a["den"], a["g"], a["dq"],
+                                 a["dk"], a["dv"], a["it"], a["B"], a["H"], a["n"], a["d"], a["tau"], a["lam"], a["T"],
+                                 a["tol"], a["chunk"], a["buf"], a["bufb"], a["stream"])
+
+
+@pytest.mark.parametrize("bad", [
+    dict(q=None), dict(g=None), dict(rho=None), dict(den=None), dict(dq=None), dict(dv=None), dict(B=0), dict(n=0),
+    dict(B=70000), dict(d=48), dict(tau=0.0), dict(lam=float("nan")), dict(T=0), dict(tol=-1.0), dict(dtype=7),
+    dict(path=9), dict(chunk=-1), dict(buf=256, bufb=16), dict(buf=257, bufb=1 << 40),
+])
+def test_backward_host_invalid_arguments_rejected_before_launch(lib, bad):
+    assert _call_bwd_host(lib, **bad) == lla.LLA_ERR_INVALID_ARG
+    assert lib.lla_last_error().decode()
+
+
+def test_backward_host_buffer_size(lib):
+    """Two halves, each holding one chunk's q, k, v, dout, rho, dq, dk, dv, denom, cg_iters (each
+    rounded up to 256 bytes) and the chunk's backward workspace."""
+    def a256(x):
+        return (x + 255) & ~255
+
+    def expect(dtype, path, C, n, d):
+        es = 2 if dtype == lla.LLA_DTYPE_BF16 else 4
+        ws = lib.lla_backward_workspace_size(dtype, path, C, 1, n, d)
+        return 2 * (4 * a256(C * n * d * es) + 4 * a256(C * n * d * 4) + 2 * a256(C * n * 4) + a256(ws))
+
+    bf, f32, ten, fp = lla.LLA_DTYPE_BF16, lla.LLA_DTYPE_FP32, lla.LLA_PATH_TENSOR, lla.LLA_PATH_FP32
+    assert lib.lla_backward_host_buffer_size(bf, ten, 8, 16, 256, 128, 0) == expect(bf, ten, 16, 256, 128)
+    assert lib.lla_backward_host_buffer_size(f32, fp, 1, 3, 100, 32, 0) == expect(f32, fp, 1, 100, 32)
+    assert lib.lla_backward_host_buffer_size(bf, ten, 2, 4, 300, 64, 3) == expect(bf, ten, 3, 300, 64)
+    assert lib.lla_backward_host_buffer_size(bf, ten, 2, 4, 300, 64, -1) == 0

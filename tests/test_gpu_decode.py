@@ -118,6 +118,33 @@ def test_decode_at_the_lm_cap_matches_the_same_cg(lla_gpu):
     assert (res[3].numpy() == 16).all()
 
 
+def test_decode_full_size_sampled(lla_gpu):
+    """The benchmark's decode configuration, in the launch the benchmark times (64 sequences x 16
+    heads = 1024 heads: the streaming form), against the float64 centred CG with the same cap T = 16
+    on sampled heads (first, last and six drawn with a fixed seed)."""
+    w = workload("decode_bf16")
+    q, k, v = make_inputs(w)
+    n = w.n
+    dev = torch.device("cuda:0")
+    res = lla.decode(q[:, :, n - 1].contiguous().to(dev), k.to(dev), v.to(dev), n, w.tau, w.lam, w.cg_max_iters,
+                     w.cg_tol, return_iters=True)
+    torch.cuda.synchronize()
+    lla.lla_sync_status()
+    out, rho, den, its = (t.cpu() for t in res)
+    assert (its == w.cg_max_iters).all()
+    assert torch.isfinite(out.float()).all() and torch.isfinite(rho).all() and (den > 0).all()
+    rng = np.random.default_rng(11)
+    heads = [(0, 0), (w.B - 1, w.H - 1)] + [(int(b), int(h)) for b, h in
+                                             zip(rng.integers(0, w.B, 6), rng.integers(0, w.H, 6))]
+    rms_v = math.sqrt(float(v[:2].double().pow(2).mean()))
+    for b, h in heads:
+        qi = q[b, h, n - 1].double().numpy()
+        K, V = k[b, h].double().numpy(), v[b, h].double().numpy()
+        r = lla_row_deflated_cg(qi, K, V, w.tau, w.lam, w.cg_max_iters, 0.0)
+        diff = np.abs(out[b, h].double().numpy() - r["out"])
+        assert (diff <= 2.0 ** -8 * np.abs(r["out"]) + 1e-3 * rms_v).all(), f"{(b, h)}: {diff.max() / rms_v:.3e}"
+
+
 def test_decode_equals_forward_last_row(lla_gpu):
     """The step is the forward pass's row n-1: both fp32 GPU paths, same T, same inputs."""
     w = workload("lm_bf16", B=2, H=2, n=500, d=64, tau=0.125, cg_max_iters=200, cg_tol=1e-6)
