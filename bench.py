@@ -289,6 +289,29 @@ def dist_setup(args):
     return world, rank, local
 
 
+def ranks_max(value, device):
+    """The largest of a float over the ranks (the slowest rank's time); the value itself with one
+    process.  device: where the reduction tensor lives (a CUDA device under NCCL, "cpu" under gloo)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world, units_per_rank_step, steps, total_ms):
+    """Whole-job units per second: every rank processes units_per_rank_step per step (weak scaling),
+    timed by the slowest rank's total_ms."""
+    return world * units_per_rank_step * steps / (total_ms / 1e3)
+
+
+def rank_workload(w, rank):
+    """Each rank draws its own inputs (seed + rank) for the same workload shape."""
+    return w.with_(seed=w.seed + rank)
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return
@@ -412,7 +435,7 @@ def run_decode(args, world, rank, local):
     torch.cuda.set_device(dev)
     name = args.workload if args.workload != "lm_bf16" else "decode_bf16"
     w = workload(name) if args.batch is None else workload(name, B=args.batch)
-    q, k, v = make_inputs(w.with_(seed=w.seed + rank))
+    q, k, v = make_inputs(rank_workload(w, rank))
     qd_host = q[:, :, w.n - 1].contiguous()
     qd, kc, vc = qd_host.to(dev), k.to(dev), v.to(dev)
     del q
@@ -454,12 +477,9 @@ def run_decode(args, world, rank, local):
     lla.lla_profile_enable(False)
     lla.lla_sync_status()
     total_ms = sum(times)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = ranks_max(total_ms, dev)
     ms_per_step = total_ms / args.steps
-    value = world * w.B * args.steps / (total_ms / 1e3)
+    value = job_throughput(world, w.B, args.steps, total_ms)
     comp, method = decode_bytes(w, T)
     kern_ms = sum(main_times) / len(main_times)
     peaks, peak_kind = load_peaks()
@@ -489,11 +509,8 @@ def run_decode(args, world, rank, local):
             if it >= args.warmup:
                 e2e_ms.append(e0.elapsed_time(e1))
         tot = sum(e2e_ms)
-        if world > 1:
-            t = torch.tensor([tot], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            tot = float(t.item())
-        e2e = {"value": world * w.B * len(e2e_ms) / (tot / 1e3), "unit": "tokens/s",
+        tot = ranks_max(tot, dev)
+        e2e = {"value": job_throughput(world, w.B, len(e2e_ms), tot), "unit": "tokens/s",
                "h2d_bytes_per_step": hq.numel() * hq.element_size(),
                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in (ho, hr, hd))}
 
@@ -533,7 +550,7 @@ def run_backward(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = workload(args.workload) if args.batch is None else workload(args.workload, B=args.batch)
-    wr = w.with_(seed=w.seed + rank)
+    wr = rank_workload(w, rank)
     qkv_host = make_inputs(wr)
     g_host = make_cotangent(wr)
     q, k, v = (t.to(dev) for t in qkv_host)
@@ -581,13 +598,10 @@ def run_backward(args, world, rank, local):
     lla.lla_profile_enable(False)
     lla.lla_sync_status()
     total_ms = sum(times)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = ranks_max(total_ms, dev)
     ms_per_step = total_ms / args.steps
     tokens = w.B * w.n
-    value = world * tokens * args.steps / (total_ms / 1e3)
+    value = job_throughput(world, tokens, args.steps, total_ms)
     flops = backward_useful_flops(w, T)
     q_ms = sum(m for m, _ in main_times) / len(main_times)          # stats kernel (moments and adjoint CG)
     call_ms = sum(t_ for _, t_ in main_times) / len(main_times)     # the whole call
@@ -644,11 +658,8 @@ def run_backward(args, world, rank, local):
             if it >= args.warmup:
                 e2e_ms.append(e0.elapsed_time(e1))
         tot = sum(e2e_ms)
-        if world > 1:
-            t = torch.tensor([tot], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            tot = float(t.item())
-        e2e = {"value": world * tokens * len(e2e_ms) / (tot / 1e3), "unit": "tokens/s",
+        tot = ranks_max(tot, dev)
+        e2e = {"value": job_throughput(world, tokens, len(e2e_ms), tot), "unit": "tokens/s",
                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout)}
 
@@ -703,10 +714,10 @@ def main():
     path = {"auto": lla.LLA_PATH_AUTO, "tensor": lla.LLA_PATH_TENSOR, "fp32": lla.LLA_PATH_FP32}[args.path]
     dtype_code = lla.LLA_DTYPE_BF16 if w.dtype == "bf16" else lla.LLA_DTYPE_FP32
     rpath = lla.lla_resolve_path(dtype_code, path, w.d)
-    qkv_host = make_inputs(w.with_(seed=w.seed + rank))
+    qkv_host = make_inputs(rank_workload(w, rank))
     q, k, v = (t.to(dev) for t in qkv_host)
     parallax = args.op == "parallax"
-    probe_host = make_probe(w.with_(seed=w.seed + rank)) if parallax else None
+    probe_host = make_probe(rank_workload(w, rank)) if parallax else None
     probe = probe_host.to(dev) if parallax else None
     out = torch.empty_like(q)
     rho = torch.empty(q.shape, dtype=torch.float32, device=dev)
@@ -752,13 +763,10 @@ def main():
     lla.lla_profile_enable(False)
     lla.lla_sync_status()
     total_ms = sum(times)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = ranks_max(total_ms, dev)
     ms_per_step = total_ms / args.steps
     tokens = w.B * w.n
-    value = world * tokens * args.steps / (total_ms / 1e3)
+    value = job_throughput(world, tokens, args.steps, total_ms)
     T = w.cg_max_iters if (w.cg_tol == 0 or parallax) else None
     if T is None:   # tolerance-driven: count the executed iterations
         _, _, _, its = lla.forward(q, k, v, w.tau, w.lam, w.cg_max_iters, w.cg_tol, path=path, return_iters=True)
@@ -804,11 +812,8 @@ def main():
             if it >= args.warmup:
                 e2e_ms.append(e0.elapsed_time(e1))
         tot = sum(e2e_ms)
-        if world > 1:
-            t = torch.tensor([tot], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            tot = float(t.item())
-        e2e = {"value": world * tokens * len(e2e_ms) / (tot / 1e3), "unit": "tokens/s",
+        tot = ranks_max(tot, dev)
+        e2e = {"value": job_throughput(world, tokens, len(e2e_ms), tot), "unit": "tokens/s",
                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in (hq, hk, hv) + ((hp,) if parallax else ())),
                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in ((ho,) if parallax else (ho, hr, hd)))}
 
