@@ -61,7 +61,8 @@ typedef enum {
  *
  * q, k, v   [B,H,n,d] bf16, read only.      out   [B,H,n,d] bf16, written.
  * rho       [B,H,n,d] fp32, written: rho_i.  denom [B,H,n] fp32, written: omega_i - mu_i.rho_i.
- * B, H, n >= 1; d in {16, 32, 64, 128}; tau > 0 (logit scale); lambda > 0 (ridge, absolute,
+ * B, H, n >= 1 with B*H <= 65535 (one grid row per (b, h) slice); d in {16, 32, 64, 128};
+ * tau > 0 (logit scale); lambda > 0 (ridge, absolute,
  * applied to the max-normalised weights); cg_max_iters >= 1; cg_tol >= 0: a query stops once
  * ||r|| <= cg_tol ||delta_i|| (cg_tol == 0: exactly cg_max_iters iterations).
  * Scratch (the tensor path's fp16 operand copies) is taken from the CUDA stream-ordered pool

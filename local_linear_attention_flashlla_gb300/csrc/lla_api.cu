@@ -140,7 +140,7 @@ static int run_problem(Problem& p, int rpath, void* workspace, size_t workspace_
 static int check_forward_args(int dtype, int path, int B, int H, int n, int d, float tau, float lambda,
                               int cg_max_iters, float cg_tol, int* rpath_out) {
     if (B < 1 || H < 1 || n < 1) return fail(LLA_ERR_INVALID_ARG, "B, H, n must be >= 1 (got %d, %d, %d)", B, H, n);
-    if ((long long)B * H > 65535LL * 1024) return fail(LLA_ERR_INVALID_ARG, "B*H too large");
+    if ((long long)B * H > 65535LL) return fail(LLA_ERR_INVALID_ARG, "B*H must be <= 65535 (one grid row per slice)");
     if ((long long)B * H * n * d > (1LL << 40)) return fail(LLA_ERR_INVALID_ARG, "problem too large");
     if (d != 16 && d != 32 && d != 64 && d != 128)
         return fail(LLA_ERR_INVALID_ARG, "head dim d must be 16, 32, 64 or 128 (got %d)", d);
@@ -410,7 +410,7 @@ int lla_parallax_forward(int dtype, int path, const void* q, const void* k, cons
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(probe) || !aligned16(out))
         return fail(LLA_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
     if (B < 1 || H < 1 || n < 1) return fail(LLA_ERR_INVALID_ARG, "B, H, n must be >= 1 (got %d, %d, %d)", B, H, n);
-    if ((long long)B * H > 65535LL * 1024) return fail(LLA_ERR_INVALID_ARG, "B*H too large");
+    if ((long long)B * H > 65535LL) return fail(LLA_ERR_INVALID_ARG, "B*H must be <= 65535 (one grid row per slice)");
     if ((long long)B * H * n * d > (1LL << 40)) return fail(LLA_ERR_INVALID_ARG, "problem too large");
     if (d != 16 && d != 32 && d != 64 && d != 128)
         return fail(LLA_ERR_INVALID_ARG, "head dim d must be 16, 32, 64 or 128 (got %d)", d);

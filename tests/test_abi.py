@@ -46,6 +46,7 @@ def _call_ex(lib, **kw):
 
 @pytest.mark.parametrize("bad", [
     dict(q=None), dict(out=None), dict(rho=None), dict(den=None), dict(q=17), dict(B=0), dict(n=0), dict(H=-1),
+    dict(B=65536), dict(B=256, H=256),
     dict(d=48), dict(d=256), dict(tau=0.0), dict(tau=-1.0), dict(tau=float("nan")), dict(lam=0.0),
     dict(lam=float("inf")), dict(T=0), dict(T=5000), dict(tol=-1.0), dict(dtype=7), dict(path=9),
 ])
@@ -85,7 +86,7 @@ def _call_parallax(lib, **kw):
 
 
 @pytest.mark.parametrize("bad", [
-    dict(q=None), dict(probe=None), dict(out=None), dict(probe=20), dict(B=0), dict(n=0), dict(d=48),
+    dict(q=None), dict(probe=None), dict(out=None), dict(probe=20), dict(B=0), dict(n=0), dict(d=48), dict(B=65536),
     dict(tau=0.0), dict(tau=float("nan")), dict(dtype=5), dict(path=-1),
 ])
 def test_parallax_invalid_arguments_rejected_before_launch(lib, bad):
