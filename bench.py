@@ -251,7 +251,7 @@ def cpu_oracle_throughput(w, qkv, budget_s=15.0, seed=123, op="lla", probe=None)
     t0 = time.perf_counter()
     _oracle_row(op, q, k, v, pr, w.tau, w.lam, 0, 0, i_mid)
     per_row = max(time.perf_counter() - t0, 1e-4)
-    n_rows = int(max(cores * 2, min(4096, budget_s * cores / per_row)))
+    n_rows = int(max(cores * 2, min(200000, budget_s * cores / per_row)))
     rows = [(int(rng.integers(len(heads))), 0, int(rng.integers(w.n))) for _ in range(n_rows)]
     chunks = [rows[c::cores] for c in range(cores)]
     ctx = mp.get_context("spawn")
@@ -418,7 +418,7 @@ def decode_cpu_baseline(w, qd, k, v, budget_s=12.0, seed=7):
     t0 = time.perf_counter()
     lla_row(qn[0, 0], kn[0, 0], vn[0, 0], w.tau, w.lam)
     per = max(time.perf_counter() - t0, 1e-4)
-    count = int(max(cores, min(w.B * w.H, 8 * cores, budget_s * cores / per)))
+    count = int(max(cores, min(100000, budget_s * cores / per)))
     rows = [(int(rng.integers(len(heads))), 0) for _ in range(count)]
     with mp.get_context("spawn").Pool(cores, initializer=_pool_init, initargs=((qn, kn, vn, w.tau, w.lam),)) as pool:
         pool.map(_pool_warm, range(cores), chunksize=1)       # every worker started, inputs received
