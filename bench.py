@@ -225,7 +225,7 @@ def _oracle_rows_worker(rows):
     return out, start, time.time()
 
 
-def cpu_oracle_throughput(w, qkv, budget_s=15.0, seed=123, op="lla", probe=None):
+def cpu_oracle_throughput(w, qkv, budget_s=8.0, seed=123, op="lla", probe=None):
     """Time the oracle on a bounded random sample of rows on all host cores; extrapolate.
 
     Per-row cost is fitted as a + b (i + 1) (the dense Sigma build is (i+1) d^2) and
