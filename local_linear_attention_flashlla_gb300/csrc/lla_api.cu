@@ -302,11 +302,14 @@ int lla_forward_host(int dtype, int path, const void* q, const void* k, const vo
     cudaError_t e = cudaSuccess;
     if (!buf && (e = cudaMallocAsync(reinterpret_cast<void**>(&buf), need, cs)) != cudaSuccess)
         return lla::cuda_fail(e, "cudaMallocAsync(host-forward buffer)");
-    // both library streams start after the caller's stream reaches this point
-    if ((e = cudaEventRecord(lla::g_he[0], cs)) != cudaSuccess) return lla::cuda_fail(e, "host forward: event record");
-    for (int i = 0; i < 2; ++i)
-        if ((e = cudaStreamWaitEvent(lla::g_hs[i], lla::g_he[0], 0)) != cudaSuccess)
-            return lla::cuda_fail(e, "host forward: stream wait");
+    // both library streams start after the caller's stream reaches this point (a pool buffer is
+    // released again on the caller's stream if that cannot be arranged)
+    e = cudaEventRecord(lla::g_he[0], cs);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(lla::g_hs[i], lla::g_he[0], 0);
+    if (e != cudaSuccess) {
+        if (!device_buffer) cudaFreeAsync(buf, cs);
+        return lla::cuda_fail(e, "host forward: stream ordering");
+    }
 
     const size_t es = dtype == LLA_DTYPE_BF16 ? 2 : 4;
     const unsigned char* hq = static_cast<const unsigned char*>(q);
@@ -566,10 +569,14 @@ int lla_backward_host(int dtype, int path, const void* q, const void* k, const v
     cudaError_t e = cudaSuccess;
     if (!buf && (e = cudaMallocAsync(reinterpret_cast<void**>(&buf), need, cs)) != cudaSuccess)
         return lla::cuda_fail(e, "cudaMallocAsync(host-backward buffer)");
-    if ((e = cudaEventRecord(lla::g_he[0], cs)) != cudaSuccess) return lla::cuda_fail(e, "host backward: event record");
-    for (int i = 0; i < 2; ++i)
-        if ((e = cudaStreamWaitEvent(lla::g_hs[i], lla::g_he[0], 0)) != cudaSuccess)
-            return lla::cuda_fail(e, "host backward: stream wait");
+    // both library streams start after the caller's stream reaches this point (a pool buffer is
+    // released again on the caller's stream if that cannot be arranged)
+    e = cudaEventRecord(lla::g_he[0], cs);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(lla::g_hs[i], lla::g_he[0], 0);
+    if (e != cudaSuccess) {
+        if (!device_buffer) cudaFreeAsync(buf, cs);
+        return lla::cuda_fail(e, "host backward: stream ordering");
+    }
 
     const size_t es = dtype == LLA_DTYPE_BF16 ? 2 : 4;
     const unsigned char* hin[4] = {static_cast<const unsigned char*>(q), static_cast<const unsigned char*>(k),
