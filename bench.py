@@ -1,7 +1,8 @@
 """Benchmark of the causal LLA forward pass (one JSON line on stdout, rank 0).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload lm_bf16] [--path auto|tensor|fp32] [--no-cpu-baseline]
+                    [--op lla|parallax|decode|backward] [--workload lm_bf16] [--batch B]
+                    [--path auto|tensor|fp32] [--no-cpu-baseline] [--no-e2e]
 
 A step is one lla_forward call over the whole workload (all heads, all queries):
 max sweep, moment sweep, CG sweeps and output sweep.  Inputs are seeded synthetic
@@ -44,9 +45,10 @@ def useful_flops(w, T):
 
 
 def executed_flops(w, T, path):
-    """Adds the logits-only max sweep and the output sweep's rho.k product."""
+    """Adds the logits-only max sweep and the output sweep's rho.k product; on the tensor path
+    (path 1) also the product of rho's fp16 remainder (R_lo) in the output sweep."""
     pairs = w.n * (w.n + 1) / 2 * w.B * w.H
-    return (6 + 3 * T) * 2 * w.d * pairs
+    return ((7 if path == 1 else 6) + 3 * T) * 2 * w.d * pairs
 
 
 def parallax_useful_flops(w):
@@ -356,7 +358,7 @@ def run_reference(args, world, rank):
     steps = []
     cb = None
     for s in range(args.warmup + args.steps):
-        cb = cpu_oracle_throughput(w, qkv, budget_s=4.0, seed=1000 + s, op=args.op, probe=extra)
+        cb = cpu_oracle_throughput(w, qkv, budget_s=2.0, seed=1000 + s, op=args.op, probe=extra)
         if s >= args.warmup:
             steps.append(cb["est_seconds_per_step"])
     sec = statistics.mean(steps)
@@ -446,7 +448,7 @@ def run_reference_decode(args):
     qd = q[:, :, w.n - 1].contiguous()
     secs, cb = [], None
     for s_ in range(args.warmup + args.steps):
-        cb = decode_cpu_baseline(w, qd, k, v, budget_s=4.0, seed=2000 + s_)
+        cb = decode_cpu_baseline(w, qd, k, v, budget_s=2.0, seed=2000 + s_)
         if s_ >= args.warmup:
             secs.append(w.B / cb["value"])
     sec = statistics.mean(secs)
