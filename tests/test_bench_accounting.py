@@ -1,0 +1,68 @@
+"""bench.py's accounting, on CPU: the FLOP and byte counts the roofline divides, and the committed
+DRAM traffic it reports.
+
+* useful forward FLOPs = (4 + 3T) passes x 2d per causal pair, the formula the workload's metric
+  is quoted with; the tensor path executes 7 + 3T passes (the max sweep, the output sweep's rho.k
+  and the product of rho's fp16 remainder), the fp32 path 6 + 3T;
+* a causal pair count of n(n+1)/2 per (b, h), checked by brute force on a tiny n;
+* decode method bytes = K in each of the T + 2 passes plus V once, plus q and the outputs;
+* the committed traffic is returned only for the exact kernel sources it was captured on, and
+  scales with the batch (independent slices); any other shape change gives none.
+"""
+import json
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from local_linear_attention_flashlla_gb300.inputs import workload  # noqa: E402
+
+
+def test_causal_pair_count_by_brute_force():
+    w = workload("lm_bf16", B=2, H=3, n=7, d=16)
+    pairs = sum(1 for _ in range(w.B * w.H) for i in range(w.n) for j in range(i + 1))
+    assert bench.useful_flops(w, 0) == 4 * 2 * w.d * pairs
+
+
+@pytest.mark.parametrize("T", [0, 1, 16])
+def test_forward_flop_formulas(T):
+    w = workload("lm_bf16")
+    pairs = w.n * (w.n + 1) / 2 * w.B * w.H
+    assert bench.useful_flops(w, T) == (4 + 3 * T) * 2 * w.d * pairs
+    assert bench.executed_flops(w, T, 1) == (7 + 3 * T) * 2 * w.d * pairs      # tensor path
+    assert bench.executed_flops(w, T, 2) == (6 + 3 * T) * 2 * w.d * pairs      # fp32 path
+
+
+def test_lm_workload_useful_flops_per_call():
+    # 8 x 16 heads, n = 4096, d = 128, T = 16: 52 passes x 256 flops x 8 390 656 pairs x 128 heads
+    w = workload("lm_bf16")
+    assert bench.useful_flops(w, 16) == pytest.approx(1.430e13, rel=1e-3)
+
+
+def test_decode_bytes():
+    w = workload("decode_bf16")
+    T = w.cg_max_iters
+    comp, method = bench.decode_bytes(w, T)
+    kv = w.B * w.H * w.n * w.d * 2
+    assert method >= (T + 2) * kv + kv
+    assert comp >= 2 * kv and comp < method
+
+
+def test_traffic_is_tied_to_the_sources_and_scales_with_the_batch(tmp_path, monkeypatch):
+    w = workload("lm_bf16")
+    doc = {"lla_tc_kernel:lm_bf16": {"source_hash": bench.kernel_source_hash("lla_tc_kernel"),
+                                     "dram_bytes_per_launch": 800}}
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(doc))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    # the sources are read from the real tree, the summary from the temporary one
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda k: doc["lla_tc_kernel:lm_bf16"]["source_hash"])
+    assert bench.load_traffic("lla_tc_kernel", w) == 800
+    assert bench.load_traffic("lla_tc_kernel", w.with_(B=2)) == 200
+    assert bench.load_traffic("lla_tc_kernel", w.with_(n=2048)) is None
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda k: "0" * 16)
+    assert bench.load_traffic("lla_tc_kernel", w) is None
