@@ -170,10 +170,12 @@ int lla_profile_read(float* main_ms, float* total_ms);
  * LLA_PATH_TENSOR, ...) exceeds the array is rejected with LLA_ERR_INVALID_ARG before anything is
  * launched; d outside {64, 128} gives LLA_ERR_UNSUPPORTED.
  *
- * The first call on each device looks up the array's device address (cudaGetSymbolAddress with
- * that device current); make that first call before any stream capture.  All calls share the
- * array: calls that overlap on the GPU (on different streams, or from different threads) race on
- * it and must be serialised by the caller.  Each call re-initialises what must start at zero.
+ * Every call looks up the array's device address in the current context (cudaGetSymbolAddress
+ * with the caller's device current; no allocation), so the address stays right after a
+ * cudaDeviceReset.  The first lookup on a device may load the library's device code: make the
+ * first call on each device before any stream capture.  All calls share the array: calls that
+ * overlap on the GPU (on different streams, or from different threads) race on it and must be
+ * serialised by the caller.  Each call re-initialises what must start at zero.
  */
 #define LLA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 int lla_forward_noalloc(const void* q, const void* k, const void* v, void* out, float* rho, float* denom,

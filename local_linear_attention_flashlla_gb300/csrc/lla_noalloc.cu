@@ -8,7 +8,6 @@
 // (fp16 operand copies, kbar and the CG iterate) in a file-scope __device__ array that exists
 // for as long as the library is loaded, and it calls no allocating routine.
 #include <cuda_runtime.h>
-#include <mutex>
 #include <stdint.h>
 #include <stdio.h>
 
@@ -21,26 +20,17 @@ namespace {
 // Fixed scratch; every GPU that loads the library holds it until the process exits.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[LLA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};   // device address of g_noalloc_scratch, per device
-
-// Device address of the scratch array on the current device.  In host code the array's name
+// Device address of the scratch array in the current context.  In host code the array's name
 // is only a host-side stand-in, not a device address, so the runtime is asked for the address
-// once per device, with that device current, and the answer is cached.
+// with the caller's device current.  The lookup is repeated on every call rather than cached:
+// the address belongs to the context that loaded the module, and a cached value would dangle
+// after cudaDeviceReset (or any teardown of the primary context) reloads the module elsewhere.
+// The lookup allocates nothing.
 cudaError_t scratch_address(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return cudaSuccess;
 }
 
