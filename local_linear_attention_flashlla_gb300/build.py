@@ -16,7 +16,6 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblla.so")
-PROBE_LIB = os.path.join(PKG, "liblla_probe.so")   # test-only tcgen05 descriptor probe
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -43,10 +42,10 @@ def _run(cmd):
 
 
 def build(verbose=False, extra_flags=()):
-    """Build liblla.so (and the test-only liblla_probe.so); returns the liblla.so path."""
+    """Build liblla.so; returns its path."""
     nvcc = nvcc_path()
     os.makedirs(BUILD, exist_ok=True)
-    groups = {LIB: sources(), PROBE_LIB: sources("probe")}
+    groups = {LIB: sources()}
     jobs = []
     for lib, srcs in groups.items():
         for s in srcs:

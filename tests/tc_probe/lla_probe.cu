@@ -2,8 +2,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
-#include "../tc_host.h"
-#include "../tc_ptx.cuh"
+#include "tc_host.h"
+#include "tc_ptx.cuh"
 #include "lla_probe.h"
 
 namespace {

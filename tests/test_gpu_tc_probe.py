@@ -1,7 +1,6 @@
 """tcgen05 descriptor/TMA/TMEM helpers checked on single 128x128x128 fp16 products
 against torch fp32 matmul (the helpers the LLA tensor kernel is built from)."""
 import ctypes
-import os
 
 import numpy as np
 import pytest
@@ -9,12 +8,17 @@ import torch
 
 pytestmark = pytest.mark.gpu
 
-HERE = os.path.dirname(os.path.abspath(__file__))
-PROBE = os.path.join(os.path.dirname(HERE), "local_linear_attention_flashlla_gb300", "liblla_probe.so")
+from tc_probe import build_probe
 
 
-def test_umma_descriptors_match_matmul(lla_gpu):
-    lib = ctypes.CDLL(PROBE)
+@pytest.fixture(scope="module")
+def probe_lib():
+    """The probe library, compiled for sm_103a on first use (a test fixture, not part of liblla)."""
+    return ctypes.CDLL(build_probe.build())
+
+
+def test_umma_descriptors_match_matmul(lla_gpu, probe_lib):
+    lib = probe_lib
     lib.lla_probe_umma.restype = ctypes.c_int
     lib.lla_probe_umma.argtypes = [ctypes.c_void_p] * 6
     g = torch.Generator().manual_seed(0)
