@@ -396,13 +396,17 @@ __device__ __forceinline__ void gemm_y_split(uint32_t y_tmem, uint32_t m_tmem, u
     }
 }
 
-template <int D, bool BWD>
+// PREC (forward only): the precise form used in tolerance mode.  The moment sweep's weights and the
+// CG sweeps' per-pair coefficients are fp16 hi + lo pairs (two TS products per block) and the CG
+// direction is hi + lo in every tile, so each carries about 22 bits, as in the backward mode.
+template <int D, bool BWD, bool PREC = false>
 __global__ void __launch_bounds__(NTHREADS, 1)
 lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g, const TcParams prm) {
     using S = TcSmem<D>;
     constexpr int NB = S::NB;
     constexpr int DH = D / 2;                       // head-dim coordinates per elementwise thread
+    constexpr bool SPLITM = BWD || PREC;            // hi + lo weights and CG coefficients
 
     // The swizzled tiles need 1024-byte alignment.  Dynamic shared memory begins 1024-aligned
     // (right after the block's reserved kilobyte), so no padding is requested; a launch where it
@@ -601,7 +605,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     const uint32_t b_addr = smem_u32(s.slot[(hprod ? fv : fk) % NSLOT]);
                     gemm_qk<D, false>(tA, p_addr, b_addr);
                     // T = (R_hi + R_lo) K^T; in the first tile also A' = (P_hi + P_lo) K^T
-                    if (!hprod && (type == SW_OUT || tile == 0 || BWD)) gemm_qk<D, true>(tA, rlo_addr, b_addr);
+                    if (!hprod && (type == SW_OUT || tile == 0 || BWD || PREC)) gemm_qk<D, true>(tA, rlo_addr, b_addr);
                     umma_commit(&s.s_full[g & 1]);
                 }
                 if (type == SW_OUT) break;
@@ -636,7 +640,8 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         if (type == SW_OUT && !(ok = WAIT(&s.slot_full[fv % NSLOT], (fv / NSLOT) & 1, err))) break;
                         tc_fence_after();
                         const uint32_t fsrc = type == SW_OUT ? fv : fk;   // V for the output, K otherwise
-                        if (BWD) gemm_y_split<D>(ty_acc, tS0 + b * 128, smem_u32(s.slot[fsrc % NSLOT]), kb > 0);
+                        if (BWD || (PREC && type != SW_OUT))
+                            gemm_y_split<D>(ty_acc, tS0 + b * 128, smem_u32(s.slot[fsrc % NSLOT]), kb > 0);
                         else gemm_y<D>(ty_acc, tS0 + b * 128, smem_u32(s.slot[fsrc % NSLOT]), kb > 0);
                         umma_commit(&s.slot_empty[fsrc % NSLOT]);
                         // the other block of a two-block sweep (the output's K, the backward's V): its
@@ -663,8 +668,9 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const bool row_ok = i < n;
         const bool tile_full = (tile + 1) * BQ <= n;     // every row of the tile exists
         // the first tile holds the rows i < d whose key scatter is rank-deficient: there the CG
-        // direction is kept to about 22 bits (hi + lo fp16 halves, one extra MMA per CG block)
-        const bool split_p = BWD || tile == 0;
+        // direction is kept to about 22 bits (hi + lo fp16 halves, one extra MMA per CG block);
+        // the precise form does so in every tile
+        const bool split_p = BWD || PREC || tile == 0;
         const size_t row_g = ((size_t)head * n + (row_ok ? i : 0)) * D + half * DH;
         // tile-transposed fp32 scratch: coordinate e of this thread's row at [e * BQ] (coalesced)
         const size_t tbase = ((size_t)(head * prm.n_tiles + tile) * D + half * DH) * BQ + row;
@@ -789,6 +795,20 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 tmem_ld_wait();
                 if (masked) coef_chunk_wh<true, 1>(v, a, c_log2, m2 - 14.f, half * 64 + 32, lim, om_part, wh_part, pk, pl);
                 else coef_chunk_wh<false, 1>(v, a, c_log2, m2 - 14.f, 0, 0, om_part, wh_part, pk, pl);
+                tmem_st16(tS + 32, pk);
+                tmem_st16(tS + 48, pl);
+            } else if constexpr (PREC) {    // hi + lo weights, split layout (gemm_y_split)
+                uint32_t pl[16];
+                tmem_ld32(tS, v);
+                tmem_ld_wait();
+                if (masked) coef_chunk<true, false, 0, true>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, half * 64, lim, om_part, pk, pl);
+                else coef_chunk<false, false, 0, true>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, 0, 0, om_part, pk, pl);
+                tmem_st16(tS, pk);
+                tmem_st16(tS + 16, pl);
+                tmem_ld32(tS + 32, v);
+                tmem_ld_wait();
+                if (masked) coef_chunk<true, false, 0, true>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, half * 64 + 32, lim, om_part, pk, pl);
+                else coef_chunk<false, false, 0, true>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, 0, 0, om_part, pk, pl);
                 tmem_st16(tS + 32, pk);
                 tmem_st16(tS + 48, pl);
             } else {
@@ -1003,7 +1023,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 tmem_ld32(tS, v);
                 tmem_ld_wait();
                 release_a();
-                if constexpr (BWD) {   // hi + lo coefficients, split layout (gemm_y_split)
+                if constexpr (SPLITM) {   // hi + lo coefficients, split layout (gemm_y_split)
                     uint32_t pl[16];
                     if (masked) coef_chunk<true, true, 0, true>(v, a, c_log2, offM, -kp_acc, 1.f, half * 64, lim, msum_part, pk, pl);
                     else coef_chunk<false, true, 0, true>(v, a, c_log2, offM, -kp_acc, 1.f, 0, 0, msum_part, pk, pl);
@@ -1318,7 +1338,7 @@ TcWs carve(void* ws, size_t N, size_t NT, bool bwd) {
 }
 
 // Pre-pass, tensor maps and the sweep kernel.  BWD: the backward's stats stage (g = dout).
-template <int D, bool BWD>
+template <int D, bool BWD, bool PREC = false>
 cudaError_t launch_d(int B, int H, int n, const void* qv, const void* kv, const void* vv, const void* gv,
                      TcParams prm, void* ws, cudaEvent_t ev_begin, cudaEvent_t ev_end, cudaStream_t stream,
                      const char** why) {
@@ -1355,7 +1375,7 @@ cudaError_t launch_d(int B, int H, int n, const void* qv, const void* kv, const 
     if (!prm.dev_err) { *why = "device error word"; return cudaErrorInvalidSymbol; }
 
     const size_t smem = sizeof(TcSmem<D>);
-    auto kern = lla_tc_kernel<D, BWD>;
+    auto kern = lla_tc_kernel<D, BWD, PREC>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) { *why = "tensor kernel shared-memory attribute"; return e; }
     dim3 grid(prm.n_tiles, (unsigned)slices);
@@ -1392,14 +1412,21 @@ size_t tensor_workspace_bytes(int B, int H, int n, int d) {
     return HDR_BYTES + 3 * align256(N * 2) + 2 * align256(NT * 4);
 }
 
+// Tolerance mode (cg_tol > 0) takes the precise form: CG run to a relative residual needs matrix-vector
+// products accurate well beyond fp16's 11 bits wherever lambda/omega is small against the key scatter.
 cudaError_t launch_tensor(const Problem& p, void* ws, cudaStream_t stream, const char** why) {
     const TcParams prm = forward_params(p);
+    const bool prec = p.cg_tol > 0.f && !p.probe;
     if (p.d == 128)
-        return launch_d<128, false>(p.B, p.H, p.n, p.q, p.k, p.v, nullptr, prm, ws, p.ev_main_begin, p.ev_main_end,
-                                    stream, why);
+        return prec ? launch_d<128, false, true>(p.B, p.H, p.n, p.q, p.k, p.v, nullptr, prm, ws, p.ev_main_begin,
+                                                 p.ev_main_end, stream, why)
+                    : launch_d<128, false>(p.B, p.H, p.n, p.q, p.k, p.v, nullptr, prm, ws, p.ev_main_begin,
+                                           p.ev_main_end, stream, why);
     if (p.d == 64)
-        return launch_d<64, false>(p.B, p.H, p.n, p.q, p.k, p.v, nullptr, prm, ws, p.ev_main_begin, p.ev_main_end,
-                                   stream, why);
+        return prec ? launch_d<64, false, true>(p.B, p.H, p.n, p.q, p.k, p.v, nullptr, prm, ws, p.ev_main_begin,
+                                                p.ev_main_end, stream, why)
+                    : launch_d<64, false>(p.B, p.H, p.n, p.q, p.k, p.v, nullptr, prm, ws, p.ev_main_begin,
+                                          p.ev_main_end, stream, why);
     *why = "tensor path supports d in {64, 128}";
     return cudaErrorInvalidValue;
 }

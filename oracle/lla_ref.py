@@ -79,6 +79,7 @@ __all__ = [
     "lla_row",
     "lla_ref",
     "lla_row_deflated_cg",
+    "cg_centred_rounded",
     "softmax_row",
     "softmax_ref",
     "parallax_row",
@@ -203,12 +204,50 @@ def lla_row_cg(q_i, K_prefix, V_prefix, tau, lam, max_iters, tol):
     return {"out": out, "rho": rho, "denom": denom, "iters": iters, "m": m, "omega": omega}
 
 
-def lla_row_deflated_cg(q_i, K_prefix, V_prefix, tau, lam, max_iters, tol, weight_noise=None):
+def cg_centred_rounded(Kc, wbar, lam_n, delta, max_iters, tol, u, rng):
+    """``cg_solve`` on Cn = sum_j wbar_j c_j c_j^T + lam_n I (rows c_j of Kc), matrix-free, with
+    every matrix-vector product perturbed the way a kernel's rounding of its product operands
+    perturbs it: each coordinate of the direction p and each per-pair coefficient wbar_j (c_j.p)
+    is multiplied by its own fresh factor (1 + xi), xi uniform in [-u, u], in every iteration.
+    u = 0 is the unperturbed iteration.  TEST INFRASTRUCTURE: a model of rounding used only to
+    measure how sensitive a capped CG result is to the arithmetic that computes it; the same
+    stopping rules as ``cg_solve``.  Returns (x, iterations executed)."""
+    Kc = _f64(Kc)
+    wbar = _f64(wbar)
+    b = _f64(delta)
+    x = np.zeros_like(b)
+    r = b.copy()
+    p = r.copy()
+    gamma = r @ r
+    b_norm = np.sqrt(gamma)
+    it = 0
+    while it < max_iters:
+        if gamma == 0.0 or np.sqrt(gamma) <= tol * b_norm:
+            break
+        ph = p * (1.0 + rng.uniform(-u, u, p.shape)) if u else p
+        coef = wbar * (Kc @ ph)
+        if u:
+            coef = coef * (1.0 + rng.uniform(-u, u, coef.shape))
+        Sp = Kc.T @ coef + lam_n * ph
+        pSp = ph @ Sp
+        if not pSp > 0.0:
+            break
+        alpha = gamma / pSp
+        x = x + alpha * ph
+        r = r - alpha * Sp
+        gamma_new = r @ r
+        p = r + (gamma_new / gamma) * ph
+        gamma = gamma_new
+        it += 1
+    return x, it
+
+
+def lla_row_deflated_cg(q_i, K_prefix, V_prefix, tau, lam, max_iters, tol, rounding=None):
     """LLA of one query with rho from CG on the centred key scatter.
 
-    weight_noise: None, or relative perturbations xi_j applied as w_j (1 + xi_j) after the
-    weights are formed (used only to measure how sensitive a row's result is to rounding
-    of the per-pair coefficients; the default computes the unperturbed iteration).
+    rounding: None (the plain float64 iteration), or (u, rng) to run the iteration through
+    ``cg_centred_rounded`` with relative perturbations of size u in every product (used only to
+    measure how sensitive a row's capped result is to rounding in the arithmetic).
 
     Steps: weights; omega, kbar = sum_j w_j k_j / omega; delta = kbar - q;
     Cn = sum_j wbar_j (k_j - kbar)(k_j - kbar)^T + (lambda/omega) I (dense);
@@ -219,15 +258,16 @@ def lla_row_deflated_cg(q_i, K_prefix, V_prefix, tau, lam, max_iters, tol, weigh
     q_i = _f64(q_i)
     K = _f64(K_prefix)
     w, m = row_weights(q_i, K, tau)
-    if weight_noise is not None:
-        w = w * (1.0 + _f64(weight_noise))
     omega = w.sum()
     wbar = w / omega
     kbar = wbar @ K
     delta = kbar - q_i
     Kc = K - kbar[None, :]
-    Cn = (Kc * wbar[:, None]).T @ Kc + (lam / omega) * np.eye(q_i.shape[0])
-    rho_p, iters = cg_solve(Cn, delta, max_iters, tol)
+    if rounding is None:
+        Cn = (Kc * wbar[:, None]).T @ Kc + (lam / omega) * np.eye(q_i.shape[0])
+        rho_p, iters = cg_solve(Cn, delta, max_iters, tol)
+    else:
+        rho_p, iters = cg_centred_rounded(Kc, wbar, lam / omega, delta, max_iters, tol, rounding[0], rounding[1])
     g = 1.0 + delta @ rho_p
     s = wbar * (1.0 - Kc @ rho_p)
     return {"out": s @ _f64(V_prefix), "rho": rho_p / g, "denom": omega / g,
@@ -252,14 +292,15 @@ def _rows_iter(shape, rows):
             yield tuple(int(t) for t in r)
 
 
-def lla_ref(q, k, v, tau, lam, rows=None, cg=None, deflated=None, noise_rel=None, noise_seed=0):
+def lla_ref(q, k, v, tau, lam, rows=None, cg=None, deflated=None, rounding_u=None, rounding_seed=0):
     """Causal LLA over [B, H, n, d] inputs, row by row.
 
     rows: None (every (b, h, i)) or an iterable of (b, h, i) triples.
     cg: None for the exact solve, else (max_iters, tol) to solve with ``cg_solve``
         on Sigma_i; deflated: (max_iters, tol) to use ``lla_row_deflated_cg``;
-    noise_rel: with ``deflated``, perturb every weight by a seeded relative amount
-        uniform in [-noise_rel, noise_rel] (sensitivity analysis).
+    rounding_u: with ``deflated``, run its CG through ``cg_centred_rounded`` with relative
+        perturbations of size rounding_u, seeded per row from (rounding_seed, b, h, i)
+        (sensitivity analysis).
     Returns (out [R, d], rho [R, d], denom [R]) in float64, R rows in the order
     given (row-major over b, h, i when rows is None).
     """
@@ -267,12 +308,11 @@ def lla_ref(q, k, v, tau, lam, rows=None, cg=None, deflated=None, noise_rel=None
     outs, rhos, dens = [], [], []
     for b, h, i in _rows_iter(q.shape, rows):
         if deflated is not None:
-            xi = None
-            if noise_rel:
-                rng = np.random.Generator(np.random.PCG64([noise_seed, b, h, i]))
-                xi = rng.uniform(-noise_rel, noise_rel, size=i + 1)
+            rounding = None
+            if rounding_u:
+                rounding = (rounding_u, np.random.Generator(np.random.PCG64([rounding_seed, b, h, i])))
             r = lla_row_deflated_cg(q[b, h, i], k[b, h, : i + 1], v[b, h, : i + 1], tau, lam,
-                                    deflated[0], deflated[1], weight_noise=xi)
+                                    deflated[0], deflated[1], rounding=rounding)
         elif cg is None:
             r = lla_row(q[b, h, i], k[b, h, : i + 1], v[b, h, : i + 1], tau, lam)
         else:

@@ -3,11 +3,10 @@
 Gates (tolerances stated here, applied per compared row):
 * fp32 inputs, CG to relative residual 1e-7: out, rho and denom within 1e-4 of the exact
   (Cholesky) solve on every compared row.
-* bf16 inputs at a fixed iteration cap: the exact solve is the reference on the rows where
-  the oracle's own float64 CG at the same cap has converged (|cg - exact| <= 2e-3 RMS(v));
-  there out must be within 2e-2 RMS(v).  On the remaining rows CG truncation itself exceeds
-  the tolerance (a property of the iteration, not of an implementation); they are checked
-  for finiteness, denom > 0 and reported.
+* bf16 inputs (``parity_util.bf16_gate``), on every compared row, element by element: within
+  (2e-2 + 3 spread) RMS(v) of the oracle's float64 centred CG at the same cap and tolerance,
+  spread being that result's rounding spread at fp32's unit roundoff (2^-24), and within 2e-2
+  RMS(v) of the exact solve where float64 CG has converged; finite, denom > 0.
 """
 import numpy as np
 import pytest
@@ -68,14 +67,14 @@ def test_fp32_path_bf16_inputs_ragged(lla_gpu, d):
     (at 16 iterations nearly every row of a 333-long d=128 sequence is in the band
     where truncation dominates)."""
     w = workload("lm_bf16", B=2, H=2, n=333, d=d, tau=1.0 / np.sqrt(d), cg_max_iters=48)
-    _bf16_gate(w, all_rows(w), FP32, min_ok_frac=0.5)
+    _bf16_gate(w, all_rows(w), FP32)
 
 
 @pytest.mark.slow
 def test_lm_bf16_full_size_fp32_path(lla_gpu):
     w = workload("lm_bf16")
-    e, ok, its = _bf16_gate(w, rows_for(w, 256), FP32)
-    assert (its.numpy() == w.cg_max_iters).mean() > 0.99
+    r = _bf16_gate(w, rows_for(w, 256), FP32)
+    assert (r["its"].numpy() == w.cg_max_iters).mean() > 0.99
 
 
 @pytest.mark.slow
@@ -88,7 +87,7 @@ def test_long_bf16_full_size_fp32_path(lla_gpu):
 @pytest.mark.parametrize("lam", [1e-3, 1e-1])
 def test_illcond_bf16_fp32_path(lla_gpu, lam):
     w = workload("illcond_bf16", lam=lam)
-    e, ok, its = _bf16_gate(w, rows_for(w, 192), FP32, lam=lam)
+    its = _bf16_gate(w, rows_for(w, 192), FP32, lam=lam)["its"]
     hist = np.bincount(its.numpy().ravel(), minlength=w.cg_max_iters + 1)
     assert hist.sum() == w.B * w.H * w.n and its.numpy().max() <= w.cg_max_iters
 

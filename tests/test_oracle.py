@@ -282,18 +282,49 @@ def test_lla_ref_batched_layout_matches_rows():
     assert np.abs(o2[1] - v[0, 0, 0]).max() < 1e-12
 
 
-def test_weight_noise_hook_is_inert_by_default_and_small_when_used():
-    """The sensitivity hook: zero noise reproduces the plain iteration exactly, small noise
-    moves a well-conditioned row by about the noise level."""
-    q, k, v = _rand(15, 30, 4)
-    i = 29
-    a = O.lla_row_deflated_cg(q[i], k[: i + 1], v[: i + 1], 0.6, 0.5, 100, 0.0)
-    b = O.lla_row_deflated_cg(q[i], k[: i + 1], v[: i + 1], 0.6, 0.5, 100, 0.0, weight_noise=np.zeros(i + 1))
-    assert np.abs(a["out"] - b["out"]).max() == 0.0
-    c = O.lla_row_deflated_cg(q[i], k[: i + 1], v[: i + 1], 0.6, 0.5, 100, 0.0,
-                              weight_noise=np.full(i + 1, 1e-6))
-    # a common relative factor on every weight: kbar, wbar unchanged; only lambda/omega shifts
-    assert np.abs(a["out"] - c["out"]).max() < 1e-5
+def test_rounding_model_cg_matches_dense_cg_when_unperturbed():
+    """The matrix-free centred CG used to model rounding: with u = 0 it takes the same steps as
+    ``cg_solve`` on the dense centred matrix (same iteration count, same iterate to summation
+    order), on a full-rank row and on a rank-deficient early row, capped and to tolerance."""
+    q, k, v = _rand(16, 40, 8)
+    rng = np.random.default_rng(0)
+    for i, T, tol in [(39, 5, 0.0), (39, 200, 1e-10), (3, 6, 0.0), (3, 200, 1e-12)]:
+        a = O.lla_row_deflated_cg(q[i], k[: i + 1], v[: i + 1], 0.6, 0.2, T, tol)
+        b = O.lla_row_deflated_cg(q[i], k[: i + 1], v[: i + 1], 0.6, 0.2, T, tol, rounding=(0.0, rng))
+        assert a["iters"] == b["iters"]
+        assert np.abs(a["out"] - b["out"]).max() < 1e-10
+        assert np.abs(a["rho"] - b["rho"]).max() < 1e-10 * max(1.0, np.abs(a["rho"]).max())
+
+
+def test_rounding_model_converged_row_moves_by_about_u():
+    """Run to convergence, a perturbation of relative size u in every product moves the solution
+    by O(u kappa): tiny for u = 1e-9, visible but bounded for u = 1e-4, and zero difference for
+    two runs with the same seed (the model is deterministic given its generator)."""
+    q, k, v = _rand(17, 60, 4)
+    i = 59
+    ex = O.lla_row(q[i], k[: i + 1], v[: i + 1], 0.6, 0.5)["out"]
+    run = lambda u, seed: O.lla_row_deflated_cg(q[i], k[: i + 1], v[: i + 1], 0.6, 0.5, 400, 1e-13,
+                                               rounding=(u, np.random.default_rng(seed)))["out"]
+    assert np.abs(run(1e-9, 1) - ex).max() < 1e-6
+    e4 = np.abs(run(1e-4, 1) - ex).max()
+    assert 0.0 < e4 < 1e-1
+    assert np.abs(run(1e-4, 5) - run(1e-4, 5)).max() == 0.0
+
+
+def test_rounding_model_capped_rows_in_truncation_band_are_sensitive():
+    """On an LM-shaped head at 16 iterations, a row in the truncation band (short prefix, CG far
+    from converged) moves by far more than a converged late row under the same fp16-level
+    perturbation: the spread the parity gate allows is a property of the row, not uniform."""
+    from local_linear_attention_flashlla_gb300.inputs import make_inputs, workload
+    w = workload("lm_bf16", B=1, H=1, n=700)
+    q, k, v = (t.double().numpy()[0, 0] for t in make_inputs(w))
+    def spread(i):
+        base = O.lla_row_deflated_cg(q[i], k[: i + 1], v[: i + 1], w.tau, w.lam, 16, 0.0)["out"]
+        dev = [np.abs(O.lla_row_deflated_cg(q[i], k[: i + 1], v[: i + 1], w.tau, w.lam, 16, 0.0,
+                                            rounding=(2.0 ** -11, np.random.default_rng(s)))["out"] - base).max()
+               for s in range(2)]
+        return max(dev)
+    assert spread(100) > 10 * spread(690)
 
 
 # --------------------------------------------------------------------------- Parallax form
