@@ -51,6 +51,48 @@ def executed_flops(w, T, path):
     return ((7 if path == 1 else 6) + 3 * T) * 2 * w.d * pairs
 
 
+# query rows per tile of each path (tensor path 1, fp32 path 2): a tile runs CG sweeps until its
+# last query stops, so in tolerance mode the work follows each tile's largest iteration count
+TILE_ROWS = {1: 128, 2: 32}
+
+
+def tile_iterations(its, tile_rows):
+    """Per query tile: the iterations it executed (the most any of its queries ran), and its causal
+    pair count.  its: int array [B, H, n].  Returns (T_tile [B, H, nt], pairs [nt])."""
+    import numpy as np
+    B, H, n = its.shape
+    nt = (n + tile_rows - 1) // tile_rows
+    pad = np.zeros((B, H, nt * tile_rows), dtype=np.int64)
+    pad[:, :, :n] = its
+    T_tile = pad.reshape(B, H, nt, tile_rows).max(axis=-1)
+    i1 = np.arange(1, nt * tile_rows + 1, dtype=np.float64)
+    i1[n:] = 0.0
+    pairs = i1.reshape(nt, tile_rows).sum(axis=-1)
+    return T_tile, pairs
+
+
+def tolerance_flops(w, its, path, precise):
+    """Tolerance mode: useful FLOPs sum (4 + 3 T_t) passes of 2d over each tile t's causal pairs,
+    T_t the iterations tile t executed; executed FLOPs add the max sweep and the output sweep's
+    rho.k product (fp32 path: 6 + 3 T_t), the tensor path's R_lo product (7 + 3 T_t), and in its
+    precise form the hi + lo halves of the moment and CG coefficients and of the CG direction
+    (8 + 5 T_t).  Returns (useful, executed, T tile mean, T pair-weighted mean)."""
+    import numpy as np
+    T_tile, pairs = tile_iterations(its, TILE_ROWS[path])
+    p = np.broadcast_to(pairs, T_tile.shape)
+    useful = float(((4 + 3 * T_tile) * p).sum()) * 2 * w.d
+    a, b = (8, 5) if (path == 1 and precise) else ((7, 3) if path == 1 else (6, 3))
+    executed = float(((a + b * T_tile) * p).sum()) * 2 * w.d
+    return useful, executed, float(T_tile.mean()), float((T_tile * p).sum() / p.sum())
+
+
+def iteration_histogram(its):
+    """Per-query CG iteration counts as {iterations: queries}, nonzero bins only."""
+    import numpy as np
+    h = np.bincount(np.asarray(its).ravel())
+    return {str(k): int(c) for k, c in enumerate(h) if c}
+
+
 def parallax_useful_flops(w):
     """Parallax form: q.k, the weighted key mean, probe.k and the value product: 4 passes of 2d."""
     return 4 * 2 * w.d * (w.n * (w.n + 1) / 2 * w.B * w.H)
@@ -303,6 +345,8 @@ def parse():
                          "decode: one decode step (use --workload decode_bf16); backward: dq, dk, dv of the forward")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch B (a smaller case for profiler captures)")
+    ap.add_argument("--lam", type=float, default=None,
+                    help="override the workload's lambda (illcond_bf16 is quoted at 1e-3, 1e-1 and 1e6)")
     return ap.parse_args()
 
 
@@ -556,7 +600,7 @@ def run_decode(args, world, rank, local):
 
     line = {"metric": METRIC_DECODE, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "vs_baseline": None, "dtype": "bf16 in, f32 compute" if w.dtype == "bf16" else "f32", "data": "synthetic",
             "config": {"workload": f"{w.name} B={w.B} H={w.H} cache n={w.n} d={w.d} tau={w.tau:.5g} lambda={w.lam} "
                                    f"cg_iters={T} cg_tol={w.cg_tol}", "l2": "flushed before every step (512 MiB write)",
                        "inputs": f"{w.dtype} caches resident in HBM"},
@@ -730,6 +774,88 @@ def run_backward(args, world, rank, local):
         torch.distributed.destroy_process_group()
 
 
+class _StreamOrderedPool:
+    """High-water mark of the device's current stream-ordered pool (the one cudaMallocAsync, and
+    so lla_forward's workspace, draws from), through the CUDA driver API."""
+    USED_MEM_HIGH = 8                      # CUmemPool_attribute
+
+    def __init__(self, device_index):
+        import ctypes
+        self.ct = ctypes
+        self.cu = ctypes.CDLL("libcuda.so.1")
+        dev = ctypes.c_int()
+        self.pool = ctypes.c_void_p()
+        if self.cu.cuDeviceGet(ctypes.byref(dev), device_index) or \
+                self.cu.cuDeviceGetMemPool(ctypes.byref(self.pool), dev):
+            raise OSError("cannot query the device's memory pool")
+
+    def reset(self):
+        zero = self.ct.c_uint64(0)
+        self.cu.cuMemPoolSetAttribute(self.pool, self.USED_MEM_HIGH, self.ct.byref(zero))
+
+    def high(self):
+        val = self.ct.c_uint64()
+        self.cu.cuMemPoolGetAttribute(self.pool, self.USED_MEM_HIGH, self.ct.byref(val))
+        return int(val.value)
+
+
+def memory_and_n_scaling(lla, w, path, dev, peak_tflops, flush, ns=(4096, 8192, 16384, 32768), steps=3):
+    """Device memory of one lla_forward call and its time at n in ns (H, B and d of w).
+
+    Memory: the caller's tensors (q, k, v in; out, rho, denom out: torch's peak allocation while
+    they exist) plus the workspace the call takes from the stream-ordered pool (the pool's high-water
+    mark during the call, workspace not supplied): peak device bytes, and per element of q.
+    Time: CUDA events around each call after a warm-up, L2 flushed before each (as the headline)."""
+    import torch
+    from local_linear_attention_flashlla_gb300.inputs import make_inputs
+    pool = _StreamOrderedPool(dev.index if dev.index is not None else 0)
+    mem, series = None, []
+    for n in ns:
+        wn = w.with_(n=n)
+        qkv_host = make_inputs(wn)
+        torch.cuda.synchronize()
+        torch.cuda.reset_peak_memory_stats(dev)
+        base = torch.cuda.memory_allocated(dev)
+        q, k, v = (t.to(dev) for t in qkv_host)
+        out = torch.empty_like(q)
+        rho = torch.empty(q.shape, dtype=torch.float32, device=dev)
+        den = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+        lla.forward(q, k, v, wn.tau, wn.lam, wn.cg_max_iters, wn.cg_tol, path=path, out=out, rho=rho, denom=den)
+        torch.cuda.synchronize()
+        pool.reset()
+        lla.forward(q, k, v, wn.tau, wn.lam, wn.cg_max_iters, wn.cg_tol, path=path, out=out, rho=rho, denom=den)
+        torch.cuda.synchronize()
+        pool_bytes = pool.high()
+        tensor_bytes = torch.cuda.max_memory_allocated(dev) - base
+        elems = wn.B * wn.H * wn.n * wn.d
+        times = []
+        for _ in range(steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            lla.forward(q, k, v, wn.tau, wn.lam, wn.cg_max_iters, wn.cg_tol, path=path, out=out, rho=rho, denom=den)
+            e1.record()
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        ms = statistics.median(times)
+        tf = useful_flops(wn, wn.cg_max_iters) / (ms / 1e3) / 1e12
+        series.append({"n": n, "ms": ms, "tflops": tf, "frac": tf / peak_tflops,
+                       "peak_device_bytes": tensor_bytes + pool_bytes, "bytes_per_element": (tensor_bytes + pool_bytes) / elems})
+        if n == w.n:
+            mem = {"n": n, "caller_tensor_bytes": tensor_bytes, "workspace_pool_bytes": pool_bytes,
+                   "peak_device_bytes": tensor_bytes + pool_bytes,
+                   "bytes_per_element": (tensor_bytes + pool_bytes) / elems,
+                   "lla_workspace_size": lla.lla_workspace_size(lla.LLA_DTYPE_BF16, path, wn.B, wn.H, wn.n, wn.d),
+                   "how": "torch peak allocation of q,k,v,out,rho,denom + the stream-ordered pool's high-water mark "
+                          "during one lla_forward call that takes its workspace from the pool"}
+        del q, k, v, out, rho, den
+        torch.cuda.empty_cache()
+    t_last = series[-1]["ms"] / series[-1]["n"] ** 2
+    for e in series:
+        e["ms_over_n2_rel_to_largest"] = (e["ms"] / e["n"] ** 2) / t_last
+    return mem, series
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup(args)
@@ -751,6 +877,8 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     w = workload(args.workload) if args.batch is None else workload(args.workload, B=args.batch)
+    if args.lam is not None:
+        w = w.with_(lam=args.lam)
     path = {"auto": lla.LLA_PATH_AUTO, "tensor": lla.LLA_PATH_TENSOR, "fp32": lla.LLA_PATH_FP32}[args.path]
     dtype_code = lla.LLA_DTYPE_BF16 if w.dtype == "bf16" else lla.LLA_DTYPE_FP32
     rpath = lla.lla_resolve_path(dtype_code, path, w.d)
@@ -808,10 +936,19 @@ def main():
     tokens = w.B * w.n
     value = job_throughput(world, tokens, args.steps, total_ms)
     T = w.cg_max_iters if (w.cg_tol == 0 or parallax) else None
-    if T is None:   # tolerance-driven: count the executed iterations
+    iters_info = None
+    if T is None:   # tolerance-driven: count the iterations each query tile executed
         _, _, _, its = lla.forward(q, k, v, w.tau, w.lam, w.cg_max_iters, w.cg_tol, path=path, return_iters=True)
-        T = float(its.float().max().item())
-    flops = parallax_useful_flops(w) if parallax else useful_flops(w, T)
+        its = its.cpu().numpy()
+        flops, flops_exec, T_mean, T_pw = tolerance_flops(w, its, rpath, precise=True)
+        T = T_pw
+        iters_info = {"tile_rows": TILE_ROWS[rpath], "tile_mean": T_mean, "pair_weighted_tile_mean": T_pw,
+                      "query_mean": float(its.mean()), "query_max": int(its.max()),
+                      "query_histogram": iteration_histogram(its)}
+    else:
+        flops = parallax_useful_flops(w) if parallax else useful_flops(w, T)
+        flops_exec = (parallax_executed_flops(w, rpath == lla.LLA_PATH_TENSOR) if parallax else
+                      executed_flops(w, T, rpath))
     tflops = world * flops * args.steps / (total_ms / 1e3) / 1e12
 
     # end to end through the public API from pinned host buffers: the LLA forward through the C-ABI
@@ -869,14 +1006,14 @@ def main():
                 "traffic": load_traffic(kern_name, w),
                 "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 flops x max SM clock",
                 "flops_counted": "useful (4+3T) passes x 2d per causal pair"}
-        dtype = "f32"
+        dtype = "bf16 in, f32 compute" if w.dtype == "bf16" else "f32"
     else:
         peak = peaks["bf16_tflops"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": None if parallax else load_traffic(kern_name, w), "peak_source": f"{peak_kind} bf16 burst",
                 "flops_counted": ("useful 4 passes (q.k, weighted key mean, probe.k, values) x 2d per causal pair"
                                   if parallax else "useful (4+3T) passes x 2d per causal pair")}
-        dtype = "f16"
+        dtype = "bf16 in, f16 MMA operands (exact), f32 accumulate and CG state"
 
     line = {"metric": METRIC_PARALLAX if parallax else METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -886,12 +1023,17 @@ def main():
                        "path": {1: "tensor", 2: "fp32"}[rpath], "l2": "flushed before every step (512 MiB write)",
                        "inputs": "bf16 q,k,v resident in HBM" if w.dtype == "bf16" else "fp32 q,k,v in HBM"},
             "tflops": tflops,
-            "tflops_executed": world * (parallax_executed_flops(w, rpath == lla.LLA_PATH_TENSOR) if parallax else
-                                        executed_flops(w, T, rpath)) * args.steps / (total_ms / 1e3) / 1e12,
+            "tflops_executed": world * flops_exec * args.steps / (total_ms / 1e3) / 1e12,
             "roofline": roof, "clocks": clocks, "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
             "dominant_kernel": {"name": kern_name, "ms_per_launch": dominant_ms,
                                 "share_of_step": dominant_ms / ms_per_step},
             "cg_iters_counted": None if parallax else T}
+    if iters_info is not None:
+        line["cg_iterations"] = iters_info
+        line["roofline"]["flops_counted"] = ("useful (4+3T_t) passes x 2d over each query tile's causal pairs, "
+                                             "T_t the iterations that tile executed")
+    if w.name == "long_bf16" and world == 1 and not parallax:
+        line["memory"], line["n_scaling"] = memory_and_n_scaling(lla, w, path, dev, peak, flush)
     if parallax:
         line["config"]["workload"] = f"{w.name} B={w.B} H={w.H} n={w.n} d={w.d} tau={w.tau:.5g} (Parallax form, probe)"
         line["config"]["probe"] = "seeded RMS-normalised Gaussian rows / sqrt(d), fp32"

@@ -66,3 +66,37 @@ def test_traffic_is_tied_to_the_sources_and_scales_with_the_batch(tmp_path, monk
     assert bench.load_traffic("lla_tc_kernel", w.with_(n=2048)) is None
     monkeypatch.setattr(bench, "kernel_source_hash", lambda k: "0" * 16)
     assert bench.load_traffic("lla_tc_kernel", w) is None
+
+
+def test_tolerance_mode_flops_by_brute_force():
+    """Tolerance mode: each query tile runs as many CG sweeps as its slowest query; the useful
+    count sums (4 + 3 T_t) passes of 2d over each tile's causal pairs, checked pair by pair on a
+    ragged shape for both tile sizes."""
+    import numpy as np
+    w = workload("lm_bf16", B=2, H=2, n=75, d=16)
+    rng = np.random.default_rng(3)
+    its = rng.integers(0, 9, size=(w.B, w.H, w.n))
+    for path, rows in ((1, 128), (2, 32)):
+        useful = executed = 0
+        for b in range(w.B):
+            for h in range(w.H):
+                for i in range(w.n):
+                    t = i // rows
+                    T = its[b, h, t * rows:(t + 1) * rows].max()
+                    a = 8 if path == 1 else 6
+                    bb = 5 if path == 1 else 3
+                    useful += (4 + 3 * T) * 2 * w.d * (i + 1)
+                    executed += (a + bb * T) * 2 * w.d * (i + 1)
+        u, e, t_mean, t_pw = bench.tolerance_flops(w, its, path, precise=True)
+        assert u == useful and e == executed
+        T_tile, pairs = bench.tile_iterations(its, rows)
+        assert t_mean == T_tile.mean() and pairs.sum() == w.n * (w.n + 1) / 2
+        # a uniform count reduces to the fixed-cap formula
+        u1, _, _, t1 = bench.tolerance_flops(w, np.full_like(its, 5), path, precise=True)
+        assert u1 == bench.useful_flops(w, 5) and t1 == 5.0
+
+
+def test_iteration_histogram_counts_every_query():
+    import numpy as np
+    its = np.array([[[0, 3, 3, 64]]])
+    assert bench.iteration_histogram(its) == {"0": 1, "3": 2, "64": 1}
