@@ -124,30 +124,59 @@ __global__ void lla_maxabs_kernel(const __nv_bfloat16* __restrict__ q, const __n
     }
 }
 
+// Scaled fp16 copies, and |k_j|^2 of every key row (natural units, fp32) into knorm [slices][npad]
+// (rows of G = d/8 consecutive 8-element groups, summed over G lanes of a warp).  The loop's trip
+// count is uniform per warp, so every lane takes part in the row sums' shuffles.
 template <int NTEN>
 __global__ void lla_to_half_kernel(const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k,
                                    const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ g,
                                    __half* q16, __half* k16, __half* v16, __half* g16, size_t count8,
-                                   const Header* __restrict__ hdr) {
+                                   const Header* __restrict__ hdr, float* __restrict__ knorm, int G, int n, int npad) {
     const __nv_bfloat16* src[4] = {q, k, v, g};
     __half* dst[4] = {q16, k16, v16, g16};
     float sc[4];
 #pragma unroll
     for (int t = 0; t < NTEN; ++t) sc[t] = pow2i(scale_exp(__uint_as_float(hdr->maxabs[t])));
-    for (size_t idx = blockIdx.x * (size_t)blockDim.x + threadIdx.x; idx < count8; idx += (size_t)gridDim.x * blockDim.x) {
+    const int lane = threadIdx.x & 31;
+    const size_t stride = (size_t)gridDim.x * blockDim.x;      // a multiple of 32
+    for (size_t base = blockIdx.x * (size_t)blockDim.x + (threadIdx.x & ~31u); base < count8; base += stride) {
+        const size_t idx = base + lane;
+        const bool in = idx < count8;
+        float ss = 0.f;
+        if (in) {
 #pragma unroll
-        for (int t = 0; t < NTEN; ++t) {
-            const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src[t]) + idx);
-            const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
-            uint4 o;
-            uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+            for (int t = 0; t < NTEN; ++t) {
+                const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src[t]) + idx);
+                const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+                uint4 o;
+                uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float2 f = __bfloat1622float2(h[u]);
-                ow[u] = pack_half2(f.x * sc[t], f.y * sc[t]);
+                for (int u = 0; u < 4; ++u) {
+                    const float2 f = __bfloat1622float2(h[u]);
+                    ow[u] = pack_half2(f.x * sc[t], f.y * sc[t]);
+                    if (t == 1) ss = fmaf(f.x, f.x, fmaf(f.y, f.y, ss));
+                }
+                reinterpret_cast<uint4*>(dst[t])[idx] = o;
             }
-            reinterpret_cast<uint4*>(dst[t])[idx] = o;
         }
+        for (int o = G >> 1; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (in && (idx % (size_t)G) == 0) {
+            const size_t r = idx / (size_t)G;          // key row over all slices
+            knorm[(r / (size_t)n) * (size_t)npad + r % (size_t)n] = ss;
+        }
+    }
+}
+
+// |k_j|^2 of the 32 keys key0 .. key0+31 (key0 a multiple of 32; rows past n read the zeroed pad)
+__device__ __forceinline__ void load_knorm32(const float* __restrict__ kn_row, int key0, float (&kn)[32]) {
+    const float4* p = reinterpret_cast<const float4*>(kn_row + key0);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        const float4 t = __ldg(p + u);
+        kn[4 * u] = t.x;
+        kn[4 * u + 1] = t.y;
+        kn[4 * u + 2] = t.z;
+        kn[4 * u + 3] = t.w;
     }
 }
 
@@ -179,6 +208,7 @@ struct TcParams {
     Header* hdr;
     float* kbar;          // kbar, tile-transposed: [B*H][n_tiles][D][128] fp32 scratch
     float* xs;            // CG iterate rho', same layout
+    const float* knorm;   // |k_j|^2 per key row: [B*H][n_tiles * 128] fp32 (zero past n)
     __nv_bfloat16* out;
     float* rho;
     float* denom;
@@ -202,12 +232,18 @@ struct Xch {
     float (*buf)[2][BQ];
     int idx, half, row;
     __device__ float swap(float v) {
+        const float* b = put(v);
+        named_bar_sync(EW_BAR, NEW);
+        return take(b);
+    }
+    // The two halves of a swap, for an exchange that rides on a barrier taken anyway.
+    __device__ const float* put(float v) {
         float* b = &buf[idx][0][0];
         idx ^= 1;
         b[half * BQ + row] = v;
-        named_bar_sync(EW_BAR, NEW);
-        return b[(1 - half) * BQ + row];
+        return b;
     }
+    __device__ float take(const float* b) const { return b[(1 - half) * BQ + row]; }
     __device__ float sum(float v) { return v + swap(v); }
     __device__ float max(float v) { return fmaxf(v, swap(v)); }
 };
@@ -320,12 +356,39 @@ __device__ __forceinline__ void coef_chunk(const float (&v)[32], const float (&a
     }
 }
 
+// Forward moment sweep: weights out_j = 2^(s_j c - off), with the running sums of out_j and of
+// out_j |k_j|^2 (kn: the chunk's 32 key norms).  SPLIT: also the fp16 remainder of every weight.
+template <bool MASKED, bool SPLIT>
+__device__ __forceinline__ void coef_chunk_wk(const float (&v)[32], const float (&kn)[32], float c_log2, float off,
+                                              int col0, int lim, uint64_t& sum2, uint64_t& tk2, uint32_t (&pk)[16],
+                                              uint32_t* pl = nullptr) {
+    const uint64_t cc = f2_pack(c_log2, c_log2), oo = f2_pack(-off, -off);
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        float x0, x1;
+        f2_unpack(f2_fma(f2_pack(v[j], v[j + 1]), cc, oo), x0, x1);
+        float m0 = ex2(x0), m1 = ex2(x1);
+        if (MASKED) {
+            m0 = (col0 + j <= lim) ? m0 : 0.f;
+            m1 = (col0 + j + 1 <= lim) ? m1 : 0.f;
+        }
+        const uint64_t m = f2_pack(m0, m1);
+        sum2 = f2_add(sum2, m);
+        tk2 = f2_fma(m, f2_pack(kn[j], kn[j + 1]), tk2);
+        pk[j >> 1] = pack_half2(m0, m1);
+        if (SPLIT) {
+            const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&pk[j >> 1]));
+            pl[j >> 1] = pack_half2(m0 - h.x, m1 - h.y);
+        }
+    }
+}
+
 // Backward moment sweep: out_j = 2^(s_j c - off) (the weights, as the moment sweep), with the
-// running sums of out_j and of out_j a_j (a = H = G V^T, the per-pair dout.v).
+// running sums of out_j, of out_j a_j (a = H = G V^T, the per-pair dout.v) and of out_j |k_j|^2.
 template <bool MASKED, int C>
-__device__ __forceinline__ void coef_chunk_wh(const float (&v)[32], const float (&a)[64], float c_log2, float off,
-                                              int col0, int lim, uint64_t& sum2, uint64_t& wh2, uint32_t (&pk)[16],
-                                              uint32_t (&pl)[16]) {
+__device__ __forceinline__ void coef_chunk_wh(const float (&v)[32], const float (&a)[64], const float (&kn)[32],
+                                              float c_log2, float off, int col0, int lim, uint64_t& sum2, uint64_t& wh2,
+                                              uint64_t& tk2, uint32_t (&pk)[16], uint32_t (&pl)[16]) {
     const uint64_t cc = f2_pack(c_log2, c_log2), oo = f2_pack(-off, -off);
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
@@ -339,6 +402,7 @@ __device__ __forceinline__ void coef_chunk_wh(const float (&v)[32], const float 
         const uint64_t m = f2_pack(m0, m1);
         sum2 = f2_add(sum2, m);
         wh2 = f2_fma(m, f2_pack(a[C * 32 + j], a[C * 32 + j + 1]), wh2);
+        tk2 = f2_fma(m, f2_pack(kn[j], kn[j + 1]), tk2);
         pk[j >> 1] = pack_half2(m0, m1);
         const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&pk[j >> 1]));
         pl[j >> 1] = pack_half2(m0 - h.x, m1 - h.y);
@@ -687,7 +751,6 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const int ek = scale_exp(mk);
         const int ev = scale_exp(__uint_as_float(prm.hdr->maxabs[2]));
         const float c_log2 = prm.tau * 1.4426950408889634f * pow2i(-(eq + ek));
-        const float kbound = 2.f * (float)D * mk;      // |(k_j - kbar).u| <= kbound * max|u|
         uint32_t g = 0, yd = 0;
         bool ok = WAIT(&s.q_full, 0, err);
         const float a_none[64] = {};                   // placeholder operand of the moment sweep
@@ -711,14 +774,17 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             if (lane == 0) mbar_arrive(&s.a_free);
         };
         // P/R tile written: every thread fences its generic-proxy writes for the async proxy, the
-        // elementwise threads meet, and one thread arrives.
-        auto publish_p = [&](int next_type) {
+        // elementwise threads meet, and one thread arrives.  With WITH_V the meeting also sums v over
+        // the row's two halves (an exchange without a barrier of its own); returns that sum.
+        auto publish_p = [&](int next_type, bool with_v = false, float v = 0.f) {
+            const float* b = with_v ? xch.put(v) : nullptr;
             fence_proxy_async_smem();
             named_bar_sync(EW_BAR, NEW);
             if (tid == 128) {
                 s.next_type = next_type;
                 mbar_arrive(&s.p_ready);
             }
+            return with_v ? v + xch.take(b) : 0.f;
         };
         auto wait_y = [&]() {
             const bool r = WAIT(&s.y_done, yd & 1, err);
@@ -772,55 +838,63 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // ---------------- MOMENT sweep ----------------
         uint64_t om_part = 0;              // two fp32 partial sums (bit pattern 0 = +0.0f, +0.0f)
         uint64_t wh_part = 0;              // backward: sum of w h
+        uint64_t tk_part = 0;              // sum of w |k|^2 (the key scatter's trace, below)
+        const float* kn_row = prm.knorm + (size_t)head * (prm.n_tiles * BQ) + half * 64;
         for (int kb = 0; kb < nkb; ++kb, ++g) {
             ok = ok && wait_s(g);
             const uint32_t tS = tS0 + (g & 1) * 128 + lane_off + half * 64;
             const int lim = lim_of(kb);
             const bool masked = !(tile_full && kb < tile);
-            float v[32];
+            float v[32], kn[32];
             uint32_t pk[16];
             if (BWD) {
                 float a[64];
                 tmem_ld32(tA + lane_off + half * 64, *reinterpret_cast<float(*)[32]>(&a[0]));
                 tmem_ld32(tA + lane_off + half * 64 + 32, *reinterpret_cast<float(*)[32]>(&a[32]));
                 tmem_ld32(tS, v);
+                load_knorm32(kn_row, kb * BK, kn);
                 tmem_ld_wait();
                 release_a();
                 uint32_t pl[16];            // hi + lo weights, split layout (gemm_y_split)
-                if (masked) coef_chunk_wh<true, 0>(v, a, c_log2, m2 - 14.f, half * 64, lim, om_part, wh_part, pk, pl);
-                else coef_chunk_wh<false, 0>(v, a, c_log2, m2 - 14.f, 0, 0, om_part, wh_part, pk, pl);
+                if (masked) coef_chunk_wh<true, 0>(v, a, kn, c_log2, m2 - 14.f, half * 64, lim, om_part, wh_part, tk_part, pk, pl);
+                else coef_chunk_wh<false, 0>(v, a, kn, c_log2, m2 - 14.f, 0, 0, om_part, wh_part, tk_part, pk, pl);
                 tmem_st16(tS, pk);
                 tmem_st16(tS + 16, pl);
                 tmem_ld32(tS + 32, v);
+                load_knorm32(kn_row, kb * BK + 32, kn);
                 tmem_ld_wait();
-                if (masked) coef_chunk_wh<true, 1>(v, a, c_log2, m2 - 14.f, half * 64 + 32, lim, om_part, wh_part, pk, pl);
-                else coef_chunk_wh<false, 1>(v, a, c_log2, m2 - 14.f, 0, 0, om_part, wh_part, pk, pl);
+                if (masked) coef_chunk_wh<true, 1>(v, a, kn, c_log2, m2 - 14.f, half * 64 + 32, lim, om_part, wh_part, tk_part, pk, pl);
+                else coef_chunk_wh<false, 1>(v, a, kn, c_log2, m2 - 14.f, 0, 0, om_part, wh_part, tk_part, pk, pl);
                 tmem_st16(tS + 32, pk);
                 tmem_st16(tS + 48, pl);
             } else if constexpr (PREC) {    // hi + lo weights, split layout (gemm_y_split)
                 uint32_t pl[16];
                 tmem_ld32(tS, v);
+                load_knorm32(kn_row, kb * BK, kn);
                 tmem_ld_wait();
-                if (masked) coef_chunk<true, false, 0, true>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, half * 64, lim, om_part, pk, pl);
-                else coef_chunk<false, false, 0, true>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, 0, 0, om_part, pk, pl);
+                if (masked) coef_chunk_wk<true, true>(v, kn, c_log2, m2 - 14.f, half * 64, lim, om_part, tk_part, pk, pl);
+                else coef_chunk_wk<false, true>(v, kn, c_log2, m2 - 14.f, 0, 0, om_part, tk_part, pk, pl);
                 tmem_st16(tS, pk);
                 tmem_st16(tS + 16, pl);
                 tmem_ld32(tS + 32, v);
+                load_knorm32(kn_row, kb * BK + 32, kn);
                 tmem_ld_wait();
-                if (masked) coef_chunk<true, false, 0, true>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, half * 64 + 32, lim, om_part, pk, pl);
-                else coef_chunk<false, false, 0, true>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, 0, 0, om_part, pk, pl);
+                if (masked) coef_chunk_wk<true, true>(v, kn, c_log2, m2 - 14.f, half * 64 + 32, lim, om_part, tk_part, pk, pl);
+                else coef_chunk_wk<false, true>(v, kn, c_log2, m2 - 14.f, 0, 0, om_part, tk_part, pk, pl);
                 tmem_st16(tS + 32, pk);
                 tmem_st16(tS + 48, pl);
             } else {
                 tmem_ld32(tS, v);
+                load_knorm32(kn_row, kb * BK, kn);
                 tmem_ld_wait();
-                if (masked) coef_chunk<true, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, half * 64, lim, om_part, pk);
-                else coef_chunk<false, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, 0, 0, om_part, pk);
+                if (masked) coef_chunk_wk<true, false>(v, kn, c_log2, m2 - 14.f, half * 64, lim, om_part, tk_part, pk);
+                else coef_chunk_wk<false, false>(v, kn, c_log2, m2 - 14.f, 0, 0, om_part, tk_part, pk);
                 tmem_st16(tS, pk);
                 tmem_ld32(tS + 32, v);
+                load_knorm32(kn_row, kb * BK + 32, kn);
                 tmem_ld_wait();
-                if (masked) coef_chunk<true, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, half * 64 + 32, lim, om_part, pk);
-                else coef_chunk<false, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, 0, 0, om_part, pk);
+                if (masked) coef_chunk_wk<true, false>(v, kn, c_log2, m2 - 14.f, half * 64 + 32, lim, om_part, tk_part, pk);
+                else coef_chunk_wk<false, false>(v, kn, c_log2, m2 - 14.f, 0, 0, om_part, tk_part, pk);
                 tmem_st16(tS + 16, pk);
             }
             tmem_st_wait();
@@ -828,6 +902,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
         ok = ok && wait_y();
         const float om_all = xch.sum(f2_total(om_part));      // every elementwise thread joins the exchange
+        const float tk_all = xch.sum(f2_total(tk_part));      // sum_j w_j |k_j|^2, weights in units of 2^-14
         const float omega = row_ok ? om_all * pow2i(-14) : 1.f;
         const float inv_om = 1.f / omega;
         const float lam_n = prm.lambda * inv_om;
@@ -849,38 +924,48 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // bit; kbar.res is recomputed, not updated, because a converging residual cancels.
         float kbr = 0.f, kpx = 0.f;
         int cg_sweeps = 0;
-        // New direction p = res + beta p_old, stored in the direction tile as fp16 x 2^sp (hi, and
-        // lo when SPLITC, the direction's form).  First pass: p into PN (DH floats of registers) and max |p|, which
-        // fixes sp; with XUPD it also stores x = XO + ALPHA p_old, p_old being the direction of
-        // the sweep just finished and XO (DH floats) the previous x.  Second pass: pack and store.
-#define LLA_SET_DIRECTION(BETA, KEEP, XUPD, ALPHA, PN, XO, SPLITC)                                         \
+        // Bound for the fp16 scales of the per-pair coefficients: |w_j (k_j - kbar).u| <= cbound |u|_2.
+        // With the key scatter's trace T = sum_j w_j |k_j - kbar|^2 = sum_j w_j |k_j|^2 - omega |kbar|^2
+        // and w_j <= 1, w_j |k_j - kbar| <= sqrt(w_j |k_j - kbar|^2) <= sqrt(T).
+        // T is taken with 2^-9 of sum_j w_j |k_j|^2 added (it covers the cancellation, and kbar's error
+        // from its fp16 weights), and 2^-8 |kbar| covers the rounded direction's kbar.u offset.  Rows whose
+        // weights sit on a few keys far from the others keep their coefficients in fp16's normal range,
+        // which a bound from max|k| alone does not.
+        float cbound = 0.f;
+        auto set_cbound = [&](float kk) {
+            const float tsum = row_ok ? tk_all * pow2i(-14) : 0.f;
+            const float tr = fmaxf(tsum - omega * kk, 0.f) + tsum * pow2i(-9);
+            cbound = (sqrtf(tr) + sqrtf(kk) * pow2i(-8)) * 1.001f;
+        };
+        // New direction p = res + beta p_old, stored in the direction tile as fp16 x 2^sp (hi, and lo when
+        // SPLITC, the direction's form), in one pass.  MPB (row-level) bounds |p|_2, hence max|p|, so the
+        // scale needs no exchange of the row maximum: |p|_2 <= |res|_2 + |beta| |p_old|_2, with |p_old|_2
+        // carried as its own bound (pn2).  With XUPD the pass also updates this thread's x = rho' to
+        // x + ALPHA p_old (XO: a previous x exists; else it starts from 0), p_old being the direction of the
+        // sweep just finished.  The scale sM of the
+        // next sweep's coefficients follows from the same bound; kbar.p (kp_acc) is set by set_kp once
+        // kbar.res of the whole row is known.
+        float pn2 = 0.f;
+#define LLA_SET_DIRECTION(BETA, KEEP, XUPD, ALPHA, XO, SPLITC, MPB)                                        \
         {                                                                                                  \
             const float osc_ = pow2i(-sp);                                                                 \
             const uint64_t b2_ = f2_pack((BETA), (BETA));                                                  \
-            float mp_ = 0.f;                                                                               \
+            const int sp_new_ = min(scale_exp((MPB) * 1.001f), 100 - ek);   /* keeps 2^(sp+ek) finite */  \
+            const uint64_t nsc2_ = f2_pack(pow2i(sp_new_), pow2i(sp_new_));                                \
             _Pragma("unroll") for (int e0 = 0; e0 < DH; e0 += 8) {                                         \
                 float po_[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};                                   \
                 if (KEEP) load_dir8(s.p, s.rlo, SPLITC, row, half * DH + e0, osc_, po_);                   \
                 if (XUPD) {                                                                                \
                     _Pragma("unroll") for (int u = 0; u < 8; ++u)                                          \
-                        xt[(e0 + u) * BQ] = fmaf((ALPHA), po_[u], XO[e0 + u]);                             \
+                        xt[(e0 + u) * BQ] = fmaf((ALPHA), po_[u], (XO) ? xt[(e0 + u) * BQ] : 0.f);          \
                 }                                                                                          \
-                _Pragma("unroll") for (int u = 0; u < 8; u += 2) {                                         \
-                    f2_unpack(f2_fma(b2_, f2_pack(po_[u], po_[u + 1]), f2_pack(res[e0 + u], res[e0 + u + 1])), \
-                              PN[e0 + u], PN[e0 + u + 1]);                                                 \
-                    mp_ = fmaxf(mp_, fmaxf(fabsf(PN[e0 + u]), fabsf(PN[e0 + u + 1])));                    \
-                }                                                                                          \
-            }                                                                                              \
-            mp_ = xch.max(mp_);                                                                            \
-            const int sp_new_ = min(scale_exp(mp_), 100 - ek);   /* keeps 2^(sp+ek) finite */             \
-            const uint64_t nsc2_ = f2_pack(pow2i(sp_new_), pow2i(sp_new_));                                \
-            _Pragma("unroll") for (int e0 = 0; e0 < DH; e0 += 8) {                                         \
                 uint4 hk_, lk_;                                                                            \
                 uint32_t* hw_ = reinterpret_cast<uint32_t*>(&hk_);                                         \
                 uint32_t* lw_ = reinterpret_cast<uint32_t*>(&lk_);                                         \
                 _Pragma("unroll") for (int u = 0; u < 8; u += 2) {                                         \
                     float x0_, x1_;                                                                        \
-                    f2_unpack(f2_mul(f2_pack(PN[e0 + u], PN[e0 + u + 1]), nsc2_), x0_, x1_);               \
+                    f2_unpack(f2_mul(f2_fma(b2_, f2_pack(po_[u], po_[u + 1]),                              \
+                                            f2_pack(res[e0 + u], res[e0 + u + 1])), nsc2_), x0_, x1_);     \
                     hw_[u >> 1] = pack_half2(x0_, x1_);                                                    \
                     const float2 hf_ = __half22float2(*reinterpret_cast<const __half2*>(&hw_[u >> 1]));   \
                     lw_[u >> 1] = pack_half2(x0_ - hf_.x, x1_ - hf_.y);                                    \
@@ -889,23 +974,32 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 if (SPLITC) *reinterpret_cast<uint4*>(tile_half(s.rlo, row, half * DH + e0)) = lk_;        \
             }                                                                                              \
             sp = sp_new_;                                                                                  \
-            sM = scale_exp(kbound * mp_ * 1.001f);                                                         \
+            pn2 = (MPB);                                                                                   \
+            sM = scale_exp(cbound * (MPB));                                                                \
             offM = m2 - (float)sM + (float)sp + (float)ek;                                                 \
-            kpx = kbr + (BETA) * kpx;                                                                      \
-            kp_acc = kpx * pow2i(sp + ek);                                                                 \
         }
+        // kbar.p of the new direction by recurrence (p = res + beta p_old), in the units of the A' product
+        auto set_kp = [&](float beta) {
+            kpx = kbr + beta * kpx;
+            kp_acc = kpx * pow2i(sp + ek);
+        };
         if constexpr (BWD) {
             // kbar from the moment sweep's Y, before the TBAR sweep reuses the accumulator
             {
                 const float ysc = pow2i(-(14 + ek)) * inv_om;
+                float kk = 0.f;
 #pragma unroll
                 for (int c = 0; c < DH / 32; ++c) {
                     float v[32];
                     tmem_ld32(tY + lane_off + half * DH + c * 32, v);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) kbt[(c * 32 + j) * BQ] = v[j] * ysc;
+                    for (int j = 0; j < 32; ++j) {
+                        kbt[(c * 32 + j) * BQ] = v[j] * ysc;
+                        kk = fmaf(v[j] * ysc, v[j] * ysc, kk);
+                    }
                 }
+                set_cbound(xch.sum(row_ok ? kk : 0.f));
             }
             // ---------------- TBAR sweep: Y = sum_j w_j (h_j - hbar) k_j ----------------
             // coefficient w (h - hbar) 2^sT; |h - hbar| <= 2 D max|dout| max|v| fixes sT
@@ -963,8 +1057,8 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             kbr = xch.sum(kr);
             rn0 = sqrtf(gamma);
             active = row_ok && gamma > 0.f && !(sqrtf(gamma) <= prm.cg_tol * rn0);
-            float pn[DH];
-            LLA_SET_DIRECTION(0.f, false, false, 0.f, pn, pn, split_p);
+            LLA_SET_DIRECTION(0.f, false, false, 0.f, false, split_p, sqrtf(gamma));
+            set_kp(0.f);
         } else {
             float kv[DH];
             const float ysc = pow2i(-(14 + ek)) * inv_om;
@@ -987,27 +1081,36 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     }
                 }
             }
-            float gp = 0.f, kr = 0.f;
+            float gp = 0.f, kr = 0.f, kk = 0.f;
 #pragma unroll
             for (int e = 0; e < DH; ++e) {
                 gp = fmaf(res[e], res[e], gp);
                 kr = fmaf(kv[e], res[e], kr);
+                kk = fmaf(kv[e], kv[e], kk);
             }
             gamma = xch.sum(gp);
             kbr = xch.sum(kr);
+            set_cbound(xch.sum(row_ok ? kk : 0.f));
             rn0 = sqrtf(gamma);
             active = row_ok && gamma > 0.f && !(sqrtf(gamma) <= prm.cg_tol * rn0);
-            float pn[DH];
-            LLA_SET_DIRECTION(0.f, false, false, 0.f, pn, pn, split_p);
+            LLA_SET_DIRECTION(0.f, false, false, 0.f, false, split_p, sqrtf(gamma));
+            set_kp(0.f);
         }
 
         // ---------------- CG sweeps ----------------
+        const float* kr_pend = nullptr;        // this half's kbar.res of the last update, in the exchange buffer
+        float beta_pend = 0.f;
         while (true) {                         // uniform across the elementwise threads
             bool go;
             if (!dynamic) go = cg_sweeps < prm.cg_max_iters;
             else go = ew_any(active) && cg_sweeps < prm.cg_max_iters;
             if (!go) break;
+            // the publishing barrier also sums kbar.res over the row, for kbar.p of the new direction
             publish_p(SW_CG);
+            if (cg_sweeps > 0) {
+                kbr = xch.take(kr_pend) + kr_pend[half * BQ + row];
+                set_kp(beta_pend);
+            }
             ++cg_sweeps;
             uint64_t msum_part = 0;
             for (int kb = 0; kb < nkb; ++kb, ++g) {
@@ -1113,18 +1216,12 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 LLA_CG_STEP(3, c1, c0);
 #undef LLA_CG_STEP
             }
-            // the previous x (this thread's own scratch), loaded while the exchange below waits
-            float xo[DH];
-#pragma unroll
-            for (int e = 0; e < DH; ++e) xo[e] = cg_sweeps > 1 ? xt[e * BQ] : 0.f;
             const float g2 = xch.sum(f2_total(g22));       // res.res
-            const float kbr_new = xch.sum(f2_total(kr2));  // kbar.res
             float beta = 0.f;
             if (upd) {
                 beta = g2 / gamma;
                 gamma = g2;
                 ++iters;
-                kbr = kbr_new;
                 if (gamma == 0.f || sqrtf(gamma) <= prm.cg_tol * rn0) active = false;
             } else {
                 active = false;
@@ -1133,12 +1230,18 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
                 for (int e = 0; e < DH; ++e) res[e] = 0.f;   // finished rows keep a zero direction
                 beta = 0.f;
-                kbr = 0.f;
             }
-            float pn[DH];
+            // this half's kbar.res goes to the exchange buffer now and is read after the next publishing
+            // barrier.  Buffers alternate: this one last held the p.Cp exchange, which the partner read
+            // before the res.res barrier above; the next write to it comes after the following sweep's
+            // y_done, which needs both halves past the read.
+            kr_pend = xch.put(active ? f2_total(kr2) : 0.f);
+            beta_pend = beta;
+            const float mpb = active ? sqrtf(gamma) + fabsf(beta) * pn2 : 0.f;   // bounds |p_new|_2
             // the form as a constant: the loops over the coordinates carry no branch on it
-            if (split_p) LLA_SET_DIRECTION(beta, true, true, alpha, pn, xo, true)
-            else LLA_SET_DIRECTION(beta, true, true, alpha, pn, xo, false)
+            const bool have_xo = cg_sweeps > 1;
+            if (split_p) LLA_SET_DIRECTION(beta, true, true, alpha, have_xo, true, mpb)
+            else LLA_SET_DIRECTION(beta, true, true, alpha, have_xo, false, mpb)
         }
 
         if constexpr (BWD) {
@@ -1251,7 +1354,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 prm.denom[(size_t)head * n + i] = omega * inv_g;
                 if (prm.cg_iters) prm.cg_iters[(size_t)head * n + i] = iters;
             }
-            const int sU = scale_exp((1.f + kbound * mxx) * 1.001f);
+            const int sU = scale_exp((1.f + cbound * sqrtf((float)D) * mxx) * 1.001f);   // |rho'|_2 <= sqrt(D) max
             const float offU = m2 - (float)sU + (float)sr + (float)ek;
             const float c_acc = (1.f + kx) * pow2i(sr + ek);
             publish_p(SW_OUT);
@@ -1320,8 +1423,10 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 struct TcWs {
     Header* hdr;
     __half *q16, *k16, *v16, *g16;
-    float *kbar, *xs;
+    float *kbar, *xs, *knorm;
 };
+// Parts, each 256-byte aligned: header, q16, k16, v16, (g16), kbar and x ([slices][tiles][D][128]
+// fp32), knorm ([slices][tiles * 128] fp32).  N = B H n D, NT = B H (tiles * 128) D.
 TcWs carve(void* ws, size_t N, size_t NT, bool bwd) {
     unsigned char* base = static_cast<unsigned char*>(ws);
     TcWs w;
@@ -1333,7 +1438,8 @@ TcWs carve(void* ws, size_t N, size_t NT, bool bwd) {
     w.g16 = nullptr;
     if (bwd) { w.g16 = reinterpret_cast<__half*>(base + off); off += align256(N * 2); }
     w.kbar = reinterpret_cast<float*>(base + off); off += align256(NT * 4);
-    w.xs = reinterpret_cast<float*>(base + off);
+    w.xs = reinterpret_cast<float*>(base + off); off += align256(NT * 4);
+    w.knorm = reinterpret_cast<float*>(base + off);
     return w;
 }
 
@@ -1347,6 +1453,12 @@ cudaError_t launch_d(int B, int H, int n, const void* qv, const void* kv, const 
     const TcWs w = carve(ws, N, NT, BWD);
     cudaError_t e = cudaMemsetAsync(w.hdr, 0, HDR_BYTES, stream);
     if (e != cudaSuccess) { *why = "workspace header clear"; return e; }
+    const int n_tiles = (n + BQ - 1) / BQ;
+    const size_t knorm_bytes = (size_t)B * H * n_tiles * BQ * 4;
+    if (n % BQ && (e = cudaMemsetAsync(w.knorm, 0, knorm_bytes, stream)) != cudaSuccess) {   // the pad past n
+        *why = "workspace key-norm clear";
+        return e;
+    }
     const size_t count8 = N / 8;
     const int pre_blocks = (int)((count8 + 255) / 256 < 152 * 8 ? (count8 + 255) / 256 : 152 * 8);
     const __nv_bfloat16* q = static_cast<const __nv_bfloat16*>(qv);
@@ -1354,7 +1466,8 @@ cudaError_t launch_d(int B, int H, int n, const void* qv, const void* kv, const 
     const __nv_bfloat16* v = static_cast<const __nv_bfloat16*>(vv);
     const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(gv);
     lla_maxabs_kernel<BWD ? 4 : 3><<<pre_blocks, 256, 0, stream>>>(q, k, v, g, count8, w.hdr);
-    lla_to_half_kernel<BWD ? 4 : 3><<<pre_blocks, 256, 0, stream>>>(q, k, v, g, w.q16, w.k16, w.v16, w.g16, count8, w.hdr);
+    lla_to_half_kernel<BWD ? 4 : 3><<<pre_blocks, 256, 0, stream>>>(q, k, v, g, w.q16, w.k16, w.v16, w.g16, count8, w.hdr,
+                                                                     w.knorm, D / 8, n, n_tiles * BQ);
     e = cudaGetLastError();
     if (e != cudaSuccess) { *why = "operand pre-pass launch"; return e; }
 
@@ -1369,6 +1482,7 @@ cudaError_t launch_d(int B, int H, int n, const void* qv, const void* kv, const 
     prm.hdr = w.hdr;
     prm.kbar = w.kbar;
     prm.xs = w.xs;
+    prm.knorm = w.knorm;
     prm.dev_err = device_error_word();
     prm.n = n;
     prm.n_tiles = (n + BQ - 1) / BQ;
@@ -1409,7 +1523,7 @@ TcParams forward_params(const Problem& p) {
 size_t tensor_workspace_bytes(int B, int H, int n, int d) {
     const size_t N = (size_t)B * H * n * d;
     const size_t NT = (size_t)B * H * ((n + BQ - 1) / BQ) * BQ * d;
-    return HDR_BYTES + 3 * align256(N * 2) + 2 * align256(NT * 4);
+    return HDR_BYTES + 3 * align256(N * 2) + 2 * align256(NT * 4) + align256(NT / d * 4);
 }
 
 // Tolerance mode (cg_tol > 0) takes the precise form: CG run to a relative residual needs matrix-vector
