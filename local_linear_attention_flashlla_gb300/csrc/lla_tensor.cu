@@ -199,6 +199,7 @@ struct TcSmem {
     uint32_t tmem_base;
     int err;
     int next_type;
+    int out_split;                                     // the output sweep's T takes R_lo as well
 };
 
 // 227 KB: the most dynamic shared memory a block may have on sm_103a
@@ -668,8 +669,11 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     tc_fence_after();
                     const uint32_t b_addr = smem_u32(s.slot[(hprod ? fv : fk) % NSLOT]);
                     gemm_qk<D, false>(tA, p_addr, b_addr);
-                    // T = (R_hi + R_lo) K^T; in the first tile also A' = (P_hi + P_lo) K^T
-                    if (!hprod && (type == SW_OUT || tile == 0 || BWD || PREC)) gemm_qk<D, true>(tA, rlo_addr, b_addr);
+                    // A' = (P_hi + P_lo) K^T where the direction carries a remainder (first tile, backward,
+                    // precise form); T = (R_hi + R_lo) K^T where the elementwise threads asked for it
+                    const bool lo_prod = type == SW_OUT ? *reinterpret_cast<volatile int*>(&s.out_split) != 0
+                                                        : (tile == 0 || BWD || PREC);
+                    if (!hprod && lo_prod) gemm_qk<D, true>(tA, rlo_addr, b_addr);
                     umma_commit(&s.s_full[g & 1]);
                 }
                 if (type == SW_OUT) break;
@@ -931,11 +935,12 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // from its fp16 weights), and 2^-8 |kbar| covers the rounded direction's kbar.u offset.  Rows whose
         // weights sit on a few keys far from the others keep their coefficients in fp16's normal range,
         // which a bound from max|k| alone does not.
-        float cbound = 0.f;
+        float cbound = 0.f, tr_om = 0.f;     // tr_om: the trace over omega, sum_j wbar_j |k_j - kbar|^2
         auto set_cbound = [&](float kk) {
             const float tsum = row_ok ? tk_all * pow2i(-14) : 0.f;
             const float tr = fmaxf(tsum - omega * kk, 0.f) + tsum * pow2i(-9);
             cbound = (sqrtf(tr) + sqrtf(kk) * pow2i(-8)) * 1.001f;
+            tr_om = tr * inv_om;
         };
         // New direction p = res + beta p_old, stored in the direction tile as fp16 x 2^sp (hi, and lo when
         // SPLITC, the direction's form), in one pass.  MPB (row-level) bounds |p|_2, hence max|p|, so the
@@ -1301,7 +1306,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     xv[e0] = t.x; xv[e0 + 1] = t.y; xv[e0 + 2] = t.z; xv[e0 + 3] = t.w;
                 }
             }
-            float dx = 0.f, mxx = 0.f;
+            float dx = 0.f, xx = 0.f;
             {
                 const float qsc = pow2i(-eq);
 #pragma unroll
@@ -1311,15 +1316,20 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #pragma unroll
                     for (int u = 0; u < 8; ++u) {
                         dx = fmaf(kv[e0 + u] - __half2float(qh[u]) * qsc, xv[e0 + u], dx);
-                        mxx = fmaxf(mxx, fabsf(xv[e0 + u]));
+                        xx = fmaf(xv[e0 + u], xv[e0 + u], xx);
                     }
                 }
-                if (!row_ok) { dx = 0.f; mxx = 0.f; }
+                if (!row_ok) { dx = 0.f; xx = 0.f; }
             }
             dx = xch.sum(dx);
-            mxx = xch.max(mxx);
+            const float xn = sqrtf(xch.sum(xx));                 // |rho'|_2, which bounds max|rho'|
             const float inv_g = 1.f / (1.f + dx);
-            const int sr = min(scale_exp(mxx), 100 - ek);
+            const int sr = min(scale_exp(xn * 1.001f), 100 - ek);
+            // R_lo (one more product per output block) only where rounding rho' to fp16 could move the
+            // output by more than 2^-9 RMS(v): the output moves by the value/key covariance times the
+            // rounding error, at most sqrt(tr_om) |rho'|_2 2^-11 (in RMS(v)).  The first tile (rank-
+            // deficient scatter) and the precise form always take it.
+            const bool split_r = PREC || tile == 0 || ew_any(row_ok && sqrtf(tr_om) * xn > 4.f);
             float kx = 0.f;
             {
                 const float rs = pow2i(sr), ris = pow2i(-sr);
@@ -1334,12 +1344,13 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                         pw[u >> 1] = pack_half2(x0, x1);
                         const float2 xh = __half22float2(*reinterpret_cast<const __half2*>(&pw[u >> 1]));
                         plw[u >> 1] = pack_half2(x0 - xh.x, x1 - xh.y);
-                        const float2 xl = __half22float2(*reinterpret_cast<const __half2*>(&plw[u >> 1]));
-                        kx = fmaf(kv[e0 + u], (xh.x + xl.x) * ris, kx);
+                        const float2 xl = split_r ? __half22float2(*reinterpret_cast<const __half2*>(&plw[u >> 1]))
+                                                  : make_float2(0.f, 0.f);
+                        kx = fmaf(kv[e0 + u], (xh.x + xl.x) * ris, kx);        // kbar . R as the products see R
                         kx = fmaf(kv[e0 + u + 1], (xh.y + xl.y) * ris, kx);
                     }
                     *reinterpret_cast<uint4*>(tile_half(s.p, row, half * DH + e0)) = pk;
-                    *reinterpret_cast<uint4*>(tile_half(s.rlo, row, half * DH + e0)) = pl;
+                    if (split_r) *reinterpret_cast<uint4*>(tile_half(s.rlo, row, half * DH + e0)) = pl;
                     if (row_ok && !prm.probe) {   // rho = rho' / (1 + delta.rho'), row-major output
                         *reinterpret_cast<float4*>(prm.rho + row_g + e0) =
                             make_float4(xv[e0] * inv_g, xv[e0 + 1] * inv_g, xv[e0 + 2] * inv_g, xv[e0 + 3] * inv_g);
@@ -1354,9 +1365,10 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 prm.denom[(size_t)head * n + i] = omega * inv_g;
                 if (prm.cg_iters) prm.cg_iters[(size_t)head * n + i] = iters;
             }
-            const int sU = scale_exp((1.f + cbound * sqrtf((float)D) * mxx) * 1.001f);   // |rho'|_2 <= sqrt(D) max
+            const int sU = scale_exp((1.f + cbound * xn) * 1.001f);
             const float offU = m2 - (float)sU + (float)sr + (float)ek;
             const float c_acc = (1.f + kx) * pow2i(sr + ek);
+            if (tid == 128) s.out_split = split_r ? 1 : 0;      // read by the T issuer after the publishing barrier
             publish_p(SW_OUT);
 
             // ---------------- OUT sweep ----------------
