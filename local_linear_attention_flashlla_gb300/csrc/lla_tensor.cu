@@ -464,7 +464,9 @@ __device__ __forceinline__ void gemm_y_split(uint32_t y_tmem, uint32_t m_tmem, u
 // PREC (forward only): the precise form used in tolerance mode.  The moment sweep's weights and the
 // CG sweeps' per-pair coefficients are fp16 hi + lo pairs (two TS products per block) and the CG
 // direction is hi + lo in every tile, so each carries about 22 bits, as in the backward mode.
-template <int D, bool BWD, bool PREC = false>
+// PROBE: the Parallax form (caller's probe, no CG).  It needs no key-scatter trace: its output sweep's
+// coefficient bound comes from max|k| alone, and it always carries the probe's fp16 remainder.
+template <int D, bool BWD, bool PREC = false, bool PROBE = false>
 __global__ void __launch_bounds__(NTHREADS, 1)
 lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g, const TcParams prm) {
@@ -887,6 +889,17 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 else coef_chunk_wk<false, true>(v, kn, c_log2, m2 - 14.f, 0, 0, om_part, tk_part, pk, pl);
                 tmem_st16(tS + 32, pk);
                 tmem_st16(tS + 48, pl);
+            } else if constexpr (PROBE) {   // weights only (the probe form takes no key norms)
+                tmem_ld32(tS, v);
+                tmem_ld_wait();
+                if (masked) coef_chunk<true, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, half * 64, lim, om_part, pk);
+                else coef_chunk<false, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, 0, 0, om_part, pk);
+                tmem_st16(tS, pk);
+                tmem_ld32(tS + 32, v);
+                tmem_ld_wait();
+                if (masked) coef_chunk<true, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, half * 64 + 32, lim, om_part, pk);
+                else coef_chunk<false, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, 0, 0, om_part, pk);
+                tmem_st16(tS + 16, pk);
             } else {
                 tmem_ld32(tS, v);
                 load_knorm32(kn_row, kb * BK, kn);
@@ -1329,7 +1342,9 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             // output by more than 2^-9 RMS(v): the output moves by the value/key covariance times the
             // rounding error, at most sqrt(tr_om) |rho'|_2 2^-11 (in RMS(v)).  The first tile (rank-
             // deficient scatter) and the precise form always take it.
-            const bool split_r = PREC || tile == 0 || ew_any(row_ok && sqrtf(tr_om) * xn > 4.f);
+            bool split_r;
+            if constexpr (PROBE) split_r = true;
+            else split_r = PREC || tile == 0 || ew_any(row_ok && sqrtf(tr_om) * xn > 4.f);
             float kx = 0.f;
             {
                 const float rs = pow2i(sr), ris = pow2i(-sr);
@@ -1365,7 +1380,10 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 prm.denom[(size_t)head * n + i] = omega * inv_g;
                 if (prm.cg_iters) prm.cg_iters[(size_t)head * n + i] = iters;
             }
-            const int sU = scale_exp((1.f + cbound * xn) * 1.001f);
+            int sU;
+            // the probe form: |k_j - kbar|_2 <= 2 sqrt(D) max|k| (no key scatter trace was taken)
+            if constexpr (PROBE) sU = scale_exp((1.f + 2.f * sqrtf((float)D) * mk * xn) * 1.001f);
+            else sU = scale_exp((1.f + cbound * xn) * 1.001f);
             const float offU = m2 - (float)sU + (float)sr + (float)ek;
             const float c_acc = (1.f + kx) * pow2i(sr + ek);
             if (tid == 128) s.out_split = split_r ? 1 : 0;      // read by the T issuer after the publishing barrier
@@ -1456,7 +1474,7 @@ TcWs carve(void* ws, size_t N, size_t NT, bool bwd) {
 }
 
 // Pre-pass, tensor maps and the sweep kernel.  BWD: the backward's stats stage (g = dout).
-template <int D, bool BWD, bool PREC = false>
+template <int D, bool BWD, bool PREC = false, bool PROBE = false>
 cudaError_t launch_d(int B, int H, int n, const void* qv, const void* kv, const void* vv, const void* gv,
                      TcParams prm, void* ws, cudaEvent_t ev_begin, cudaEvent_t ev_end, cudaStream_t stream,
                      const char** why) {
@@ -1501,7 +1519,7 @@ cudaError_t launch_d(int B, int H, int n, const void* qv, const void* kv, const 
     if (!prm.dev_err) { *why = "device error word"; return cudaErrorInvalidSymbol; }
 
     const size_t smem = sizeof(TcSmem<D>);
-    auto kern = lla_tc_kernel<D, BWD, PREC>;
+    auto kern = lla_tc_kernel<D, BWD, PREC, PROBE>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) { *why = "tensor kernel shared-memory attribute"; return e; }
     dim3 grid(prm.n_tiles, (unsigned)slices);
@@ -1543,16 +1561,24 @@ size_t tensor_workspace_bytes(int B, int H, int n, int d) {
 cudaError_t launch_tensor(const Problem& p, void* ws, cudaStream_t stream, const char** why) {
     const TcParams prm = forward_params(p);
     const bool prec = p.cg_tol > 0.f && !p.probe;
-    if (p.d == 128)
+    if (p.d == 128) {
+        if (p.probe)
+            return launch_d<128, false, false, true>(p.B, p.H, p.n, p.q, p.k, p.v, nullptr, prm, ws, p.ev_main_begin,
+                                                     p.ev_main_end, stream, why);
         return prec ? launch_d<128, false, true>(p.B, p.H, p.n, p.q, p.k, p.v, nullptr, prm, ws, p.ev_main_begin,
                                                  p.ev_main_end, stream, why)
                     : launch_d<128, false>(p.B, p.H, p.n, p.q, p.k, p.v, nullptr, prm, ws, p.ev_main_begin,
                                            p.ev_main_end, stream, why);
-    if (p.d == 64)
+    }
+    if (p.d == 64) {
+        if (p.probe)
+            return launch_d<64, false, false, true>(p.B, p.H, p.n, p.q, p.k, p.v, nullptr, prm, ws, p.ev_main_begin,
+                                                    p.ev_main_end, stream, why);
         return prec ? launch_d<64, false, true>(p.B, p.H, p.n, p.q, p.k, p.v, nullptr, prm, ws, p.ev_main_begin,
                                                 p.ev_main_end, stream, why)
                     : launch_d<64, false>(p.B, p.H, p.n, p.q, p.k, p.v, nullptr, prm, ws, p.ev_main_begin,
                                           p.ev_main_end, stream, why);
+    }
     *why = "tensor path supports d in {64, 128}";
     return cudaErrorInvalidValue;
 }
