@@ -23,8 +23,11 @@
 //
 // Thread layout (256 threads): row r = tid / 8 is owned by the 8 consecutive lanes
 // 8r .. 8r+7 of one warp.  For pair tiles each lane handles keys j = lane8 + 8c; for
-// d-vectors each lane handles coordinates e = lane8 + 8c.  Row reductions are 3 xor
-// shuffles; the per-row CG vectors live in registers.
+// d-vectors each lane handles groups of VW = min(4, d/8) consecutive coordinates,
+// e = VW (lane8 + 8 g) + u.  Shared rows are padded to d + 4 floats, so the vector loads of the 8
+// lanes of a row group fall in distinct 16-byte bank slots and every shared-memory operand is read
+// VW values per instruction.  Row reductions are 3 xor shuffles; the per-row CG vectors live in
+// registers.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -38,6 +41,33 @@ constexpr int BQ = 32;
 constexpr int BK = 32;
 constexpr int NT = 256;
 constexpr int JPT = BK / 8;  // keys per lane in a pair tile
+
+// Row pitch of the shared tiles (floats) and the lane's vector width along the head dimension.
+template <int D>
+struct Lay {
+    static constexpr int E = D / 8;               // coordinates per lane
+    static constexpr int VW = E < 4 ? E : 4;      // consecutive coordinates per vector access
+    static constexpr int LD = D + 4;              // padded pitch
+    // coordinate of this lane's slot c
+    static __device__ __forceinline__ int coord(int l8, int c) { return VW * (l8 + 8 * (c / VW)) + c % VW; }
+};
+
+template <int VW>
+struct Vec;
+template <>
+struct Vec<4> {
+    static __device__ __forceinline__ void ld(const float* p, float (&o)[4]) {
+        const float4 t = *reinterpret_cast<const float4*>(p);
+        o[0] = t.x; o[1] = t.y; o[2] = t.z; o[3] = t.w;
+    }
+};
+template <>
+struct Vec<2> {
+    static __device__ __forceinline__ void ld(const float* p, float (&o)[2]) {
+        const float2 t = *reinterpret_cast<const float2*>(p);
+        o[0] = t.x; o[1] = t.y;
+    }
+};
 
 __device__ __forceinline__ float ld_f(const float* p) { return __ldg(p); }
 __device__ __forceinline__ float ld_f(const __nv_bfloat16* p) { return __bfloat162float(*p); }
@@ -59,50 +89,83 @@ __device__ __forceinline__ float row_max8(float v) {
 
 template <int D>
 struct Smem {
-    float q[BQ][D + 1];    // query rows
-    float p[BQ][D + 1];    // second operand rows: CG direction p, then rho'
-    float kb[BK][D + 1];   // key block
-    float vb[BK][D + 1];   // value block (output sweep)
-    float m[BQ][BK + 1];   // per-pair coefficients of the current block
+    static constexpr int LD = Lay<D>::LD;
+    __align__(16) float q[BQ][LD];    // query rows
+    __align__(16) float p[BQ][LD];    // second operand rows: CG direction p, then rho'
+    __align__(16) float kb[BK][LD];   // key block
+    __align__(16) float vb[BK][LD];   // value block (output sweep)
+    float m[BQ][BK + 1];              // per-pair coefficients of the current block
 };
 
-// Stage rows [row0, row0+rows) of a [n, D] slice into dst (zero beyond n).
+// 8 consecutive elements of a row as fp32 (one 16-byte load for bf16, two for fp32).
+__device__ __forceinline__ void ld8(const float* src, float (&o)[8]) {
+    const float4 a = __ldg(reinterpret_cast<const float4*>(src));
+    const float4 b = __ldg(reinterpret_cast<const float4*>(src) + 1);
+    o[0] = a.x; o[1] = a.y; o[2] = a.z; o[3] = a.w; o[4] = b.x; o[5] = b.y; o[6] = b.z; o[7] = b.w;
+}
+__device__ __forceinline__ void ld8(const __nv_bfloat16* src, float (&o)[8]) {
+    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src));
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const float2 f = __bfloat1622float2(h[u]);
+        o[2 * u] = f.x;
+        o[2 * u + 1] = f.y;
+    }
+}
+
+// Stage rows [row0, row0+rows) of a [n, D] slice into dst (zero beyond n), 8 elements per access.
 template <int D, typename T>
-__device__ __forceinline__ void load_rows(float (*dst)[D + 1], const T* src, int row0, int rows, int n) {
-    for (int idx = threadIdx.x; idx < rows * D; idx += NT) {
-        const int r = idx / D, e = idx - r * D;
+__device__ __forceinline__ void load_rows(float (*dst)[Lay<D>::LD], const T* src, int row0, int rows, int n) {
+    for (int idx = threadIdx.x; idx < rows * (D / 8); idx += NT) {
+        const int r = idx / (D / 8), e = (idx - r * (D / 8)) * 8;
         const int g = row0 + r;
-        dst[r][e] = (g < n) ? ld_f(src + (size_t)g * D + e) : 0.f;
+        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (g < n) ld8(src + (size_t)g * D + e, v);
+        *reinterpret_cast<float4*>(&dst[r][e]) = make_float4(v[0], v[1], v[2], v[3]);
+        *reinterpret_cast<float4*>(&dst[r][e + 4]) = make_float4(v[4], v[5], v[6], v[7]);
     }
 }
 
 // Pair tile: for this lane's keys j = lane8 + 8c, s[c] = q_r.k_j and a[c] = p_r.k_j.
 template <int D, bool SECOND>
 __device__ __forceinline__ void pair_tile(const Smem<D>& sm, int r, int l8, float (&s)[JPT], float (&a)[JPT]) {
+    constexpr int VW = Lay<D>::VW;
 #pragma unroll
     for (int c = 0; c < JPT; ++c) { s[c] = 0.f; a[c] = 0.f; }
-#pragma unroll 8
-    for (int e = 0; e < D; ++e) {
-        const float qe = sm.q[r][e];
-        const float pe = SECOND ? sm.p[r][e] : 0.f;
+#pragma unroll 2
+    for (int e = 0; e < D; e += VW) {
+        float qv[VW], pv[VW];
+        Vec<VW>::ld(&sm.q[r][e], qv);
+        if (SECOND) Vec<VW>::ld(&sm.p[r][e], pv);
 #pragma unroll
         for (int c = 0; c < JPT; ++c) {
-            const float ke = sm.kb[l8 + 8 * c][e];
-            s[c] = fmaf(qe, ke, s[c]);
-            if (SECOND) a[c] = fmaf(pe, ke, a[c]);
+            float kv[VW];
+            Vec<VW>::ld(&sm.kb[l8 + 8 * c][e], kv);
+#pragma unroll
+            for (int u = 0; u < VW; ++u) {
+                s[c] = fmaf(qv[u], kv[u], s[c]);
+                if (SECOND) a[c] = fmaf(pv[u], kv[u], a[c]);
+            }
         }
     }
 }
 
-// acc[c'] += sum_j m[r][j] * blk[j][e], e = l8 + 8c'.
+// acc[c] += sum_j m[r][j] * blk[j][e(c)] over this lane's coordinates.
 template <int D>
-__device__ __forceinline__ void accumulate_rows(const Smem<D>& sm, const float (*blk)[D + 1], int r, int l8,
+__device__ __forceinline__ void accumulate_rows(const Smem<D>& sm, const float (*blk)[Lay<D>::LD], int r, int l8,
                                                 float (&acc)[D / 8]) {
+    constexpr int VW = Lay<D>::VW, E = D / 8;
 #pragma unroll 4
     for (int j = 0; j < BK; ++j) {
         const float mj = sm.m[r][j];
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) acc[c] = fmaf(mj, blk[j][l8 + 8 * c], acc[c]);
+        for (int g = 0; g < E / VW; ++g) {
+            float bv[VW];
+            Vec<VW>::ld(&blk[j][VW * (l8 + 8 * g)], bv);
+#pragma unroll
+            for (int u = 0; u < VW; ++u) acc[g * VW + u] = fmaf(mj, bv[u], acc[g * VW + u]);
+        }
     }
 }
 
@@ -176,7 +239,7 @@ lla_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
 #pragma unroll
     for (int c = 0; c < E; ++c) {
         kbar[c] = acc[c] * inv_omega;
-        delta[c] = kbar[c] - sm.q[r][l8 + 8 * c];
+        delta[c] = kbar[c] - sm.q[r][Lay<D>::coord(l8, c)];
     }
 
     // ---- (2) CG on (C/omega) rho' = delta ----------------------------------------------------
@@ -198,7 +261,7 @@ lla_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
     for (int it = 0; it < cg_max_iters; ++it) {
         if (!__syncthreads_or(active ? 1 : 0)) break;
 #pragma unroll
-        for (int c = 0; c < E; ++c) sm.p[r][l8 + 8 * c] = pv[c];
+        for (int c = 0; c < E; ++c) sm.p[r][Lay<D>::coord(l8, c)] = pv[c];
         float kp = 0.f;
 #pragma unroll
         for (int c = 0; c < E; ++c) kp = fmaf(kbar[c], pv[c], kp);
@@ -261,7 +324,7 @@ lla_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
     if (probe) {
         const float* pr = probe + (head * (size_t)n + (row_ok ? i : 0)) * D;
 #pragma unroll
-        for (int c = 0; c < E; ++c) x[c] = row_ok ? pr[l8 + 8 * c] : 0.f;
+        for (int c = 0; c < E; ++c) x[c] = row_ok ? pr[Lay<D>::coord(l8, c)] : 0.f;
     }
     float dx = 0.f, kx = 0.f;
 #pragma unroll
@@ -273,7 +336,7 @@ lla_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
     kx = row_sum8(kx);
     __syncthreads();
 #pragma unroll
-    for (int c = 0; c < E; ++c) sm.p[r][l8 + 8 * c] = x[c];
+    for (int c = 0; c < E; ++c) sm.p[r][Lay<D>::coord(l8, c)] = x[c];
 #pragma unroll
     for (int c = 0; c < E; ++c) acc[c] = 0.f;
     float usum_part = 0.f;
@@ -303,7 +366,7 @@ lla_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
         const float inv_g = 1.f / (1.f + dx);
 #pragma unroll
         for (int c = 0; c < E; ++c) {
-            const int e = l8 + 8 * c;
+            const int e = Lay<D>::coord(l8, c);
             st_f(out + base + e, acc[c] * inv_u);
             if (!probe) rho[base + e] = x[c] * inv_g;
         }
