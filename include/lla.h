@@ -64,7 +64,14 @@ typedef enum {
  * B, H, n >= 1 with B*H <= 65535 (one grid row per (b, h) slice); d in {16, 32, 64, 128};
  * tau > 0 (logit scale); lambda > 0 (ridge, absolute,
  * applied to the max-normalised weights); cg_max_iters >= 1; cg_tol >= 0: a query stops once
- * ||r|| <= cg_tol ||delta_i|| (cg_tol == 0: exactly cg_max_iters iterations).
+ * ||r|| <= cg_tol ||delta_i|| (cg_tol == 0: exactly cg_max_iters iterations).  CG runs on the
+ * centred system (C_i/omega_i) rho'_i = delta_i, delta_i = kbar_i - q_i, which Sherman-Morrison maps
+ * exactly to Eq. (7)'s Sigma_i rho_i = mu_i; the tolerance is relative to ||delta_i||, and iteration
+ * counts are those of the centred iteration.
+ * With cg_tol > 0 the tensor path runs its precise form: the moment weights, the CG coefficients
+ * and the CG direction are carried as fp16 hi + lo pairs (about 22 bits; two more MMAs per CG block),
+ * which solving to a relative residual needs where lambda/omega_i is small against the keys' scatter.
+ * With cg_tol == 0 (a fixed iteration count) it runs the fp16 form.
  * Scratch (the tensor path's fp16 operand copies) is taken from the CUDA stream-ordered pool
  * with cudaMallocAsync/cudaFreeAsync on `stream`; use lla_forward_ex to pass it instead.
  */

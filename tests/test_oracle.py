@@ -498,3 +498,34 @@ def test_gradient_at_a_tie_takes_either_side():
     assert np.abs((dK1[1] + dK1[3]) - (dK3[1] + dK3[3])).max() < 1e-12
     keep = [0, 2, 4]
     assert np.abs(dK1[keep] - dK3[keep]).max() < 1e-12
+
+
+def test_fp32_coefficient_error_behind_the_gates_model():
+    """The parity gate's rounding model perturbs the fp32 path's per-pair CG coefficients at u = 2^-20
+    (tests/parity_util.py).  That figure is the 90% quantile of the relative error a float32 evaluation
+    of w_j (k_j.p - kbar.p) (two d-term dot products, each a sequential fp32 FMA chain) makes against
+    float64 on LM-shaped rows; the median sits near 2^-22.  Re-measured here on a smaller sample."""
+    from local_linear_attention_flashlla_gb300.inputs import make_inputs, workload
+    w = workload("lm_bf16", B=1, H=2, n=1024)
+    q, k, _ = (t.double().numpy()[0] for t in make_inputs(w))
+    rng = np.random.default_rng(1)
+    errs = []
+    for h in range(w.H):
+        for i in rng.integers(64, w.n, 8):
+            K, qi = k[h, : i + 1], q[h, i]
+            s = w.tau * K @ qi
+            W = np.exp(s - s.max())
+            kbar = (W / W.sum()) @ K
+            p = rng.standard_normal(w.d)
+            exact = W * ((K - kbar) @ p)
+            K32, p32, kb32 = K.astype(np.float32), p.astype(np.float32), kbar.astype(np.float32)
+            a = np.zeros(len(K), np.float32)
+            kp = np.float32(0.0)
+            for e in range(w.d):
+                a = (a + K32[:, e] * p32[e]).astype(np.float32)
+                kp = np.float32(kp + kb32[e] * p32[e])
+            m32 = (W.astype(np.float32) * (a - kp)).astype(np.float64)
+            errs.append(np.abs(m32 - exact) / np.abs(exact))
+    e = np.concatenate(errs)
+    assert 2.0 ** -24 < np.quantile(e, 0.5) < 2.0 ** -21
+    assert 2.0 ** -22 < np.quantile(e, 0.9) < 2.0 ** -19
