@@ -284,6 +284,7 @@ lla_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
         const int sV = key_ok ? sc_exp(__uint_as_float(prm.kmax[kidx + 1]) * 1.01f) : 0;
         const float tau = prm.tau;
         const float fs = tau * pow2i(-(eq + ek)), f1 = pow2i(-(ek + er)), f2 = pow2i(-(ek + ey)), fh = pow2i(-(ev + eg));
+        const float fs2 = fs * 1.4426950408889634f;      // the logits' scale in log2 units (weights via ex2)
         const float gq = pow2i(sK - eq), gy = -pow2i(sK - ey), gr = pow2i(sK - er), gv = pow2i(sV - eg);
         bool ok = true;
         for (int t = 0; t < nst; ++t) {
@@ -311,7 +312,7 @@ lla_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                         const float4* rp = reinterpret_cast<const float4*>(&s.rec[t & 1][16 * half + qq + w]);
                         const float4 r0 = rp[0], r1 = rp[1];
                         // r0 = (m, jm, inv_omega, hbar), r1 = (kb_rp, kb_y, sd, rp_scale)
-                        const float wb = expf(fmaf(sv[qq + w], fs, -r0.x)) * r0.z;
+                        const float wb = ex2(fmaf(sv[qq + w], fs2, -r0.x * 1.4426950408889634f)) * r0.z;
                         const float Ah = 1.f - fmaf(a1[qq + w], f1, -r1.x);
                         const float Bh = fmaf(hv[qq + w], fh, -r0.w) - fmaf(a2[qq + w], f2, -r1.y);
                         const float ds = wb * Ah * Bh;
@@ -530,9 +531,11 @@ lla_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         const int er = sc_exp(__uint_as_float(prm.ry[0])), ey = sc_exp(__uint_as_float(prm.ry[1]));
         const float tau = prm.tau;
         const float fs = tau * pow2i(-(eq + ek)), f1 = pow2i(-(ek + er)), f2 = pow2i(-(ek + ey)), fh = pow2i(-(ev + eg));
+        const float fs2 = fs * 1.4426950408889634f;      // the logits' scale in log2 units (weights via ex2)
         const float gq = pow2i(-eq), gy = pow2i(-ey), gr = pow2i(-er), gvv = pow2i(-eg), gk = pow2i(-ek);
         BwdRowRec R{};
         if (row_ok) R = prm.rec[(size_t)head * n + i];
+        const float m2 = R.m * 1.4426950408889634f;     // the row maximum in log2 units
         float acc[D / 2];
 #pragma unroll
         for (int e = 0; e < D / 2; ++e) acc[e] = 0.f;
@@ -559,7 +562,7 @@ lla_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                     const bool valid = row_ok && j <= i;
                     float ds = 0.f, mk = 0.f, mv = 0.f;
                     if (valid) {
-                        const float wb = expf(fmaf(sv[jj], fs, -R.m)) * R.inv_omega;
+                        const float wb = ex2(fmaf(sv[jj], fs2, -m2)) * R.inv_omega;
                         const float Ah = 1.f - fmaf(a1[jj], f1, -R.kb_rp);
                         const float Bh = fmaf(hv[jj], fh, -R.hbar) - fmaf(a2[jj], f2, -R.kb_y);
                         ds = wb * Ah * Bh;
