@@ -385,11 +385,11 @@ __device__ __forceinline__ void coef_chunk_wk(const float (&v)[32], const float 
 }
 
 // Backward moment sweep: out_j = 2^(s_j c - off) (the weights, as the moment sweep), with the
-// running sums of out_j, of out_j a_j (a = H = G V^T, the per-pair dout.v) and of out_j |k_j|^2.
+// running sums of out_j and of out_j a_j (a = H = G V^T, the per-pair dout.v).
 template <bool MASKED, int C>
-__device__ __forceinline__ void coef_chunk_wh(const float (&v)[32], const float (&a)[64], const float (&kn)[32],
-                                              float c_log2, float off, int col0, int lim, uint64_t& sum2, uint64_t& wh2,
-                                              uint64_t& tk2, uint32_t (&pk)[16], uint32_t (&pl)[16]) {
+__device__ __forceinline__ void coef_chunk_wh(const float (&v)[32], const float (&a)[64], float c_log2, float off,
+                                              int col0, int lim, uint64_t& sum2, uint64_t& wh2, uint32_t (&pk)[16],
+                                              uint32_t (&pl)[16]) {
     const uint64_t cc = f2_pack(c_log2, c_log2), oo = f2_pack(-off, -off);
 #pragma unroll
     for (int j = 0; j < 32; j += 2) {
@@ -403,7 +403,6 @@ __device__ __forceinline__ void coef_chunk_wh(const float (&v)[32], const float 
         const uint64_t m = f2_pack(m0, m1);
         sum2 = f2_add(sum2, m);
         wh2 = f2_fma(m, f2_pack(a[C * 32 + j], a[C * 32 + j + 1]), wh2);
-        tk2 = f2_fma(m, f2_pack(kn[j], kn[j + 1]), tk2);
         pk[j >> 1] = pack_half2(m0, m1);
         const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&pk[j >> 1]));
         pl[j >> 1] = pack_half2(m0 - h.x, m1 - h.y);
@@ -858,19 +857,17 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 tmem_ld32(tA + lane_off + half * 64, *reinterpret_cast<float(*)[32]>(&a[0]));
                 tmem_ld32(tA + lane_off + half * 64 + 32, *reinterpret_cast<float(*)[32]>(&a[32]));
                 tmem_ld32(tS, v);
-                load_knorm32(kn_row, kb * BK, kn);
                 tmem_ld_wait();
                 release_a();
                 uint32_t pl[16];            // hi + lo weights, split layout (gemm_y_split)
-                if (masked) coef_chunk_wh<true, 0>(v, a, kn, c_log2, m2 - 14.f, half * 64, lim, om_part, wh_part, tk_part, pk, pl);
-                else coef_chunk_wh<false, 0>(v, a, kn, c_log2, m2 - 14.f, 0, 0, om_part, wh_part, tk_part, pk, pl);
+                if (masked) coef_chunk_wh<true, 0>(v, a, c_log2, m2 - 14.f, half * 64, lim, om_part, wh_part, pk, pl);
+                else coef_chunk_wh<false, 0>(v, a, c_log2, m2 - 14.f, 0, 0, om_part, wh_part, pk, pl);
                 tmem_st16(tS, pk);
                 tmem_st16(tS + 16, pl);
                 tmem_ld32(tS + 32, v);
-                load_knorm32(kn_row, kb * BK + 32, kn);
                 tmem_ld_wait();
-                if (masked) coef_chunk_wh<true, 1>(v, a, kn, c_log2, m2 - 14.f, half * 64 + 32, lim, om_part, wh_part, tk_part, pk, pl);
-                else coef_chunk_wh<false, 1>(v, a, kn, c_log2, m2 - 14.f, 0, 0, om_part, wh_part, tk_part, pk, pl);
+                if (masked) coef_chunk_wh<true, 1>(v, a, c_log2, m2 - 14.f, half * 64 + 32, lim, om_part, wh_part, pk, pl);
+                else coef_chunk_wh<false, 1>(v, a, c_log2, m2 - 14.f, 0, 0, om_part, wh_part, pk, pl);
                 tmem_st16(tS + 32, pk);
                 tmem_st16(tS + 48, pl);
             } else if constexpr (PREC) {    // hi + lo weights, split layout (gemm_y_split)
@@ -950,6 +947,10 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // which a bound from max|k| alone does not.
         float cbound = 0.f, tr_om = 0.f;     // tr_om: the trace over omega, sum_j wbar_j |k_j - kbar|^2
         auto set_cbound = [&](float kk) {
+            if constexpr (BWD) {   // hi + lo coefficients throughout: the bound from max|k| suffices
+                cbound = (2.f * sqrtf((float)D) * mk + sqrtf(kk) * pow2i(-8)) * 1.001f;
+                return;
+            }
             const float tsum = row_ok ? tk_all * pow2i(-14) : 0.f;
             const float tr = fmaxf(tsum - omega * kk, 0.f) + tsum * pow2i(-9);
             cbound = (sqrtf(tr) + sqrtf(kk) * pow2i(-8)) * 1.001f;
