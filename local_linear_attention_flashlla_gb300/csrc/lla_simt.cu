@@ -127,6 +127,46 @@ __device__ __forceinline__ void load_rows(float (*dst)[Lay<D>::LD], const T* src
     }
 }
 
+// One BK-row block of a [n, D] slice held in registers (8 elements per group, PER groups per
+// thread): loaded while the previous block is computed, stored to shared memory after it.  For
+// d <= 32 the registers would cost the second resident CTA, so there the block is staged
+// synchronously at store() (load() only records where it comes from).
+template <int D, typename T, bool PF = (D >= 64)>
+struct BlockPrefetch {
+    static constexpr int G = BK * (D / 8);
+    static constexpr int PER = (G + NT - 1) / NT;
+    float v[PER][8];
+    __device__ __forceinline__ void load(const T* src, int row0, int n) {
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const int idx = threadIdx.x + u * NT;
+            const int r = idx / (D / 8), e = (idx - r * (D / 8)) * 8;
+            const int g = row0 + r;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) v[u][t] = 0.f;
+            if (idx < G && g < n) ld8(src + (size_t)g * D + e, v[u]);
+        }
+    }
+    __device__ __forceinline__ void store(float (*dst)[Lay<D>::LD]) const {
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+            const int idx = threadIdx.x + u * NT;
+            if (idx < G) {
+                const int r = idx / (D / 8), e = (idx - r * (D / 8)) * 8;
+                *reinterpret_cast<float4*>(&dst[r][e]) = make_float4(v[u][0], v[u][1], v[u][2], v[u][3]);
+                *reinterpret_cast<float4*>(&dst[r][e + 4]) = make_float4(v[u][4], v[u][5], v[u][6], v[u][7]);
+            }
+        }
+    }
+};
+template <int D, typename T>
+struct BlockPrefetch<D, T, false> {
+    const T* src_ = nullptr;
+    int row0_ = 0, n_ = 0;
+    __device__ __forceinline__ void load(const T* src, int row0, int n) { src_ = src; row0_ = row0; n_ = n; }
+    __device__ __forceinline__ void store(float (*dst)[Lay<D>::LD]) const { load_rows<D>(dst, src_, row0_, BK, n_); }
+};
+
 // Pair tile: for this lane's keys j = lane8 + 8c, s[c] = q_r.k_j and a[c] = p_r.k_j.
 template <int D, bool SECOND>
 __device__ __forceinline__ void pair_tile(const Smem<D>& sm, int r, int l8, float (&s)[JPT], float (&a)[JPT]) {
@@ -196,10 +236,13 @@ lla_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
     load_rows<D>(sm.q, qh, i0, BQ, n);
 
     // ---- (0) exact row maximum of the logits ---------------------------------------------
+    BlockPrefetch<D, T> pk;
     float m_row = -INFINITY;
+    pk.load(kh, 0, n);
     for (int kb = 0; kb < n_blocks; ++kb) {
         __syncthreads();
-        load_rows<D>(sm.kb, kh, kb * BK, BK, n);
+        pk.store(sm.kb);
+        if (kb + 1 < n_blocks) pk.load(kh, (kb + 1) * BK, n);   // in flight while this block computes
         __syncthreads();
         float s[JPT], a[JPT];
         pair_tile<D, false>(sm, r, l8, s, a);
@@ -216,9 +259,11 @@ lla_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
 #pragma unroll
     for (int c = 0; c < E; ++c) acc[c] = 0.f;
     float omega_part = 0.f;
+    pk.load(kh, 0, n);
     for (int kb = 0; kb < n_blocks; ++kb) {
         __syncthreads();
-        load_rows<D>(sm.kb, kh, kb * BK, BK, n);
+        pk.store(sm.kb);
+        if (kb + 1 < n_blocks) pk.load(kh, (kb + 1) * BK, n);
         __syncthreads();
         float s[JPT], a[JPT];
         pair_tile<D, false>(sm, r, l8, s, a);
@@ -269,9 +314,11 @@ lla_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
 #pragma unroll
         for (int c = 0; c < E; ++c) acc[c] = 0.f;
         float msum_part = 0.f;
+        pk.load(kh, 0, n);
         for (int kb = 0; kb < n_blocks; ++kb) {
             __syncthreads();
-            load_rows<D>(sm.kb, kh, kb * BK, BK, n);
+            pk.store(sm.kb);
+            if (kb + 1 < n_blocks) pk.load(kh, (kb + 1) * BK, n);
             __syncthreads();
             float s[JPT], a[JPT];
             pair_tile<D, true>(sm, r, l8, s, a);
@@ -341,10 +388,17 @@ lla_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
     for (int c = 0; c < E; ++c) acc[c] = 0.f;
     float usum_part = 0.f;
     const float c1 = 1.f + kx;
+    BlockPrefetch<D, T> pv_;
+    pk.load(kh, 0, n);
+    pv_.load(vh, 0, n);
     for (int kb = 0; kb < n_blocks; ++kb) {
         __syncthreads();
-        load_rows<D>(sm.kb, kh, kb * BK, BK, n);
-        load_rows<D>(sm.vb, vh, kb * BK, BK, n);
+        pk.store(sm.kb);
+        pv_.store(sm.vb);
+        if (kb + 1 < n_blocks) {
+            pk.load(kh, (kb + 1) * BK, n);
+            pv_.load(vh, (kb + 1) * BK, n);
+        }
         __syncthreads();
         float s[JPT], a[JPT];
         pair_tile<D, true>(sm, r, l8, s, a);
