@@ -162,8 +162,10 @@ lla_bwd_stats_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* 
     extern __shared__ __align__(16) unsigned char smem_raw[];
     QSmem<D>& sm = *reinterpret_cast<QSmem<D>*>(smem_raw);
 
-    const int tile = n_tiles - 1 - (int)blockIdx.x;  // longest causal ranges first
-    const size_t head = blockIdx.y;
+    int rank, head_i;
+    causal_order(3 * (size_t)n * D * sizeof(T), rank, head_i);   // keys, values and upstream gradients
+    const int tile = n_tiles - 1 - rank;
+    const size_t head = (size_t)head_i;
     const T* qh = q + head * (size_t)n * D;
     const T* kh = k + head * (size_t)n * D;
     const T* vh = v + head * (size_t)n * D;
@@ -495,8 +497,10 @@ lla_bwd_key_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __
     extern __shared__ __align__(16) unsigned char smem_raw[];
     S& sm = *reinterpret_cast<S*>(smem_raw);
     const int tid = threadIdx.x;
-    const int j0 = (int)blockIdx.x * KB2;       // the earliest keys have the longest query range: first
-    const size_t head = blockIdx.y;
+    int rank, head_i;                           // the earliest keys have the longest query range
+    causal_order(3 * (size_t)n * D * sizeof(T), rank, head_i);   // queries, upstream gradients, u
+    const int j0 = rank * KB2;
+    const size_t head = (size_t)head_i;
     const size_t hoff = head * (size_t)n * D;
 
     stage_cols<D, KP>(sm.kT, k + hoff, j0, KB2, n);
@@ -603,8 +607,10 @@ lla_bwd_dq_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __r
     extern __shared__ __align__(16) unsigned char smem_raw[];
     S& sm = *reinterpret_cast<S*>(smem_raw);
     const int tid = threadIdx.x;
-    const int i0 = (n_tiles - 1 - (int)blockIdx.x) * QB3;    // longest causal ranges first
-    const size_t head = blockIdx.y;
+    int rank, head_i;
+    causal_order(2 * (size_t)n * D * sizeof(T), rank, head_i);   // keys and values of a head
+    const int i0 = (n_tiles - 1 - rank) * QB3;
+    const size_t head = (size_t)head_i;
     const size_t hoff = head * (size_t)n * D;
     const int last_key = min(n - 1, i0 + QB3 - 1);
 

@@ -180,8 +180,9 @@ lla_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = prm.n;
-    const int j0 = (int)blockIdx.x * KB;           // the earliest keys have the longest query range: first
-    const int head = blockIdx.y;
+    int rank, head;                                // the earliest keys have the longest query range
+    causal_order((size_t)6 * n * D, rank, head);   // fp16 queries, upstream gradients and rho' of a head
+    const int j0 = rank * KB;
     const int nst = (n - j0 + QS - 1) / QS;        // query steps i0 = j0 + QS t, t < nst
 
     if (tid == 0) {
@@ -436,8 +437,9 @@ lla_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int n = prm.n;
-    const int i0 = (prm.n_tiles - 1 - (int)blockIdx.x) * KB;   // longest causal ranges first
-    const int head = blockIdx.y;
+    int rank, head;
+    causal_order((size_t)4 * n * D, rank, head);                // fp16 keys and values of a head
+    const int i0 = (prm.n_tiles - 1 - rank) * KB;
     const int last = min(n - 1, i0 + KB - 1);
     const int nst = last / QS + 1;                              // key steps j0 = QS t
 

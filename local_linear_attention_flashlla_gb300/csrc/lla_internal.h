@@ -126,6 +126,26 @@ cudaError_t launch_simt(const Problem& p, cudaStream_t stream);
 size_t tensor_workspace_bytes(int B, int H, int n, int d);
 cudaError_t launch_tensor(const Problem& p, void* workspace, cudaStream_t stream, const char** why);
 
+#ifdef __CUDACC__
+// Dispatch order of the causal kernels.  A tile's cost grows with the length of its causal range,
+// so a grid of (tile, head) CTAs is dispatched heaviest first: the CTAs that start last are the
+// lightest, and the tail in which SMs idle is short.  The order runs over groups of heads whose
+// operands (head_bytes each) fit in 32 MB together, so the CTAs running at once read L2-resident
+// keys and values.  Block (x, y) of a grid (tiles, heads) maps to rank (0 = the heaviest tile of its
+// head) and head; the map is a bijection of the grid.
+__device__ __forceinline__ void causal_order(size_t head_bytes, int& rank, int& head) {
+    const int nt = (int)gridDim.x, nh = (int)gridDim.y;
+    const int lin = (int)blockIdx.x + (int)blockIdx.y * nt;
+    const size_t fit = (size_t(32) << 20) / (head_bytes > 0 ? head_bytes : 1);
+    const int group = (int)(fit < 1 ? 1 : fit > (size_t)nh ? (size_t)nh : fit);
+    const int g0 = lin / (group * nt) * group;            // first head of this CTA's group
+    const int gh = min(group, nh - g0);                   // heads in the group
+    const int w = lin - g0 * nt;                          // position in the group, < gh * nt
+    rank = w / gh;
+    head = g0 + w % gh;
+}
+#endif
+
 // Record a failure for lla_last_error() and return status (defined in lla_api.cu).
 int set_error(int status, const char* message);
 

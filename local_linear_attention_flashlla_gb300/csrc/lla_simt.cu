@@ -218,8 +218,10 @@ lla_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
     extern __shared__ __align__(16) unsigned char smem_raw[];
     Smem<D>& sm = *reinterpret_cast<Smem<D>*>(smem_raw);
 
-    const int tile = n_tiles - 1 - (int)blockIdx.x;  // longest causal ranges first
-    const size_t head = blockIdx.y;
+    int rank, head_i;
+    causal_order(2 * (size_t)n * D * sizeof(T), rank, head_i);   // keys and values of a head
+    const int tile = n_tiles - 1 - rank;
+    const size_t head = (size_t)head_i;
     const T* qh = q + head * (size_t)n * D;
     const T* kh = k + head * (size_t)n * D;
     const T* vh = v + head * (size_t)n * D;

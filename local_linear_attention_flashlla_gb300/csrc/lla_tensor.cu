@@ -488,8 +488,9 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 #define WAIT(bar, par, e) mbar_wait_abortable(bar, par, e, abort_flag)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int tile = prm.n_tiles - 1 - (int)blockIdx.x;
-    const int head = blockIdx.y;
+    int rank, head;
+    causal_order((size_t)4 * prm.n * D, rank, head);    // fp16 keys and values of a head
+    const int tile = prm.n_tiles - 1 - rank;
     const int n = prm.n;
     const int nkb = tile + 1;
     const bool dynamic = prm.cg_tol > 0.f;
