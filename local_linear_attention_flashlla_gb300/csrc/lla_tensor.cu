@@ -298,6 +298,17 @@ __device__ __forceinline__ void load_dir8(const unsigned char* hi, const unsigne
     }
 }
 
+// The 8 fp16 values of h, times sc.
+__device__ __forceinline__ void dir8_hi(const uint4& h, float sc, float (&o)[8]) {
+    const __half2* h2 = reinterpret_cast<const __half2*>(&h);
+    const uint64_t sc2 = f2_pack(sc, sc);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const float2 a = __half22float2(h2[u]);
+        f2_unpack(f2_mul(f2_pack(a.x, a.y), sc2), o[2 * u], o[2 * u + 1]);
+    }
+}
+
 // One 16-coordinate chunk C of this thread's DH coordinates of
 //   cp = (C/omega) p_hat = Y ysc - kbar msc + lam_n p_hat
 // (and, with DOT, the partial dot p_hat.cp as two fp32 partial sums).  SPLIT: the direction tile
@@ -964,7 +975,8 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // x + ALPHA p_old (XO: a previous x exists; else it starts from 0), p_old being the direction of the
         // sweep just finished.  The scale sM of the
         // next sweep's coefficients follows from the same bound; kbar.p (kp_acc) is set by set_kp once
-        // kbar.res of the whole row is known.
+        // kbar.res of the whole row is known.  The fp16-only form reads every p_old group before it
+        // writes any (one batch of shared loads instead of a load per group behind the stores).
         float pn2 = 0.f;
 #define LLA_SET_DIRECTION(BETA, KEEP, XUPD, ALPHA, XO, SPLITC, MPB)                                        \
         {                                                                                                  \
@@ -972,6 +984,30 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             const uint64_t b2_ = f2_pack((BETA), (BETA));                                                  \
             const int sp_new_ = min(scale_exp((MPB) * 1.001f), 100 - ek);   /* keeps 2^(sp+ek) finite */  \
             const uint64_t nsc2_ = f2_pack(pow2i(sp_new_), pow2i(sp_new_));                                \
+            if (!(SPLITC)) {                                                                               \
+                uint4 ph_[DH / 8];                                                                         \
+                _Pragma("unroll") for (int g_ = 0; g_ < DH / 8; ++g_)                                      \
+                    ph_[g_] = (KEEP) ? *reinterpret_cast<const uint4*>(tile_half(s.p, row, half * DH + 8 * g_)) \
+                                     : make_uint4(0u, 0u, 0u, 0u);                                         \
+                _Pragma("unroll") for (int g_ = 0; g_ < DH / 8; ++g_) {                                    \
+                    const int e0 = 8 * g_;                                                                 \
+                    float po_[8];                                                                          \
+                    dir8_hi(ph_[g_], osc_, po_);                                                           \
+                    if (XUPD) {                                                                            \
+                        _Pragma("unroll") for (int u = 0; u < 8; ++u)                                      \
+                            xt[(e0 + u) * BQ] = fmaf((ALPHA), po_[u], (XO) ? xt[(e0 + u) * BQ] : 0.f);      \
+                    }                                                                                      \
+                    uint32_t* hw_ = reinterpret_cast<uint32_t*>(&ph_[g_]);                                 \
+                    _Pragma("unroll") for (int u = 0; u < 8; u += 2) {                                     \
+                        float x0_, x1_;                                                                    \
+                        f2_unpack(f2_mul(f2_fma(b2_, f2_pack(po_[u], po_[u + 1]),                          \
+                                                f2_pack(res[e0 + u], res[e0 + u + 1])), nsc2_), x0_, x1_); \
+                        hw_[u >> 1] = pack_half2(x0_, x1_);                                                \
+                    }                                                                                      \
+                }                                                                                          \
+                _Pragma("unroll") for (int g_ = 0; g_ < DH / 8; ++g_)                                      \
+                    *reinterpret_cast<uint4*>(tile_half(s.p, row, half * DH + 8 * g_)) = ph_[g_];          \
+            } else                                                                                         \
             _Pragma("unroll") for (int e0 = 0; e0 < DH; e0 += 8) {                                         \
                 float po_[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};                                   \
                 if (KEEP) load_dir8(s.p, s.rlo, SPLITC, row, half * DH + e0, osc_, po_);                   \
