@@ -180,6 +180,12 @@ __device__ __forceinline__ void load_knorm32(const float* __restrict__ kn_row, i
     }
 }
 
+// Pulls the two 128-byte lines of a thread half's 64 key norms of a block into L1 (lanes 0 and 1),
+// a block ahead of their loads: all lanes of a warp then read them at L1 latency, not L2's.
+__device__ __forceinline__ void prefetch_knorm64(const float* kn_row, int key0, int lane) {
+    if (lane < 2) asm volatile("prefetch.global.L1 [%0];" ::"l"(kn_row + key0 + 32 * lane));
+}
+
 // ------------------------------------------------------------------------------------------
 template <int D>
 struct TcSmem {
@@ -810,6 +816,10 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             return r;
         };
 
+        // the moment sweep's key norms (forward): this half's 64 keys of every block
+        const float* kn_row = prm.knorm + (size_t)head * (prm.n_tiles * BQ) + half * 64;
+        if (!BWD && !PROBE) prefetch_knorm64(kn_row, 0, lane);
+
         // ---------------- MAX sweep ----------------
         float mx = -INFINITY;
         int jmx = 0;                        // backward: first key index attaining the maximum
@@ -856,8 +866,8 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         uint64_t om_part = 0;              // two fp32 partial sums (bit pattern 0 = +0.0f, +0.0f)
         uint64_t wh_part = 0;              // backward: sum of w h
         uint64_t tk_part = 0;              // sum of w |k|^2 (the key scatter's trace, below)
-        const float* kn_row = prm.knorm + (size_t)head * (prm.n_tiles * BQ) + half * 64;
         for (int kb = 0; kb < nkb; ++kb, ++g) {
+            if (!BWD && !PROBE && kb + 1 < nkb) prefetch_knorm64(kn_row, (kb + 1) * BK, lane);
             ok = ok && wait_s(g);
             const uint32_t tS = tS0 + (g & 1) * 128 + lane_off + half * 64;
             const int lim = lim_of(kb);
