@@ -62,8 +62,12 @@ enum SweepType : int { SW_MAX = 0, SW_MOMENT = 1, SW_CG = 2, SW_OUT = 3, SW_TBAR
 
 // Sweep order without a tolerance: MAX, MOMENT, (backward: TBAR), T x CG, then OUT (forward) or
 // the end (backward).  With a tolerance the elementwise threads publish each later sweep's type.
+// NO_MAX (the precise and Parallax forms, TcParams::mode 1): the same without the MAX sweep; the
+// MOMENT sweep finds the row maximum itself (a reference from its first block, the exact maximum by
+// its end).
 template <bool BWD>
-__device__ __forceinline__ int static_sweep(int sweep, int cg_sweeps, int T) {
+__device__ __forceinline__ int static_sweep(int sweep, int cg_sweeps, int T, bool no_max) {
+    if (!BWD && no_max) ++sweep;
     if (sweep == 0) return SW_MAX;
     if (sweep == 1) return SW_MOMENT;
     if (BWD && sweep == 2) return SW_TBAR;
@@ -227,6 +231,12 @@ struct TcParams {
     BwdRowRec* rec;
     float* yvec;          // [B,H,n,D] fp32
     unsigned* dev_err;
+    // 0 = every tile with its MAX sweep; 1 (precise and Parallax forms) = no MAX sweep, each tile
+    // writes tile_flag (1: a row's maximum exceeded its first block's by more than the weights' fp16
+    // headroom, the tile's results are void); 2 = every tile whose flag is set, with its MAX sweep
+    // (the others return).
+    int mode;
+    int* tile_flag;       // [B*H][n_tiles]
     int n, n_tiles;
     float tau, lambda, cg_tol;
     int cg_max_iters;
@@ -490,6 +500,10 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     constexpr int NB = S::NB;
     constexpr int DH = D / 2;                       // head-dim coordinates per elementwise thread
     constexpr bool SPLITM = BWD || PREC;            // hi + lo weights and CG coefficients
+    // The forms launched without MAX sweeps (mode 1, then mode 2 for the marked tiles): the precise
+    // form and the Parallax form.  The fixed-cap form keeps them: without, its CG updates measured
+    // about 1 000 cycles slower each (their row exchanges), more than the MAX sweep costs.
+    constexpr bool NO_MAX_FORM = !BWD && (PREC || PROBE);
 
     // The swizzled tiles need 1024-byte alignment.  Dynamic shared memory begins 1024-aligned
     // (right after the block's reserved kilobyte), so no padding is requested; a launch where it
@@ -508,9 +522,14 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     int rank, head;
     causal_order((size_t)4 * prm.n * D, rank, head);    // fp16 keys and values of a head
     const int tile = prm.n_tiles - 1 - rank;
+    // the second forward launch redoes only the tiles the first one marked (uniform per CTA, before
+    // any barrier or TMEM allocation)
+    if (NO_MAX_FORM && prm.mode == 2 && prm.tile_flag[(size_t)head * prm.n_tiles + tile] == 0) return;
     const int n = prm.n;
     const int nkb = tile + 1;
     const bool dynamic = prm.cg_tol > 0.f;
+    const bool no_max = NO_MAX_FORM && prm.mode == 1;
+    const int n_static = BWD ? 3 : (no_max ? 1 : 2);   // leading sweeps of a fixed type in every mode
 
     if (tid == 0) {
         s.err = *abort_flag ? 1 : 0;           // another CTA of this launch already gave up
@@ -563,7 +582,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             int cg_sweeps = 0;
             for (int sweep = 0; !*err; ++sweep) {
                 int type;
-                if (sweep < (BWD ? 3 : 2) || !dynamic) type = static_sweep<BWD>(sweep, cg_sweeps, prm.cg_max_iters);
+                if (sweep < n_static || !dynamic) type = static_sweep<BWD>(sweep, cg_sweeps, prm.cg_max_iters, no_max);
                 else {
                     if (!WAIT(&s.p_ready, pr & 1, err)) break;
                     ++pr;
@@ -599,7 +618,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             int cg_sweeps = 0;
             for (int sweep = 0; ok; ++sweep) {
                 int type;
-                if (sweep < (BWD ? 3 : 2) || !dynamic) type = static_sweep<BWD>(sweep, cg_sweeps, prm.cg_max_iters);
+                if (sweep < n_static || !dynamic) type = static_sweep<BWD>(sweep, cg_sweeps, prm.cg_max_iters, no_max);
                 else {
                     if (!(ok = WAIT(&s.p_ready, pr & 1, err))) break;
                     ++pr;
@@ -642,7 +661,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             for (int sweep = 0; ok; ++sweep) {
                 int type;
                 bool have_p = false;
-                if (sweep < (BWD ? 3 : 2) || !dynamic) type = static_sweep<BWD>(sweep, cg_sweeps, prm.cg_max_iters);
+                if (sweep < n_static || !dynamic) type = static_sweep<BWD>(sweep, cg_sweeps, prm.cg_max_iters, no_max);
                 else {
                     if (!(ok = WAIT(&s.p_ready, pr & 1, err))) break;
                     ++pr;
@@ -708,7 +727,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             int cg_sweeps = 0;
             for (int sweep = 0; ok; ++sweep) {
                 int type;
-                if (sweep < (BWD ? 3 : 2) || !dynamic) type = static_sweep<BWD>(sweep, cg_sweeps, prm.cg_max_iters);
+                if (sweep < n_static || !dynamic) type = static_sweep<BWD>(sweep, cg_sweeps, prm.cg_max_iters, no_max);
                 else {
                     if (!(ok = WAIT(&s.p_ready, pr & 1, err))) break;
                     ++pr;
@@ -820,9 +839,40 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const float* kn_row = prm.knorm + (size_t)head * (prm.n_tiles * BQ) + half * 64;
         if (!BWD && !PROBE) prefetch_knorm64(kn_row, 0, lane);
 
-        // ---------------- MAX sweep ----------------
+        // largest valid entry of one 32-key chunk of S (columns col0 .. col0 + 31; -inf for none)
+        auto vmax32 = [&](const float (&v)[32], bool masked, int col0, int lim) {
+            float m = -INFINITY;
+            if (!masked) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) m = fmaxf(m, v[j]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) m = fmaxf(m, (col0 + j <= lim) ? v[j] : -INFINITY);
+            }
+            return m;
+        };
+        // The row maximum m2 (log2 units).  The moment sweep's weights are w 2^wsc in fp16 relative
+        // to a reference mref2: the maximum itself after a MAX sweep (wsc = 14, w <= 1); without one,
+        // the first block's maximum, with 2^6 of headroom for the later blocks (wsc = 8), the exact
+        // maximum taken along the sweep.
+        float m2 = 0.f, mref2 = 0.f;
+        int wsc = 14;
         float mx = -INFINITY;
         int jmx = 0;                        // backward: first key index attaining the maximum
+        if (no_max) {
+            ok = ok && wait_s(g);           // the moment sweep's first block (waited again there)
+            const uint32_t tS = tS0 + (g & 1) * 128 + lane_off + half * 64;
+            float v0[32], v1[32];
+            tmem_ld32(tS, v0);
+            tmem_ld32(tS + 32, v1);
+            tmem_ld_wait();
+            const int lim = lim_of(0);
+            const bool masked = !(tile_full && 0 < tile);
+            const float bm = xch.max(fmaxf(vmax32(v0, masked, half * 64, lim), vmax32(v1, masked, half * 64 + 32, lim)));
+            mref2 = (row_ok && bm > -INFINITY) ? bm * c_log2 : 0.f;
+            wsc = 8;
+        } else {
+        // ---------------- MAX sweep ----------------
         for (int kb = 0; kb < nkb; ++kb, ++g) {
             ok = ok && wait_s(g);
             const uint32_t tS = tS0 + (g & 1) * 128 + lane_off + half * 64;
@@ -860,7 +910,10 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         } else {
             mx = xch.max(mx);
         }
-        const float m2 = row_ok ? mx * c_log2 : 0.f;
+        m2 = row_ok ? mx * c_log2 : 0.f;
+        mref2 = m2;
+        }
+        float mrun = -INFINITY;             // no MAX sweep: the largest valid S entry so far
 
         // ---------------- MOMENT sweep ----------------
         uint64_t om_part = 0;              // two fp32 partial sums (bit pattern 0 = +0.0f, +0.0f)
@@ -882,14 +935,14 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 tmem_ld_wait();
                 release_a();
                 uint32_t pl[16];            // hi + lo weights, split layout (gemm_y_split)
-                if (masked) coef_chunk_wh<true, 0>(v, a, c_log2, m2 - 14.f, half * 64, lim, om_part, wh_part, pk, pl);
-                else coef_chunk_wh<false, 0>(v, a, c_log2, m2 - 14.f, 0, 0, om_part, wh_part, pk, pl);
+                if (masked) coef_chunk_wh<true, 0>(v, a, c_log2, mref2 - (float)wsc, half * 64, lim, om_part, wh_part, pk, pl);
+                else coef_chunk_wh<false, 0>(v, a, c_log2, mref2 - (float)wsc, 0, 0, om_part, wh_part, pk, pl);
                 tmem_st16(tS, pk);
                 tmem_st16(tS + 16, pl);
                 tmem_ld32(tS + 32, v);
                 tmem_ld_wait();
-                if (masked) coef_chunk_wh<true, 1>(v, a, c_log2, m2 - 14.f, half * 64 + 32, lim, om_part, wh_part, pk, pl);
-                else coef_chunk_wh<false, 1>(v, a, c_log2, m2 - 14.f, 0, 0, om_part, wh_part, pk, pl);
+                if (masked) coef_chunk_wh<true, 1>(v, a, c_log2, mref2 - (float)wsc, half * 64 + 32, lim, om_part, wh_part, pk, pl);
+                else coef_chunk_wh<false, 1>(v, a, c_log2, mref2 - (float)wsc, 0, 0, om_part, wh_part, pk, pl);
                 tmem_st16(tS + 32, pk);
                 tmem_st16(tS + 48, pl);
             } else if constexpr (PREC) {    // hi + lo weights, split layout (gemm_y_split)
@@ -897,40 +950,46 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 tmem_ld32(tS, v);
                 load_knorm32(kn_row, kb * BK, kn);
                 tmem_ld_wait();
-                if (masked) coef_chunk_wk<true, true>(v, kn, c_log2, m2 - 14.f, half * 64, lim, om_part, tk_part, pk, pl);
-                else coef_chunk_wk<false, true>(v, kn, c_log2, m2 - 14.f, 0, 0, om_part, tk_part, pk, pl);
+                if (no_max) mrun = fmaxf(mrun, vmax32(v, masked, half * 64, lim));
+                if (masked) coef_chunk_wk<true, true>(v, kn, c_log2, mref2 - (float)wsc, half * 64, lim, om_part, tk_part, pk, pl);
+                else coef_chunk_wk<false, true>(v, kn, c_log2, mref2 - (float)wsc, 0, 0, om_part, tk_part, pk, pl);
                 tmem_st16(tS, pk);
                 tmem_st16(tS + 16, pl);
                 tmem_ld32(tS + 32, v);
                 load_knorm32(kn_row, kb * BK + 32, kn);
                 tmem_ld_wait();
-                if (masked) coef_chunk_wk<true, true>(v, kn, c_log2, m2 - 14.f, half * 64 + 32, lim, om_part, tk_part, pk, pl);
-                else coef_chunk_wk<false, true>(v, kn, c_log2, m2 - 14.f, 0, 0, om_part, tk_part, pk, pl);
+                if (no_max) mrun = fmaxf(mrun, vmax32(v, masked, half * 64 + 32, lim));
+                if (masked) coef_chunk_wk<true, true>(v, kn, c_log2, mref2 - (float)wsc, half * 64 + 32, lim, om_part, tk_part, pk, pl);
+                else coef_chunk_wk<false, true>(v, kn, c_log2, mref2 - (float)wsc, 0, 0, om_part, tk_part, pk, pl);
                 tmem_st16(tS + 32, pk);
                 tmem_st16(tS + 48, pl);
             } else if constexpr (PROBE) {   // weights only (the probe form takes no key norms)
                 tmem_ld32(tS, v);
                 tmem_ld_wait();
-                if (masked) coef_chunk<true, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, half * 64, lim, om_part, pk);
-                else coef_chunk<false, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, 0, 0, om_part, pk);
+                if (no_max) mrun = fmaxf(mrun, vmax32(v, masked, half * 64, lim));
+                if (masked) coef_chunk<true, false, 0>(v, a_none, c_log2, mref2 - (float)wsc, 0.f, 0.f, half * 64, lim, om_part, pk);
+                else coef_chunk<false, false, 0>(v, a_none, c_log2, mref2 - (float)wsc, 0.f, 0.f, 0, 0, om_part, pk);
                 tmem_st16(tS, pk);
                 tmem_ld32(tS + 32, v);
                 tmem_ld_wait();
-                if (masked) coef_chunk<true, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, half * 64 + 32, lim, om_part, pk);
-                else coef_chunk<false, false, 0>(v, a_none, c_log2, m2 - 14.f, 0.f, 0.f, 0, 0, om_part, pk);
+                if (no_max) mrun = fmaxf(mrun, vmax32(v, masked, half * 64 + 32, lim));
+                if (masked) coef_chunk<true, false, 0>(v, a_none, c_log2, mref2 - (float)wsc, 0.f, 0.f, half * 64 + 32, lim, om_part, pk);
+                else coef_chunk<false, false, 0>(v, a_none, c_log2, mref2 - (float)wsc, 0.f, 0.f, 0, 0, om_part, pk);
                 tmem_st16(tS + 16, pk);
             } else {
                 tmem_ld32(tS, v);
                 load_knorm32(kn_row, kb * BK, kn);
                 tmem_ld_wait();
-                if (masked) coef_chunk_wk<true, false>(v, kn, c_log2, m2 - 14.f, half * 64, lim, om_part, tk_part, pk);
-                else coef_chunk_wk<false, false>(v, kn, c_log2, m2 - 14.f, 0, 0, om_part, tk_part, pk);
+                if (no_max) mrun = fmaxf(mrun, vmax32(v, masked, half * 64, lim));
+                if (masked) coef_chunk_wk<true, false>(v, kn, c_log2, mref2 - (float)wsc, half * 64, lim, om_part, tk_part, pk);
+                else coef_chunk_wk<false, false>(v, kn, c_log2, mref2 - (float)wsc, 0, 0, om_part, tk_part, pk);
                 tmem_st16(tS, pk);
                 tmem_ld32(tS + 32, v);
                 load_knorm32(kn_row, kb * BK + 32, kn);
                 tmem_ld_wait();
-                if (masked) coef_chunk_wk<true, false>(v, kn, c_log2, m2 - 14.f, half * 64 + 32, lim, om_part, tk_part, pk);
-                else coef_chunk_wk<false, false>(v, kn, c_log2, m2 - 14.f, 0, 0, om_part, tk_part, pk);
+                if (no_max) mrun = fmaxf(mrun, vmax32(v, masked, half * 64 + 32, lim));
+                if (masked) coef_chunk_wk<true, false>(v, kn, c_log2, mref2 - (float)wsc, half * 64 + 32, lim, om_part, tk_part, pk);
+                else coef_chunk_wk<false, false>(v, kn, c_log2, mref2 - (float)wsc, 0, 0, om_part, tk_part, pk);
                 tmem_st16(tS + 16, pk);
             }
             tmem_st_wait();
@@ -938,8 +997,18 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
         ok = ok && wait_y();
         const float om_all = xch.sum(f2_total(om_part));      // every elementwise thread joins the exchange
-        const float tk_all = xch.sum(f2_total(tk_part));      // sum_j w_j |k_j|^2, weights in units of 2^-14
-        const float omega = row_ok ? om_all * pow2i(-14) : 1.f;
+        const float tk_all = xch.sum(f2_total(tk_part));      // sum_j w_j |k_j|^2, weights in units of 2^-wsc
+        float wunit = pow2i(-14);                             // the moment sums' unit, relative to the maximum
+        if (no_max) {
+            const float mt = xch.max(mrun);
+            m2 = (row_ok && mt > -INFINITY) ? mt * c_log2 : 0.f;
+            // a weight 2^(m2 - mref2 + 8) in fp16 stays below 2^15.5 (65504 is the largest finite value):
+            // past that the tile's moments may hold an overflow, and its results are redone with a MAX sweep
+            const bool over = ew_any(row_ok && m2 - mref2 > 7.5f);
+            if (tid == 128) prm.tile_flag[(size_t)head * prm.n_tiles + tile] = over ? 1 : 0;
+            wunit = pow2i(-wsc) * exp2f(mref2 - m2);
+        }
+        const float omega = row_ok ? om_all * wunit : 1.f;
         const float inv_om = 1.f / omega;
         const float lam_n = prm.lambda * inv_om;
         // backward: hbar in units of H (dout.v 2^(eg+ev)); TBAR's right-hand side, in res
@@ -973,7 +1042,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                 cbound = (2.f * sqrtf((float)D) * mk + sqrtf(kk) * pow2i(-8)) * 1.001f;
                 return;
             }
-            const float tsum = row_ok ? tk_all * pow2i(-14) : 0.f;
+            const float tsum = row_ok ? tk_all * wunit : 0.f;
             const float tr = fmaxf(tsum - omega * kk, 0.f) + tsum * pow2i(-9);
             cbound = (sqrtf(tr) + sqrtf(kk) * pow2i(-8)) * 1.001f;
             tr_om = tr * inv_om;
@@ -1052,7 +1121,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if constexpr (BWD) {
             // kbar from the moment sweep's Y, before the TBAR sweep reuses the accumulator
             {
-                const float ysc = pow2i(-(14 + ek)) * inv_om;
+                const float ysc = wunit * pow2i(-ek) * inv_om;
                 float kk = 0.f;
 #pragma unroll
                 for (int c = 0; c < DH / 32; ++c) {
@@ -1127,7 +1196,7 @@ lla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             set_kp(0.f);
         } else {
             float kv[DH];
-            const float ysc = pow2i(-(14 + ek)) * inv_om;
+            const float ysc = wunit * pow2i(-ek) * inv_om;
             const float qsc = pow2i(-eq);
 #pragma unroll
             for (int c = 0; c < DH / 32; ++c) {
@@ -1502,10 +1571,12 @@ struct TcWs {
     Header* hdr;
     __half *q16, *k16, *v16, *g16;
     float *kbar, *xs, *knorm;
+    int* tile_flag;
 };
 // Parts, each 256-byte aligned: header, q16, k16, v16, (g16), kbar and x ([slices][tiles][D][128]
-// fp32), knorm ([slices][tiles * 128] fp32).  N = B H n D, NT = B H (tiles * 128) D.
-TcWs carve(void* ws, size_t N, size_t NT, bool bwd) {
+// fp32), knorm ([slices][tiles * 128] fp32), tile flags ([slices][tiles] int).  N = B H n D,
+// NT = B H (tiles * 128) D.
+TcWs carve(void* ws, size_t N, size_t NT, int D, bool bwd) {
     unsigned char* base = static_cast<unsigned char*>(ws);
     TcWs w;
     w.hdr = reinterpret_cast<Header*>(base);
@@ -1517,7 +1588,8 @@ TcWs carve(void* ws, size_t N, size_t NT, bool bwd) {
     if (bwd) { w.g16 = reinterpret_cast<__half*>(base + off); off += align256(N * 2); }
     w.kbar = reinterpret_cast<float*>(base + off); off += align256(NT * 4);
     w.xs = reinterpret_cast<float*>(base + off); off += align256(NT * 4);
-    w.knorm = reinterpret_cast<float*>(base + off);
+    w.knorm = reinterpret_cast<float*>(base + off); off += align256(NT / D * 4);
+    w.tile_flag = reinterpret_cast<int*>(base + off);
     return w;
 }
 
@@ -1528,7 +1600,7 @@ cudaError_t launch_d(int B, int H, int n, const void* qv, const void* kv, const 
                      const char** why) {
     const size_t N = (size_t)B * H * n * D;
     const size_t NT = (size_t)B * H * ((n + BQ - 1) / BQ) * BQ * D;   // padded to whole tiles
-    const TcWs w = carve(ws, N, NT, BWD);
+    const TcWs w = carve(ws, N, NT, D, BWD);
     cudaError_t e = cudaMemsetAsync(w.hdr, 0, HDR_BYTES, stream);
     if (e != cudaSuccess) { *why = "workspace header clear"; return e; }
     const int n_tiles = (n + BQ - 1) / BQ;
@@ -1561,6 +1633,7 @@ cudaError_t launch_d(int B, int H, int n, const void* qv, const void* kv, const 
     prm.kbar = w.kbar;
     prm.xs = w.xs;
     prm.knorm = w.knorm;
+    prm.tile_flag = w.tile_flag;
     prm.dev_err = device_error_word();
     prm.n = n;
     prm.n_tiles = (n + BQ - 1) / BQ;
@@ -1575,9 +1648,16 @@ cudaError_t launch_d(int B, int H, int n, const void* qv, const void* kv, const 
         *why = "profiling event record";
         return e;
     }
-    kern<<<grid, NTHREADS, smem, stream>>>(tq, tk, tv, tg, prm);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) { *why = "tensor kernel launch"; return e; }
+    // The precise and Parallax forms: a launch without MAX sweeps, then one that redoes, with them,
+    // the tiles it marked (the marks are rare; the second launch's other CTAs return at once).  The
+    // fixed-cap form and the backward: one launch with MAX sweeps.
+    constexpr bool two = !BWD && (PREC || PROBE);
+    for (int mode = two ? 1 : 0; mode <= (two ? 2 : 0); ++mode) {
+        prm.mode = mode;
+        kern<<<grid, NTHREADS, smem, stream>>>(tq, tk, tv, tg, prm);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) { *why = "tensor kernel launch"; return e; }
+    }
     if (ev_end && (e = cudaEventRecord(ev_end, stream)) != cudaSuccess) *why = "profiling event record";
     return e;
 }
@@ -1601,7 +1681,8 @@ TcParams forward_params(const Problem& p) {
 size_t tensor_workspace_bytes(int B, int H, int n, int d) {
     const size_t N = (size_t)B * H * n * d;
     const size_t NT = (size_t)B * H * ((n + BQ - 1) / BQ) * BQ * d;
-    return HDR_BYTES + 3 * align256(N * 2) + 2 * align256(NT * 4) + align256(NT / d * 4);
+    return HDR_BYTES + 3 * align256(N * 2) + 2 * align256(NT * 4) + align256(NT / d * 4) +
+           align256(NT / d / BQ * 4);
 }
 
 // Tolerance mode (cg_tol > 0) takes the precise form: CG run to a relative residual needs matrix-vector
@@ -1634,7 +1715,7 @@ cudaError_t launch_tensor(const Problem& p, void* ws, cudaStream_t stream, const
 TensorOperands tensor_backward_operands(void* ws, int B, int H, int n, int d) {
     const size_t N = (size_t)B * H * n * d;
     const size_t NT = (size_t)B * H * ((n + BQ - 1) / BQ) * BQ * d;
-    const TcWs w = carve(ws, N, NT, true);
+    const TcWs w = carve(ws, N, NT, d, true);
     TensorOperands o;
     o.maxabs = w.hdr->maxabs;
     o.q16 = w.q16;

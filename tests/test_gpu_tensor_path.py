@@ -12,6 +12,8 @@ Gate (``parity_util.bf16_gate``), on every compared row, element by element:
 * finite, denom > 0.
 The output is bf16, so one output ulp is already 4e-3 to 1.6e-2 RMS(v) for |out| in [0.5, 4).
 """
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -159,3 +161,27 @@ def test_illcond_bf16_lambda_1e6_is_softmax_through_lla_forward(lla_gpu):
     sm = softmax_rows(qkv, w, rows)
     rms_v = float(torch.sqrt(torch.mean(qkv[2].float() ** 2)))
     assert np.abs(pick(out, rows) - sm).max() / rms_v <= 2e-2
+
+
+def _rows_past_first_block_headroom(q, k, tau):
+    """Rows whose causal maximum of tau q.k exceeds the maximum over the first 128 keys by more than
+    7.5 in log2 units: the launch without a MAX sweep cannot hold their weights in fp16 and marks
+    their tiles for the second launch, which redoes them with one."""
+    qd, kd = q.double(), k.double()
+    s = tau * torch.einsum("bhid,bhjd->bhij", qd, kd)
+    n = s.shape[-1]
+    causal = torch.ones(n, n, dtype=torch.bool).tril()
+    s = s.masked_fill(~causal, -math.inf)
+    jump = (s.amax(-1) - s[..., :128].amax(-1)) * (1.0 / math.log(2.0))
+    return int((jump > 7.5).sum())
+
+
+def test_tensor_path_row_maximum_far_past_the_first_block(lla_gpu):
+    """Tolerance mode (the precise form, launched without MAX sweeps).  Keys 128..255 scaled by 4, so
+    most rows past the first tile have their maximum far above the first key block's: those tiles are
+    redone by the MAX-sweep launch.  Every row within 2e-2 of the float64 CG at the same tolerance."""
+    w = workload("lm_bf16", B=1, H=2, n=300, tau=1.0 / np.sqrt(128), cg_max_iters=96, cg_tol=1e-5)
+    q, k, v = (t.clone() for t in make_inputs(w))
+    k[:, :, 128:256] = (k[:, :, 128:256].float() * 4.0).bfloat16()
+    assert _rows_past_first_block_headroom(q, k, w.tau) > 100
+    bf16_gate(w, all_rows(w), TC, inputs=(q, k, v), max_loose_frac=0.01)
