@@ -92,15 +92,19 @@ __global__ void lla_bwd_ry16_kernel(const float* __restrict__ rho, const BwdRowR
 }
 
 // ---- the dk/dv kernel -----------------------------------------------------------------------------
+// Stages of the query-side ring: each step's six tiles (48 KB at d = 128) come from L2, and two
+// stages left the products waiting on their loads.
+constexpr int KV_STAGES = 3;
+
 template <int D>
 struct KvSmem {
     static constexpr int KT = KB * D * 2;     // [128 x D] fp16, SW128 boxes of 64 columns
     static constexpr int QT = QS * D * 2;     // [32 x D] fp16
     unsigned char k[KT];
     unsigned char v[KT];
-    unsigned char st[2][NTILE][QT];           // two stages of q, g, rh, rl, yh, yl
-    BwdRowRec rec[2][QS];                     // and the step's per-query records
-    uint64_t kv_full, st_full[2], st_empty[2], prod_full[2], coef_ready[2], acc_free[2], acc_done;
+    unsigned char st[KV_STAGES][NTILE][QT];   // stages of q, g, rh, rl, yh, yl
+    BwdRowRec rec[KV_STAGES][QS];             // and the step's per-query records
+    uint64_t kv_full, st_full[KV_STAGES], st_empty[KV_STAGES], prod_full[2], coef_ready[2], acc_free[2], acc_done;
     uint32_t tmem_base;
     int err;
 };
@@ -188,9 +192,11 @@ lla_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
     if (tid == 0) {
         s.err = *abort_flag ? 1 : 0;
         mbar_init(&s.kv_full, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < KV_STAGES; ++i) {
             mbar_init(&s.st_full[i], 1);
             mbar_init(&s.st_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&s.prod_full[i], 1);
             mbar_init(&s.coef_ready[i], NEW / 32);
             mbar_init(&s.acc_free[i], 1);
@@ -217,7 +223,7 @@ lla_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                 tma_load_3d(s.v + bx * KB * 128, &tm_v, &s.kv_full, bx * 64, j0, head);
             }
             for (int t = 0; t < nst && !*err; ++t) {
-                const int st = t & 1, f = t >> 1;
+                const int st = t % KV_STAGES, f = t / KV_STAGES;
                 if (f >= 1 && !WAIT(&s.st_empty[st], (f - 1) & 1)) break;
                 const int i0 = j0 + QS * t;
                 const uint32_t rbytes = (uint32_t)(min(QS, n - i0) * sizeof(BwdRowRec));   // rows past n: not read
@@ -227,7 +233,8 @@ lla_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                         tma_load_3d(s.st[st][m] + bx * QS * 128, maps[m], &s.st_full[st], bx * 64, i0, head);
                 bulk_load(s.rec[st], prm.rec + (size_t)head * n + i0, rbytes, &s.st_full[st]);
             }
-            for (int t = nst > 2 ? nst - 2 : 0; t < nst; ++t) drain(&s.st_full[t & 1], (t >> 1) & 1);
+            for (int t = nst > KV_STAGES ? nst - KV_STAGES : 0; t < nst; ++t)
+                drain(&s.st_full[t % KV_STAGES], (t / KV_STAGES) & 1);
             drain(&s.kv_full, 0);
         }
     } else if (warp == 9) {
@@ -237,8 +244,8 @@ lla_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
             bool ok = WAIT(&s.kv_full, 0);
             for (int t = 0; t <= nst && ok; ++t) {
                 if (t < nst) {   // products of step t into buffer t & 1
-                    const int st = t & 1, pb = t & 1;
-                    if (!(ok = WAIT(&s.st_full[st], (t >> 1) & 1))) break;
+                    const int st = t % KV_STAGES, pb = t & 1;
+                    if (!(ok = WAIT(&s.st_full[st], (t / KV_STAGES) & 1))) break;
                     // the buffer's coefficients of step t - 2 were read by that step's sums
                     if (t >= 2 && !(ok = WAIT(&s.acc_free[pb], ((t - 2) >> 1) & 1))) break;
                     tc_fence_after();
@@ -252,7 +259,7 @@ lla_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                     umma_commit(&s.prod_full[pb]);
                 }
                 if (t >= 1) {    // sums of step t - 1
-                    const int u = t - 1, st = u & 1, pb = u & 1;
+                    const int u = t - 1, st = u % KV_STAGES, pb = u & 1;
                     if (!(ok = WAIT(&s.coef_ready[pb], (u >> 1) & 1))) break;
                     tc_fence_after();
                     const uint32_t base = tP + pb * 128;
@@ -310,7 +317,7 @@ lla_bwd_kv_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_cons
                     const bool valid = key_ok && i < n && j <= i;
                     float c_q = 0.f, c_w = 0.f, c_r = 0.f;
                     if (valid) {
-                        const float4* rp = reinterpret_cast<const float4*>(&s.rec[t & 1][16 * half + qq + w]);
+                        const float4* rp = reinterpret_cast<const float4*>(&s.rec[t % KV_STAGES][16 * half + qq + w]);
                         const float4 r0 = rp[0], r1 = rp[1];
                         // r0 = (m, jm, inv_omega, hbar), r1 = (kb_rp, kb_y, sd, rp_scale)
                         const float wb = ex2(fmaf(sv[qq + w], fs2, -r0.x * 1.4426950408889634f)) * r0.z;
