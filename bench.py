@@ -996,7 +996,9 @@ def main():
 
     peaks, peak_kind = load_peaks()
     # fp32 path: one kernel per step; tensor path: max|x| pre-pass, fp16 conversion, fused sweep kernel
-    launches_per_step = 1 if rpath == lla.LLA_PATH_FP32 else 3
+    # (the precise and Parallax forms launch the fused kernel twice: without MAX sweeps, then again
+    # for the tiles the first launch marked)
+    launches_per_step = 1 if rpath == lla.LLA_PATH_FP32 else (4 if (parallax or w.cg_tol > 0) else 3)
     kern_name = "lla_simt_kernel" if rpath == lla.LLA_PATH_FP32 else "lla_tc_kernel"
     dominant_ms = sum(main_times) / len(main_times)
     achieved = flops / (dominant_ms / 1e3) / 1e12
