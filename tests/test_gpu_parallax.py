@@ -83,10 +83,11 @@ def test_parallax_full_size_sampled(lla_gpu):
     assert excess.max() <= 0.0, f"worst |err|/RMS(v) {e.max():.3e}, excess {excess.max():.3e}"
 
 
-def test_parallax_tensor_path_row_maximum_far_past_the_first_block(lla_gpu):
+@pytest.mark.parametrize("d", [64, 128])
+def test_parallax_tensor_path_row_maximum_far_past_the_first_block(lla_gpu, d):
     """Keys 128..255 scaled by 4: rows past the first tile have their maximum far above the first key
     block's (the tiles the launch without a MAX sweep marks for the second launch).  Same bound."""
-    w = workload("lm_bf16", B=1, H=2, n=300, d=128, tau=1.0 / math.sqrt(128))
+    w = workload("lm_bf16", B=1, H=2, n=300, d=d, tau=1.0 / math.sqrt(d))
     q, k, v = (t.clone() for t in make_inputs(w))
     k[:, :, 128:256] = (k[:, :, 128:256].float() * 4.0).bfloat16()
     r = make_probe(w)

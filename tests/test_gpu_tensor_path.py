@@ -176,11 +176,12 @@ def _rows_past_first_block_headroom(q, k, tau):
     return int((jump > 7.5).sum())
 
 
-def test_tensor_path_row_maximum_far_past_the_first_block(lla_gpu):
+@pytest.mark.parametrize("d", [64, 128])
+def test_tensor_path_row_maximum_far_past_the_first_block(lla_gpu, d):
     """Tolerance mode (the precise form, launched without MAX sweeps).  Keys 128..255 scaled by 4, so
     most rows past the first tile have their maximum far above the first key block's: those tiles are
     redone by the MAX-sweep launch.  Every row within 2e-2 of the float64 CG at the same tolerance."""
-    w = workload("lm_bf16", B=1, H=2, n=300, tau=1.0 / np.sqrt(128), cg_max_iters=96, cg_tol=1e-5)
+    w = workload("lm_bf16", B=1, H=2, n=300, d=d, tau=1.0 / np.sqrt(d), cg_max_iters=96, cg_tol=1e-5)
     q, k, v = (t.clone() for t in make_inputs(w))
     k[:, :, 128:256] = (k[:, :, 128:256].float() * 4.0).bfloat16()
     assert _rows_past_first_block_headroom(q, k, w.tau) > 100
