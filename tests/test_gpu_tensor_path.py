@@ -49,9 +49,11 @@ def test_tensor_path_ragged_at_the_lm_cap(lla_gpu, d):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-def test_tensor_path_tolerance_mode(lla_gpu, d):
-    """cg_tol > 0: per-query stopping (the precise hi + lo form); iteration counts within the cap."""
-    w = workload("lm_bf16", B=1, H=3, n=300, d=d, tau=1.0 / np.sqrt(d), cg_max_iters=96, cg_tol=1e-5)
+@pytest.mark.parametrize("n", [1, 129, 300])
+def test_tensor_path_tolerance_mode(lla_gpu, d, n):
+    """cg_tol > 0: per-query stopping (the precise hi + lo form, launched without MAX sweeps: one
+    row, a tile and one, a ragged multi-tile shape); iteration counts within the cap."""
+    w = workload("lm_bf16", B=1, H=3, n=n, d=d, tau=1.0 / np.sqrt(d), cg_max_iters=96, cg_tol=1e-5)
     r = bf16_gate(w, all_rows(w), TC, max_loose_frac=0.01)
     its = r["its"].numpy()
     assert its.max() <= 96 and its.min() >= 1
