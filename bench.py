@@ -194,6 +194,7 @@ KERNEL_SOURCES = {
     "lla_tc_kernel_bwd": ("lla_tensor.cu", "tc_ptx.cuh", "tc_host.h", "lla_internal.h"),
     "lla_simt_kernel": ("lla_simt.cu", "lla_internal.h"),
     "lla_decode_kernel": ("lla_decode.cu", "lla_internal.h"),
+    "lla_decode_mom_kernel": ("lla_decode_tc.cu", "tc_ptx.cuh", "tc_host.h", "lla_internal.h"),
     "lla_bwd_stats_kernel": ("lla_backward.cu", "lla_internal.h"),
     "lla_bwd_dq_key_kernels": ("lla_backward.cu", "lla_internal.h"),
 }
@@ -343,6 +344,8 @@ def parse():
     ap.add_argument("--op", choices=["lla", "parallax", "decode", "backward"], default="lla",
                     help="lla: the LLA forward (default); parallax: the Parallax form with a synthetic probe; "
                          "decode: one decode step (use --workload decode_bf16); backward: dq, dk, dv of the forward")
+    ap.add_argument("--decode-form", choices=["auto", "moment", "stream", "cluster"], default="auto",
+                    help="decode: the form (auto = moment for bf16 caches at d=128)")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch B (a smaller case for profiler captures)")
     ap.add_argument("--lam", type=float, default=None,
@@ -423,15 +426,18 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def decode_bytes(w, T):
+def decode_bytes(w, T, moment):
     """(compulsory, method) HBM bytes of one decode step.  Compulsory: the caches, q and the
-    outputs once.  Method: K read in each of the T + 2 passes (moments, T CG iterations, output)
-    and V once, as the three-phase algorithm reads them when the cache does not stay on chip."""
+    outputs once.  Method: the moment form reads K twice (the logits' maximum and kbar, then the
+    centred moments) and V once; the CUDA-core forms read K in each of the T + 2 passes (moments,
+    T CG iterations, output) and V once, as the three-phase algorithm reads them when the cache
+    does not stay on chip."""
     e = 2 if w.dtype == "bf16" else 4
     heads = w.B * w.H
     cache = heads * w.n * w.d * e
     small = heads * w.d * (e + e + 4) + heads * 4          # q, out, rho, denom
-    return 2 * cache + small, (T + 2) * cache + cache + small
+    comp = 2 * cache + small
+    return comp, comp + cache if moment else (T + 2) * cache + cache + small
 
 
 def _decode_oracle_worker(rows):
@@ -530,8 +536,13 @@ def run_decode(args, world, rank, local):
     stream = torch.cuda.current_stream()
     T = w.cg_max_iters
 
+    form = {"auto": lla.LLA_DECODE_AUTO, "moment": lla.LLA_DECODE_MOMENT, "stream": lla.LLA_DECODE_STREAM,
+            "cluster": lla.LLA_DECODE_CLUSTER}[args.decode_form]
+    moment = form == lla.LLA_DECODE_MOMENT or (form == lla.LLA_DECODE_AUTO and w.dtype == "bf16" and w.d == 128)
+    kname = "lla_decode_mom_kernel" if moment else "lla_decode_kernel"
+
     def step(qq=qd):
-        lla.decode(qq, kc, vc, w.n, w.tau, w.lam, T, w.cg_tol, out=out, rho=rho, denom=den)
+        lla.decode(qq, kc, vc, w.n, w.tau, w.lam, T, w.cg_tol, out=out, rho=rho, denom=den, form=form)
 
     for _ in range(args.warmup):
         step()
@@ -564,7 +575,7 @@ def run_decode(args, world, rank, local):
     total_ms = ranks_max(total_ms, dev)
     ms_per_step = total_ms / args.steps
     value = job_throughput(world, w.B, args.steps, total_ms)
-    comp, method = decode_bytes(w, T)
+    comp, method = decode_bytes(w, T, moment)
     kern_ms = sum(main_times) / len(main_times)
     peaks, peak_kind = load_peaks()
     hbm = peaks.get("hbm_gbs", 6800.0)
@@ -600,20 +611,29 @@ def run_decode(args, world, rank, local):
 
     line = {"metric": METRIC_DECODE, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16 in, f32 compute" if w.dtype == "bf16" else "f32", "data": "synthetic",
+            "vs_baseline": None, "dtype": ("bf16 in, bf16 products (w k as three terms), f32 accumulate and CG" if moment else
+                      "bf16 in, f32 compute") if w.dtype == "bf16" else "f32", "data": "synthetic",
             "config": {"workload": f"{w.name} B={w.B} H={w.H} cache n={w.n} d={w.d} tau={w.tau:.5g} lambda={w.lam} "
                                    f"cg_iters={T} cg_tol={w.cg_tol}", "l2": "flushed before every step (512 MiB write)",
                        "inputs": f"{w.dtype} caches resident in HBM"},
             "hbm_gbs": method / (ms_per_step / 1e3) / 1e9,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                         "traffic": load_traffic("lla_decode_kernel", w),
+                         "traffic": load_traffic(kname, w),
                          "peak_source": f"{peak_kind} copy bandwidth",
-                         "bytes_counted": f"method bytes {method} per step: K in each of T+2 passes, V once, q and "
-                                          f"outputs once (compulsory: {comp})"},
+                         "bytes_counted": (f"method bytes {method} per step: K twice, V once, q and outputs once "
+                                           f"(compulsory: {comp})") if moment else
+                                          (f"method bytes {method} per step: K in each of T+2 passes, V once, q and "
+                                           f"outputs once (compulsory: {comp})")},
             "clocks": clocks, "e2e": e2e, "gpu_launches": args.steps,
-            "dominant_kernel": {"name": "lla_decode_kernel", "ms_per_launch": kern_ms,
-                                "share_of_step": kern_ms / ms_per_step},
+            "decode_form": "moment" if moment else args.decode_form,
+            "dominant_kernel": {"name": kname, "ms_per_launch": kern_ms, "share_of_step": kern_ms / ms_per_step},
             "cg_iters_counted": T}
+    if moment:
+        # the products D += A^T [K | V] with A carried as three bf16 terms: 3 x 2 x d x 2d per key
+        flops = 3 * 2 * w.d * 2 * w.d * w.n * w.B * w.H
+        line["tensor_pipe"] = {"tflops": flops / (kern_ms / 1e3) / 1e12, "of_bf16_peak":
+                               flops / (kern_ms / 1e3) / 1e12 / peaks.get("bf16_tflops", 1935.5),
+                               "flops_counted": "3 bf16 terms x 2 x d x 2d per cached key (the issued products)"}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = decode_cpu_baseline(w, qd_host, k, v)
     if rank == 0:

@@ -212,12 +212,19 @@ int lla_parallax_forward(int dtype, int path, const void* q, const void* k, cons
                          void* out, int B, int H, int n, int d, float tau, void* workspace, size_t workspace_bytes,
                          void* stream);
 
+typedef enum {
+    LLA_DECODE_AUTO = 0,         /* LLA_DECODE_MOMENT for bf16 caches at d = 128, else a CUDA-core form */
+    LLA_DECODE_MOMENT = 1,       /* tcgen05: the weighted moments of the cache in one pass, CG on them */
+    LLA_DECODE_STREAM = 2,       /* CUDA cores, a CTA per head, K re-read every CG iteration */
+    LLA_DECODE_CLUSTER = 3       /* CUDA cores, an 8-CTA cluster per head holding K in shared memory */
+} lla_decode_form;
+
 /*
  * lla_decode -- one decode step: a new query per (b, h) against its key/value cache (Local
  * Linear Attention reading notes, section 2.2: the FlashLLA cache is Theta(n d); the new
  * query's causal prefix is the whole cache).  The result equals row n-1 of lla_forward on the
- * sequence whose keys and values are the cache, computed by the same centred CG (fp32
- * arithmetic, CUDA cores: one query row per head makes the step bound by reading the cache).
+ * sequence whose keys and values are the cache, computed by the same centred CG with fp32
+ * accumulation and CG state (one query row per head: the step is bound by reading the cache).
  *
  * q       [B,H,d] in dtype, the new position's query.
  * k, v    [B,H,n_cap,d] in dtype: rows 0..n-1 are the cache (the new key/value at n-1); rows
@@ -225,15 +232,36 @@ int lla_parallax_forward(int dtype, int path, const void* q, const void* k, cons
  *         be passed as it grows.
  * out     [B,H,d] in dtype.  rho [B,H,d] fp32.  denom [B,H] fp32.  cg_iters NULL or [B,H] int32.
  * tau, lambda, cg_max_iters, cg_tol: as for lla_forward.
- * All pointers are device pointers, 16-byte aligned, owned by the caller.  No scratch.  The n
- * weights of a head live in shared memory: n above lla_decode_max_n(d) gives
- * LLA_ERR_UNSUPPORTED.  Other errors as for lla_forward_ex.
+ * All pointers are device pointers, 16-byte aligned, owned by the caller.  No scratch.  Errors
+ * as for lla_forward_ex.  The form is LLA_DECODE_AUTO (see lla_decode_ex): for bf16 caches at
+ * d = 128 the moment form, which has no limit on n; otherwise a CUDA-core form, which keeps the
+ * n weights of a head in shared memory, so n above lla_decode_max_n(d) gives LLA_ERR_UNSUPPORTED.
  */
 int lla_decode(int dtype, const void* q, const void* k, const void* v, void* out, float* rho, float* denom,
                int* cg_iters, int B, int H, int n, int n_cap, int d, float tau, float lambda, int cg_max_iters,
                float cg_tol, void* stream);
 
-/* Largest cache length n that lla_decode accepts for head dim d (0 when d is unsupported). */
+/*
+ * lla_decode_ex -- lla_decode with the form chosen by the caller (an lla_decode_form value).
+ * Every form computes the same step, the centred CG of the reading notes' section 2.2 on the
+ * new query's system, and differs only in how the operator C is applied:
+ *   LLA_DECODE_MOMENT   (bf16 caches, d = 128 only) reads K and V once and forms, on the tensor
+ *       cores, Cu = sum_j w_j k_j k_j^T and Hk = sum_j w_j k_j v_j^T (d x d, fp32 accumulation,
+ *       the weighted keys carried as three bf16 terms, so as accurate as fp32 arithmetic), with
+ *       omega, mu~ = sum_j w_j k_j and nu = sum_j w_j v_j; then runs the CG on the d x d moments:
+ *       C p = Cu p - mu~ (kbar.p) - kbar (mu~.p - omega kbar.p), and the output
+ *       sum_j u_j v_j = (1 + kbar.rho') nu - Hk^T rho'.  No limit on n.
+ *   LLA_DECODE_STREAM   applies C with a pass over the cache per CG iteration (K read T+2 times).
+ *   LLA_DECODE_CLUSTER  as STREAM, with an eighth of K held in each CTA of an 8-CTA cluster; n must
+ *       leave an eighth of the cache within a CTA's shared memory, else LLA_ERR_UNSUPPORTED.
+ * An unsupported dtype or d for the chosen form gives LLA_ERR_UNSUPPORTED.
+ */
+int lla_decode_ex(int form, int dtype, const void* q, const void* k, const void* v, void* out, float* rho,
+                  float* denom, int* cg_iters, int B, int H, int n, int n_cap, int d, float tau, float lambda,
+                  int cg_max_iters, float cg_tol, void* stream);
+
+/* Largest cache length n that the CUDA-core decode forms accept for head dim d (0 when d is
+ * unsupported).  The moment form (bf16, d = 128) has no such limit. */
 int lla_decode_max_n(int d);
 
 /*

@@ -18,16 +18,18 @@ __all__ = [
     "lla_workspace_size", "lla_resolve_path", "lla_sync_status", "lla_selftest_device_timeout", "lla_last_error",
     "lla_version",
     "lla_profile_enable", "lla_profile_read", "lla_forward_noalloc", "lla_parallax_forward", "parallax_forward",
-    "lla_decode", "lla_decode_max_n", "decode", "lla_backward", "lla_backward_workspace_size", "backward",
+    "lla_decode", "lla_decode_ex", "lla_decode_max_n", "decode", "lla_backward", "lla_backward_workspace_size", "backward",
     "lla_backward_host", "lla_backward_host_buffer_size", "backward_host",
     "LLA_OK", "LLA_ERR_INVALID_ARG", "LLA_ERR_UNSUPPORTED", "LLA_ERR_CUDA", "LLA_ERR_DEVICE_TIMEOUT",
     "LLA_DTYPE_BF16", "LLA_DTYPE_FP32", "LLA_PATH_AUTO", "LLA_PATH_TENSOR", "LLA_PATH_FP32",
+    "LLA_DECODE_AUTO", "LLA_DECODE_MOMENT", "LLA_DECODE_STREAM", "LLA_DECODE_CLUSTER",
     "EXPORTED_SYMBOLS",
 ]
 
 LLA_OK, LLA_ERR_INVALID_ARG, LLA_ERR_UNSUPPORTED, LLA_ERR_CUDA, LLA_ERR_DEVICE_TIMEOUT = range(5)
 LLA_DTYPE_BF16, LLA_DTYPE_FP32 = 0, 1
 LLA_PATH_AUTO, LLA_PATH_TENSOR, LLA_PATH_FP32 = 0, 1, 2
+LLA_DECODE_AUTO, LLA_DECODE_MOMENT, LLA_DECODE_STREAM, LLA_DECODE_CLUSTER = 0, 1, 2, 3
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB = None
@@ -54,6 +56,8 @@ _SIGNATURES = {
                                       _c_float, _vp, _c_size, _vp]),
     "lla_decode": (_c_int, [_c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int, _c_int,
                             _c_float, _c_float, _c_int, _c_float, _vp]),
+    "lla_decode_ex": (_c_int, [_c_int, _c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _c_int,
+                               _c_int, _c_float, _c_float, _c_int, _c_float, _vp]),
     "lla_decode_max_n": (_c_int, [_c_int]),
     "lla_backward": (_c_int, [_c_int, _c_int, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int,
                               _c_int, _c_int, _c_float, _c_float, _c_int, _c_float, _vp, _c_size, _vp]),
@@ -196,16 +200,24 @@ def lla_decode(dtype, q_ptr, k_ptr, v_ptr, out_ptr, rho_ptr, denom_ptr, iters_pt
                                      n_cap, d, tau, lam, cg_max_iters, cg_tol, stream_ptr))
 
 
+def lla_decode_ex(form, dtype, q_ptr, k_ptr, v_ptr, out_ptr, rho_ptr, denom_ptr, iters_ptr, B, H, n, n_cap, d, tau,
+                  lam, cg_max_iters, cg_tol, stream_ptr):
+    """Raw decode-step entry point with the form chosen (an LLA_DECODE_* value); raises LLAError."""
+    _check(load_library().lla_decode_ex(form, dtype, q_ptr, k_ptr, v_ptr, out_ptr, rho_ptr, denom_ptr, iters_ptr, B,
+                                        H, n, n_cap, d, tau, lam, cg_max_iters, cg_tol, stream_ptr))
+
+
 def lla_decode_max_n(d):
     return load_library().lla_decode_max_n(d)
 
 
 def decode(q, k_cache, v_cache, n, tau, lam, cg_max_iters, cg_tol=0.0, *, return_iters=False, out=None, rho=None,
-           denom=None, stream=None):
+           denom=None, form=LLA_DECODE_AUTO, stream=None):
     """One decode step: q [B, H, d] against caches [B, H, n_cap, d] whose first n rows are valid.
 
     Returns (out [B, H, d], rho [B, H, d] fp32, denom [B, H] fp32) and, with return_iters, the
-    CG iteration counts [B, H].  Equals row n-1 of forward() on the cached sequence.
+    CG iteration counts [B, H].  Equals row n-1 of forward() on the cached sequence.  form: an
+    LLA_DECODE_* value (include/lla.h, lla_decode_ex).
     """
     import torch
     if not (q.is_cuda and k_cache.is_cuda and v_cache.is_cuda):
@@ -226,9 +238,9 @@ def decode(q, k_cache, v_cache, n, tau, lam, cg_max_iters, cg_tol=0.0, *, return
     if denom is None:
         denom = torch.empty((B, H), dtype=torch.float32, device=q.device)
     iters = torch.empty((B, H), dtype=torch.int32, device=q.device) if return_iters else None
-    lla_decode(dtype, q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(), rho.data_ptr(),
-               denom.data_ptr(), None if iters is None else iters.data_ptr(), B, H, int(n), n_cap, d, float(tau),
-               float(lam), int(cg_max_iters), float(cg_tol), _stream_ptr(stream))
+    lla_decode_ex(int(form), dtype, q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), out.data_ptr(),
+                  rho.data_ptr(), denom.data_ptr(), None if iters is None else iters.data_ptr(), B, H, int(n), n_cap, d,
+                  float(tau), float(lam), int(cg_max_iters), float(cg_tol), _stream_ptr(stream))
     if return_iters:
         return out, rho, denom, iters
     return out, rho, denom

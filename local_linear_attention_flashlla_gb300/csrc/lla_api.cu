@@ -429,9 +429,20 @@ int lla_parallax_forward(int dtype, int path, const void* q, const void* k, cons
     return lla::run_problem(p, rpath, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
+static_assert(LLA_DECODE_AUTO == lla::kDecodeAuto && LLA_DECODE_MOMENT == lla::kDecodeMoment &&
+                  LLA_DECODE_STREAM == lla::kDecodeStream && LLA_DECODE_CLUSTER == lla::kDecodeCluster,
+              "decode form values");
+
 int lla_decode(int dtype, const void* q, const void* k, const void* v, void* out, float* rho, float* denom,
                int* cg_iters, int B, int H, int n, int n_cap, int d, float tau, float lambda, int cg_max_iters,
                float cg_tol, void* stream_) {
+    return lla_decode_ex(LLA_DECODE_AUTO, dtype, q, k, v, out, rho, denom, cg_iters, B, H, n, n_cap, d, tau, lambda,
+                         cg_max_iters, cg_tol, stream_);
+}
+
+int lla_decode_ex(int form, int dtype, const void* q, const void* k, const void* v, void* out, float* rho,
+                  float* denom, int* cg_iters, int B, int H, int n, int n_cap, int d, float tau, float lambda,
+                  int cg_max_iters, float cg_tol, void* stream_) {
     lla::g_msg[0] = '\0';
     if (!q || !k || !v || !out || !rho || !denom) return fail(LLA_ERR_INVALID_ARG, "null tensor pointer");
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(rho) ||
@@ -448,12 +459,25 @@ int lla_decode(int dtype, const void* q, const void* k, const void* v, void* out
     if (cg_max_iters < 1 || cg_max_iters > 4096) return fail(LLA_ERR_INVALID_ARG, "cg_max_iters must be in [1, 4096]");
     if (!(cg_tol >= 0.f) || !(cg_tol < 1e30f)) return fail(LLA_ERR_INVALID_ARG, "cg_tol must be finite and >= 0");
     if (dtype != LLA_DTYPE_BF16 && dtype != LLA_DTYPE_FP32) return fail(LLA_ERR_INVALID_ARG, "unknown dtype %d", dtype);
-    if (lla::decode_smem_bytes(n, d) > (size_t)LLA_DECODE_SMEM_LIMIT)
-        return fail(LLA_ERR_UNSUPPORTED, "decode keeps the n weights in shared memory: n = %d is above the limit %d",
-                    n, lla_decode_max_n(d));
-    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (form < LLA_DECODE_AUTO || form > LLA_DECODE_CLUSTER) return fail(LLA_ERR_INVALID_ARG, "unknown decode form %d", form);
     lla::DecodeProblem p{q, k, v, out, rho, denom, cg_iters, B, H, n, n_cap, d, tau, lambda, cg_max_iters, cg_tol,
-                         dtype, nullptr, nullptr};
+                         dtype, nullptr, nullptr, form, nullptr};
+    if (form == LLA_DECODE_AUTO) p.form = lla::decode_moment_supported(p) ? LLA_DECODE_MOMENT : LLA_DECODE_AUTO;
+    if (p.form == LLA_DECODE_MOMENT) {
+        if (!lla::decode_moment_supported(p))
+            return fail(LLA_ERR_UNSUPPORTED, "the moment form needs bf16 caches and d = 128");
+        p.dev_err = lla::device_error_word();
+        if (!p.dev_err) return fail(LLA_ERR_CUDA, "lla_decode: device error word not found");
+    } else {
+        if (lla::decode_smem_bytes(n, d) > (size_t)LLA_DECODE_SMEM_LIMIT)
+            return fail(LLA_ERR_UNSUPPORTED,
+                        "the CUDA-core decode forms keep the n weights in shared memory: n = %d is above the limit %d",
+                        n, lla_decode_max_n(d));
+        if (p.form == LLA_DECODE_CLUSTER && !lla::decode_cluster_fits(n, d, dtype))
+            return fail(LLA_ERR_UNSUPPORTED, "the cluster form holds an eighth of the cache per CTA: n = %d is too long",
+                        n);
+    }
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
     if (lla::g_prof_on) {
         for (int i = 0; i < 4; ++i)
             if (!lla::g_ev[i]) {

@@ -795,7 +795,9 @@ constexpr long long kClusterMaxHeads = 64;
 
 template <int D, typename T>
 cudaError_t launch_dec_pick(const DecodeProblem& p, cudaStream_t stream) {
-    if (cl_smem_bytes<D, T>(p.n) <= (size_t)kMaxDynSmem && (long long)p.B * p.H <= kClusterMaxHeads)
+    const bool fits = cl_smem_bytes<D, T>(p.n) <= (size_t)kMaxDynSmem;
+    if (p.form == kDecodeCluster) return fits ? launch_dec_cluster<D, T>(p, stream) : cudaErrorInvalidValue;
+    if (p.form != kDecodeStream && fits && (long long)p.B * p.H <= kClusterMaxHeads)
         return launch_dec_cluster<D, T>(p, stream);
     return launch_dec<D, T>(p, stream);
 }
@@ -824,7 +826,23 @@ size_t decode_smem_bytes(int n, int d) {
     return base + (size_t)n * sizeof(float);
 }
 
+template <typename T>
+size_t cl_smem_dim(int n, int d) {
+    switch (d) {
+        case 16: return cl_smem_bytes<16, T>(n);
+        case 32: return cl_smem_bytes<32, T>(n);
+        case 64: return cl_smem_bytes<64, T>(n);
+        default: return cl_smem_bytes<128, T>(n);
+    }
+}
+
+bool decode_cluster_fits(int n, int d, int dtype) {
+    const size_t b = dtype == 1 ? cl_smem_dim<float>(n, d) : cl_smem_dim<__nv_bfloat16>(n, d);
+    return b <= (size_t)kMaxDynSmem;
+}
+
 cudaError_t launch_decode(const DecodeProblem& p, cudaStream_t stream) {
+    if (p.form == kDecodeMoment) return launch_decode_moment(p, stream);
     if (p.dtype == 1) return launch_dec_dim<float>(p, stream);
     return launch_dec_dim<__nv_bfloat16>(p, stream);
 }

@@ -47,9 +47,16 @@ struct DecodeProblem {
     float cg_tol;
     int dtype;           // lla_dtype
     cudaEvent_t ev_main_begin, ev_main_end;
+    int form;            // DecodeForm, resolved (never kDecodeAuto)
+    unsigned* dev_err;   // the device error word (the moment form's bounded waits)
 };
+// Decode forms (the values of lla_decode_form in include/lla.h).
+enum DecodeForm : int { kDecodeAuto = 0, kDecodeMoment = 1, kDecodeStream = 2, kDecodeCluster = 3 };
 size_t decode_smem_bytes(int n, int d);
+bool decode_cluster_fits(int n, int d, int dtype);
+bool decode_moment_supported(const DecodeProblem& p);
 cudaError_t launch_decode(const DecodeProblem& p, cudaStream_t stream);
+cudaError_t launch_decode_moment(const DecodeProblem& p, cudaStream_t stream);
 
 // Backward pass: gradients of sum_i dout_i.out_i with respect to q, k, v (all fp32 outputs).
 struct BackwardProblem {

@@ -39,4 +39,20 @@ inline bool make_tmap_f16_3d(CUtensorMap* map, const void* base, uint64_t inner,
     return r == CUDA_SUCCESS;
 }
 
+// 3-D 16-bit tensor [slices][rows][inner] (inner contiguous) whose slices lie slice_rows >= rows
+// rows apart: rows past `rows` of a slice read as zeros, never as the memory behind them.  Box
+// [1][box_rows][64], 128-byte swizzle.  type: CU_TENSOR_MAP_DATA_TYPE_FLOAT16 or _BFLOAT16.
+inline bool make_tmap_16b_3d_strided(CUtensorMap* map, const void* base, CUtensorMapDataType type, uint64_t inner,
+                                     uint64_t rows, uint64_t slices, uint64_t slice_rows, uint32_t box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc || slice_rows < rows) return false;
+    cuuint64_t dims[3] = {inner, rows, slices};
+    cuuint64_t strides[2] = {inner * 2, inner * slice_rows * 2};
+    cuuint32_t box[3] = {64, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, type, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace lla

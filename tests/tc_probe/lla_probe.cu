@@ -1,4 +1,5 @@
 // Single-CTA tcgen05 probe: see lla_probe.h.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -99,6 +100,79 @@ probe_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ C
     if (warp == 0) tmem_dealloc(tbase, 512);
     if (tid == 0) *status = s.err;
 }
+// ---- moment product: D[128 x 256] = At^T [K | V], bf16, A and B both MN-major ----------------
+// At, K, V are [64 rows][128] (a row = one key).  A (At viewed as [M = 128][K = 64 keys]) is written
+// by threads in the 128-byte-swizzle layout of 64-row boxes; K and V arrive by TMA as four
+// [64 x 64] boxes at a uniform 8 KB stride (K cols 0-63, K cols 64-127, V cols 0-63, V cols 64-127),
+// read as one N = 256 operand.
+struct __align__(1024) ProbeMnSmem {
+    __nv_bfloat16 a[64 * 128];
+    __nv_bfloat16 b[64 * 256];
+    uint64_t bar_tma, bar_mma;
+    uint32_t tmem_base;
+    int err;
+};
+
+__global__ void __launch_bounds__(128, 1)
+probe_mn_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                const __nv_bfloat16* __restrict__ At, float* D, int* status) {
+    extern __shared__ unsigned char raw[];
+    ProbeMnSmem& s = *reinterpret_cast<ProbeMnSmem*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        s.err = 0;
+        mbar_init(&s.bar_tma, 1);
+        mbar_init(&s.bar_mma, 1);
+        mbar_fence_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&s.tmem_base, 256);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tD = s.tmem_base;
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&s.bar_tma, 64 * 256 * 2);
+        for (int bx = 0; bx < 2; ++bx) {
+            tma_load_3d(s.b + bx * 64 * 64, &tm_k, &s.bar_tma, bx * 64, 0, 0);
+            tma_load_3d(s.b + (2 + bx) * 64 * 64, &tm_v, &s.bar_tma, bx * 64, 0, 0);
+        }
+    }
+    {   // thread: half a key row of At
+        const int r = tid >> 1, c0 = (tid & 1) * 64;
+        unsigned char* a = reinterpret_cast<unsigned char*>(s.a);
+        for (int c = c0; c < c0 + 64; ++c)
+            *reinterpret_cast<__nv_bfloat16*>(a + sw128_offset(r, c, 64)) = At[r * 128 + c];
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        if (mbar_wait(&s.bar_tma, 0, &s.err)) {
+            tc_fence_after();
+            const uint32_t id = idesc_bf16(128, 256, true, true);
+            for (int ks = 0; ks < 4; ++ks)
+                umma_ss(tD, sdesc_sw128(smem_u32(s.a) + ks * 2048, 8192, 1024),
+                        sdesc_sw128(smem_u32(s.b) + ks * 2048, 8192, 1024), id, ks > 0);
+        }
+        umma_commit(&s.bar_mma);
+    }
+    __syncwarp();
+    mbar_wait(&s.bar_mma, 0, &s.err);
+    tc_fence_after();
+    const int row = warp * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    float v[32];
+    for (int g = 0; g < 8; ++g) {
+        tmem_ld32(tD + lane_base + g * 32, v);
+        tmem_ld_wait();
+        for (int j = 0; j < 32; ++j) D[row * 256 + g * 32 + j] = v[j];
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tD, 256);
+    if (tid == 0) *status = s.err;
+}
 }  // namespace
 
 extern "C" int lla_probe_umma(const void* A, const void* B, const void* B2, float* D1, float* D2, float* D3) {
@@ -113,6 +187,28 @@ extern "C" int lla_probe_umma(const void* A, const void* B, const void* B2, floa
     e = cudaFuncSetAttribute(probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e == cudaSuccess) {
         probe_kernel<<<1, 128, smem>>>(ta, tb, tb2, static_cast<const __half*>(A), D1, D2, D3, status);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    int h = 0;
+    if (e == cudaSuccess) e = cudaMemcpy(&h, status, sizeof(int), cudaMemcpyDeviceToHost);
+    cudaFree(status);
+    if (e != cudaSuccess) return (int)e;
+    return h ? 9999 : 0;
+}
+
+extern "C" int lla_probe_umma_mn(const void* At, const void* K, const void* V, float* D) {
+    CUtensorMap tk, tv;
+    if (!lla::make_tmap_16b_3d_strided(&tk, K, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, 64, 1, 64, 64) ||
+        !lla::make_tmap_16b_3d_strided(&tv, V, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 128, 64, 1, 64, 64))
+        return (int)cudaErrorInvalidValue;
+    int* status = nullptr;
+    cudaError_t e = cudaMalloc(&status, sizeof(int));
+    if (e != cudaSuccess) return (int)e;
+    const size_t smem = sizeof(ProbeMnSmem) + 1024;
+    e = cudaFuncSetAttribute(probe_mn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) {
+        probe_mn_kernel<<<1, 128, smem>>>(tk, tv, static_cast<const __nv_bfloat16*>(At), D, status);
         e = cudaGetLastError();
     }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();

@@ -123,12 +123,36 @@ def test_decode_invalid_arguments_rejected_before_launch(lib, bad):
     assert lib.lla_last_error().decode()
 
 
+def _call_decode_ex(lib, form, **kw):
+    a = dict(dtype=0, q=16, k=32, v=48, out=64, rho=80, den=96, it=None, B=1, H=1, n=8, n_cap=8, d=64, tau=0.1,
+             lam=1.0, T=4, tol=0.0, stream=None)
+    a.update(kw)
+    return lib.lla_decode_ex(form, a["dtype"], a["q"], a["k"], a["v"], a["out"], a["rho"], a["den"], a["it"], a["B"],
+                             a["H"], a["n"], a["n_cap"], a["d"], a["tau"], a["lam"], a["T"], a["tol"], a["stream"])
+
+
 def test_decode_cache_length_limit(lib):
+    """The CUDA-core forms keep a head's n weights in shared memory (the moment form, which AUTO
+    takes for bf16 caches at d = 128, has no such limit and is not called here: it needs a GPU)."""
     for d in (16, 32, 64, 128):
         m = lib.lla_decode_max_n(d)
         assert 32768 <= m < 60000
-        assert _call_decode(lib, d=d, n=m + 1, n_cap=m + 1) == lla.LLA_ERR_UNSUPPORTED
+        assert _call_decode(lib, dtype=1, d=d, n=m + 1, n_cap=m + 1) == lla.LLA_ERR_UNSUPPORTED
+        assert _call_decode_ex(lib, lla.LLA_DECODE_STREAM, d=d, n=m + 1, n_cap=m + 1) == lla.LLA_ERR_UNSUPPORTED
     assert lib.lla_decode_max_n(48) == 0
+
+
+@pytest.mark.parametrize("form,kw,status", [
+    (lla.LLA_DECODE_MOMENT, dict(dtype=1, d=128), lla.LLA_ERR_UNSUPPORTED),      # fp32 caches
+    (lla.LLA_DECODE_MOMENT, dict(d=64), lla.LLA_ERR_UNSUPPORTED),                # d != 128
+    (lla.LLA_DECODE_CLUSTER, dict(d=128, n=40000, n_cap=40000), lla.LLA_ERR_UNSUPPORTED),   # an eighth too long
+    (7, dict(), lla.LLA_ERR_INVALID_ARG),
+    (-1, dict(), lla.LLA_ERR_INVALID_ARG),
+    (lla.LLA_DECODE_MOMENT, dict(d=128, B=0), lla.LLA_ERR_INVALID_ARG),
+])
+def test_decode_form_rejected_before_launch(lib, form, kw, status):
+    assert _call_decode_ex(lib, form, **kw) == status
+    assert lib.lla_last_error().decode()
 
 
 def _call_backward(lib, **kw):

@@ -46,10 +46,14 @@ def test_lm_workload_useful_flops_per_call():
 def test_decode_bytes():
     w = workload("decode_bf16")
     T = w.cg_max_iters
-    comp, method = bench.decode_bytes(w, T)
+    comp, method = bench.decode_bytes(w, T, moment=False)
     kv = w.B * w.H * w.n * w.d * 2
     assert method >= (T + 2) * kv + kv
     assert comp >= 2 * kv and comp < method
+    # the moment form reads K twice and V once
+    comp_m, method_m = bench.decode_bytes(w, T, moment=True)
+    assert comp_m == comp and method_m == comp + kv
+    assert comp - 2 * kv == w.B * w.H * (w.d * (2 + 2 + 4) + 4)
 
 
 def test_traffic_is_tied_to_the_sources_and_scales_with_the_batch(tmp_path, monkeypatch):

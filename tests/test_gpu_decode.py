@@ -9,6 +9,9 @@ LLA definition at that row.  Gates, per (b, h):
 * at the LM configuration's fixed cap T = 16 the reference is the oracle's float64 run of the
   same centred CG for 16 iterations (truncation is part of the definition being compared), with
   the same bounds as the fp32 forward path at a fixed cap on converged rows.
+Three forms compute the step (include/lla.h, lla_decode_ex): the moment form (tcgen05, the
+default for bf16 caches at d = 128), and the streaming and cluster forms on CUDA cores.  Each
+meets the same gates.
 """
 import math
 
@@ -21,10 +24,12 @@ from local_linear_attention_flashlla_gb300.inputs import make_inputs, workload
 from oracle.lla_ref import lla_row, lla_row_deflated_cg
 
 pytestmark = pytest.mark.gpu
+MOMENT, STREAM, CLUSTER = lla.LLA_DECODE_MOMENT, lla.LLA_DECODE_STREAM, lla.LLA_DECODE_CLUSTER
+FORMS = {"moment": MOMENT, "stream": STREAM, "cluster": CLUSTER}
 
 
-def _decode(w, n_cap=None, tol=None, iters=None):
-    q, k, v = make_inputs(w)                     # [B, H, n, d]; the last row is the new token
+def _decode(w, n_cap=None, tol=None, iters=None, form=lla.LLA_DECODE_AUTO, inputs=None):
+    q, k, v = make_inputs(w) if inputs is None else inputs   # [B, H, n, d]; the last row is the new token
     n = w.n
     n_cap = n if n_cap is None else n_cap
     dev = torch.device("cuda:0")
@@ -35,8 +40,9 @@ def _decode(w, n_cap=None, tol=None, iters=None):
     if n_cap > n:                                # rows past n must not be read
         kc[:, :, n:] = float("nan")
         vc[:, :, n:] = float("nan")
-    res = lla.decode(q[:, :, n - 1].to(dev), kc.to(dev), vc.to(dev), n, w.tau, w.lam,
-                     w.cg_max_iters if iters is None else iters, w.cg_tol if tol is None else tol, return_iters=True)
+    res = lla.decode(q[:, :, n - 1].contiguous().to(dev), kc.to(dev), vc.to(dev), n, w.tau, w.lam,
+                     w.cg_max_iters if iters is None else iters, w.cg_tol if tol is None else tol, return_iters=True,
+                     form=form)
     torch.cuda.synchronize()
     lla.lla_sync_status()
     return (q, k, v), [t.cpu() for t in res]
@@ -71,12 +77,53 @@ def test_decode_converged_matches_exact_solve(lla_gpu, dtype, d, n):
 
 @pytest.mark.parametrize("dtype,n,B", [("bf16", 8000, 1), ("fp32", 4000, 1), ("bf16", 600, 50)])
 def test_decode_streaming_form(lla_gpu, dtype, n, B):
-    """The streaming form (K re-read every pass) serves caches too long for an eighth to sit in a
-    CTA's shared memory, and batches of more than 64 heads; the cluster form the rest.  Both
-    meet the same gate."""
+    """The streaming form (K re-read every pass): for fp32 caches AUTO takes it for caches too long
+    for an eighth to sit in a CTA's shared memory, and batches of more than 64 heads; the cluster
+    form the rest.  At bf16 it is asked for by name."""
     w = workload("lm_bf16", B=B, H=3, n=n, d=128, dtype=dtype, tau=1.0 / math.sqrt(128), cg_max_iters=576,
                  cg_tol=1e-6)
-    qkv, res = _decode(w)
+    qkv, res = _decode(w, form=STREAM if dtype == "bf16" else lla.LLA_DECODE_AUTO)
+    _gate(w, qkv, res, lambda qi, K, V: lla_row(qi, K, V, w.tau, w.lam))
+
+
+@pytest.mark.parametrize("n", [1, 63, 64, 65, 129, 700])
+def test_decode_moment_form_chunks_and_ragged_tail(lla_gpu, n):
+    """The moment form over one key, one chunk of 64 keys, a chunk and one, and several chunks with
+    a ragged last one (keys past n read as zeros and weighted 0)."""
+    w = workload("lm_bf16", B=2, H=3, n=n, d=128, tau=1.0 / math.sqrt(128), cg_max_iters=576, cg_tol=1e-6)
+    qkv, res = _decode(w, form=MOMENT)
+    _gate(w, qkv, res, lambda qi, K, V: lla_row(qi, K, V, w.tau, w.lam))
+
+
+def _rising_logits(w, step):
+    """Inputs whose logits rise by about `step` per chunk of 64 keys: key j moves along the new
+    query by (step * (j // 64)) / (tau |q|^2), so the weight sits on the last keys, which share a
+    component along q many times their spread.  The caches hold the bf16 values."""
+    q, k, v = make_inputs(w)
+    qn = q[:, :, w.n - 1:w.n].double()
+    shift = step * (torch.arange(w.n, dtype=torch.float64) // 64).view(1, 1, -1, 1)
+    k = (k.double() + shift * qn / (w.tau * (qn * qn).sum(-1, keepdim=True))).to(k.dtype)
+    return q, k, v
+
+
+@pytest.mark.parametrize("form", ["moment", "stream"])
+def test_decode_rising_maximum(lla_gpu, form):
+    """Logits rising by ~3 per chunk over 11 chunks: every running maximum grows chunk after chunk,
+    and the weighted keys share a large common component, which moments about any point but kbar
+    would cancel at second order (the moment form centres on the exact kbar of its first pass).
+    Same gate as every form."""
+    w = workload("lm_bf16", B=2, H=3, n=700, d=128, tau=1.0 / math.sqrt(128), cg_max_iters=576, cg_tol=1e-6)
+    inputs = _rising_logits(w, 3.0)
+    qkv, res = _decode(w, form=FORMS[form], inputs=inputs)
+    _gate(w, qkv, res, lambda qi, K, V: lla_row(qi, K, V, w.tau, w.lam))
+
+
+@pytest.mark.parametrize("B,n", [(80, 130), (160, 65)])
+def test_decode_moment_form_many_heads_per_cta(lla_gpu, B, n):
+    """More heads than SMs: each CTA takes two to five heads in turn, alternating its two TMEM
+    accumulators and moment buffers (every head gated)."""
+    w = workload("lm_bf16", B=B, H=4, n=n, d=128, tau=1.0 / math.sqrt(128), cg_max_iters=576, cg_tol=1e-6)
+    qkv, res = _decode(w, form=MOMENT)
     _gate(w, qkv, res, lambda qi, K, V: lla_row(qi, K, V, w.tau, w.lam))
 
 
@@ -92,20 +139,20 @@ def test_decode_streaming_form_small_heads(lla_gpu, dtype, d):
     _gate(w, qkv, res, lambda qi, K, V: lla_row(qi, K, V, w.tau, w.lam))
 
 
-@pytest.mark.parametrize("B", [2, 75])
-def test_decode_reads_only_the_valid_cache_rows(lla_gpu, B):
-    """n_cap > n: rows past n hold NaN and must not reach the result (B = 2: the cluster form;
-    B = 75, 150 heads: the streaming form)."""
+@pytest.mark.parametrize("form,B", [("moment", 2), ("moment", 100), ("cluster", 2), ("stream", 75)])
+def test_decode_reads_only_the_valid_cache_rows(lla_gpu, form, B):
+    """n_cap > n: rows past n hold NaN and must not reach the result."""
     w = workload("lm_bf16", B=B, H=2, n=200, d=128, tau=1.0 / math.sqrt(128), cg_max_iters=300, cg_tol=1e-6)
-    qkv, res = _decode(w, n_cap=333)
+    qkv, res = _decode(w, n_cap=333, form=FORMS[form])
     assert all(np.isfinite(t.double().numpy()).all() for t in res[:3])
     _gate(w, qkv, res, lambda qi, K, V: lla_row(qi, K, V, w.tau, w.lam))
 
 
-def test_decode_at_the_lm_cap_matches_the_same_cg(lla_gpu):
+@pytest.mark.parametrize("form", ["moment", "stream", "cluster"])
+def test_decode_at_the_lm_cap_matches_the_same_cg(lla_gpu, form):
     """T = 16, tolerance 0 (the LM configuration): reference = float64 centred CG, 16 iterations."""
     w = workload("lm_bf16", B=2, H=4, n=2048, d=128)
-    qkv, res = _decode(w)
+    qkv, res = _decode(w, form=FORMS[form])
     q, k, v = (t.double().numpy() for t in qkv)
     out = res[0].double().numpy()
     rms_v = math.sqrt(float(np.mean(v ** 2)))
@@ -120,8 +167,8 @@ def test_decode_at_the_lm_cap_matches_the_same_cg(lla_gpu):
 
 def test_decode_full_size_sampled(lla_gpu):
     """The benchmark's decode configuration, in the launch the benchmark times (64 sequences x 16
-    heads = 1024 heads: the streaming form), against the float64 centred CG with the same cap T = 16
-    on sampled heads (first, last and six drawn with a fixed seed)."""
+    heads = 1024 heads: the moment form, about seven heads per CTA), against the float64 centred CG
+    with the same cap T = 16 on sampled heads (first, last and six drawn with a fixed seed)."""
     w = workload("decode_bf16")
     q, k, v = make_inputs(w)
     n = w.n

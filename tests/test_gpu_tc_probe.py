@@ -39,3 +39,21 @@ def test_umma_descriptors_match_matmul(lla_gpu, probe_lib):
             close = [k for k, v in alt.items() if (d - v).abs().max().item() < 1e-3]
             msgs.append(f"{name}: max err {err} (matches {close})")
     assert not msgs, "; ".join(msgs)
+
+
+def test_umma_mn_major_bf16_moment_product(lla_gpu, probe_lib):
+    """The decode moment product's form: D[128 x 256] = At^T [K | V] with bf16 operands, A written
+    by threads and B loaded by TMA, both MN-major (64-row boxes at an 8 KB stride), N = 256."""
+    lib = probe_lib
+    lib.lla_probe_umma_mn.restype = ctypes.c_int
+    lib.lla_probe_umma_mn.argtypes = [ctypes.c_void_p] * 4
+    g = torch.Generator().manual_seed(1)
+    dev = torch.device("cuda:0")
+    At, K, V = (torch.randint(-8, 9, (64, 128), generator=g).to(torch.bfloat16).to(dev) / 4 for _ in range(3))
+    D = torch.full((128, 256), float("nan"), device=dev)
+    rc = lib.lla_probe_umma_mn(At.data_ptr(), K.data_ptr(), V.data_ptr(), D.data_ptr())
+    torch.cuda.synchronize()
+    assert rc == 0, rc
+    want = At.float().T @ torch.cat([K.float(), V.float()], dim=1)
+    err = (D - want).abs().max().item()
+    assert err <= 1e-3, f"MN-major bf16 product: max err {err}"
