@@ -26,8 +26,8 @@
 // TMA delivers K and V.
 //
 // Roles (512 threads, one CTA per SM; a CTA takes heads blockIdx.x, blockIdx.x + gridDim.x, ...):
-//   warp 0, lane 0   TMA: chunks of K (pass 1) and of K and V (pass 2) into a 3-stage ring; rows
-//                    past n read as zeros;
+//   warp 0, lane 0   TMA: chunks of 128 keys of K (pass 1) and of 64 keys of K and V (pass 2), a
+//                    32 KB stage each, into a 3-stage ring; rows past n read as zeros;
 //   warp 1, lane 0   MMA issue (warp 1 owns TMEM: two 256-column accumulators, heads in turn);
 //                    every chunk of either pass is handed back through it, in order;
 //   warps 4-11       elementwise, 4 threads per key row (32 coordinates each): logits, weights,
@@ -126,7 +126,8 @@ lla_decode_mom_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
     MomSmem& s = *reinterpret_cast<MomSmem*>(smem_raw);
     volatile int* err = &s.err;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nch = (prm.n + CK - 1) / CK;                 // chunks per pass; a head is 2 nch chunks
+    const int nch1 = (prm.n + 2 * CK - 1) / (2 * CK);      // pass-1 chunks (128 keys of K)
+    const int nch = (prm.n + CK - 1) / CK;                 // pass-2 chunks (64 keys of K and V)
     const int nloc = (prm.nheads - 1 - (int)blockIdx.x) / (int)gridDim.x + 1;   // grid <= heads
 
     if (tid == 0) {
@@ -165,14 +166,19 @@ lla_decode_mom_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
             bool ok = true;
             for (int hl = 0; hl < nloc && ok; ++hl) {
                 const int head = (int)blockIdx.x + hl * (int)gridDim.x;
-                for (int c2 = 0; c2 < 2 * nch; ++c2) {
-                    const int st = g % NSTAGE, f = g / NSTAGE, c = c2 < nch ? c2 : c2 - nch;
-                    const bool with_v = c2 >= nch;
+                for (int c2 = 0; c2 < nch1 + nch; ++c2) {
+                    const int st = g % NSTAGE, f = g / NSTAGE;
                     if (f >= 1 && !(ok = mbar_wait(&s.st_empty[st], (f - 1) & 1, err))) break;
-                    mbar_arrive_expect_tx(&s.st_full[st], (with_v ? 4 : 2) * BOX);
+                    mbar_arrive_expect_tx(&s.st_full[st], 4 * BOX);
                     for (int bx = 0; bx < 2; ++bx) {
-                        tma_load_3d(s.kv[st][bx], &tm_k, &s.st_full[st], bx * 64, c * CK, head);
-                        if (with_v) tma_load_3d(s.kv[st][2 + bx], &tm_v, &s.st_full[st], bx * 64, c * CK, head);
+                        if (c2 < nch1) {   // K rows y .. y+63 into boxes 0, 1 and y+64 .. y+127 into 2, 3
+                            tma_load_3d(s.kv[st][bx], &tm_k, &s.st_full[st], bx * 64, c2 * 2 * CK, head);
+                            tma_load_3d(s.kv[st][2 + bx], &tm_k, &s.st_full[st], bx * 64, c2 * 2 * CK + CK, head);
+                        } else {
+                            const int c = c2 - nch1;
+                            tma_load_3d(s.kv[st][bx], &tm_k, &s.st_full[st], bx * 64, c * CK, head);
+                            tma_load_3d(s.kv[st][2 + bx], &tm_v, &s.st_full[st], bx * 64, c * CK, head);
+                        }
                     }
                     ++g;
                 }
@@ -189,8 +195,8 @@ lla_decode_mom_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
             for (int hl = 0; hl < nloc && ok; ++hl) {
                 const int db = hl & 1;
                 const uint32_t tD = tbase + db * 256;
-                for (int c2 = 0; c2 < 2 * nch; ++c2) {
-                    const int st = g % NSTAGE, ab = g & 1, c = c2 - nch;
+                for (int c2 = 0; c2 < nch1 + nch; ++c2) {
+                    const int st = g % NSTAGE, ab = g & 1, c = c2 - nch1;
                     if (!(ok = mbar_wait(&s.st_full[st], (g / NSTAGE) & 1, err))) break;
                     if (!(ok = mbar_wait(&s.a_full[ab], (g >> 1) & 1, err))) break;
                     if (c >= 0) {
@@ -231,9 +237,8 @@ lla_decode_mom_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
             gcol[i] = box * 64 + (qd & 1) * 32 + 8 * j;
         }
         const float tau = prm.tau;
-        // the logit of this thread's key in the chunk at stage st (its 32 coordinates left in kp)
-        auto logit = [&](int st, const uint32_t (&qp)[16], uint32_t (&kp)[16]) {
-            const unsigned char* kbx = s.kv[st][box];
+        // the logit of this thread's key in a box pair (its 32 coordinates left in kp)
+        auto logit = [&](const unsigned char* kbx, const uint32_t (&qp)[16], uint32_t (&kp)[16]) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uint4 t = *reinterpret_cast<const uint4*>(kbx + goff[i]);
@@ -264,32 +269,35 @@ lla_decode_mom_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
             float acc[32], om = 0.f, mt = -INFINITY;   // acc: then kbar, this thread's 32 coordinates
 #pragma unroll
             for (int e = 0; e < 32; ++e) acc[e] = 0.f;
-            for (int c = 0; c < nch; ++c, ++g) {
+            for (int c = 0; c < nch1; ++c, ++g) {
                 const int st = g % NSTAGE, ab = g & 1;
                 mbar_wait(&s.st_full[st], (g / NSTAGE) & 1, err);
-                uint32_t kp[16];
-                const float sj = logit(st, qp, kp);
+#pragma unroll 1
+                for (int h2 = 0; h2 < 2; ++h2) {         // keys r and r + 64 of the chunk's 128
+                    uint32_t kp[16];
+                    const float sj = logit(s.kv[st][2 * h2 + box], qp, kp);
+                    if (c * 2 * CK + h2 * CK + r < prm.n) {
+                        if (sj > mt) {
+                            const float f = expf(mt - sj);    // 0 while nothing was summed
+                            om *= f;
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) acc[e] *= f;
+                            mt = sj;
+                        }
+                        const float w = expf(sj - mt);
+                        om += w;
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) {
+                            acc[2 * u] = fmaf(w, bf_lo(kp[u]), acc[2 * u]);
+                            acc[2 * u + 1] = fmaf(w, bf_hi(kp[u]), acc[2 * u + 1]);
+                        }
+                    }
+                }
                 // hand the stage back through the MMA issuer once it has taken chunk g - 2's hand-off
                 // (the barrier then never runs two phases ahead of its waiter)
                 if (g >= 2) mbar_wait(&s.a_free[ab], ((g - 2) >> 1) & 1, err);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s.a_full[ab]);   // the stage's reads are done
-                if (c * CK + r < prm.n) {
-                    if (sj > mt) {
-                        const float f = expf(mt - sj);        // 0 while nothing was summed
-                        om *= f;
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) acc[e] *= f;
-                        mt = sj;
-                    }
-                    const float w = expf(sj - mt);
-                    om += w;
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        acc[2 * u] = fmaf(w, bf_lo(kp[u]), acc[2 * u]);
-                        acc[2 * u + 1] = fmaf(w, bf_hi(kp[u]), acc[2 * u + 1]);
-                    }
-                }
             }
             // combine: the warp's 8 rows against the warp's maximum, then the 8 warps
             {
@@ -348,7 +356,7 @@ lla_decode_mom_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                 const int st = g % NSTAGE, ab = g & 1;
                 mbar_wait(&s.st_full[st], (g / NSTAGE) & 1, err);
                 uint32_t kp[16];
-                const float sj = logit(st, qp, kp);
+                const float sj = logit(s.kv[st][box], qp, kp);
                 const float w = c * CK + r < prm.n ? expf(sj - m) : 0.f;
                 // this chunk's A buffer was last read by the products of chunk g - 2
                 if (g >= 2) mbar_wait(&s.a_free[ab], ((g - 2) >> 1) & 1, err);
