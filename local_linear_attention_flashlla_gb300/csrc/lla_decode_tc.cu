@@ -93,6 +93,29 @@ struct MomParams {
     float tau, lambda, cg_tol;
 };
 
+// tma_load_3d with an L2 cache policy (from createpolicy) for the loaded lines.
+__device__ __forceinline__ void tma_load_3d_hint(void* smem_dst, const void* tmap, uint64_t* bar, int x, int y, int z,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;"
+        ::"r"(smem_u32(smem_dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z),
+          "l"(policy)
+        : "memory");
+}
+// L2 policies for all of an access's lines: keep them (a later pass reads them again) or let them
+// go first (last use).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 __device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity))
@@ -162,6 +185,8 @@ lla_decode_mom_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
             // ================================ TMA producer ================================
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
+            // pass 1's K is read again by pass 2: keep it in L2; pass 2's K and V are last uses
+            const uint64_t keep = l2_policy_evict_last(), last = l2_policy_evict_first();
             int g = 0;
             bool ok = true;
             for (int hl = 0; hl < nloc && ok; ++hl) {
@@ -172,12 +197,13 @@ lla_decode_mom_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
                     mbar_arrive_expect_tx(&s.st_full[st], 4 * BOX);
                     for (int bx = 0; bx < 2; ++bx) {
                         if (c2 < nch1) {   // K rows y .. y+63 into boxes 0, 1 and y+64 .. y+127 into 2, 3
-                            tma_load_3d(s.kv[st][bx], &tm_k, &s.st_full[st], bx * 64, c2 * 2 * CK, head);
-                            tma_load_3d(s.kv[st][2 + bx], &tm_k, &s.st_full[st], bx * 64, c2 * 2 * CK + CK, head);
-                        } else {
-                            const int c = c2 - nch1;
-                            tma_load_3d(s.kv[st][bx], &tm_k, &s.st_full[st], bx * 64, c * CK, head);
-                            tma_load_3d(s.kv[st][2 + bx], &tm_v, &s.st_full[st], bx * 64, c * CK, head);
+                            tma_load_3d_hint(s.kv[st][bx], &tm_k, &s.st_full[st], bx * 64, c2 * 2 * CK, head, keep);
+                            tma_load_3d_hint(s.kv[st][2 + bx], &tm_k, &s.st_full[st], bx * 64, c2 * 2 * CK + CK, head,
+                                             keep);
+                        } else {           // pass 2 from the last chunk down: the latest-read K first
+                            const int c = nch - 1 - (c2 - nch1);
+                            tma_load_3d_hint(s.kv[st][bx], &tm_k, &s.st_full[st], bx * 64, c * CK, head, last);
+                            tma_load_3d_hint(s.kv[st][2 + bx], &tm_v, &s.st_full[st], bx * 64, c * CK, head, last);
                         }
                     }
                     ++g;
@@ -352,7 +378,7 @@ lla_decode_mom_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_con
             float rs[32], nu[32];
 #pragma unroll
             for (int e = 0; e < 32; ++e) rs[e] = nu[e] = 0.f;
-            for (int c = 0; c < nch; ++c, ++g) {
+            for (int c = nch - 1; c >= 0; --c, ++g) {      // the chunks in the order TMA delivers them
                 const int st = g % NSTAGE, ab = g & 1;
                 mbar_wait(&s.st_full[st], (g / NSTAGE) & 1, err);
                 uint32_t kp[16];
