@@ -538,7 +538,8 @@ def run_decode(args, world, rank, local):
 
     form = {"auto": lla.LLA_DECODE_AUTO, "moment": lla.LLA_DECODE_MOMENT, "stream": lla.LLA_DECODE_STREAM,
             "cluster": lla.LLA_DECODE_CLUSTER}[args.decode_form]
-    moment = form == lla.LLA_DECODE_MOMENT or (form == lla.LLA_DECODE_AUTO and w.dtype == "bf16" and w.d == 128)
+    moment = form == lla.LLA_DECODE_MOMENT or (form == lla.LLA_DECODE_AUTO and w.dtype == "bf16" and w.d == 128 and
+                                               (w.n <= 16384 or w.n > lla.lla_decode_max_n(w.d)))
     kname = "lla_decode_mom_kernel" if moment else "lla_decode_kernel"
 
     def step(qq=qd):

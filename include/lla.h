@@ -213,7 +213,8 @@ int lla_parallax_forward(int dtype, int path, const void* q, const void* k, cons
                          void* stream);
 
 typedef enum {
-    LLA_DECODE_AUTO = 0,         /* LLA_DECODE_MOMENT for bf16 caches at d = 128, else a CUDA-core form */
+    LLA_DECODE_AUTO = 0,         /* LLA_DECODE_MOMENT for bf16 caches at d = 128 with n <= 16384 or n past
+                                    lla_decode_max_n(128), else a CUDA-core form */
     LLA_DECODE_MOMENT = 1,       /* tcgen05: the weighted moments of the cache in one pass, CG on them */
     LLA_DECODE_STREAM = 2,       /* CUDA cores, a CTA per head, K re-read every CG iteration */
     LLA_DECODE_CLUSTER = 3       /* CUDA cores, an 8-CTA cluster per head holding K in shared memory */
@@ -234,8 +235,9 @@ typedef enum {
  * tau, lambda, cg_max_iters, cg_tol: as for lla_forward.
  * All pointers are device pointers, 16-byte aligned, owned by the caller.  No scratch.  Errors
  * as for lla_forward_ex.  The form is LLA_DECODE_AUTO (see lla_decode_ex): for bf16 caches at
- * d = 128 the moment form, which has no limit on n; otherwise a CUDA-core form, which keeps the
- * n weights of a head in shared memory, so n above lla_decode_max_n(d) gives LLA_ERR_UNSUPPORTED.
+ * d = 128 the moment form up to n = 16384 and past lla_decode_max_n(128); otherwise a CUDA-core
+ * form, which keeps the n weights of a head in shared memory, so n above lla_decode_max_n(d) gives
+ * LLA_ERR_UNSUPPORTED for fp32 caches or d < 128.
  */
 int lla_decode(int dtype, const void* q, const void* k, const void* v, void* out, float* rho, float* denom,
                int* cg_iters, int B, int H, int n, int n_cap, int d, float tau, float lambda, int cg_max_iters,
@@ -245,12 +247,15 @@ int lla_decode(int dtype, const void* q, const void* k, const void* v, void* out
  * lla_decode_ex -- lla_decode with the form chosen by the caller (an lla_decode_form value).
  * Every form computes the same step, the centred CG of the reading notes' section 2.2 on the
  * new query's system, and differs only in how the operator C is applied:
- *   LLA_DECODE_MOMENT   (bf16 caches, d = 128 only) reads K and V once and forms, on the tensor
- *       cores, Cu = sum_j w_j k_j k_j^T and Hk = sum_j w_j k_j v_j^T (d x d, fp32 accumulation,
- *       the weighted keys carried as three bf16 terms, so as accurate as fp32 arithmetic), with
- *       omega, mu~ = sum_j w_j k_j and nu = sum_j w_j v_j; then runs the CG on the d x d moments:
- *       C p = Cu p - mu~ (kbar.p) - kbar (mu~.p - omega kbar.p), and the output
- *       sum_j u_j v_j = (1 + kbar.rho') nu - Hk^T rho'.  No limit on n.
+ *   LLA_DECODE_MOMENT   (bf16 caches, d = 128 only) reads K twice and V once: a first pass gives
+ *       the logits' maximum, omega and kbar; the second forms, on the tensor cores,
+ *       Cc = sum_j w_j (k_j - kbar) k_j^T and Hc = sum_j w_j (k_j - kbar) v_j^T (d x d, fp32
+ *       accumulation, the weighted centred keys carried as three bf16 terms), with
+ *       r = sum_j w_j (k_j - kbar) and nu = sum_j w_j v_j; then runs the CG on the d x d moments:
+ *       C p = Cc p - r (kbar.p), and the output sum_j u_j v_j = nu - Hc^T rho',
+ *       sum_j u_j = omega - r.rho'.  No limit on n; its moment sums drift with n (denom measured
+ *       1e-4 relative at 16384 keys, 3.4e-4 at 53952, where the CUDA-core forms stay below 1e-6),
+ *       hence AUTO's rule.
  *   LLA_DECODE_STREAM   applies C with a pass over the cache per CG iteration (K read T+2 times).
  *   LLA_DECODE_CLUSTER  as STREAM, with an eighth of K held in each CTA of an 8-CTA cluster; n must
  *       leave an eighth of the cache within a CTA's shared memory, else LLA_ERR_UNSUPPORTED.

@@ -429,6 +429,8 @@ int lla_parallax_forward(int dtype, int path, const void* q, const void* k, cons
     return lla::run_problem(p, rpath, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
+constexpr int kDecodeMomentAutoMaxN = 16384;
+
 static_assert(LLA_DECODE_AUTO == lla::kDecodeAuto && LLA_DECODE_MOMENT == lla::kDecodeMoment &&
                   LLA_DECODE_STREAM == lla::kDecodeStream && LLA_DECODE_CLUSTER == lla::kDecodeCluster,
               "decode form values");
@@ -462,7 +464,14 @@ int lla_decode_ex(int form, int dtype, const void* q, const void* k, const void*
     if (form < LLA_DECODE_AUTO || form > LLA_DECODE_CLUSTER) return fail(LLA_ERR_INVALID_ARG, "unknown decode form %d", form);
     lla::DecodeProblem p{q, k, v, out, rho, denom, cg_iters, B, H, n, n_cap, d, tau, lambda, cg_max_iters, cg_tol,
                          dtype, nullptr, nullptr, form, nullptr};
-    if (form == LLA_DECODE_AUTO) p.form = lla::decode_moment_supported(p) ? LLA_DECODE_MOMENT : LLA_DECODE_AUTO;
+    // AUTO: the moment form's fp32 moment sums drift with the cache length (denom measured 2e-5
+    // relative at 4096 keys, 1e-4 at 16384, 2e-4 at 32768, 3.4e-4 at 53952, where the CUDA-core forms
+    // stay below 1e-6), so past kDecodeMomentAutoMaxN it takes a CUDA-core form while one fits
+    if (form == LLA_DECODE_AUTO)
+        p.form = lla::decode_moment_supported(p) &&
+                         (n <= kDecodeMomentAutoMaxN || lla::decode_smem_bytes(n, d) > (size_t)LLA_DECODE_SMEM_LIMIT)
+                     ? LLA_DECODE_MOMENT
+                     : LLA_DECODE_AUTO;
     if (p.form == LLA_DECODE_MOMENT) {
         if (!lla::decode_moment_supported(p))
             return fail(LLA_ERR_UNSUPPORTED, "the moment form needs bf16 caches and d = 128");

@@ -203,3 +203,34 @@ def test_decode_equals_forward_last_row(lla_gpu):
     rms_v = math.sqrt(float(qkv[2].double().pow(2).mean()))
     diff = (res[0].double() - o[:, :, -1].cpu().double()).abs()
     assert float(diff.max()) <= 2.0 ** -7 * float(o[:, :, -1].abs().max()) + 1e-4 * rms_v
+
+
+def test_decode_moment_form_beyond_the_cuda_core_limit(lla_gpu):
+    """A cache 1000 keys longer than the CUDA-core forms accept (they keep n weights in shared
+    memory): AUTO takes the moment form, which keeps none.  out and rho meet the usual gate.  denom
+    is held to 5e-4: the moment form's fp32 sums drift with n (denom measured 2e-5 relative at 4096
+    keys, 1e-4 at 16384, 2.1e-4 at 32768 and 3.4e-4 here), which is why AUTO takes the CUDA-core
+    forms between 16384 keys and their limit."""
+    n = lla.lla_decode_max_n(128) + 1000
+    w = workload("lm_bf16", B=1, H=2, n=n, d=128, tau=1.0 / math.sqrt(128), cg_max_iters=576, cg_tol=1e-6)
+    qkv, res = _decode(w)
+    q, k, v = (t.double().numpy() for t in qkv)
+    out, rho, den, _ = (t.double().numpy() for t in res)
+    rms_v = math.sqrt(float(np.mean(v ** 2)))
+    for h in range(w.H):
+        r = lla_row(q[0, h, n - 1], k[0, h, :n], v[0, h, :n], w.tau, w.lam)
+        assert (np.abs(out[0, h] - r["out"]) <= 2.0 ** -8 * np.abs(r["out"]) + 1e-4 * rms_v).all()
+        assert np.abs(rho[0, h] - r["rho"]).max() <= 2e-4 * math.sqrt(float(np.mean(r["rho"] ** 2)))
+        assert abs(den[0, h] - r["denom"]) <= 5e-4 * abs(r["denom"])
+    with pytest.raises(lla.LLAError):
+        _decode(w, form=STREAM)
+
+
+def test_decode_auto_takes_a_cuda_core_form_between_16k_and_their_limit(lla_gpu):
+    """At 32768 keys AUTO takes a CUDA-core form (the moment form's denom drifts to 2e-4 there),
+    which meets the usual gate; the moment form, asked for by name, still serves the call."""
+    w = workload("lm_bf16", B=1, H=2, n=32768, d=128, tau=1.0 / math.sqrt(128), cg_max_iters=576, cg_tol=1e-6)
+    qkv, res = _decode(w)
+    _gate(w, qkv, res, lambda qi, K, V: lla_row(qi, K, V, w.tau, w.lam))
+    _, res_m = _decode(w, form=MOMENT)
+    assert torch.isfinite(res_m[0].float()).all() and (res_m[2] > 0).all()
