@@ -426,6 +426,14 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def decode_uses_moment_form(w, form, max_n):
+    """Whether the decode call runs the moment form: asked for by name, or AUTO's choice (include/lla.h:
+    bf16 caches at d = 128 with n <= 16384, or n past max_n, the CUDA-core forms' limit)."""
+    if form == "moment":
+        return True
+    return form == "auto" and w.dtype == "bf16" and w.d == 128 and (w.n <= 16384 or w.n > max_n)
+
+
 def decode_bytes(w, T, moment):
     """(compulsory, method) HBM bytes of one decode step.  Compulsory: the caches, q and the
     outputs once.  Method: the moment form reads K twice (the logits' maximum and kbar, then the
@@ -538,8 +546,7 @@ def run_decode(args, world, rank, local):
 
     form = {"auto": lla.LLA_DECODE_AUTO, "moment": lla.LLA_DECODE_MOMENT, "stream": lla.LLA_DECODE_STREAM,
             "cluster": lla.LLA_DECODE_CLUSTER}[args.decode_form]
-    moment = form == lla.LLA_DECODE_MOMENT or (form == lla.LLA_DECODE_AUTO and w.dtype == "bf16" and w.d == 128 and
-                                               (w.n <= 16384 or w.n > lla.lla_decode_max_n(w.d)))
+    moment = decode_uses_moment_form(w, args.decode_form, lla.lla_decode_max_n(w.d))
     kname = "lla_decode_mom_kernel" if moment else "lla_decode_kernel"
 
     def step(qq=qd):

@@ -56,6 +56,18 @@ def test_decode_bytes():
     assert comp - 2 * kv == w.B * w.H * (w.d * (2 + 2 + 4) + 4)
 
 
+def test_decode_form_accounting_follows_the_auto_rule():
+    lim = 52952
+    w = workload("decode_bf16")
+    assert bench.decode_uses_moment_form(w, "auto", lim)                       # n = 4096
+    assert not bench.decode_uses_moment_form(w.with_(n=32768), "auto", lim)   # a CUDA-core form
+    assert bench.decode_uses_moment_form(w.with_(n=60000), "auto", lim)       # past their limit
+    assert not bench.decode_uses_moment_form(w.with_(dtype="fp32"), "auto", lim)
+    assert not bench.decode_uses_moment_form(w.with_(d=64), "auto", lim)
+    assert bench.decode_uses_moment_form(w.with_(n=32768), "moment", lim)
+    assert not bench.decode_uses_moment_form(w, "stream", lim)
+
+
 def test_traffic_is_tied_to_the_sources_and_scales_with_the_batch(tmp_path, monkeypatch):
     w = workload("lm_bf16")
     doc = {"lla_tc_kernel:lm_bf16": {"source_hash": bench.kernel_source_hash("lla_tc_kernel"),
